@@ -1,0 +1,261 @@
+"""Seeded synthetic inputs for the paged KV-cache decode workloads.
+
+This module is the only code shared by the CPU oracle (``oracle/``) and the CUDA
+product path (``paged_kv_cache_137_gb300/``).  It draws random numbers and casts
+them to storage dtypes; it holds none of the method's arithmetic (no block
+tables, no slots, no attention).  Every draw comes from its own numpy PCG64
+stream keyed by (config seed, purpose, index), so a test can regenerate the
+inputs of one sequence without drawing the whole workload.
+
+The five workloads follow the synthetic configurations the method is measured
+on (decode of one new token per sequence over a pool of fixed-size blocks):
+
+* ``tiny_fp32``        1 layer, 4 seqs, 4 q heads = 4 KV heads, head_dim 64,
+                       block 16, pool 64 blocks, ctx ~ U[1,128], fp32.
+* ``qwen_gqa_bf16``    28 q heads / 4 KV heads, head_dim 128, block 16, pool
+                       8,500 blocks, 64 seqs, ctx ~ U[256,4096], bf16.
+* ``prefix_fork_bf16`` 32 q / 8 KV heads, head_dim 128, block 16, 256 seqs
+                       sharing a 1,024-token prefix, private tails ~ U[1,512],
+                       25% of sequences forked mid-block (copy-on-write), bf16.
+* ``long_mha_bf16``    32 q = 32 KV heads, head_dim 128, block 32, 8 seqs,
+                       ctx ~ U[16384,32768], every 97th key scaled by 8, bf16,
+                       512-token split-K partitions.
+* ``fp8_churn``        64 q / 8 KV heads, head_dim 128, block 16, 512 seqs,
+                       ctx log-uniform on [64,8192], E4M3 KV with one scale per
+                       tensor, pool 65,536 blocks scrambled by 10k alloc/free
+                       churn operations.
+
+Ranges are integer and inclusive; values are N(0,1) drawn in fp32 and rounded
+to the storage dtype with PyTorch's round-to-nearest-even cast.
+"""
+from __future__ import annotations
+
+import math
+from dataclasses import dataclass, field, replace
+
+import numpy as np
+import torch
+
+__all__ = [
+    "Workload", "CONFIGS", "get", "scaled",
+    "rng", "context_lens", "free_order", "churn_ops", "q_for_seq", "kv_for_seq",
+    "prefix_kv", "fork_layout", "fp8_scales", "TORCH_DTYPES",
+]
+
+TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
+
+# Purpose keys of the independent random streams.
+_CTX, _ORDER, _CHURN, _Q, _K, _V, _PREFIX_K, _PREFIX_V, _TAIL = range(9)
+
+
+@dataclass(frozen=True)
+class Workload:
+    name: str
+    seed: int
+    num_seqs: int
+    num_q_heads: int
+    num_kv_heads: int
+    head_dim: int
+    block_size: int
+    num_blocks: int
+    kv_dtype: str              # "f32" | "f16" | "bf16" | "e4m3"
+    q_dtype: str               # "f32" | "f16" | "bf16"
+    ctx_range: tuple = (1, 1)  # inclusive
+    ctx_dist: str = "uniform"  # "uniform" | "loguniform" | "prefix_fork"
+    num_layers: int = 1
+    prefix_len: int = 0
+    tail_range: tuple = (0, 0)
+    fork_fraction: float = 0.0
+    spike_every: int = 0       # every n-th logical key (1-based) is scaled
+    spike_scale: float = 1.0
+    partition_tokens: int = 0  # split-K partition size, 0 = library default
+    churn: int = 0             # alloc/free operations applied before the workload
+    shuffled_pool: bool = True
+    extra: dict = field(default_factory=dict)
+
+    @property
+    def group(self) -> int:
+        return self.num_q_heads // self.num_kv_heads
+
+    @property
+    def kv_bytes(self) -> int:
+        return 1 if self.kv_dtype == "e4m3" else (4 if self.kv_dtype == "f32" else 2)
+
+    @property
+    def src_dtype(self) -> str:
+        """dtype of the new K/V handed to the slot write (the q dtype)."""
+        return self.q_dtype
+
+
+CONFIGS = {
+    "tiny_fp32": Workload(
+        name="tiny_fp32", seed=1371, num_seqs=4, num_q_heads=4, num_kv_heads=4,
+        head_dim=64, block_size=16, num_blocks=64, kv_dtype="f32", q_dtype="f32",
+        ctx_range=(1, 128)),
+    "qwen_gqa_bf16": Workload(
+        name="qwen_gqa_bf16", seed=1372, num_seqs=64, num_q_heads=28, num_kv_heads=4,
+        head_dim=128, block_size=16, num_blocks=8500, kv_dtype="bf16", q_dtype="bf16",
+        ctx_range=(256, 4096)),
+    "prefix_fork_bf16": Workload(
+        name="prefix_fork_bf16", seed=1373, num_seqs=256, num_q_heads=32, num_kv_heads=8,
+        head_dim=128, block_size=16, num_blocks=8192, kv_dtype="bf16", q_dtype="bf16",
+        ctx_dist="prefix_fork", prefix_len=1024, tail_range=(1, 512), fork_fraction=0.25),
+    "long_mha_bf16": Workload(
+        name="long_mha_bf16", seed=1374, num_seqs=8, num_q_heads=32, num_kv_heads=32,
+        head_dim=128, block_size=32, num_blocks=8192, kv_dtype="bf16", q_dtype="bf16",
+        ctx_range=(16384, 32768), spike_every=97, spike_scale=8.0, partition_tokens=512),
+    "fp8_churn": Workload(
+        name="fp8_churn", seed=1375, num_seqs=512, num_q_heads=64, num_kv_heads=8,
+        head_dim=128, block_size=16, num_blocks=65536, kv_dtype="e4m3", q_dtype="bf16",
+        ctx_range=(64, 8192), ctx_dist="loguniform", churn=10000),
+}
+
+
+def get(name: str) -> Workload:
+    return CONFIGS[name]
+
+
+def scaled(w: Workload, **overrides) -> Workload:
+    """A copy of a workload with some fields replaced (smaller parity cases)."""
+    return replace(w, **overrides)
+
+
+def rng(w: Workload, purpose: int, index: int = 0, attempt: int = 0) -> np.random.Generator:
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence([w.seed, purpose, index, attempt])))
+
+
+def _cast(x32: np.ndarray, dtype: str) -> torch.Tensor:
+    t = torch.from_numpy(np.ascontiguousarray(x32, dtype=np.float32))
+    return t.to(TORCH_DTYPES[dtype])
+
+
+def _blocks(n: int, t: int) -> int:
+    return -(-n // t)
+
+
+def context_lens(w: Workload) -> np.ndarray:
+    """Attended context length per sequence (the new token included).
+
+    For ``uniform`` and ``loguniform`` draws the lengths are redrawn (attempt
+    1, 2, ...) until the whole batch fits the pool; the attempt that was
+    accepted is recorded in ``last_attempt``.  ``prefix_fork`` lengths are
+    prefix + tail (see :func:`fork_layout`).
+    """
+    if w.ctx_dist == "prefix_fork":
+        return fork_layout(w)["ctx"]
+    lo, hi = w.ctx_range
+    for attempt in range(1000):
+        g = rng(w, _CTX, 0, attempt)
+        if w.ctx_dist == "uniform":
+            ctx = g.integers(lo, hi, size=w.num_seqs, endpoint=True)
+        elif w.ctx_dist == "loguniform":
+            u = g.uniform(math.log(lo), math.log(hi), size=w.num_seqs)
+            ctx = np.clip(np.floor(np.exp(u)), lo, hi)
+        else:
+            raise ValueError(w.ctx_dist)
+        ctx = ctx.astype(np.int64)
+        if sum(_blocks(int(c), w.block_size) for c in ctx) <= w.num_blocks:
+            context_lens.last_attempt = attempt
+            return ctx
+    raise RuntimeError("no context-length draw fits the pool")
+
+
+context_lens.last_attempt = 0
+
+
+def free_order(w: Workload) -> np.ndarray:
+    """Initial free-stack order, top first: a random permutation of the pool
+    (or 0, 1, 2, ... when the pool is not shuffled)."""
+    if not w.shuffled_pool:
+        return np.arange(w.num_blocks, dtype=np.int32)
+    return rng(w, _ORDER).permutation(w.num_blocks).astype(np.int32)
+
+
+def churn_ops(w: Workload) -> tuple[np.ndarray, np.ndarray]:
+    """Random numbers for the allocate/free churn: per operation a coin in
+    [0,1) (allocate when < 0.5) and a pick in [0,1) that selects which live
+    block to free as floor(pick * live_count)."""
+    g = rng(w, _CHURN)
+    coin = g.random(w.churn)
+    pick = g.random(w.churn)
+    return coin, pick
+
+
+def q_for_seq(w: Workload, seq: int) -> torch.Tensor:
+    """q of one sequence, [num_q_heads, head_dim] in the q dtype."""
+    x = rng(w, _Q, seq).standard_normal((w.num_q_heads, w.head_dim), dtype=np.float32)
+    return _cast(x, w.q_dtype)
+
+
+def kv_for_seq(w: Workload, seq: int, n_tokens: int, first_pos: int = 0,
+               stream_index: int | None = None) -> tuple[torch.Tensor, torch.Tensor]:
+    """K and V of ``n_tokens`` tokens at logical positions first_pos.. of one
+    sequence, each [n_tokens, num_kv_heads, head_dim] in the source dtype.
+
+    The draws of one sequence come from its own stream, so that the K/V of
+    positions [a, b) do not depend on how the range is cut into calls: the
+    stream is advanced past ``first_pos`` tokens first.  Keys at logical
+    positions p with (p + 1) % spike_every == 0 are multiplied by spike_scale
+    in fp32 before the cast.
+    """
+    idx = seq if stream_index is None else stream_index
+    per_tok = w.num_kv_heads * w.head_dim
+    out = []
+    for purpose in (_K, _V):
+        g = rng(w, purpose, idx)
+        if first_pos:
+            _ = g.standard_normal(first_pos * per_tok, dtype=np.float32)
+        x = g.standard_normal((n_tokens, w.num_kv_heads, w.head_dim), dtype=np.float32)
+        if purpose == _K and w.spike_every:
+            pos = np.arange(first_pos, first_pos + n_tokens)
+            hit = (pos + 1) % w.spike_every == 0
+            x[hit] *= np.float32(w.spike_scale)
+        out.append(_cast(x, w.src_dtype))
+    return out[0], out[1]
+
+
+def prefix_kv(w: Workload) -> tuple[torch.Tensor, torch.Tensor]:
+    """K/V of the shared prefix of the prefix-fork workload."""
+    per = (w.prefix_len, w.num_kv_heads, w.head_dim)
+    k = rng(w, _PREFIX_K).standard_normal(per, dtype=np.float32)
+    v = rng(w, _PREFIX_V).standard_normal(per, dtype=np.float32)
+    return _cast(k, w.src_dtype), _cast(v, w.src_dtype)
+
+
+def fork_layout(w: Workload) -> dict:
+    """Structure of the prefix-fork workload.
+
+    ``num_parents = num_seqs * (1 - fork_fraction)`` parents share the prefix
+    and each owns a private tail drawn from ``tail_range``; a parent's prior
+    length before the decode step is prefix + tail - 1.  The first
+    ``num_children`` parents whose prior length is not a multiple of the block
+    size (a fork in the middle of a block) each get one child.  The batch
+    order is children first, then parents; ``ctx`` is in batch order, and a
+    child attends the same length as its parent.
+    """
+    n_children = int(round(w.num_seqs * w.fork_fraction))
+    n_parents = w.num_seqs - n_children
+    lo, hi = w.tail_range
+    for attempt in range(1000):
+        tails = rng(w, _TAIL, 0, attempt).integers(lo, hi, size=n_parents, endpoint=True)
+        prior = w.prefix_len + tails - 1
+        mid = np.nonzero(prior % w.block_size != 0)[0]
+        if len(mid) >= n_children:
+            parent_of_child = mid[:n_children].astype(np.int64)
+            ctx_parents = (w.prefix_len + tails).astype(np.int64)
+            ctx = np.concatenate([ctx_parents[parent_of_child], ctx_parents])
+            return {"tails": tails.astype(np.int64), "parent_of_child": parent_of_child,
+                    "num_parents": n_parents, "num_children": n_children, "ctx": ctx}
+    raise RuntimeError("could not draw enough mid-block forks")
+
+
+def fp8_scales(amax_k: float, amax_v: float) -> dict:
+    """Per-tensor E4M3 scales from the absolute maxima of all K (V) values:
+    scale = amax / 448 in fp32 and the reciprocal the slot write multiplies by,
+    inv = fp32(1 / scale).  448 is the largest finite E4M3 value."""
+    out = {}
+    for name, a in (("k", amax_k), ("v", amax_v)):
+        s = np.float32(np.float32(a) / np.float32(448.0))
+        out[name + "_scale"] = float(s)
+        out[name + "_inv_scale"] = float(np.float32(np.float32(1.0) / s))
+    return out
