@@ -1,0 +1,330 @@
+"""Benchmark: one decode step of paged attention on GB300.
+
+A step is the whole hot path over one batch: copy-on-write block copies (none
+in this workload), the slot write of the step's new K/V, and decode attention
+through the block tables (with its split-K merge).  The default workload is the
+Qwen2.5-7B-shaped layer in bf16: 28 query / 4 KV heads, head_dim 128, block
+16, pool 8,500 blocks, 64 sequences with contexts uniform on [256, 4096].
+
+Prints one JSON line.  ``value`` is the attention's algorithmic K/V bytes
+(every cached K/V element once) divided by the device time of the step, in
+GB/s, inputs resident in HBM, L2 flushed before every timed step; ``e2e`` is
+the same metric through the C ABI with the step's inputs copied from pinned
+host memory and the output copied back inside the timed region.  With
+``--impl reference`` the CPU oracle is timed on the host instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+DEFAULT_CONFIG = "qwen_gqa_bf16"
+METRIC = "paged decode attention KV GB/s & fraction of GB300 HBM peak; decode tokens/s"
+KERNEL_SOURCES = ["attention.cu", "attention_simt.cuh", "attention.h", "device_common.cuh"]
+
+
+def parse():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
+    ap.add_argument("--config", default=DEFAULT_CONFIG)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    return ap.parse_args()
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_source_hash() -> str:
+    h = hashlib.sha256()
+    for n in KERNEL_SOURCES:
+        h.update(open(os.path.join(ROOT, "paged_kv_cache_137_gb300", "csrc", n), "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_for(config: str):
+    """DRAM bytes per attention launch from the committed ncu summary, if it
+    was taken on the current kernel sources."""
+    p = os.path.join(ROOT, "profiles", "attention_traffic.json")
+    if not os.path.exists(p):
+        return None
+    d = json.load(open(p))
+    e = d.get(config)
+    if not e or e.get("kernel_sha") != kernel_source_hash():
+        return None
+    return e.get("dram_bytes_per_launch")
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons while running."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index: int):
+        self.index = index
+        self.samples = []
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except (FileNotFoundError, OSError):
+            self.proc = None
+        return self
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) == 6:
+                self.samples.append(parts)
+
+    def __exit__(self, *exc):
+        if self.proc:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if not self.samples:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
+        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
+        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[2 + i] == "Active"})
+        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
+                "reasons": reasons, "samples": len(self.samples)}
+
+
+def dist_setup(args):
+    import torch
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        if args.impl == "gb300":
+            torch.cuda.set_device(local)
+            dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+        else:
+            dist.init_process_group("gloo")
+    return world, rank, local
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([x], dtype=torch.float64, device="cuda")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+# ------------------------------------------------------------------ oracle
+def time_oracle(config: str, seconds: float, max_passes: int | None = None):
+    """The CPU oracle on the host: one pass = decode attention of the whole
+    batch (pool built beforehand, not timed); passes repeat until ``seconds``.
+    Returns (GB/s of algorithmic K/V bytes, tokens/s, passes, elapsed)."""
+    import math
+    import numpy as np
+    import workloads as W
+    from oracle import attention as OA
+    from oracle import scenario as OS
+    w = W.get(config)
+    sc = W.fp8_scales(*W.kv_amax(w)) if w.kv_dtype == "e4m3" else {}
+    scn = OS.build(w, scales=sc)
+    q = scn.q_f64()
+    tables = scn.tables
+    kv_bytes = 2 * int(np.sum(scn.ctx)) * w.num_kv_heads * w.head_dim * w.kv_bytes
+    passes, t0 = 0, time.perf_counter()
+    while True:
+        OA.paged_attention_decode(q, scn.pool, tables, scn.ctx, 1.0 / math.sqrt(w.head_dim),
+                                  sc.get("k_scale", 1.0), sc.get("v_scale", 1.0))
+        passes += 1
+        el = time.perf_counter() - t0
+        if el >= seconds or (max_passes and passes >= max_passes):
+            break
+    return kv_bytes * passes / el / 1e9, w.num_seqs * passes / el, passes, el, kv_bytes
+
+
+def run_reference(args, world, rank):
+    if rank != 0:
+        return
+    t_steps = []
+    gbs = tps = None
+    for _ in range(args.warmup):
+        time_oracle(args.config, 0.0, max_passes=1)
+    for _ in range(args.steps):
+        g, t, passes, el, kvb = time_oracle(args.config, 0.0, max_passes=1)
+        t_steps.append(el)
+    ms = 1e3 * statistics.mean(t_steps)
+    gbs = kvb / (ms / 1e3) / 1e9
+    import workloads as W
+    w = W.get(args.config)
+    line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.config, "num_seqs": w.num_seqs,
+                       "kv_bytes_per_step": kvb, "sample": "the whole batch, one pass per step"},
+            "tokens_per_s": round(w.num_seqs / (ms / 1e3), 3),
+            "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                             "sample": "whole batch of the workload, one pass per step"},
+            "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+# --------------------------------------------------------------------- GPU
+def run_gpu(args, world, rank, local):
+    import numpy as np
+    import torch
+    import workloads as W
+    import paged_kv_cache_137_gb300 as pkv
+    from paged_kv_cache_137_gb300 import scenario as PS
+
+    pkv.build()
+    torch.cuda.set_device(local)
+    dev_name = f"cuda:{local}"
+    w = W.get(args.config)
+    sc = W.fp8_scales(*W.kv_amax(w)) if w.kv_dtype == "e4m3" else {}
+    scn = PS.materialize(PS.plan(w), dev_name, sc)
+    stream = torch.cuda.current_stream()
+    kv_bytes = scn.kv_bytes()
+    props = torch.cuda.get_device_properties(local)
+    flush = torch.empty(2 * props.L2_cache_size // 4 + 1024, dtype=torch.float32, device=dev_name)
+    n_pairs = len(scn.plan.cow_pairs)
+    splits = -(-scn.plan.max_blocks * w.block_size // scn.partition)
+    launches_per_step = 1 + 1 + (1 if splits > 1 else 0) + (-(-n_pairs // 1024) if n_pairs else 0)
+
+    for _ in range(max(args.warmup, 3)):
+        scn.step()
+    torch.cuda.synchronize()
+
+    K = args.steps
+    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(K)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        for k in range(K):
+            flush.fill_(float(k))
+            ev[k][0].record(stream)
+            scn.copy_blocks()
+            scn.write_step()
+            ev[k][1].record(stream)
+            scn.attend()
+            ev[k][2].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    step_ms = [ev[k][0].elapsed_time(ev[k][2]) for k in range(K)]
+    attn_ms = [ev[k][1].elapsed_time(ev[k][2]) for k in range(K)]
+    ms = max_over_ranks(statistics.mean(step_ms), world)
+    attn = statistics.mean(attn_ms)
+    value = world * kv_bytes / (ms / 1e3) / 1e9
+
+    # end to end through the C ABI from pinned host buffers
+    host = {n: getattr(scn, n).cpu().pin_memory() for n in ("q", "k_new", "v_new", "step_slots",
+                                                          "tables", "ctx")}
+    out_host = torch.empty_like(scn.out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        for n, t in host.items():
+            getattr(scn, n).copy_(t, non_blocking=True)
+        scn.step()
+        out_host.copy_(scn.out, non_blocking=True)
+        torch.cuda.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(K):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / K, world)
+    e2e_val = world * kv_bytes / e2e_s / 1e9
+
+    peak, peak_kind = peaks()
+    achieved = kv_bytes / (attn / 1e3) / 1e9
+    line = {
+        "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
+        "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4), "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "bf16" if w.kv_dtype == "bf16" else w.kv_dtype,
+        "data": "synthetic",
+        "config": {"workload": args.config, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                   "num_blocks": w.num_blocks, "context_tokens": int(scn.plan.ctx.sum()),
+                   "kv_bytes_per_step": kv_bytes, "partition_tokens": scn.partition,
+                   "l2": "flushed before every timed step (write of 2x L2); K/V larger than L2",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "tokens_per_s": round(world * w.num_seqs / (ms / 1e3), 1),
+        "frac_of_hbm_peak": round(value / peak, 4),
+        "roofline": {"bound": "hbm", "kernel": "pkv_attention_decode (decode + split-K merge)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
+                     "frac": round(achieved / peak, 4), "peak_source": peak_kind,
+                     "traffic": traffic_for(args.config), "attention_ms": round(attn, 4)},
+        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": K * launches_per_step,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        g, t, passes, el, _ = time_oracle(args.config, args.cpu_seconds)
+        line["cpu_baseline"] = {"value": round(g, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+                                "sample": f"whole batch of {args.config}, {passes} pass(es) in {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    args = parse()
+    # the oracle is timed on one host thread
+    for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
+        os.environ.setdefault(v, "1")
+    world, rank, local = dist_setup(args)
+    if args.impl == "reference":
+        run_reference(args, world, rank)
+    else:
+        run_gpu(args, world, rank, local)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,249 @@
+/*
+ * pkv.h — C ABI of the GB300 paged KV-cache library (libpkv.so).
+ *
+ * The library implements the data path of PagedAttention: a pool of equally
+ * sized physical KV blocks handed out through per-sequence block tables, the
+ * slot write of each step's new keys and values, the copy-on-write block copy,
+ * and single-token decode attention that gathers K/V through the tables.
+ *
+ * Sources (web pages on PagedAttention):
+ *   [A] "PagedAttention Memory Management" (apxml course page), sections
+ *       "Calculating Physical Block Sizes" and "Complex Topologies and Memory
+ *       Sharing".
+ *   [B] "What problem does PagedAttention solve for the KV cache in vLLM?"
+ *       (katajob Q&A), sections "The paging idea" and "Sharing, the second
+ *       dividend".
+ *   [C] foundry page on paged block allocation for the KV cache, sections
+ *       "In and out", "Concept", "The knobs".
+ *   [D] "PagedAttention, clearly explained" (thread).
+ *
+ * Conventions
+ *   - Every call that can fail returns a pkv_status; pkv_last_error() gives a
+ *     message for the calling thread's last failure.
+ *   - Host allocator calls are all-or-nothing: on error nothing changes.
+ *   - Device buffers are owned by the caller (plain device pointers).  The
+ *     library never allocates or frees device memory.  A pool handle owns only
+ *     host-side allocator state.
+ *   - Device calls enqueue kernels on the given CUDA stream (a cudaStream_t
+ *     passed as void*, NULL = legacy default stream) and return without
+ *     synchronising; a launch failure returns PKV_ERR_CUDA.
+ *   - A pool handle is not thread-safe; use one thread per handle.
+ *
+ * Memory layout of one layer's cache (the pages fix none; this is the
+ * library's reading of "one large pre-allocated tensor per layer" [C]):
+ *   k_cache, v_cache : [num_blocks][num_kv_heads][block_size][head_dim]
+ *   elements of kv_dtype, row-major, 16-byte aligned base.  Physical slot s is
+ *   block s / block_size, offset s % block_size.  A block id names the same
+ *   slot range in every layer's tensors, so one block holds
+ *   pkv_block_bytes(L, ...) bytes over all layers [A].
+ */
+#ifndef PKV_H
+#define PKV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define PKV_API __attribute__((visibility("default")))
+#else
+#define PKV_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PKV_OK = 0,
+  PKV_ERR_INVALID_ARG = 1,   /* bad pointer, size, id or dtype combination */
+  PKV_ERR_OUT_OF_BLOCKS = 2, /* the free-block stack cannot satisfy the call */
+  PKV_ERR_UNKNOWN_SEQ = 3,   /* no live sequence with that id */
+  PKV_ERR_UNSUPPORTED = 4,   /* valid but not compiled (head_dim, block_size, group) */
+  PKV_ERR_CUDA = 5           /* a CUDA runtime call or kernel launch failed */
+} pkv_status;
+
+/* Element types.  PKV_E4M3 is the OCP 8-bit E4M3 ("FN": no infinities,
+ * max 448) format with one scale per tensor; the cache stores
+ * e4m3(round_fp32(x * inv_scale)) and reads back e4m3 * scale. */
+typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_E4M3 = 3 } pkv_dtype;
+
+/* Shape of one layer's K/V cache tensors. */
+typedef struct {
+  int32_t num_blocks;   /* physical blocks in the pool */
+  int32_t num_kv_heads; /* N_kv */
+  int32_t head_dim;     /* D_head: 64 or 128 */
+  int32_t block_size;   /* T_block tokens per block: 16 or 32 */
+  int32_t kv_dtype;     /* pkv_dtype of the cache */
+} pkv_kv_desc;
+
+typedef struct pkv_pool pkv_pool;
+
+/* ------------------------------------------------------------ sizing [A] */
+
+/* Bytes of one physical block, 2 * L * N_kv * D_head * T_block * P_bytes
+ * ([A] "Calculating Physical Block Sizes").  Returns 0 if a factor is <= 0. */
+PKV_API uint64_t pkv_block_bytes(int32_t num_layers, int32_t num_kv_heads, int32_t head_dim,
+                         int32_t block_size, int32_t elem_bytes);
+
+/* Whole blocks that fit budget_bytes (floor); 0 if block_bytes is 0. */
+PKV_API uint64_t pkv_num_blocks_for_budget(uint64_t budget_bytes, uint64_t block_bytes);
+
+/* Bytes per element of a pkv_dtype, 0 if unknown. */
+PKV_API int32_t pkv_dtype_bytes(int32_t dtype);
+
+/* ------------------------------------------------- host allocator [B][C][D]
+ * A free-block stack, per-sequence block tables and per-block reference
+ * counts.  Blocks are popped one per block_size tokens, only when the
+ * previous block is full [D][C "Concept"]; fork copies the table and counts
+ * each shared block once more [C "Concept"][A "Complex Topologies"]; a token
+ * written into a partly filled block that other sequences still map first
+ * moves this sequence onto a private copy (copy-on-write) [B "Sharing"];
+ * finishing a sequence returns blocks whose count reaches zero [D].
+ * Order rules (needed to reproduce tables exactly): the stack is LIFO; the
+ * initial order is given top first (default: block 0 on top, then 1, 2, ...);
+ * freeing pushes a sequence's blocks in logical order. */
+
+/* Create an allocator over num_blocks blocks of block_size tokens.
+ * initial_free_order: NULL or a host array of num_blocks distinct ids in
+ * [0, num_blocks), top of the stack first.  *out receives the handle. */
+PKV_API pkv_status pkv_pool_create(int32_t num_blocks, int32_t block_size,
+                           const int32_t* initial_free_order, pkv_pool** out);
+PKV_API void pkv_pool_destroy(pkv_pool* pool);
+
+/* Register an empty sequence.  INVALID_ARG if the id is live. */
+PKV_API pkv_status pkv_seq_create(pkv_pool* pool, int64_t seq_id);
+
+/* Reserve slots for n_new tokens of one sequence.
+ * slots_out   : host int64[n_new], slot of each new token
+ *               (block * block_size + offset).
+ * cow_out     : host int32[2 * cow_cap], receives (src, dst) block pairs that
+ *               must be copied (pkv_copy_blocks) before the tokens are
+ *               written; at most one pair per call.  May be NULL if cow_cap 0.
+ * n_cow_out   : number of pairs written.
+ * OUT_OF_BLOCKS if the stack cannot supply the blocks; INVALID_ARG if a copy
+ * is needed and cow_cap is 0.  All-or-nothing. */
+PKV_API pkv_status pkv_seq_append(pkv_pool* pool, int64_t seq_id, int32_t n_new, int64_t* slots_out,
+                          int32_t* cow_out, int32_t cow_cap, int32_t* n_cow_out);
+
+/* One decode step: append one token to each of n_seqs sequences, in order.
+ * slots_out: host int64[n_seqs]; cow_out / cow_cap / n_cow_out as above (at
+ * most n_seqs pairs).  All-or-nothing over the whole batch: if any sequence
+ * cannot be served, no sequence changes. */
+PKV_API pkv_status pkv_batch_append(pkv_pool* pool, const int64_t* seq_ids, int32_t n_seqs,
+                            int64_t* slots_out, int32_t* cow_out, int32_t cow_cap,
+                            int32_t* n_cow_out);
+
+/* The child (a new id) maps every block of the parent; counts + 1. */
+PKV_API pkv_status pkv_seq_fork(pkv_pool* pool, int64_t parent_id, int64_t child_id);
+
+/* Finish a sequence and return its unshared blocks to the stack. */
+PKV_API pkv_status pkv_seq_free(pkv_pool* pool, int64_t seq_id);
+
+/* Copy one block table (logical order) into out[cap]; *n_blocks and
+ * *context_len receive its length and the sequence's token count.  out may
+ * be NULL when cap is 0 (query only); INVALID_ARG if cap is too small. */
+PKV_API pkv_status pkv_seq_table(const pkv_pool* pool, int64_t seq_id, int32_t* out, int32_t cap,
+                         int32_t* n_blocks, int64_t* context_len);
+
+/* Tables of a batch as host int32[n_seqs][max_blocks], padded with -1, and
+ * their context lengths int32[n_seqs].  INVALID_ARG if a table is longer
+ * than max_blocks or a length exceeds INT32_MAX. */
+PKV_API pkv_status pkv_block_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_t n_seqs,
+                            int32_t max_blocks, int32_t* tables_out, int32_t* context_lens_out);
+
+/* Reference count of one block (0 = free). */
+PKV_API pkv_status pkv_block_refcount(const pkv_pool* pool, int32_t block, int32_t* refcount);
+
+/* Blocks on the free stack. */
+PKV_API int32_t pkv_num_free_blocks(const pkv_pool* pool);
+
+/* The free stack, top first, into out[cap]; *n receives its size. */
+PKV_API pkv_status pkv_free_stack(const pkv_pool* pool, int32_t* out, int32_t cap, int32_t* n);
+
+/* Live sequences, tokens they hold, and token slots their blocks provide
+ * (shared blocks counted once); slots - tokens is the reserved-but-empty
+ * space the pages call waste ([C "Evals"]). */
+PKV_API pkv_status pkv_pool_usage(const pkv_pool* pool, int64_t* live_seqs, int64_t* live_tokens,
+                          int64_t* used_blocks);
+
+/* ------------------------------------------------------ device kernels */
+
+/* Slot write ("the number of new tokens about to be written" [C "In and
+ * out"]): for token i with slot_mapping[i] = s >= 0,
+ *   k_cache[s / T][h][s % T][:] = k[i][h][:]   (and v likewise)
+ * for every KV head h.  Tokens with s < 0, or s >= num_blocks * T, are
+ * skipped.
+ *   k, v          : device [n_tokens][num_kv_heads][head_dim] of src_dtype
+ *                   (F32, F16 or BF16), 16-byte aligned, contiguous.
+ *   slot_mapping  : device int64[n_tokens].
+ *   k_inv_scale, v_inv_scale : for an E4M3 cache the stored byte is
+ *                   e4m3_satfinite(round_fp32(x * inv_scale)); ignored
+ *                   otherwise.  A 16/32-bit cache requires src_dtype ==
+ *                   kv_dtype and stores the input bits unchanged. */
+PKV_API pkv_status pkv_write(void* k_cache, void* v_cache, const void* k, const void* v,
+                     int32_t src_dtype, const int64_t* slot_mapping, int32_t n_tokens,
+                     const pkv_kv_desc* desc, float k_inv_scale, float v_inv_scale,
+                     void* stream);
+
+/* Copy-on-write block copy ([B "Sharing"], [C "Concept"]): for each pair
+ * (src, dst) and each layer l, block dst of k_caches[l] and v_caches[l]
+ * becomes a byte copy of block src.
+ *   k_caches, v_caches : host arrays of num_layers device pointers (<= 128).
+ *   src_dst            : HOST int32[2 * n_pairs] (as returned by the
+ *                        allocator); ids are checked against num_blocks.
+ * Pairs must not overlap (no dst appears twice or as another pair's src); the
+ * allocator never produces overlapping pairs. */
+PKV_API pkv_status pkv_copy_blocks(void* const* k_caches, void* const* v_caches, int32_t num_layers,
+                           const int32_t* src_dst, int32_t n_pairs, const pkv_kv_desc* desc,
+                           void* stream);
+
+/* Workspace bytes pkv_attention_decode needs for these sizes (split-K
+ * partial results and merge counters).  0 if no split is needed. */
+PKV_API size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks,
+                                     const pkv_kv_desc* desc, int32_t partition_tokens);
+
+/* Partition (tokens per split) pkv_attention_decode uses for these sizes. */
+PKV_API int32_t pkv_attention_partition(int32_t num_seqs, int32_t max_blocks, const pkv_kv_desc* desc,
+                                int32_t partition_tokens);
+
+/* Single-token decode attention through block tables ([D]: "the attention
+ * kernel reads the block table and gathers keys and values"; [C "Concept"]):
+ *   out[s][j][:] = softmax_p( q[s][j] . K_s[p] * softmax_scale ) V_s[p]
+ * over logical positions p in [0, context_lens[s]), where
+ *   K_s[p] = k_cache[block_tables[s][p / T]][j / G][p % T][:] * k_scale
+ * (V likewise), G = num_q_heads / num_kv_heads (query head j reads KV head
+ * j / G).  k_scale / v_scale multiply E4M3 caches and are ignored otherwise.
+ *   out, q        : device [num_seqs][num_q_heads][head_dim] of q_dtype
+ *                   (F32 with an F32 cache, F16 or BF16 with 16-bit and E4M3
+ *                   caches); out has q's dtype.
+ *   block_tables  : device int32[num_seqs][max_blocks]; entries past
+ *                   ceil(ctx / T) are not read.
+ *   context_lens  : device int32[num_seqs]; a length of 0 gives a zero output.
+ *   partition_tokens : tokens per split-K partition, 0 = automatic; a
+ *                   multiple of 64 and of block_size.  Split boundaries are
+ *                   fixed logical positions, so results do not depend on
+ *                   which physical blocks hold the tokens.
+ *   workspace     : device buffer of at least
+ *                   pkv_attention_workspace_bytes(...) bytes, 256-byte
+ *                   aligned, ZERO-FILLED before its first use (every call
+ *                   leaves it zeroed again); may be NULL if that size is 0.
+ *                   Calls that share one workspace must not overlap in time.
+ * Inputs the kernel finds invalid (a table entry outside [0, num_blocks) or a
+ * context length outside [0, max_blocks * T]) make the affected heads' output
+ * NaN; nothing outside the given buffers is read or written. */
+PKV_API pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_dtype, const void* k_cache,
+                                const void* v_cache, const int32_t* block_tables,
+                                int32_t max_blocks, const int32_t* context_lens,
+                                int32_t num_seqs, int32_t num_q_heads, const pkv_kv_desc* desc,
+                                float softmax_scale, float k_scale, float v_scale,
+                                int32_t partition_tokens, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Message of the calling thread's last failure ("" if none). */
+PKV_API const char* pkv_last_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PKV_H */

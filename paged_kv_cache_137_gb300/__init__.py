@@ -1,0 +1,340 @@
+"""GB300-native paged KV cache: Python binding of libpkv.so.
+
+The functions below carry the names of the C ABI in ``include/pkv.h`` and do
+argument marshalling only (tensor checks, pointers, the current CUDA stream);
+every step of the data path runs in the library's CUDA kernels or its native
+host allocator.  Device memory comes from PyTorch tensors owned by the caller.
+There is no fallback: if the library is not built, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+import torch
+
+from ._build import LIB, build  # noqa: F401
+
+PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OUT_OF_BLOCKS, PKV_ERR_UNKNOWN_SEQ, PKV_ERR_UNSUPPORTED, \
+    PKV_ERR_CUDA = range(6)
+PKV_F32, PKV_F16, PKV_BF16, PKV_E4M3 = range(4)
+
+STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "OUT_OF_BLOCKS", 3: "UNKNOWN_SEQ", 4: "UNSUPPORTED",
+                5: "CUDA"}
+DTYPE_OF_NAME = {"f32": PKV_F32, "f16": PKV_F16, "bf16": PKV_BF16, "e4m3": PKV_E4M3}
+TORCH_OF_DTYPE = {PKV_F32: torch.float32, PKV_F16: torch.float16, PKV_BF16: torch.bfloat16,
+                  PKV_E4M3: torch.uint8}
+
+
+class PkvError(RuntimeError):
+    def __init__(self, status: int, message: str):
+        super().__init__(f"{STATUS_NAMES.get(status, status)}: {message}")
+        self.status = status
+        self.code = STATUS_NAMES.get(status, str(status))
+
+
+class pkv_kv_desc(ctypes.Structure):
+    _fields_ = [("num_blocks", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
+                ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
+                ("kv_dtype", ctypes.c_int32)]
+
+    @property
+    def elem_bytes(self) -> int:
+        return {PKV_F32: 4, PKV_F16: 2, PKV_BF16: 2, PKV_E4M3: 1}[self.kv_dtype]
+
+    @property
+    def torch_dtype(self):
+        return TORCH_OF_DTYPE[self.kv_dtype]
+
+    @property
+    def cache_shape(self):
+        return (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
+
+
+def kv_desc(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype) -> pkv_kv_desc:
+    if isinstance(kv_dtype, str):
+        kv_dtype = DTYPE_OF_NAME[kv_dtype]
+    return pkv_kv_desc(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype)
+
+
+_lib = None
+_P = ctypes.c_void_p
+_I32, _I64, _U64, _F = ctypes.c_int32, ctypes.c_int64, ctypes.c_uint64, ctypes.c_float
+_PI32, _PI64 = ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+_PDESC = ctypes.POINTER(pkv_kv_desc)
+
+_SIGNATURES = {
+    "pkv_block_bytes": (_U64, [_I32, _I32, _I32, _I32, _I32]),
+    "pkv_num_blocks_for_budget": (_U64, [_U64, _U64]),
+    "pkv_dtype_bytes": (_I32, [_I32]),
+    "pkv_pool_create": (_I32, [_I32, _I32, _PI32, ctypes.POINTER(_P)]),
+    "pkv_pool_destroy": (None, [_P]),
+    "pkv_seq_create": (_I32, [_P, _I64]),
+    "pkv_seq_append": (_I32, [_P, _I64, _I32, _PI64, _PI32, _I32, _PI32]),
+    "pkv_batch_append": (_I32, [_P, _PI64, _I32, _PI64, _PI32, _I32, _PI32]),
+    "pkv_seq_fork": (_I32, [_P, _I64, _I64]),
+    "pkv_seq_free": (_I32, [_P, _I64]),
+    "pkv_seq_table": (_I32, [_P, _I64, _PI32, _I32, _PI32, _PI64]),
+    "pkv_block_tables": (_I32, [_P, _PI64, _I32, _I32, _PI32, _PI32]),
+    "pkv_block_refcount": (_I32, [_P, _I32, _PI32]),
+    "pkv_num_free_blocks": (_I32, [_P]),
+    "pkv_free_stack": (_I32, [_P, _PI32, _I32, _PI32]),
+    "pkv_pool_usage": (_I32, [_P, _PI64, _PI64, _PI64]),
+    "pkv_write": (_I32, [_P, _P, _P, _P, _I32, _P, _I32, _PDESC, _F, _F, _P]),
+    "pkv_copy_blocks": (_I32, [ctypes.POINTER(_P), ctypes.POINTER(_P), _I32, _PI32, _I32, _PDESC, _P]),
+    "pkv_attention_workspace_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _PDESC, _I32]),
+    "pkv_attention_partition": (_I32, [_I32, _I32, _PDESC, _I32]),
+    "pkv_attention_decode": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F, _F, _F,
+                                    _I32, _P, ctypes.c_size_t, _P]),
+    "pkv_last_error": (ctypes.c_char_p, []),
+}
+EXPORTED = tuple(_SIGNATURES)
+
+
+def lib():
+    """The loaded libpkv (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(LIB):
+            raise RuntimeError(f"{LIB} is missing: build it with paged_kv_cache_137_gb300.build()")
+        handle = ctypes.CDLL(LIB)
+        for name, (res, args) in _SIGNATURES.items():
+            fn = getattr(handle, name)
+            fn.restype = res
+            fn.argtypes = args
+        _lib = handle
+    return _lib
+
+
+def _check(status: int):
+    if status != PKV_OK:
+        raise PkvError(status, lib().pkv_last_error().decode())
+
+
+def _i32p(a: np.ndarray):
+    return a.ctypes.data_as(_PI32)
+
+
+def _i64p(a: np.ndarray):
+    return a.ctypes.data_as(_PI64)
+
+
+def _stream(stream) -> int | None:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return stream.cuda_stream if hasattr(stream, "cuda_stream") else int(stream)
+
+
+def _dev(t: torch.Tensor, name: str, dtype=None):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise ValueError(f"{name} must be {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    m = {torch.float32: PKV_F32, torch.float16: PKV_F16, torch.bfloat16: PKV_BF16}
+    if t.dtype not in m:
+        raise ValueError(f"unsupported dtype {t.dtype}")
+    return m[t.dtype]
+
+
+# ------------------------------------------------------------------ sizing
+def pkv_block_bytes(num_layers, num_kv_heads, head_dim, block_size, elem_bytes) -> int:
+    return int(lib().pkv_block_bytes(num_layers, num_kv_heads, head_dim, block_size, elem_bytes))
+
+
+def pkv_num_blocks_for_budget(budget_bytes, block_bytes) -> int:
+    return int(lib().pkv_num_blocks_for_budget(int(budget_bytes), int(block_bytes)))
+
+
+def pkv_dtype_bytes(dtype) -> int:
+    return int(lib().pkv_dtype_bytes(DTYPE_OF_NAME.get(dtype, dtype)))
+
+
+# --------------------------------------------------------------- allocator
+class Pool:
+    """A native block allocator (free stack, tables, reference counts)."""
+
+    def __init__(self, num_blocks: int, block_size: int, initial_free_order=None):
+        self.num_blocks, self.block_size = int(num_blocks), int(block_size)
+        h = _P()
+        order = None
+        if initial_free_order is not None:
+            order = np.ascontiguousarray(initial_free_order, dtype=np.int32)
+            if order.shape != (self.num_blocks,):
+                raise ValueError("initial_free_order must hold num_blocks ids")
+        _check(lib().pkv_pool_create(self.num_blocks, self.block_size,
+                                     _i32p(order) if order is not None else None, ctypes.byref(h)))
+        self._h = h
+
+    def __del__(self):
+        if getattr(self, "_h", None) and _lib is not None:
+            _lib.pkv_pool_destroy(self._h)
+            self._h = None
+
+    @property
+    def handle(self):
+        return self._h
+
+    def seq_create(self, seq_id: int):
+        _check(lib().pkv_seq_create(self._h, int(seq_id)))
+
+    def seq_append(self, seq_id: int, n_new: int):
+        """-> (slots int64[n_new], cow pairs int32[n, 2])"""
+        slots = np.empty(max(n_new, 1), dtype=np.int64)
+        cow = np.empty(2, dtype=np.int32)
+        n_cow = ctypes.c_int32(0)
+        _check(lib().pkv_seq_append(self._h, int(seq_id), int(n_new), _i64p(slots), _i32p(cow), 1,
+                                    ctypes.byref(n_cow)))
+        return slots[:n_new], cow[:2 * n_cow.value].reshape(-1, 2)
+
+    def batch_append(self, seq_ids):
+        """One token per sequence, all-or-nothing -> (slots int64[B], cow int32[n, 2])"""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = len(ids)
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        cow = np.empty(2 * max(n, 1), dtype=np.int32)
+        n_cow = ctypes.c_int32(0)
+        _check(lib().pkv_batch_append(self._h, _i64p(ids), n, _i64p(slots), _i32p(cow), n,
+                                      ctypes.byref(n_cow)))
+        return slots[:n], cow[:2 * n_cow.value].reshape(-1, 2)
+
+    def seq_fork(self, parent: int, child: int):
+        _check(lib().pkv_seq_fork(self._h, int(parent), int(child)))
+
+    def seq_free(self, seq_id: int):
+        _check(lib().pkv_seq_free(self._h, int(seq_id)))
+
+    def seq_table(self, seq_id: int):
+        """-> (table int32[n_blocks], context_len)"""
+        n = ctypes.c_int32(0)
+        ln = ctypes.c_int64(0)
+        _check(lib().pkv_seq_table(self._h, int(seq_id), None, 0, ctypes.byref(n), ctypes.byref(ln)))
+        out = np.empty(max(n.value, 1), dtype=np.int32)
+        _check(lib().pkv_seq_table(self._h, int(seq_id), _i32p(out), len(out), ctypes.byref(n),
+                                   ctypes.byref(ln)))
+        return out[:n.value], ln.value
+
+    def block_tables(self, seq_ids, max_blocks: int):
+        """-> (tables int32[B, max_blocks] padded with -1, context_lens int32[B])"""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        tables = np.empty((len(ids), max_blocks), dtype=np.int32)
+        ctx = np.empty(len(ids), dtype=np.int32)
+        _check(lib().pkv_block_tables(self._h, _i64p(ids), len(ids), int(max_blocks), _i32p(tables),
+                                      _i32p(ctx)))
+        return tables, ctx
+
+    def block_refcount(self, block: int) -> int:
+        rc = ctypes.c_int32(0)
+        _check(lib().pkv_block_refcount(self._h, int(block), ctypes.byref(rc)))
+        return rc.value
+
+    def num_free_blocks(self) -> int:
+        return int(lib().pkv_num_free_blocks(self._h))
+
+    def free_stack(self) -> np.ndarray:
+        """The free stack, top first."""
+        n = ctypes.c_int32(0)
+        _check(lib().pkv_free_stack(self._h, None, 0, ctypes.byref(n)))
+        out = np.empty(max(n.value, 1), dtype=np.int32)
+        _check(lib().pkv_free_stack(self._h, _i32p(out), len(out), ctypes.byref(n)))
+        return out[:n.value]
+
+    def usage(self):
+        """-> (live sequences, live tokens, blocks in use)"""
+        a, b, c = ctypes.c_int64(), ctypes.c_int64(), ctypes.c_int64()
+        _check(lib().pkv_pool_usage(self._h, ctypes.byref(a), ctypes.byref(b), ctypes.byref(c)))
+        return a.value, b.value, c.value
+
+
+def pkv_pool_create(num_blocks, block_size, initial_free_order=None) -> Pool:
+    return Pool(num_blocks, block_size, initial_free_order)
+
+
+# ------------------------------------------------------------------ device
+def empty_cache(desc: pkv_kv_desc, device="cuda", fill_byte: int | None = None):
+    """One layer's (K, V) cache tensors [num_blocks, N_kv, T, D]."""
+    k = torch.empty(desc.cache_shape, dtype=desc.torch_dtype, device=device)
+    v = torch.empty_like(k)
+    if fill_byte is not None:
+        k.view(torch.uint8).fill_(fill_byte)
+        v.view(torch.uint8).fill_(fill_byte)
+    return k, v
+
+
+def pkv_write(k_cache, v_cache, k, v, slot_mapping, desc: pkv_kv_desc, k_inv_scale=1.0,
+              v_inv_scale=1.0, stream=None):
+    """Write each token's K/V [n, N_kv, D] into its slot (slot_mapping int64[n])."""
+    n = k.shape[0]
+    if k.shape != (n, desc.num_kv_heads, desc.head_dim) or v.shape != k.shape or v.dtype != k.dtype:
+        raise ValueError("k and v must be [n_tokens, num_kv_heads, head_dim] of one dtype")
+    if slot_mapping.shape != (n,):
+        raise ValueError("slot_mapping must be int64[n_tokens]")
+    for t, name in ((k_cache, "k_cache"), (v_cache, "v_cache")):
+        if tuple(t.shape) != desc.cache_shape or t.dtype != desc.torch_dtype:
+            raise ValueError(f"{name} must be {desc.torch_dtype}{desc.cache_shape}")
+    _check(lib().pkv_write(_dev(k_cache, "k_cache"), _dev(v_cache, "v_cache"), _dev(k, "k"),
+                           _dev(v, "v"), _dtype_code(k), _dev(slot_mapping, "slot_mapping", torch.int64),
+                           n, ctypes.byref(desc), float(k_inv_scale), float(v_inv_scale),
+                           _stream(stream)))
+
+
+def pkv_copy_blocks(k_caches, v_caches, src_dst, desc: pkv_kv_desc, stream=None):
+    """Copy blocks src -> dst in every layer; src_dst is a host int32 [n, 2]."""
+    pairs = np.ascontiguousarray(np.asarray(src_dst, dtype=np.int32).reshape(-1))
+    n = len(pairs) // 2
+    if n == 0:
+        return
+    if len(k_caches) != len(v_caches):
+        raise ValueError("k_caches and v_caches differ in length")
+    for t in list(k_caches) + list(v_caches):
+        if tuple(t.shape) != desc.cache_shape or t.dtype != desc.torch_dtype:
+            raise ValueError("cache tensors do not match desc")
+    kp = (_P * len(k_caches))(*[_dev(t, "k_cache") for t in k_caches])
+    vp = (_P * len(v_caches))(*[_dev(t, "v_cache") for t in v_caches])
+    _check(lib().pkv_copy_blocks(kp, vp, len(k_caches), _i32p(pairs), n, ctypes.byref(desc),
+                                 _stream(stream)))
+
+
+def pkv_attention_workspace_bytes(num_seqs, num_q_heads, max_blocks, desc: pkv_kv_desc,
+                                  partition_tokens=0) -> int:
+    return int(lib().pkv_attention_workspace_bytes(num_seqs, num_q_heads, max_blocks,
+                                                   ctypes.byref(desc), partition_tokens))
+
+
+def pkv_attention_partition(num_seqs, max_blocks, desc: pkv_kv_desc, partition_tokens=0) -> int:
+    return int(lib().pkv_attention_partition(num_seqs, max_blocks, ctypes.byref(desc), partition_tokens))
+
+
+def workspace_for(num_seqs, num_q_heads, max_blocks, desc, partition_tokens=0, device="cuda"):
+    """A zero-filled workspace tensor of the size the decode call needs (None if 0)."""
+    n = pkv_attention_workspace_bytes(num_seqs, num_q_heads, max_blocks, desc, partition_tokens)
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
+
+
+def pkv_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, desc: pkv_kv_desc,
+                         softmax_scale, k_scale=1.0, v_scale=1.0, partition_tokens=0,
+                         workspace=None, stream=None):
+    """Decode attention of q [B, Hq, D] through block tables int32[B, max_blocks]."""
+    b, hq, d = q.shape
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    if block_tables.dim() != 2 or block_tables.shape[0] != b:
+        raise ValueError("block_tables must be int32[B, max_blocks]")
+    if context_lens.shape != (b,):
+        raise ValueError("context_lens must be int32[B]")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    _check(lib().pkv_attention_decode(
+        _dev(out, "out"), _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache", desc.torch_dtype),
+        _dev(v_cache, "v_cache", desc.torch_dtype), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), b, hq,
+        ctypes.byref(desc), float(softmax_scale), float(k_scale), float(v_scale),
+        int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)))
+    return out

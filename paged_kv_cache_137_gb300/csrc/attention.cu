@@ -1,0 +1,217 @@
+// Decode attention front end: argument checks, split-K partition choice,
+// workspace layout, kernel selection and the split-K merge.
+//
+// Split-K (flash-decoding) is not described on the pages; it is how one
+// sequence's positions are spread over several CTAs when the batch alone
+// cannot fill the GPU.  Each split reports its running maximum m_i (log2
+// domain), sum l_i and unnormalised output a_i; the merge forms
+//   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  o = sum_i a_i 2^(m_i - M) / L,
+// which equals the softmax over the union of the splits' positions.
+#include <algorithm>
+
+#include <math_constants.h>
+
+#include "attention.h"
+#include "device_common.cuh"
+
+namespace pkv {
+
+// launch_decode_simt<KV, Q> is instantiated in attention_simt_<kv>_<q>.cu.
+
+namespace {
+
+constexpr int kTargetUnits = 2048;  // split-K work units the automatic partition aims for
+constexpr int kMinPartition = 256;
+constexpr int kMaxPartition = 8192;
+
+int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx) {
+  // Expected (sequence, head, split) units if lengths spread evenly up to max_ctx.
+  const int64_t est_tokens = num_seqs * num_kv_heads * std::max<int64_t>(max_ctx, 1) / 2;
+  int32_t p = kMinPartition;
+  while (p < kMaxPartition && est_tokens / p > kTargetUnits) p *= 2;
+  return p;
+}
+
+size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+struct WsLayout {
+  size_t m_off, l_off, acc_off, bytes;
+};
+
+WsLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t splits, int64_t head_dim) {
+  WsLayout w{};
+  if (splits <= 1) return w;
+  const size_t n = static_cast<size_t>(num_seqs * num_q_heads * splits);
+  w.m_off = 0;
+  w.l_off = align_up(n * sizeof(float), 256);
+  w.acc_off = w.l_off + align_up(n * sizeof(float), 256);
+  w.bytes = w.acc_off + align_up(n * head_dim * sizeof(float), 256);
+  return w;
+}
+
+template <typename Q, int D>
+__global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
+  const int qh = blockIdx.x, seq = blockIdx.y;
+  const int ctx = a.ctx_lens[seq];
+  if (ctx < 0 || ctx > a.max_blocks * a.block_size) return;  // written by the decode kernel
+  const int nsplit = max(1, (ctx + a.partition - 1) / a.partition);
+  if (nsplit <= 1) return;
+  const size_t base = (static_cast<size_t>(seq) * a.num_q_heads + qh) * a.max_splits;
+  float M = -CUDART_INF_F;
+  for (int i = 0; i < nsplit; ++i) M = fmaxf(M, a.ws_m[base + i]);
+  for (int d = threadIdx.x; d < D; d += blockDim.x) {
+    float L = 0.f, A = 0.f;
+    if (M != -CUDART_INF_F) {
+      for (int i = 0; i < nsplit; ++i) {
+        const float f = exp2f(a.ws_m[base + i] - M);
+        L = fmaf(a.ws_l[base + i], f, L);
+        A = fmaf(a.ws_acc[(base + i) * D + d], f, A);
+      }
+    }
+    const float o = (L > 0.f || L != L) ? A / L : 0.f;
+    store_elem<Q>(a.out, (static_cast<size_t>(seq) * a.num_q_heads + qh) * D + d, o);
+  }
+}
+
+template <typename Q>
+pkv_status launch_merge(const DecodeArgs& a, int head_dim, cudaStream_t st) {
+  const dim3 grid(a.num_q_heads, a.num_seqs);
+  if (head_dim == 128) merge_kernel<Q, 128><<<grid, 128, 0, st>>>(a);
+  else merge_kernel<Q, 64><<<grid, 64, 0, st>>>(a);
+  return check_launch("pkv_attention_decode (merge)");
+}
+
+pkv_status resolve_partition(int32_t requested, int32_t num_seqs, int32_t max_blocks,
+                             const pkv_kv_desc* d, int32_t* out) {
+  if (requested < 0) return fail(PKV_ERR_INVALID_ARG, "partition_tokens is negative");
+  if (requested > 0) {
+    if (requested % 64 != 0 || requested % d->block_size != 0)
+      return fail(PKV_ERR_INVALID_ARG, "partition_tokens must be a multiple of 64 and of block_size");
+    *out = requested;
+    return PKV_OK;
+  }
+  *out = auto_partition(num_seqs, d->num_kv_heads, static_cast<int64_t>(max_blocks) * d->block_size);
+  return PKV_OK;
+}
+
+int64_t num_splits(int32_t max_blocks, int32_t block_size, int32_t partition) {
+  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * block_size;
+  return std::max<int64_t>(1, (max_ctx + partition - 1) / partition);
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" int32_t pkv_attention_partition(int32_t num_seqs, int32_t max_blocks,
+                                           const pkv_kv_desc* desc, int32_t partition_tokens) {
+  if (check_desc(desc) != PKV_OK || num_seqs < 0 || max_blocks < 0) return 0;
+  int32_t p = 0;
+  if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
+  return p;
+}
+
+extern "C" size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                                int32_t max_blocks, const pkv_kv_desc* desc,
+                                                int32_t partition_tokens) {
+  if (check_desc(desc) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 || max_blocks <= 0) return 0;
+  int32_t p = 0;
+  if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
+  const int64_t s = num_splits(max_blocks, desc->block_size, p);
+  return workspace_layout(num_seqs, num_q_heads, s, desc->head_dim).bytes;
+}
+
+extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_dtype,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_tables, int32_t max_blocks,
+                                           const int32_t* context_lens, int32_t num_seqs,
+                                           int32_t num_q_heads, const pkv_kv_desc* desc,
+                                           float softmax_scale, float k_scale, float v_scale,
+                                           int32_t partition_tokens, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (num_seqs < 0 || num_q_heads <= 0 || max_blocks < 0)
+    return fail(PKV_ERR_INVALID_ARG, "negative size or no query heads");
+  if (num_seqs == 0) return PKV_OK;
+  if (num_seqs > 65535) return fail(PKV_ERR_UNSUPPORTED, "more than 65535 sequences per call");
+  if (max_blocks == 0) return fail(PKV_ERR_INVALID_ARG, "max_blocks is 0");
+  if (num_q_heads % desc->num_kv_heads != 0)
+    return fail(PKV_ERR_INVALID_ARG, "num_q_heads must be a multiple of num_kv_heads");
+  if (!out || !q || !k_cache || !v_cache || !block_tables || !context_lens)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  for (const void* p : {static_cast<const void*>(out), q, k_cache, v_cache})
+    if (!aligned(p, 16)) return fail(PKV_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  if (!aligned(block_tables, 4) || !aligned(context_lens, 4))
+    return fail(PKV_ERR_INVALID_ARG, "tables misaligned");
+  if (static_cast<int64_t>(max_blocks) * desc->block_size > (int64_t{1} << 30))
+    return fail(PKV_ERR_UNSUPPORTED, "context longer than 2^30 tokens");
+  if (!(softmax_scale == softmax_scale)) return fail(PKV_ERR_INVALID_ARG, "softmax_scale is NaN");
+
+  const int kv = desc->kv_dtype;
+  const bool pair_ok = (kv == PKV_F32 && q_dtype == PKV_F32) ||
+                       (kv == PKV_F16 && q_dtype == PKV_F16) ||
+                       (kv == PKV_BF16 && q_dtype == PKV_BF16) ||
+                       (kv == PKV_E4M3 && (q_dtype == PKV_F16 || q_dtype == PKV_BF16));
+  if (!pair_ok) return fail(PKV_ERR_INVALID_ARG, "unsupported (kv_dtype, q_dtype) pair");
+
+  const int group = num_q_heads / desc->num_kv_heads;
+  int gm = 1;
+  while (gm < group) gm = gm == 1 ? 4 : gm * 2;
+  if (gm > 16) return fail(PKV_ERR_UNSUPPORTED, "more than 16 query heads per KV head");
+
+  int32_t partition = 0;
+  st = resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &partition);
+  if (st != PKV_OK) return st;
+  const int64_t splits = num_splits(max_blocks, desc->block_size, partition);
+  if (splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits");
+  const WsLayout ws = workspace_layout(num_seqs, num_q_heads, splits, desc->head_dim);
+  if (ws.bytes > 0) {
+    if (!workspace || workspace_bytes < ws.bytes)
+      return fail(PKV_ERR_INVALID_ARG, "workspace missing or smaller than pkv_attention_workspace_bytes");
+    if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
+  }
+
+  DecodeArgs a{};
+  a.out = out;
+  a.q = q;
+  a.k_cache = k_cache;
+  a.v_cache = v_cache;
+  a.tables = block_tables;
+  a.ctx_lens = context_lens;
+  uint8_t* wsb = static_cast<uint8_t*>(workspace);
+  a.ws_m = ws.bytes ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+  a.ws_l = ws.bytes ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
+  a.ws_acc = ws.bytes ? reinterpret_cast<float*>(wsb + ws.acc_off) : nullptr;
+  a.max_blocks = max_blocks;
+  a.num_seqs = num_seqs;
+  a.num_q_heads = num_q_heads;
+  a.num_kv_heads = desc->num_kv_heads;
+  a.group = group;
+  a.num_blocks = desc->num_blocks;
+  a.block_size = desc->block_size;
+  a.partition = partition;
+  a.max_splits = static_cast<int32_t>(splits);
+  const bool fp8 = kv == PKV_E4M3;
+  a.qk_scale = softmax_scale * (fp8 ? k_scale : 1.0f) * 1.4426950408889634f;
+  a.v_scale = fp8 ? v_scale : 1.0f;
+
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int D = desc->head_dim;
+  switch (kv) {
+    case PKV_F32: st = launch_decode_simt<F32, F32>(a, D, gm, s); break;
+    case PKV_F16: st = launch_decode_simt<F16, F16>(a, D, gm, s); break;
+    case PKV_BF16: st = launch_decode_simt<BF16, BF16>(a, D, gm, s); break;
+    case PKV_E4M3:
+      st = q_dtype == PKV_F16 ? launch_decode_simt<E4M3, F16>(a, D, gm, s)
+                              : launch_decode_simt<E4M3, BF16>(a, D, gm, s);
+      break;
+  }
+  if (st != PKV_OK || splits <= 1) return st;
+  switch (q_dtype) {
+    case PKV_F32: return launch_merge<F32>(a, D, s);
+    case PKV_F16: return launch_merge<F16>(a, D, s);
+    default: return launch_merge<BF16>(a, D, s);
+  }
+}

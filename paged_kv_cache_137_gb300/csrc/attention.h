@@ -1,0 +1,37 @@
+// Internal interface between the decode-attention front end (attention.cu) and
+// the kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pkv.h"
+
+namespace pkv {
+
+// Everything a decode-attention kernel needs; passed by value as the kernel
+// parameter.
+struct DecodeArgs {
+  void* out;                 // [B][Hq][D] q dtype
+  const void* q;             // [B][Hq][D] q dtype
+  const void* k_cache;       // [num_blocks][N_kv][T][D]
+  const void* v_cache;
+  const int32_t* tables;     // [B][max_blocks]
+  const int32_t* ctx_lens;   // [B]
+  float* ws_m;               // split-K partial maxima   [B][Hq][S] (log2 domain)
+  float* ws_l;               // split-K partial sums      [B][Hq][S]
+  float* ws_acc;             // split-K partial outputs   [B][Hq][S][D]
+  int32_t max_blocks, num_seqs, num_q_heads, num_kv_heads, group, num_blocks, block_size;
+  int32_t partition;         // tokens per split (multiple of 64 and of T)
+  int32_t max_splits;        // S
+  float qk_scale;            // softmax_scale * k_scale * log2(e)
+  float v_scale;             // 1, or the E4M3 V scale
+};
+
+// Launch the CUDA-core decode kernel for one (cache dtype, q dtype) pair;
+// returns PKV_ERR_UNSUPPORTED for a shape it was not compiled for.
+template <typename KV, typename Q>
+pkv_status launch_decode_simt(const DecodeArgs& a, int head_dim, int group_padded,
+                              cudaStream_t stream);
+
+}  // namespace pkv

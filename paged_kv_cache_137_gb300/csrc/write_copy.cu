@@ -1,0 +1,188 @@
+// Slot write and copy-on-write block copy.
+//
+// Slot write: each decode step writes the new tokens' keys and values into the
+// slots the allocator reserved (foundry page on paged block allocation, "In
+// and out": the number of new tokens about to be written).  Block copy: a
+// shared block is copied before a branch writes into it (same page,
+// "Concept"; katajob Q&A, "Sharing, the second dividend").
+//
+// Both are tiny, latency-bound kernels: 16-byte vector accesses, one thread
+// per 8-element unit of a (token, head) row for the write and one CTA per
+// (pair, layer, K|V) tile for the copy.  The copy takes its pairs and layer
+// pointers as kernel parameters, so it needs no device-side staging buffer.
+#include <algorithm>
+#include <type_traits>
+
+#include "device_common.cuh"
+
+namespace pkv {
+namespace {
+
+struct WriteArgs {
+  void* cache[2];       // K, V caches
+  const void* src[2];   // K, V inputs [n_tokens][n_kv][D]
+  float inv_scale[2];
+  const int64_t* slots;
+  int64_t n_tokens;
+  int32_t n_kv, head_dim, block_size, num_blocks;
+};
+
+// One unit = 8 consecutive elements of one (token, head) row.
+template <typename Src, typename Dst>
+__global__ void __launch_bounds__(256) write_kernel(const WriteArgs a) {
+  const int which = blockIdx.y;  // 0 = K, 1 = V
+  const int units_per_row = a.head_dim / 8;
+  const int64_t units = a.n_tokens * a.n_kv * units_per_row;
+  const int64_t limit = static_cast<int64_t>(a.num_blocks) * a.block_size;
+  for (int64_t u = blockIdx.x * int64_t(blockDim.x) + threadIdx.x; u < units;
+       u += int64_t(gridDim.x) * blockDim.x) {
+    const int64_t tok = u / (a.n_kv * units_per_row);
+    const int rem = static_cast<int>(u - tok * a.n_kv * units_per_row);
+    const int h = rem / units_per_row;
+    const int d0 = (rem - h * units_per_row) * 8;
+    const int64_t slot = a.slots[tok];
+    if (slot < 0 || slot >= limit) continue;
+    const int64_t blk = slot / a.block_size;
+    const int off = static_cast<int>(slot - blk * a.block_size);
+    const size_t src_idx = (static_cast<size_t>(tok) * a.n_kv + h) * a.head_dim + d0;
+    const size_t dst_idx =
+        ((static_cast<size_t>(blk) * a.n_kv + h) * a.block_size + off) * a.head_dim + d0;
+    if constexpr (std::is_same<Dst, E4M3>::value) {
+      float f[8];
+      LoadF32<Src, 8>::run(static_cast<const typename Src::raw*>(a.src[which]) + src_idx, f);
+      const float inv = a.inv_scale[which];
+      uint2 packed;
+      uint16_t* q = reinterpret_cast<uint16_t*>(&packed);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) q[i] = f32x2_to_e4m3x2(f[2 * i] * inv, f[2 * i + 1] * inv);
+      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.cache[which]) + dst_idx) = packed;
+    } else {
+      static_assert(std::is_same<Src, Dst>::value, "16/32-bit caches store the input type");
+      using raw = typename Src::raw;
+      const uint4* s = reinterpret_cast<const uint4*>(static_cast<const raw*>(a.src[which]) + src_idx);
+      uint4* d = reinterpret_cast<uint4*>(static_cast<raw*>(a.cache[which]) + dst_idx);
+#pragma unroll
+      for (int i = 0; i < Src::bytes / 2; ++i) d[i] = s[i];
+    }
+  }
+}
+
+constexpr int kMaxCopyLayers = 128;
+constexpr int kMaxCopyPairs = 1024;
+
+struct CopyArgs {
+  void* k[kMaxCopyLayers];
+  void* v[kMaxCopyLayers];
+  int32_t src[kMaxCopyPairs];
+  int32_t dst[kMaxCopyPairs];
+  int64_t block_bytes;  // bytes of one block in one layer's K (or V) tensor
+};
+
+// grid: (pair, layer, K|V); each CTA copies one block of one tensor.
+__global__ void __launch_bounds__(256) copy_blocks_kernel(const __grid_constant__ CopyArgs a) {
+  const int pair = blockIdx.x, layer = blockIdx.y;
+  uint8_t* base = static_cast<uint8_t*>(blockIdx.z == 0 ? a.k[layer] : a.v[layer]);
+  const uint4* s = reinterpret_cast<const uint4*>(base + a.src[pair] * a.block_bytes);
+  uint4* d = reinterpret_cast<uint4*>(base + a.dst[pair] * a.block_bytes);
+  const int64_t n = a.block_bytes / 16;
+  for (int64_t i = threadIdx.x; i < n; i += blockDim.x) d[i] = s[i];
+}
+
+template <typename Src, typename Dst>
+pkv_status launch_write(const WriteArgs& a, cudaStream_t st) {
+  const int64_t units = a.n_tokens * a.n_kv * (a.head_dim / 8);
+  const int threads = 256;
+  const int64_t blocks = std::min<int64_t>((units + threads - 1) / threads, 4096);
+  write_kernel<Src, Dst><<<dim3(static_cast<unsigned>(blocks), 2), threads, 0, st>>>(a);
+  return check_launch("pkv_write");
+}
+
+}  // namespace
+}  // namespace pkv
+
+using namespace pkv;
+
+extern "C" pkv_status pkv_write(void* k_cache, void* v_cache, const void* k, const void* v,
+                                int32_t src_dtype, const int64_t* slot_mapping, int32_t n_tokens,
+                                const pkv_kv_desc* desc, float k_inv_scale, float v_inv_scale,
+                                void* stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (n_tokens < 0) return fail(PKV_ERR_INVALID_ARG, "n_tokens is negative");
+  if (n_tokens == 0) return PKV_OK;
+  if (!k_cache || !v_cache || !k || !v || !slot_mapping)
+    return fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  for (const void* p : {static_cast<const void*>(k_cache), static_cast<const void*>(v_cache), k, v})
+    if (!aligned(p, 16)) return fail(PKV_ERR_INVALID_ARG, "buffers must be 16-byte aligned");
+  if (!aligned(slot_mapping, 8)) return fail(PKV_ERR_INVALID_ARG, "slot_mapping misaligned");
+  WriteArgs a{};
+  a.cache[0] = k_cache;
+  a.cache[1] = v_cache;
+  a.src[0] = k;
+  a.src[1] = v;
+  a.inv_scale[0] = k_inv_scale;
+  a.inv_scale[1] = v_inv_scale;
+  a.slots = slot_mapping;
+  a.n_tokens = n_tokens;
+  a.n_kv = desc->num_kv_heads;
+  a.head_dim = desc->head_dim;
+  a.block_size = desc->block_size;
+  a.num_blocks = desc->num_blocks;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int kv = desc->kv_dtype;
+  if (kv == PKV_E4M3) {
+    switch (src_dtype) {
+      case PKV_F32: return launch_write<F32, E4M3>(a, s);
+      case PKV_F16: return launch_write<F16, E4M3>(a, s);
+      case PKV_BF16: return launch_write<BF16, E4M3>(a, s);
+      default: return fail(PKV_ERR_INVALID_ARG, "src_dtype must be F32, F16 or BF16");
+    }
+  }
+  if (src_dtype != kv)
+    return fail(PKV_ERR_INVALID_ARG, "a 16/32-bit cache needs src_dtype == kv_dtype");
+  switch (kv) {
+    case PKV_F32: return launch_write<F32, F32>(a, s);
+    case PKV_F16: return launch_write<F16, F16>(a, s);
+    case PKV_BF16: return launch_write<BF16, BF16>(a, s);
+  }
+  return fail(PKV_ERR_INVALID_ARG, "unknown kv_dtype");
+}
+
+extern "C" pkv_status pkv_copy_blocks(void* const* k_caches, void* const* v_caches,
+                                      int32_t num_layers, const int32_t* src_dst, int32_t n_pairs,
+                                      const pkv_kv_desc* desc, void* stream) {
+  pkv_status st = check_desc(desc);
+  if (st != PKV_OK) return st;
+  if (n_pairs < 0) return fail(PKV_ERR_INVALID_ARG, "n_pairs is negative");
+  if (n_pairs == 0) return PKV_OK;
+  if (num_layers <= 0 || num_layers > kMaxCopyLayers)
+    return fail(PKV_ERR_INVALID_ARG, "num_layers must be in [1, 128]");
+  if (!k_caches || !v_caches || !src_dst) return fail(PKV_ERR_INVALID_ARG, "NULL pointer");
+  for (int32_t l = 0; l < num_layers; ++l) {
+    if (!k_caches[l] || !v_caches[l]) return fail(PKV_ERR_INVALID_ARG, "NULL layer pointer");
+    if (!aligned(k_caches[l], 16) || !aligned(v_caches[l], 16))
+      return fail(PKV_ERR_INVALID_ARG, "caches must be 16-byte aligned");
+  }
+  for (int32_t i = 0; i < 2 * n_pairs; ++i)
+    if (src_dst[i] < 0 || src_dst[i] >= desc->num_blocks)
+      return fail(PKV_ERR_INVALID_ARG, "block id out of range");
+  CopyArgs a;
+  for (int32_t l = 0; l < num_layers; ++l) {
+    a.k[l] = k_caches[l];
+    a.v[l] = v_caches[l];
+  }
+  a.block_bytes = static_cast<int64_t>(desc->num_kv_heads) * desc->block_size * desc->head_dim *
+                  pkv_dtype_bytes(desc->kv_dtype);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  for (int32_t base = 0; base < n_pairs; base += kMaxCopyPairs) {
+    const int32_t n = std::min(kMaxCopyPairs, n_pairs - base);
+    for (int32_t i = 0; i < n; ++i) {
+      a.src[i] = src_dst[2 * (base + i)];
+      a.dst[i] = src_dst[2 * (base + i) + 1];
+    }
+    copy_blocks_kernel<<<dim3(n, num_layers, 2), 256, 0, s>>>(a);
+    st = check_launch("pkv_copy_blocks");
+    if (st != PKV_OK) return st;
+  }
+  return PKV_OK;
+}

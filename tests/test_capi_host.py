@@ -1,0 +1,175 @@
+"""The C ABI on the host (no GPU): the library loads, exports what the header
+declares, and its native allocator reproduces the oracle's tables, slots,
+copy-on-write pairs, reference counts and free stack bit for bit."""
+import json
+import os
+import random
+import re
+
+import numpy as np
+import pytest
+
+import workloads as W
+from oracle import scenario as OS
+from oracle.allocator import AllocError, BlockAllocator
+
+import paged_kv_cache_137_gb300 as pkv
+from paged_kv_cache_137_gb300 import scenario as PS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+GOLD = json.load(open(os.path.join(ROOT, "tests", "golden", "sizing_examples.json")))
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pkv.build()
+    pkv.lib()
+
+
+def header_functions():
+    names = set()
+    for fn in os.listdir(os.path.join(ROOT, "include")):
+        if fn.endswith(".h"):
+            text = open(os.path.join(ROOT, "include", fn)).read()
+            names |= set(re.findall(r"\b(pkv_[a-z0-9_]+)\s*\(", text))
+    return sorted(names)
+
+
+def test_every_declared_symbol_is_exported():
+    names = header_functions()
+    assert "pkv_attention_decode" in names and "pkv_write" in names and "pkv_copy_blocks" in names
+    handle = pkv.lib()
+    for n in names:
+        assert hasattr(handle, n), f"{n} declared in include/ but not exported"
+
+
+def test_binding_covers_the_header():
+    assert set(header_functions()) <= set(pkv.EXPORTED)
+
+
+def test_block_bytes_and_budget():
+    g = GOLD["block_bytes"]
+    assert pkv.pkv_block_bytes(g["num_layers"], g["num_kv_heads"], g["head_dim"], g["block_size"],
+                               g["elem_bytes"]) == g["bytes"]
+    assert pkv.pkv_block_bytes(0, 1, 1, 1, 1) == 0
+    g = GOLD["pool_capacity"]
+    n = pkv.pkv_num_blocks_for_budget(g["kv_budget_bytes"], g["block_bytes"])
+    assert abs(n - g["approx_blocks"]) / g["approx_blocks"] < g["rel_tol"]
+    assert pkv.pkv_dtype_bytes("e4m3") == 1 and pkv.pkv_dtype_bytes("bf16") == 2
+
+
+def _compare(native: pkv.Pool, ref: BlockAllocator, live):
+    assert native.num_free_blocks() == ref.num_free()
+    assert native.free_stack().tolist() == ref.free_stack_top_first()
+    for s in live:
+        tab, ln = native.seq_table(s)
+        assert tab.tolist() == ref.table(s) and ln == ref.context_len(s)
+    for b in range(ref.num_blocks):
+        assert native.block_refcount(b) == ref.block_refcount(b)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_native_allocator_matches_oracle_on_random_ops(seed):
+    rnd = random.Random(100 + seed)
+    t = rnd.choice([16, 32])
+    nb = rnd.choice([16, 64, 200])
+    order = rnd.sample(range(nb), nb)
+    native, ref = pkv.Pool(nb, t, order), BlockAllocator(nb, t, order)
+    live, nxt = [], 0
+    for step in range(400):
+        op = rnd.random()
+        if op < 0.15 or not live:
+            native.seq_create(nxt)
+            ref.create(nxt)
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.55:
+            s, n = rnd.choice(live), rnd.randint(0, 2 * t + 3)
+            try:
+                exp = ref.append(s, n)
+            except AllocError as e:
+                with pytest.raises(pkv.PkvError) as got:
+                    native.seq_append(s, n)
+                assert got.value.code == e.code
+            else:
+                slots, cow = native.seq_append(s, n)
+                assert slots.tolist() == exp[0] and [tuple(x) for x in cow.tolist()] == exp[1]
+        elif op < 0.7:
+            batch = rnd.sample(live, min(len(live), rnd.randint(1, 6)))
+            try:
+                exp = ref.append_batch(batch, 1)
+            except AllocError as e:
+                with pytest.raises(pkv.PkvError) as got:
+                    native.batch_append(batch)
+                assert got.value.code == e.code
+            else:
+                slots, cow = native.batch_append(batch)
+                assert slots.tolist() == exp[0] and [tuple(x) for x in cow.tolist()] == exp[1]
+        elif op < 0.82:
+            parent = rnd.choice(live)
+            native.seq_fork(parent, nxt)
+            ref.fork(parent, nxt)
+            live.append(nxt)
+            nxt += 1
+        else:
+            s = live.pop(rnd.randrange(len(live)))
+            native.seq_free(s)
+            ref.free_seq(s)
+        if step % 25 == 0:
+            _compare(native, ref, live)
+    _compare(native, ref, live)
+
+
+def test_errors_leave_state_unchanged():
+    p = pkv.Pool(4, 16)
+    p.seq_create(0)
+    p.seq_append(0, 40)
+    before = (p.free_stack().tolist(), p.seq_table(0)[0].tolist())
+    with pytest.raises(pkv.PkvError) as e:
+        p.seq_append(0, 40)
+    assert e.value.code == "OUT_OF_BLOCKS"
+    p.seq_create(1)
+    p.seq_create(2)
+    with pytest.raises(pkv.PkvError):
+        p.batch_append([1, 2])
+    assert (p.free_stack().tolist(), p.seq_table(0)[0].tolist()) == before
+    assert p.seq_table(1)[1] == 0 and p.seq_table(2)[1] == 0
+    with pytest.raises(pkv.PkvError) as e:
+        p.seq_append(9, 1)
+    assert e.value.code == "UNKNOWN_SEQ"
+    with pytest.raises(pkv.PkvError) as e:
+        p.seq_create(1)
+    assert e.value.code == "INVALID_ARG"
+    with pytest.raises(pkv.PkvError):
+        pkv.Pool(3, 16, [0, 1, 1])
+    with pytest.raises(pkv.PkvError):
+        p.block_refcount(4)
+
+
+def test_block_tables_padding_and_usage():
+    p = pkv.Pool(8, 16, [7, 6, 5, 4, 3, 2, 1, 0])
+    p.seq_create(5)
+    p.seq_append(5, 20)
+    p.seq_create(6)
+    tables, ctx = p.block_tables([5, 6], 3)
+    assert tables.tolist() == [[7, 6, -1], [-1, -1, -1]] and ctx.tolist() == [20, 0]
+    with pytest.raises(pkv.PkvError):
+        p.block_tables([5], 1)
+    assert p.usage() == (2, 20, 2)
+
+
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen_gqa_bf16", "prefix_fork_bf16", "long_mha_bf16",
+                                  "fp8_churn"])
+def test_workload_plans_match_oracle(name):
+    w = W.get(name)
+    native = PS.plan(w)
+    ref = OS.build(w, write_seqs=[], scales={"k_inv_scale": 1.0, "v_inv_scale": 1.0})
+    assert native.seq_ids == ref.seq_ids
+    assert native.step_slots.tolist() == ref.step_slots
+    assert [tuple(x) for x in native.cow_pairs.tolist()] == ref.cow_pairs
+    for r, s in enumerate(ref.seq_ids):
+        tab = ref.alloc.table(s)
+        assert native.tables[r, :len(tab)].tolist() == tab
+        assert np.all(native.tables[r, len(tab):] == -1)
+        assert native.ctx_i32[r] == ref.ctx[r]
+    assert native.pool.free_stack().tolist() == ref.alloc.free_stack_top_first()

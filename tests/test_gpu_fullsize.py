@@ -1,0 +1,79 @@
+"""GPU parity at the full sizes of the five workloads, in the launch
+configuration the benchmark times: the GPU runs the whole batch; the oracle
+recomputes a sample of sequences one by one (their pool blocks bit-exact,
+their outputs within tolerance)."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as OA
+from oracle import scenario as OS
+
+import paged_kv_cache_137_gb300 as pkv
+from paged_kv_cache_137_gb300 import scenario as PS
+
+from test_gpu_parity import TOL, scales_for
+
+pytestmark = pytest.mark.gpu
+
+FULL = ["tiny_fp32", "qwen_gqa_bf16", "prefix_fork_bf16", "long_mha_bf16", "fp8_churn"]
+
+
+def sample_rows(ctx, k=4, seed=0):
+    rng = np.random.default_rng(seed)
+    rows = {0, len(ctx) - 1, int(np.argmax(ctx)), int(np.argmin(ctx))}
+    rows |= set(rng.choice(len(ctx), size=min(k, len(ctx)), replace=False).tolist())
+    return sorted(rows)
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pkv.build()
+    assert torch.cuda.is_available()
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_sampled(name):
+    w = W.get(name)
+    sc = scales_for(w)
+    dev = PS.materialize(PS.plan(w), "cuda", sc)
+    out = dev.step()
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    assert not np.isnan(got).any()
+    rows = sample_rows(dev.plan.ctx)
+    ref_scn = OS.build(w, write_seqs=rows, scales=sc)
+    ref = OA.paged_attention_decode(ref_scn.q_f64(), ref_scn.pool, ref_scn.tables, ref_scn.ctx,
+                                    1.0 / math.sqrt(w.head_dim), sc.get("k_scale", 1.0),
+                                    sc.get("v_scale", 1.0), seqs=rows)
+    err = np.abs(got[rows] - ref[rows])
+    max_tol, mean_tol = TOL[w.kv_dtype]
+    assert err.max() <= max_tol, f"max abs error {err.max():.3g}"
+    if mean_tol is not None:
+        assert err.mean() <= mean_tol, f"mean abs error {err.mean():.3g}"
+    # the sampled sequences' blocks hold exactly the oracle's bytes
+    kc = dev.k_cache.view(torch.uint8)
+    vc = dev.v_cache.view(torch.uint8)
+    for r in rows:
+        for b in ref_scn.alloc.table(ref_scn.seq_ids[r]):
+            assert np.array_equal(kc[b].cpu().numpy().reshape(-1), ref_scn.pool.k[b].view(np.uint8).reshape(-1))
+            assert np.array_equal(vc[b].cpu().numpy().reshape(-1), ref_scn.pool.v[b].view(np.uint8).reshape(-1))
+
+
+def test_longest_context_at_table_capacity():
+    """A sequence whose length fills its table exactly (ctx = max_blocks * T),
+    next to a one-token sequence."""
+    w = W.scaled(W.get("long_mha_bf16"), num_seqs=2, num_q_heads=8, num_kv_heads=8, num_blocks=1100,
+                 ctx_range=(32768, 32768))
+    dev = PS.materialize(PS.plan(w), "cuda")
+    assert dev.plan.max_blocks * w.block_size == 32768
+    out = dev.step()
+    torch.cuda.synchronize()
+    ref_scn = OS.build(w, write_seqs=[0])
+    ref = OA.paged_attention_decode(ref_scn.q_f64(), ref_scn.pool, ref_scn.tables, ref_scn.ctx,
+                                    1.0 / math.sqrt(w.head_dim), seqs=[0])
+    err = np.abs(out.double().cpu().numpy()[0] - ref[0])
+    assert err.max() <= 2e-2 and err.mean() <= 2e-3

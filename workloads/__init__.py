@@ -31,7 +31,8 @@ to the storage dtype with PyTorch's round-to-nearest-even cast.
 from __future__ import annotations
 
 import math
-from dataclasses import dataclass, field, replace
+import functools
+from dataclasses import dataclass, replace
 
 import numpy as np
 import torch
@@ -39,7 +40,7 @@ import torch
 __all__ = [
     "Workload", "CONFIGS", "get", "scaled",
     "rng", "context_lens", "free_order", "churn_ops", "q_for_seq", "kv_for_seq",
-    "prefix_kv", "fork_layout", "fp8_scales", "TORCH_DTYPES",
+    "prefix_kv", "fork_layout", "fp8_scales", "kv_amax", "TORCH_DTYPES",
 ]
 
 TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -71,7 +72,6 @@ class Workload:
     partition_tokens: int = 0  # split-K partition size, 0 = library default
     churn: int = 0             # alloc/free operations applied before the workload
     shuffled_pool: bool = True
-    extra: dict = field(default_factory=dict)
 
     @property
     def group(self) -> int:
@@ -259,3 +259,18 @@ def fp8_scales(amax_k: float, amax_v: float) -> dict:
         out[name + "_scale"] = float(s)
         out[name + "_inv_scale"] = float(np.float32(np.float32(1.0) / s))
     return out
+
+
+@functools.lru_cache(maxsize=8)
+def kv_amax(w: Workload) -> tuple[float, float]:
+    """Largest |K| and |V| over every token of every sequence of a workload
+    (positions 0 .. ctx - 1, in the source dtype), the statistic the per-tensor
+    E4M3 scales are computed from."""
+    if w.ctx_dist == "prefix_fork":
+        raise NotImplementedError("per-tensor scales are defined for independent sequences")
+    ak = av = 0.0
+    for s, c in enumerate(context_lens(w)):
+        k, v = kv_for_seq(w, s, int(c))
+        ak = max(ak, float(k.float().abs().max()))
+        av = max(av, float(v.float().abs().max()))
+    return ak, av
