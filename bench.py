@@ -20,7 +20,6 @@ import hashlib
 import json
 import os
 import statistics
-import subprocess
 import sys
 import threading
 import time
@@ -36,8 +35,8 @@ KERNEL_SOURCES = ["attention.cu", "attention_simt.cuh", "attention.h", "device_c
 def parse():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=20)
-    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", default="gb300", choices=["gb300", "reference"])
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
@@ -74,52 +73,56 @@ def traffic_for(config: str):
 
 
 class ClockSampler:
-    """nvidia-smi samples of SM clock and throttle reasons while running."""
+    """SM clock and throttle reasons sampled through NVML (ctypes, read-only)
+    every ~0.5 ms while the timed region runs; nvidia-smi when NVML is absent."""
 
-    FIELDS = ("clocks.sm,clocks.max.sm,clocks_event_reasons.hw_slowdown,"
-              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
-              "clocks_event_reasons.sw_power_cap")
+    REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
+               0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
     def __init__(self, index: int):
-        self.index = index
-        self.samples = []
-        self.proc = None
+        import ctypes
+        self.samples, self.max_mhz, self.stop = [], None, threading.Event()
+        self.nvml = None
+        try:
+            nv = ctypes.CDLL("libnvidia-ml.so.1")
+            h = ctypes.c_void_p()
+            if nv.nvmlInit_v2() == 0 and nv.nvmlDeviceGetHandleByIndex_v2(index, ctypes.byref(h)) == 0:
+                self.nvml, self.handle = nv, h
+                mx = ctypes.c_uint()
+                if nv.nvmlDeviceGetMaxClockInfo(h, 1, ctypes.byref(mx)) == 0:
+                    self.max_mhz = float(mx.value)
+                fn = getattr(nv, "nvmlDeviceGetCurrentClocksEventReasons", None) or \
+                    nv.nvmlDeviceGetCurrentClocksThrottleReasons
+                self.reasons_fn = fn
+        except OSError:
+            self.nvml = None
+
+    def _poll(self):
+        import ctypes
+        clk, rs = ctypes.c_uint(), ctypes.c_ulonglong()
+        while not self.stop.is_set():
+            if self.nvml.nvmlDeviceGetClockInfo(self.handle, 1, ctypes.byref(clk)) == 0 and \
+                    self.reasons_fn(self.handle, ctypes.byref(rs)) == 0:
+                self.samples.append((float(clk.value), int(rs.value)))
+            time.sleep(0.0005)
 
     def __enter__(self):
-        try:
-            self.proc = subprocess.Popen(
-                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.FIELDS}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
-                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
-            self.thread = threading.Thread(target=self._read, daemon=True)
+        if self.nvml is not None:
+            self.thread = threading.Thread(target=self._poll, daemon=True)
             self.thread.start()
-        except (FileNotFoundError, OSError):
-            self.proc = None
         return self
 
-    def _read(self):
-        for line in self.proc.stdout:
-            parts = [x.strip() for x in line.split(",")]
-            if len(parts) == 6:
-                self.samples.append(parts)
-
     def __exit__(self, *exc):
-        if self.proc:
-            self.proc.terminate()
-            try:
-                self.proc.wait(timeout=5)
-            except subprocess.TimeoutExpired:
-                self.proc.kill()
+        self.stop.set()
+        if self.nvml is not None:
+            self.thread.join(timeout=2)
 
     def summary(self):
         if not self.samples:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["unsampled"], "samples": 0}
-        sm = [float(s[0]) for s in self.samples if s[0].replace(".", "").isdigit()]
-        mx = [float(s[1]) for s in self.samples if s[1].replace(".", "").isdigit()]
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        reasons = sorted({names[i] for s in self.samples for i in range(4) if s[2 + i] == "Active"})
-        return {"sm_mhz": statistics.median(sm) if sm else None, "sm_max_mhz": max(mx) if mx else None,
-                "reasons": reasons, "samples": len(self.samples)}
+            return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
+        reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
+        return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
+                "reasons": reasons, "samples": len(self.samples), "source": "nvml"}
 
 
 def dist_setup(args):
@@ -154,55 +157,58 @@ def max_over_ranks(x: float, world: int) -> float:
 
 
 # ------------------------------------------------------------------ oracle
-def time_oracle(config: str, seconds: float, max_passes: int | None = None):
-    """The CPU oracle on the host: one pass = decode attention of the whole
-    batch (pool built beforehand, not timed); passes repeat until ``seconds``.
-    Returns (GB/s of algorithmic K/V bytes, tokens/s, passes, elapsed)."""
-    import math
-    import numpy as np
-    import workloads as W
-    from oracle import attention as OA
-    from oracle import scenario as OS
-    w = W.get(config)
-    sc = W.fp8_scales(*W.kv_amax(w)) if w.kv_dtype == "e4m3" else {}
-    scn = OS.build(w, scales=sc)
-    q = scn.q_f64()
-    tables = scn.tables
-    kv_bytes = 2 * int(np.sum(scn.ctx)) * w.num_kv_heads * w.head_dim * w.kv_bytes
-    passes, t0 = 0, time.perf_counter()
-    while True:
-        OA.paged_attention_decode(q, scn.pool, tables, scn.ctx, 1.0 / math.sqrt(w.head_dim),
-                                  sc.get("k_scale", 1.0), sc.get("v_scale", 1.0))
-        passes += 1
-        el = time.perf_counter() - t0
-        if el >= seconds or (max_passes and passes >= max_passes):
-            break
-    return kv_bytes * passes / el / 1e9, w.num_seqs * passes / el, passes, el, kv_bytes
+class OracleRunner:
+    """The CPU oracle on the host.  One pass = decode attention of the whole
+    batch of the workload over the oracle's pool (built once, not timed)."""
+
+    def __init__(self, config: str):
+        import numpy as np
+        import workloads as W
+        from oracle import scenario as OS
+        self.w = w = W.get(config)
+        self.sc = W.fp8_scales(*W.kv_amax(w)) if w.kv_dtype == "e4m3" else {}
+        self.scn = OS.build(w, scales=self.sc)
+        self.q = self.scn.q_f64()
+        self.tables = self.scn.tables
+        self.kv_bytes = 2 * int(np.sum(self.scn.ctx)) * w.num_kv_heads * w.head_dim * w.kv_bytes
+
+    def one_pass(self) -> float:
+        import math
+        from oracle import attention as OA
+        t0 = time.perf_counter()
+        OA.paged_attention_decode(self.q, self.scn.pool, self.tables, self.scn.ctx,
+                                  1.0 / math.sqrt(self.w.head_dim), self.sc.get("k_scale", 1.0),
+                                  self.sc.get("v_scale", 1.0))
+        return time.perf_counter() - t0
+
+    def timed(self, seconds: float):
+        """Passes until ``seconds`` elapse -> (GB/s, passes, elapsed)."""
+        el, passes = 0.0, 0
+        while passes == 0 or el < seconds:
+            el += self.one_pass()
+            passes += 1
+        return self.kv_bytes * passes / el / 1e9, passes, el
 
 
 def run_reference(args, world, rank):
     if rank != 0:
         return
-    t_steps = []
-    gbs = tps = None
+    r = OracleRunner(args.config)
     for _ in range(args.warmup):
-        time_oracle(args.config, 0.0, max_passes=1)
-    for _ in range(args.steps):
-        g, t, passes, el, kvb = time_oracle(args.config, 0.0, max_passes=1)
-        t_steps.append(el)
+        r.one_pass()
+    t_steps = [r.one_pass() for _ in range(args.steps)]
     ms = 1e3 * statistics.mean(t_steps)
-    gbs = kvb / (ms / 1e3) / 1e9
-    import workloads as W
-    w = W.get(args.config)
+    gbs = r.kv_bytes / (ms / 1e3) / 1e9
+    w = r.w
+    sample = f"whole batch of {args.config} ({w.num_seqs} sequences), one pass per step"
     line = {"metric": METRIC, "value": round(gbs, 4), "unit": "GB/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(ms, 3),
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
             "data": "synthetic", "impl": "reference",
-            "config": {"workload": args.config, "num_seqs": w.num_seqs,
-                       "kv_bytes_per_step": kvb, "sample": "the whole batch, one pass per step"},
+            "config": {"workload": args.config, "num_seqs": w.num_seqs, "kv_bytes_per_step": r.kv_bytes},
             "tokens_per_s": round(w.num_seqs / (ms / 1e3), 3),
             "cpu_baseline": {"value": round(gbs, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
-                             "sample": "whole batch of the workload, one pass per step"},
+                             "sample": sample},
             "e2e": {"value": round(gbs, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                     "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
@@ -304,7 +310,7 @@ def run_gpu(args, world, rank, local):
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
-        g, t, passes, el, _ = time_oracle(args.config, args.cpu_seconds)
+        g, passes, el = OracleRunner(args.config).timed(args.cpu_seconds)
         line["cpu_baseline"] = {"value": round(g, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
                                 "sample": f"whole batch of {args.config}, {passes} pass(es) in {el:.1f} s"}
     if rank == 0:

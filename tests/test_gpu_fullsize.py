@@ -64,9 +64,8 @@ def test_full_size_sampled(name):
 
 
 def test_longest_context_at_table_capacity():
-    """A sequence whose length fills its table exactly (ctx = max_blocks * T),
-    next to a one-token sequence."""
-    w = W.scaled(W.get("long_mha_bf16"), num_seqs=2, num_q_heads=8, num_kv_heads=8, num_blocks=1100,
+    """Sequences whose length fills the table exactly (ctx = max_blocks * T)."""
+    w = W.scaled(W.get("long_mha_bf16"), num_seqs=2, num_q_heads=8, num_kv_heads=8, num_blocks=2100,
                  ctx_range=(32768, 32768))
     dev = PS.materialize(PS.plan(w), "cuda")
     assert dev.plan.max_blocks * w.block_size == 32768
