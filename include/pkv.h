@@ -239,6 +239,32 @@ PKV_API pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_dtyp
                                 int32_t partition_tokens, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* Bytes of the fixed scratch array behind pkv_attention_decode_noalloc. */
+#define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
+
+/* Decode attention that allocates nothing.  The pages have no counterpart;
+ * this is a library convenience for callers that cannot allocate device
+ * memory: a plug-in whose host runtime owns all device memory and hands it
+ * only input and output buffers, or a serving loop that must not call
+ * cudaMalloc (which can synchronise the device) while it runs.
+ * Arguments and result are those of pkv_attention_decode without the
+ * workspace: the split-K scratch is a fixed array of
+ * PKV_NOALLOC_SCRATCH_BYTES (16 MiB) in device memory that the library
+ * declares and every GPU that loads the library holds until the process
+ * exits.  Sizes whose scratch (pkv_attention_workspace_bytes) exceeds it are
+ * rejected with PKV_ERR_INVALID_ARG before anything runs.
+ * The first call on a device, with that device current, looks up the array's
+ * device address (cudaGetSymbolAddress) and caches it; make that first call
+ * before any stream capture.  All calls on a device share the array: calls
+ * that overlap on the GPU race; nothing needs clearing between calls. */
+PKV_API pkv_status pkv_attention_decode_noalloc(void* out, const void* q, int32_t q_dtype,
+                                                const void* k_cache, const void* v_cache,
+                                                const int32_t* block_tables, int32_t max_blocks,
+                                                const int32_t* context_lens, int32_t num_seqs,
+                                                int32_t num_q_heads, const pkv_kv_desc* desc,
+                                                float softmax_scale, float k_scale, float v_scale,
+                                                int32_t partition_tokens, void* stream);
+
 /* Message of the calling thread's last failure ("" if none). */
 PKV_API const char* pkv_last_error(void);
 

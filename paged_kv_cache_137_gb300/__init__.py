@@ -87,8 +87,11 @@ _SIGNATURES = {
     "pkv_attention_partition": (_I32, [_I32, _I32, _PDESC, _I32]),
     "pkv_attention_decode": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F, _F, _F,
                                     _I32, _P, ctypes.c_size_t, _P]),
+    "pkv_attention_decode_noalloc": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F,
+                                            _F, _F, _I32, _P]),
     "pkv_last_error": (ctypes.c_char_p, []),
 }
+NOALLOC_SCRATCH_BYTES = 16 << 20
 EXPORTED = tuple(_SIGNATURES)
 
 
@@ -337,4 +340,26 @@ def pkv_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, d
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), b, hq,
         ctypes.byref(desc), float(softmax_scale), float(k_scale), float(v_scale),
         int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def pkv_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context_lens,
+                                 desc: pkv_kv_desc, softmax_scale, k_scale=1.0, v_scale=1.0,
+                                 partition_tokens=0, stream=None):
+    """Decode attention for callers that cannot allocate device memory (for
+    example a plug-in whose host owns all device memory, or a loop that must
+    not call cudaMalloc): the split-K scratch is the library's own fixed
+    16 MiB device array.  Same result as pkv_attention_decode; sizes that need
+    more scratch raise INVALID_ARG."""
+    b, hq, d = q.shape
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    if block_tables.dim() != 2 or block_tables.shape[0] != b or context_lens.shape != (b,):
+        raise ValueError("block_tables must be int32[B, max_blocks], context_lens int32[B]")
+    _check(lib().pkv_attention_decode_noalloc(
+        _dev(out, "out"), _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache", desc.torch_dtype),
+        _dev(v_cache, "v_cache", desc.torch_dtype), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), b, hq,
+        ctypes.byref(desc), float(softmax_scale), float(k_scale), float(v_scale),
+        int(partition_tokens), _stream(stream)))
     return out
