@@ -41,6 +41,10 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--partition", type=int, default=None,
+                    help="split-K partition in tokens (default: the workload's, else automatic)")
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc", "persistent"],
+                    help="decode kernel (auto = tensor-core where it applies)")
     return ap.parse_args()
 
 
@@ -223,18 +227,24 @@ def run_gpu(args, world, rank, local):
     from paged_kv_cache_137_gb300 import scenario as PS
 
     pkv.build()
+    pkv.pkv_set_attention_kernel(args.kernel)
     torch.cuda.set_device(local)
     dev_name = f"cuda:{local}"
     w = W.get(args.config)
     sc = W.fp8_scales(*W.kv_amax(w)) if w.kv_dtype == "e4m3" else {}
-    scn = PS.materialize(PS.plan(w), dev_name, sc)
+    scn = PS.materialize(PS.plan(w), dev_name, sc, partition_tokens=args.partition)
     stream = torch.cuda.current_stream()
     kv_bytes = scn.kv_bytes()
     props = torch.cuda.get_device_properties(local)
     flush = torch.empty(2 * props.L2_cache_size // 4 + 1024, dtype=torch.float32, device=dev_name)
     n_pairs = len(scn.plan.cow_pairs)
-    splits = -(-scn.plan.max_blocks * w.block_size // scn.partition)
-    launches_per_step = 1 + 1 + (1 if splits > 1 else 0) + (-(-n_pairs // 1024) if n_pairs else 0)
+    resolved = pkv.pkv_attention_partition(len(scn.plan.seq_ids), scn.plan.max_blocks, scn.desc,
+                                           scn.partition)
+    splits = -(-scn.plan.max_blocks * w.block_size // resolved)
+    # write + decode (+ the separate merge of the CUDA-core kernel) + block copies
+    separate_merge = args.kernel == "simt" or w.kv_dtype == "f32"
+    launches_per_step = 2 + (1 if separate_merge and splits > 1 else 0) + \
+        (-(-n_pairs // 1024) if n_pairs else 0)
 
     for _ in range(max(args.warmup, 3)):
         scn.step()
@@ -300,7 +310,7 @@ def run_gpu(args, world, rank, local):
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": round(world * w.num_seqs / (ms / 1e3), 1),
         "frac_of_hbm_peak": round(value / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": "pkv_attention_decode (decode + split-K merge)",
+        "roofline": {"bound": "hbm", "kernel": f"pkv_attention_decode ({args.kernel} kernel)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic_for(args.config), "attention_ms": round(attn, 4)},

@@ -202,6 +202,23 @@ PKV_API pkv_status pkv_copy_blocks(void* const* k_caches, void* const* v_caches,
 PKV_API size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks,
                                      const pkv_kv_desc* desc, int32_t partition_tokens);
 
+/* Decode-attention kernel selection, process-wide (default AUTO).  AUTO uses
+ * the tensor-core kernel (TMA-staged tiles, MMA for q.K^T and p.V, fixed
+ * splits) for 16-bit and E4M3 caches with head_dim 128 (16-bit also 64),
+ * groups of up to 16 query heads and partitions of at most 1024 blocks, and
+ * the CUDA-core kernel otherwise.  SIMT forces the CUDA-core kernel;
+ * TENSOR_CORE makes pkv_attention_decode return PKV_ERR_UNSUPPORTED for sizes
+ * it does not cover; PERSISTENT selects, for partition_tokens 0, the
+ * persistent stream-K schedule of the tensor-core kernel (one CTA per SM,
+ * equal tile shares, partial merges), falling back like TENSOR_CORE when the
+ * workspace is smaller than pkv_attention_workspace_bytes(..., 0).  All
+ * kernels compute the same result within rounding. */
+#define PKV_KERNEL_AUTO 0
+#define PKV_KERNEL_SIMT 1
+#define PKV_KERNEL_TENSOR_CORE 2
+#define PKV_KERNEL_PERSISTENT 3
+PKV_API pkv_status pkv_set_attention_kernel(int32_t kind);
+
 /* Partition (tokens per split) pkv_attention_decode uses for these sizes. */
 PKV_API int32_t pkv_attention_partition(int32_t num_seqs, int32_t max_blocks, const pkv_kv_desc* desc,
                                 int32_t partition_tokens);
@@ -219,10 +236,12 @@ PKV_API int32_t pkv_attention_partition(int32_t num_seqs, int32_t max_blocks, co
  *   block_tables  : device int32[num_seqs][max_blocks]; entries past
  *                   ceil(ctx / T) are not read.
  *   context_lens  : device int32[num_seqs]; a length of 0 gives a zero output.
- *   partition_tokens : tokens per split-K partition, 0 = automatic; a
- *                   multiple of 64 and of block_size.  Split boundaries are
- *                   fixed logical positions, so results do not depend on
- *                   which physical blocks hold the tokens.
+ *   partition_tokens : tokens per split-K partition, or 0 for an automatic
+ *                   choice; a multiple of 64 and of block_size.  Split and
+ *                   tile boundaries depend only on logical positions and
+ *                   lengths, so results do not depend on which physical
+ *                   blocks hold the tokens (see PKV_KERNEL_PERSISTENT for the
+ *                   stream-K schedule).
  *   workspace     : device buffer of at least
  *                   pkv_attention_workspace_bytes(...) bytes, 256-byte
  *                   aligned, ZERO-FILLED before its first use (every call
@@ -256,7 +275,9 @@ PKV_API pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_dtyp
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress) and caches it; make that first call
  * before any stream capture.  All calls on a device share the array: calls
- * that overlap on the GPU race; nothing needs clearing between calls. */
+ * that overlap on the GPU race.  Each call clears the array's split-K
+ * counters on its stream before the kernel runs; nothing else needs
+ * clearing between calls. */
 PKV_API pkv_status pkv_attention_decode_noalloc(void* out, const void* q, int32_t q_dtype,
                                                 const void* k_cache, const void* v_cache,
                                                 const int32_t* block_tables, int32_t max_blocks,

@@ -19,6 +19,9 @@ from ._build import LIB, build  # noqa: F401
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OUT_OF_BLOCKS, PKV_ERR_UNKNOWN_SEQ, PKV_ERR_UNSUPPORTED, \
     PKV_ERR_CUDA = range(6)
 PKV_F32, PKV_F16, PKV_BF16, PKV_E4M3 = range(4)
+PKV_KERNEL_AUTO, PKV_KERNEL_SIMT, PKV_KERNEL_TENSOR_CORE, PKV_KERNEL_PERSISTENT = range(4)
+KERNEL_OF_NAME = {"auto": PKV_KERNEL_AUTO, "simt": PKV_KERNEL_SIMT, "tc": PKV_KERNEL_TENSOR_CORE,
+                  "persistent": PKV_KERNEL_PERSISTENT}
 
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "OUT_OF_BLOCKS", 3: "UNKNOWN_SEQ", 4: "UNSUPPORTED",
                 5: "CUDA"}
@@ -87,6 +90,7 @@ _SIGNATURES = {
     "pkv_attention_partition": (_I32, [_I32, _I32, _PDESC, _I32]),
     "pkv_attention_decode": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F, _F, _F,
                                     _I32, _P, ctypes.c_size_t, _P]),
+    "pkv_set_attention_kernel": (_I32, [_I32]),
     "pkv_attention_decode_noalloc": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F,
                                             _F, _F, _I32, _P]),
     "pkv_last_error": (ctypes.c_char_p, []),
@@ -312,6 +316,11 @@ def pkv_attention_workspace_bytes(num_seqs, num_q_heads, max_blocks, desc: pkv_k
 
 def pkv_attention_partition(num_seqs, max_blocks, desc: pkv_kv_desc, partition_tokens=0) -> int:
     return int(lib().pkv_attention_partition(num_seqs, max_blocks, ctypes.byref(desc), partition_tokens))
+
+
+def pkv_set_attention_kernel(kind) -> None:
+    """Process-wide decode kernel choice: "auto", "simt", "tc" or "persistent"."""
+    _check(lib().pkv_set_attention_kernel(KERNEL_OF_NAME.get(kind, kind)))
 
 
 def workspace_for(num_seqs, num_q_heads, max_blocks, desc, partition_tokens=0, device="cuda"):

@@ -8,7 +8,11 @@
 //   M = max_i m_i,  L = sum_i l_i 2^(m_i - M),  o = sum_i a_i 2^(m_i - M) / L,
 // which equals the softmax over the union of the splits' positions.
 #include <algorithm>
+#include <atomic>
+#include <mutex>
 
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <math_constants.h>
 
 #include "attention.h"
@@ -16,11 +20,18 @@
 
 namespace pkv {
 
-// launch_decode_simt<KV, Q> is instantiated in attention_simt_<kv>_<q>.cu.
+// launch_decode_simt<KV, Q> is instantiated in attention_simt_<kv>_<q>.cu and
+// launch_decode_tc<KV, Q> in attention_tc_<kv>_<q>.cu.
+template <typename KV, typename Q>
+pkv_status launch_decode_tc(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
+                            const CUtensorMap& vmap, cudaStream_t stream);
+template <typename KV, typename Q>
+pkv_status launch_decode_persist(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
+                                 const CUtensorMap& vmap, cudaStream_t stream);
 
 namespace {
 
-constexpr int kTargetUnits = 2048;  // split-K work units the automatic partition aims for
+constexpr int kTargetUnits = 608;   // split-K work units the automatic partition aims for (4 per SM)
 constexpr int kMinPartition = 256;
 constexpr int kMaxPartition = 8192;
 
@@ -35,18 +46,90 @@ int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx) 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t m_off, l_off, acc_off, bytes;
+  size_t counter_off, m_off, l_off, acc_off, bytes;
 };
 
-WsLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t splits, int64_t head_dim) {
+// Workspace: split-K arrival counters (zero between calls), then the
+// partial maxima, sums and unnormalised outputs, each 256-byte aligned.
+WsLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t num_kv_heads,
+                          int64_t splits, int64_t head_dim) {
   WsLayout w{};
   if (splits <= 1) return w;
   const size_t n = static_cast<size_t>(num_seqs * num_q_heads * splits);
-  w.m_off = 0;
-  w.l_off = align_up(n * sizeof(float), 256);
+  w.counter_off = 0;
+  w.m_off = align_up(static_cast<size_t>(num_seqs * num_kv_heads) * sizeof(int), 256);
+  w.l_off = w.m_off + align_up(n * sizeof(float), 256);
   w.acc_off = w.l_off + align_up(n * sizeof(float), 256);
   w.bytes = w.acc_off + align_up(n * head_dim * sizeof(float), 256);
   return w;
+}
+
+// Workspace of the persistent kernel: the same counters, then two partial
+// slots of 16 rows x (max, sum, head_dim outputs) per CTA.
+WsLayout persist_layout(int64_t num_seqs, int64_t num_kv_heads, int64_t head_dim) {
+  WsLayout w{};
+  w.counter_off = 0;
+  w.m_off = align_up(static_cast<size_t>(num_seqs * num_kv_heads) * sizeof(int), 256);
+  w.l_off = w.acc_off = w.m_off;
+  w.bytes = w.m_off + align_up(static_cast<size_t>(kPersistMaxCtas) * 2 * 16 * (head_dim + 2) *
+                                   sizeof(float), 256);
+  return w;
+}
+
+// Process-wide kernel choice (pkv_set_attention_kernel).
+std::atomic<int> g_kernel_choice{PKV_KERNEL_AUTO};
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q{};
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+// The pool as a 2-D byte tensor [num_blocks * N_kv * T rows][row_bytes],
+// read in boxes of T rows x 128 bytes with the 128-byte swizzle.
+pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d) {
+  auto fn = encode_fn();
+  if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
+  const cuuint64_t row_bytes = static_cast<cuuint64_t>(d->head_dim) * pkv_dtype_bytes(d->kv_dtype);
+  const cuuint64_t rows = static_cast<cuuint64_t>(d->num_blocks) * d->num_kv_heads * d->block_size;
+  const cuuint64_t dims[2] = {row_bytes, rows};
+  const cuuint64_t strides[1] = {row_bytes};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(d->block_size)};
+  const cuuint32_t estr[2] = {1, 1};
+  const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
+                        box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) {
+    set_error("cuTensorMapEncodeTiled failed (%d)", static_cast<int>(r));
+    return PKV_ERR_CUDA;
+  }
+  return PKV_OK;
+}
+
+// Whether the persistent kernel is used for an automatic partition.
+bool persist_eligible(const pkv_kv_desc* d, int num_seqs, int num_q_heads) {
+  if (d->kv_dtype == PKV_F32 || num_q_heads % d->num_kv_heads != 0) return false;
+  if (num_q_heads / d->num_kv_heads > 16 || num_seqs > kPersistMaxSeqs) return false;
+  if (static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * d->block_size > INT32_MAX) return false;
+  return d->kv_dtype == PKV_E4M3 ? d->head_dim == 128 : (d->head_dim == 128 || d->head_dim == 64);
+}
+
+// Whether the tensor-core kernel covers these sizes.
+bool tc_supported(const pkv_kv_desc* d, int q_dtype, int group, int partition) {
+  if (d->kv_dtype == PKV_F32) return false;
+  if (group > 16) return false;
+  if (partition / d->block_size > 1024) return false;
+  if (static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * d->block_size > INT32_MAX) return false;
+  if (d->kv_dtype == PKV_E4M3) return d->head_dim == 128 && (q_dtype == PKV_F16 || q_dtype == PKV_BF16);
+  return d->head_dim == 128 || d->head_dim == 64;
 }
 
 template <typename Q, int D>
@@ -119,7 +202,32 @@ extern "C" size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_
   int32_t p = 0;
   if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
   const int64_t s = num_splits(max_blocks, desc->block_size, p);
-  return workspace_layout(num_seqs, num_q_heads, s, desc->head_dim).bytes;
+  size_t bytes = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim).bytes;
+  if (partition_tokens == 0 && persist_eligible(desc, num_seqs, num_q_heads))
+    bytes = std::max(bytes, persist_layout(num_seqs, desc->num_kv_heads, desc->head_dim).bytes);
+  return bytes;
+}
+
+namespace pkv {
+size_t attention_counter_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks,
+                               const pkv_kv_desc* desc, int32_t partition_tokens) {
+  if (check_desc(desc) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 || max_blocks <= 0) return 0;
+  int32_t p = 0;
+  if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
+  const int64_t s = num_splits(max_blocks, desc->block_size, p);
+  const WsLayout w = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim);
+  const bool persist = partition_tokens == 0 && persist_eligible(desc, num_seqs, num_q_heads);
+  if (!w.bytes && !persist) return 0;
+  return align_up(static_cast<size_t>(num_seqs) * desc->num_kv_heads * sizeof(int), 256);
+}
+}  // namespace pkv
+
+extern "C" pkv_status pkv_set_attention_kernel(int32_t kind) {
+  if (kind != PKV_KERNEL_AUTO && kind != PKV_KERNEL_SIMT && kind != PKV_KERNEL_TENSOR_CORE &&
+      kind != PKV_KERNEL_PERSISTENT)
+    return fail(PKV_ERR_INVALID_ARG, "unknown attention kernel kind");
+  g_kernel_choice.store(kind);
+  return PKV_OK;
 }
 
 extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_dtype,
@@ -166,7 +274,16 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
   if (st != PKV_OK) return st;
   const int64_t splits = num_splits(max_blocks, desc->block_size, partition);
   if (splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits");
-  const WsLayout ws = workspace_layout(num_seqs, num_q_heads, splits, desc->head_dim);
+  const int choice = g_kernel_choice.load();
+  // The persistent schedule needs its own workspace; with a smaller (or no)
+  // workspace the fixed-split schedule runs instead.
+  const WsLayout pws = persist_layout(num_seqs, desc->num_kv_heads, desc->head_dim);
+  const bool persist = partition_tokens == 0 && choice == PKV_KERNEL_PERSISTENT &&
+                       persist_eligible(desc, num_seqs, num_q_heads) && workspace != nullptr &&
+                       workspace_bytes >= pws.bytes;
+  const WsLayout ws = persist ? pws
+                              : workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, splits,
+                                                 desc->head_dim);
   if (ws.bytes > 0) {
     if (!workspace || workspace_bytes < ws.bytes)
       return fail(PKV_ERR_INVALID_ARG, "workspace missing or smaller than pkv_attention_workspace_bytes");
@@ -184,6 +301,8 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
   a.ws_m = ws.bytes ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
   a.ws_l = ws.bytes ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
   a.ws_acc = ws.bytes ? reinterpret_cast<float*>(wsb + ws.acc_off) : nullptr;
+  a.counters = ws.bytes ? reinterpret_cast<int*>(wsb + ws.counter_off) : nullptr;
+  a.ws_part = persist ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
   a.max_blocks = max_blocks;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -199,6 +318,31 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim;
+  const bool tc_ok = tc_supported(desc, q_dtype, group, partition);
+  if ((choice == PKV_KERNEL_TENSOR_CORE || choice == PKV_KERNEL_PERSISTENT) && !tc_ok && !persist)
+    return fail(PKV_ERR_UNSUPPORTED, "the tensor-core kernel does not cover these sizes");
+  if (persist || (tc_ok && choice != PKV_KERNEL_SIMT)) {
+    CUtensorMap kmap, vmap;
+    st = pool_map(&kmap, k_cache, desc);
+    if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc);
+    if (st != PKV_OK) return st;
+    if (persist) {
+      switch (kv) {
+        case PKV_F16: return launch_decode_persist<F16, F16>(a, D, kmap, vmap, s);
+        case PKV_BF16: return launch_decode_persist<BF16, BF16>(a, D, kmap, vmap, s);
+        default:
+          return q_dtype == PKV_F16 ? launch_decode_persist<E4M3, F16>(a, D, kmap, vmap, s)
+                                    : launch_decode_persist<E4M3, BF16>(a, D, kmap, vmap, s);
+      }
+    }
+    switch (kv) {
+      case PKV_F16: return launch_decode_tc<F16, F16>(a, D, kmap, vmap, s);
+      case PKV_BF16: return launch_decode_tc<BF16, BF16>(a, D, kmap, vmap, s);
+      default:
+        return q_dtype == PKV_F16 ? launch_decode_tc<E4M3, F16>(a, D, kmap, vmap, s)
+                                  : launch_decode_tc<E4M3, BF16>(a, D, kmap, vmap, s);
+    }
+  }
   switch (kv) {
     case PKV_F32: st = launch_decode_simt<F32, F32>(a, D, gm, s); break;
     case PKV_F16: st = launch_decode_simt<F16, F16>(a, D, gm, s); break;

@@ -21,12 +21,25 @@ struct DecodeArgs {
   float* ws_m;               // split-K partial maxima   [B][Hq][S] (log2 domain)
   float* ws_l;               // split-K partial sums      [B][Hq][S]
   float* ws_acc;             // split-K partial outputs   [B][Hq][S][D]
+  int* counters;             // split-K arrival counters  [B][N_kv], zero between calls
+  float* ws_part;            // persistent kernel: 2 partial slots per CTA
+  int32_t stages;            // persistent kernel: ring slots
   int32_t max_blocks, num_seqs, num_q_heads, num_kv_heads, group, num_blocks, block_size;
   int32_t partition;         // tokens per split (multiple of 64 and of T)
   int32_t max_splits;        // S
   float qk_scale;            // softmax_scale * k_scale * log2(e)
   float v_scale;             // 1, or the E4M3 V scale
 };
+
+// Limits of the persistent tensor-core kernel (shared by host and device code).
+constexpr int kPersistMaxCtas = 256;   // grid size cap (one CTA per SM)
+constexpr int kPersistMaxSeqs = 4096;  // per-call batch held in shared memory
+
+// Bytes at the start of a decode workspace that hold the split-K arrival
+// counters (they must be zero when a call starts; every call leaves them
+// zero).  0 when the sizes need no split.
+size_t attention_counter_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks,
+                               const pkv_kv_desc* desc, int32_t partition_tokens);
 
 // Launch the CUDA-core decode kernel for one (cache dtype, q dtype) pair;
 // returns PKV_ERR_UNSUPPORTED for a shape it was not compiled for.

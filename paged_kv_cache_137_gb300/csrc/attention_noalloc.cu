@@ -19,11 +19,14 @@
 // should come before any stream capture.
 //
 // Every call on a device shares the one array, which keeps whatever the last
-// call left in it.  The decode kernels write every scratch value before they
-// read it within the same call, so nothing has to be cleared between calls;
-// calls that overlap on the GPU (two streams at once) race on the array.
+// call left in it.  Only the split-K arrival counters at its start must be
+// zero when a call begins; each call clears them on its stream before the
+// decode kernel runs (a memset, not an allocation).  Every other scratch
+// value is written before it is read within the same call.  Calls that
+// overlap on the GPU (two streams at once) race on the array.
 #include <mutex>
 
+#include "attention.h"
 #include "device_common.cuh"
 
 namespace pkv {
@@ -42,20 +45,16 @@ void* g_scratch_addr[kMaxDevices] = {};
 pkv_status scratch_on_current_device(void** out) {
   int dev = -1;
   cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) {
-    set_error("pkv_attention_decode_noalloc: cudaGetDevice: %s", cudaGetErrorString(e));
-    return PKV_ERR_CUDA;
-  }
+  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode_noalloc: cudaGetDevice", e);
   if (dev < 0 || dev >= kMaxDevices)
     return fail(PKV_ERR_UNSUPPORTED, "pkv_attention_decode_noalloc: device index above 63");
   std::lock_guard<std::mutex> lock(g_scratch_mu);
   if (g_scratch_addr[dev] == nullptr) {
     void* p = nullptr;
     e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
-    if (e != cudaSuccess || p == nullptr) {
-      set_error("pkv_attention_decode_noalloc: cudaGetSymbolAddress: %s", cudaGetErrorString(e));
-      return PKV_ERR_CUDA;
-    }
+    if (e != cudaSuccess) return cuda_fail("pkv_attention_decode_noalloc: cudaGetSymbolAddress", e);
+    if (p == nullptr)
+      return fail(PKV_ERR_CUDA, "pkv_attention_decode_noalloc: cudaGetSymbolAddress gave NULL");
     g_scratch_addr[dev] = p;
   }
   *out = g_scratch_addr[dev];
@@ -85,6 +84,10 @@ extern "C" pkv_status pkv_attention_decode_noalloc(
   if (need > 0) {
     const pkv_status st = scratch_on_current_device(&scratch);
     if (st != PKV_OK) return st;
+    const size_t counters = attention_counter_bytes(num_seqs, num_q_heads, max_blocks, desc,
+                                                    partition_tokens);
+    const cudaError_t e = cudaMemsetAsync(scratch, 0, counters, static_cast<cudaStream_t>(stream));
+    if (e != cudaSuccess) return cuda_fail("pkv_attention_decode_noalloc: clearing the counters", e);
   }
   return pkv_attention_decode(out, q, q_dtype, k_cache, v_cache, block_tables, max_blocks,
                               context_lens, num_seqs, num_q_heads, desc, softmax_scale, k_scale,

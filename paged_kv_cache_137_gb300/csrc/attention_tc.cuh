@@ -1,0 +1,597 @@
+// Tensor-core paged decode attention with TMA-staged K/V tiles.
+//
+// What it computes is the same as the CUDA-core kernel (attention_simt.cuh):
+// for the G query heads of one KV head, softmax(q . K^T * scale) V over the
+// logical positions of one split, K/V gathered through the block table (the
+// katajob Q&A, "The paging idea"; the foundry page on paged block allocation,
+// "Concept").
+//
+// How, on GB300:
+//  * One CTA (4 warps) per (split, KV head, sequence).  The split's block ids
+//    are read once into shared memory.  Thread 0 feeds a ring of NS stages:
+//    each stage is a 64-token tile of K and of V, fetched as one 2-D TMA box
+//    of T rows x 128 bytes per (block, 128-byte column slab) at row
+//    (block * N_kv + head) * T of the pool viewed as [rows][row_bytes], with
+//    the hardware 128-byte swizzle so that ldmatrix reads are conflict-free.
+//    Completion is tracked by one mbarrier per stage (expect-tx bytes).
+//  * Each warp owns 16 tokens of a tile.  q . K^T is an m16n8k16 MMA with the
+//    (up to 16) query heads of the group as the M rows, so each K element is
+//    read from shared memory once for all heads; the online softmax runs on
+//    the accumulator fragments (quad shuffles for the row maxima); p . V is a
+//    second m16n8k16 MMA whose A operand is the probability fragment reused
+//    from registers.  16-bit caches use bf16/f16 MMAs; an E4M3 cache is
+//    converted to f16 in registers (exact) and q is converted to f16.
+//  * Tokens past the context end are masked to -inf, and their V rows are
+//    zeroed in shared memory before the p . V MMA (0 * NaN would poison it).
+//  * The four warps' (max, sum, output) are merged through shared memory.
+//    With several splits, each CTA writes its partial and the last CTA of the
+//    (sequence, KV head) to finish (an atomic counter, no waiting) merges all
+//    splits and resets the counter to zero.
+//  * Every mbarrier wait is bounded; a timeout turns the heads' output into NaN
+//    after waiting (also bounded) for the copies still in flight.
+#pragma once
+
+#include <cuda.h>
+#include <math_constants.h>
+
+#include <type_traits>
+
+#include "attention.h"
+#include "device_common.cuh"
+
+namespace pkv {
+namespace tc {
+
+constexpr int kWarps = 4;
+constexpr int kThreads = kWarps * 32;
+constexpr int kTile = 64;                 // tokens per stage, 16 per warp
+constexpr int kHalfBytes = kTile * 128;   // one 128-byte column slab of a tile
+constexpr int kMaxTableEntries = 1024;    // block ids of one split kept in shared memory
+constexpr uint64_t kWaitNs = 50000000ull;  // a stage wait gives up after 50 ms
+constexpr uint64_t kDrainNs = 10000000ull; // after a give-up, 10 ms per copy in flight
+
+template <typename KV, int D>
+struct Geom {
+  static constexpr int kElemBytes = KV::bytes;
+  static constexpr int kRowBytes = D * kElemBytes;
+  static constexpr int kSlabs = kRowBytes / 128;  // 128-byte column slabs per row
+  static constexpr int kTileBytes = kSlabs * kHalfBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K and V
+  static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte slabs");
+};
+
+// ------------------------------------------------------------------ PTX
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait: false if the phase did not complete within limit_ns (or
+// 2^26 attempts, whichever comes first).
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t i = 0; i < (1u << 26); ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 63) == 63 && global_ns() - t0 > limit_ns) return false;
+  }
+  return false;
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3}], [%4];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_t(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                          uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+template <bool BF>
+__device__ __forceinline__ void mma16816(float* c, uint32_t a0, uint32_t a1, uint32_t a2,
+                                         uint32_t a3, uint32_t b0, uint32_t b1) {
+  if constexpr (BF) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+        " {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  } else {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7},"
+        " {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(c[0]), "+f"(c[1]), "+f"(c[2]), "+f"(c[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+  }
+}
+
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t sel) {
+  uint32_t d;
+  asm("prmt.b32 %0, %1, %1, %2;" : "=r"(d) : "r"(a), "r"(sel));
+  return d;
+}
+
+__device__ __forceinline__ uint32_t e4m3x2_f16x2(uint32_t two_bytes) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(static_cast<uint16_t>(two_bytes)));
+  return r;
+}
+
+template <bool BF>
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+  if constexpr (BF) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  } else {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+  }
+}
+
+// Byte offset of 16-byte chunk c of tile row r under the 128-byte swizzle
+// (the tile base is 1024-byte aligned; chunk c lives in slab c / 8).
+__device__ __forceinline__ uint32_t swz(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+// ------------------------------------------------------- tile building blocks
+// One warp's online-softmax state for up to 16 query heads (rows g, g + 8).
+template <int D>
+struct WarpState {
+  float o[D / 8][4];
+  float m[2], l[2];
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int n = 0; n < D / 8; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m[0] = m[1] = -CUDART_INF_F;
+    l[0] = l[1] = 0.f;
+  }
+};
+
+// q fragments (A operand of q . K^T) of the G heads stored row-major at qrows
+// (global or shared memory); rows >= G are zero.  For an E4M3 cache q becomes
+// f16 with head_dim permuted within each 16-element step so that one 32-bit
+// K load of 4 bytes serves both halves of the k-step.
+template <typename KV, typename Q, int D>
+__device__ __forceinline__ void load_q(uint32_t (&qa)[D / 16][4], const typename Q::raw* qrows,
+                                       int G, int g, int q4) {
+  constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks)
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+      const int row = g + 8 * h;
+      uint32_t lo = 0, hi = 0;
+      if (row < G) {
+        if constexpr (!kFp8) {
+          const uint32_t* qp = reinterpret_cast<const uint32_t*>(qrows + row * D + 16 * ks + 2 * q4);
+          lo = qp[0];
+          hi = qp[4];
+        } else {
+          float f[4];
+          LoadF32<Q, 4>::run(qrows + row * D + 16 * ks + 4 * q4, f);
+          lo = pack2<false>(f[0], f[1]);
+          hi = pack2<false>(f[2], f[3]);
+        }
+      }
+      qa[ks][h] = lo;      // a0 (row g) / a1 (row g + 8)
+      qa[ks][2 + h] = hi;  // a2 / a3
+    }
+}
+
+// Column of head_dim held by fragment column j of p . V n-tile n.
+template <bool kFp8>
+__device__ __forceinline__ int out_col(int n, int j, int q4) {
+  if constexpr (!kFp8) return 8 * n + 2 * q4 + j;
+  else return 16 * (n >> 1) + 4 * q4 + 2 * j + (n & 1);
+}
+
+// One warp's 16 tokens (tile rows row0 .. row0 + 15, nvalid of them inside
+// the context) folded into its state.  kt/vt: the stage's K and V tiles.
+// Returns true if V rows were zeroed (generic writes the caller must fence
+// before the slot is refilled by TMA).
+template <typename KV, int D>
+__device__ __forceinline__ bool tile_step(WarpState<D>& st, const uint32_t (&qa)[D / 16][4],
+                                          const uint8_t* kt, uint8_t* vt, int row0, int nvalid,
+                                          float qk_scale, int lane) {
+  using G_ = Geom<KV, D>;
+  constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
+  constexpr bool kBf = std::is_same<KV, BF16>::value;
+  constexpr int KS = D / 16;
+  constexpr int NT = D / 8;
+  const int q4 = lane & 3;
+  bool zeroed = false;
+  if (nvalid < 16) {  // zero the V rows past the context end
+    const int nz = (16 - nvalid) * G_::kSlabs * 8;
+    for (int i = lane; i < nz; i += 32) {
+      const int r = row0 + nvalid + i / (G_::kSlabs * 8);
+      const int c = i % (G_::kSlabs * 8);
+      *reinterpret_cast<uint4*>(vt + swz(r, c)) = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+    zeroed = true;
+  }
+  const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+  const int li = lane & 7, mi = lane >> 3;
+
+  // S = q . K^T : two n-tiles of 8 tokens
+  float sc[2][4];
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt) {
+    sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
+    const int r = row0 + 8 * nt + li;
+    if constexpr (!kFp8) {
+#pragma unroll
+      for (int ks = 0; ks < KS; ks += 2) {
+        uint32_t b0, b1, b2, b3;
+        ldsm_x4(kbase + swz(r, 2 * ks + mi), b0, b1, b2, b3);
+        mma16816<kBf>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+        mma16816<kBf>(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+      }
+    } else {
+#pragma unroll
+      for (int c0 = 0; c0 < KS; c0 += 4) {
+        uint32_t w[4];
+        ldsm_x4(kbase + swz(r, c0 + mi), w[0], w[1], w[2], w[3]);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          const int ks = c0 + j;
+          mma16816<false>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3],
+                          e4m3x2_f16x2(w[j] & 0xffffu), e4m3x2_f16x2(w[j] >> 16));
+        }
+      }
+    }
+  }
+
+  // online softmax on the fragments: rows g (h = 0) and g + 8 (h = 1)
+  float p[2][4];
+  float corr[2];
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float mx = -CUDART_INF_F;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int col = 8 * nt + 2 * q4 + j;
+        float v = sc[nt][2 * h + j] * qk_scale;
+        v = col < nvalid ? v : -CUDART_INF_F;
+        sc[nt][2 * h + j] = v;
+        mx = fmaxf(mx, v);
+      }
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 1));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 2));
+    const float mn = fmaxf(st.m[h], mx);
+    corr[h] = exp2f(st.m[h] - mn);
+    st.m[h] = mn;
+    float sum = 0.f;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const float e = exp2f(sc[nt][2 * h + j] - mn);
+        p[nt][2 * h + j] = e;
+        sum += e;
+      }
+    st.l[h] = st.l[h] * corr[h] + sum;
+  }
+#pragma unroll
+  for (int n = 0; n < NT; ++n) {
+    st.o[n][0] *= corr[0];
+    st.o[n][1] *= corr[0];
+    st.o[n][2] *= corr[1];
+    st.o[n][3] *= corr[1];
+  }
+  const uint32_t pa0 = pack2<kBf>(p[0][0], p[0][1]);
+  const uint32_t pa1 = pack2<kBf>(p[0][2], p[0][3]);
+  const uint32_t pa2 = pack2<kBf>(p[1][0], p[1][1]);
+  const uint32_t pa3 = pack2<kBf>(p[1][2], p[1][3]);
+
+  // O += P . V
+  const int rv = row0 + (mi & 1) * 8 + li;
+  if constexpr (!kFp8) {
+#pragma unroll
+    for (int c = 0; c < NT; c += 2) {
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(vbase + swz(rv, c + (mi >> 1)), b0, b1, b2, b3);
+      mma16816<kBf>(st.o[c], pa0, pa1, pa2, pa3, b0, b1);
+      mma16816<kBf>(st.o[c + 1], pa0, pa1, pa2, pa3, b2, b3);
+    }
+  } else {
+#pragma unroll
+    for (int c = 0; c < D / 16; c += 2) {
+      uint32_t w0, w1, w2, w3;  // (tok 0-7, c), (tok 8-15, c), (0-7, c+1), (8-15, c+1)
+      ldsm_x4_t(vbase + swz(rv, c + (mi >> 1)), w0, w1, w2, w3);
+      const uint32_t x0 = prmt(w0, 0x3120), x1 = prmt(w1, 0x3120);
+      const uint32_t x2 = prmt(w2, 0x3120), x3 = prmt(w3, 0x3120);
+      // chunk c: even d -> n-tile 2c, odd d -> 2c + 1
+      mma16816<false>(st.o[2 * c], pa0, pa1, pa2, pa3, e4m3x2_f16x2(x0 & 0xffffu),
+                      e4m3x2_f16x2(x1 & 0xffffu));
+      mma16816<false>(st.o[2 * c + 1], pa0, pa1, pa2, pa3, e4m3x2_f16x2(x0 >> 16),
+                      e4m3x2_f16x2(x1 >> 16));
+      mma16816<false>(st.o[2 * c + 2], pa0, pa1, pa2, pa3, e4m3x2_f16x2(x2 & 0xffffu),
+                      e4m3x2_f16x2(x3 & 0xffffu));
+      mma16816<false>(st.o[2 * c + 3], pa0, pa1, pa2, pa3, e4m3x2_f16x2(x2 >> 16),
+                      e4m3x2_f16x2(x3 >> 16));
+    }
+  }
+  return zeroed;
+}
+
+// Publish one warp's state to the merge buffers: mS/lS [warp][16] (all 16
+// rows), oS [warp][ostride rows][D] (rows < G).  The sums are completed across
+// the quad first.
+template <typename KV, int D>
+__device__ __forceinline__ void publish(const WarpState<D>& st, float* mS, float* lS, float* oS,
+                                        int warp, int G, int ostride, int lane) {
+  constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
+  const int g = lane >> 2, q4 = lane & 3;
+#pragma unroll
+  for (int h = 0; h < 2; ++h) {
+    float l = st.l[h];
+    l += __shfl_xor_sync(0xffffffffu, l, 1);
+    l += __shfl_xor_sync(0xffffffffu, l, 2);
+    if (q4 == 0) {
+      mS[warp * 16 + g + 8 * h] = st.m[h];
+      lS[warp * 16 + g + 8 * h] = l;
+    }
+  }
+#pragma unroll
+  for (int n = 0; n < D / 8; ++n)
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      const int d = out_col<kFp8>(n, j, q4);
+      if (g < G) oS[(warp * ostride + g) * D + d] = st.o[n][j];
+      if (g + 8 < G) oS[(warp * ostride + g + 8) * D + d] = st.o[n][2 + j];
+    }
+}
+
+// Combine nw published states for row `row`, column d:
+// M = max m_w, L = sum l_w 2^(m_w - M), A = sum o_w 2^(m_w - M).
+__device__ __forceinline__ void combine_warps(const float* mS, const float* lS, const float* oS,
+                                              int nw, int ostride, int row, int d, int D, float& M,
+                                              float& L, float& A) {
+  M = -CUDART_INF_F;
+  for (int w = 0; w < nw; ++w) M = fmaxf(M, mS[w * 16 + row]);
+  L = 0.f;
+  A = 0.f;
+  if (M != -CUDART_INF_F) {
+    for (int w = 0; w < nw; ++w) {
+      const float f = exp2f(mS[w * 16 + row] - M);
+      L = fmaf(lS[w * 16 + row], f, L);
+      A = fmaf(oS[(w * ostride + row) * D + d], f, A);
+    }
+  }
+}
+
+// ------------------------------------------------------------------ kernel
+template <typename KV, typename Q, int D, int T, int NS>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap) {
+  using G_ = Geom<KV, D>;
+  constexpr int KS = D / 16;        // k-steps of q . K^T
+  constexpr int BPT = kTile / T;    // blocks per tile
+  constexpr int kBoxBytes = T * 128;
+  static_assert(kTile % T == 0, "a tile holds whole blocks");
+
+  const int split = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q4 = lane & 3;
+  const int G = a.group;
+  const int ctx = a.ctx_lens[seq];
+  const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T;
+  const int nsplit = bad_ctx ? 1 : max(1, (ctx + a.partition - 1) / a.partition);
+  if (split >= nsplit) return;
+  const int t_begin = split * a.partition;
+  const int t_end = bad_ctx ? 0 : min(t_begin + a.partition, ctx);
+  const int first_blk = t_begin / T;
+  const int n_blk = (t_end - t_begin + T - 1) / T;
+  const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* stages = smem;                                            // NS * kStageBytes
+  int32_t* s_tab = reinterpret_cast<int32_t*>(smem + NS * G_::kStageBytes);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_tab + kMaxTableEntries);
+  __shared__ int s_bad, s_last;
+
+  static_assert(NS * G_::kStageBytes >= (2 * kWarps * 16 + kWarps * 16 * D) * 4,
+                "the warp merge reuses the stage buffers");
+  if (tid == 0) {
+    s_bad = bad_ctx ? 1 : 0;
+    for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&s_bar[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    fence_proxy_async();
+  }
+  for (int i = tid; i < n_blk; i += kThreads)
+    s_tab[i] = a.tables[static_cast<size_t>(seq) * a.max_blocks + first_blk + i];
+
+  uint32_t qa[KS][4];
+  load_q<KV, Q, D>(qa, static_cast<const typename Q::raw*>(a.q) +
+                           (static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G) * D,
+                   G, g, q4);
+  __syncthreads();
+
+  // ---------------------------------------------------------- producer
+  // Warp 0 refills a stage with one warp instruction: lane l issues box l
+  // (block l / (2 * slabs), slab, K|V), which starts the tile's boxes
+  // together instead of one after another from a single thread.
+  constexpr int BPB = BPT * G_::kSlabs * 2;  // boxes per tile
+  static_assert(BPB <= 32, "one lane per box");
+  auto issue = [&](int tile) {
+    const int s = tile % NS;
+    uint8_t* kt = stages + s * G_::kStageBytes;
+    const int lb0 = (tile * kTile) / T;  // first logical block of the tile within the split
+    const int blk = lane / (G_::kSlabs * 2), sl = (lane / 2) % G_::kSlabs, isv = lane & 1;
+    int phys = -1;
+    bool inb = false;
+    if (lane < BPB && lb0 + blk < n_blk) {
+      inb = true;
+      phys = s_tab[lb0 + blk];
+    }
+    const bool good = inb && phys >= 0 && phys < a.num_blocks;
+    const unsigned okmask = __ballot_sync(0xffffffffu, good);
+    const unsigned badmask = __ballot_sync(0xffffffffu, inb && !good);
+    const uint32_t bar = smem_u32(&s_bar[s]);
+    if (lane == 0) {
+      if (badmask) s_bad = 1;
+      mbar_arrive_expect_tx(bar, __popc(okmask) * static_cast<uint32_t>(kBoxBytes));
+    }
+    __syncwarp();
+    if (good)
+      tma_load_2d(smem_u32(kt + (isv ? G_::kTileBytes : 0) + sl * kHalfBytes + blk * kBoxBytes),
+                  isv ? &vmap : &kmap, sl * 128, (phys * a.num_kv_heads + kvh) * T, bar);
+  };
+  if (warp == 0)
+    for (int t = 0; t < NS && t < n_tiles; ++t) issue(t);
+
+  // ---------------------------------------------------------- consumers
+  WarpState<D> st;
+  st.reset();
+  bool timed_out = false;
+  int stalled_at = -1;
+  for (int tile = 0; tile < n_tiles; ++tile) {
+    const int s = tile % NS;
+    const uint32_t parity = (tile / NS) & 1;
+    const bool arrived = mbar_wait(smem_u32(&s_bar[s]), parity, kWaitNs);
+    const uint8_t* kt = stages + s * G_::kStageBytes;
+    uint8_t* vt = stages + s * G_::kStageBytes + G_::kTileBytes;
+    const int row0 = warp * 16;
+    const int tok0 = t_begin + tile * kTile + row0;
+    const int nvalid = min(16, t_end - tok0);
+    if (arrived && nvalid > 0 && tile_step<KV, D>(st, qa, kt, vt, row0, nvalid, a.qk_scale, lane))
+      fence_proxy_async();  // the zeroed rows, before the slot is refilled by TMA
+    if (__syncthreads_or(!arrived)) {
+      timed_out = true;
+      stalled_at = tile;
+      break;
+    }
+    if (warp == 0 && tile + NS < n_tiles) issue(tile + NS);
+  }
+
+  if (timed_out) {
+    // wait (bounded) for the copies still in flight, tiles stalled_at ..
+    // stalled_at + NS - 1, before the CTA's shared memory can be reused
+    if (tid == 0) {
+      s_bad = 1;
+      for (int t = stalled_at; t < n_tiles && t < stalled_at + NS; ++t)
+        mbar_wait(smem_u32(&s_bar[t % NS]), (t / NS) & 1, kDrainNs);
+    }
+    __syncthreads();
+  }
+
+  // ---------------------------------------------------- merge the warps
+  float* mS = reinterpret_cast<float*>(smem);  // stages are idle now
+  float* lS = mS + kWarps * 16;
+  float* oS = lS + kWarps * 16;                // [warp][16 rows][D]
+  publish<KV, D>(st, mS, lS, oS, warp, G, 16, lane);
+  __syncthreads();
+
+  const bool any_bad = s_bad != 0;
+  const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
+  for (int i = tid; i < G * D; i += kThreads) {
+    const int row = i / D, d = i % D;
+    float M, L, A;
+    combine_warps(mS, lS, oS, kWarps, 16, row, d, D, M, L, A);
+    A *= a.v_scale;
+    if (nsplit == 1) {
+      const float out = any_bad ? CUDART_NAN_F : (L > 0.f ? A / L : 0.f);
+      store_elem<Q>(a.out, (head0 + row) * D + d, out);
+    } else {
+      const size_t pidx = (head0 + row) * a.max_splits + split;
+      a.ws_acc[pidx * D + d] = any_bad ? CUDART_NAN_F : A;
+      if (d == 0) {
+        a.ws_m[pidx] = M;
+        a.ws_l[pidx] = any_bad ? CUDART_NAN_F : L;
+      }
+    }
+  }
+  if (nsplit == 1) return;
+
+  // ------------------------------------------- split-K: the last CTA merges
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
+    s_last = prev == nsplit - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  for (int i = tid; i < G * D; i += kThreads) {
+    const int row = i / D, d = i % D;
+    const size_t base = (head0 + row) * a.max_splits;
+    float M = -CUDART_INF_F;
+    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(a.ws_m + base + sp));
+    float L = 0.f, A = 0.f;
+    if (M != -CUDART_INF_F) {
+      for (int sp = 0; sp < nsplit; ++sp) {
+        const float f = exp2f(__ldcg(a.ws_m + base + sp) - M);
+        L = fmaf(__ldcg(a.ws_l + base + sp), f, L);
+        A = fmaf(__ldcg(a.ws_acc + (base + sp) * D + d), f, A);
+      }
+    }
+    const float out = (L > 0.f || L != L) ? A / L : 0.f;
+    store_elem<Q>(a.out, (head0 + row) * D + d, out);
+  }
+  if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
+}
+
+template <typename KV, int D, int NS>
+constexpr int smem_bytes() {
+  return NS * Geom<KV, D>::kStageBytes + kMaxTableEntries * 4 + NS * 8 + 1024;
+}
+
+}  // namespace tc
+
+// Launch the tensor-core decode kernel for one (cache, q) dtype pair.
+template <typename KV, typename Q>
+pkv_status launch_decode_tc(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
+                            const CUtensorMap& vmap, cudaStream_t stream);
+
+}  // namespace pkv

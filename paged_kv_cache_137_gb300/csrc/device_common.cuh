@@ -159,6 +159,14 @@ inline pkv_status check_launch(const char* what) {
   return PKV_OK;
 }
 
+// A failed runtime call: record the message and clear the runtime's sticky
+// last-error slot so that a later launch check does not report it again.
+inline pkv_status cuda_fail(const char* what, cudaError_t e) {
+  set_error("%s: %s", what, cudaGetErrorString(e));
+  (void)cudaGetLastError();
+  return PKV_ERR_CUDA;
+}
+
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
 inline pkv_status check_desc(const pkv_kv_desc* d) {

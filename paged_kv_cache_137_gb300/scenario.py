@@ -29,7 +29,7 @@ import torch
 import workloads as W
 
 from . import (Pool, empty_cache, kv_desc, pkv_attention_decode, pkv_copy_blocks, pkv_write,
-               workspace_for, pkv_attention_partition)
+               workspace_for)
 
 CHURN_ID0 = 1 << 40
 POISON_BYTE = 0xFF
@@ -121,7 +121,7 @@ class DeviceScenario:
     v_new: torch.Tensor
     workspace: torch.Tensor | None
     scales: dict
-    partition: int
+    partition: int           # partition_tokens passed to the decode call (0 = automatic)
     softmax_scale: float
 
     def copy_blocks(self, stream=None):
@@ -202,5 +202,5 @@ def materialize(p: Plan, device="cuda", scales: dict | None = None, chunk_tokens
         tables=torch.from_numpy(p.tables).to(device), ctx=torch.from_numpy(p.ctx_i32).to(device),
         step_slots=torch.from_numpy(np.asarray(p.step_slots, dtype=np.int64)).to(device),
         k_new=k_new, v_new=v_new, workspace=ws, scales=scales,
-        partition=pkv_attention_partition(len(p.seq_ids), p.max_blocks, desc, part),
+        partition=part,
         softmax_scale=1.0 / math.sqrt(w.head_dim))

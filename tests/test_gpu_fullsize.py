@@ -40,20 +40,28 @@ def test_full_size_sampled(name):
     w = W.get(name)
     sc = scales_for(w)
     dev = PS.materialize(PS.plan(w), "cuda", sc)
-    out = dev.step()
+    dev.copy_blocks()
+    dev.write_step()
+    outs = {}
+    try:
+        for k in ("simt", "tc", "persistent") if w.kv_dtype != "f32" else ("simt",):
+            pkv.pkv_set_attention_kernel(k)
+            outs[k] = dev.attend().double().cpu().numpy().copy()
+    finally:
+        pkv.pkv_set_attention_kernel("auto")
     torch.cuda.synchronize()
-    got = out.double().cpu().numpy()
-    assert not np.isnan(got).any()
     rows = sample_rows(dev.plan.ctx)
     ref_scn = OS.build(w, write_seqs=rows, scales=sc)
     ref = OA.paged_attention_decode(ref_scn.q_f64(), ref_scn.pool, ref_scn.tables, ref_scn.ctx,
                                     1.0 / math.sqrt(w.head_dim), sc.get("k_scale", 1.0),
                                     sc.get("v_scale", 1.0), seqs=rows)
-    err = np.abs(got[rows] - ref[rows])
     max_tol, mean_tol = TOL[w.kv_dtype]
-    assert err.max() <= max_tol, f"max abs error {err.max():.3g}"
-    if mean_tol is not None:
-        assert err.mean() <= mean_tol, f"mean abs error {err.mean():.3g}"
+    for k, got in outs.items():
+        assert not np.isnan(got).any(), k
+        err = np.abs(got[rows] - ref[rows])
+        assert err.max() <= max_tol, f"{k}: max abs error {err.max():.3g}"
+        if mean_tol is not None:
+            assert err.mean() <= mean_tol, f"{k}: mean abs error {err.mean():.3g}"
     # the sampled sequences' blocks hold exactly the oracle's bytes
     kc = dev.k_cache.view(torch.uint8)
     vc = dev.v_cache.view(torch.uint8)

@@ -75,9 +75,25 @@ def built():
     assert torch.cuda.is_available()
 
 
+@pytest.fixture(params=["simt", "tc", "persistent"])
+def kernel(request):
+    """Run a test once per decode kernel (CUDA-core, tensor-core with fixed
+    splits, tensor-core persistent stream-K)."""
+    pkv.pkv_set_attention_kernel(request.param)
+    yield request.param
+    pkv.pkv_set_attention_kernel("auto")
+
+
+def tc_covers(w):
+    return w.kv_dtype != "f32" and w.num_q_heads // w.num_kv_heads <= 16 and \
+        (w.head_dim == 128 or (w.head_dim == 64 and w.kv_dtype != "e4m3"))
+
+
 @pytest.mark.parametrize("name", list(SMALL))
-def test_step_matches_oracle(name):
+def test_step_matches_oracle(name, kernel):
     w = SMALL[name]
+    if kernel in ("tc", "persistent") and not tc_covers(w):
+        pytest.skip("the tensor-core kernel does not cover this cache")
     sc = scales_for(w)
     dev = PS.materialize(PS.plan(w), "cuda", sc)
     out = dev.step()
@@ -96,8 +112,8 @@ def test_step_matches_oracle(name):
 
 
 @pytest.mark.parametrize("name", ["qwen_small", "long_small", "fp8_small"])
-@pytest.mark.parametrize("partition", [64, 128, 512, 4096])
-def test_partition_sizes_agree_with_oracle(name, partition):
+@pytest.mark.parametrize("partition", [0, 64, 128, 512, 4096])
+def test_partition_sizes_agree_with_oracle(name, partition, kernel):
     w = SMALL[name]
     if partition % w.block_size:
         pytest.skip("partition must be a multiple of the block size")
@@ -109,7 +125,7 @@ def test_partition_sizes_agree_with_oracle(name, partition):
     check_close(out.double().cpu().numpy(), oracle_out(ref), w.kv_dtype)
 
 
-def test_physical_permutation_is_bit_identical():
+def test_physical_permutation_is_bit_identical(kernel):
     w = SMALL["qwen_small"]
     a = PS.materialize(PS.plan(W.scaled(w, shuffled_pool=False)), "cuda").step().clone()
     dev_b = PS.materialize(PS.plan(w), "cuda")
@@ -119,7 +135,7 @@ def test_physical_permutation_is_bit_identical():
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
 
 
-def test_shared_prefix_equals_private_copies_bitwise():
+def test_shared_prefix_equals_private_copies_bitwise(kernel):
     """A forked sequence reading shared prefix blocks gives the same bits as a
     sequence holding a private copy of the same prefix."""
     w = W.scaled(W.get("qwen_gqa_bf16"), num_blocks=64)
@@ -168,7 +184,7 @@ def _single_block_case(ctx_len, poison=True):
     return desc, kc, vc, k, v, q, tables
 
 
-def test_single_token_context_returns_its_value_exactly():
+def test_single_token_context_returns_its_value_exactly(kernel):
     desc, kc, vc, k, v, q, tables = _single_block_case(1)
     out = torch.empty_like(q)
     pkv.pkv_attention_decode(out, q, kc, vc, tables, torch.tensor([1], dtype=torch.int32).cuda(),
@@ -178,7 +194,7 @@ def test_single_token_context_returns_its_value_exactly():
     assert torch.equal(out[0].cpu(), expect)
 
 
-def test_zero_context_gives_zero_and_poison_is_never_read():
+def test_zero_context_gives_zero_and_poison_is_never_read(kernel):
     desc, kc, vc, k, v, q, tables = _single_block_case(5)
     out = torch.full_like(q, 7.0)
     pkv.pkv_attention_decode(out, q, kc, vc, tables, torch.tensor([0], dtype=torch.int32).cuda(),
@@ -191,7 +207,7 @@ def test_zero_context_gives_zero_and_poison_is_never_read():
     assert not torch.isnan(out).any()   # slots 5..15 of the block hold NaN bits
 
 
-def test_invalid_table_entry_or_length_gives_nan():
+def test_invalid_table_entry_or_length_gives_nan(kernel):
     desc, kc, vc, k, v, q, tables = _single_block_case(16)
     out = torch.zeros_like(q)
     bad = torch.tensor([[3, 99]], dtype=torch.int32).cuda()   # 99 >= num_blocks
@@ -253,3 +269,83 @@ def test_copy_blocks_multi_layer_bit_exact():
         # compare raw bits: random bf16 patterns include NaNs
         assert torch.equal(kc.view(torch.int16), ek.view(torch.int16))
         assert torch.equal(vc.view(torch.int16), ev.view(torch.int16))
+
+
+@pytest.mark.parametrize("name", ["qwen_small", "prefix_small", "fp8_small", "gqa16_d64"])
+def test_kernels_agree(name):
+    """The CUDA-core and tensor-core kernels on the same device state."""
+    w = SMALL[name]
+    dev = PS.materialize(PS.plan(w), "cuda", scales_for(w))
+    dev.copy_blocks()
+    dev.write_step()
+    outs = []
+    try:
+        for k in ("simt", "tc", "persistent"):
+            pkv.pkv_set_attention_kernel(k)
+            outs.append(dev.attend().double().cpu().numpy().copy())
+    finally:
+        pkv.pkv_set_attention_kernel("auto")
+    torch.cuda.synchronize()
+    for o in outs[1:]:
+        assert np.abs(outs[0] - o).max() <= TOL[w.kv_dtype][0]
+
+
+def test_split_counters_are_zero_after_a_call():
+    """The fused split-K merge leaves its arrival counters at zero."""
+    w = SMALL["long_small"]
+    dev = PS.materialize(PS.plan(w), "cuda", partition_tokens=512)
+    for _ in range(3):
+        dev.step()
+    torch.cuda.synchronize()
+    n = len(dev.plan.seq_ids) * w.num_kv_heads
+    assert torch.count_nonzero(dev.workspace[: 4 * n]).item() == 0
+
+
+@pytest.mark.parametrize("name", ["qwen_small", "fp8_small", "gqa16_d64"])
+def test_persistent_kernel_with_edited_lengths(name, kernel):
+    """The automatic schedule (the persistent stream-K kernel for the tensor
+    cores) with some lengths cut to 0, 1, 63, 64 and 65 tokens, so that empty
+    sequences, one-token sequences and tile edges sit between long ones."""
+    w = SMALL[name]
+    if kernel in ("tc", "persistent") and not tc_covers(w):
+        pytest.skip("the tensor-core kernel does not cover this cache")
+    sc = scales_for(w)
+    dev = PS.materialize(PS.plan(w), "cuda", sc, partition_tokens=0)
+    dev.copy_blocks()
+    dev.write_step()
+    ctx = dev.plan.ctx.copy()
+    cut = {0: 0, 1: 1, 2: 63, 3: 64, 4: 65}
+    for r, n in cut.items():
+        if r < len(ctx):
+            ctx[r] = min(n, ctx[r])
+    dev.ctx.copy_(torch.from_numpy(ctx.astype(np.int32)))
+    out = dev.attend(partition_tokens=0).double().cpu().numpy()
+    torch.cuda.synchronize()
+    ref_scn = OS.build(w, scales=sc)
+    ref = OA.paged_attention_decode(ref_scn.q_f64(), ref_scn.pool, ref_scn.tables, ctx,
+                                    1.0 / math.sqrt(w.head_dim), sc.get("k_scale", 1.0),
+                                    sc.get("v_scale", 1.0))
+    check_close(out, ref, w.kv_dtype)
+    if ctx[0] == 0:
+        assert np.all(out[0] == 0)
+
+
+def test_persistent_kernel_batch_of_one_and_many_ctas():
+    """A single short sequence (fewer tiles than CTAs) and a single long one
+    (every CTA holds a piece of the same pair)."""
+    pkv.pkv_set_attention_kernel("persistent")
+    try:
+        _one_and_many()
+    finally:
+        pkv.pkv_set_attention_kernel("auto")
+
+
+def _one_and_many():
+    for ctx_range in [(40, 40), (30000, 30000)]:
+        w = W.scaled(W.get("long_mha_bf16"), num_seqs=1, num_q_heads=8, num_kv_heads=1,
+                     num_blocks=1000, ctx_range=ctx_range, partition_tokens=0, seed=97)
+        dev = PS.materialize(PS.plan(w), "cuda")
+        out = dev.step().double().cpu().numpy()
+        torch.cuda.synchronize()
+        ref_scn = OS.build(w)
+        check_close(out, oracle_out(ref_scn), "bf16")
