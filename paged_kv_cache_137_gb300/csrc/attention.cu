@@ -65,14 +65,17 @@ WsLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t num_kv_
 }
 
 // Workspace of the persistent kernel: the same counters, then two partial
-// slots of 16 rows x (max, sum, head_dim outputs) per CTA.
-WsLayout persist_layout(int64_t num_seqs, int64_t num_kv_heads, int64_t head_dim) {
+// slots per CTA of (head group x query group) rows of (max, sum, head_dim
+// outputs).
+WsLayout persist_layout(int64_t num_seqs, const pkv_kv_desc* d, int64_t num_q_heads) {
   WsLayout w{};
+  const int64_t qrows = persist_head_group(d->num_kv_heads, d->block_size) *
+                        (num_q_heads / d->num_kv_heads);
   w.counter_off = 0;
-  w.m_off = align_up(static_cast<size_t>(num_seqs * num_kv_heads) * sizeof(int), 256);
+  w.m_off = align_up(static_cast<size_t>(num_seqs * d->num_kv_heads) * sizeof(int), 256);
   w.l_off = w.acc_off = w.m_off;
-  w.bytes = w.m_off + align_up(static_cast<size_t>(kPersistMaxCtas) * 2 * 16 * (head_dim + 2) *
-                                   sizeof(float), 256);
+  w.bytes = w.m_off + align_up(static_cast<size_t>(kPersistMaxCtas) * 2 * qrows *
+                                   (d->head_dim + 2) * sizeof(float), 256);
   return w;
 }
 
@@ -94,15 +97,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // The pool as a 2-D byte tensor [num_blocks * N_kv * T rows][row_bytes],
-// read in boxes of T rows x 128 bytes with the 128-byte swizzle.
-pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d) {
+// read in boxes of box_rows rows x 128 bytes with the 128-byte swizzle.
+pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d, int box_rows) {
   auto fn = encode_fn();
   if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(d->head_dim) * pkv_dtype_bytes(d->kv_dtype);
   const cuuint64_t rows = static_cast<cuuint64_t>(d->num_blocks) * d->num_kv_heads * d->block_size;
   const cuuint64_t dims[2] = {row_bytes, rows};
   const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(d->block_size)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -204,7 +207,7 @@ extern "C" size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_
   const int64_t s = num_splits(max_blocks, desc->block_size, p);
   size_t bytes = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim).bytes;
   if (partition_tokens == 0 && persist_eligible(desc, num_seqs, num_q_heads))
-    bytes = std::max(bytes, persist_layout(num_seqs, desc->num_kv_heads, desc->head_dim).bytes);
+    bytes = std::max(bytes, persist_layout(num_seqs, desc, num_q_heads).bytes);
   return bytes;
 }
 
@@ -277,7 +280,7 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
   const int choice = g_kernel_choice.load();
   // The persistent schedule needs its own workspace; with a smaller (or no)
   // workspace the fixed-split schedule runs instead.
-  const WsLayout pws = persist_layout(num_seqs, desc->num_kv_heads, desc->head_dim);
+  const WsLayout pws = persist_layout(num_seqs, desc, num_q_heads);
   const bool persist = partition_tokens == 0 && choice == PKV_KERNEL_PERSISTENT &&
                        persist_eligible(desc, num_seqs, num_q_heads) && workspace != nullptr &&
                        workspace_bytes >= pws.bytes;
@@ -323,8 +326,10 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
     return fail(PKV_ERR_UNSUPPORTED, "the tensor-core kernel does not cover these sizes");
   if (persist || (tc_ok && choice != PKV_KERNEL_SIMT)) {
     CUtensorMap kmap, vmap;
-    st = pool_map(&kmap, k_cache, desc);
-    if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc);
+    a.hg = persist ? persist_head_group(desc->num_kv_heads, desc->block_size) : 1;
+    const int box_rows = a.hg * desc->block_size;
+    st = pool_map(&kmap, k_cache, desc, box_rows);
+    if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc, box_rows);
     if (st != PKV_OK) return st;
     if (persist) {
       switch (kv) {

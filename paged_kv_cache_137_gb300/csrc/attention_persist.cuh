@@ -4,34 +4,40 @@
 // idea": keys and values gathered through the block table), scheduled for
 // GB300 so that every SM streams K/V at full rate from launch to finish:
 //
-//  * One CTA per SM for the whole call.  The work is the list of 64-token
-//    tiles of every (sequence, KV head) pair, in (sequence, head, tile) order;
-//    CTA c takes the contiguous slice [c*W/C, (c+1)*W/C) of the W tiles, so
-//    every CTA moves the same number of tiles whatever the length mix.
+//  * Tiles span KV heads.  One block of the pool holds its N_kv heads' T
+//    token rows back to back, so HG consecutive heads of a block are one
+//    contiguous run of HG * T rows.  A tile is 64 rows: HG heads of
+//    64 / (HG * T) blocks, fetched as one 2-D TMA box per (block, 128-byte
+//    slab, K|V).  With block size 16 and four or more KV heads that is one
+//    8 KB box per slab instead of four 2 KB boxes: the per-box issue cost of
+//    the copy engine, not DRAM, limited the one-head tiles.
+//  * One CTA per SM for the whole call.  The work is the list of tiles of
+//    every (sequence, head group) pair, in (sequence, group, tile) order; CTA
+//    c takes the contiguous slice [c*W/C, (c+1)*W/C) of the W tiles, so every
+//    CTA moves the same number of tiles whatever the length mix.
 //  * Warp 8 is the producer: it walks its slice, takes the block ids of the
 //    coming tiles from the table (read one 32-lane window ahead), and issues
-//    one 2-D TMA box per (block, 128-byte slab) of K and V into a ring of
-//    `stages` slots, a whole batch of tiles in one warp instruction (one box
-//    per lane), completing each slot's "full" mbarrier by byte count.  The
-//    first two tiles of each pair also carry the pair's q rows (a bulk copy).
-//    A slot is refilled as soon as its consumers release it ("empty"
-//    mbarrier), so the pipeline never drains at pair boundaries.
+//    a batch of tiles' boxes in one warp instruction (one box per lane) into a
+//    ring of `stages` slots, completing each slot's "full" mbarrier by byte
+//    count.  The first two tiles of each pair also carry the pair's q rows (a
+//    bulk copy).  A slot is refilled as soon as its consumers release it
+//    ("empty" mbarrier), so the pipeline never drains at pair boundaries.
 //  * Warps 0-7 are consumers in two groups of four; group g takes the tiles
-//    with an index of parity g, and each warp takes 16 tokens of a tile
-//    (MMA q.K^T, online softmax, MMA p.V in tile_step()).  Two groups keep two
-//    warps per scheduler in flight, which hides the MMA latency chain.  At the
-//    end of a pair's tiles in this CTA the eight warps merge their states in
-//    shared memory.  A pair the CTA holds entirely is written out directly; a
-//    pair shared with neighbouring CTAs is written as a partial (max, sum,
-//    unnormalised output) to one of the CTA's two partial slots, and the last
-//    of the pair's CTAs to arrive (an atomic counter, never a wait) merges the
-//    pieces, writes the output and resets the counter.
-//  * Sequences with no tiles (context 0, or an invalid length) get a zero (or
-//    NaN) output from CTA (sequence mod C).
+//    with an index of parity g, and warp w of a group takes the tile's rows
+//    16w .. 16w + 15, i.e. 16 tokens of one head (MMA q.K^T, online softmax,
+//    MMA p.V in tile_step()).  At the end of a pair's tiles in this CTA the
+//    warps that hold the same head merge their states in shared memory.  A
+//    pair the CTA holds entirely is written out directly; a pair shared with
+//    neighbouring CTAs is written as a partial (max, sum, unnormalised output)
+//    to one of the CTA's two partial slots, and the last of the pair's CTAs to
+//    arrive (an atomic counter, never a wait) merges the pieces, writes the
+//    output and resets the counter.
 //  * The ring depth is a multiple of the group count, so a slot is always
 //    consumed by the same group: parity waits only ever target the next phase
 //    of a barrier (with slots alternating between groups a group running
 //    ahead could wait two phases ahead and see a false completion).
+//  * Sequences with no tiles (context 0, or an invalid length) get a zero (or
+//    NaN) output from CTA (sequence mod C).
 //  * Every mbarrier wait is bounded in time; a stall stops the producer and
 //    the consumers' waits, turns the affected outputs into NaN, and the CTA
 //    waits (bounded) for its copies in flight before it exits.
@@ -50,18 +56,18 @@ constexpr int kProducerWarp = kConsumerWarps;            // warp 8
 constexpr int kPersistThreads = (kConsumerWarps + 1) * 32;
 constexpr int kPersistMaxStages = 8;
 
-__host__ __device__ constexpr int q_slot_bytes(int D) { return 16 * D * 2; }
+// Bytes of one ring slot's q rows (qrows = HG * G rows of D 16-bit values).
+__host__ __device__ constexpr int q_slot_bytes(int qrows, int D) {
+  return (qrows * D * 2 + 127) / 128 * 128;
+}
 
 // Dynamic shared memory of the persistent kernel (bytes, with alignment slack).
 __host__ __device__ constexpr size_t persist_smem_bytes(int stage_bytes, int D, int stages,
-                                                        int num_seqs, int group) {
-  return 1024 + static_cast<size_t>(stages) * (stage_bytes + q_slot_bytes(D)) +
+                                                        int num_seqs, int group, int qrows) {
+  return 1024 + static_cast<size_t>(stages) * (stage_bytes + q_slot_bytes(qrows, D)) +
          (2 * kConsumerWarps * 16 + kConsumerWarps * group * D) * 4 + (2 * num_seqs + 1) * 4 +
          stages * 4 + 8 + 2 * stages * 8;
 }
-
-// Floats of one CTA partial slot: 16 rows of (max, sum, D outputs).
-__host__ __device__ constexpr int part_slot_floats(int D) { return 16 * (D + 2); }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
@@ -82,11 +88,11 @@ __device__ __forceinline__ void consumer_sync() {
 }
 
 struct Cursor {
-  int s, h, j, nt;  // sequence, KV head, tile within the pair, tiles of the pair
+  int s, h, j, nt;  // sequence, head group, tile within the pair, tiles of the pair
 };
 
-// Tile t of the global list: cum[s] <= t < cum[s + 1] (cum holds N_kv * tiles).
-__device__ __forceinline__ Cursor locate(const int* cum, int B, int nkv, int t) {
+// Tile t of the global list: cum[s] <= t < cum[s + 1] (cum holds groups * tiles).
+__device__ __forceinline__ Cursor locate(const int* cum, int B, int ngroups, int t) {
   int lo = 0, hi = B;
   while (hi - lo > 1) {
     const int mid = (lo + hi) >> 1;
@@ -95,22 +101,22 @@ __device__ __forceinline__ Cursor locate(const int* cum, int B, int nkv, int t) 
   }
   Cursor r;
   r.s = lo;
-  r.nt = (cum[lo + 1] - cum[lo]) / nkv;
+  r.nt = (cum[lo + 1] - cum[lo]) / ngroups;
   const int local = t - cum[lo];
   r.h = local / r.nt;
   r.j = local - r.h * r.nt;
   return r;
 }
 
-__device__ __forceinline__ void advance(Cursor& r, const int* cum, int nkv) {
+__device__ __forceinline__ void advance(Cursor& r, const int* cum, int ngroups) {
   if (++r.j < r.nt) return;
   r.j = 0;
-  if (++r.h < nkv) return;
+  if (++r.h < ngroups) return;
   r.h = 0;
   do {
     ++r.s;
   } while (cum[r.s + 1] == cum[r.s]);
-  r.nt = (cum[r.s + 1] - cum[r.s]) / nkv;
+  r.nt = (cum[r.s + 1] - cum[r.s]) / ngroups;
 }
 
 struct Split {
@@ -128,17 +134,21 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
                           const __grid_constant__ CUtensorMap vmap) {
   using G_ = Geom<KV, D>;
   constexpr int KS = D / 16;
-  constexpr int BPT = kTile / T;
-  constexpr int kBoxBytes = T * 128;
-  constexpr int QB = q_slot_bytes(D);
-  constexpr int PS = part_slot_floats(D);
   constexpr unsigned FULL = 0xffffffffu;
-  static_assert(BPT <= 32, "one lane per block of a tile");
 
   const int NS = a.stages;
   const int C = gridDim.x, c = blockIdx.x;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int B = a.num_seqs, NKV = a.num_kv_heads, G = a.group;
+  const int HG = a.hg;                   // KV heads per tile
+  const int NHG = NKV / HG;              // head groups
+  const int BPT = kTile / (HG * T);      // blocks per tile
+  const int TOKS = BPT * T;              // tokens of one head per tile (64 / HG)
+  const int box_rows = HG * T;
+  const uint32_t box_bytes = static_cast<uint32_t>(box_rows) * 128u;
+  const int QROWS = HG * G;              // q rows of a pair
+  const int QB = q_slot_bytes(QROWS, D);
+  const int PS = QROWS * (D + 2);        // floats of one partial slot
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -157,13 +167,13 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   __shared__ volatile int s_abort;
   __shared__ int s_last, s_segbad;
 
-  // ---- tiles per sequence and their prefix sum (cum[s] = N_kv * tiles before s)
+  // ---- tiles per sequence and their prefix sum (cum[s] = groups * tiles before s)
   const int max_ctx = a.max_blocks * T;
   for (int s = tid; s < B; s += kPersistThreads) {
     const int v = a.ctx_lens[s];
     ctxs[s] = v;
-    const int nt = (v <= 0 || v > max_ctx) ? 0 : (v + kTile - 1) / kTile;
-    cum[s + 1] = nt * NKV;
+    const int nt = (v <= 0 || v > max_ctx) ? 0 : (v + TOKS - 1) / TOKS;
+    cum[s + 1] = nt * NHG;
   }
   if (tid == 0) {
     cum[0] = 0;
@@ -217,21 +227,19 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
   int issued = 0;  // producer: tiles issued
   if (warp == kProducerWarp) {
     // ------------------------------------------------------------ producer
-    // Tiles are issued in batches of TPB: one warp instruction in which lane
-    // l issues box l (tile l / BPB; block, slab and K|V from l % BPB), since
-    // the issue path of a single thread limits how many boxes per second it
-    // can start.  Block ids are fetched a window of TPW tiles at a time (lane
-    // l holds block l % BPT of tile l / BPT), double-buffered one window ahead
-    // so that table reads never sit on the issue path.
-    constexpr int BPB = BPT * G_::kSlabs * 2;  // boxes per tile
-    constexpr int TPB = 32 / BPB;              // tiles per issue batch
-    constexpr int TPW = 32 / BPT;              // tiles per id window
-    static_assert(BPB <= 16 && TPW % TPB == 0, "batches never straddle id windows");
+    // A batch of tiles is issued with one warp instruction: lane l issues box
+    // l (tile l / BPB; block, slab and K|V from l % BPB).  Block ids are
+    // fetched a window of TPW tiles at a time (lane l holds block l % BPT of
+    // tile l / BPT), double-buffered one window ahead so that table reads
+    // never sit on the issue path.
+    const int BPB = BPT * G_::kSlabs * 2;  // boxes per tile (<= 16)
+    const int TPB = 32 / BPB;              // tiles per issue batch
+    const int TPW = 32 / BPT;              // tiles per id window
     constexpr int kNoBlock = INT_MIN, kBadBlock = INT_MIN + 1;
     auto window_ids = [&](int w0) {
       const int t = w0 + lane / BPT;
       if (t >= len) return kNoBlock;
-      const Cursor cu = locate(cum, B, NKV, start + t);
+      const Cursor cu = locate(cum, B, NHG, start + t);
       const int lb = cu.j * BPT + lane % BPT;
       if (lb >= (ctxs[cu.s] + T - 1) / T) return kNoBlock;
       const int v = a.tables[static_cast<size_t>(cu.s) * a.max_blocks + lb];
@@ -240,17 +248,27 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     int cur_ids = window_ids(0), nxt_ids = window_ids(TPW);
     int nb = 0;
     for (int k = 0; k < len; k += nb) {
-      // a batch never holds more tiles than the ring, nor crosses an id window
-      nb = min(min(TPB, len - k), min(NS, TPW - k % TPW));
+      // A batch never holds more tiles than the ring, nor crosses an id
+      // window.  Only its first slot is waited for; the tiles after it join
+      // the batch if their slots are already free, so a released slot is
+      // refilled at once instead of after the whole batch has drained.
+      const int cap = min(min(TPB, len - k), min(NS, TPW - k % TPW));
       if (k > 0 && k % TPW == 0) {
         cur_ids = nxt_ids;
         nxt_ids = window_ids(k + TPW);
       }
-      bool ok = true;
-      if (lane == 0)
-        for (int t = k; t < k + nb; ++t)
-          if (t >= NS) ok = ok && mbar_wait(smem_u32(&empty[t % NS]), ((t / NS) - 1) & 1, kWaitNs);
-      if (!__shfl_sync(FULL, ok ? 1 : 0, 0)) s_abort = 1;
+      int n = 0;
+      if (lane == 0) {
+        bool ok = k < NS || mbar_wait(smem_u32(&empty[k % NS]), ((k / NS) - 1) & 1, kWaitNs);
+        if (ok) {
+          n = 1;
+          while (n < cap && (k + n < NS ||
+                             mbar_try_wait(smem_u32(&empty[(k + n) % NS]), (((k + n) / NS) - 1) & 1)))
+            ++n;
+        }
+      }
+      nb = __shfl_sync(FULL, n, 0);
+      if (nb == 0) s_abort = 1;
       if (__shfl_sync(FULL, s_abort, 0)) break;
 
       // this lane's box: tile k + lane / BPB
@@ -263,33 +281,33 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
       // per-tile bookkeeping by lane i for tile k + i; the first two tiles of
       // a pair in this CTA also carry its q rows (one for each consumer group)
       Cursor cu{0, 0, 0, 1};
-      if (lane < nb) cu = locate(cum, B, NKV, start + k + lane);
+      if (lane < nb) cu = locate(cum, B, NHG, start + k + lane);
       const int t_local = k + lane;
       const bool with_q = lane < nb && (cu.j <= 1 || t_local <= 1);
       if (lane < nb) {
         const int slot = t_local % NS;
         const unsigned tmask = ((1u << BPB) - 1u) << (lane * BPB);
         sbad[slot] = (badmask & tmask) != 0;
-        const uint32_t bytes = __popc(okmask & tmask) * static_cast<uint32_t>(kBoxBytes) +
-                               (with_q ? static_cast<uint32_t>(G) * D * 2u : 0u);
+        const uint32_t bytes = __popc(okmask & tmask) * box_bytes +
+                               (with_q ? static_cast<uint32_t>(QROWS) * D * 2u : 0u);
         mbar_arrive_expect_tx(smem_u32(&full[slot]), bytes);
       }
-      const int h = __shfl_sync(FULL, cu.h, tt < nb ? tt : 0);
+      const int hg = __shfl_sync(FULL, cu.h, tt < nb ? tt : 0);
       __syncwarp();
       if (mine && id >= 0) {
         const int slot = (k + tt) % NS;
         const uint8_t* tile_base = ring + static_cast<size_t>(slot) * G_::kStageBytes +
                                    (isv ? G_::kTileBytes : 0);
-        tma_load_2d(smem_u32(tile_base + sl * kHalfBytes + blk * kBoxBytes), isv ? &vmap : &kmap,
-                    sl * 128, (id * NKV + h) * T, smem_u32(&full[slot]));
+        tma_load_2d(smem_u32(tile_base + sl * kHalfBytes + blk * box_bytes), isv ? &vmap : &kmap,
+                    sl * 128, (id * NKV + hg * HG) * T, smem_u32(&full[slot]));
       }
       if (with_q) {
         const int slot = t_local % NS;
         const typename Q::raw* qsrc = static_cast<const typename Q::raw*>(a.q) +
                                       (static_cast<size_t>(cu.s) * a.num_q_heads +
-                                       static_cast<size_t>(cu.h) * G) * D;
+                                       static_cast<size_t>(cu.h) * QROWS) * D;
         bulk_load(smem_u32(qbuf + static_cast<size_t>(slot) * QB), qsrc,
-                  static_cast<uint32_t>(G) * D * 2u, smem_u32(&full[slot]));
+                  static_cast<uint32_t>(QROWS) * D * 2u, smem_u32(&full[slot]));
       }
       issued = k + nb;
     }
@@ -297,14 +315,18 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
     // ------------------------------------------------------------ consumers
     const int g = lane >> 2, q4 = lane & 3;
     const int group = warp / kWarps, row0 = (warp % kWarps) * 16;
+    // the warp's 16 tile rows: block row0 / box_rows of the tile, head
+    // (row0 % box_rows) / T of the group, tokens from (row0 % T)
+    const int my_head = (row0 % box_rows) / T;
+    const int my_tok = (row0 / box_rows) * T + row0 % T;
     WarpState<D> st;
     st.reset();
     uint32_t qa[KS][4];
-    Cursor cur = locate(cum, B, NKV, start);
+    Cursor cur = locate(cum, B, NHG, start);
     int seg_j0 = cur.j;
     bool first_seg = true, seg_bad = false, need_q = true;
     for (int k = 0; k < len; ++k) {
-      const int s = cur.s, h = cur.h, j = cur.j;
+      const int s = cur.s, hg = cur.h, j = cur.j;
       if (k % kGroups == group && s_abort) {
         seg_bad = true;  // after a stall nothing more is waited for or released
       } else if (k % kGroups == group) {
@@ -317,13 +339,14 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
         uint8_t* kt = ring + static_cast<size_t>(slot) * G_::kStageBytes;
         uint8_t* vt = kt + G_::kTileBytes;
         if (need_q) {  // this group's first tile of the pair carries q
-          load_q<KV, Q, D>(
-              qa, reinterpret_cast<const typename Q::raw*>(qbuf + static_cast<size_t>(slot) * QB), G,
-              g, q4);
+          load_q<KV, Q, D>(qa,
+                           reinterpret_cast<const typename Q::raw*>(qbuf + static_cast<size_t>(slot) * QB) +
+                               static_cast<size_t>(my_head) * G * D,
+                           G, g, q4);
           need_q = false;
         }
         seg_bad |= sbad[slot] != 0;
-        const int nvalid = min(16, ctxs[s] - (j * kTile + row0));
+        const int nvalid = min(16, ctxs[s] - (j * TOKS + my_tok));
         bool zeroed = false;
         if (arrived && nvalid > 0)
           zeroed = tile_step<KV, D>(st, qa, kt, vt, row0, nvalid, a.qk_scale, lane);
@@ -339,58 +362,70 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
         publish<KV, D>(st, mS, lS, oS, warp, G, G, lane);
         consumer_sync();
         const bool bad = s_segbad != 0;
-        const size_t head0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(h) * G;
+        const size_t head0 = static_cast<size_t>(s) * a.num_q_heads + static_cast<size_t>(hg) * QROWS;
         float* part = a.ws_part + static_cast<size_t>(2 * c + (first_seg ? 0 : 1)) * PS;
-        for (int i = tid; i < G * D; i += kConsumerWarps * 32) {
-          const int row = i / D, d = i - (i / D) * D;
-          float M, L, A;
-          combine_warps(mS, lS, oS, kConsumerWarps, G, row, d, D, M, L, A);
+        for (int i = tid; i < QROWS * D; i += kConsumerWarps * 32) {
+          const int qr = i / D, d = i - qr * D;  // qr = head * G + row
+          const int hh = qr / G, row = qr - hh * G;
+          // the warps that hold head hh (both groups, every 16-token unit)
+          float M = -CUDART_INF_F;
+          for (int w = 0; w < kConsumerWarps; ++w)
+            if ((((w % kWarps) * 16) % box_rows) / T == hh) M = fmaxf(M, mS[w * 16 + row]);
+          float L = 0.f, A = 0.f;
+          if (M != -CUDART_INF_F) {
+            for (int w = 0; w < kConsumerWarps; ++w) {
+              if ((((w % kWarps) * 16) % box_rows) / T != hh) continue;
+              const float f = exp2f(mS[w * 16 + row] - M);
+              L = fmaf(lS[w * 16 + row], f, L);
+              A = fmaf(oS[(w * G + row) * D + d], f, A);
+            }
+          }
           if (complete) {
             const float o = bad ? CUDART_NAN_F : (L > 0.f ? A * a.v_scale / L : 0.f);
-            store_elem<Q>(a.out, (head0 + row) * D + d, o);
+            store_elem<Q>(a.out, (head0 + qr) * D + d, o);
           } else {
-            part[row * (D + 2) + 2 + d] = bad ? CUDART_NAN_F : A;
+            part[qr * (D + 2) + 2 + d] = bad ? CUDART_NAN_F : A;
             if (d == 0) {
-              part[row * (D + 2)] = M;
-              part[row * (D + 2) + 1] = bad ? CUDART_NAN_F : L;
+              part[qr * (D + 2)] = M;
+              part[qr * (D + 2) + 1] = bad ? CUDART_NAN_F : L;
             }
           }
         }
         if (!complete) __threadfence();
         consumer_sync();
         if (!complete) {
-          const int P0 = cum[s] + h * cur.nt;
+          const int P0 = cum[s] + hg * cur.nt;
           const int c0 = sp.owner(P0), c1 = sp.owner(P0 + cur.nt - 1);
           if (tid == 0) {
-            const int prev = atomicAdd(&a.counters[static_cast<size_t>(s) * NKV + h], 1);
+            const int prev = atomicAdd(&a.counters[static_cast<size_t>(s) * NHG + hg], 1);
             s_last = prev == c1 - c0;
           }
           consumer_sync();
           if (s_last) {
             __threadfence();
-            for (int i = tid; i < G * D; i += kConsumerWarps * 32) {
-              const int row = i / D, d = i - (i / D) * D;
+            for (int i = tid; i < QROWS * D; i += kConsumerWarps * 32) {
+              const int qr = i / D, d = i - qr * D;
               float M = -CUDART_INF_F;
               for (int cc = c0; cc <= c1; ++cc) {
                 const int which = cc == c0 ? (sp.start(cc) == P0 ? 0 : 1) : 0;
                 M = fmaxf(M, __ldcg(a.ws_part + static_cast<size_t>(2 * cc + which) * PS +
-                                    row * (D + 2)));
+                                    qr * (D + 2)));
               }
               float L = 0.f, A = 0.f;
               if (M != -CUDART_INF_F) {
                 for (int cc = c0; cc <= c1; ++cc) {
                   const int which = cc == c0 ? (sp.start(cc) == P0 ? 0 : 1) : 0;
                   const float* pp =
-                      a.ws_part + static_cast<size_t>(2 * cc + which) * PS + row * (D + 2);
+                      a.ws_part + static_cast<size_t>(2 * cc + which) * PS + qr * (D + 2);
                   const float f = exp2f(__ldcg(pp) - M);
                   L = fmaf(__ldcg(pp + 1), f, L);
                   A = fmaf(__ldcg(pp + 2 + d), f, A);
                 }
               }
               const float o = (L > 0.f || L != L) ? A * a.v_scale / L : 0.f;
-              store_elem<Q>(a.out, (head0 + row) * D + d, o);
+              store_elem<Q>(a.out, (head0 + qr) * D + d, o);
             }
-            if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(s) * NKV + h], 0);
+            if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(s) * NHG + hg], 0);
           }
         }
         if (tid == 0) s_segbad = 0;
@@ -401,7 +436,7 @@ __global__ void __launch_bounds__(kPersistThreads, 1)
         need_q = true;
       }
       if (k + 1 < len) {
-        advance(cur, cum, NKV);
+        advance(cur, cum, NHG);
         if (seg_last) seg_j0 = cur.j;
       }
     }

@@ -409,7 +409,7 @@ __device__ __forceinline__ void combine_warps(const float* mS, const float* lS, 
 
 // ------------------------------------------------------------------ kernel
 template <typename KV, typename Q, int D, int T, int NS>
-__global__ void __launch_bounds__(kThreads, 2)
+__global__ void __launch_bounds__(kThreads, 3)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
   using G_ = Geom<KV, D>;

@@ -55,11 +55,13 @@ pkv_status launch_persist_dt(DecodeArgs a, const CUtensorMap& kmap, const CUtens
   // slot is always consumed by the same group and each parity wait targets
   // the next phase of its barrier (the producer clamps its batches to it).
   constexpr int kMinStages = kGroups;
+  const int qrows = a.hg * a.group;
   int ns = kPersistMaxStages / kGroups * kGroups;
   while (ns > kMinStages && persist_smem_bytes(Geom<KV, D>::kStageBytes, D, ns, a.num_seqs,
-                                               a.group) > static_cast<size_t>(smem_max))
+                                               a.group, qrows) > static_cast<size_t>(smem_max))
     ns -= kGroups;
-  const size_t smem = persist_smem_bytes(Geom<KV, D>::kStageBytes, D, ns, a.num_seqs, a.group);
+  const size_t smem =
+      persist_smem_bytes(Geom<KV, D>::kStageBytes, D, ns, a.num_seqs, a.group, qrows);
   if (smem > static_cast<size_t>(smem_max))
     return fail(PKV_ERR_UNSUPPORTED, "persistent kernel: shared memory too small for this batch");
   static std::atomic<uint64_t> configured{0};
