@@ -26,21 +26,48 @@ template <typename KV, typename Q>
 pkv_status launch_decode_tc(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
                             const CUtensorMap& vmap, cudaStream_t stream);
 template <typename KV, typename Q>
-pkv_status launch_decode_persist(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
-                                 const CUtensorMap& vmap, cudaStream_t stream);
+pkv_status launch_decode_stream(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, cudaStream_t stream);
 
 namespace {
 
-constexpr int kTargetUnits = 608;   // split-K work units the automatic partition aims for (4 per SM)
 constexpr int kMinPartition = 256;
 constexpr int kMaxPartition = 8192;
+constexpr int kSplitCtasPerSm = 3;     // resident tensor-core split CTAs per SM
+constexpr int kDefaultSms = 152;       // used when no device can be queried
 
-int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx) {
-  // Expected (sequence, head, split) units if lengths spread evenly up to max_ctx.
-  const int64_t est_tokens = num_seqs * num_kv_heads * std::max<int64_t>(max_ctx, 1) / 2;
-  int32_t p = kMinPartition;
-  while (p < kMaxPartition && est_tokens / p > kTargetUnits) p *= 2;
-  return p;
+int device_sms() {
+  static std::atomic<int> cache[64];
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return kDefaultSms;
+  }
+  if (dev < 64 && cache[dev].load() > 0) return cache[dev].load();
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms <= 0) {
+    cudaGetLastError();
+    return kDefaultSms;
+  }
+  if (dev < 64) cache[dev].store(sms);
+  return sms;
+}
+
+// Automatic partition: the fewest tokens per split (a multiple of 64 and of
+// the block size) for which the expected (sequence, head, split) units fit in
+// one wave of resident CTAs, so that no unit waits for a slot; with more
+// (sequence, head) pairs than slots, no split at all (up to the maximum).
+// Lengths are expected to spread evenly up to max_ctx, and each pair's last
+// split to be half full.
+int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx, int32_t block_size) {
+  const int64_t slots = static_cast<int64_t>(device_sms()) * kSplitCtasPerSm;
+  const int64_t pairs = num_seqs * num_kv_heads;
+  const int64_t est_tokens = pairs * std::max<int64_t>(max_ctx, 1) / 2;
+  const int32_t step = std::max<int32_t>(64, block_size);
+  if (2 * slots <= pairs + 2) return kMaxPartition;
+  const int64_t free_slots = slots - pairs / 2;
+  int64_t p = (est_tokens + free_slots - 1) / free_slots;
+  p = (p + step - 1) / step * step;
+  return static_cast<int32_t>(std::min<int64_t>(kMaxPartition, std::max<int64_t>(kMinPartition, p)));
 }
 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
@@ -64,20 +91,40 @@ WsLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t num_kv_
   return w;
 }
 
-// Workspace of the persistent kernel: the same counters, then two partial
-// slots per CTA of (head group x query group) rows of (max, sum, head_dim
-// outputs).
-WsLayout persist_layout(int64_t num_seqs, const pkv_kv_desc* d, int64_t num_q_heads) {
+constexpr int kStreamCtasPerSm = 3;  // the stream-K kernel's launch bound
+
+// CTAs of the stream-K kernel on the current device: three per SM (0 if the
+// device cannot be queried).  Cached per device.
+int stream_ctas() {
+  static std::atomic<int> cache[64];
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  if (dev < 64 && cache[dev].load() > 0) return cache[dev].load();
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
+    cudaGetLastError();
+    return 0;
+  }
+  const int c = sms * kStreamCtasPerSm;
+  if (dev < 64) cache[dev].store(c);
+  return c;
+}
+
+// Workspace of the stream-K kernel: the same counters, then two partial
+// slots per CTA of G rows of (max, sum, head_dim outputs).
+WsLayout stream_layout(int64_t num_seqs, const pkv_kv_desc* d, int64_t num_q_heads, int64_t ctas) {
   WsLayout w{};
-  const int64_t qrows = persist_head_group(d->num_kv_heads, d->block_size) *
-                        (num_q_heads / d->num_kv_heads);
+  const int64_t group = num_q_heads / d->num_kv_heads;
   w.counter_off = 0;
   w.m_off = align_up(static_cast<size_t>(num_seqs * d->num_kv_heads) * sizeof(int), 256);
   w.l_off = w.acc_off = w.m_off;
-  w.bytes = w.m_off + align_up(static_cast<size_t>(kPersistMaxCtas) * 2 * qrows *
-                                   (d->head_dim + 2) * sizeof(float), 256);
+  w.bytes = w.m_off + align_up(static_cast<size_t>(ctas) * 2 * group * (d->head_dim + 2) *
+                                   sizeof(float), 256);
   return w;
 }
+
 
 // Process-wide kernel choice (pkv_set_attention_kernel).
 std::atomic<int> g_kernel_choice{PKV_KERNEL_AUTO};
@@ -97,15 +144,15 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
 }
 
 // The pool as a 2-D byte tensor [num_blocks * N_kv * T rows][row_bytes],
-// read in boxes of box_rows rows x 128 bytes with the 128-byte swizzle.
-pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d, int box_rows) {
+// read in boxes of T rows x 128 bytes with the 128-byte swizzle.
+pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d) {
   auto fn = encode_fn();
   if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(d->head_dim) * pkv_dtype_bytes(d->kv_dtype);
   const cuuint64_t rows = static_cast<cuuint64_t>(d->num_blocks) * d->num_kv_heads * d->block_size;
   const cuuint64_t dims[2] = {row_bytes, rows};
   const cuuint64_t strides[1] = {row_bytes};
-  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t box[2] = {128, static_cast<cuuint32_t>(d->block_size)};
   const cuuint32_t estr[2] = {1, 1};
   const CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides,
                         box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
@@ -117,11 +164,13 @@ pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d, in
   return PKV_OK;
 }
 
-// Whether the persistent kernel is used for an automatic partition.
-bool persist_eligible(const pkv_kv_desc* d, int num_seqs, int num_q_heads) {
+// Whether the stream-K kernel covers these sizes (automatic partition only).
+bool stream_eligible(const pkv_kv_desc* d, int num_seqs, int num_q_heads, int max_blocks) {
   if (d->kv_dtype == PKV_F32 || num_q_heads % d->num_kv_heads != 0) return false;
-  if (num_q_heads / d->num_kv_heads > 16 || num_seqs > kPersistMaxSeqs) return false;
+  if (num_q_heads / d->num_kv_heads > 16 || num_seqs > kStreamMaxSeqs) return false;
   if (static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * d->block_size > INT32_MAX) return false;
+  const int64_t tiles = (static_cast<int64_t>(max_blocks) * d->block_size + 63) / 64;
+  if (tiles * d->num_kv_heads * num_seqs > INT32_MAX) return false;
   return d->kv_dtype == PKV_E4M3 ? d->head_dim == 128 : (d->head_dim == 128 || d->head_dim == 64);
 }
 
@@ -176,7 +225,8 @@ pkv_status resolve_partition(int32_t requested, int32_t num_seqs, int32_t max_bl
     *out = requested;
     return PKV_OK;
   }
-  *out = auto_partition(num_seqs, d->num_kv_heads, static_cast<int64_t>(max_blocks) * d->block_size);
+  *out = auto_partition(num_seqs, d->num_kv_heads, static_cast<int64_t>(max_blocks) * d->block_size,
+                        d->block_size);
   return PKV_OK;
 }
 
@@ -206,8 +256,10 @@ extern "C" size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_
   if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
   const int64_t s = num_splits(max_blocks, desc->block_size, p);
   size_t bytes = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim).bytes;
-  if (partition_tokens == 0 && persist_eligible(desc, num_seqs, num_q_heads))
-    bytes = std::max(bytes, persist_layout(num_seqs, desc, num_q_heads).bytes);
+  if (partition_tokens == 0 && stream_eligible(desc, num_seqs, num_q_heads, max_blocks)) {
+    const int ctas = stream_ctas();
+    if (ctas > 0) bytes = std::max(bytes, stream_layout(num_seqs, desc, num_q_heads, ctas).bytes);
+  }
   return bytes;
 }
 
@@ -219,8 +271,8 @@ size_t attention_counter_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t ma
   if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
   const int64_t s = num_splits(max_blocks, desc->block_size, p);
   const WsLayout w = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim);
-  const bool persist = partition_tokens == 0 && persist_eligible(desc, num_seqs, num_q_heads);
-  if (!w.bytes && !persist) return 0;
+  const bool stream = partition_tokens == 0 && stream_eligible(desc, num_seqs, num_q_heads, max_blocks);
+  if (!w.bytes && !stream) return 0;
   return align_up(static_cast<size_t>(num_seqs) * desc->num_kv_heads * sizeof(int), 256);
 }
 }  // namespace pkv
@@ -278,13 +330,15 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
   const int64_t splits = num_splits(max_blocks, desc->block_size, partition);
   if (splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits");
   const int choice = g_kernel_choice.load();
-  // The persistent schedule needs its own workspace; with a smaller (or no)
+  // The stream-K schedule needs its own workspace; with a smaller (or no)
   // workspace the fixed-split schedule runs instead.
-  const WsLayout pws = persist_layout(num_seqs, desc, num_q_heads);
-  const bool persist = partition_tokens == 0 && choice == PKV_KERNEL_PERSISTENT &&
-                       persist_eligible(desc, num_seqs, num_q_heads) && workspace != nullptr &&
-                       workspace_bytes >= pws.bytes;
-  const WsLayout ws = persist ? pws
+  const int ctas = stream_ctas();
+  const WsLayout pws = stream_layout(num_seqs, desc, num_q_heads, ctas);
+  const bool use_stream = partition_tokens == 0 && choice == PKV_KERNEL_PERSISTENT && ctas > 0 &&
+                          stream_eligible(desc, num_seqs, num_q_heads, max_blocks) &&
+                          workspace != nullptr && workspace_bytes >= pws.bytes &&
+                          tc_supported(desc, q_dtype, group, 64);
+  const WsLayout ws = use_stream ? pws
                               : workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, splits,
                                                  desc->head_dim);
   if (ws.bytes > 0) {
@@ -305,7 +359,8 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
   a.ws_l = ws.bytes ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
   a.ws_acc = ws.bytes ? reinterpret_cast<float*>(wsb + ws.acc_off) : nullptr;
   a.counters = ws.bytes ? reinterpret_cast<int*>(wsb + ws.counter_off) : nullptr;
-  a.ws_part = persist ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+  a.ws_part = use_stream ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+  a.ctas = use_stream ? ctas : 0;
   a.max_blocks = max_blocks;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -322,22 +377,20 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim;
   const bool tc_ok = tc_supported(desc, q_dtype, group, partition);
-  if ((choice == PKV_KERNEL_TENSOR_CORE || choice == PKV_KERNEL_PERSISTENT) && !tc_ok && !persist)
+  if ((choice == PKV_KERNEL_TENSOR_CORE || choice == PKV_KERNEL_PERSISTENT) && !tc_ok && !use_stream)
     return fail(PKV_ERR_UNSUPPORTED, "the tensor-core kernel does not cover these sizes");
-  if (persist || (tc_ok && choice != PKV_KERNEL_SIMT)) {
+  if (use_stream || (tc_ok && choice != PKV_KERNEL_SIMT)) {
     CUtensorMap kmap, vmap;
-    a.hg = persist ? persist_head_group(desc->num_kv_heads, desc->block_size) : 1;
-    const int box_rows = a.hg * desc->block_size;
-    st = pool_map(&kmap, k_cache, desc, box_rows);
-    if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc, box_rows);
+    st = pool_map(&kmap, k_cache, desc);
+    if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc);
     if (st != PKV_OK) return st;
-    if (persist) {
+    if (use_stream) {
       switch (kv) {
-        case PKV_F16: return launch_decode_persist<F16, F16>(a, D, kmap, vmap, s);
-        case PKV_BF16: return launch_decode_persist<BF16, BF16>(a, D, kmap, vmap, s);
+        case PKV_F16: return launch_decode_stream<F16, F16>(a, D, kmap, vmap, s);
+        case PKV_BF16: return launch_decode_stream<BF16, BF16>(a, D, kmap, vmap, s);
         default:
-          return q_dtype == PKV_F16 ? launch_decode_persist<E4M3, F16>(a, D, kmap, vmap, s)
-                                    : launch_decode_persist<E4M3, BF16>(a, D, kmap, vmap, s);
+          return q_dtype == PKV_F16 ? launch_decode_stream<E4M3, F16>(a, D, kmap, vmap, s)
+                                    : launch_decode_stream<E4M3, BF16>(a, D, kmap, vmap, s);
       }
     }
     switch (kv) {

@@ -22,9 +22,8 @@ struct DecodeArgs {
   float* ws_l;               // split-K partial sums      [B][Hq][S]
   float* ws_acc;             // split-K partial outputs   [B][Hq][S][D]
   int* counters;             // split-K arrival counters  [B][N_kv], zero between calls
-  float* ws_part;            // persistent kernel: 2 partial slots per CTA
-  int32_t stages;            // persistent kernel: ring slots
-  int32_t hg;                // persistent kernel: KV heads per tile (head group)
+  float* ws_part;            // stream-K kernel: 2 partial slots per CTA, [ctas][2][G][D + 2]
+  int32_t ctas;              // stream-K kernel: grid size (three CTAs per SM)
   int32_t max_blocks, num_seqs, num_q_heads, num_kv_heads, group, num_blocks, block_size;
   int32_t partition;         // tokens per split (multiple of 64 and of T)
   int32_t max_splits;        // S
@@ -32,18 +31,9 @@ struct DecodeArgs {
   float v_scale;             // 1, or the E4M3 V scale
 };
 
-// Limits of the persistent tensor-core kernel (shared by host and device code).
-constexpr int kPersistMaxCtas = 256;   // grid size cap (one CTA per SM)
-constexpr int kPersistMaxSeqs = 4096;  // per-call batch held in shared memory
-
-// Persistent kernel tiling: a tile is 64 rows of the pool, HG consecutive KV
-// heads of 64 / (HG * T) blocks, so that one TMA box carries HG heads of a
-// block.  HG is the largest power of two <= 64 / T that divides N_kv.
-inline int persist_head_group(int num_kv_heads, int block_size) {
-  int hg = 64 / block_size;
-  while (hg > 1 && num_kv_heads % hg != 0) hg /= 2;
-  return hg;
-}
+// Limits of the stream-K tensor-core kernel: the per-sequence tile prefix sum
+// is built in its 64 KiB ring ((num_seqs + 1) ints), and tile indices are int.
+constexpr int kStreamMaxSeqs = 16383;
 
 // Bytes at the start of a decode workspace that hold the split-K arrival
 // counters (they must be zero when a call starts; every call leaves them

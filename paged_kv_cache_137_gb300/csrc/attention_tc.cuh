@@ -563,21 +563,74 @@ __global__ void __launch_bounds__(kThreads, 3)
   __syncthreads();
   if (!s_last) return;
   __threadfence();
-  for (int i = tid; i < G * D; i += kThreads) {
-    const int row = i / D, d = i % D;
-    const size_t base = (head0 + row) * a.max_splits;
-    float M = -CUDART_INF_F;
-    for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(a.ws_m + base + sp));
-    float L = 0.f, A = 0.f;
-    if (M != -CUDART_INF_F) {
-      for (int sp = 0; sp < nsplit; ++sp) {
-        const float f = exp2f(__ldcg(a.ws_m + base + sp) - M);
-        L = fmaf(__ldcg(a.ws_l + base + sp), f, L);
-        A = fmaf(__ldcg(a.ws_acc + (base + sp) * D + d), f, A);
+  // Every load below is a global round trip of several microseconds while
+  // the GPU streams, so all splits' partials are first gathered into the
+  // (idle) stage buffers with independent loads, then combined.
+  const int nacc = G * nsplit * D;
+  float* g_acc = reinterpret_cast<float*>(smem);
+  float* g_m = g_acc + nacc;
+  float* g_l = g_m + G * nsplit;
+  if (G * nsplit <= kThreads && nacc + 2 * G * nsplit <= NS * G_::kStageBytes / 4) {
+    float mv = 0.f, lv = 0.f;
+    if (tid < G * nsplit) {
+      const size_t pidx = (head0 + tid / nsplit) * a.max_splits + tid % nsplit;
+      mv = __ldcg(a.ws_m + pidx);
+      lv = __ldcg(a.ws_l + pidx);
+    }
+    constexpr int kU = 8;  // float4 loads in flight per thread
+    for (int i0 = 0; i0 < nacc / 4; i0 += kU * kThreads) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i < nacc / 4) {
+          const int e = 4 * i, row = e / (nsplit * D), rem = e - row * nsplit * D;
+          const int sp = rem / D, d = rem - sp * D;
+          v[u] = __ldcg(reinterpret_cast<const float4*>(
+              a.ws_acc + ((head0 + row) * a.max_splits + sp) * D + d));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i < nacc / 4) reinterpret_cast<float4*>(g_acc)[i] = v[u];
       }
     }
-    const float out = (L > 0.f || L != L) ? A / L : 0.f;
-    store_elem<Q>(a.out, (head0 + row) * D + d, out);
+    if (tid < G * nsplit) {
+      g_m[tid] = mv;
+      g_l[tid] = lv;
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += kThreads) {
+      const int row = i / D, d = i % D;
+      float M = -CUDART_INF_F;
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, g_m[row * nsplit + sp]);
+      float L = 0.f, A = 0.f;
+      if (M != -CUDART_INF_F) {
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const float f = exp2f(g_m[row * nsplit + sp] - M);
+          L = fmaf(g_l[row * nsplit + sp], f, L);
+          A = fmaf(g_acc[(row * nsplit + sp) * D + d], f, A);
+        }
+      }
+      store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
+    }
+  } else {
+    for (int i = tid; i < G * D; i += kThreads) {
+      const int row = i / D, d = i % D;
+      const size_t base = (head0 + row) * a.max_splits;
+      float M = -CUDART_INF_F;
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(a.ws_m + base + sp));
+      float L = 0.f, A = 0.f;
+      if (M != -CUDART_INF_F) {
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const float f = exp2f(__ldcg(a.ws_m + base + sp) - M);
+          L = fmaf(__ldcg(a.ws_l + base + sp), f, L);
+          A = fmaf(__ldcg(a.ws_acc + (base + sp) * D + d), f, A);
+        }
+      }
+      store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
+    }
   }
   if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
 }

@@ -4,7 +4,7 @@
 
 #include <atomic>
 
-#include "attention_persist.cuh"
+#include "attention_stream.cuh"
 
 namespace pkv {
 namespace tc {
@@ -37,62 +37,53 @@ pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
   return check_launch("pkv_attention_decode (tensor core)");
 }
 
-// Persistent kernel: one CTA per SM (at most kPersistMaxCtas), as many ring
-// slots as the opt-in shared memory allows (2..8).
+// Stream-K kernel: a.ctas CTAs (three per SM, one wave), 64 KiB ring each.
 template <typename KV, typename Q, int D, int T>
-pkv_status launch_persist_dt(DecodeArgs a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                             cudaStream_t st) {
-  auto kernel = decode_persist_kernel<KV, Q, D, T>;
-  int dev = 0, sms = 0, optin = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev);
-  cudaFuncAttributes fa{};
-  if (e == cudaSuccess) e = cudaFuncGetAttributes(&fa, kernel);
-  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode (device query)", e);
-  const int smem_max = optin - static_cast<int>(fa.sharedSizeBytes);  // dynamic part
-  // The ring depth is a multiple of the consumer-group count, so that every
-  // slot is always consumed by the same group and each parity wait targets
-  // the next phase of its barrier (the producer clamps its batches to it).
-  constexpr int kMinStages = kGroups;
-  const int qrows = a.hg * a.group;
-  int ns = kPersistMaxStages / kGroups * kGroups;
-  while (ns > kMinStages && persist_smem_bytes(Geom<KV, D>::kStageBytes, D, ns, a.num_seqs,
-                                               a.group, qrows) > static_cast<size_t>(smem_max))
-    ns -= kGroups;
-  const size_t smem =
-      persist_smem_bytes(Geom<KV, D>::kStageBytes, D, ns, a.num_seqs, a.group, qrows);
-  if (smem > static_cast<size_t>(smem_max))
-    return fail(PKV_ERR_UNSUPPORTED, "persistent kernel: shared memory too small for this batch");
+pkv_status launch_stream_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                            cudaStream_t st) {
+  constexpr int smem = stream_smem_bytes<KV, D>();
+  auto kernel = decode_stream_kernel<KV, Q, D, T>;
   static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaGetDevice", e);
   const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
   if (!bit || !(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem_max);
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaFuncSetAttribute", e);
     configured.fetch_or(bit);
   }
-  a.stages = ns;
-  const int ctas = sms < kPersistMaxCtas ? sms : kPersistMaxCtas;
-  kernel<<<ctas, kPersistThreads, smem, st>>>(a, kmap, vmap);
-  return check_launch("pkv_attention_decode (persistent)");
+  // One wave: if fewer than three CTAs fit on an SM, shrink the grid to what
+  // is resident (the partial slots are sized for three per SM).
+  static std::atomic<int> occupancy[64];
+  int occ = dev < 64 ? occupancy[dev].load() : 0;
+  if (occ == 0) {
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem);
+    if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: occupancy query", e);
+    if (occ < 1) return fail(PKV_ERR_UNSUPPORTED, "stream-K kernel: no CTA fits on an SM");
+    if (dev < 64) occupancy[dev].store(occ);
+  }
+  const int ctas = occ >= kStreamCtasPerSm ? a.ctas : a.ctas / kStreamCtasPerSm * occ;
+  kernel<<<ctas, kThreads, smem, st>>>(a, kmap, vmap);
+  return check_launch("pkv_attention_decode (stream-K)");
 }
 
 }  // namespace tc
 
 template <typename KV, typename Q>
-pkv_status launch_decode_persist(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
-                                 const CUtensorMap& vmap, cudaStream_t st) {
+pkv_status launch_decode_stream(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
+                                const CUtensorMap& vmap, cudaStream_t st) {
   const int T = a.block_size;
   if constexpr (std::is_same<KV, E4M3>::value) {
-    if (head_dim == 128 && T == 16) return tc::launch_persist_dt<KV, Q, 128, 16>(a, kmap, vmap, st);
-    if (head_dim == 128 && T == 32) return tc::launch_persist_dt<KV, Q, 128, 32>(a, kmap, vmap, st);
+    if (head_dim == 128 && T == 16) return tc::launch_stream_dt<KV, Q, 128, 16>(a, kmap, vmap, st);
+    if (head_dim == 128 && T == 32) return tc::launch_stream_dt<KV, Q, 128, 32>(a, kmap, vmap, st);
   } else {
-    if (head_dim == 128 && T == 16) return tc::launch_persist_dt<KV, Q, 128, 16>(a, kmap, vmap, st);
-    if (head_dim == 128 && T == 32) return tc::launch_persist_dt<KV, Q, 128, 32>(a, kmap, vmap, st);
-    if (head_dim == 64 && T == 16) return tc::launch_persist_dt<KV, Q, 64, 16>(a, kmap, vmap, st);
-    if (head_dim == 64 && T == 32) return tc::launch_persist_dt<KV, Q, 64, 32>(a, kmap, vmap, st);
+    if (head_dim == 128 && T == 16) return tc::launch_stream_dt<KV, Q, 128, 16>(a, kmap, vmap, st);
+    if (head_dim == 128 && T == 32) return tc::launch_stream_dt<KV, Q, 128, 32>(a, kmap, vmap, st);
+    if (head_dim == 64 && T == 16) return tc::launch_stream_dt<KV, Q, 64, 16>(a, kmap, vmap, st);
+    if (head_dim == 64 && T == 32) return tc::launch_stream_dt<KV, Q, 64, 32>(a, kmap, vmap, st);
   }
-  return fail(PKV_ERR_UNSUPPORTED, "persistent kernel: head_dim/block_size not compiled");
+  return fail(PKV_ERR_UNSUPPORTED, "stream-K kernel: head_dim/block_size not compiled");
 }
 
 template <typename KV, typename Q>
