@@ -95,6 +95,9 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int g = lane >> 2, q4 = lane & 3;
   const int B = a.num_seqs, NKV = a.num_kv_heads, G = a.group, HQ = a.num_q_heads;
+  // Launched as a programmatic dependent of the previous kernel in the
+  // stream: nothing that kernel may write is read before it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int max_ctx = a.max_blocks * T;
   const int PS = G * (D + 2);  // floats of one partial slot
 

@@ -24,9 +24,8 @@
 //  * Tokens past the context end are masked to -inf, and their V rows are
 //    zeroed in shared memory before the p . V MMA (0 * NaN would poison it).
 //  * The four warps' (max, sum, output) are merged through shared memory.
-//    With several splits, each CTA writes its partial and the last CTA of the
-//    (sequence, KV head) to finish (an atomic counter, no waiting) merges all
-//    splits and resets the counter to zero.
+//    With several splits, each CTA writes its partial and a small merge grid,
+//    launched as a programmatic dependent of this one, combines the splits.
 //  * Every mbarrier wait is bounded; a timeout turns the heads' output into NaN
 //    after waiting (also bounded) for the copies still in flight.
 #pragma once
@@ -418,8 +417,16 @@ __global__ void __launch_bounds__(kThreads, 3)
   constexpr int kBoxBytes = T * 128;
   static_assert(kTile % T == 0, "a tile holds whole blocks");
 
-  const int split = blockIdx.x, kvh = blockIdx.y, seq = blockIdx.z;
+  // split-major grid: every pair's first split is dispatched before any
+  // second split, so that the short last splits of long pairs come last
+  const int kvh = blockIdx.x, seq = blockIdx.y, split = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Launched as a programmatic dependent of the previous kernel in the
+  // stream: nothing that kernel may write is read before it has completed.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the split-K merge grid may be scheduled once every CTA of this grid has
+  // started (it waits for this grid's completion before reading anything)
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int g = lane >> 2, q4 = lane & 3;
   const int G = a.group;
   const int ctx = a.ctx_lens[seq];
@@ -438,7 +445,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   uint8_t* stages = smem;                                            // NS * kStageBytes
   int32_t* s_tab = reinterpret_cast<int32_t*>(smem + NS * G_::kStageBytes);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_tab + kMaxTableEntries);
-  __shared__ int s_bad, s_last;
+  __shared__ int s_bad;
 
   static_assert(NS * G_::kStageBytes >= (2 * kWarps * 16 + kWarps * 16 * D) * 4,
                 "the warp merge reuses the stage buffers");
@@ -551,26 +558,34 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
     }
   }
-  if (nsplit == 1) return;
+}
 
-  // ------------------------------------------- split-K: the last CTA merges
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
-    s_last = prev == nsplit - 1;
-  }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  // Every load below is a global round trip of several microseconds while
-  // the GPU streams, so all splits' partials are first gathered into the
-  // (idle) stage buffers with independent loads, then combined.
+// ------------------------------------------------------- split-K merge kernel
+// One CTA per (KV head, sequence) with more than one split: gathers every
+// split's (max, sum, unnormalised output) into shared memory with independent
+// loads, then forms M = max m_i, L = sum l_i 2^(m_i - M),
+// o = sum a_i 2^(m_i - M) / L for the group's G heads.  It is launched as a
+// programmatic dependent of the decode kernel: it may start while the decode
+// grid drains and waits (griddepcontrol.wait) until that grid has completed
+// and its writes are visible, so the partials need no fences or counters.
+constexpr int kMergeSmemBytes = 48 * 1024;
+
+template <typename Q, int D>
+__global__ void __launch_bounds__(kThreads) merge_splits_kernel(const DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int kvh = blockIdx.x, seq = blockIdx.y, tid = threadIdx.x;
+  const int ctx = a.ctx_lens[seq];
+  if (ctx < 0 || ctx > a.max_blocks * a.block_size) return;  // written by the decode kernel
+  const int nsplit = max(1, (ctx + a.partition - 1) / a.partition);
+  if (nsplit <= 1) return;
+  const int G = a.group;
+  const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
+  extern __shared__ float4 merge_smem[];
+  float* g_acc = reinterpret_cast<float*>(merge_smem);
   const int nacc = G * nsplit * D;
-  float* g_acc = reinterpret_cast<float*>(smem);
   float* g_m = g_acc + nacc;
   float* g_l = g_m + G * nsplit;
-  if (G * nsplit <= kThreads && nacc + 2 * G * nsplit <= NS * G_::kStageBytes / 4) {
+  if (G * nsplit <= kThreads && nacc + 2 * G * nsplit <= kMergeSmemBytes / 4) {
     float mv = 0.f, lv = 0.f;
     if (tid < G * nsplit) {
       const size_t pidx = (head0 + tid / nsplit) * a.max_splits + tid % nsplit;
@@ -632,7 +647,6 @@ __global__ void __launch_bounds__(kThreads, 3)
       store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
     }
   }
-  if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
 }
 
 template <typename KV, int D, int NS>

@@ -3,11 +3,31 @@
 #pragma once
 
 #include <atomic>
+#include <utility>
 
 #include "attention_stream.cuh"
 
 namespace pkv {
 namespace tc {
+
+// Launch with programmatic stream serialization: the grid may be scheduled
+// while the previous kernel in the stream drains; the kernel itself waits
+// (griddepcontrol.wait) before reading its inputs.
+template <typename... Params, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, int threads, size_t smem,
+                             cudaStream_t st, Args&&... args) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = grid;
+  cfg.blockDim = dim3(threads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
+}
 
 // Stages per CTA: 64 KiB of ring for every cache type (three CTAs per SM).
 template <typename KV, int D>
@@ -32,9 +52,16 @@ pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
     if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaFuncSetAttribute", e);
     configured.fetch_or(bit);
   }
-  const dim3 grid(a.max_splits, a.num_kv_heads, a.num_seqs);
-  kernel<<<grid, kThreads, smem, st>>>(a, kmap, vmap);
-  return check_launch("pkv_attention_decode (tensor core)");
+  const dim3 grid(a.num_kv_heads, a.num_seqs, a.max_splits);
+  e = launch_dependent(kernel, grid, kThreads, smem, st, a, kmap, vmap);
+  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: launch", e);
+  pkv_status s = check_launch("pkv_attention_decode (tensor core)");
+  if (s != PKV_OK || a.max_splits <= 1) return s;
+  // the split-K merge, likewise a programmatic dependent of the decode grid
+  e = launch_dependent(merge_splits_kernel<Q, D>, dim3(a.num_kv_heads, a.num_seqs), kThreads,
+                       kMergeSmemBytes, st, a);
+  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: split-K merge launch", e);
+  return check_launch("pkv_attention_decode (split-K merge)");
 }
 
 // Stream-K kernel: a.ctas CTAs (three per SM, one wave), 64 KiB ring each.
@@ -64,7 +91,8 @@ pkv_status launch_stream_dt(const DecodeArgs& a, const CUtensorMap& kmap, const 
     if (dev < 64) occupancy[dev].store(occ);
   }
   const int ctas = occ >= kStreamCtasPerSm ? a.ctas : a.ctas / kStreamCtasPerSm * occ;
-  kernel<<<ctas, kThreads, smem, st>>>(a, kmap, vmap);
+  e = launch_dependent(kernel, dim3(ctas), kThreads, smem, st, a, kmap, vmap);
+  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: stream-K launch", e);
   return check_launch("pkv_attention_decode (stream-K)");
 }
 

@@ -30,6 +30,9 @@ struct WriteArgs {
 // One unit = 8 consecutive elements of one (token, head) row.
 template <typename Src, typename Dst>
 __global__ void __launch_bounds__(256) write_kernel(const WriteArgs a) {
+  // a decode kernel launched after this one as a programmatic dependent may
+  // be scheduled now; it waits for this grid's completion before its reads
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int which = blockIdx.y;  // 0 = K, 1 = V
   const int units_per_row = a.head_dim / 8;
   const int64_t units = a.n_tokens * a.n_kv * units_per_row;
@@ -80,6 +83,7 @@ struct CopyArgs {
 
 // grid: (pair, layer, K|V); each CTA copies one block of one tensor.
 __global__ void __launch_bounds__(256) copy_blocks_kernel(const __grid_constant__ CopyArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int pair = blockIdx.x, layer = blockIdx.y;
   uint8_t* base = static_cast<uint8_t*>(blockIdx.z == 0 ? a.k[layer] : a.v[layer]);
   const uint4* s = reinterpret_cast<const uint4*>(base + a.src[pair] * a.block_bytes);
