@@ -8,7 +8,8 @@ Qwen2.5-7B-shaped layer in bf16: 28 query / 4 KV heads, head_dim 128, block
 
 Prints one JSON line.  ``value`` is the attention's algorithmic K/V bytes
 (every cached K/V element once) divided by the device time of the step, in
-GB/s, inputs resident in HBM, L2 evicted before every timed step; ``e2e`` is
+GB/s, inputs resident in HBM and larger than L2, the K timed steps replayed
+back to back from one CUDA graph; ``e2e`` is
 the same metric through the C ABI with the step's inputs copied from pinned
 host memory and the output copied back inside the timed region.  With
 ``--impl reference`` the CPU oracle is timed on the host instead.
@@ -29,7 +30,9 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = "qwen_gqa_bf16"
 METRIC = "paged decode attention KV GB/s & fraction of GB300 HBM peak; decode tokens/s"
-KERNEL_SOURCES = ["attention.cu", "attention_simt.cuh", "attention.h", "device_common.cuh"]
+KERNEL_SOURCES = ["attention.cu", "attention.h", "attention_simt.cuh", "attention_tc.cuh",
+                  "attention_tc_launch.cuh", "attention_stream.cuh", "device_common.cuh"]
+NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 
 def parse():
@@ -61,6 +64,16 @@ def kernel_source_hash() -> str:
     for n in KERNEL_SOURCES:
         h.update(open(os.path.join(ROOT, "paged_kv_cache_137_gb300", "csrc", n), "rb").read())
     return h.hexdigest()[:16]
+
+
+def attention_kernels(kernel: str, w, splits: int) -> str:
+    """The kernels one attention call launches (timed together, as one graph)."""
+    if w.kv_dtype == "f32" or kernel == "simt":
+        k = "decode_simt_kernel"
+        return k + (" + merge_kernel" if splits > 1 else "")
+    if kernel == "persistent":
+        return "decode_stream_kernel"
+    return "decode_tc_kernel (split-K merge fused)"
 
 
 def traffic_for(config: str):
@@ -236,7 +249,7 @@ def run_gpu(args, world, rank, local):
     stream = torch.cuda.current_stream()
     kv_bytes = scn.kv_bytes()
     props = torch.cuda.get_device_properties(local)
-    # L2 eviction before every timed step: a READ of a buffer twice the L2
+    # L2 eviction for the isolated figures: a READ of a buffer twice the L2
     # size.  Writing it instead would leave the L2 full of dirty lines whose
     # write-back to HBM then competes with the step's own reads (about 10 %
     # of the attention time on this workload), a cost no decode step sees.
@@ -247,8 +260,8 @@ def run_gpu(args, world, rank, local):
                                            scn.partition)
     splits = -(-scn.plan.max_blocks * w.block_size // resolved)
     # write + decode (+ the separate merge of the CUDA-core kernel) + block copies
-    # the split-K merge is its own launch, except in the stream-K kernel
-    separate_merge = args.kernel != "persistent" or w.kv_dtype == "f32"
+    # the split-K merge is its own launch only in the CUDA-core path
+    separate_merge = args.kernel == "simt" or w.kv_dtype == "f32"
     attn_launches = 1 + (1 if separate_merge and splits > 1 else 0)
     launches_per_step = 1 + attn_launches + (-(-n_pairs // 1024) if n_pairs else 0)
 
@@ -259,11 +272,46 @@ def run_gpu(args, world, rank, local):
             scn.step()
     stream.wait_stream(side)
     torch.cuda.synchronize()
-    # The step (block copies, slot write, decode attention) is captured once
-    # as a CUDA graph and replayed, as a serving loop would: the timed region
-    # then holds GPU work only, not the host cost of each library call (that
-    # cost is in the end-to-end figure below, which calls the C ABI).  The
-    # attention alone is captured too, for the roofline of its kernel.
+    # Timed region: the K steps (block copies, slot write, decode attention)
+    # captured back to back in ONE CUDA graph, replayed once, as a serving
+    # loop replays a whole decode step: no library call and no graph launch
+    # sits between two steps (one graph launch costs several microseconds on
+    # its own).  No L2 flush between steps: the K/V each step reads is larger
+    # than the L2.  K attention calls in a second graph give the decode
+    # kernel's average duration for the roofline.  The isolated figures (one
+    # step per graph launch, the L2 evicted by a read before each) are
+    # reported beside them.
+    K = args.steps
+    g_steps, g_attns = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_steps):
+        for _ in range(K):
+            scn.copy_blocks()
+            scn.write_step()
+            scn.attend()
+    with torch.cuda.graph(g_attns):
+        for _ in range(K):
+            scn.attend()
+    g_steps.replay()
+    g_attns.replay()
+    torch.cuda.synchronize()
+
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev[0].record(stream)
+        g_steps.replay()
+        ev[1].record(stream)
+        ev[2].record(stream)
+        g_attns.replay()
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(ev[0].elapsed_time(ev[1]) / K, world)
+    attn = ev[2].elapsed_time(ev[3]) / K
+    value = world * kv_bytes / (ms / 1e3) / 1e9
+
+    # isolated: one step (or one attention call) per graph launch, L2 evicted
     g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step):
         scn.copy_blocks()
@@ -271,30 +319,46 @@ def run_gpu(args, world, rank, local):
         scn.attend()
     with torch.cuda.graph(g_attn):
         scn.attend()
+    iso = {"step": [], "attention": []}
+    for _ in range(20):
+        for name, g in (("step", g_step), ("attention", g_attn)):
+            torch.sum(flush, dim=(0,), out=flush_sink)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            iso[name].append((a, b))
     torch.cuda.synchronize()
+    iso_ms = {k: statistics.median(a.elapsed_time(b) for a, b in v) for k, v in iso.items()}
 
-    K = args.steps
-    ev = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(K)]
-    barrier(world)
-    torch.cuda.synchronize()
-    with ClockSampler(local) as clk:
-        for k in range(K):
-            torch.sum(flush, dim=(0,), out=flush_sink)
-            ev[k][0].record(stream)
-            g_step.replay()
-            ev[k][1].record(stream)
-        for k in range(K):
-            torch.sum(flush, dim=(0,), out=flush_sink)
-            ev[k][2].record(stream)
-            g_attn.replay()
-            ev[k][3].record(stream)
+    # the step's small kernels: 20 calls captured in one graph, so the graph's
+    # launch cost is spread over them (each call rewrites the same slots or
+    # copies the same blocks)
+    def per_call_us(fn, reps=20):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            for _ in range(reps):
+                fn()
+        g.replay()
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        g.replay()
+        b.record(stream)
         torch.cuda.synchronize()
-        barrier(world)
-    step_ms = [ev[k][0].elapsed_time(ev[k][1]) for k in range(K)]
-    attn_ms = [ev[k][2].elapsed_time(ev[k][3]) for k in range(K)]
-    ms = max_over_ranks(statistics.mean(step_ms), world)
-    attn = statistics.mean(attn_ms)
-    value = world * kv_bytes / (ms / 1e3) / 1e9
+        return a.elapsed_time(b) * 1e3 / reps
+
+    kvb = w.kv_bytes
+    n_new = len(scn.plan.seq_ids) * w.num_kv_heads * w.head_dim
+    write_bytes = 2 * n_new * (scn.k_new.element_size() + kvb) + 8 * len(scn.plan.seq_ids)
+    write_us = per_call_us(scn.write_step)
+    aux = {"slot_write_us": round(write_us, 2),
+           "slot_write_GBs": round(write_bytes / (write_us * 1e3), 2),
+           "copy_blocks_pairs": n_pairs}
+    if n_pairs:
+        copy_us = per_call_us(scn.copy_blocks)
+        block_bytes = w.num_kv_heads * w.block_size * w.head_dim * kvb
+        aux["copy_blocks_us"] = round(copy_us, 2)
+        aux["copy_blocks_GBs"] = round(2 * 2 * n_pairs * block_bytes / (copy_us * 1e3), 2)
 
     # end to end through the C ABI from pinned host buffers
     host = {n: getattr(scn, n).cpu().pin_memory() for n in ("q", "k_new", "v_new", "step_slots",
@@ -331,19 +395,26 @@ def run_gpu(args, world, rank, local):
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
                    "num_blocks": w.num_blocks, "context_tokens": int(scn.plan.ctx.sum()),
                    "kv_bytes_per_step": kv_bytes, "partition_tokens": scn.partition,
-                   "l2": ("inputs larger than L2 (K/V %d MB vs %d MB L2); L2 also evicted before every "
-                          "timed step by reading a 2x-L2 buffer" % (kv_bytes >> 20, props.L2_cache_size >> 20)),
-                   "launch": "step captured as one CUDA graph and replayed",
+                   "l2": ("inputs larger than L2 (K/V %d MB vs %d MB L2), no flush between steps"
+                          % (kv_bytes >> 20, props.L2_cache_size >> 20)),
+                   "launch": "the K steps captured back to back in one CUDA graph, replayed once",
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": round(world * w.num_seqs / (ms / 1e3), 1),
         "frac_of_hbm_peak": round(value / peak, 4),
-        "roofline": {"bound": "hbm", "kernel": f"pkv_attention_decode ({args.kernel} kernel)",
+        "frac_of_nominal_hbm": round(value / NOMINAL_HBM_GBS, 4),
+        "roofline": {"bound": "hbm", "kernel": attention_kernels(args.kernel, w, splits),
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic_for(args.config), "attention_ms": round(attn, 4)},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
         "gpu_launches": K * (launches_per_step + attn_launches),
+        "aux": aux,
+        "isolated": {"what": "one step (one attention call) per graph launch, L2 evicted by reading a "
+                             "2x-L2 buffer before each; median of 20",
+                     "step_ms": round(iso_ms["step"], 4), "attention_ms": round(iso_ms["attention"], 4),
+                     "value": round(world * kv_bytes / (iso_ms["step"] / 1e3) / 1e9, 2),
+                     "attention_GBs": round(kv_bytes / (iso_ms["attention"] / 1e3) / 1e9, 2)},
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:

@@ -24,8 +24,10 @@
 //  * Tokens past the context end are masked to -inf, and their V rows are
 //    zeroed in shared memory before the p . V MMA (0 * NaN would poison it).
 //  * The four warps' (max, sum, output) are merged through shared memory.
-//    With several splits, each CTA writes its partial and a small merge grid,
-//    launched as a programmatic dependent of this one, combines the splits.
+//    A pair's tiles are shared out evenly over its splits.  With several
+//    splits, each CTA writes its partial and the last CTA of the (sequence,
+//    KV head) to finish (an atomic counter, no waiting) gathers all splits'
+//    partials into shared memory, merges them and resets the counter.
 //  * Every mbarrier wait is bounded; a timeout turns the heads' output into NaN
 //    after waiting (also bounded) for the copies still in flight.
 #pragma once
@@ -406,6 +408,82 @@ __device__ __forceinline__ void combine_warps(const float* mS, const float* lS, 
   }
 }
 
+// Combine the nsplit partials (max m_i, sum l_i, unnormalised output a_i) of
+// the G heads at head0:  M = max m_i, L = sum l_i 2^(m_i - M),
+// o = sum a_i 2^(m_i - M) / L.  Every load is a global round trip of several
+// microseconds while the GPU streams, so all partials are first gathered into
+// shared memory (stage, `cap` floats) with independent loads.
+template <typename Q, int D>
+__device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit, float* stage, int cap) {
+  const int tid = threadIdx.x, G = a.group;
+  const int nacc = G * nsplit * D;
+  float* g_acc = stage;
+  float* g_m = g_acc + nacc;
+  float* g_l = g_m + G * nsplit;
+  if (G * nsplit <= kThreads && nacc + 2 * G * nsplit <= cap) {
+    float mv = 0.f, lv = 0.f;
+    if (tid < G * nsplit) {
+      const size_t pidx = (head0 + tid / nsplit) * a.max_splits + tid % nsplit;
+      mv = __ldcg(a.ws_m + pidx);
+      lv = __ldcg(a.ws_l + pidx);
+    }
+    constexpr int kU = 8;  // float4 loads in flight per thread
+    for (int i0 = 0; i0 < nacc / 4; i0 += kU * kThreads) {
+      float4 v[kU];
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i < nacc / 4) {
+          const int e = 4 * i, row = e / (nsplit * D), rem = e - row * nsplit * D;
+          const int sp = rem / D, d = rem - sp * D;
+          v[u] = __ldcg(reinterpret_cast<const float4*>(
+              a.ws_acc + ((head0 + row) * a.max_splits + sp) * D + d));
+        }
+      }
+#pragma unroll
+      for (int u = 0; u < kU; ++u) {
+        const int i = i0 + u * kThreads + tid;
+        if (i < nacc / 4) reinterpret_cast<float4*>(g_acc)[i] = v[u];
+      }
+    }
+    if (tid < G * nsplit) {
+      g_m[tid] = mv;
+      g_l[tid] = lv;
+    }
+    __syncthreads();
+    for (int i = tid; i < G * D; i += kThreads) {
+      const int row = i / D, d = i % D;
+      float M = -CUDART_INF_F;
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, g_m[row * nsplit + sp]);
+      float L = 0.f, A = 0.f;
+      if (M != -CUDART_INF_F) {
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const float f = exp2f(g_m[row * nsplit + sp] - M);
+          L = fmaf(g_l[row * nsplit + sp], f, L);
+          A = fmaf(g_acc[(row * nsplit + sp) * D + d], f, A);
+        }
+      }
+      store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
+    }
+  } else {
+    for (int i = tid; i < G * D; i += kThreads) {
+      const int row = i / D, d = i % D;
+      const size_t base = (head0 + row) * a.max_splits;
+      float M = -CUDART_INF_F;
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(a.ws_m + base + sp));
+      float L = 0.f, A = 0.f;
+      if (M != -CUDART_INF_F) {
+        for (int sp = 0; sp < nsplit; ++sp) {
+          const float f = exp2f(__ldcg(a.ws_m + base + sp) - M);
+          L = fmaf(__ldcg(a.ws_l + base + sp), f, L);
+          A = fmaf(__ldcg(a.ws_acc + (base + sp) * D + d), f, A);
+        }
+      }
+      store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
+    }
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 template <typename KV, typename Q, int D, int T, int NS>
 __global__ void __launch_bounds__(kThreads, 3)
@@ -424,17 +502,19 @@ __global__ void __launch_bounds__(kThreads, 3)
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: nothing that kernel may write is read before it has completed.
   asm volatile("griddepcontrol.wait;" ::: "memory");
-  // the split-K merge grid may be scheduled once every CTA of this grid has
-  // started (it waits for this grid's completion before reading anything)
-  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   const int g = lane >> 2, q4 = lane & 3;
   const int G = a.group;
   const int ctx = a.ctx_lens[seq];
   const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T;
   const int nsplit = bad_ctx ? 1 : max(1, (ctx + a.partition - 1) / a.partition);
   if (split >= nsplit) return;
-  const int t_begin = split * a.partition;
-  const int t_end = bad_ctx ? 0 : min(t_begin + a.partition, ctx);
+  // The pair's n_t tiles are shared out evenly: split i takes tiles
+  // [i n_t / nsplit, (i + 1) n_t / nsplit), at most partition / 64 of them.
+  // Near-equal pieces keep the longest units of the grid on pairs that need
+  // no merge, and the boundaries still depend only on the length.
+  const int64_t n_t = bad_ctx ? 0 : (ctx + kTile - 1) / kTile;
+  const int t_begin = static_cast<int>(split * n_t / nsplit) * kTile;
+  const int t_end = bad_ctx ? 0 : min(static_cast<int>((split + 1) * n_t / nsplit) * kTile, ctx);
   const int first_blk = t_begin / T;
   const int n_blk = (t_end - t_begin + T - 1) / T;
   const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
@@ -445,7 +525,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   uint8_t* stages = smem;                                            // NS * kStageBytes
   int32_t* s_tab = reinterpret_cast<int32_t*>(smem + NS * G_::kStageBytes);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_tab + kMaxTableEntries);
-  __shared__ int s_bad;
+  __shared__ int s_bad, s_last;
 
   static_assert(NS * G_::kStageBytes >= (2 * kWarps * 16 + kWarps * 16 * D) * 4,
                 "the warp merge reuses the stage buffers");
@@ -558,95 +638,23 @@ __global__ void __launch_bounds__(kThreads, 3)
       }
     }
   }
-}
 
-// ------------------------------------------------------- split-K merge kernel
-// One CTA per (KV head, sequence) with more than one split: gathers every
-// split's (max, sum, unnormalised output) into shared memory with independent
-// loads, then forms M = max m_i, L = sum l_i 2^(m_i - M),
-// o = sum a_i 2^(m_i - M) / L for the group's G heads.  It is launched as a
-// programmatic dependent of the decode kernel: it may start while the decode
-// grid drains and waits (griddepcontrol.wait) until that grid has completed
-// and its writes are visible, so the partials need no fences or counters.
-constexpr int kMergeSmemBytes = 48 * 1024;
+  if (nsplit == 1) return;
 
-template <typename Q, int D>
-__global__ void __launch_bounds__(kThreads) merge_splits_kernel(const DecodeArgs a) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const int kvh = blockIdx.x, seq = blockIdx.y, tid = threadIdx.x;
-  const int ctx = a.ctx_lens[seq];
-  if (ctx < 0 || ctx > a.max_blocks * a.block_size) return;  // written by the decode kernel
-  const int nsplit = max(1, (ctx + a.partition - 1) / a.partition);
-  if (nsplit <= 1) return;
-  const int G = a.group;
-  const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
-  extern __shared__ float4 merge_smem[];
-  float* g_acc = reinterpret_cast<float*>(merge_smem);
-  const int nacc = G * nsplit * D;
-  float* g_m = g_acc + nacc;
-  float* g_l = g_m + G * nsplit;
-  if (G * nsplit <= kThreads && nacc + 2 * G * nsplit <= kMergeSmemBytes / 4) {
-    float mv = 0.f, lv = 0.f;
-    if (tid < G * nsplit) {
-      const size_t pidx = (head0 + tid / nsplit) * a.max_splits + tid % nsplit;
-      mv = __ldcg(a.ws_m + pidx);
-      lv = __ldcg(a.ws_l + pidx);
-    }
-    constexpr int kU = 8;  // float4 loads in flight per thread
-    for (int i0 = 0; i0 < nacc / 4; i0 += kU * kThreads) {
-      float4 v[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * kThreads + tid;
-        if (i < nacc / 4) {
-          const int e = 4 * i, row = e / (nsplit * D), rem = e - row * nsplit * D;
-          const int sp = rem / D, d = rem - sp * D;
-          v[u] = __ldcg(reinterpret_cast<const float4*>(
-              a.ws_acc + ((head0 + row) * a.max_splits + sp) * D + d));
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * kThreads + tid;
-        if (i < nacc / 4) reinterpret_cast<float4*>(g_acc)[i] = v[u];
-      }
-    }
-    if (tid < G * nsplit) {
-      g_m[tid] = mv;
-      g_l[tid] = lv;
-    }
-    __syncthreads();
-    for (int i = tid; i < G * D; i += kThreads) {
-      const int row = i / D, d = i % D;
-      float M = -CUDART_INF_F;
-      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, g_m[row * nsplit + sp]);
-      float L = 0.f, A = 0.f;
-      if (M != -CUDART_INF_F) {
-        for (int sp = 0; sp < nsplit; ++sp) {
-          const float f = exp2f(g_m[row * nsplit + sp] - M);
-          L = fmaf(g_l[row * nsplit + sp], f, L);
-          A = fmaf(g_acc[(row * nsplit + sp) * D + d], f, A);
-        }
-      }
-      store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
-    }
-  } else {
-    for (int i = tid; i < G * D; i += kThreads) {
-      const int row = i / D, d = i % D;
-      const size_t base = (head0 + row) * a.max_splits;
-      float M = -CUDART_INF_F;
-      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(a.ws_m + base + sp));
-      float L = 0.f, A = 0.f;
-      if (M != -CUDART_INF_F) {
-        for (int sp = 0; sp < nsplit; ++sp) {
-          const float f = exp2f(__ldcg(a.ws_m + base + sp) - M);
-          L = fmaf(__ldcg(a.ws_l + base + sp), f, L);
-          A = fmaf(__ldcg(a.ws_acc + (base + sp) * D + d), f, A);
-        }
-      }
-      store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
-    }
+  // ------------------------------------------- split-K: the last CTA merges
+  // Each CTA counts itself in (an atomic counter, never a wait); the last of
+  // the pair's splits to finish combines all partials and resets the counter.
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
+    s_last = prev == nsplit - 1;
   }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  merge_splits<Q, D>(a, head0, nsplit, reinterpret_cast<float*>(smem), NS * G_::kStageBytes / 4);
+  if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
 }
 
 template <typename KV, int D, int NS>

@@ -55,13 +55,7 @@ pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
   const dim3 grid(a.num_kv_heads, a.num_seqs, a.max_splits);
   e = launch_dependent(kernel, grid, kThreads, smem, st, a, kmap, vmap);
   if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: launch", e);
-  pkv_status s = check_launch("pkv_attention_decode (tensor core)");
-  if (s != PKV_OK || a.max_splits <= 1) return s;
-  // the split-K merge, likewise a programmatic dependent of the decode grid
-  e = launch_dependent(merge_splits_kernel<Q, D>, dim3(a.num_kv_heads, a.num_seqs), kThreads,
-                       kMergeSmemBytes, st, a);
-  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: split-K merge launch", e);
-  return check_launch("pkv_attention_decode (split-K merge)");
+  return check_launch("pkv_attention_decode (tensor core)");
 }
 
 // Stream-K kernel: a.ctas CTAs (three per SM, one wave), 64 KiB ring each.
