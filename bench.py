@@ -76,15 +76,17 @@ def attention_kernels(kernel: str, w, splits: int) -> str:
     return "decode_tc_kernel (split-K merge fused)"
 
 
-def traffic_for(config: str):
+def traffic_for(config: str, kernels: str):
     """DRAM bytes per attention launch from the committed ncu summary, if it
-    was taken on the current kernel sources."""
+    was taken on the current kernel sources and the same kernel."""
     p = os.path.join(ROOT, "profiles", "attention_traffic.json")
     if not os.path.exists(p):
         return None
     d = json.load(open(p))
     e = d.get(config)
     if not e or e.get("kernel_sha") != kernel_source_hash():
+        return None
+    if not kernels.startswith(e.get("kernel", "?").split("<")[0]):
         return None
     return e.get("dram_bytes_per_launch")
 
@@ -385,6 +387,8 @@ def run_gpu(args, world, rank, local):
     e2e_val = world * kv_bytes / e2e_s / 1e9
 
     peak, peak_kind = peaks()
+    kernels = attention_kernels(args.kernel, w, splits)
+    traffic = traffic_for(args.config, kernels)
     achieved = kv_bytes / (attn / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -402,10 +406,11 @@ def run_gpu(args, world, rank, local):
         "tokens_per_s": round(world * w.num_seqs / (ms / 1e3), 1),
         "frac_of_hbm_peak": round(value / peak, 4),
         "frac_of_nominal_hbm": round(value / NOMINAL_HBM_GBS, 4),
-        "roofline": {"bound": "hbm", "kernel": attention_kernels(args.kernel, w, splits),
+        "roofline": {"bound": "hbm", "kernel": kernels,
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
-                     "traffic": traffic_for(args.config), "attention_ms": round(attn, 4)},
+                     "traffic": traffic, "attention_ms": round(attn, 4),
+                     **({"dram_achieved": round(traffic / (attn / 1e3) / 1e9, 2)} if traffic else {})},
         "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
         "gpu_launches": K * (launches_per_step + attn_launches),
