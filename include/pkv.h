@@ -203,23 +203,30 @@ PKV_API size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_hea
                                      const pkv_kv_desc* desc, int32_t partition_tokens);
 
 /* Decode-attention kernel selection, process-wide (default AUTO).  AUTO uses
- * the tensor-core kernel (TMA-staged tiles, MMA for q.K^T and p.V, fixed
- * splits) for 16-bit and E4M3 caches with head_dim 128 (16-bit also 64),
- * groups of up to 16 query heads and partitions of at most 1024 blocks, and
- * the CUDA-core kernel otherwise.  SIMT forces the CUDA-core kernel;
- * TENSOR_CORE makes pkv_attention_decode return PKV_ERR_UNSUPPORTED for sizes
- * it does not cover; PERSISTENT selects, for partition_tokens 0, the
- * persistent stream-K schedule of the tensor-core kernel (one CTA per SM,
- * equal tile shares, partial merges), falling back like TENSOR_CORE when the
- * workspace is smaller than pkv_attention_workspace_bytes(..., 0).  All
- * kernels compute the same result within rounding. */
+ * the tensor-core kernel (TMA-staged tiles, MMA for q.K^T and p.V, one CTA per
+ * (KV head, sequence, split), split-K merge fused) for 16-bit and E4M3 caches
+ * with head_dim 128 (16-bit also 64), groups of up to 16 query heads and
+ * partitions of at most 1024 blocks, and the CUDA-core kernel otherwise.  SIMT
+ * forces the CUDA-core kernel; TENSOR_CORE makes pkv_attention_decode return
+ * PKV_ERR_UNSUPPORTED for sizes it does not cover; PERSISTENT selects, for
+ * partition_tokens 0, the stream-K schedule of the tensor-core kernel (one wave
+ * of three CTAs per SM, each taking an equal slice of all (sequence, KV head,
+ * 64-token tile) work, shared pairs merged by the last CTA to finish), falling
+ * back like TENSOR_CORE when the workspace is smaller than
+ * pkv_attention_workspace_bytes(..., 0).  All kernels compute the same result
+ * within rounding. */
 #define PKV_KERNEL_AUTO 0
 #define PKV_KERNEL_SIMT 1
 #define PKV_KERNEL_TENSOR_CORE 2
 #define PKV_KERNEL_PERSISTENT 3
 PKV_API pkv_status pkv_set_attention_kernel(int32_t kind);
 
-/* Partition (tokens per split) pkv_attention_decode uses for these sizes. */
+/* Partition (tokens per split) pkv_attention_decode uses for these sizes.
+ * A pair of context ctx gets ceil(ctx / partition) splits (the tensor-core
+ * kernel shares its 64-token tiles evenly over them).  For partition_tokens 0
+ * it is the smallest multiple of 64 (and of the block size) for which the
+ * expected splits fit in one wave of resident CTAs on the current device, or
+ * 8192 when the (sequence, KV head) pairs alone exceed the slots. */
 PKV_API int32_t pkv_attention_partition(int32_t num_seqs, int32_t max_blocks, const pkv_kv_desc* desc,
                                 int32_t partition_tokens);
 
@@ -247,6 +254,9 @@ PKV_API int32_t pkv_attention_partition(int32_t num_seqs, int32_t max_blocks, co
  *                   aligned, ZERO-FILLED before its first use (every call
  *                   leaves it zeroed again); may be NULL if that size is 0.
  *                   Calls that share one workspace must not overlap in time.
+ * The tensor-core kernels are launched with programmatic stream
+ * serialization: they may be scheduled while the previous kernel in the stream
+ * drains, and read no input before that kernel has completed.
  * Inputs the kernel finds invalid (a table entry outside [0, num_blocks) or a
  * context length outside [0, max_blocks * T]) make the affected heads' output
  * NaN; nothing outside the given buffers is read or written. */
