@@ -1,4 +1,4 @@
-"""CPU oracle for paged KV-cache decode attention (TEST INFRASTRUCTURE ONLY).
+"""CPU oracle for paged KV-cache attention (TEST INFRASTRUCTURE ONLY).
 
 A plain, slow, obviously correct restatement of what the paged decode path
 computes, written from the PagedAttention pages (the apxml course page
@@ -19,10 +19,11 @@ Modules
     e4m3       OCP E4M3 (FN) encode/decode
     pool       the physical K/V pool: slot writes and block copies
     attention  decode attention gathered through block tables
+    prefill    multi-query (prefill) causal attention through block tables
     scenario   the five synthetic workloads built with the pieces above
 
 Parity pins: every function is checked in ``tests/test_oracle_*.py`` against
 values the pages print, closed forms, brute force and library routines; none
 is unpinned.
 """
-from . import sizing, allocator, e4m3, pool, attention  # noqa: F401
+from . import sizing, allocator, e4m3, pool, attention, prefill  # noqa: F401

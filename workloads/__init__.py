@@ -38,6 +38,7 @@ import numpy as np
 import torch
 
 __all__ = [
+    "q_for_chunk", "chunk_lens",
     "Workload", "CONFIGS", "get", "scaled",
     "rng", "context_lens", "free_order", "churn_ops", "q_for_seq", "kv_for_seq",
     "prefix_kv", "fork_layout", "fp8_scales", "kv_amax", "TORCH_DTYPES",
@@ -46,7 +47,7 @@ __all__ = [
 TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
 
 # Purpose keys of the independent random streams.
-_CTX, _ORDER, _CHURN, _Q, _K, _V, _PREFIX_K, _PREFIX_V, _TAIL = range(9)
+_CTX, _ORDER, _CHURN, _Q, _K, _V, _PREFIX_K, _PREFIX_V, _TAIL, _PREFILL_Q = range(10)
 
 
 @dataclass(frozen=True)
@@ -185,6 +186,22 @@ def q_for_seq(w: Workload, seq: int) -> torch.Tensor:
     """q of one sequence, [num_q_heads, head_dim] in the q dtype."""
     x = rng(w, _Q, seq).standard_normal((w.num_q_heads, w.head_dim), dtype=np.float32)
     return _cast(x, w.q_dtype)
+
+
+def q_for_chunk(w: Workload, seq: int, n_tokens: int) -> torch.Tensor:
+    """Queries of a prefill chunk of ``n_tokens`` tokens of one sequence,
+    [n_tokens, num_q_heads, head_dim] in the q dtype (their own stream, so they
+    do not depend on the decode queries)."""
+    x = rng(w, _PREFILL_Q, seq).standard_normal((n_tokens, w.num_q_heads, w.head_dim),
+                                                 dtype=np.float32)
+    return _cast(x, w.q_dtype)
+
+
+def chunk_lens(w: Workload, ctx, chunk: int) -> np.ndarray:
+    """Prefill chunk lengths: the last min(ctx, chunk) positions of each
+    sequence are its chunk (a sequence shorter than the chunk is a whole
+    prompt)."""
+    return np.minimum(np.asarray(ctx, dtype=np.int64), chunk)
 
 
 def kv_for_seq(w: Workload, seq: int, n_tokens: int, first_pos: int = 0,
