@@ -296,6 +296,41 @@ PKV_API pkv_status pkv_attention_decode_noalloc(void* out, const void* q, int32_
                                                 float softmax_scale, float k_scale, float v_scale,
                                                 int32_t partition_tokens, void* stream);
 
+/* Prefill (multi-query, causal) attention through block tables: the chunk
+ * of sequence s is its last n_s = query_start[s+1] - query_start[s] logical
+ * positions ctx_s - n_s .. ctx_s - 1, whose K/V are already in the pool
+ * (written by pkv_write, like a decode step's token); the query at position
+ * p attends to positions 0 .. p ("What the KV cache is": every earlier
+ * token's key and value serve the next token's attention; "The paging idea":
+ * a sequence starts with the blocks of its prompt; [T]: later tokens attend
+ * over the cached prompt):
+ *   out[r][j][:] = softmax_{p' <= p}( q[r][j] . K_s[p'] * softmax_scale ) V_s[p']
+ * for row r = query_start[s] + i at position p = ctx_s - n_s + i, K_s, V_s
+ * gathered through block_tables as in pkv_attention_decode (query head j
+ * reads KV head j / G).  A one-token chunk is decode attention.
+ *   out, q        : device [total_q][num_q_heads][head_dim], chunks packed in
+ *                   sequence order; q dtype = the cache dtype (F16 or BF16).
+ *   query_start   : device int32[num_seqs + 1], non-decreasing, [0] = 0,
+ *                   [num_seqs] = total_q.
+ *   max_query_len : >= every n_s (sets the grid).
+ *   context_lens  : device int32[num_seqs], chunk included (n_s <= ctx_s).
+ *   k_scale, v_scale : reserved for E4M3 caches (not supported yet).
+ * Supports 16-bit caches with head_dim 64 or 128 and block size 16 or 32
+ * (others: PKV_ERR_UNSUPPORTED).  A sequence whose lengths are invalid
+ * (ctx outside [0, max_blocks * T], n_s > ctx_s or n_s > max_query_len) or
+ * whose table holds an entry outside [0, num_blocks) gets NaN rows; rows
+ * outside [0, total_q) are never written.  Launched like the tensor-core
+ * decode kernel (programmatic stream serialization); asynchronous on
+ * `stream`. */
+PKV_API pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_dtype,
+                                         const void* k_cache, const void* v_cache,
+                                         const int32_t* block_tables, int32_t max_blocks,
+                                         const int32_t* context_lens, const int32_t* query_start,
+                                         int32_t num_seqs, int32_t total_q, int32_t max_query_len,
+                                         int32_t num_q_heads, const pkv_kv_desc* desc,
+                                         float softmax_scale, float k_scale, float v_scale,
+                                         void* stream);
+
 /* Message of the calling thread's last failure ("" if none). */
 PKV_API const char* pkv_last_error(void);
 

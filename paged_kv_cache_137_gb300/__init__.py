@@ -93,6 +93,8 @@ _SIGNATURES = {
     "pkv_set_attention_kernel": (_I32, [_I32]),
     "pkv_attention_decode_noalloc": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F,
                                             _F, _F, _I32, _P]),
+    "pkv_attention_prefill": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
+                                     _PDESC, _F, _F, _F, _P]),
     "pkv_last_error": (ctypes.c_char_p, []),
 }
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -349,6 +351,29 @@ def pkv_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, d
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), b, hq,
         ctypes.byref(desc), float(softmax_scale), float(k_scale), float(v_scale),
         int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def pkv_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
+                          desc: pkv_kv_desc, softmax_scale, max_query_len=None, k_scale=1.0,
+                          v_scale=1.0, stream=None):
+    """Prefill attention of packed chunks q [total_q, Hq, D]; query_start
+    int32[B + 1] (device) gives each sequence's rows.  ``max_query_len``
+    defaults to the longest chunk (read back from query_start)."""
+    total_q, hq, d = q.shape
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    b = context_lens.shape[0]
+    if block_tables.dim() != 2 or block_tables.shape[0] != b or query_start.shape != (b + 1,):
+        raise ValueError("block_tables int32[B, max_blocks], query_start int32[B + 1] expected")
+    if max_query_len is None:
+        max_query_len = int((query_start[1:] - query_start[:-1]).max().item()) if b else 0
+    _check(lib().pkv_attention_prefill(
+        _dev(out, "out"), _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache", desc.torch_dtype),
+        _dev(v_cache, "v_cache", desc.torch_dtype), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32),
+        _dev(query_start, "query_start", torch.int32), b, total_q, int(max_query_len), hq,
+        ctypes.byref(desc), float(softmax_scale), float(k_scale), float(v_scale), _stream(stream)))
     return out
 
 

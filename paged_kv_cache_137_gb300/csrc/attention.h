@@ -2,6 +2,7 @@
 // the kernel translation units.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -40,6 +41,11 @@ constexpr int kStreamMaxSeqs = 16383;
 // zero).  0 when the sizes need no split.
 size_t attention_counter_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks,
                                const pkv_kv_desc* desc, int32_t partition_tokens);
+
+// TMA tensor map of one pool tensor viewed as bytes [num_blocks * N_kv * T
+// rows][D * P_kv], read in boxes of T rows x 128 bytes with the 128-byte
+// swizzle (defined in attention.cu, shared by the decode and prefill paths).
+pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d);
 
 // Launch the CUDA-core decode kernel for one (cache dtype, q dtype) pair;
 // returns PKV_ERR_UNSUPPORTED for a shape it was not compiled for.

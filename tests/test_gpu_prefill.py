@@ -1,0 +1,164 @@
+"""GPU parity of prefill attention (pkv_attention_prefill) against the CPU
+oracle: max-abs 2e-2 and mean-abs 2e-3 for 16-bit caches.
+
+The device state is the decode workloads' (each sequence's prior tokens and
+the step token written through pkv_write); a sequence's chunk is its last
+min(ctx, chunk) positions, whose K/V are therefore in the pool."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import prefill as OP
+from oracle import scenario as OS
+
+import paged_kv_cache_137_gb300 as pkv
+from paged_kv_cache_137_gb300 import scenario as PS
+
+pytestmark = pytest.mark.gpu
+
+TOL = (2e-2, 2e-3)
+
+CASES = {
+    "qwen_small": W.scaled(W.get("qwen_gqa_bf16"), num_seqs=8, num_blocks=600, ctx_range=(1, 1000)),
+    "qwen_small_f16": W.scaled(W.get("qwen_gqa_bf16"), num_seqs=6, num_blocks=500,
+                               ctx_range=(1, 900), kv_dtype="f16", q_dtype="f16", seed=91),
+    "mha_t32": W.scaled(W.get("long_mha_bf16"), num_seqs=3, num_q_heads=4, num_kv_heads=4,
+                        num_blocks=200, ctx_range=(300, 1500), seed=94),
+    "gqa16_d64": W.scaled(W.get("qwen_gqa_bf16"), num_seqs=5, num_q_heads=32, num_kv_heads=2,
+                          head_dim=64, num_blocks=300, ctx_range=(1, 800), block_size=32, seed=93),
+}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pkv.build()
+    assert torch.cuda.is_available()
+
+
+_STATE = {}
+
+
+def state(name):
+    """(device scenario, oracle scenario) of a case, built once."""
+    if name not in _STATE:
+        w = CASES[name]
+        dev = PS.materialize(PS.plan(w), "cuda")
+        dev.copy_blocks()
+        dev.write_step()
+        torch.cuda.synchronize()
+        _STATE[name] = (dev, OS.build(w))
+    return _STATE[name]
+
+
+def chunk_inputs(dev, n):
+    """Packed queries of chunk lengths n (per batch row) and the row offsets."""
+    w = dev.plan.w
+    qs = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    q = torch.cat([W.q_for_chunk(w, s, int(n[r])) for r, s in enumerate(dev.plan.seq_ids)])
+    return q, qs
+
+
+def run_prefill(dev, q, qs, ctx=None, max_query_len=None):
+    w = dev.plan.w
+    out = torch.full_like(q, float("nan"), device="cuda")
+    qd = q.to("cuda")
+    ctx_t = dev.ctx if ctx is None else torch.from_numpy(np.asarray(ctx, dtype=np.int32)).cuda()
+    pkv.pkv_attention_prefill(out, qd, dev.k_cache, dev.v_cache, dev.tables, ctx_t,
+                              torch.from_numpy(qs).cuda(), dev.desc, 1.0 / math.sqrt(w.head_dim),
+                              max_query_len=max_query_len)
+    torch.cuda.synchronize()
+    return out
+
+
+def oracle(scn, q, qs, ctx=None):
+    return OP.paged_attention_prefill(q.double().numpy(), scn.pool, scn.tables,
+                                      scn.ctx if ctx is None else ctx, qs,
+                                      1.0 / math.sqrt(scn.w.head_dim))
+
+
+def check(got, ref):
+    g = got.double().cpu().numpy()
+    assert not np.isnan(g).any(), "NaN in the GPU output"
+    err = np.abs(g - ref)
+    assert err.max() <= TOL[0], f"max abs error {err.max():.3g}"
+    assert err.mean() <= TOL[1], f"mean abs error {err.mean():.3g}"
+
+
+@pytest.mark.parametrize("name", list(CASES))
+@pytest.mark.parametrize("chunk", [1, 37, 64, 200, 10 ** 6])
+def test_prefill_matches_oracle(name, chunk):
+    dev, scn = state(name)
+    n = W.chunk_lens(dev.plan.w, dev.plan.ctx, chunk)
+    q, qs = chunk_inputs(dev, n)
+    check(run_prefill(dev, q, qs), oracle(scn, q, qs))
+
+
+@pytest.mark.parametrize("name", ["qwen_small", "gqa16_d64"])
+def test_one_token_chunks_match_decode_kernel(name):
+    """A one-token chunk with the decode query is decode attention."""
+    dev, _ = state(name)
+    qs = np.arange(len(dev.plan.seq_ids) + 1, dtype=np.int32)
+    pre = run_prefill(dev, dev.q.cpu(), qs)
+    dec = dev.attend().clone()
+    torch.cuda.synchronize()
+    err = (pre.double() - dec.double()).abs()
+    assert err.max().item() <= TOL[0]
+
+
+def test_empty_chunks_and_whole_prompts_mixed():
+    dev, scn = state("qwen_small")
+    ctx = dev.plan.ctx
+    n = np.array([0 if r % 3 == 0 else (int(ctx[r]) if r % 3 == 1 else min(int(ctx[r]), 65))
+                  for r in range(len(ctx))])
+    q, qs = chunk_inputs(dev, n)
+    got = run_prefill(dev, q, qs)
+    check(got, oracle(scn, q, qs))
+
+
+def test_invalid_chunk_gives_nan_rows_and_leaves_others():
+    dev, scn = state("qwen_small")
+    ctx = dev.plan.ctx.copy()
+    n = np.minimum(ctx, 20)
+    q, qs = chunk_inputs(dev, n)
+    bad_ctx = ctx.copy()
+    bad_ctx[2] = int(n[2]) - 1           # fewer positions than queries
+    got = run_prefill(dev, q, qs, ctx=bad_ctx).double().cpu().numpy()
+    assert np.isnan(got[qs[2]:qs[3]]).all()
+    keep = np.ones(len(got), dtype=bool)
+    keep[qs[2]:qs[3]] = False
+    ref = oracle(scn, q, qs)
+    assert np.abs(got[keep] - ref[keep]).max() <= TOL[0]
+
+
+def test_physical_blocks_do_not_change_the_output():
+    """Tile boundaries depend only on logical positions: a different
+    permutation of the pool gives bit-identical outputs."""
+    w = CASES["qwen_small"]
+    outs, tables = [], []
+    for shuffled in (True, False):
+        wv = W.scaled(w, shuffled_pool=shuffled)
+        dev = PS.materialize(PS.plan(wv), "cuda")
+        dev.copy_blocks()
+        dev.write_step()
+        n = W.chunk_lens(wv, dev.plan.ctx, 100)
+        q, qs = chunk_inputs(dev, n)
+        outs.append(run_prefill(dev, q, qs))
+        tables.append(dev.plan.tables)
+    assert not np.array_equal(tables[0], tables[1])
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+
+
+def test_unsupported_cache_is_rejected():
+    w = W.scaled(W.get("fp8_churn"), num_seqs=2, num_blocks=64, churn=0, ctx_range=(1, 100))
+    desc = pkv.kv_desc(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, "e4m3")
+    kc, vc = pkv.empty_cache(desc, "cuda")
+    q = torch.zeros(3, w.num_q_heads, w.head_dim, dtype=torch.bfloat16, device="cuda")
+    with pytest.raises(pkv.PkvError):
+        pkv.pkv_attention_prefill(torch.empty_like(q), q, kc, vc,
+                                  torch.zeros(2, 8, dtype=torch.int32, device="cuda"),
+                                  torch.tensor([2, 1], dtype=torch.int32, device="cuda"),
+                                  torch.tensor([0, 2, 3], dtype=torch.int32, device="cuda"),
+                                  desc, 0.1)
