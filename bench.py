@@ -430,16 +430,221 @@ def run_gpu(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+# ------------------------------------------------------------------ prefill
+PREFILL_METRIC = "paged prefill attention TFLOP/s (causal, algorithmic) & fraction of GB300 bf16 tensor peak"
+
+
+def prefill_flops(w, ctx, n) -> int:
+    """Algorithmic FLOPs of causal chunked prefill: each query at position p
+    multiplies with p + 1 keys and values, 4 D flops per (query head, key)."""
+    return int(sum(4 * w.head_dim * w.num_q_heads * (int(n[i]) * (int(ctx[i]) - int(n[i])) +
+                                                     int(n[i]) * (int(n[i]) + 1) // 2)
+                   for i in range(len(ctx))))
+
+
+class PrefillOracle:
+    """The CPU oracle's prefill attention over a bounded sample of sequences
+    of the workload (the pool built once, not timed)."""
+
+    def __init__(self, config: str, n_seqs: int = 2):
+        import numpy as np
+        import workloads as W
+        from oracle import scenario as OS
+        self.w = w = W.get(config)
+        self.scn = OS.build(w, write_seqs=list(range(n_seqs)))
+        self.rows = list(range(n_seqs))
+        ctx = self.scn.ctx
+        self.n = W.chunk_lens(w, ctx, w.prefill_chunk)
+        self.qs = np.concatenate([[0], np.cumsum(self.n)])
+        self.q = np.concatenate([W.q_for_chunk(w, s, int(self.n[r])).double().numpy()
+                                 for r, s in enumerate(self.scn.seq_ids)])
+        self.flops = prefill_flops(w, ctx[:n_seqs], self.n[:n_seqs])
+
+    def one_pass(self) -> float:
+        import math
+        from oracle import prefill as OP
+        t0 = time.perf_counter()
+        OP.paged_attention_prefill(self.q, self.scn.pool, self.scn.tables, self.scn.ctx, self.qs,
+                                   1.0 / math.sqrt(self.w.head_dim), seqs=self.rows)
+        return time.perf_counter() - t0
+
+
+def run_prefill_reference(args, world, rank):
+    if rank != 0:
+        return
+    r = PrefillOracle(args.config)
+    for _ in range(args.warmup):
+        r.one_pass()
+    t = [r.one_pass() for _ in range(args.steps)]
+    sec = statistics.mean(t)
+    tf = r.flops / sec / 1e12
+    sample = f"sequences 0-1 of {args.config} (their whole chunks), one pass per step"
+    line = {"metric": PREFILL_METRIC, "value": round(tf, 6), "unit": "TFLOP/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(sec * 1e3, 3),
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+            "data": "synthetic", "impl": "reference",
+            "config": {"workload": args.config, "flops_per_step": r.flops},
+            "cpu_baseline": {"value": round(tf, 6), "unit": "TFLOP/s", "cores": 1, "kind": "oracle",
+                             "sample": sample},
+            "e2e": {"value": round(tf, 6), "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_prefill_gpu(args, world, rank, local):
+    import math
+    import numpy as np
+    import torch
+    import workloads as W
+    import paged_kv_cache_137_gb300 as pkv
+    from paged_kv_cache_137_gb300 import scenario as PS
+
+    pkv.build()
+    torch.cuda.set_device(local)
+    dev_name = f"cuda:{local}"
+    w = W.get(args.config)
+    scn = PS.materialize(PS.plan(w), dev_name)
+    scn.copy_blocks()
+    scn.write_step()
+    ctx = scn.plan.ctx
+    n = W.chunk_lens(w, ctx, w.prefill_chunk)
+    qs_np = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    total_q = int(qs_np[-1])
+    q = torch.cat([W.q_for_chunk(w, s, int(n[r])) for r, s in enumerate(scn.plan.seq_ids)]).to(dev_name)
+    out = torch.empty_like(q)
+    qs = torch.from_numpy(qs_np).to(dev_name)
+    # the chunk's K/V and slots (the same values the pool already holds)
+    kv = [W.kv_for_seq(w, s, int(n[r]), first_pos=int(ctx[r]) - int(n[r]))
+          for r, s in enumerate(scn.plan.seq_ids)]
+    k_new = torch.cat([k for k, _ in kv]).to(dev_name)
+    v_new = torch.cat([v for _, v in kv]).to(dev_name)
+    slots_np = np.concatenate([
+        [int(scn.plan.tables[r][p // w.block_size]) * w.block_size + p % w.block_size
+         for p in range(int(ctx[r]) - int(n[r]), int(ctx[r]))] for r in range(len(ctx))]).astype(np.int64)
+    slots = torch.from_numpy(slots_np).to(dev_name)
+    scale = 1.0 / math.sqrt(w.head_dim)
+    max_q = int(n.max())
+    flops = prefill_flops(w, ctx, n)
+    stream = torch.cuda.current_stream()
+
+    def attend():
+        pkv.pkv_attention_prefill(out, q, scn.k_cache, scn.v_cache, scn.tables, scn.ctx, qs, scn.desc,
+                                  scale, max_query_len=max_q)
+
+    def step():
+        pkv.pkv_write(scn.k_cache, scn.v_cache, k_new, v_new, slots, scn.desc)
+        attend()
+
+    side = torch.cuda.Stream(device=dev_name)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(max(args.warmup, 3)):
+            step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+    K = args.steps
+    g_steps, g_attns = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g_steps):
+        for _ in range(K):
+            step()
+    with torch.cuda.graph(g_attns):
+        for _ in range(K):
+            attend()
+    g_steps.replay()
+    g_attns.replay()
+    torch.cuda.synchronize()
+    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
+    barrier(world)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        ev[0].record(stream)
+        g_steps.replay()
+        ev[1].record(stream)
+        ev[2].record(stream)
+        g_attns.replay()
+        ev[3].record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    ms = max_over_ranks(ev[0].elapsed_time(ev[1]) / K, world)
+    attn = ev[2].elapsed_time(ev[3]) / K
+    value = world * flops / (ms / 1e3) / 1e12
+
+    # end to end through the C ABI from pinned host buffers
+    host = {"q": q.cpu().pin_memory(), "k": k_new.cpu().pin_memory(), "v": v_new.cpu().pin_memory(),
+            "slots": slots.cpu().pin_memory()}
+    out_host = torch.empty_like(out, device="cpu").pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    d2h = out_host.numel() * out_host.element_size()
+
+    def e2e_step():
+        q.copy_(host["q"], non_blocking=True)
+        k_new.copy_(host["k"], non_blocking=True)
+        v_new.copy_(host["v"], non_blocking=True)
+        slots.copy_(host["slots"], non_blocking=True)
+        step()
+        out_host.copy_(out, non_blocking=True)
+        torch.cuda.synchronize()
+
+    for _ in range(3):
+        e2e_step()
+    barrier(world)
+    t0 = time.perf_counter()
+    for _ in range(min(K, 50)):
+        e2e_step()
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / min(K, 50), world)
+
+    d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
+        if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
+    peak, peak_kind = (float(d["bf16_tflops"]), "measured") if "bf16_tflops" in d else (1900.0, "fallback")
+    achieved = flops / (attn / 1e3) / 1e12
+    line = {
+        "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
+        "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": w.kv_dtype,
+        "data": "synthetic",
+        "config": {"workload": args.config, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
+                   "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
+                   "chunk": w.prefill_chunk, "query_tokens": total_q,
+                   "context_tokens": int(ctx.sum()), "flops_per_step": flops,
+                   "l2": "no flush between steps (K/V of the chunks' contexts re-read each step)",
+                   "launch": "the K steps captured back to back in one CUDA graph, replayed once",
+                   "parallelism": "replicas" if world > 1 else "single"},
+        "tokens_per_s": round(world * total_q / (ms / 1e3), 1),
+        "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel (mma.sync m16n8k16)",
+                     "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
+                     "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} bf16 burst",
+                     "traffic": None, "attention_ms": round(attn, 4)},
+        "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                "ms_per_step": round(e2e_s * 1e3, 4)},
+        "gpu_launches": 2 * K + K,
+        "clocks": clk.summary(),
+    }
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        r = PrefillOracle(args.config)
+        t, passes, el = 0.0, 0, 0.0
+        while passes == 0 or el < args.cpu_seconds:
+            el += r.one_pass()
+            passes += 1
+        line["cpu_baseline"] = {"value": round(r.flops * passes / el / 1e12, 6), "unit": "TFLOP/s",
+                                "cores": 1, "kind": "oracle",
+                                "sample": f"sequences 0-1 of {args.config}, {passes} pass(es) in {el:.1f} s"}
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
 def main():
     args = parse()
     # the oracle is timed on one host thread
     for v in ("OMP_NUM_THREADS", "OPENBLAS_NUM_THREADS", "MKL_NUM_THREADS"):
         os.environ.setdefault(v, "1")
     world, rank, local = dist_setup(args)
+    import workloads as W
+    prefill = W.get(args.config).prefill_chunk > 0
     if args.impl == "reference":
-        run_reference(args, world, rank)
+        (run_prefill_reference if prefill else run_reference)(args, world, rank)
     else:
-        run_gpu(args, world, rank, local)
+        (run_prefill_gpu if prefill else run_gpu)(args, world, rank, local)
     if world > 1:
         import torch.distributed as dist
         dist.destroy_process_group()

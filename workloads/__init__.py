@@ -73,6 +73,7 @@ class Workload:
     partition_tokens: int = 0  # split-K partition size, 0 = library default
     churn: int = 0             # alloc/free operations applied before the workload
     shuffled_pool: bool = True
+    prefill_chunk: int = 0     # > 0: a prefill workload, chunks of the last positions
 
     @property
     def group(self) -> int:
@@ -109,6 +110,13 @@ CONFIGS = {
         name="fp8_churn", seed=1375, num_seqs=512, num_q_heads=64, num_kv_heads=8,
         head_dim=128, block_size=16, num_blocks=65536, kv_dtype="e4m3", q_dtype="bf16",
         ctx_range=(64, 8192), ctx_dist="loguniform", churn=10000),
+    # chunked prefill on the Qwen-shaped layer: each sequence's last 512
+    # positions are the chunk, attending to its cached prefix and causally
+    # within the chunk
+    "qwen_prefill_bf16": Workload(
+        name="qwen_prefill_bf16", seed=1376, num_seqs=16, num_q_heads=28, num_kv_heads=4,
+        head_dim=128, block_size=16, num_blocks=4500, kv_dtype="bf16", q_dtype="bf16",
+        ctx_range=(1024, 4096), prefill_chunk=512),
 }
 
 
