@@ -136,7 +136,9 @@ PKV_API pkv_status pkv_batch_append(pkv_pool* pool, const int64_t* seq_ids, int3
 /* The child (a new id) maps every block of the parent; counts + 1. */
 PKV_API pkv_status pkv_seq_fork(pkv_pool* pool, int64_t parent_id, int64_t child_id);
 
-/* Finish a sequence and return its unshared blocks to the stack. */
+/* Finish a sequence and return its unshared blocks to the stack (with prefix
+ * caching, a published block whose count reaches 0 is kept for reuse
+ * instead: see pkv_pool_enable_prefix_cache). */
 PKV_API pkv_status pkv_seq_free(pkv_pool* pool, int64_t seq_id);
 
 /* Copy one block table (logical order) into out[cap]; *n_blocks and
@@ -154,7 +156,8 @@ PKV_API pkv_status pkv_block_tables(const pkv_pool* pool, const int64_t* seq_ids
 /* Reference count of one block (0 = free). */
 PKV_API pkv_status pkv_block_refcount(const pkv_pool* pool, int32_t block, int32_t* refcount);
 
-/* Blocks on the free stack. */
+/* Blocks an append can take: the free stack, plus (with prefix caching) the
+ * published blocks nobody references. */
 PKV_API int32_t pkv_num_free_blocks(const pkv_pool* pool);
 
 /* The free stack, top first, into out[cap]; *n receives its size. */
@@ -330,6 +333,51 @@ PKV_API pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_dty
                                          int32_t num_q_heads, const pkv_kv_desc* desc,
                                          float softmax_scale, float k_scale, float v_scale,
                                          void* stream);
+
+/* ---------------------------------------------------------- prefix caching
+ * [F "The knobs"]: enable_prefix_caching hashes each filled block so that
+ * unrelated requests share physical blocks; [F "Failure modes"]: sharing is
+ * block-granular (block size 32: a shared 1,000-token prefix reuses at most
+ * 992 tokens; a divergence inside a block loses the whole block); [Q "Sharing,
+ * the second dividend"]: when the tokens match, the blocks holding their KV
+ * state are reused and that part of prefill is skipped.
+ *
+ * A full block whose token ids are known is published under the exact key
+ * (entry of the previous block, its block_size token ids); a block whose
+ * content is already published keeps the existing entry.  A published block
+ * whose count reaches 0 is kept, least recently freed first (a sequence's
+ * last block before its first), and taken again by a matching lookup or, once
+ * the free stack is empty, evicted by an append (its entry dropped).  A
+ * rolled-back append unpublishes the blocks it filled. */
+
+/* Turn prefix caching on; only while the pool has no sequence. */
+PKV_API pkv_status pkv_pool_enable_prefix_cache(pkv_pool* pool);
+
+/* Create a sequence from a prompt of n_tokens token ids (host): it takes the
+ * longest chain of published blocks matching the prompt's first full blocks,
+ * at most (n_tokens - 1) / block_size of them (at least one prompt token is
+ * left to compute), counts + 1.  *n_cached receives the tokens it holds (a
+ * multiple of block_size); the caller appends the rest with
+ * pkv_seq_append_tokens and writes only their K/V. */
+PKV_API pkv_status pkv_seq_create_cached(pkv_pool* pool, int64_t seq_id, const int32_t* token_ids,
+                                 int32_t n_tokens, int32_t* n_cached);
+
+/* pkv_seq_append with the token ids of the new positions (host
+ * int32[n_new]); blocks it fills are published.  Ids are kept only while
+ * every earlier position's id is known (a plain pkv_seq_append stops them). */
+PKV_API pkv_status pkv_seq_append_tokens(pkv_pool* pool, int64_t seq_id, const int32_t* token_ids,
+                                 int32_t n_new, int64_t* slots_out, int32_t* cow_out,
+                                 int32_t cow_cap, int32_t* n_cow_out);
+
+/* Published blocks, published blocks at count 0, prompt tokens served from
+ * the cache so far, and evictions. */
+PKV_API pkv_status pkv_prefix_cache_stats(const pkv_pool* pool, int64_t* published_blocks,
+                                  int64_t* reusable_blocks, int64_t* hit_tokens,
+                                  int64_t* evictions);
+
+/* The reusable (published, count 0) blocks in eviction order, first to go
+ * first, into out[cap]; *n receives their number. */
+PKV_API pkv_status pkv_reusable_blocks(const pkv_pool* pool, int32_t* out, int32_t cap, int32_t* n);
 
 /* Message of the calling thread's last failure ("" if none). */
 PKV_API const char* pkv_last_error(void);

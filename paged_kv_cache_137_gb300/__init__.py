@@ -95,6 +95,11 @@ _SIGNATURES = {
                                             _F, _F, _I32, _P]),
     "pkv_attention_prefill": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
                                      _PDESC, _F, _F, _F, _P]),
+    "pkv_pool_enable_prefix_cache": (_I32, [_P]),
+    "pkv_seq_create_cached": (_I32, [_P, _I64, _PI32, _I32, _PI32]),
+    "pkv_seq_append_tokens": (_I32, [_P, _I64, _PI32, _I32, _PI64, _PI32, _I32, _PI32]),
+    "pkv_prefix_cache_stats": (_I32, [_P, _PI64, _PI64, _PI64, _PI64]),
+    "pkv_reusable_blocks": (_I32, [_P, _PI32, _I32, _PI32]),
     "pkv_last_error": (ctypes.c_char_p, []),
 }
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -252,6 +257,43 @@ class Pool:
         _check(lib().pkv_free_stack(self._h, None, 0, ctypes.byref(n)))
         out = np.empty(max(n.value, 1), dtype=np.int32)
         _check(lib().pkv_free_stack(self._h, _i32p(out), len(out), ctypes.byref(n)))
+        return out[:n.value]
+
+    # --- prefix caching
+    def enable_prefix_cache(self):
+        _check(lib().pkv_pool_enable_prefix_cache(self._h))
+
+    def seq_create_cached(self, seq_id: int, token_ids) -> int:
+        """Create a sequence from a prompt; -> tokens served from the cache."""
+        ids = np.ascontiguousarray(token_ids, dtype=np.int32)
+        n = ctypes.c_int32(0)
+        _check(lib().pkv_seq_create_cached(self._h, int(seq_id), _i32p(ids), len(ids),
+                                           ctypes.byref(n)))
+        return n.value
+
+    def seq_append_tokens(self, seq_id: int, token_ids):
+        """Append tokens with their ids -> (slots int64[n], cow pairs int32[n, 2])"""
+        ids = np.ascontiguousarray(token_ids, dtype=np.int32)
+        n_new = len(ids)
+        slots = np.empty(max(n_new, 1), dtype=np.int64)
+        cow = np.empty(2, dtype=np.int32)
+        n_cow = ctypes.c_int32(0)
+        _check(lib().pkv_seq_append_tokens(self._h, int(seq_id), _i32p(ids), n_new, _i64p(slots),
+                                           _i32p(cow), 1, ctypes.byref(n_cow)))
+        return slots[:n_new], cow[:2 * n_cow.value].reshape(-1, 2)
+
+    def prefix_cache_stats(self):
+        """-> (published blocks, reusable blocks, cached prompt tokens served, evictions)"""
+        v = [ctypes.c_int64() for _ in range(4)]
+        _check(lib().pkv_prefix_cache_stats(self._h, *[ctypes.byref(x) for x in v]))
+        return tuple(x.value for x in v)
+
+    def reusable_blocks(self) -> np.ndarray:
+        """Published blocks at count 0, first to be evicted first."""
+        n = ctypes.c_int32(0)
+        _check(lib().pkv_reusable_blocks(self._h, None, 0, ctypes.byref(n)))
+        out = np.empty(max(n.value, 1), dtype=np.int32)
+        _check(lib().pkv_reusable_blocks(self._h, _i32p(out), len(out), ctypes.byref(n)))
         return out[:n.value]
 
     def usage(self):

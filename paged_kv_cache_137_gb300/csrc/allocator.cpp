@@ -11,6 +11,19 @@
 // (the shared prompt blocks' count equals the number of sequences mapping
 // them).
 //
+// Prefix caching (foundry page, "The knobs": enable_prefix_caching hashes each
+// filled block so that unrelated requests share physical blocks; "Failure
+// modes": sharing is block-granular; katajob Q&A, "Sharing, the second
+// dividend": if the tokens match, the blocks holding their KV state are reused
+// and that part of prefill is skipped) is optional per pool.  A full block is
+// published under the exact key (entry of the previous block, its T token
+// ids); a new sequence created from a prompt takes the longest chain of
+// published blocks that matches its first tokens, keeping at least one prompt
+// token to compute.  A published block whose count drops to zero is kept, in
+// least-recently-freed order, and handed out again only when the free stack
+// is empty (eviction: the oldest first, a sequence's last block before its
+// first).
+//
 // Every mutating call first works out how many blocks it will pop and fails
 // before touching anything when the stack is short, so calls are
 // all-or-nothing.  A batch append keeps an undo record per sequence and rolls
@@ -20,7 +33,9 @@
 #include <cstdint>
 #include <cstring>
 #include <limits>
+#include <list>
 #include <new>
+#include <string>
 #include <unordered_map>
 #include <vector>
 
@@ -46,6 +61,17 @@ void clear_error() { g_last_error.clear(); }
 struct Seq {
   std::vector<int32_t> table;  // logical block -> physical block
   int64_t len = 0;             // tokens written (slots reserved)
+  // prefix caching: token ids of positions 0 .. len - 1 while they are known
+  // (tokens.size() == len), and per full block the cache entry of its content
+  // (-1: not published / unknown)
+  std::vector<int32_t> tokens;
+  std::vector<int64_t> chain;
+};
+
+// One published block and its content key bytes (parent entry, token ids).
+struct CacheEntry {
+  std::string key;
+  int32_t block;
 };
 
 // What one single-sequence append changed, enough to undo it.
@@ -53,6 +79,8 @@ struct AppendUndo {
   int64_t seq_id;
   int64_t old_len;
   size_t old_table_size;
+  size_t old_chain_size;
+  size_t old_tokens_size;
   bool cow;
   int32_t cow_index;
   int32_t cow_src;
@@ -66,12 +94,113 @@ struct pkv_pool {
   std::vector<int32_t> free_stack;  // top = back()
   std::vector<int32_t> refcount;
   std::unordered_map<int64_t, pkv::Seq> seqs;
+  // prefix cache (off unless enabled)
+  bool caching = false;
+  int64_t next_entry = 1;                                 // entry 0 is the root (no parent)
+  std::unordered_map<std::string, int64_t> key_to_entry;  // key bytes -> entry
+  std::unordered_map<int64_t, pkv::CacheEntry> entries;   // entry -> key, block
+  std::vector<int64_t> block_entry;                       // block -> entry, -1 if none
+  std::list<int32_t> lru;                                 // cached blocks at count 0, oldest first
+  std::vector<std::list<int32_t>::iterator> lru_pos;
+  std::vector<char> in_lru;
+  int64_t hit_tokens = 0, evictions = 0;
 };
 
 namespace pkv {
 namespace {
 
 inline int64_t blocks_for(int64_t tokens, int32_t t) { return (tokens + t - 1) / t; }
+
+// Blocks a pop can hand out: the free stack, then (with prefix caching) the
+// cached blocks nobody references.
+inline int64_t available(const pkv_pool* p) {
+  return static_cast<int64_t>(p->free_stack.size()) + static_cast<int64_t>(p->lru.size());
+}
+
+std::string cache_key(int64_t parent, const int32_t* tokens, int32_t t) {
+  std::string k(sizeof(int64_t) + sizeof(int32_t) * t, '\0');
+  std::memcpy(&k[0], &parent, sizeof(int64_t));
+  std::memcpy(&k[sizeof(int64_t)], tokens, sizeof(int32_t) * t);
+  return k;
+}
+
+void unpublish(pkv_pool* p, int32_t b) {
+  const int64_t e = p->block_entry[b];
+  if (e < 0) return;
+  auto it = p->entries.find(e);
+  if (it != p->entries.end()) {
+    p->key_to_entry.erase(it->second.key);
+    p->entries.erase(it);
+  }
+  p->block_entry[b] = -1;
+}
+
+// Take a block: the top of the free stack, else evict the least recently
+// freed cached block (its entry is dropped).  The caller checked available().
+int32_t pop_block(pkv_pool* p) {
+  if (!p->free_stack.empty()) {
+    const int32_t b = p->free_stack.back();
+    p->free_stack.pop_back();
+    return b;
+  }
+  const int32_t b = p->lru.front();
+  p->lru.pop_front();
+  p->in_lru[b] = 0;
+  unpublish(p, b);
+  ++p->evictions;
+  return b;
+}
+
+// A block whose count reached zero: kept for reuse if it is published, else
+// back on the free stack.
+void release_block(pkv_pool* p, int32_t b) {
+  if (p->caching && p->block_entry[b] >= 0) {
+    p->lru.push_back(b);
+    p->lru_pos[b] = std::prev(p->lru.end());
+    p->in_lru[b] = 1;
+  } else {
+    p->free_stack.push_back(b);
+  }
+}
+
+// A cached block taken by a lookup: out of the reuse list if it was there.
+void acquire_cached(pkv_pool* p, int32_t b) {
+  if (p->in_lru[b]) {
+    p->lru.erase(p->lru_pos[b]);
+    p->in_lru[b] = 0;
+  }
+  p->refcount[b] += 1;
+}
+
+// Publish the blocks of s filled by positions [old_len, s.len) (token ids
+// known): each gets the entry of an equal published block or a new one.
+void publish_filled(pkv_pool* p, pkv::Seq& s, int64_t old_len) {
+  const int32_t t = p->block_size;
+  (void)old_len;
+  for (int64_t i = static_cast<int64_t>(s.chain.size()); (i + 1) * t <= s.len; ++i) {
+    const int64_t parent = i == 0 ? 0 : s.chain[i - 1];
+    if (parent < 0 || static_cast<int64_t>(s.tokens.size()) < (i + 1) * t) {
+      s.chain.push_back(-1);
+      continue;
+    }
+    const std::string key = cache_key(parent, &s.tokens[i * t], t);
+    auto it = p->key_to_entry.find(key);
+    if (it != p->key_to_entry.end()) {
+      s.chain.push_back(it->second);  // equal content already published elsewhere
+      continue;
+    }
+    const int32_t b = s.table[i];
+    if (p->block_entry[b] >= 0) {  // shared with a fork sibling that published it
+      s.chain.push_back(p->block_entry[b]);
+      continue;
+    }
+    const int64_t e = p->next_entry++;
+    p->key_to_entry.emplace(key, e);
+    p->entries.emplace(e, CacheEntry{key, b});
+    p->block_entry[b] = e;
+    s.chain.push_back(e);
+  }
+}
 
 // Blocks an append of n_new tokens pops, and whether its first token lands in
 // a shared, partly filled block (copy-on-write).
@@ -83,12 +212,13 @@ int64_t blocks_needed(const pkv_pool* p, const Seq& s, int64_t n_new, bool* cow)
 }
 
 pkv_status append_one(pkv_pool* p, int64_t seq_id, Seq& s, int64_t n_new, int64_t* slots_out,
-                      int32_t* cow_out, int32_t cow_cap, int32_t* n_cow, AppendUndo* undo) {
+                      int32_t* cow_out, int32_t cow_cap, int32_t* n_cow, AppendUndo* undo,
+                      const int32_t* token_ids = nullptr) {
   bool cow = false;
   const int64_t need = blocks_needed(p, s, n_new, &cow);
-  if (need > static_cast<int64_t>(p->free_stack.size())) {
-    set_error("sequence %lld needs %lld blocks, %zu free", (long long)seq_id, (long long)need,
-              p->free_stack.size());
+  if (need > available(p)) {
+    set_error("sequence %lld needs %lld blocks, %lld free", (long long)seq_id, (long long)need,
+              (long long)available(p));
     return PKV_ERR_OUT_OF_BLOCKS;
   }
   if (cow && (cow_out == nullptr || *n_cow >= cow_cap)) {
@@ -101,6 +231,8 @@ pkv_status append_one(pkv_pool* p, int64_t seq_id, Seq& s, int64_t n_new, int64_
     undo->seq_id = seq_id;
     undo->old_len = s.len;
     undo->old_table_size = s.table.size();
+    undo->old_chain_size = s.chain.size();
+    undo->old_tokens_size = s.tokens.size();
     undo->cow = cow;
     undo->cow_index = cow ? static_cast<int32_t>(s.len / t) : -1;
     undo->cow_src = cow ? s.table[s.len / t] : -1;
@@ -108,14 +240,12 @@ pkv_status append_one(pkv_pool* p, int64_t seq_id, Seq& s, int64_t n_new, int64_
   const int64_t start = s.len;
   for (int64_t pos = start; pos < start + n_new; ++pos) {
     if (pos % t == 0) {
-      const int32_t b = p->free_stack.back();
-      p->free_stack.pop_back();
+      const int32_t b = pop_block(p);
       p->refcount[b] = 1;
       s.table.push_back(b);
     } else if (pos == start && cow) {
       const int32_t src = s.table[pos / t];
-      const int32_t dst = p->free_stack.back();
-      p->free_stack.pop_back();
+      const int32_t dst = pop_block(p);
       p->refcount[dst] = 1;
       p->refcount[src] -= 1;
       s.table[pos / t] = dst;
@@ -125,7 +255,13 @@ pkv_status append_one(pkv_pool* p, int64_t seq_id, Seq& s, int64_t n_new, int64_
     }
     if (slots_out) slots_out[pos - start] = static_cast<int64_t>(s.table[pos / t]) * t + pos % t;
   }
+  // token ids are kept only while every earlier position's id is known
+  if (p->caching) {
+    if (token_ids && static_cast<int64_t>(s.tokens.size()) == start)
+      s.tokens.insert(s.tokens.end(), token_ids, token_ids + n_new);
+  }
   s.len = start + n_new;
+  if (p->caching) publish_filled(p, s, start);
   return PKV_OK;
 }
 
@@ -137,8 +273,11 @@ void undo_append(pkv_pool* p, const AppendUndo& u) {
     const int32_t b = s.table.back();
     s.table.pop_back();
     p->refcount[b] = 0;
+    if (p->caching) unpublish(p, b);  // published by the undone append
     p->free_stack.push_back(b);
   }
+  s.chain.resize(std::min(s.chain.size(), u.old_chain_size));
+  s.tokens.resize(std::min(s.tokens.size(), u.old_tokens_size));
   if (u.cow) {
     const int32_t dst = s.table[u.cow_index];
     p->refcount[dst] = 0;
@@ -246,6 +385,32 @@ pkv_status pkv_batch_append(pkv_pool* pool, const int64_t* seq_ids, int32_t n_se
   if (n_seqs > 0 && (!seq_ids || !slots_out))
     return fail(PKV_ERR_INVALID_ARG, "seq_ids or slots_out is NULL");
   if (cow_cap < 0) return fail(PKV_ERR_INVALID_ARG, "cow_cap is negative");
+  // check the whole batch first, so that a short pool changes nothing (and
+  // no cached block is evicted for a batch that then fails)
+  // (in batch order, with running totals, so that the first failing
+  // sequence and its error are the ones a sequential append would meet)
+  {
+    int64_t need = 0, cows = 0;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      auto it = pool->seqs.find(seq_ids[i]);
+      if (it == pool->seqs.end()) {
+        pkv::set_error("unknown sequence %lld", (long long)seq_ids[i]);
+        return PKV_ERR_UNKNOWN_SEQ;
+      }
+      bool cow = false;
+      need += pkv::blocks_needed(pool, it->second, 1, &cow);
+      if (need > pkv::available(pool)) {
+        pkv::set_error("sequence %lld: the batch needs %lld blocks, %lld free",
+                       (long long)seq_ids[i], (long long)need, (long long)pkv::available(pool));
+        return PKV_ERR_OUT_OF_BLOCKS;
+      }
+      if (cow && (cow_out == nullptr || ++cows > cow_cap)) {
+        pkv::set_error("sequence %lld needs a copy-on-write pair but cow_cap is exhausted",
+                       (long long)seq_ids[i]);
+        return PKV_ERR_INVALID_ARG;
+      }
+    }
+  }
   std::vector<pkv::AppendUndo> undo;
   undo.reserve(n_seqs);
   int32_t n_cow = 0;
@@ -295,8 +460,17 @@ pkv_status pkv_seq_free(pkv_pool* pool, int64_t seq_id) {
     pkv::set_error("unknown sequence %lld", (long long)seq_id);
     return PKV_ERR_UNKNOWN_SEQ;
   }
-  for (int32_t b : it->second.table) {
-    if (--pool->refcount[b] == 0) pool->free_stack.push_back(b);
+  const auto& tab = it->second.table;
+  if (pool->caching) {
+    // published blocks are kept last block first, so that a sequence's tail
+    // is evicted before its prefix
+    for (auto b = tab.rbegin(); b != tab.rend(); ++b)
+      if (pool->block_entry[*b] >= 0 && --pool->refcount[*b] == 0) pkv::release_block(pool, *b);
+    for (int32_t b : tab)
+      if (pool->block_entry[b] < 0 && --pool->refcount[b] == 0) pool->free_stack.push_back(b);
+  } else {
+    for (int32_t b : tab)
+      if (--pool->refcount[b] == 0) pool->free_stack.push_back(b);
   }
   pool->seqs.erase(it);
   return PKV_OK;
@@ -357,7 +531,7 @@ pkv_status pkv_block_refcount(const pkv_pool* pool, int32_t block, int32_t* refc
 }
 
 int32_t pkv_num_free_blocks(const pkv_pool* pool) {
-  return pool ? static_cast<int32_t>(pool->free_stack.size()) : 0;
+  return pool ? static_cast<int32_t>(pkv::available(pool)) : 0;
 }
 
 pkv_status pkv_free_stack(const pkv_pool* pool, int32_t* out, int32_t cap, int32_t* n) {
@@ -377,7 +551,90 @@ pkv_status pkv_pool_usage(const pkv_pool* pool, int64_t* live_seqs, int64_t* liv
   for (const auto& kv : pool->seqs) tokens += kv.second.len;
   if (live_seqs) *live_seqs = static_cast<int64_t>(pool->seqs.size());
   if (live_tokens) *live_tokens = tokens;
-  if (used_blocks) *used_blocks = pool->num_blocks - static_cast<int64_t>(pool->free_stack.size());
+  if (used_blocks) *used_blocks = pool->num_blocks - pkv::available(pool);
+  return PKV_OK;
+}
+
+pkv_status pkv_pool_enable_prefix_cache(pkv_pool* pool) {
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (pool->caching) return PKV_OK;
+  if (!pool->seqs.empty()) return fail(PKV_ERR_INVALID_ARG, "enable prefix caching before any sequence");
+  pool->caching = true;
+  pool->block_entry.assign(pool->num_blocks, -1);
+  pool->lru_pos.resize(pool->num_blocks);
+  pool->in_lru.assign(pool->num_blocks, 0);
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_create_cached(pkv_pool* pool, int64_t seq_id, const int32_t* token_ids,
+                                 int32_t n_tokens, int32_t* n_cached) {
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (!pool->caching) return fail(PKV_ERR_INVALID_ARG, "prefix caching is not enabled");
+  if (n_tokens < 0 || (n_tokens > 0 && !token_ids)) return fail(PKV_ERR_INVALID_ARG, "bad token ids");
+  if (pool->seqs.count(seq_id)) {
+    pkv::set_error("sequence %lld exists", (long long)seq_id);
+    return PKV_ERR_INVALID_ARG;
+  }
+  pkv::Seq s;
+  const int32_t t = pool->block_size;
+  // the longest chain of published blocks matching the prompt's first full
+  // blocks, leaving at least one prompt token to compute
+  const int64_t max_blocks = n_tokens > 0 ? (static_cast<int64_t>(n_tokens) - 1) / t : 0;
+  for (int64_t i = 0; i < max_blocks; ++i) {
+    const int64_t parent = i == 0 ? 0 : s.chain.back();
+    auto it = pool->key_to_entry.find(pkv::cache_key(parent, token_ids + i * t, t));
+    if (it == pool->key_to_entry.end()) break;
+    const int32_t b = pool->entries.at(it->second).block;
+    pkv::acquire_cached(pool, b);
+    s.table.push_back(b);
+    s.chain.push_back(it->second);
+  }
+  s.len = static_cast<int64_t>(s.table.size()) * t;
+  s.tokens.assign(token_ids, token_ids + s.len);
+  pool->hit_tokens += s.len;
+  if (n_cached) *n_cached = static_cast<int32_t>(s.len);
+  pool->seqs.emplace(seq_id, std::move(s));
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_append_tokens(pkv_pool* pool, int64_t seq_id, const int32_t* token_ids,
+                                 int32_t n_new, int64_t* slots_out, int32_t* cow_out,
+                                 int32_t cow_cap, int32_t* n_cow_out) {
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (n_new < 0) return fail(PKV_ERR_INVALID_ARG, "n_new is negative");
+  if (n_new > 0 && (!slots_out || !token_ids))
+    return fail(PKV_ERR_INVALID_ARG, "slots_out or token_ids is NULL");
+  if (cow_cap < 0) return fail(PKV_ERR_INVALID_ARG, "cow_cap is negative");
+  auto it = pool->seqs.find(seq_id);
+  if (it == pool->seqs.end()) {
+    pkv::set_error("unknown sequence %lld", (long long)seq_id);
+    return PKV_ERR_UNKNOWN_SEQ;
+  }
+  int32_t n_cow = 0;
+  const pkv_status st = pkv::append_one(pool, seq_id, it->second, n_new, slots_out, cow_out,
+                                        cow_cap, &n_cow, nullptr, token_ids);
+  if (n_cow_out) *n_cow_out = (st == PKV_OK) ? n_cow : 0;
+  return st;
+}
+
+pkv_status pkv_prefix_cache_stats(const pkv_pool* pool, int64_t* published_blocks,
+                                  int64_t* reusable_blocks, int64_t* hit_tokens,
+                                  int64_t* evictions) {
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (published_blocks) *published_blocks = static_cast<int64_t>(pool->entries.size());
+  if (reusable_blocks) *reusable_blocks = static_cast<int64_t>(pool->lru.size());
+  if (hit_tokens) *hit_tokens = pool->hit_tokens;
+  if (evictions) *evictions = pool->evictions;
+  return PKV_OK;
+}
+
+pkv_status pkv_reusable_blocks(const pkv_pool* pool, int32_t* out, int32_t cap, int32_t* n) {
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  const int32_t sz = static_cast<int32_t>(pool->lru.size());
+  if (cap > 0 && !out) return fail(PKV_ERR_INVALID_ARG, "out is NULL");
+  if (cap > 0 && cap < sz) return fail(PKV_ERR_INVALID_ARG, "cap is smaller than the list");
+  if (cap > 0) std::copy(pool->lru.begin(), pool->lru.end(), out);
+  if (n) *n = sz;
   return PKV_OK;
 }
 
