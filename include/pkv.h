@@ -379,6 +379,35 @@ PKV_API pkv_status pkv_prefix_cache_stats(const pkv_pool* pool, int64_t* publish
  * first, into out[cap]; *n receives their number. */
 PKV_API pkv_status pkv_reusable_blocks(const pkv_pool* pool, int32_t* out, int32_t cap, int32_t* n);
 
+/* -------------------------------------------------------------- preemption
+ * [F "The knobs"]: when the pool cannot satisfy a running sequence the engine
+ * preempts it, drops its blocks and re-prefills it later (recompute);
+ * [F "Effect"]: the scheduler preempts running sequences rather than failing
+ * them, and a request can be preempted and restarted several times; [F
+ * "Failure modes"]: the free-block watermark. */
+
+/* One decode step with preemption: append one token to each sequence in
+ * batch order, which is priority order.  When sequence i cannot get a block,
+ * the lowest-priority sequence still running (the last one in the batch not
+ * yet preempted, possibly i itself) is preempted (its blocks are freed as by
+ * pkv_seq_free and it no longer exists) until i fits or is itself preempted.
+ * slots_out[i] = -1 for preempted sequences (pkv_write skips negative slots);
+ * preempted_out (host int64[n_seqs]) receives the preempted ids in order,
+ * *n_preempted_out their number; cow_out must hold n_seqs pairs.  Never
+ * fails for lack of blocks; UNKNOWN_SEQ / INVALID_ARG (a duplicate id) change
+ * nothing.  A preempted sequence is re-admitted later with all its tokens
+ * (recompute), e.g. by pkv_seq_admit or pkv_seq_create_cached. */
+PKV_API pkv_status pkv_batch_append_preempt(pkv_pool* pool, const int64_t* seq_ids, int32_t n_seqs,
+                                    int64_t* slots_out, int32_t* cow_out, int32_t cow_cap,
+                                    int32_t* n_cow_out, int64_t* preempted_out,
+                                    int32_t* n_preempted_out);
+
+/* Admit a new sequence of n_tokens tokens (create + append) only if at least
+ * watermark_blocks blocks stay free afterwards; else OUT_OF_BLOCKS and no
+ * change.  slots_out: host int64[n_tokens]. */
+PKV_API pkv_status pkv_seq_admit(pkv_pool* pool, int64_t seq_id, int32_t n_tokens,
+                         int32_t watermark_blocks, int64_t* slots_out);
+
 /* Message of the calling thread's last failure ("" if none). */
 PKV_API const char* pkv_last_error(void);
 

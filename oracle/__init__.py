@@ -20,10 +20,12 @@ Modules
     pool       the physical K/V pool: slot writes and block copies
     attention  decode attention gathered through block tables
     prefill    multi-query (prefill) causal attention through block tables
+    prefix_cache  block allocator with prefix caching (published full blocks)
+    preemption    preemption by recompute, watermark admission
     scenario   the five synthetic workloads built with the pieces above
 
 Parity pins: every function is checked in ``tests/test_oracle_*.py`` against
 values the pages print, closed forms, brute force and library routines; none
 is unpinned.
 """
-from . import sizing, allocator, e4m3, pool, attention, prefill  # noqa: F401
+from . import sizing, allocator, e4m3, pool, attention, prefill, prefix_cache, preemption  # noqa: F401

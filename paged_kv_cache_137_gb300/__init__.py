@@ -100,6 +100,8 @@ _SIGNATURES = {
     "pkv_seq_append_tokens": (_I32, [_P, _I64, _PI32, _I32, _PI64, _PI32, _I32, _PI32]),
     "pkv_prefix_cache_stats": (_I32, [_P, _PI64, _PI64, _PI64, _PI64]),
     "pkv_reusable_blocks": (_I32, [_P, _PI32, _I32, _PI32]),
+    "pkv_batch_append_preempt": (_I32, [_P, _PI64, _I32, _PI64, _PI32, _I32, _PI32, _PI64, _PI32]),
+    "pkv_seq_admit": (_I32, [_P, _I64, _I32, _I32, _PI64]),
     "pkv_last_error": (ctypes.c_char_p, []),
 }
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -295,6 +297,28 @@ class Pool:
         out = np.empty(max(n.value, 1), dtype=np.int32)
         _check(lib().pkv_reusable_blocks(self._h, _i32p(out), len(out), ctypes.byref(n)))
         return out[:n.value]
+
+    # --- preemption
+    def batch_append_preempt(self, seq_ids):
+        """One token per sequence in priority order, preempting the lowest
+        priority when the pool runs dry -> (slots int64[B] (-1 = preempted),
+        cow int32[n, 2], preempted ids)"""
+        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
+        n = len(ids)
+        slots = np.empty(max(n, 1), dtype=np.int64)
+        cow = np.empty(2 * max(n, 1), dtype=np.int32)
+        pre = np.empty(max(n, 1), dtype=np.int64)
+        n_cow, n_pre = ctypes.c_int32(0), ctypes.c_int32(0)
+        _check(lib().pkv_batch_append_preempt(self._h, _i64p(ids), n, _i64p(slots), _i32p(cow), n,
+                                              ctypes.byref(n_cow), _i64p(pre), ctypes.byref(n_pre)))
+        return slots[:n], cow[:2 * n_cow.value].reshape(-1, 2), list(pre[:n_pre.value])
+
+    def seq_admit(self, seq_id: int, n_tokens: int, watermark_blocks: int = 0):
+        """Create + append n_tokens if watermark_blocks stay free -> slots"""
+        slots = np.empty(max(n_tokens, 1), dtype=np.int64)
+        _check(lib().pkv_seq_admit(self._h, int(seq_id), int(n_tokens), int(watermark_blocks),
+                                   _i64p(slots)))
+        return slots[:n_tokens]
 
     def usage(self):
         """-> (live sequences, live tokens, blocks in use)"""

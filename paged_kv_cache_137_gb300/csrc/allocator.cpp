@@ -288,6 +288,23 @@ void undo_append(pkv_pool* p, const AppendUndo& u) {
   s.len = u.old_len;
 }
 
+// Finish a sequence: its blocks whose count reaches zero go back on the stack
+// in logical order (published ones are kept for reuse, last block first, so
+// that a sequence's tail is evicted before its prefix).
+void free_seq_blocks(pkv_pool* pool, std::unordered_map<int64_t, pkv::Seq>::iterator it) {
+  const auto& tab = it->second.table;
+  if (pool->caching) {
+    for (auto b = tab.rbegin(); b != tab.rend(); ++b)
+      if (pool->block_entry[*b] >= 0 && --pool->refcount[*b] == 0) release_block(pool, *b);
+    for (int32_t b : tab)
+      if (pool->block_entry[b] < 0 && --pool->refcount[b] == 0) pool->free_stack.push_back(b);
+  } else {
+    for (int32_t b : tab)
+      if (--pool->refcount[b] == 0) pool->free_stack.push_back(b);
+  }
+  pool->seqs.erase(it);
+}
+
 }  // namespace
 }  // namespace pkv
 
@@ -460,19 +477,7 @@ pkv_status pkv_seq_free(pkv_pool* pool, int64_t seq_id) {
     pkv::set_error("unknown sequence %lld", (long long)seq_id);
     return PKV_ERR_UNKNOWN_SEQ;
   }
-  const auto& tab = it->second.table;
-  if (pool->caching) {
-    // published blocks are kept last block first, so that a sequence's tail
-    // is evicted before its prefix
-    for (auto b = tab.rbegin(); b != tab.rend(); ++b)
-      if (pool->block_entry[*b] >= 0 && --pool->refcount[*b] == 0) pkv::release_block(pool, *b);
-    for (int32_t b : tab)
-      if (pool->block_entry[b] < 0 && --pool->refcount[b] == 0) pool->free_stack.push_back(b);
-  } else {
-    for (int32_t b : tab)
-      if (--pool->refcount[b] == 0) pool->free_stack.push_back(b);
-  }
-  pool->seqs.erase(it);
+  pkv::free_seq_blocks(pool, it);
   return PKV_OK;
 }
 
@@ -636,6 +641,82 @@ pkv_status pkv_reusable_blocks(const pkv_pool* pool, int32_t* out, int32_t cap, 
   if (cap > 0) std::copy(pool->lru.begin(), pool->lru.end(), out);
   if (n) *n = sz;
   return PKV_OK;
+}
+
+// ------------------------------------------------------------- preemption
+// Foundry page, "The knobs" and "Effect": when the pool cannot satisfy a
+// running sequence the engine preempts it, drops its blocks and re-prefills
+// it later (recompute), instead of failing; "Failure modes": a free-block
+// watermark keeps admissions from driving the pool into constant preemption.
+
+
+pkv_status pkv_batch_append_preempt(pkv_pool* pool, const int64_t* seq_ids, int32_t n_seqs,
+                                    int64_t* slots_out, int32_t* cow_out, int32_t cow_cap,
+                                    int32_t* n_cow_out, int64_t* preempted_out,
+                                    int32_t* n_preempted_out) {
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (n_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "n_seqs is negative");
+  if (n_seqs > 0 && (!seq_ids || !slots_out || !preempted_out))
+    return fail(PKV_ERR_INVALID_ARG, "seq_ids, slots_out or preempted_out is NULL");
+  if (cow_cap < n_seqs || (n_seqs > 0 && !cow_out))
+    return fail(PKV_ERR_INVALID_ARG, "cow_out must hold n_seqs pairs");
+  {
+    std::unordered_map<int64_t, int> seen;
+    for (int32_t i = 0; i < n_seqs; ++i) {
+      if (!pool->seqs.count(seq_ids[i])) {
+        pkv::set_error("unknown sequence %lld", (long long)seq_ids[i]);
+        return PKV_ERR_UNKNOWN_SEQ;
+      }
+      if (seen[seq_ids[i]]++) return fail(PKV_ERR_INVALID_ARG, "a sequence appears twice in the batch");
+    }
+  }
+  // batch order is priority order: the sequence preempted is always the
+  // lowest-priority one still running (possibly the one being served)
+  std::vector<char> alive(n_seqs, 1);
+  int32_t last_alive = n_seqs - 1, n_cow = 0, n_pre = 0;
+  for (int32_t i = 0; i < n_seqs; ++i) {
+    slots_out[i] = -1;
+    if (!alive[i]) continue;
+    for (;;) {
+      auto it = pool->seqs.find(seq_ids[i]);
+      bool cow = false;
+      if (pkv::blocks_needed(pool, it->second, 1, &cow) <= pkv::available(pool)) {
+        pkv::append_one(pool, seq_ids[i], it->second, 1, slots_out + i, cow_out, cow_cap, &n_cow,
+                        nullptr);
+        break;
+      }
+      while (!alive[last_alive]) --last_alive;
+      const int32_t j = last_alive;
+      pkv::free_seq_blocks(pool, pool->seqs.find(seq_ids[j]));
+      alive[j] = 0;
+      preempted_out[n_pre++] = seq_ids[j];
+      if (j == i) break;
+    }
+  }
+  if (n_cow_out) *n_cow_out = n_cow;
+  if (n_preempted_out) *n_preempted_out = n_pre;
+  return PKV_OK;
+}
+
+pkv_status pkv_seq_admit(pkv_pool* pool, int64_t seq_id, int32_t n_tokens, int32_t watermark_blocks,
+                         int64_t* slots_out) {
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (n_tokens < 0 || watermark_blocks < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (n_tokens > 0 && !slots_out) return fail(PKV_ERR_INVALID_ARG, "slots_out is NULL");
+  if (pool->seqs.count(seq_id)) {
+    pkv::set_error("sequence %lld exists", (long long)seq_id);
+    return PKV_ERR_INVALID_ARG;
+  }
+  const int64_t need = pkv::blocks_for(n_tokens, pool->block_size);
+  if (need + watermark_blocks > pkv::available(pool)) {
+    pkv::set_error("admitting %d tokens needs %lld blocks above a watermark of %d; %lld free",
+                   n_tokens, (long long)need, watermark_blocks, (long long)pkv::available(pool));
+    return PKV_ERR_OUT_OF_BLOCKS;
+  }
+  auto ins = pool->seqs.emplace(seq_id, pkv::Seq{});
+  int32_t n_cow = 0;
+  return pkv::append_one(pool, seq_id, ins.first->second, n_tokens, slots_out, nullptr, 0, &n_cow,
+                         nullptr);
 }
 
 }  // extern "C"
