@@ -1,8 +1,9 @@
 """Benchmark: one decode step of paged attention on GB300.
 
 A step is the whole hot path over one batch: copy-on-write block copies (none
-in this workload), the slot write of the step's new K/V, and decode attention
-through the block tables (with its split-K merge).  The default workload is the
+in this workload), then the slot write of the step's new K/V and decode
+attention through the block tables (with its split-K merge), one fused launch
+(pkv_decode_step).  The default workload is the
 Qwen2.5-7B-shaped layer in bf16: 28 query / 4 KV heads, head_dim 128, block
 16, pool 8,500 blocks, 64 sequences with contexts uniform on [256, 4096].
 
@@ -262,10 +263,13 @@ def run_gpu(args, world, rank, local):
                                            scn.partition)
     splits = -(-scn.plan.max_blocks * w.block_size // resolved)
     # write + decode (+ the separate merge of the CUDA-core kernel) + block copies
-    # the split-K merge is its own launch only in the CUDA-core path
+    # the split-K merge is its own launch only in the CUDA-core path, and so
+    # is the slot write outside the tensor-core split kernel (which fuses it)
     separate_merge = args.kernel == "simt" or w.kv_dtype == "f32"
+    fused_write = not separate_merge and args.kernel != "persistent"
     attn_launches = 1 + (1 if separate_merge and splits > 1 else 0)
-    launches_per_step = 1 + attn_launches + (-(-n_pairs // 1024) if n_pairs else 0)
+    launches_per_step = (0 if fused_write else 1) + attn_launches + \
+        (-(-n_pairs // 1024) if n_pairs else 0)
 
     side = torch.cuda.Stream(device=dev_name)
     side.wait_stream(stream)
@@ -287,9 +291,7 @@ def run_gpu(args, world, rank, local):
     g_steps, g_attns = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_steps):
         for _ in range(K):
-            scn.copy_blocks()
-            scn.write_step()
-            scn.attend()
+            scn.step()
     with torch.cuda.graph(g_attns):
         for _ in range(K):
             scn.attend()
@@ -316,9 +318,7 @@ def run_gpu(args, world, rank, local):
     # isolated: one step (or one attention call) per graph launch, L2 evicted
     g_step, g_attn = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
     with torch.cuda.graph(g_step):
-        scn.copy_blocks()
-        scn.write_step()
-        scn.attend()
+        scn.step()
     with torch.cuda.graph(g_attn):
         scn.attend()
     iso = {"step": [], "attention": []}
@@ -363,8 +363,7 @@ def run_gpu(args, world, rank, local):
         aux["copy_blocks_GBs"] = round(2 * 2 * n_pairs * block_bytes / (copy_us * 1e3), 2)
 
     # end to end through the C ABI from pinned host buffers
-    host = {n: getattr(scn, n).cpu().pin_memory() for n in ("q", "k_new", "v_new", "step_slots",
-                                                          "tables", "ctx")}
+    host = {n: getattr(scn, n).cpu().pin_memory() for n in ("q", "k_new", "v_new", "tables", "ctx")}
     out_host = torch.empty_like(scn.out, device="cpu").pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values())
     d2h = out_host.numel() * out_host.element_size()

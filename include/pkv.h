@@ -271,6 +271,29 @@ PKV_API pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_dtyp
                                 int32_t partition_tokens, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* One decode step: the step's new K/V of each sequence written at its logical
+ * position ctx_s - 1 (the slot its block table gives: [F "In and out"], the
+ * new tokens written into reserved slots; R3: the context length counts the
+ * step's token), then pkv_attention_decode over positions 0 .. ctx_s - 1.
+ * The same as pkv_write (slots of positions ctx_s - 1) followed by
+ * pkv_attention_decode, in one launch where the tensor-core split kernel
+ * applies: the CTA that holds position ctx_s - 1 stores the token before it
+ * reads that tile (else a small write kernel runs first).
+ *   k_new, v_new : device [num_seqs][num_kv_heads][head_dim] in q_dtype
+ *                  (E4M3 caches: rounded as x * k_inv_scale / x *
+ *                  v_inv_scale, as pkv_write does).
+ * A sequence with context 0 (or an invalid length or table entry) writes
+ * nothing.  Block copies (copy-on-write) must run before this call.  Other
+ * arguments as pkv_attention_decode. */
+PKV_API pkv_status pkv_decode_step(void* out, const void* q, int32_t q_dtype, void* k_cache,
+                                   void* v_cache, const void* k_new, const void* v_new,
+                                   const int32_t* block_tables, int32_t max_blocks,
+                                   const int32_t* context_lens, int32_t num_seqs,
+                                   int32_t num_q_heads, const pkv_kv_desc* desc,
+                                   float softmax_scale, float k_scale, float v_scale,
+                                   float k_inv_scale, float v_inv_scale, int32_t partition_tokens,
+                                   void* workspace, size_t workspace_bytes, void* stream);
+
 /* Bytes of the fixed scratch array behind pkv_attention_decode_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 

@@ -102,6 +102,8 @@ _SIGNATURES = {
     "pkv_reusable_blocks": (_I32, [_P, _PI32, _I32, _PI32]),
     "pkv_batch_append_preempt": (_I32, [_P, _PI64, _I32, _PI64, _PI32, _I32, _PI32, _PI64, _PI32]),
     "pkv_seq_admit": (_I32, [_P, _I64, _I32, _I32, _PI64]),
+    "pkv_decode_step": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F, _F,
+                               _F, _F, _F, _I32, _P, ctypes.c_size_t, _P]),
     "pkv_last_error": (ctypes.c_char_p, []),
 }
 NOALLOC_SCRATCH_BYTES = 16 << 20
@@ -416,6 +418,31 @@ def pkv_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, d
         _dev(v_cache, "v_cache", desc.torch_dtype), _dev(block_tables, "block_tables", torch.int32),
         block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), b, hq,
         ctypes.byref(desc), float(softmax_scale), float(k_scale), float(v_scale),
+        int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def pkv_decode_step(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                    desc: pkv_kv_desc, softmax_scale, k_scale=1.0, v_scale=1.0, k_inv_scale=1.0,
+                    v_inv_scale=1.0, partition_tokens=0, workspace=None, stream=None):
+    """The step's K/V written at position ctx - 1 of each sequence, then decode
+    attention (one launch where the tensor-core split kernel applies)."""
+    b, hq, d = q.shape
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    if k_new.shape != v_new.shape or k_new.shape[0] != b or k_new.dtype != q.dtype:
+        raise ValueError("k_new, v_new must be [B, N_kv, D] in q's dtype")
+    if block_tables.dim() != 2 or block_tables.shape[0] != b or context_lens.shape != (b,):
+        raise ValueError("block_tables int32[B, max_blocks], context_lens int32[B] expected")
+    ws_ptr, ws_bytes = None, 0
+    if workspace is not None:
+        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+    _check(lib().pkv_decode_step(
+        _dev(out, "out"), _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache", desc.torch_dtype),
+        _dev(v_cache, "v_cache", desc.torch_dtype), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), b, hq, ctypes.byref(desc),
+        float(softmax_scale), float(k_scale), float(v_scale), float(k_inv_scale), float(v_inv_scale),
         int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)))
     return out
 

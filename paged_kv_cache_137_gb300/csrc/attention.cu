@@ -286,14 +286,17 @@ extern "C" pkv_status pkv_set_attention_kernel(int32_t kind) {
   return PKV_OK;
 }
 
-extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_dtype,
-                                           const void* k_cache, const void* v_cache,
-                                           const int32_t* block_tables, int32_t max_blocks,
-                                           const int32_t* context_lens, int32_t num_seqs,
-                                           int32_t num_q_heads, const pkv_kv_desc* desc,
-                                           float softmax_scale, float k_scale, float v_scale,
-                                           int32_t partition_tokens, void* workspace,
-                                           size_t workspace_bytes, void* stream) {
+namespace pkv {
+namespace {
+// Decode attention, optionally preceded by the step's slot write (k_new set):
+// fused into the tensor-core split kernel, else a small write kernel first.
+pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_cache,
+                       const void* v_cache, const int32_t* block_tables, int32_t max_blocks,
+                       const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads,
+                       const pkv_kv_desc* desc, float softmax_scale, float k_scale, float v_scale,
+                       int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+                       void* stream, const void* k_new, const void* v_new, float k_inv,
+                       float v_inv) {
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_q_heads <= 0 || max_blocks < 0)
@@ -380,6 +383,19 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
   const bool tc_ok = tc_supported(desc, q_dtype, group, partition);
   if ((choice == PKV_KERNEL_TENSOR_CORE || choice == PKV_KERNEL_PERSISTENT) && !tc_ok && !use_stream)
     return fail(PKV_ERR_UNSUPPORTED, "the tensor-core kernel does not cover these sizes");
+  if (k_new) {
+    if (!use_stream && tc_ok && choice != PKV_KERNEL_SIMT) {
+      a.k_new = k_new;  // fused into the split kernel
+      a.v_new = v_new;
+      a.k_inv = kv == PKV_E4M3 ? k_inv : 1.0f;
+      a.v_inv = kv == PKV_E4M3 ? v_inv : 1.0f;
+    } else {
+      st = launch_write_last(const_cast<void*>(k_cache), const_cast<void*>(v_cache), k_new, v_new,
+                             q_dtype, k_inv, v_inv, block_tables, max_blocks, context_lens,
+                             num_seqs, desc, s);
+      if (st != PKV_OK) return st;
+    }
+  }
   if (use_stream || (tc_ok && choice != PKV_KERNEL_SIMT)) {
     CUtensorMap kmap, vmap;
     st = pool_map(&kmap, k_cache, desc);
@@ -417,4 +433,36 @@ extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_d
     case PKV_F16: return launch_merge<F16>(a, D, s);
     default: return launch_merge<BF16>(a, D, s);
   }
+}
+}  // namespace
+}  // namespace pkv
+
+extern "C" pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_dtype,
+                                           const void* k_cache, const void* v_cache,
+                                           const int32_t* block_tables, int32_t max_blocks,
+                                           const int32_t* context_lens, int32_t num_seqs,
+                                           int32_t num_q_heads, const pkv_kv_desc* desc,
+                                           float softmax_scale, float k_scale, float v_scale,
+                                           int32_t partition_tokens, void* workspace,
+                                           size_t workspace_bytes, void* stream) {
+  return decode_impl(out, q, q_dtype, k_cache, v_cache, block_tables, max_blocks, context_lens,
+                     num_seqs, num_q_heads, desc, softmax_scale, k_scale, v_scale, partition_tokens,
+                     workspace, workspace_bytes, stream, nullptr, nullptr, 1.0f, 1.0f);
+}
+
+extern "C" pkv_status pkv_decode_step(void* out, const void* q, int32_t q_dtype, void* k_cache,
+                                      void* v_cache, const void* k_new, const void* v_new,
+                                      const int32_t* block_tables, int32_t max_blocks,
+                                      const int32_t* context_lens, int32_t num_seqs,
+                                      int32_t num_q_heads, const pkv_kv_desc* desc,
+                                      float softmax_scale, float k_scale, float v_scale,
+                                      float k_inv_scale, float v_inv_scale,
+                                      int32_t partition_tokens, void* workspace,
+                                      size_t workspace_bytes, void* stream) {
+  if (num_seqs > 0 && (!k_new || !v_new)) return fail(PKV_ERR_INVALID_ARG, "k_new or v_new is NULL");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  return decode_impl(out, q, q_dtype, k_cache, v_cache, block_tables, max_blocks, context_lens,
+                     num_seqs, num_q_heads, desc, softmax_scale, k_scale, v_scale, partition_tokens,
+                     workspace, workspace_bytes, stream, k_new, v_new, k_inv_scale, v_inv_scale);
 }

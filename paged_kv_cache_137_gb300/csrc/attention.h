@@ -25,6 +25,12 @@ struct DecodeArgs {
   int* counters;             // split-K arrival counters  [B][N_kv], zero between calls
   float* ws_part;            // stream-K kernel: 2 partial slots per CTA, [ctas][2][G][D + 2]
   int32_t ctas;              // stream-K kernel: grid size (three CTAs per SM)
+  // fused slot write (tensor-core split kernel): when k_new is set, the CTA
+  // holding position ctx - 1 of (sequence, KV head) first stores that
+  // token's K/V ([B][N_kv][D], q dtype), E4M3-rounded with k_inv / v_inv
+  const void* k_new;
+  const void* v_new;
+  float k_inv, v_inv;
   int32_t max_blocks, num_seqs, num_q_heads, num_kv_heads, group, num_blocks, block_size;
   int32_t partition;         // tokens per split (multiple of 64 and of T)
   int32_t max_splits;        // S
@@ -46,6 +52,13 @@ size_t attention_counter_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t ma
 // rows][D * P_kv], read in boxes of T rows x 128 bytes with the 128-byte
 // swizzle (defined in attention.cu, shared by the decode and prefill paths).
 pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d);
+
+// Write the step's K/V row of each sequence at logical position ctx - 1
+// through its block table (a small kernel; defined in write_copy.cu).
+pkv_status launch_write_last(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                             int32_t src_dtype, float k_inv_scale, float v_inv_scale,
+                             const int32_t* tables, int32_t max_blocks, const int32_t* ctx_lens,
+                             int32_t num_seqs, const pkv_kv_desc* desc, cudaStream_t st);
 
 // Launch the CUDA-core decode kernel for one (cache dtype, q dtype) pair;
 // returns PKV_ERR_UNSUPPORTED for a shape it was not compiled for.

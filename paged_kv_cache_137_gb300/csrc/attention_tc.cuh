@@ -538,6 +538,23 @@ __global__ void __launch_bounds__(kThreads, 3)
   for (int i = tid; i < n_blk; i += kThreads)
     s_tab[i] = a.tables[static_cast<size_t>(seq) * a.max_blocks + first_blk + i];
 
+  // Fused slot write: the split holding position ctx - 1 stores the step's
+  // token of its KV head before any copy is issued (a block never spans two
+  // splits, and other heads' rows are disjoint, so no other CTA reads it).
+  if (a.k_new != nullptr && !bad_ctx && ctx > 0 && split == nsplit - 1) {
+    const int p = ctx - 1;
+    const int blk = a.tables[static_cast<size_t>(seq) * a.max_blocks + p / T];
+    constexpr int kUnits = D / 8;
+    if (blk >= 0 && blk < a.num_blocks && tid < 2 * kUnits) {
+      const int which = tid / kUnits, d0 = (tid % kUnits) * 8;
+      const size_t src = (static_cast<size_t>(seq) * a.num_kv_heads + kvh) * D + d0;
+      const size_t dst = ((static_cast<size_t>(blk) * a.num_kv_heads + kvh) * T + p % T) * D + d0;
+      store8<Q, KV>(static_cast<const typename Q::raw*>(which ? a.v_new : a.k_new) + src,
+                    static_cast<typename KV::raw*>(const_cast<void*>(which ? a.v_cache : a.k_cache)) + dst,
+                    which ? a.v_inv : a.k_inv);
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // before the TMA reads it
+    }
+  }
   uint32_t qa[KS][4];
   load_q<KV, Q, D>(qa, static_cast<const typename Q::raw*>(a.q) +
                            (static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G) * D,

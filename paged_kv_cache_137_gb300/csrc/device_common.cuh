@@ -8,6 +8,8 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <type_traits>
+
 #include "common.h"
 
 namespace pkv {
@@ -165,6 +167,29 @@ inline pkv_status cuda_fail(const char* what, cudaError_t e) {
   set_error("%s: %s", what, cudaGetErrorString(e));
   (void)cudaGetLastError();
   return PKV_ERR_CUDA;
+}
+
+// Store 8 consecutive K/V elements of the source type into the cache type:
+// a plain copy for a 16/32-bit cache (which stores the input type), or
+// x * inv rounded to E4M3 (nearest even, saturating) for an E4M3 cache.
+// src and dst are 8-element aligned.
+template <typename Src, typename Dst>
+__device__ __forceinline__ void store8(const void* src, void* dst, float inv) {
+  if constexpr (std::is_same<Dst, E4M3>::value) {
+    float f[8];
+    LoadF32<Src, 8>::run(src, f);
+    uint2 packed;
+    uint16_t* q = reinterpret_cast<uint16_t*>(&packed);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) q[i] = f32x2_to_e4m3x2(f[2 * i] * inv, f[2 * i + 1] * inv);
+    *reinterpret_cast<uint2*>(dst) = packed;
+  } else {
+    static_assert(std::is_same<Src, Dst>::value, "16/32-bit caches store the input type");
+    const uint4* s = reinterpret_cast<const uint4*>(src);
+    uint4* d = reinterpret_cast<uint4*>(dst);
+#pragma unroll
+    for (int i = 0; i < Src::bytes / 2; ++i) d[i] = s[i];
+  }
 }
 
 inline bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }

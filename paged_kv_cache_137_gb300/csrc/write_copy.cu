@@ -50,23 +50,40 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteArgs a) {
     const size_t src_idx = (static_cast<size_t>(tok) * a.n_kv + h) * a.head_dim + d0;
     const size_t dst_idx =
         ((static_cast<size_t>(blk) * a.n_kv + h) * a.block_size + off) * a.head_dim + d0;
-    if constexpr (std::is_same<Dst, E4M3>::value) {
-      float f[8];
-      LoadF32<Src, 8>::run(static_cast<const typename Src::raw*>(a.src[which]) + src_idx, f);
-      const float inv = a.inv_scale[which];
-      uint2 packed;
-      uint16_t* q = reinterpret_cast<uint16_t*>(&packed);
-#pragma unroll
-      for (int i = 0; i < 4; ++i) q[i] = f32x2_to_e4m3x2(f[2 * i] * inv, f[2 * i + 1] * inv);
-      *reinterpret_cast<uint2*>(static_cast<uint8_t*>(a.cache[which]) + dst_idx) = packed;
-    } else {
-      static_assert(std::is_same<Src, Dst>::value, "16/32-bit caches store the input type");
-      using raw = typename Src::raw;
-      const uint4* s = reinterpret_cast<const uint4*>(static_cast<const raw*>(a.src[which]) + src_idx);
-      uint4* d = reinterpret_cast<uint4*>(static_cast<raw*>(a.cache[which]) + dst_idx);
-#pragma unroll
-      for (int i = 0; i < Src::bytes / 2; ++i) d[i] = s[i];
-    }
+    store8<Src, Dst>(static_cast<const typename Src::raw*>(a.src[which]) + src_idx,
+                     static_cast<typename Dst::raw*>(a.cache[which]) + dst_idx, a.inv_scale[which]);
+  }
+}
+
+// The step's token of each sequence: K/V row [n_kv][D] of batch row s written
+// at logical position ctx_s - 1 through its block table (nothing for a
+// length outside [1, max_blocks * T] or a table entry outside the pool).
+struct WriteLastArgs {
+  void* cache[2];
+  const void* src[2];   // [B][n_kv][D]
+  float inv_scale[2];
+  const int32_t* tables;
+  const int32_t* ctx_lens;
+  int32_t max_blocks, n_kv, head_dim, block_size, num_blocks;
+};
+
+template <typename Src, typename Dst>
+__global__ void __launch_bounds__(128) write_last_kernel(const WriteLastArgs a) {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  const int s = blockIdx.x, which = blockIdx.y;
+  const int ctx = a.ctx_lens[s];
+  if (ctx < 1 || ctx > a.max_blocks * a.block_size) return;
+  const int p = ctx - 1;
+  const int blk = a.tables[static_cast<size_t>(s) * a.max_blocks + p / a.block_size];
+  if (blk < 0 || blk >= a.num_blocks) return;
+  const int units = a.n_kv * (a.head_dim / 8);
+  for (int u = threadIdx.x; u < units; u += blockDim.x) {
+    const int h = u / (a.head_dim / 8), d0 = (u % (a.head_dim / 8)) * 8;
+    const size_t src_idx = (static_cast<size_t>(s) * a.n_kv + h) * a.head_dim + d0;
+    const size_t dst_idx =
+        ((static_cast<size_t>(blk) * a.n_kv + h) * a.block_size + p % a.block_size) * a.head_dim + d0;
+    store8<Src, Dst>(static_cast<const typename Src::raw*>(a.src[which]) + src_idx,
+                     static_cast<typename Dst::raw*>(a.cache[which]) + dst_idx, a.inv_scale[which]);
   }
 }
 
@@ -190,3 +207,49 @@ extern "C" pkv_status pkv_copy_blocks(void* const* k_caches, void* const* v_cach
   }
   return PKV_OK;
 }
+
+namespace pkv {
+
+template <typename Src, typename Dst>
+static pkv_status launch_write_last_dt(const WriteLastArgs& a, int32_t num_seqs, cudaStream_t st) {
+  write_last_kernel<Src, Dst><<<dim3(num_seqs, 2), 128, 0, st>>>(a);
+  return check_launch("pkv_decode_step (write)");
+}
+
+pkv_status launch_write_last(void* k_cache, void* v_cache, const void* k_new, const void* v_new,
+                             int32_t src_dtype, float k_inv_scale, float v_inv_scale,
+                             const int32_t* tables, int32_t max_blocks, const int32_t* ctx_lens,
+                             int32_t num_seqs, const pkv_kv_desc* desc, cudaStream_t st) {
+  WriteLastArgs a{};
+  a.cache[0] = k_cache;
+  a.cache[1] = v_cache;
+  a.src[0] = k_new;
+  a.src[1] = v_new;
+  a.inv_scale[0] = k_inv_scale;
+  a.inv_scale[1] = v_inv_scale;
+  a.tables = tables;
+  a.ctx_lens = ctx_lens;
+  a.max_blocks = max_blocks;
+  a.n_kv = desc->num_kv_heads;
+  a.head_dim = desc->head_dim;
+  a.block_size = desc->block_size;
+  a.num_blocks = desc->num_blocks;
+  const int kv = desc->kv_dtype;
+  if (kv == PKV_E4M3) {
+    switch (src_dtype) {
+      case PKV_F32: return launch_write_last_dt<F32, E4M3>(a, num_seqs, st);
+      case PKV_F16: return launch_write_last_dt<F16, E4M3>(a, num_seqs, st);
+      case PKV_BF16: return launch_write_last_dt<BF16, E4M3>(a, num_seqs, st);
+      default: return fail(PKV_ERR_INVALID_ARG, "k_new dtype must be F32, F16 or BF16");
+    }
+  }
+  if (src_dtype != kv) return fail(PKV_ERR_INVALID_ARG, "a 16/32-bit cache needs k_new of its dtype");
+  switch (kv) {
+    case PKV_F32: return launch_write_last_dt<F32, F32>(a, num_seqs, st);
+    case PKV_F16: return launch_write_last_dt<F16, F16>(a, num_seqs, st);
+    case PKV_BF16: return launch_write_last_dt<BF16, BF16>(a, num_seqs, st);
+  }
+  return fail(PKV_ERR_INVALID_ARG, "unknown kv_dtype");
+}
+
+}  // namespace pkv

@@ -28,8 +28,8 @@ import torch
 
 import workloads as W
 
-from . import (Pool, empty_cache, kv_desc, pkv_attention_decode, pkv_copy_blocks, pkv_write,
-               workspace_for)
+from . import (Pool, empty_cache, kv_desc, pkv_attention_decode, pkv_copy_blocks,
+               pkv_decode_step, pkv_write, workspace_for)
 
 CHURN_ID0 = 1 << 40
 POISON_BYTE = 0xFF
@@ -139,11 +139,20 @@ class DeviceScenario:
                                     self.softmax_scale, self.scales.get("k_scale", 1.0),
                                     self.scales.get("v_scale", 1.0), p, ws, stream)
 
+    def decode_step(self, stream=None, out=None):
+        """Slot write of the step's token fused with attention (pkv_decode_step)."""
+        return pkv_decode_step(self.out if out is None else out, self.q, self.k_cache, self.v_cache,
+                               self.k_new, self.v_new, self.tables, self.ctx, self.desc,
+                               self.softmax_scale, self.scales.get("k_scale", 1.0),
+                               self.scales.get("v_scale", 1.0), self.scales.get("k_inv_scale", 1.0),
+                               self.scales.get("v_inv_scale", 1.0), self.partition, self.workspace,
+                               stream)
+
     def step(self, stream=None):
-        """One decode step of the hot path: block copies, slot write, attention."""
+        """One decode step of the hot path: block copies, then the slot write
+        fused with attention."""
         self.copy_blocks(stream)
-        self.write_step(stream)
-        return self.attend(stream)
+        return self.decode_step(stream)
 
     def kv_bytes(self) -> int:
         """Algorithmic K/V bytes one attention call reads: each element once."""
