@@ -32,7 +32,7 @@ def _worker(rank, world, port, out):
 
 def test_max_over_ranks_and_barrier_with_gloo():
     world = 2
-    with mp.Manager() as m:
+    with mp.get_context("spawn").Manager() as m:
         out = m.dict()
         mp.spawn(_worker, args=(world, free_port(), out), nprocs=world, join=True)
         assert dict(out) == {0: 3.0, 1: 3.0}
