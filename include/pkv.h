@@ -335,14 +335,16 @@ PKV_API pkv_status pkv_attention_decode_noalloc(void* out, const void* q, int32_
  * gathered through block_tables as in pkv_attention_decode (query head j
  * reads KV head j / G).  A one-token chunk is decode attention.
  *   out, q        : device [total_q][num_q_heads][head_dim], chunks packed in
- *                   sequence order; q dtype = the cache dtype (F16 or BF16).
+ *                   sequence order; q dtype = the cache dtype (F16 or BF16),
+ *                   or F16 / BF16 with an E4M3 cache (K, V read as
+ *                   e4m3 * k_scale / v_scale).
  *   query_start   : device int32[num_seqs + 1], non-decreasing, [0] = 0,
  *                   [num_seqs] = total_q.
  *   max_query_len : >= every n_s (sets the grid).
  *   context_lens  : device int32[num_seqs], chunk included (n_s <= ctx_s).
- *   k_scale, v_scale : reserved for E4M3 caches (not supported yet).
- * Supports 16-bit caches with head_dim 64 or 128 and block size 16 or 32
- * (others: PKV_ERR_UNSUPPORTED).  A sequence whose lengths are invalid
+ *   k_scale, v_scale : E4M3 scales (ignored for 16-bit caches).
+ * Supports 16-bit caches with head_dim 64 or 128 and E4M3 caches with
+ * head_dim 128, block size 16 or 32 (others: PKV_ERR_UNSUPPORTED).  A sequence whose lengths are invalid
  * (ctx outside [0, max_blocks * T], n_s > ctx_s or n_s > max_query_len) or
  * whose table holds an entry outside [0, num_blocks) gets NaN rows; rows
  * outside [0, total_q) are never written.  Launched like the tensor-core

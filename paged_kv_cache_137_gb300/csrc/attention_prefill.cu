@@ -44,16 +44,19 @@ struct PrefillArgs {
   const int32_t* query_start; // [B + 1] row offsets of the chunks in q / out
   int32_t max_blocks, num_seqs, total_q, max_q_tiles, num_q_heads, num_kv_heads, group,
       num_blocks;
-  float qk_scale;             // softmax_scale * log2(e)
+  float qk_scale;             // softmax_scale * log2(e) (* k_scale for E4M3)
+  float v_scale;              // 1, or the E4M3 V scale
 };
 
-template <typename KV, int D, int T, int NS>
+template <typename KV, typename Q, int D, int T, int NS>
 __global__ void __launch_bounds__(kThreads, 2)
     prefill_tc_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap kmap,
                       const __grid_constant__ CUtensorMap vmap) {
   using G_ = Geom<KV, D>;
-  using raw = typename KV::raw;
-  constexpr bool kBf = std::is_same<KV, BF16>::value;
+  using raw = typename Q::raw;                  // q and out
+  constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
+  constexpr bool kBf = std::is_same<KV, BF16>::value;   // MMA type: bf16, else f16
+  constexpr bool kOutBf = std::is_same<Q, BF16>::value;
   constexpr int KS = D / 16;
   constexpr int NT = D / 8;
   constexpr int BPT = kTile / T;
@@ -79,8 +82,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (bad) {  // invalid lengths: the chunk's rows of head j become NaN
     if (qt_rev == 0)
       for (int i = tid; i < n * D; i += kThreads)
-        store_elem<KV>(a.out, (static_cast<size_t>(q0 + i / D) * HQ + j) * D + i % D,
-                       CUDART_NAN_F);
+        store_elem<Q>(a.out, (static_cast<size_t>(q0 + i / D) * HQ + j) * D + i % D,
+                      CUDART_NAN_F);
     return;
   }
   const int ntq = (n + kTile - 1) / kTile;
@@ -160,11 +163,20 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int h = 0; h < 2; ++h) {
       uint32_t lo = 0, hi = 0;
       if (rvalid[h]) {
-        const uint32_t* qp = reinterpret_cast<const uint32_t*>(
-            static_cast<const raw*>(a.q) +
-            (static_cast<size_t>(q0 + wr0 + g + 8 * h) * HQ + j) * D + 16 * ks + 2 * q4);
-        lo = qp[0];
-        hi = qp[4];
+        const raw* qrow =
+            static_cast<const raw*>(a.q) + (static_cast<size_t>(q0 + wr0 + g + 8 * h) * HQ + j) * D;
+        if constexpr (!kFp8) {
+          const uint32_t* qp = reinterpret_cast<const uint32_t*>(qrow + 16 * ks + 2 * q4);
+          lo = qp[0];
+          hi = qp[4];
+        } else {
+          // f16, head_dim permuted within the 16-element step so that one
+          // 4-byte K load serves both halves of the k-step
+          float f[4];
+          LoadF32<Q, 4>::run(qrow + 16 * ks + 4 * q4, f);
+          lo = pack2<false>(f[0], f[1]);
+          hi = pack2<false>(f[2], f[3]);
+        }
       }
       qa[ks][h] = lo;
       qa[ks][2 + h] = hi;
@@ -202,12 +214,26 @@ __global__ void __launch_bounds__(kThreads, 2)
       for (int nt = 0; nt < 8; ++nt) {
         sc[nt][0] = sc[nt][1] = sc[nt][2] = sc[nt][3] = 0.f;
         const int r = 8 * nt + li;
+        if constexpr (!kFp8) {
 #pragma unroll
-        for (int ks = 0; ks < KS; ks += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4(kbase + swz(r, 2 * ks + mi), b0, b1, b2, b3);
-          mma16816<kBf>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
-          mma16816<kBf>(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+          for (int ks = 0; ks < KS; ks += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4(kbase + swz(r, 2 * ks + mi), b0, b1, b2, b3);
+            mma16816<kBf>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
+            mma16816<kBf>(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
+          }
+        } else {
+#pragma unroll
+          for (int c0 = 0; c0 < KS; c0 += 4) {
+            uint32_t w[4];
+            ldsm_x4(kbase + swz(r, c0 + mi), w[0], w[1], w[2], w[3]);
+#pragma unroll
+            for (int jj = 0; jj < 4; ++jj) {
+              const int ks = c0 + jj;
+              mma16816<false>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3],
+                              e4m3x2_f16x2(w[jj] & 0xffffu), e4m3x2_f16x2(w[jj] >> 16));
+            }
+          }
         }
       }
       // causal mask and online softmax, rows g (h = 0) and g + 8 (h = 1)
@@ -256,12 +282,31 @@ __global__ void __launch_bounds__(kThreads, 2)
         const uint32_t pa2 = pack2<kBf>(sc[2 * kk + 1][0], sc[2 * kk + 1][1]);
         const uint32_t pa3 = pack2<kBf>(sc[2 * kk + 1][2], sc[2 * kk + 1][3]);
         const int rv = 16 * kk + (mi & 1) * 8 + li;
+        if constexpr (!kFp8) {
 #pragma unroll
-        for (int c = 0; c < NT; c += 2) {
-          uint32_t b0, b1, b2, b3;
-          ldsm_x4_t(vbase + swz(rv, c + (mi >> 1)), b0, b1, b2, b3);
-          mma16816<kBf>(o[c], pa0, pa1, pa2, pa3, b0, b1);
-          mma16816<kBf>(o[c + 1], pa0, pa1, pa2, pa3, b2, b3);
+          for (int c = 0; c < NT; c += 2) {
+            uint32_t b0, b1, b2, b3;
+            ldsm_x4_t(vbase + swz(rv, c + (mi >> 1)), b0, b1, b2, b3);
+            mma16816<kBf>(o[c], pa0, pa1, pa2, pa3, b0, b1);
+            mma16816<kBf>(o[c + 1], pa0, pa1, pa2, pa3, b2, b3);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < D / 16; c += 2) {
+            uint32_t w0, w1, w2, w3;  // (keys 0-7, chunk c), (8-15, c), (0-7, c + 1), (8-15, c + 1)
+            ldsm_x4_t(vbase + swz(rv, c + (mi >> 1)), w0, w1, w2, w3);
+            const uint32_t x0 = prmt(w0, 0x3120), x1 = prmt(w1, 0x3120);
+            const uint32_t x2 = prmt(w2, 0x3120), x3 = prmt(w3, 0x3120);
+            // chunk c: even head_dim index -> n-tile 2c, odd -> 2c + 1
+            mma16816<false>(o[2 * c], pa0, pa1, pa2, pa3, e4m3x2_f16x2(x0 & 0xffffu),
+                            e4m3x2_f16x2(x1 & 0xffffu));
+            mma16816<false>(o[2 * c + 1], pa0, pa1, pa2, pa3, e4m3x2_f16x2(x0 >> 16),
+                            e4m3x2_f16x2(x1 >> 16));
+            mma16816<false>(o[2 * c + 2], pa0, pa1, pa2, pa3, e4m3x2_f16x2(x2 & 0xffffu),
+                            e4m3x2_f16x2(x3 & 0xffffu));
+            mma16816<false>(o[2 * c + 3], pa0, pa1, pa2, pa3, e4m3x2_f16x2(x2 >> 16),
+                            e4m3x2_f16x2(x3 >> 16));
+          }
         }
       }
     }
@@ -292,14 +337,27 @@ __global__ void __launch_bounds__(kThreads, 2)
     L += __shfl_xor_sync(FULL, L, 1);
     L += __shfl_xor_sync(FULL, L, 2);
     if (!warp_any || !rvalid[h]) continue;
-    const float inv = (L > 0.f || L != L) ? 1.f / L : 0.f;
+    const float inv = (L > 0.f || L != L) ? a.v_scale / L : 0.f;
     raw* orow = static_cast<raw*>(a.out) +
                 (static_cast<size_t>(q0 + wr0 + g + 8 * h) * HQ + j) * D;
+    if constexpr (!kFp8) {
 #pragma unroll
-    for (int c = 0; c < NT; ++c) {
-      const float x0 = any_bad ? CUDART_NAN_F : o[c][2 * h] * inv;
-      const float x1 = any_bad ? CUDART_NAN_F : o[c][2 * h + 1] * inv;
-      *reinterpret_cast<uint32_t*>(orow + 8 * c + 2 * q4) = pack2<kBf>(x0, x1);
+      for (int c = 0; c < NT; ++c) {
+        const float x0 = any_bad ? CUDART_NAN_F : o[c][2 * h] * inv;
+        const float x1 = any_bad ? CUDART_NAN_F : o[c][2 * h + 1] * inv;
+        *reinterpret_cast<uint32_t*>(orow + 8 * c + 2 * q4) = pack2<kOutBf>(x0, x1);
+      }
+    } else {
+      // n-tile n holds head_dim 16 (n / 2) + 4 q4 + 2 jj + (n % 2): the two
+      // n-tiles of a pair give adjacent columns
+#pragma unroll
+      for (int c = 0; c < NT; c += 2)
+#pragma unroll
+        for (int jj = 0; jj < 2; ++jj) {
+          const float x0 = any_bad ? CUDART_NAN_F : o[c][2 * h + jj] * inv;
+          const float x1 = any_bad ? CUDART_NAN_F : o[c + 1][2 * h + jj] * inv;
+          *reinterpret_cast<uint32_t*>(orow + 16 * (c / 2) + 4 * q4 + 2 * jj) = pack2<kOutBf>(x0, x1);
+        }
     }
   }
 }
@@ -309,12 +367,12 @@ constexpr int prefill_smem_bytes() {
   return 1024 + NS * Geom<KV, D>::kStageBytes + NS * 8;
 }
 
-template <typename KV, int D, int T>
+template <typename KV, typename Q, int D, int T>
 pkv_status launch_prefill_dt(const PrefillArgs& a, const CUtensorMap& kmap,
                              const CUtensorMap& vmap, cudaStream_t st) {
   constexpr int NS = Geom<KV, D>::kStageBytes >= 32768 ? 2 : 4;  // 64 KiB ring
   constexpr int smem = prefill_smem_bytes<KV, D, NS>();
-  auto kernel = prefill_tc_kernel<KV, D, T, NS>;
+  auto kernel = prefill_tc_kernel<KV, Q, D, T, NS>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
@@ -340,13 +398,15 @@ pkv_status launch_prefill_dt(const PrefillArgs& a, const CUtensorMap& kmap,
   return check_launch("pkv_attention_prefill");
 }
 
-template <typename KV>
+template <typename KV, typename Q>
 pkv_status launch_prefill(const PrefillArgs& a, int D, int T, const CUtensorMap& kmap,
                           const CUtensorMap& vmap, cudaStream_t st) {
-  if (D == 128 && T == 16) return launch_prefill_dt<KV, 128, 16>(a, kmap, vmap, st);
-  if (D == 128 && T == 32) return launch_prefill_dt<KV, 128, 32>(a, kmap, vmap, st);
-  if (D == 64 && T == 16) return launch_prefill_dt<KV, 64, 16>(a, kmap, vmap, st);
-  if (D == 64 && T == 32) return launch_prefill_dt<KV, 64, 32>(a, kmap, vmap, st);
+  if (D == 128 && T == 16) return launch_prefill_dt<KV, Q, 128, 16>(a, kmap, vmap, st);
+  if (D == 128 && T == 32) return launch_prefill_dt<KV, Q, 128, 32>(a, kmap, vmap, st);
+  if constexpr (!std::is_same<KV, E4M3>::value) {
+    if (D == 64 && T == 16) return launch_prefill_dt<KV, Q, 64, 16>(a, kmap, vmap, st);
+    if (D == 64 && T == 32) return launch_prefill_dt<KV, Q, 64, 32>(a, kmap, vmap, st);
+  }
   return fail(PKV_ERR_UNSUPPORTED, "pkv_attention_prefill: head_dim/block_size not compiled");
 }
 
@@ -364,8 +424,6 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
                                             int32_t num_q_heads, const pkv_kv_desc* desc,
                                             float softmax_scale, float k_scale, float v_scale,
                                             void* stream) {
-  (void)k_scale;
-  (void)v_scale;
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || total_q < 0 || max_query_len < 0 || num_q_heads <= 0 || max_blocks < 0)
@@ -388,8 +446,10 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
     return fail(PKV_ERR_UNSUPPORTED, "pool larger than 2^31 rows");
   if (!(softmax_scale == softmax_scale)) return fail(PKV_ERR_INVALID_ARG, "softmax_scale is NaN");
   const int kv = desc->kv_dtype;
-  if (!((kv == PKV_BF16 && q_dtype == PKV_BF16) || (kv == PKV_F16 && q_dtype == PKV_F16)))
-    return fail(PKV_ERR_UNSUPPORTED, "pkv_attention_prefill: 16-bit caches with the same q dtype only");
+  if (!((kv == PKV_BF16 && q_dtype == PKV_BF16) || (kv == PKV_F16 && q_dtype == PKV_F16) ||
+        (kv == PKV_E4M3 && (q_dtype == PKV_F16 || q_dtype == PKV_BF16))))
+    return fail(PKV_ERR_UNSUPPORTED,
+                "pkv_attention_prefill: 16-bit caches with the same q dtype, or E4M3 with f16/bf16 q");
   const int64_t q_tiles = (static_cast<int64_t>(max_query_len) + 63) / 64;
   if (q_tiles > 65535) return fail(PKV_ERR_UNSUPPORTED, "max_query_len too large");
 
@@ -407,14 +467,18 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
   a.num_kv_heads = desc->num_kv_heads;
   a.group = num_q_heads / desc->num_kv_heads;
   a.num_blocks = desc->num_blocks;
-  a.qk_scale = softmax_scale * 1.4426950408889634f;
+  const bool fp8 = kv == PKV_E4M3;
+  a.qk_scale = softmax_scale * (fp8 ? k_scale : 1.0f) * 1.4426950408889634f;
+  a.v_scale = fp8 ? v_scale : 1.0f;
 
   CUtensorMap kmap, vmap;
   st = pool_map(&kmap, k_cache, desc);
   if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc);
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  return kv == PKV_BF16
-             ? tc::launch_prefill<BF16>(a, desc->head_dim, desc->block_size, kmap, vmap, s)
-             : tc::launch_prefill<F16>(a, desc->head_dim, desc->block_size, kmap, vmap, s);
+  const int D = desc->head_dim, T = desc->block_size;
+  if (kv == PKV_BF16) return tc::launch_prefill<BF16, BF16>(a, D, T, kmap, vmap, s);
+  if (kv == PKV_F16) return tc::launch_prefill<F16, F16>(a, D, T, kmap, vmap, s);
+  return q_dtype == PKV_F16 ? tc::launch_prefill<E4M3, F16>(a, D, T, kmap, vmap, s)
+                            : tc::launch_prefill<E4M3, BF16>(a, D, T, kmap, vmap, s);
 }

@@ -19,7 +19,7 @@ from paged_kv_cache_137_gb300 import scenario as PS
 
 pytestmark = pytest.mark.gpu
 
-TOL = (2e-2, 2e-3)
+TOL = {"bf16": (2e-2, 2e-3), "f16": (2e-2, 2e-3), "e4m3": (6e-2, None)}
 
 CASES = {
     "qwen_small": W.scaled(W.get("qwen_gqa_bf16"), num_seqs=8, num_blocks=600, ctx_range=(1, 1000)),
@@ -29,7 +29,13 @@ CASES = {
                         num_blocks=200, ctx_range=(300, 1500), seed=94),
     "gqa16_d64": W.scaled(W.get("qwen_gqa_bf16"), num_seqs=5, num_q_heads=32, num_kv_heads=2,
                           head_dim=64, num_blocks=300, ctx_range=(1, 800), block_size=32, seed=93),
+    "fp8_small": W.scaled(W.get("fp8_churn"), num_seqs=6, num_blocks=1024, churn=300,
+                          ctx_range=(1, 900)),
 }
+
+
+def scales_for(w):
+    return W.fp8_scales(*W.kv_amax(w)) if w.kv_dtype == "e4m3" else {}
 
 
 @pytest.fixture(scope="module", autouse=True)
@@ -45,11 +51,12 @@ def state(name):
     """(device scenario, oracle scenario) of a case, built once."""
     if name not in _STATE:
         w = CASES[name]
-        dev = PS.materialize(PS.plan(w), "cuda")
+        sc = scales_for(w)
+        dev = PS.materialize(PS.plan(w), "cuda", sc)
         dev.copy_blocks()
         dev.write_step()
         torch.cuda.synchronize()
-        _STATE[name] = (dev, OS.build(w))
+        _STATE[name] = (dev, OS.build(w, scales=sc))
     return _STATE[name]
 
 
@@ -68,7 +75,8 @@ def run_prefill(dev, q, qs, ctx=None, max_query_len=None):
     ctx_t = dev.ctx if ctx is None else torch.from_numpy(np.asarray(ctx, dtype=np.int32)).cuda()
     pkv.pkv_attention_prefill(out, qd, dev.k_cache, dev.v_cache, dev.tables, ctx_t,
                               torch.from_numpy(qs).cuda(), dev.desc, 1.0 / math.sqrt(w.head_dim),
-                              max_query_len=max_query_len)
+                              max_query_len=max_query_len, k_scale=dev.scales.get("k_scale", 1.0),
+                              v_scale=dev.scales.get("v_scale", 1.0))
     torch.cuda.synchronize()
     return out
 
@@ -76,15 +84,18 @@ def run_prefill(dev, q, qs, ctx=None, max_query_len=None):
 def oracle(scn, q, qs, ctx=None):
     return OP.paged_attention_prefill(q.double().numpy(), scn.pool, scn.tables,
                                       scn.ctx if ctx is None else ctx, qs,
-                                      1.0 / math.sqrt(scn.w.head_dim))
+                                      1.0 / math.sqrt(scn.w.head_dim),
+                                      scn.scales.get("k_scale", 1.0), scn.scales.get("v_scale", 1.0))
 
 
-def check(got, ref):
+def check(got, ref, kv_dtype="bf16"):
     g = got.double().cpu().numpy()
     assert not np.isnan(g).any(), "NaN in the GPU output"
     err = np.abs(g - ref)
-    assert err.max() <= TOL[0], f"max abs error {err.max():.3g}"
-    assert err.mean() <= TOL[1], f"mean abs error {err.mean():.3g}"
+    max_tol, mean_tol = TOL[kv_dtype]
+    assert err.max() <= max_tol, f"max abs error {err.max():.3g}"
+    if mean_tol is not None:
+        assert err.mean() <= mean_tol, f"mean abs error {err.mean():.3g}"
 
 
 @pytest.mark.parametrize("name", list(CASES))
@@ -93,10 +104,10 @@ def test_prefill_matches_oracle(name, chunk):
     dev, scn = state(name)
     n = W.chunk_lens(dev.plan.w, dev.plan.ctx, chunk)
     q, qs = chunk_inputs(dev, n)
-    check(run_prefill(dev, q, qs), oracle(scn, q, qs))
+    check(run_prefill(dev, q, qs), oracle(scn, q, qs), dev.plan.w.kv_dtype)
 
 
-@pytest.mark.parametrize("name", ["qwen_small", "gqa16_d64"])
+@pytest.mark.parametrize("name", ["qwen_small", "gqa16_d64", "fp8_small"])
 def test_one_token_chunks_match_decode_kernel(name):
     """A one-token chunk with the decode query is decode attention."""
     dev, _ = state(name)
@@ -105,7 +116,7 @@ def test_one_token_chunks_match_decode_kernel(name):
     dec = dev.attend().clone()
     torch.cuda.synchronize()
     err = (pre.double() - dec.double()).abs()
-    assert err.max().item() <= TOL[0]
+    assert err.max().item() <= TOL[dev.plan.w.kv_dtype][0]
 
 
 def test_empty_chunks_and_whole_prompts_mixed():
@@ -130,7 +141,7 @@ def test_invalid_chunk_gives_nan_rows_and_leaves_others():
     keep = np.ones(len(got), dtype=bool)
     keep[qs[2]:qs[3]] = False
     ref = oracle(scn, q, qs)
-    assert np.abs(got[keep] - ref[keep]).max() <= TOL[0]
+    assert np.abs(got[keep] - ref[keep]).max() <= TOL["bf16"][0]
 
 
 def test_physical_blocks_do_not_change_the_output():
@@ -152,10 +163,10 @@ def test_physical_blocks_do_not_change_the_output():
 
 
 def test_unsupported_cache_is_rejected():
-    w = W.scaled(W.get("fp8_churn"), num_seqs=2, num_blocks=64, churn=0, ctx_range=(1, 100))
-    desc = pkv.kv_desc(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, "e4m3")
+    w = W.get("tiny_fp32")
+    desc = pkv.kv_desc(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, "f32")
     kc, vc = pkv.empty_cache(desc, "cuda")
-    q = torch.zeros(3, w.num_q_heads, w.head_dim, dtype=torch.bfloat16, device="cuda")
+    q = torch.zeros(3, w.num_q_heads, w.head_dim, dtype=torch.float32, device="cuda")
     with pytest.raises(pkv.PkvError):
         pkv.pkv_attention_prefill(torch.empty_like(q), q, kc, vc,
                                   torch.zeros(2, 8, dtype=torch.int32, device="cuda"),
