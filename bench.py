@@ -49,6 +49,10 @@ def parse():
                     help="split-K partition in tokens (default: the workload's, else automatic)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc", "persistent"],
                     help="decode kernel (auto = tensor-core where it applies)")
+    ap.add_argument("--block-size", type=int, default=None,
+                    help="ablation: tokens per block (the pool keeps the same token capacity)")
+    ap.add_argument("--kv-dtype", default=None, choices=["bf16", "f16", "e4m3"],
+                    help="ablation: cache dtype (q stays 16-bit)")
     return ap.parse_args()
 
 
@@ -65,6 +69,22 @@ def kernel_source_hash() -> str:
     for n in KERNEL_SOURCES:
         h.update(open(os.path.join(ROOT, "paged_kv_cache_137_gb300", "csrc", n), "rb").read())
     return h.hexdigest()[:16]
+
+
+def workload_of(args):
+    """The configured workload, with the ablation overrides applied: another
+    block size keeps the pool's token capacity (plus one block per sequence,
+    so that the same context lengths are drawn), another cache dtype keeps
+    the shapes."""
+    import workloads as W
+    w = W.get(args.config)
+    if args.block_size and args.block_size != w.block_size:
+        nb = -(-w.num_blocks * w.block_size // args.block_size) + w.num_seqs
+        w = W.scaled(w, block_size=args.block_size, num_blocks=nb)
+    if args.kv_dtype and args.kv_dtype != w.kv_dtype:
+        q = w.q_dtype if args.kv_dtype == "e4m3" else args.kv_dtype
+        w = W.scaled(w, kv_dtype=args.kv_dtype, q_dtype="bf16" if q == "f32" else q)
+    return w
 
 
 def attention_kernels(kernel: str, w, splits: int) -> str:
@@ -247,7 +267,7 @@ def run_gpu(args, world, rank, local):
     pkv.pkv_set_attention_kernel(args.kernel)
     torch.cuda.set_device(local)
     dev_name = f"cuda:{local}"
-    w = W.get(args.config)
+    w = workload_of(args)
     sc = W.fp8_scales(*W.kv_amax(w)) if w.kv_dtype == "e4m3" else {}
     scn = PS.materialize(PS.plan(w), dev_name, sc, partition_tokens=args.partition)
     stream = torch.cuda.current_stream()
@@ -388,7 +408,8 @@ def run_gpu(args, world, rank, local):
 
     peak, peak_kind = peaks()
     kernels = attention_kernels(args.kernel, w, splits)
-    traffic = traffic_for(args.config, kernels)
+    # the profiled counters describe the configured workload only
+    traffic = traffic_for(args.config, kernels) if w == W.get(args.config) else None
     achieved = kv_bytes / (attn / 1e3) / 1e9
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
@@ -399,6 +420,9 @@ def run_gpu(args, world, rank, local):
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
                    "num_blocks": w.num_blocks, "context_tokens": int(scn.plan.ctx.sum()),
                    "kv_bytes_per_step": kv_bytes, "partition_tokens": scn.partition,
+                   "kv_dtype": w.kv_dtype, "table_entries": int(np.ceil(scn.plan.ctx / w.block_size).sum()),
+                   "waste_slots_per_seq": round(float((np.ceil(scn.plan.ctx / w.block_size) * w.block_size
+                                                       - scn.plan.ctx).mean()), 2),
                    "l2": ("inputs larger than L2 (K/V %d MB vs %d MB L2), no flush between steps"
                           % (kv_bytes >> 20, props.L2_cache_size >> 20)),
                    "launch": "the K steps captured back to back in one CUDA graph, replayed once",
