@@ -71,6 +71,25 @@ def kernel_source_hash() -> str:
     return h.hexdigest()[:16]
 
 
+def allocator_step_us(plan, steps: int = 200) -> float:
+    """Host time of one decode step of the native allocator for the plan's
+    batch: pkv_batch_append of one token per sequence, then pkv_block_tables
+    for the whole batch (a fresh pool replaying the plan's prefill)."""
+    import numpy as np
+    import paged_kv_cache_137_gb300 as pkv
+    w = plan.w
+    pool = pkv.Pool(w.num_blocks + len(plan.seq_ids) * (steps // w.block_size + 2), w.block_size)
+    for s, c in zip(plan.seq_ids, plan.ctx):
+        pool.seq_create(s)
+        pool.seq_append(s, int(c))
+    max_blocks = plan.max_blocks + steps // w.block_size + 2
+    t0 = time.perf_counter()
+    for _ in range(steps):
+        pool.batch_append(plan.seq_ids)
+        pool.block_tables(plan.seq_ids, max_blocks)
+    return (time.perf_counter() - t0) / steps * 1e6
+
+
 def workload_of(args):
     """The configured workload, with the ablation overrides applied: another
     block size keeps the pool's token capacity (plus one block per sequence,
@@ -382,6 +401,10 @@ def run_gpu(args, world, rank, local):
         block_bytes = w.num_kv_heads * w.block_size * w.head_dim * kvb
         aux["copy_blocks_us"] = round(copy_us, 2)
         aux["copy_blocks_GBs"] = round(2 * 2 * n_pairs * block_bytes / (copy_us * 1e3), 2)
+
+    # the host allocator's step (native C++): one token appended to each of the
+    # batch's sequences and their block tables exported, on a copy of the plan
+    aux["allocator_step_us"] = round(allocator_step_us(scn.plan), 2)
 
     # end to end through the C ABI from pinned host buffers
     host = {n: getattr(scn, n).cpu().pin_memory() for n in ("q", "k_new", "v_new", "tables", "ctx")}
