@@ -78,7 +78,11 @@ def allocator_step_us(plan, steps: int = 200) -> float:
     import numpy as np
     import paged_kv_cache_137_gb300 as pkv
     w = plan.w
-    pool = pkv.Pool(w.num_blocks + len(plan.seq_ids) * (steps // w.block_size + 2), w.block_size)
+    t = w.block_size
+    # private blocks for every sequence (a forked plan's shared prefix is
+    # replayed per sequence), plus room for the timed appends
+    need = sum(-(-int(c) // t) for c in plan.ctx) + len(plan.seq_ids) * (steps // t + 2)
+    pool = pkv.Pool(max(w.num_blocks, need), t)
     for s, c in zip(plan.seq_ids, plan.ctx):
         pool.seq_create(s)
         pool.seq_append(s, int(c))

@@ -13,8 +13,8 @@
 //  * One CTA (4 warps) per (64-query tile, query head, sequence); the grid
 //    column index counts tiles from the END of the chunk, so the tiles with
 //    the most keys are dispatched first.
-//  * K/V of 64-token tiles of the head's KV head are fetched as 2-D TMA boxes
-//    of T rows x 128 bytes per (block, slab, K|V) into a ring of stages, one
+//  * K/V of 64-token tiles of the head's KV head are fetched as TMA boxes of
+//    T rows (all their bytes) per (block, K|V) into a ring of stages, one
 //    lane of warp 0 per box, completion by expect-tx mbarriers; block ids
 //    are loaded one tile ahead.
 //  * Each warp owns 16 query rows and sweeps all 64 keys of every tile:
@@ -60,8 +60,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int KS = D / 16;
   constexpr int NT = D / 8;
   constexpr int BPT = kTile / T;
-  constexpr int kBoxBytes = T * 128;
-  constexpr int BPB = BPT * G_::kSlabs * 2;  // boxes per tile
+  constexpr int kBoxBytes = T * G_::kRowBytes;    // one (block, head) box: all its slabs
+  constexpr int BPB = BPT * 2;  // boxes per tile
   constexpr unsigned FULL = 0xffffffffu;
   static_assert(BPB <= 32, "one lane per box");
 
@@ -109,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
 
   // ---------------------------------------------------------- producer
-  const int bx_blk = lane / (G_::kSlabs * 2), bx_sl = (lane / 2) % G_::kSlabs, bx_v = lane & 1;
+  const int bx_blk = lane / 2, bx_v = lane & 1;
   constexpr int kNoBox = -1, kBadBox = -2;
   auto box_id = [&](int t) {
     const int lb = t * BPT + bx_blk;
@@ -128,9 +128,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncwarp();
     if (id >= 0)
-      tma_load_2d(smem_u32(ring + slot * G_::kStageBytes + (bx_v ? G_::kTileBytes : 0) +
-                           bx_sl * kHalfBytes + bx_blk * kBoxBytes),
-                  bx_v ? &vmap : &kmap, bx_sl * 128, (id * a.num_kv_heads + kvh) * T, bar);
+      tma_box<KV, D>(smem_u32(ring + slot * G_::kStageBytes + (bx_v ? G_::kTileBytes : 0) +
+                              bx_blk * kBoxBytes),
+                     bx_v ? &vmap : &kmap, (id * a.num_kv_heads + kvh) * T, bar);
   };
   int nid = kNoBox;
   if (warp == 0) {
@@ -201,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int nz = (kTile - z0) * G_::kSlabs * 8;
       for (int i = tid; i < nz; i += kThreads) {
         const int r = z0 + i / (G_::kSlabs * 8), c = i % (G_::kSlabs * 8);
-        *reinterpret_cast<uint4*>(vt + swz(r, c)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vt + swz<G_::kSlabs>(r, c)) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async();  // before the slot is refilled by TMA
       __syncthreads();
@@ -218,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int ks = 0; ks < KS; ks += 2) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + swz(r, 2 * ks + mi), b0, b1, b2, b3);
+            ldsm_x4(kbase + swz<G_::kSlabs>(r, 2 * ks + mi), b0, b1, b2, b3);
             mma16816<kBf>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
             mma16816<kBf>(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
           }
@@ -226,7 +226,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int c0 = 0; c0 < KS; c0 += 4) {
             uint32_t w[4];
-            ldsm_x4(kbase + swz(r, c0 + mi), w[0], w[1], w[2], w[3]);
+            ldsm_x4(kbase + swz<G_::kSlabs>(r, c0 + mi), w[0], w[1], w[2], w[3]);
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
               const int ks = c0 + jj;
@@ -286,7 +286,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int c = 0; c < NT; c += 2) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vbase + swz(rv, c + (mi >> 1)), b0, b1, b2, b3);
+            ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, c + (mi >> 1)), b0, b1, b2, b3);
             mma16816<kBf>(o[c], pa0, pa1, pa2, pa3, b0, b1);
             mma16816<kBf>(o[c + 1], pa0, pa1, pa2, pa3, b2, b3);
           }
@@ -294,7 +294,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int c = 0; c < D / 16; c += 2) {
             uint32_t w0, w1, w2, w3;  // (keys 0-7, chunk c), (8-15, c), (0-7, c + 1), (8-15, c + 1)
-            ldsm_x4_t(vbase + swz(rv, c + (mi >> 1)), w0, w1, w2, w3);
+            ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, c + (mi >> 1)), w0, w1, w2, w3);
             const uint32_t x0 = prmt(w0, 0x3120), x1 = prmt(w1, 0x3120);
             const uint32_t x2 = prmt(w2, 0x3120), x3 = prmt(w3, 0x3120);
             // chunk c: even head_dim index -> n-tile 2c, odd -> 2c + 1

@@ -12,7 +12,7 @@
 //    tiles whatever the length mix, and no CTA waits for another.
 //  * Inside a CTA the pipeline is the split kernel's: four warps, a 64 KiB
 //    ring of 2 (16-bit, head_dim 128) or 4 stages of one tile's K and V,
-//    fetched as one 2-D TMA box of T rows x 128 bytes per (block, slab, K|V)
+//    fetched as one TMA box of T rows (all their bytes) per (block, K|V)
 //    by the lanes of warp 0, which refills a stage as soon as the four warps
 //    have consumed it.  The block ids of the next tile are loaded one tile
 //    ahead, so table reads never sit between a free stage and its refill.
@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
   constexpr int KS = D / 16;
   constexpr int NT = D / 8;
   constexpr int BPT = kTile / T;                 // blocks per tile
-  constexpr int kBoxBytes = T * 128;
-  constexpr int BPB = BPT * G_::kSlabs * 2;      // boxes per tile
+  constexpr int kBoxBytes = T * G_::kRowBytes;    // one (block, head) box: all its slabs
+  constexpr int BPB = BPT * 2;                   // boxes per tile
   constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
   constexpr unsigned FULL = 0xffffffffu;
   static_assert(NS >= 2 && NS * G_::kStageBytes == kStreamRingBytes, "ring of whole stages");
@@ -193,12 +193,12 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
   };
 
   // ---------------------------------------------------------- producer side
-  // Lane l < BPB of warp 0 fetches box l of a tile: block l / (2 * slabs),
-  // slab (l / 2) % slabs, K (even l) or V (odd l).  The block ids of tile t
+  // Lane l < BPB of warp 0 fetches box l of a tile: block l / 2, K (even l)
+  // or V (odd l), each box all slabs of the block's T rows of one head.  The block ids of tile t
   // come from s_ids[t % NS], filled by an asynchronous copy (cp.async) issued
   // when tile t - NS was issued, a whole ring ahead, so a table read never
   // sits between a freed stage and its refill.
-  const int bx_blk = lane / (G_::kSlabs * 2), bx_sl = (lane / 2) % G_::kSlabs, bx_v = lane & 1;
+  const int bx_blk = lane / 2, bx_v = lane & 1;
   constexpr int kNoBox = -1, kBadBox = -2;
   auto box_lb = [&](const StreamCursor& r) {  // logical block of this lane's box, or -1
     const int lb = r.j * BPT + bx_blk;
@@ -224,9 +224,9 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
     }
     __syncwarp();
     if (id >= 0)
-      tma_load_2d(smem_u32(ring + slot * G_::kStageBytes + (bx_v ? G_::kTileBytes : 0) +
-                           bx_sl * kHalfBytes + bx_blk * kBoxBytes),
-                  bx_v ? &vmap : &kmap, bx_sl * 128, (id * NKV + r.h) * T, bar);
+      tma_box<KV, D>(smem_u32(ring + slot * G_::kStageBytes + (bx_v ? G_::kTileBytes : 0) +
+                              bx_blk * kBoxBytes),
+                     bx_v ? &vmap : &kmap, (id * NKV + r.h) * T, bar);
   };
 
   StreamCursor icur = cur;  // warp 0: the next tile to issue

@@ -9,10 +9,11 @@
 // How, on GB300:
 //  * One CTA (4 warps) per (split, KV head, sequence).  The split's block ids
 //    are read once into shared memory.  Thread 0 feeds a ring of NS stages:
-//    each stage is a 64-token tile of K and of V, fetched as one 2-D TMA box
-//    of T rows x 128 bytes per (block, 128-byte column slab) at row
-//    (block * N_kv + head) * T of the pool viewed as [rows][row_bytes], with
-//    the hardware 128-byte swizzle so that ldmatrix reads are conflict-free.
+//    each stage is a 64-token tile of K and of V, fetched as one TMA box per
+//    block: its T rows of the head, at row (block * N_kv + head) * T of the
+//    pool viewed as [rows][row_bytes] (a 3-D (128 bytes, slab, row) view for
+//    256-byte rows, so one box carries both slabs), with the hardware 128-byte
+//    swizzle so that ldmatrix reads are conflict-free.
 //    Completion is tracked by one mbarrier per stage (expect-tx bytes).
 //  * Each warp owns 16 tokens of a tile.  q . K^T is an m16n8k16 MMA with the
 //    (up to 16) query heads of the group as the M rows, so each K element is
@@ -46,7 +47,6 @@ namespace tc {
 constexpr int kWarps = 4;
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 64;                 // tokens per stage, 16 per warp
-constexpr int kHalfBytes = kTile * 128;   // one 128-byte column slab of a tile
 constexpr int kMaxTableEntries = 1024;    // block ids of one split kept in shared memory
 constexpr uint64_t kWaitNs = 50000000ull;  // a stage wait gives up after 50 ms
 constexpr uint64_t kDrainNs = 10000000ull; // after a give-up, 10 ms per copy in flight
@@ -55,8 +55,8 @@ template <typename KV, int D>
 struct Geom {
   static constexpr int kElemBytes = KV::bytes;
   static constexpr int kRowBytes = D * kElemBytes;
-  static constexpr int kSlabs = kRowBytes / 128;  // 128-byte column slabs per row
-  static constexpr int kTileBytes = kSlabs * kHalfBytes;
+  static constexpr int kSlabs = kRowBytes / 128;  // 128-byte column slabs per row (1 or 2)
+  static constexpr int kTileBytes = kTile * kRowBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K and V
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte slabs");
 };
@@ -106,6 +106,15 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
 
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
 }
 
 __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map, int x, int y,
@@ -172,10 +181,23 @@ __device__ __forceinline__ uint32_t pack2(float lo, float hi) {
   }
 }
 
-// Byte offset of 16-byte chunk c of tile row r under the 128-byte swizzle
-// (the tile base is 1024-byte aligned; chunk c lives in slab c / 8).
+// Byte offset of 16-byte chunk c of tile row r under the 128-byte swizzle.
+// A tile stores its rows back to back, each as S 128-byte lines (one per
+// 128-byte slab of the row, the order a TMA box over (bytes, slab, row)
+// writes them), and the swizzle XORs a chunk's index with its line's index
+// mod 8 (the tile base is 1024-byte aligned).
+template <int S>
 __device__ __forceinline__ uint32_t swz(int r, int c) {
-  return static_cast<uint32_t>((c >> 3) * kHalfBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+  const int line = r * S + (c >> 3);
+  return static_cast<uint32_t>((line << 7) + (((c & 7) ^ (line & 7)) << 4));
+}
+
+// One TMA box of a (block, KV head): its T rows, all slabs of each row (a 2-D
+// map for 128-byte rows, a 3-D (bytes, slab, row) map for 256-byte rows).
+template <typename KV, int D>
+__device__ __forceinline__ void tma_box(uint32_t dst, const CUtensorMap* map, int row, uint32_t bar) {
+  if constexpr (Geom<KV, D>::kSlabs == 1) tma_load_2d(dst, map, 0, row, bar);
+  else tma_load_3d(dst, map, 0, 0, row, bar);
 }
 
 // ------------------------------------------------------- tile building blocks
@@ -250,7 +272,7 @@ __device__ __forceinline__ bool tile_step(WarpState<D>& st, const uint32_t (&qa)
     for (int i = lane; i < nz; i += 32) {
       const int r = row0 + nvalid + i / (G_::kSlabs * 8);
       const int c = i % (G_::kSlabs * 8);
-      *reinterpret_cast<uint4*>(vt + swz(r, c)) = make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(vt + swz<G_::kSlabs>(r, c)) = make_uint4(0, 0, 0, 0);
     }
     __syncwarp();
     zeroed = true;
@@ -268,7 +290,7 @@ __device__ __forceinline__ bool tile_step(WarpState<D>& st, const uint32_t (&qa)
 #pragma unroll
       for (int ks = 0; ks < KS; ks += 2) {
         uint32_t b0, b1, b2, b3;
-        ldsm_x4(kbase + swz(r, 2 * ks + mi), b0, b1, b2, b3);
+        ldsm_x4(kbase + swz<G_::kSlabs>(r, 2 * ks + mi), b0, b1, b2, b3);
         mma16816<kBf>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
         mma16816<kBf>(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
       }
@@ -276,7 +298,7 @@ __device__ __forceinline__ bool tile_step(WarpState<D>& st, const uint32_t (&qa)
 #pragma unroll
       for (int c0 = 0; c0 < KS; c0 += 4) {
         uint32_t w[4];
-        ldsm_x4(kbase + swz(r, c0 + mi), w[0], w[1], w[2], w[3]);
+        ldsm_x4(kbase + swz<G_::kSlabs>(r, c0 + mi), w[0], w[1], w[2], w[3]);
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
           const int ks = c0 + j;
@@ -337,7 +359,7 @@ __device__ __forceinline__ bool tile_step(WarpState<D>& st, const uint32_t (&qa)
 #pragma unroll
     for (int c = 0; c < NT; c += 2) {
       uint32_t b0, b1, b2, b3;
-      ldsm_x4_t(vbase + swz(rv, c + (mi >> 1)), b0, b1, b2, b3);
+      ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, c + (mi >> 1)), b0, b1, b2, b3);
       mma16816<kBf>(st.o[c], pa0, pa1, pa2, pa3, b0, b1);
       mma16816<kBf>(st.o[c + 1], pa0, pa1, pa2, pa3, b2, b3);
     }
@@ -345,7 +367,7 @@ __device__ __forceinline__ bool tile_step(WarpState<D>& st, const uint32_t (&qa)
 #pragma unroll
     for (int c = 0; c < D / 16; c += 2) {
       uint32_t w0, w1, w2, w3;  // (tok 0-7, c), (tok 8-15, c), (0-7, c+1), (8-15, c+1)
-      ldsm_x4_t(vbase + swz(rv, c + (mi >> 1)), w0, w1, w2, w3);
+      ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, c + (mi >> 1)), w0, w1, w2, w3);
       const uint32_t x0 = prmt(w0, 0x3120), x1 = prmt(w1, 0x3120);
       const uint32_t x2 = prmt(w2, 0x3120), x3 = prmt(w3, 0x3120);
       // chunk c: even d -> n-tile 2c, odd d -> 2c + 1
@@ -492,7 +514,7 @@ __global__ void __launch_bounds__(kThreads, 3)
   using G_ = Geom<KV, D>;
   constexpr int KS = D / 16;        // k-steps of q . K^T
   constexpr int BPT = kTile / T;    // blocks per tile
-  constexpr int kBoxBytes = T * 128;
+  constexpr int kBoxBytes = T * G_::kRowBytes;  // one (block, head) box: all its slabs
   static_assert(kTile % T == 0, "a tile holds whole blocks");
 
   // split-major grid: every pair's first split is dispatched before any
@@ -563,15 +585,15 @@ __global__ void __launch_bounds__(kThreads, 3)
 
   // ---------------------------------------------------------- producer
   // Warp 0 refills a stage with one warp instruction: lane l issues box l
-  // (block l / (2 * slabs), slab, K|V), which starts the tile's boxes
-  // together instead of one after another from a single thread.
-  constexpr int BPB = BPT * G_::kSlabs * 2;  // boxes per tile
+  // (block l / 2, K|V), which starts the tile's boxes together instead of one
+  // after another from a single thread.
+  constexpr int BPB = BPT * 2;  // boxes per tile
   static_assert(BPB <= 32, "one lane per box");
   auto issue = [&](int tile) {
     const int s = tile % NS;
     uint8_t* kt = stages + s * G_::kStageBytes;
     const int lb0 = (tile * kTile) / T;  // first logical block of the tile within the split
-    const int blk = lane / (G_::kSlabs * 2), sl = (lane / 2) % G_::kSlabs, isv = lane & 1;
+    const int blk = lane / 2, isv = lane & 1;
     int phys = -1;
     bool inb = false;
     if (lane < BPB && lb0 + blk < n_blk) {
@@ -588,8 +610,8 @@ __global__ void __launch_bounds__(kThreads, 3)
     }
     __syncwarp();
     if (good)
-      tma_load_2d(smem_u32(kt + (isv ? G_::kTileBytes : 0) + sl * kHalfBytes + blk * kBoxBytes),
-                  isv ? &vmap : &kmap, sl * 128, (phys * a.num_kv_heads + kvh) * T, bar);
+      tma_box<KV, D>(smem_u32(kt + (isv ? G_::kTileBytes : 0) + blk * kBoxBytes), isv ? &vmap : &kmap,
+                     (phys * a.num_kv_heads + kvh) * T, bar);
   };
   if (warp == 0)
     for (int t = 0; t < NS && t < n_tiles; ++t) issue(t);
