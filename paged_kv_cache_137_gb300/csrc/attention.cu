@@ -217,17 +217,18 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// The pool as a byte tensor of num_blocks * N_kv * T rows: [rows][row_bytes]
-// for 128-byte rows, [rows][2 slabs][128 bytes] for 256-byte rows, read in
-// boxes of T whole rows with the 128-byte swizzle.
-pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d) {
+// The pool as a byte tensor of num_blocks * N_kv * T rows, read with the
+// 128-byte swizzle: [rows][row_bytes] in boxes of T rows x 128 bytes (one
+// slab), or, for 256-byte rows and whole_rows, [rows][2 slabs][128 bytes] in
+// boxes of T whole rows.
+pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d, bool whole_rows) {
   auto fn = encode_fn();
   if (!fn) return fail(PKV_ERR_CUDA, "cuTensorMapEncodeTiled is unavailable");
   const cuuint64_t row_bytes = static_cast<cuuint64_t>(d->head_dim) * pkv_dtype_bytes(d->kv_dtype);
   const cuuint64_t rows = static_cast<cuuint64_t>(d->num_blocks) * d->num_kv_heads * d->block_size;
   const cuuint32_t t = static_cast<cuuint32_t>(d->block_size);
   CUresult r;
-  if (row_bytes == 256) {
+  if (row_bytes == 256 && whole_rows) {
     // (128 bytes, slab, row): one box carries both 128-byte slabs of T rows
     const cuuint64_t dims[3] = {128, 2, rows};
     const cuuint64_t strides[2] = {128, row_bytes};
@@ -239,7 +240,7 @@ pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d) {
   } else {
     const cuuint64_t dims[2] = {row_bytes, rows};
     const cuuint64_t strides[1] = {row_bytes};
-    const cuuint32_t box[2] = {static_cast<cuuint32_t>(row_bytes), t};
+    const cuuint32_t box[2] = {128, t};
     const cuuint32_t estr[2] = {1, 1};
     r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 2, const_cast<void*>(base), dims, strides, box, estr,
            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,

@@ -49,10 +49,11 @@ size_t attention_counter_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t ma
                                const pkv_kv_desc* desc, int32_t partition_tokens);
 
 // TMA tensor map of one pool tensor viewed as bytes [num_blocks * N_kv * T
-// rows][D * P_kv] (a 3-D (128 bytes, slab, row) view for 256-byte rows), read
-// in boxes of T whole rows with the 128-byte swizzle (defined in
-// attention.cu, shared by the decode and prefill paths).
-pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d);
+// rows][D * P_kv], read with the 128-byte swizzle in boxes of T rows: whole
+// rows (a 3-D (128 bytes, slab, row) view for 256-byte rows; the decode
+// kernels) or one 128-byte slab per box (whole_rows false; prefill).
+// Defined in attention.cu.
+pkv_status pool_map(CUtensorMap* map, const void* base, const pkv_kv_desc* d, bool whole_rows = true);
 
 // Write the step's K/V row of each sequence at logical position ctx - 1
 // through its block table (a small kernel; defined in write_copy.cu).

@@ -13,10 +13,14 @@
 //  * One CTA (4 warps) per (64-query tile, query head, sequence); the grid
 //    column index counts tiles from the END of the chunk, so the tiles with
 //    the most keys are dispatched first.
-//  * K/V of 64-token tiles of the head's KV head are fetched as TMA boxes of
-//    T rows (all their bytes) per (block, K|V) into a ring of stages, one
+//  * K/V of 64-token tiles of the head's KV head are fetched as 2-D TMA boxes
+//    of T rows x 128 bytes per (block, slab, K|V) into a ring of stages, one
 //    lane of warp 0 per box, completion by expect-tx mbarriers; block ids
-//    are loaded one tile ahead.
+//    are loaded one tile ahead.  A tile keeps its 128-byte slabs apart, so
+//    the 8 rows an ldmatrix reads sit on 8 distinct swizzle phases (with
+//    whole 256-byte rows back to back, rows r and r + 4 would share one and
+//    every K and V fragment load would take two bank passes; the tile is
+//    read 64 times, so that matters here, unlike in decode).
 //  * Each warp owns 16 query rows and sweeps all 64 keys of every tile:
 //    S = Q K^T by mma.sync m16n8k16 (8 key n-tiles), positions after the
 //    row's query masked to -inf, online softmax in the log2 domain on the
@@ -35,6 +39,19 @@
 
 namespace pkv {
 namespace tc {
+namespace {
+
+constexpr int kSlabBytes = kTile * 128;   // one 128-byte column slab of a tile
+
+// Byte offset of 16-byte chunk c of tile row r: slab c / 8, then the row's
+// 128-byte line, the chunk index XORed with the row index mod 8 (the
+// 128-byte swizzle of a box of 128-byte rows; the tile base is 1024-byte
+// aligned).
+__device__ __forceinline__ uint32_t swz_slab(int r, int c) {
+  return static_cast<uint32_t>((c >> 3) * kSlabBytes + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+}
+
+}  // namespace
 
 struct PrefillArgs {
   void* out;                  // [total_q][Hq][D]
@@ -60,8 +77,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   constexpr int KS = D / 16;
   constexpr int NT = D / 8;
   constexpr int BPT = kTile / T;
-  constexpr int kBoxBytes = T * G_::kRowBytes;    // one (block, head) box: all its slabs
-  constexpr int BPB = BPT * 2;  // boxes per tile
+  constexpr int kBoxBytes = T * 128;              // one (block, slab) box
+  constexpr int BPB = BPT * G_::kSlabs * 2;      // boxes per tile
   constexpr unsigned FULL = 0xffffffffu;
   static_assert(BPB <= 32, "one lane per box");
 
@@ -109,7 +126,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   __syncthreads();
 
   // ---------------------------------------------------------- producer
-  const int bx_blk = lane / 2, bx_v = lane & 1;
+  const int bx_blk = lane / (G_::kSlabs * 2), bx_sl = (lane / 2) % G_::kSlabs, bx_v = lane & 1;
   constexpr int kNoBox = -1, kBadBox = -2;
   auto box_id = [&](int t) {
     const int lb = t * BPT + bx_blk;
@@ -128,9 +145,9 @@ __global__ void __launch_bounds__(kThreads, 2)
     }
     __syncwarp();
     if (id >= 0)
-      tma_box<KV, D>(smem_u32(ring + slot * G_::kStageBytes + (bx_v ? G_::kTileBytes : 0) +
-                              bx_blk * kBoxBytes),
-                     bx_v ? &vmap : &kmap, (id * a.num_kv_heads + kvh) * T, bar);
+      tma_load_2d(smem_u32(ring + slot * G_::kStageBytes + (bx_v ? G_::kTileBytes : 0) +
+                           bx_sl * kSlabBytes + bx_blk * kBoxBytes),
+                  bx_v ? &vmap : &kmap, bx_sl * 128, (id * a.num_kv_heads + kvh) * T, bar);
   };
   int nid = kNoBox;
   if (warp == 0) {
@@ -201,7 +218,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       const int nz = (kTile - z0) * G_::kSlabs * 8;
       for (int i = tid; i < nz; i += kThreads) {
         const int r = z0 + i / (G_::kSlabs * 8), c = i % (G_::kSlabs * 8);
-        *reinterpret_cast<uint4*>(vt + swz<G_::kSlabs>(r, c)) = make_uint4(0, 0, 0, 0);
+        *reinterpret_cast<uint4*>(vt + swz_slab(r, c)) = make_uint4(0, 0, 0, 0);
       }
       fence_proxy_async();  // before the slot is refilled by TMA
       __syncthreads();
@@ -218,7 +235,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int ks = 0; ks < KS; ks += 2) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4(kbase + swz<G_::kSlabs>(r, 2 * ks + mi), b0, b1, b2, b3);
+            ldsm_x4(kbase + swz_slab(r, 2 * ks + mi), b0, b1, b2, b3);
             mma16816<kBf>(sc[nt], qa[ks][0], qa[ks][1], qa[ks][2], qa[ks][3], b0, b1);
             mma16816<kBf>(sc[nt], qa[ks + 1][0], qa[ks + 1][1], qa[ks + 1][2], qa[ks + 1][3], b2, b3);
           }
@@ -226,7 +243,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int c0 = 0; c0 < KS; c0 += 4) {
             uint32_t w[4];
-            ldsm_x4(kbase + swz<G_::kSlabs>(r, c0 + mi), w[0], w[1], w[2], w[3]);
+            ldsm_x4(kbase + swz_slab(r, c0 + mi), w[0], w[1], w[2], w[3]);
 #pragma unroll
             for (int jj = 0; jj < 4; ++jj) {
               const int ks = c0 + jj;
@@ -286,7 +303,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int c = 0; c < NT; c += 2) {
             uint32_t b0, b1, b2, b3;
-            ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, c + (mi >> 1)), b0, b1, b2, b3);
+            ldsm_x4_t(vbase + swz_slab(rv, c + (mi >> 1)), b0, b1, b2, b3);
             mma16816<kBf>(o[c], pa0, pa1, pa2, pa3, b0, b1);
             mma16816<kBf>(o[c + 1], pa0, pa1, pa2, pa3, b2, b3);
           }
@@ -294,7 +311,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int c = 0; c < D / 16; c += 2) {
             uint32_t w0, w1, w2, w3;  // (keys 0-7, chunk c), (8-15, c), (0-7, c + 1), (8-15, c + 1)
-            ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, c + (mi >> 1)), w0, w1, w2, w3);
+            ldsm_x4_t(vbase + swz_slab(rv, c + (mi >> 1)), w0, w1, w2, w3);
             const uint32_t x0 = prmt(w0, 0x3120), x1 = prmt(w1, 0x3120);
             const uint32_t x2 = prmt(w2, 0x3120), x3 = prmt(w3, 0x3120);
             // chunk c: even head_dim index -> n-tile 2c, odd -> 2c + 1
@@ -472,8 +489,8 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
   a.v_scale = fp8 ? v_scale : 1.0f;
 
   CUtensorMap kmap, vmap;
-  st = pool_map(&kmap, k_cache, desc);
-  if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc);
+  st = pool_map(&kmap, k_cache, desc, false);
+  if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc, false);
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim, T = desc->block_size;
