@@ -51,6 +51,8 @@ def parse():
                     help="decode kernel (auto = tensor-core where it applies)")
     ap.add_argument("--block-size", type=int, default=None,
                     help="ablation: tokens per block (the pool keeps the same token capacity)")
+    ap.add_argument("--fp8-scales", default="tensor", choices=["tensor", "head"],
+                    help="ablation: E4M3 scales per tensor or per KV head")
     ap.add_argument("--kv-dtype", default=None, choices=["bf16", "f16", "e4m3"],
                     help="ablation: cache dtype (q stays 16-bit)")
     return ap.parse_args()
@@ -291,7 +293,9 @@ def run_gpu(args, world, rank, local):
     torch.cuda.set_device(local)
     dev_name = f"cuda:{local}"
     w = workload_of(args)
-    sc = W.fp8_scales(*W.kv_amax(w)) if w.kv_dtype == "e4m3" else {}
+    sc = {}
+    if w.kv_dtype == "e4m3":
+        sc = W.fp8_head_scales(w) if args.fp8_scales == "head" else W.fp8_scales(*W.kv_amax(w))
     scn = PS.materialize(PS.plan(w), dev_name, sc, partition_tokens=args.partition)
     stream = torch.cuda.current_stream()
     kv_bytes = scn.kv_bytes()
@@ -448,6 +452,7 @@ def run_gpu(args, world, rank, local):
                    "num_blocks": w.num_blocks, "context_tokens": int(scn.plan.ctx.sum()),
                    "kv_bytes_per_step": kv_bytes, "partition_tokens": scn.partition,
                    "kv_dtype": w.kv_dtype, "table_entries": int(np.ceil(scn.plan.ctx / w.block_size).sum()),
+                   **({"fp8_scales": args.fp8_scales} if w.kv_dtype == "e4m3" else {}),
                    "waste_slots_per_seq": round(float((np.ceil(scn.plan.ctx / w.block_size) * w.block_size
                                                        - scn.plan.ctx).mean()), 2),
                    "l2": ("inputs larger than L2 (K/V %d MB vs %d MB L2), no flush between steps"

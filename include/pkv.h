@@ -63,17 +63,26 @@ typedef enum {
 } pkv_status;
 
 /* Element types.  PKV_E4M3 is the OCP 8-bit E4M3 ("FN": no infinities,
- * max 448) format with one scale per tensor; the cache stores
- * e4m3(round_fp32(x * inv_scale)) and reads back e4m3 * scale. */
+ * max 448) format with one scale per tensor (or per KV head, see
+ * pkv_kv_desc.head_scales); the cache stores e4m3(round_fp32(x * inv_scale))
+ * and reads back e4m3 * scale. */
 typedef enum { PKV_F32 = 0, PKV_F16 = 1, PKV_BF16 = 2, PKV_E4M3 = 3 } pkv_dtype;
 
-/* Shape of one layer's K/V cache tensors. */
+/* Shape of one layer's K/V cache tensors.
+ * head_scales (E4M3 caches only; NULL otherwise): device float32
+ * [4][num_kv_heads], 4-byte aligned, owned by the caller: row 0 the K scale
+ * of each KV head, row 1 the V scale, row 2 the K inverse scale (what a slot
+ * write multiplies by), row 3 the V inverse scale.  When set, KV head h is
+ * stored and read with its own scales and the per-tensor scale arguments of
+ * every call are ignored; NULL keeps the per-tensor arguments.  A cache's
+ * bytes must be written and read with the same choice. */
 typedef struct {
   int32_t num_blocks;   /* physical blocks in the pool */
   int32_t num_kv_heads; /* N_kv */
   int32_t head_dim;     /* D_head: 64 or 128 */
   int32_t block_size;   /* T_block tokens per block: 16 or 32 */
   int32_t kv_dtype;     /* pkv_dtype of the cache */
+  const float* head_scales; /* per-KV-head E4M3 scales, or NULL */
 } pkv_kv_desc;
 
 typedef struct pkv_pool pkv_pool;

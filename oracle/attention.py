@@ -20,6 +20,10 @@ Readings where the pages are silent:
 * Grouped-query attention maps query head j to KV head j // (Hq / N_kv).
 * A context length of zero yields a zero output.
 * The context length counts the token written in this step.
+* An E4M3 cache is read as e4m3 * scale with one scale per tensor, or one
+  per KV head (k_scale, v_scale given as arrays [N_kv]; the pages fix only
+  the one-byte element size, so the per-head variant is the same decoding
+  with KV head h's own scale).
 """
 from __future__ import annotations
 
@@ -38,6 +42,13 @@ def gather_sequence(cache: dict, table, ctx: int, kv_head: int, block_size: int,
     blocks, which = np.unique(block_of_p, return_inverse=True)
     tiles = np.stack([cache[int(b)][kv_head] for b in blocks])  # [n_blocks, T, D]
     return bits_to_f64(tiles[which, offset_of_p], kv_dtype, scale)
+
+
+def head_scale(scale, h: int) -> float:
+    """The E4M3 scale that KV head h is read with: the number itself for a
+    per-tensor scale, element h of a per-head array."""
+    a = np.asarray(scale)
+    return float(a.reshape(-1)[h]) if a.ndim else float(a)
 
 
 def softmax_attention(q: np.ndarray, k: np.ndarray, v: np.ndarray, scale: float) -> np.ndarray:
@@ -69,8 +80,10 @@ def paged_attention_decode(q: np.ndarray, pool, tables, context_lens, softmax_sc
             if ctx == 0:
                 out[s, h * group:(h + 1) * group] = 0.0
                 continue
-            k = gather_sequence(pool.k, tables[s], ctx, h, pool.block_size, pool.kv_dtype, k_scale)
-            v = gather_sequence(pool.v, tables[s], ctx, h, pool.block_size, pool.kv_dtype, v_scale)
+            k = gather_sequence(pool.k, tables[s], ctx, h, pool.block_size, pool.kv_dtype,
+                                head_scale(k_scale, h))
+            v = gather_sequence(pool.v, tables[s], ctx, h, pool.block_size, pool.kv_dtype,
+                                head_scale(v_scale, h))
             for j in range(h * group, (h + 1) * group):
                 out[s, j] = softmax_attention(q[s, j], k, v, softmax_scale)
     return out

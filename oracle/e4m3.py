@@ -77,8 +77,9 @@ def _encode(x: np.ndarray) -> np.ndarray:
     return out
 
 
-def quantize_fp32(x: np.ndarray, inv_scale: float) -> np.ndarray:
+def quantize_fp32(x: np.ndarray, inv_scale) -> np.ndarray:
     """The slot write of an FP8 cache: the fp32 product x * inv_scale (one
-    IEEE fp32 rounding), then the E4M3 encoding of that product."""
-    prod = np.asarray(x, dtype=np.float32) * np.float32(inv_scale)
+    IEEE fp32 rounding), then the E4M3 encoding of that product.  inv_scale
+    is a number or an array that broadcasts against x."""
+    prod = np.asarray(x, dtype=np.float32) * np.asarray(inv_scale, dtype=np.float32)
     return encode(prod.astype(np.float64))

@@ -16,7 +16,9 @@ Readings (the pages fix no in-block layout):
 * Slot s is block s // block_size, offset s % block_size.  A negative slot
   means "write nothing" for that token.
 * An FP8 (E4M3) cache stores the byte of fp32(x * inv_scale); 16- and 32-bit
-  caches store the input's bits unchanged.
+  caches store the input's bits unchanged.  The inverse scale is one number
+  per tensor, or one per KV head (an array of N_kv values): head h of every
+  token is then multiplied by its own inv_scale[h].
 * A block copy copies the raw bytes of K and V of every layer.
 
 Storage is kept as raw bit patterns (uint16 for f16/bf16, uint32 for f32,
@@ -71,11 +73,17 @@ class PoolModel:
         return np.full(shape, self.fill, dtype=STORAGE[self.kv_dtype])
 
     def write(self, k_bits: np.ndarray, v_bits: np.ndarray, src_dtype: str, slots,
-              k_inv_scale: float = 1.0, v_inv_scale: float = 1.0):
-        """Store token i's K/V [N_kv, head_dim] at slot slots[i]."""
+              k_inv_scale=1.0, v_inv_scale=1.0):
+        """Store token i's K/V [N_kv, head_dim] at slot slots[i].  The inverse
+        scales are numbers (per tensor) or arrays [N_kv] (per KV head)."""
         slots = [int(s) for s in slots]
         for cache, src, inv in ((self.k, k_bits, k_inv_scale), (self.v, v_bits, v_inv_scale)):
             if self.kv_dtype == "e4m3":
+                inv = np.asarray(inv, dtype=np.float32)
+                if inv.ndim:                  # per KV head: axis 1 of [tokens, N_kv, D]
+                    if inv.shape != (self.num_kv_heads,):
+                        raise ValueError("per-head scales need one value per KV head")
+                    inv = inv.reshape(1, -1, 1)
                 stored = e4m3.quantize_fp32(f32_of_bits(src, src_dtype), inv)
             else:
                 if src_dtype != self.kv_dtype:

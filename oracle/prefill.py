@@ -27,7 +27,7 @@ from __future__ import annotations
 
 import numpy as np
 
-from .attention import gather_sequence
+from .attention import gather_sequence, head_scale
 
 
 def causal_mask(first_pos: int, n_queries: int, ctx: int) -> np.ndarray:
@@ -66,8 +66,10 @@ def paged_attention_prefill(q: np.ndarray, pool, tables, context_lens, query_sta
             raise ValueError(f"sequence {s}: {n} queries but context {ctx}")
         mask = causal_mask(ctx - n, n, ctx)
         for h in range(n_kv):
-            k = gather_sequence(pool.k, tables[s], ctx, h, pool.block_size, pool.kv_dtype, k_scale)
-            v = gather_sequence(pool.v, tables[s], ctx, h, pool.block_size, pool.kv_dtype, v_scale)
+            k = gather_sequence(pool.k, tables[s], ctx, h, pool.block_size, pool.kv_dtype,
+                                head_scale(k_scale, h))
+            v = gather_sequence(pool.v, tables[s], ctx, h, pool.block_size, pool.kv_dtype,
+                                head_scale(v_scale, h))
             for j in range(h * group, (h + 1) * group):
                 logits = (q[r0:r1, j] @ k.T) * softmax_scale
                 logits = np.where(mask, logits, -np.inf)

@@ -40,7 +40,7 @@ class PkvError(RuntimeError):
 class pkv_kv_desc(ctypes.Structure):
     _fields_ = [("num_blocks", ctypes.c_int32), ("num_kv_heads", ctypes.c_int32),
                 ("head_dim", ctypes.c_int32), ("block_size", ctypes.c_int32),
-                ("kv_dtype", ctypes.c_int32)]
+                ("kv_dtype", ctypes.c_int32), ("head_scales", ctypes.c_void_p)]
 
     @property
     def elem_bytes(self) -> int:
@@ -55,10 +55,27 @@ class pkv_kv_desc(ctypes.Structure):
         return (self.num_blocks, self.num_kv_heads, self.block_size, self.head_dim)
 
 
-def kv_desc(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype) -> pkv_kv_desc:
+def kv_desc(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype, head_scales=None) -> pkv_kv_desc:
+    """The cache descriptor.  head_scales (E4M3 caches): a contiguous float32
+    device tensor [4, num_kv_heads] holding each KV head's K scale, V scale,
+    K inverse and V inverse scale; the descriptor keeps a reference to it."""
     if isinstance(kv_dtype, str):
         kv_dtype = DTYPE_OF_NAME[kv_dtype]
-    return pkv_kv_desc(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype)
+    d = pkv_kv_desc(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype)
+    if head_scales is not None:
+        import torch
+        if (head_scales.dtype != torch.float32 or tuple(head_scales.shape) != (4, num_kv_heads)
+                or not head_scales.is_contiguous()):
+            raise ValueError("head_scales must be a contiguous float32 tensor [4, num_kv_heads]")
+        d.head_scales = head_scales.data_ptr()
+        d._head_scales = head_scales
+    return d
+
+
+def with_head_scales(desc: pkv_kv_desc, head_scales) -> pkv_kv_desc:
+    """A copy of ``desc`` with per-KV-head E4M3 scales (see kv_desc)."""
+    return kv_desc(desc.num_blocks, desc.num_kv_heads, desc.head_dim, desc.block_size, desc.kv_dtype,
+                   head_scales)
 
 
 _lib = None

@@ -392,6 +392,8 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   const bool fp8 = kv == PKV_E4M3;
   a.qk_scale = softmax_scale * (fp8 ? k_scale : 1.0f) * 1.4426950408889634f;
   a.v_scale = fp8 ? v_scale : 1.0f;
+  a.head_scales = desc->head_scales;
+  a.softmax_scale = softmax_scale;
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim;

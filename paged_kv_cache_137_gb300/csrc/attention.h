@@ -36,6 +36,10 @@ struct DecodeArgs {
   int32_t max_splits;        // S
   float qk_scale;            // softmax_scale * k_scale * log2(e)
   float v_scale;             // 1, or the E4M3 V scale
+  // E4M3 per-KV-head scales [4][N_kv] (K, V, K inverse, V inverse), or
+  // NULL; when set they replace qk_scale's k_scale, v_scale, k_inv, v_inv
+  const float* head_scales;
+  float softmax_scale;
 };
 
 // Limits of the stream-K tensor-core kernel: the per-sequence tile prefix sum

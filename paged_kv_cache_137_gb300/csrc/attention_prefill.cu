@@ -63,6 +63,8 @@ struct PrefillArgs {
       num_blocks;
   float qk_scale;             // softmax_scale * log2(e) (* k_scale for E4M3)
   float v_scale;              // 1, or the E4M3 V scale
+  const float* head_scales;   // E4M3 per-KV-head scales [4][N_kv], or NULL (replace the two above)
+  float softmax_scale;
 };
 
 template <typename KV, typename Q, int D, int T, int NS>
@@ -112,6 +114,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int kv_end = first + r_end;            // keys 0 .. kv_end - 1
   const int n_kv_tiles = (kv_end + kTile - 1) / kTile;
   const int kvh = j / a.group;
+  const HeadScales hs = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale, a.qk_scale,
+                                    a.v_scale, 1.f, 1.f);
 
   extern __shared__ uint8_t smem_raw[];
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
@@ -263,7 +267,7 @@ __global__ void __launch_bounds__(kThreads, 2)
 #pragma unroll
           for (int jj = 0; jj < 2; ++jj) {
             const int pos = tile_base + 8 * nt + 2 * q4 + jj;
-            float v = sc[nt][2 * h + jj] * a.qk_scale;
+            float v = sc[nt][2 * h + jj] * hs.qk;
             v = pos <= qpos[h] ? v : -CUDART_INF_F;
             sc[nt][2 * h + jj] = v;
             mx = fmaxf(mx, v);
@@ -354,7 +358,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     L += __shfl_xor_sync(FULL, L, 1);
     L += __shfl_xor_sync(FULL, L, 2);
     if (!warp_any || !rvalid[h]) continue;
-    const float inv = (L > 0.f || L != L) ? a.v_scale / L : 0.f;
+    const float inv = (L > 0.f || L != L) ? hs.v / L : 0.f;
     raw* orow = static_cast<raw*>(a.out) +
                 (static_cast<size_t>(q0 + wr0 + g + 8 * h) * HQ + j) * D;
     if constexpr (!kFp8) {
@@ -487,6 +491,8 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
   const bool fp8 = kv == PKV_E4M3;
   a.qk_scale = softmax_scale * (fp8 ? k_scale : 1.0f) * 1.4426950408889634f;
   a.v_scale = fp8 ? v_scale : 1.0f;
+  a.head_scales = desc->head_scales;
+  a.softmax_scale = softmax_scale;
 
   CUtensorMap kmap, vmap;
   st = pool_map(&kmap, k_cache, desc, false);

@@ -49,6 +49,8 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const Deco
   const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T;
   const int nsplit = bad_ctx ? 1 : max(1, (ctx + a.partition - 1) / a.partition);
   if (split >= nsplit) return;
+  const HeadScales sc = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale,
+                                    a.qk_scale, a.v_scale, a.k_inv, a.v_inv);
   const int t_begin = split * a.partition;
   const int t_end = bad_ctx ? 0 : min(t_begin + a.partition, ctx);
 
@@ -70,7 +72,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const Deco
     float x = 0.f;
     if (j < G)
       x = load_elem<Q>(a.q, (static_cast<size_t>(seq) * a.num_q_heads + kvh * G + j) * D + d) *
-          a.qk_scale;
+          sc.qk;
     q_s[j][d] = x;
   }
   __syncthreads();
@@ -188,7 +190,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const Deco
         A = fmaf(acc_s[w][j][d], f, A);
       }
     }
-    A *= a.v_scale;
+    A *= sc.v;
     const int qh = kvh * G + j;
     if (nsplit == 1) {
       const float o = any_bad ? CUDART_NAN_F : (L > 0.f ? A / L : 0.f);

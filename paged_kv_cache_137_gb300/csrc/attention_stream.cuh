@@ -266,6 +266,11 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
            (static_cast<size_t>(r.s) * HQ + static_cast<size_t>(r.h) * G) * D;
   };
   load_q<KV, Q, D>(qa, q_rows(cur), G, g, q4);
+  auto scales_of = [&](const StreamCursor& r) {
+    return head_scales(a.head_scales, a.num_kv_heads, r.h, a.softmax_scale, a.qk_scale, a.v_scale,
+                       a.k_inv, a.v_inv);
+  };
+  HeadScales sc = scales_of(cur);
   bool aborted = false, seg_bad = false, first_seg = true;
   int stalled_at = len, seg_j0 = cur.j;
   StreamCursor shared_pairs[2];  // a slice shares at most its first and its last pair
@@ -278,7 +283,7 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
     uint8_t* kt = ring + slot * G_::kStageBytes;
     uint8_t* vt = kt + G_::kTileBytes;
     if (arrived && nvalid > 0 &&
-        tile_step<KV, D>(st, qa, kt, vt, warp * 16, nvalid, a.qk_scale, lane))
+        tile_step<KV, D>(st, qa, kt, vt, warp * 16, nvalid, sc.qk, lane))
       fence_proxy_async();  // the zeroed rows, before the slot is refilled by TMA
     seg_bad |= !arrived || s_bad[slot] != 0;
     if (__syncthreads_or(!arrived) && !aborted) {
@@ -346,7 +351,7 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
           const int row = g + 8 * h;
           if (row >= G) continue;
           if (complete) {
-            const float inv = (L > 0.f || L != L) ? a.v_scale / L : 0.f;
+            const float inv = (L > 0.f || L != L) ? sc.v / L : 0.f;
 #pragma unroll
             for (int n = 0; n < NT; ++n)
 #pragma unroll
@@ -360,7 +365,7 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
 #pragma unroll
               for (int jj = 0; jj < 2; ++jj)
                 pr[2 + out_col<kFp8>(n, jj, q4)] =
-                    seg_bad ? CUDART_NAN_F : st.o[n][2 * h + jj] * a.v_scale;
+                    seg_bad ? CUDART_NAN_F : st.o[n][2 * h + jj] * sc.v;
             if (q4 == 0) {
               pr[0] = st.m[h];
               pr[1] = seg_bad ? CUDART_NAN_F : L;
@@ -379,6 +384,7 @@ __global__ void __launch_bounds__(kThreads, kStreamCtasPerSm)
         advance(cur);
         seg_j0 = cur.j;
         load_q<KV, Q, D>(qa, q_rows(cur), G, g, q4);
+        sc = scales_of(cur);
       }
     } else {
       advance(cur);

@@ -530,6 +530,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T;
   const int nsplit = bad_ctx ? 1 : max(1, (ctx + a.partition - 1) / a.partition);
   if (split >= nsplit) return;
+  const HeadScales sc = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale,
+                                    a.qk_scale, a.v_scale, a.k_inv, a.v_inv);
   // The pair's n_t tiles are shared out evenly: split i takes tiles
   // [i n_t / nsplit, (i + 1) n_t / nsplit), at most partition / 64 of them.
   // Near-equal pieces keep the longest units of the grid on pairs that need
@@ -573,7 +575,7 @@ __global__ void __launch_bounds__(kThreads, 3)
       const size_t dst = ((static_cast<size_t>(blk) * a.num_kv_heads + kvh) * T + p % T) * D + d0;
       store8<Q, KV>(static_cast<const typename Q::raw*>(which ? a.v_new : a.k_new) + src,
                     static_cast<typename KV::raw*>(const_cast<void*>(which ? a.v_cache : a.k_cache)) + dst,
-                    which ? a.v_inv : a.k_inv);
+                    which ? sc.v_inv : sc.k_inv);
       asm volatile("fence.proxy.async.global;" ::: "memory");  // before the TMA reads it
     }
   }
@@ -630,7 +632,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int row0 = warp * 16;
     const int tok0 = t_begin + tile * kTile + row0;
     const int nvalid = min(16, t_end - tok0);
-    if (arrived && nvalid > 0 && tile_step<KV, D>(st, qa, kt, vt, row0, nvalid, a.qk_scale, lane))
+    if (arrived && nvalid > 0 && tile_step<KV, D>(st, qa, kt, vt, row0, nvalid, sc.qk, lane))
       fence_proxy_async();  // the zeroed rows, before the slot is refilled by TMA
     if (__syncthreads_or(!arrived)) {
       timed_out = true;
@@ -664,7 +666,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int row = i / D, d = i % D;
     float M, L, A;
     combine_warps(mS, lS, oS, kWarps, 16, row, d, D, M, L, A);
-    A *= a.v_scale;
+    A *= sc.v;
     if (nsplit == 1) {
       const float out = any_bad ? CUDART_NAN_F : (L > 0.f ? A / L : 0.f);
       store_elem<Q>(a.out, (head0 + row) * D + d, out);

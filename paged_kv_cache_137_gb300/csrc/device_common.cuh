@@ -204,7 +204,26 @@ inline pkv_status check_desc(const pkv_kv_desc* d) {
     return fail(PKV_ERR_UNSUPPORTED, "head_dim must be 64 or 128");
   if (d->block_size != 16 && d->block_size != 32)
     return fail(PKV_ERR_UNSUPPORTED, "block_size must be 16 or 32");
+  if (d->head_scales != nullptr) {
+    if (d->kv_dtype != PKV_E4M3) return fail(PKV_ERR_INVALID_ARG, "head_scales need an E4M3 cache");
+    if (!aligned(d->head_scales, 4)) return fail(PKV_ERR_INVALID_ARG, "head_scales misaligned");
+  }
   return PKV_OK;
+}
+
+// Scales of KV head h of an E4M3 cache: the per-head table when there is one
+// ([4][n_kv]: K scale, V scale, K inverse, V inverse), else the per-tensor
+// values.  qk folds the K scale into the log2-domain logit scale in the
+// order the host folds a per-tensor one: (softmax_scale * k_scale) * log2(e).
+struct HeadScales {
+  float qk, v, k_inv, v_inv;
+};
+__device__ __forceinline__ HeadScales head_scales(const float* table, int n_kv, int h,
+                                                  float softmax_scale, float qk, float v,
+                                                  float k_inv, float v_inv) {
+  if (table == nullptr) return {qk, v, k_inv, v_inv};
+  return {(softmax_scale * table[h]) * 1.4426950408889634f, table[n_kv + h], table[2 * n_kv + h],
+          table[3 * n_kv + h]};
 }
 
 }  // namespace pkv

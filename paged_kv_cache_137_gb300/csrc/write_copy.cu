@@ -18,10 +18,18 @@
 namespace pkv {
 namespace {
 
+// The E4M3 inverse scale of K (which = 0) or V of KV head h: the per-head
+// table's rows 2 and 3 when there is one, else the per-tensor value.
+__device__ __forceinline__ float inv_of(const float* head_scales, const float* inv_scale, int n_kv,
+                                        int which, int h) {
+  return head_scales ? head_scales[(2 + which) * n_kv + h] : inv_scale[which];
+}
+
 struct WriteArgs {
   void* cache[2];       // K, V caches
   const void* src[2];   // K, V inputs [n_tokens][n_kv][D]
   float inv_scale[2];
+  const float* head_scales;  // E4M3 per-head scales [4][n_kv], or NULL
   const int64_t* slots;
   int64_t n_tokens;
   int32_t n_kv, head_dim, block_size, num_blocks;
@@ -51,7 +59,8 @@ __global__ void __launch_bounds__(256) write_kernel(const WriteArgs a) {
     const size_t dst_idx =
         ((static_cast<size_t>(blk) * a.n_kv + h) * a.block_size + off) * a.head_dim + d0;
     store8<Src, Dst>(static_cast<const typename Src::raw*>(a.src[which]) + src_idx,
-                     static_cast<typename Dst::raw*>(a.cache[which]) + dst_idx, a.inv_scale[which]);
+                     static_cast<typename Dst::raw*>(a.cache[which]) + dst_idx,
+                     inv_of(a.head_scales, a.inv_scale, a.n_kv, which, h));
   }
 }
 
@@ -62,6 +71,7 @@ struct WriteLastArgs {
   void* cache[2];
   const void* src[2];   // [B][n_kv][D]
   float inv_scale[2];
+  const float* head_scales;
   const int32_t* tables;
   const int32_t* ctx_lens;
   int32_t max_blocks, n_kv, head_dim, block_size, num_blocks;
@@ -83,7 +93,8 @@ __global__ void __launch_bounds__(128) write_last_kernel(const WriteLastArgs a) 
     const size_t dst_idx =
         ((static_cast<size_t>(blk) * a.n_kv + h) * a.block_size + p % a.block_size) * a.head_dim + d0;
     store8<Src, Dst>(static_cast<const typename Src::raw*>(a.src[which]) + src_idx,
-                     static_cast<typename Dst::raw*>(a.cache[which]) + dst_idx, a.inv_scale[which]);
+                     static_cast<typename Dst::raw*>(a.cache[which]) + dst_idx,
+                     inv_of(a.head_scales, a.inv_scale, a.n_kv, which, h));
   }
 }
 
@@ -143,6 +154,7 @@ extern "C" pkv_status pkv_write(void* k_cache, void* v_cache, const void* k, con
   a.src[1] = v;
   a.inv_scale[0] = k_inv_scale;
   a.inv_scale[1] = v_inv_scale;
+  a.head_scales = desc->head_scales;
   a.slots = slot_mapping;
   a.n_tokens = n_tokens;
   a.n_kv = desc->num_kv_heads;
@@ -227,6 +239,7 @@ pkv_status launch_write_last(void* k_cache, void* v_cache, const void* k_new, co
   a.src[1] = v_new;
   a.inv_scale[0] = k_inv_scale;
   a.inv_scale[1] = v_inv_scale;
+  a.head_scales = desc->head_scales;
   a.tables = tables;
   a.ctx_lens = ctx_lens;
   a.max_blocks = max_blocks;

@@ -120,7 +120,7 @@ class DeviceScenario:
     k_new: torch.Tensor
     v_new: torch.Tensor
     workspace: torch.Tensor | None
-    scales: dict
+    scales: dict             # per-tensor E4M3 scale arguments ({} with per-head scales in desc)
     partition: int           # partition_tokens passed to the decode call (0 = automatic)
     softmax_scale: float
 
@@ -172,7 +172,15 @@ def materialize(p: Plan, device="cuda", scales: dict | None = None, chunk_tokens
     scales = dict(scales or {})
     if w.kv_dtype == "e4m3" and "k_inv_scale" not in scales:
         raise ValueError("an E4M3 cache needs its scales")
-    desc = kv_desc(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.kv_dtype)
+    head_scales = None
+    if np.ndim(scales.get("k_scale", 1.0)) > 0:
+        # per-KV-head scales go in the descriptor; the per-tensor arguments
+        # of every call are then ignored (left at 1)
+        rows = [np.asarray(scales[n], dtype=np.float32)
+                for n in ("k_scale", "v_scale", "k_inv_scale", "v_inv_scale")]
+        head_scales = torch.from_numpy(np.stack(rows)).to(device)
+        scales = {}
+    desc = kv_desc(w.num_blocks, w.num_kv_heads, w.head_dim, w.block_size, w.kv_dtype, head_scales)
     k_cache, v_cache = empty_cache(desc, device, fill_byte=POISON_BYTE)
     kinv, vinv = scales.get("k_inv_scale", 1.0), scales.get("v_inv_scale", 1.0)
 

@@ -173,3 +173,25 @@ def test_workload_plans_match_oracle(name):
         assert np.all(native.tables[r, len(tab):] == -1)
         assert native.ctx_i32[r] == ref.ctx[r]
     assert native.pool.free_stack().tolist() == ref.alloc.free_stack_top_first()
+
+
+def test_descriptor_head_scales_are_checked_before_any_launch():
+    """Per-head scales belong to E4M3 caches: a 16-bit descriptor carrying a
+    table is rejected by argument checking (no device work), an E4M3 one is
+    accepted (an empty write), and the descriptor's layout matches the
+    header's (six fields, the pointer last)."""
+    import ctypes
+    lib = pkv.lib()
+    assert [f for f, _ in pkv.pkv_kv_desc._fields_][-1] == "head_scales"
+    fake = ctypes.c_void_p(0x1000)            # never dereferenced: the calls stop at validation
+    nothing = ctypes.c_void_p(0x2000)
+    for dtype, want in (("bf16", pkv.PKV_ERR_INVALID_ARG), ("e4m3", pkv.PKV_OK)):
+        d = pkv.kv_desc(16, 2, 128, 16, dtype)
+        d.head_scales = fake.value
+        st = lib.pkv_write(nothing, nothing, nothing, nothing, pkv.PKV_BF16, None, 0,
+                           ctypes.byref(d), 1.0, 1.0, None)
+        assert st == want, (dtype, st, lib.pkv_last_error())
+    d = pkv.kv_desc(16, 2, 128, 16, "e4m3")
+    d.head_scales = 0x1002                    # not 4-byte aligned
+    assert lib.pkv_write(nothing, nothing, nothing, nothing, pkv.PKV_BF16, None, 0,
+                         ctypes.byref(d), 1.0, 1.0, None) == pkv.PKV_ERR_INVALID_ARG

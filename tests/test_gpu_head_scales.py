@@ -1,0 +1,149 @@
+"""E4M3 caches with per-KV-head scales on the GPU, against the oracle.
+
+Bit-exact: the pool bytes after the slot writes (prefill writes, the step's
+fused or separate write).  Attention: max-abs 6e-2 times the magnitude of the
+KV head (its gain 2^(-g h)) against the oracle on the dequantised cache, for
+every decode kernel and for prefill.  Per-head scales equal to a per-tensor
+scale give bit-identical pools and outputs.  And the ablation the per-head
+scales are for: with KV heads whose magnitudes differ by up to 2^21, one
+scale per tensor flushes the smallest heads to zero (mean error 100% of their
+outputs' magnitude), while per-head scales keep every head at E4M3's own few
+percent.
+"""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import workloads as W
+from oracle import attention as OA
+from oracle import prefill as OP
+from oracle import scenario as OS
+
+import paged_kv_cache_137_gb300 as pkv
+from paged_kv_cache_137_gb300 import scenario as PS
+
+pytestmark = pytest.mark.gpu
+
+FP8 = W.scaled(W.get("fp8_churn"), num_seqs=12, num_blocks=2048, churn=500, ctx_range=(1, 1500))
+SPREAD = W.scaled(FP8, head_gain_log2=3.0, seed=1391)        # KV heads 2^0 .. 2^-21
+CASES = {"fp8": FP8, "spread": SPREAD}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def built():
+    pkv.build()
+    assert torch.cuda.is_available()
+
+
+@pytest.fixture(params=["auto", "simt", "tc", "persistent"])
+def kernel(request):
+    pkv.pkv_set_attention_kernel(request.param)
+    yield request.param
+    pkv.pkv_set_attention_kernel("auto")
+
+
+def bits(t):
+    return t.contiguous().view(torch.uint8).cpu().numpy().reshape(-1)
+
+
+def q_head_gain(w):
+    return np.repeat(W.head_gains(w).astype(np.float64), w.group)[None, :, None]
+
+
+def oracle_decode(scn, sc):
+    return OA.paged_attention_decode(scn.q_f64(), scn.pool, scn.tables, scn.ctx,
+                                     1.0 / math.sqrt(scn.w.head_dim), sc["k_scale"], sc["v_scale"])
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_per_head_step_matches_the_oracle(name, kernel):
+    w = CASES[name]
+    sc = W.fp8_head_scales(w)
+    dev = PS.materialize(PS.plan(w), "cuda", sc)
+    out = dev.step().double().cpu().numpy()
+    torch.cuda.synchronize()
+    ref = OS.build(w, scales=sc)
+    assert np.array_equal(bits(dev.k_cache), ref.pool.dense("k").view(np.uint8).reshape(-1))
+    assert np.array_equal(bits(dev.v_cache), ref.pool.dense("v").view(np.uint8).reshape(-1))
+    err = np.abs(out - oracle_decode(ref, sc)) / q_head_gain(w)
+    assert not np.isnan(out).any() and err.max() <= 6e-2
+
+
+def test_equal_per_head_scales_are_bit_identical_to_per_tensor(kernel):
+    w = FP8
+    st = W.fp8_scales(*W.kv_amax(w))
+    sh = {n: np.full(w.num_kv_heads, v, dtype=np.float32) for n, v in st.items()}
+    p = PS.plan(w)
+    a = PS.materialize(p, "cuda", st)
+    oa = a.step().clone()
+    b = PS.materialize(p, "cuda", sh)
+    ob = b.step().clone()
+    torch.cuda.synchronize()
+    assert b.desc.head_scales and not a.desc.head_scales
+    assert torch.equal(a.k_cache.view(torch.uint8), b.k_cache.view(torch.uint8))
+    assert torch.equal(a.v_cache.view(torch.uint8), b.v_cache.view(torch.uint8))
+    assert torch.equal(oa.view(torch.int16), ob.view(torch.int16))
+
+
+def test_fused_step_equals_write_then_attend_with_per_head_scales():
+    w = SPREAD
+    sc = W.fp8_head_scales(w)
+    p = PS.plan(w)
+    a = PS.materialize(p, "cuda", sc, partition_tokens=0)
+    a.copy_blocks()
+    a.write_step()
+    out_a = a.attend().clone()
+    b = PS.materialize(p, "cuda", sc, partition_tokens=0)
+    b.copy_blocks()
+    out_b = b.decode_step().clone()
+    torch.cuda.synchronize()
+    assert torch.equal(a.k_cache.view(torch.uint8), b.k_cache.view(torch.uint8))
+    assert torch.equal(a.v_cache.view(torch.uint8), b.v_cache.view(torch.uint8))
+    assert torch.equal(out_a.view(torch.int16), out_b.view(torch.int16))
+
+
+def test_prefill_with_per_head_scales_matches_the_oracle():
+    w = SPREAD
+    sc = W.fp8_head_scales(w)
+    dev = PS.materialize(PS.plan(w), "cuda", sc)
+    dev.copy_blocks()
+    dev.write_step()
+    n = W.chunk_lens(w, dev.plan.ctx, 200)
+    qs = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    q = torch.cat([W.q_for_chunk(w, s, int(n[r])) for r, s in enumerate(dev.plan.seq_ids)])
+    out = torch.full_like(q, float("nan"), device="cuda")
+    pkv.pkv_attention_prefill(out, q.cuda(), dev.k_cache, dev.v_cache, dev.tables, dev.ctx,
+                              torch.from_numpy(qs).cuda(), dev.desc, 1.0 / math.sqrt(w.head_dim))
+    torch.cuda.synchronize()
+    scn = OS.build(w, scales=sc)
+    ref = OP.paged_attention_prefill(q.double().numpy(), scn.pool, scn.tables, scn.ctx, qs,
+                                     1.0 / math.sqrt(w.head_dim), sc["k_scale"], sc["v_scale"])
+    got = out.double().cpu().numpy()
+    err = np.abs(got - ref) / q_head_gain(w)
+    assert not np.isnan(got).any() and err.max() <= 6e-2
+
+
+def test_per_head_scales_keep_small_heads_accurate():
+    """Quantisation error against attention over the unquantised bf16 values
+    (the oracle on a bf16 cache of the same draws): per KV head, the mean
+    absolute error over its group's outputs divided by their mean magnitude."""
+    w = SPREAD
+    exact_w = W.scaled(w, kv_dtype="bf16")
+    exact = OS.build(exact_w)
+    ref = OA.paged_attention_decode(exact.q_f64(), exact.pool, exact.tables, exact.ctx,
+                                    1.0 / math.sqrt(w.head_dim))
+    rel = {}
+    for kind, sc in (("tensor", W.fp8_scales(*W.kv_amax(w))), ("head", W.fp8_head_scales(w))):
+        dev = PS.materialize(PS.plan(w), "cuda", sc)
+        out = dev.step().double().cpu().numpy()
+        torch.cuda.synchronize()
+        e = np.abs(out - ref).reshape(len(out), w.num_kv_heads, w.group, -1)
+        r = np.abs(ref).reshape(len(out), w.num_kv_heads, w.group, -1)
+        rel[kind] = e.mean(axis=(0, 2, 3)) / r.mean(axis=(0, 2, 3))
+        print(f"E4M3 scales per {kind}: mean error / mean magnitude per KV head",
+              np.array2string(rel[kind], precision=4))
+    assert (rel["head"] <= 0.05).all(), rel["head"]
+    assert (rel["tensor"][-2:] >= 0.9).all(), rel["tensor"]     # the 2^-18 and 2^-21 heads
+    assert (rel["head"][-3:] < rel["tensor"][-3:] / 4).all()

@@ -26,7 +26,10 @@ on (decode of one new token per sequence over a pool of fixed-size blocks):
                        churn operations.
 
 Ranges are integer and inclusive; values are N(0,1) drawn in fp32 and rounded
-to the storage dtype with PyTorch's round-to-nearest-even cast.
+to the storage dtype with PyTorch's round-to-nearest-even cast.  A workload
+with ``head_gain_log2`` g > 0 multiplies KV head h's keys and values by
+2^(-g h) in fp32 before the cast (heads of very different magnitude, the case
+per-head FP8 scales are for).
 """
 from __future__ import annotations
 
@@ -42,6 +45,7 @@ __all__ = [
     "Workload", "CONFIGS", "get", "scaled",
     "rng", "context_lens", "free_order", "churn_ops", "q_for_seq", "kv_for_seq",
     "prefix_kv", "fork_layout", "fp8_scales", "kv_amax", "TORCH_DTYPES",
+    "head_gains", "kv_amax_heads", "fp8_head_scales",
 ]
 
 TORCH_DTYPES = {"f32": torch.float32, "f16": torch.float16, "bf16": torch.bfloat16}
@@ -74,6 +78,7 @@ class Workload:
     churn: int = 0             # alloc/free operations applied before the workload
     shuffled_pool: bool = True
     prefill_chunk: int = 0     # > 0: a prefill workload, chunks of the last positions
+    head_gain_log2: float = 0.0  # KV head h's K and V multiplied by 2^(-head_gain_log2 * h)
 
     @property
     def group(self) -> int:
@@ -235,8 +240,16 @@ def kv_for_seq(w: Workload, seq: int, n_tokens: int, first_pos: int = 0,
             pos = np.arange(first_pos, first_pos + n_tokens)
             hit = (pos + 1) % w.spike_every == 0
             x[hit] *= np.float32(w.spike_scale)
+        if w.head_gain_log2:
+            x *= head_gains(w)[None, :, None]
         out.append(_cast(x, w.src_dtype))
     return out[0], out[1]
+
+
+def head_gains(w: Workload) -> np.ndarray:
+    """fp32 [num_kv_heads]: the factor 2^(-head_gain_log2 * h) of KV head h."""
+    h = np.arange(w.num_kv_heads, dtype=np.float64)
+    return np.exp2(-w.head_gain_log2 * h).astype(np.float32)
 
 
 def prefix_kv(w: Workload) -> tuple[torch.Tensor, torch.Tensor]:
@@ -244,6 +257,9 @@ def prefix_kv(w: Workload) -> tuple[torch.Tensor, torch.Tensor]:
     per = (w.prefix_len, w.num_kv_heads, w.head_dim)
     k = rng(w, _PREFIX_K).standard_normal(per, dtype=np.float32)
     v = rng(w, _PREFIX_V).standard_normal(per, dtype=np.float32)
+    if w.head_gain_log2:
+        k *= head_gains(w)[None, :, None]
+        v *= head_gains(w)[None, :, None]
     return _cast(k, w.src_dtype), _cast(v, w.src_dtype)
 
 
@@ -274,28 +290,45 @@ def fork_layout(w: Workload) -> dict:
     raise RuntimeError("could not draw enough mid-block forks")
 
 
-def fp8_scales(amax_k: float, amax_v: float) -> dict:
-    """Per-tensor E4M3 scales from the absolute maxima of all K (V) values:
-    scale = amax / 448 in fp32 and the reciprocal the slot write multiplies by,
-    inv = fp32(1 / scale).  448 is the largest finite E4M3 value."""
+def fp8_scales(amax_k, amax_v) -> dict:
+    """E4M3 scales from the absolute maxima of the K (V) values: scale =
+    amax / 448 in fp32 and the reciprocal the slot write multiplies by,
+    inv = fp32(1 / scale).  448 is the largest finite E4M3 value.  Numbers
+    give per-tensor scales (floats); arrays [N_kv] give per-KV-head scales
+    (float32 arrays)."""
     out = {}
     for name, a in (("k", amax_k), ("v", amax_v)):
-        s = np.float32(np.float32(a) / np.float32(448.0))
-        out[name + "_scale"] = float(s)
-        out[name + "_inv_scale"] = float(np.float32(np.float32(1.0) / s))
+        s = np.asarray(a, dtype=np.float32) / np.float32(448.0)
+        inv = np.float32(1.0) / s
+        scalar = np.ndim(a) == 0
+        out[name + "_scale"] = float(s) if scalar else s.astype(np.float32)
+        out[name + "_inv_scale"] = float(inv) if scalar else inv.astype(np.float32)
     return out
 
 
 @functools.lru_cache(maxsize=8)
-def kv_amax(w: Workload) -> tuple[float, float]:
-    """Largest |K| and |V| over every token of every sequence of a workload
-    (positions 0 .. ctx - 1, in the source dtype), the statistic the per-tensor
-    E4M3 scales are computed from."""
+def kv_amax_heads(w: Workload) -> tuple[np.ndarray, np.ndarray]:
+    """Largest |K| and |V| of each KV head over every token of every sequence
+    of a workload (positions 0 .. ctx - 1, in the source dtype): float64
+    arrays [num_kv_heads], the statistic per-head E4M3 scales come from."""
     if w.ctx_dist == "prefix_fork":
-        raise NotImplementedError("per-tensor scales are defined for independent sequences")
-    ak = av = 0.0
+        raise NotImplementedError("scales from maxima are defined for independent sequences")
+    ak = np.zeros(w.num_kv_heads)
+    av = np.zeros(w.num_kv_heads)
     for s, c in enumerate(context_lens(w)):
         k, v = kv_for_seq(w, s, int(c))
-        ak = max(ak, float(k.float().abs().max()))
-        av = max(av, float(v.float().abs().max()))
+        ak = np.maximum(ak, k.float().abs().amax(dim=(0, 2)).double().numpy())
+        av = np.maximum(av, v.float().abs().amax(dim=(0, 2)).double().numpy())
     return ak, av
+
+
+def kv_amax(w: Workload) -> tuple[float, float]:
+    """Largest |K| and |V| over every token of every sequence of a workload,
+    the statistic the per-tensor E4M3 scales are computed from."""
+    ak, av = kv_amax_heads(w)
+    return float(ak.max()), float(av.max())
+
+
+def fp8_head_scales(w: Workload) -> dict:
+    """Per-KV-head E4M3 scales of a workload (fp8_scales of the per-head maxima)."""
+    return fp8_scales(*kv_amax_heads(w))
