@@ -341,12 +341,16 @@ __device__ __forceinline__ bool tile_step(WarpState<D>& st, const uint32_t (&qa)
       }
     st.l[h] = st.l[h] * corr[h] + sum;
   }
+  // a row whose maximum did not grow has corr exactly 1: the rescale is
+  // skipped when that holds for every row of the warp (the result is the same)
+  if (__any_sync(0xffffffffu, corr[0] != 1.f || corr[1] != 1.f)) {
 #pragma unroll
-  for (int n = 0; n < NT; ++n) {
-    st.o[n][0] *= corr[0];
-    st.o[n][1] *= corr[0];
-    st.o[n][2] *= corr[1];
-    st.o[n][3] *= corr[1];
+    for (int n = 0; n < NT; ++n) {
+      st.o[n][0] *= corr[0];
+      st.o[n][1] *= corr[0];
+      st.o[n][2] *= corr[1];
+      st.o[n][3] *= corr[1];
+    }
   }
   const uint32_t pa0 = pack2<kBf>(p[0][0], p[0][1]);
   const uint32_t pa1 = pack2<kBf>(p[0][2], p[0][3]);
@@ -409,6 +413,214 @@ __device__ __forceinline__ void publish(const WarpState<D>& st, float* mS, float
       const int d = out_col<kFp8>(n, j, q4);
       if (g < G) oS[(warp * ostride + g) * D + d] = st.o[n][j];
       if (g + 8 < G) oS[(warp * ostride + g + 8) * D + d] = st.o[n][2 + j];
+    }
+}
+
+// ---------------------------------- head-columns form (query group <= 8)
+// With at most 8 query heads per KV head the products run with the tokens as
+// the MMA rows: S^T = K q^T (m16n8k16: 16 tokens x 8 heads, k = head_dim) and
+// O^T += V^T P^T (16 head_dim rows x 8 heads, k = 16 tokens).  No MMA row is
+// padding, so a warp issues half the MMAs of the head-rows form and keeps
+// half the accumulators (32 instead of 64 at head_dim 128); P^T reaches the
+// B operand of the second product through a warp transpose (movmatrix).
+// Lane (g, q4) holds heads 2 q4 and 2 q4 + 1.
+
+__device__ __forceinline__ uint32_t movmatrix_t(uint32_t a) {
+  uint32_t d;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(d) : "r"(a));
+  return d;
+}
+
+template <int D>
+struct WarpStateT {
+  float o[D / 16][4];  // O^T m-tile mt: (row g, head 2q4), (g, 2q4 + 1), (g + 8, 2q4), (g + 8, 2q4 + 1)
+  float m[2], l[2];    // heads 2 q4 + j
+  __device__ __forceinline__ void reset() {
+#pragma unroll
+    for (int n = 0; n < D / 16; ++n) o[n][0] = o[n][1] = o[n][2] = o[n][3] = 0.f;
+    m[0] = m[1] = -CUDART_INF_F;
+    l[0] = l[1] = 0.f;
+  }
+};
+
+// q as the B operand of S^T = K q^T: for k-step ks lane (g, q4) holds head
+// g's elements k = 2 q4, 2 q4 + 1 (qb[ks][0]) and 2 q4 + 8, 2 q4 + 9
+// (qb[ks][1]); heads >= G are zero.  For an E4M3 cache q becomes f16 and the
+// k order within a 16-element step is the one the K bytes arrive in: lane q4
+// holds head_dim 4 q4 .. 4 q4 + 3 of the step.
+template <typename KV, typename Q, int D>
+__device__ __forceinline__ void load_qt(uint32_t (&qb)[D / 16][2], const typename Q::raw* qrows,
+                                        int G, int g, int q4) {
+  constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
+#pragma unroll
+  for (int ks = 0; ks < D / 16; ++ks) {
+    uint32_t lo = 0, hi = 0;
+    if (g < G) {
+      if constexpr (!kFp8) {
+        const uint32_t* qp = reinterpret_cast<const uint32_t*>(qrows + g * D + 16 * ks + 2 * q4);
+        lo = qp[0];
+        hi = qp[4];
+      } else {
+        float f[4];
+        LoadF32<Q, 4>::run(qrows + g * D + 16 * ks + 4 * q4, f);
+        lo = pack2<false>(f[0], f[1]);
+        hi = pack2<false>(f[2], f[3]);
+      }
+    }
+    qb[ks][0] = lo;
+    qb[ks][1] = hi;
+  }
+}
+
+// head_dim held by O^T m-tile mt, fragment row g (+ 8 when hi).  E4M3 V
+// arrives as byte pairs (d, d + 1) of one token: rows g and g + 8 of an
+// m-tile hold d = 16 mt + 2 g and 16 mt + 2 g + 1.
+template <bool kFp8>
+__device__ __forceinline__ int out_row_t(int mt, int g, int hi) {
+  if constexpr (!kFp8) return 16 * mt + g + 8 * hi;
+  else return 16 * mt + 2 * g + hi;
+}
+
+// tile_step in the head-columns form (same contract).
+template <typename KV, int D>
+__device__ __forceinline__ bool tile_step_t(WarpStateT<D>& st, const uint32_t (&qb)[D / 16][2],
+                                            const uint8_t* kt, uint8_t* vt, int row0, int nvalid,
+                                            float qk_scale, int lane) {
+  using G_ = Geom<KV, D>;
+  constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
+  constexpr bool kBf = std::is_same<KV, BF16>::value;
+  constexpr int KS = D / 16;
+  constexpr int MT = D / 16;
+  const int g = lane >> 2;
+  bool zeroed = false;
+  if (nvalid < 16) {  // zero the V rows past the context end
+    const int nz = (16 - nvalid) * G_::kSlabs * 8;
+    for (int i = lane; i < nz; i += 32) {
+      const int r = row0 + nvalid + i / (G_::kSlabs * 8);
+      const int c = i % (G_::kSlabs * 8);
+      *reinterpret_cast<uint4*>(vt + swz<G_::kSlabs>(r, c)) = make_uint4(0, 0, 0, 0);
+    }
+    __syncwarp();
+    zeroed = true;
+  }
+  const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+  const int li = lane & 7, mi = lane >> 3;
+
+  // S^T = K q^T: 16 tokens x 8 heads
+  float sc[4] = {0.f, 0.f, 0.f, 0.f};
+  if constexpr (!kFp8) {
+    // matrix mi: tokens (mi & 1) * 8 .., 16-byte chunk 2 ks + (mi >> 1)
+    const int r = row0 + (mi & 1) * 8 + li;
+#pragma unroll
+    for (int ks = 0; ks < KS; ++ks) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4(kbase + swz<G_::kSlabs>(r, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+      mma16816<kBf>(sc, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+    }
+  } else {
+    // matrix mi: tokens (mi & 1) * 8 .., 16-byte chunk ks + (mi >> 1): one
+    // load serves two k-steps; a register holds head_dim 4 q4 .. 4 q4 + 3
+    const int r = row0 + (mi & 1) * 8 + li;
+#pragma unroll
+    for (int ks = 0; ks < KS; ks += 2) {
+      uint32_t w0, w1, w2, w3;
+      ldsm_x4(kbase + swz<G_::kSlabs>(r, ks + (mi >> 1)), w0, w1, w2, w3);
+      mma16816<false>(sc, e4m3x2_f16x2(w0 & 0xffffu), e4m3x2_f16x2(w1 & 0xffffu),
+                      e4m3x2_f16x2(w0 >> 16), e4m3x2_f16x2(w1 >> 16), qb[ks][0], qb[ks][1]);
+      mma16816<false>(sc, e4m3x2_f16x2(w2 & 0xffffu), e4m3x2_f16x2(w3 & 0xffffu),
+                      e4m3x2_f16x2(w2 >> 16), e4m3x2_f16x2(w3 >> 16), qb[ks + 1][0],
+                      qb[ks + 1][1]);
+    }
+  }
+
+  // online softmax over the tokens (rows g, g + 8) of heads 2 q4 + j
+  float p[4];
+  float corr[2];
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    const float v0 = g < nvalid ? sc[j] * qk_scale : -CUDART_INF_F;
+    const float v1 = g + 8 < nvalid ? sc[2 + j] * qk_scale : -CUDART_INF_F;
+    float mx = fmaxf(v0, v1);
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+    mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+    const float mn = fmaxf(st.m[j], mx);
+    corr[j] = exp2f(st.m[j] - mn);
+    st.m[j] = mn;
+    p[j] = exp2f(v0 - mn);
+    p[2 + j] = exp2f(v1 - mn);
+    st.l[j] = st.l[j] * corr[j] + (p[j] + p[2 + j]);
+  }
+  // a head whose maximum did not grow has corr exactly 1: the rescale is
+  // skipped when that holds for every head of the warp (the result is the same)
+  if (__any_sync(0xffffffffu, corr[0] != 1.f || corr[1] != 1.f)) {
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      st.o[mt][0] *= corr[0];
+      st.o[mt][1] *= corr[1];
+      st.o[mt][2] *= corr[0];
+      st.o[mt][3] *= corr[1];
+    }
+  }
+  // P^T as the B operand (k = tokens, n = heads): the transposes of the
+  // (tokens 0-7) x heads and (tokens 8-15) x heads blocks
+  const uint32_t pb0 = movmatrix_t(pack2<kBf>(p[0], p[1]));
+  const uint32_t pb1 = movmatrix_t(pack2<kBf>(p[2], p[3]));
+
+  // O^T += V^T P^T
+  if constexpr (!kFp8) {
+    // matrix mi: tokens (mi >> 1) * 8 .., 16-byte chunk 2 mt + (mi & 1)
+    const int rv = row0 + (mi >> 1) * 8 + li;
+#pragma unroll
+    for (int mt = 0; mt < MT; ++mt) {
+      uint32_t a0, a1, a2, a3;
+      ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, 2 * mt + (mi & 1)), a0, a1, a2, a3);
+      mma16816<kBf>(st.o[mt], a0, a1, a2, a3, pb0, pb1);
+    }
+  } else {
+    // matrix mi: tokens (mi & 1) * 8 .., 16-byte chunk mt + (mi >> 1); a
+    // register holds tokens 2 q4, 2 q4 + 1 of head_dim pair (2 g, 2 g + 1)
+    const int rv = row0 + (mi & 1) * 8 + li;
+#pragma unroll
+    for (int mt = 0; mt < MT; mt += 2) {
+      uint32_t w0, w1, w2, w3;  // (tok 0-7, mt), (tok 8-15, mt), (0-7, mt+1), (8-15, mt+1)
+      ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, mt + (mi >> 1)), w0, w1, w2, w3);
+      const uint32_t x0 = prmt(w0, 0x3120), x1 = prmt(w1, 0x3120);
+      const uint32_t x2 = prmt(w2, 0x3120), x3 = prmt(w3, 0x3120);
+      mma16816<false>(st.o[mt], e4m3x2_f16x2(x0 & 0xffffu), e4m3x2_f16x2(x0 >> 16),
+                      e4m3x2_f16x2(x1 & 0xffffu), e4m3x2_f16x2(x1 >> 16), pb0, pb1);
+      mma16816<false>(st.o[mt + 1], e4m3x2_f16x2(x2 & 0xffffu), e4m3x2_f16x2(x2 >> 16),
+                      e4m3x2_f16x2(x3 & 0xffffu), e4m3x2_f16x2(x3 >> 16), pb0, pb1);
+    }
+  }
+  return zeroed;
+}
+
+// publish in the head-columns form: mS/lS [warp][16] (heads < 8), oS
+// [warp][ostride][D] (heads < G).  The sums are completed across the eight
+// token rows first.
+template <typename KV, int D>
+__device__ __forceinline__ void publish_t(const WarpStateT<D>& st, float* mS, float* lS, float* oS,
+                                          int warp, int G, int ostride, int lane) {
+  constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
+  const int g = lane >> 2, q4 = lane & 3;
+#pragma unroll
+  for (int j = 0; j < 2; ++j) {
+    float l = st.l[j];
+    l += __shfl_xor_sync(0xffffffffu, l, 4);
+    l += __shfl_xor_sync(0xffffffffu, l, 8);
+    l += __shfl_xor_sync(0xffffffffu, l, 16);
+    if (g == 0) {
+      mS[warp * 16 + 2 * q4 + j] = st.m[j];
+      lS[warp * 16 + 2 * q4 + j] = l;
+    }
+  }
+#pragma unroll
+  for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      const int head = 2 * q4 + (e & 1);
+      if (head < G) oS[(warp * ostride + head) * D + out_row_t<kFp8>(mt, g, e >> 1)] = st.o[mt][e];
     }
 }
 
@@ -507,11 +719,13 @@ __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit, floa
 }
 
 // ------------------------------------------------------------------ kernel
-template <typename KV, typename Q, int D, int T, int NS>
+// HC: the head-columns form of the tile products (query group <= 8).
+template <typename KV, typename Q, int D, int T, int NS, bool HC>
 __global__ void __launch_bounds__(kThreads, 3)
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
   using G_ = Geom<KV, D>;
+  using State = std::conditional_t<HC, WarpStateT<D>, WarpState<D>>;
   constexpr int KS = D / 16;        // k-steps of q . K^T
   constexpr int BPT = kTile / T;    // blocks per tile
   constexpr int kBoxBytes = T * G_::kRowBytes;  // one (block, head) box: all its slabs
@@ -579,10 +793,13 @@ __global__ void __launch_bounds__(kThreads, 3)
       asm volatile("fence.proxy.async.global;" ::: "memory");  // before the TMA reads it
     }
   }
-  uint32_t qa[KS][4];
-  load_q<KV, Q, D>(qa, static_cast<const typename Q::raw*>(a.q) +
-                           (static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G) * D,
-                   G, g, q4);
+  uint32_t qa[KS][HC ? 2 : 4];
+  {
+    const typename Q::raw* qrows = static_cast<const typename Q::raw*>(a.q) +
+        (static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G) * D;
+    if constexpr (HC) load_qt<KV, Q, D>(qa, qrows, G, g, q4);
+    else load_q<KV, Q, D>(qa, qrows, G, g, q4);
+  }
   __syncthreads();
 
   // ---------------------------------------------------------- producer
@@ -619,7 +836,7 @@ __global__ void __launch_bounds__(kThreads, 3)
     for (int t = 0; t < NS && t < n_tiles; ++t) issue(t);
 
   // ---------------------------------------------------------- consumers
-  WarpState<D> st;
+  State st;
   st.reset();
   bool timed_out = false;
   int stalled_at = -1;
@@ -632,8 +849,12 @@ __global__ void __launch_bounds__(kThreads, 3)
     const int row0 = warp * 16;
     const int tok0 = t_begin + tile * kTile + row0;
     const int nvalid = min(16, t_end - tok0);
-    if (arrived && nvalid > 0 && tile_step<KV, D>(st, qa, kt, vt, row0, nvalid, sc.qk, lane))
-      fence_proxy_async();  // the zeroed rows, before the slot is refilled by TMA
+    bool zeroed = false;
+    if (arrived && nvalid > 0) {
+      if constexpr (HC) zeroed = tile_step_t<KV, D>(st, qa, kt, vt, row0, nvalid, sc.qk, lane);
+      else zeroed = tile_step<KV, D>(st, qa, kt, vt, row0, nvalid, sc.qk, lane);
+    }
+    if (zeroed) fence_proxy_async();  // the zeroed rows, before the slot is refilled by TMA
     if (__syncthreads_or(!arrived)) {
       timed_out = true;
       stalled_at = tile;
@@ -657,7 +878,8 @@ __global__ void __launch_bounds__(kThreads, 3)
   float* mS = reinterpret_cast<float*>(smem);  // stages are idle now
   float* lS = mS + kWarps * 16;
   float* oS = lS + kWarps * 16;                // [warp][16 rows][D]
-  publish<KV, D>(st, mS, lS, oS, warp, G, 16, lane);
+  if constexpr (HC) publish_t<KV, D>(st, mS, lS, oS, warp, G, 16, lane);
+  else publish<KV, D>(st, mS, lS, oS, warp, G, 16, lane);
   __syncthreads();
 
   const bool any_bad = s_bad != 0;

@@ -40,17 +40,19 @@ pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
                      cudaStream_t st) {
   constexpr int NS = stages<KV, D>();
   constexpr int smem = smem_bytes<KV, D, NS>();
-  auto kernel = decode_tc_kernel<KV, Q, D, T, NS>;
-  // the shared-memory opt-in is per device
-  static std::atomic<uint64_t> configured{0};
+  // query groups of up to 8 heads take the head-columns form
+  const bool hc = a.group <= 8;
+  auto kernel = hc ? decode_tc_kernel<KV, Q, D, T, NS, true> : decode_tc_kernel<KV, Q, D, T, NS, false>;
+  // the shared-memory opt-in is per device and kernel
+  static std::atomic<uint64_t> configured[2] = {0, 0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaGetDevice", e);
   const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
-  if (!bit || !(configured.load() & bit)) {
+  if (!bit || !(configured[hc].load() & bit)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaFuncSetAttribute", e);
-    configured.fetch_or(bit);
+    configured[hc].fetch_or(bit);
   }
   const dim3 grid(a.num_kv_heads, a.num_seqs, a.max_splits);
   e = launch_dependent(kernel, grid, kThreads, smem, st, a, kmap, vmap);
