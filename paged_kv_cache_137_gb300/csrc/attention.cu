@@ -33,7 +33,9 @@ namespace {
 
 constexpr int kMinPartition = 256;
 constexpr int kMaxPartition = 8192;
-constexpr int kSplitCtasPerSm = 3;     // resident tensor-core split CTAs per SM
+// Resident tensor-core split CTAs per SM: four for E4M3 caches (the
+// head-columns kernel that every query group up to 8 takes), else three.
+int resident_split_ctas(const pkv_kv_desc* d) { return d->kv_dtype == PKV_E4M3 ? 4 : 3; }
 constexpr int kDefaultSms = 152;       // used when no device can be queried
 
 int device_sms() {
@@ -58,8 +60,9 @@ int device_sms() {
 // (sequence, head) pairs than slots, no split at all (up to the maximum).
 // Lengths are expected to spread evenly up to max_ctx, and each pair's last
 // split to be half full.
-int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx, int32_t block_size) {
-  const int64_t slots = static_cast<int64_t>(device_sms()) * kSplitCtasPerSm;
+int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx, int32_t block_size,
+                       int ctas_per_sm) {
+  const int64_t slots = static_cast<int64_t>(device_sms()) * ctas_per_sm;
   const int64_t pairs = num_seqs * num_kv_heads;
   const int64_t est_tokens = pairs * std::max<int64_t>(max_ctx, 1) / 2;
   const int32_t step = std::max<int32_t>(64, block_size);
@@ -192,7 +195,7 @@ pkv_status resolve_partition(int32_t requested, int32_t num_seqs, int32_t max_bl
     return PKV_OK;
   }
   *out = auto_partition(num_seqs, d->num_kv_heads, static_cast<int64_t>(max_blocks) * d->block_size,
-                        d->block_size);
+                        d->block_size, resident_split_ctas(d));
   return PKV_OK;
 }
 

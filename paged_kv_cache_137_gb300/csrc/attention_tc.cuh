@@ -719,9 +719,16 @@ __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit, floa
 }
 
 // ------------------------------------------------------------------ kernel
+// Resident CTAs per SM the split kernel is compiled for: four for the E4M3
+// head-columns form (126 registers, a 48 KiB ring), three otherwise.
+template <typename KV, bool HC>
+constexpr int split_ctas_per_sm() {
+  return HC && std::is_same<KV, E4M3>::value ? 4 : 3;
+}
+
 // HC: the head-columns form of the tile products (query group <= 8).
 template <typename KV, typename Q, int D, int T, int NS, bool HC>
-__global__ void __launch_bounds__(kThreads, 3)
+__global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
   using G_ = Geom<KV, D>;

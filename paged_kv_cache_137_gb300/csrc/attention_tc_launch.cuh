@@ -29,35 +29,43 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, int threads, 
   return cudaLaunchKernelEx(&cfg, kernel, std::forward<Args>(args)...);
 }
 
-// Stages per CTA: 64 KiB of ring for every cache type (three CTAs per SM).
-template <typename KV, int D>
+// Stages per CTA: 64 KiB of ring at three CTAs per SM (2 x 32 KiB or
+// 4 x 16 KiB), 48 KiB (3 x 16 KiB) at four.
+template <typename KV, int D, bool HC>
 constexpr int stages() {
-  return Geom<KV, D>::kStageBytes >= 32768 ? 2 : 4;
+  if (Geom<KV, D>::kStageBytes >= 32768) return 2;
+  return split_ctas_per_sm<KV, HC>() == 4 ? 3 : 4;
 }
 
-template <typename KV, typename Q, int D, int T>
-pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                     cudaStream_t st) {
-  constexpr int NS = stages<KV, D>();
+template <typename KV, typename Q, int D, int T, bool HC>
+pkv_status launch_form(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                       cudaStream_t st) {
+  constexpr int NS = stages<KV, D, HC>();
   constexpr int smem = smem_bytes<KV, D, NS>();
-  // query groups of up to 8 heads take the head-columns form
-  const bool hc = a.group <= 8;
-  auto kernel = hc ? decode_tc_kernel<KV, Q, D, T, NS, true> : decode_tc_kernel<KV, Q, D, T, NS, false>;
-  // the shared-memory opt-in is per device and kernel
-  static std::atomic<uint64_t> configured[2] = {0, 0};
+  auto kernel = decode_tc_kernel<KV, Q, D, T, NS, HC>;
+  // the shared-memory opt-in is per device
+  static std::atomic<uint64_t> configured{0};
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaGetDevice", e);
   const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
-  if (!bit || !(configured[hc].load() & bit)) {
+  if (!bit || !(configured.load() & bit)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
     if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaFuncSetAttribute", e);
-    configured[hc].fetch_or(bit);
+    configured.fetch_or(bit);
   }
   const dim3 grid(a.num_kv_heads, a.num_seqs, a.max_splits);
   e = launch_dependent(kernel, grid, kThreads, smem, st, a, kmap, vmap);
   if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: launch", e);
   return check_launch("pkv_attention_decode (tensor core)");
+}
+
+// query groups of up to 8 heads take the head-columns form
+template <typename KV, typename Q, int D, int T>
+pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                     cudaStream_t st) {
+  return a.group <= 8 ? launch_form<KV, Q, D, T, true>(a, kmap, vmap, st)
+                      : launch_form<KV, Q, D, T, false>(a, kmap, vmap, st);
 }
 
 // Stream-K kernel: a.ctas CTAs (three per SM, one wave), 64 KiB ring each.
