@@ -666,7 +666,7 @@ def run_prefill_gpu(args, world, rank, local):
                    "launch": "the K steps captured back to back in one CUDA graph, replayed once",
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": round(world * total_q / (ms / 1e3), 1),
-        "roofline": {"bound": "tensor", "kernel": "prefill_tc_kernel (mma.sync m16n8k16)",
+        "roofline": {"bound": "tensor", "kernel": "prefill_umma_kernel (tcgen05.mma, TMEM accumulators)" if w.head_dim == 128 and w.kv_dtype in ("bf16", "f16") else "prefill_tc_kernel (mma.sync m16n8k16)",
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} bf16 burst",
                      "traffic": None, "attention_ms": round(attn, 4)},

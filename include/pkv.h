@@ -368,6 +368,17 @@ PKV_API pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_dty
                                          float softmax_scale, float k_scale, float v_scale,
                                          void* stream);
 
+/* Prefill kernel choice, process-wide: PKV_PREFILL_AUTO (tcgen05 UMMA with
+ * TMEM accumulators for 16-bit caches with head_dim 128, the mma.sync kernel
+ * otherwise), PKV_PREFILL_MMA_SYNC (always the mma.sync kernel) or
+ * PKV_PREFILL_TCGEN05 (the tcgen05 kernel; other caches then return
+ * PKV_ERR_UNSUPPORTED).  Both compute the same attention; their results
+ * differ by rounding only.  PKV_ERR_INVALID_ARG for another value. */
+#define PKV_PREFILL_AUTO 0
+#define PKV_PREFILL_MMA_SYNC 1
+#define PKV_PREFILL_TCGEN05 2
+PKV_API pkv_status pkv_set_prefill_kernel(int32_t kind);
+
 /* ---------------------------------------------------------- prefix caching
  * [F "The knobs"]: enable_prefix_caching hashes each filled block so that
  * unrelated requests share physical blocks; [F "Failure modes"]: sharing is

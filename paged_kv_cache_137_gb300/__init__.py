@@ -108,6 +108,7 @@ _SIGNATURES = {
     "pkv_attention_decode": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F, _F, _F,
                                     _I32, _P, ctypes.c_size_t, _P]),
     "pkv_set_attention_kernel": (_I32, [_I32]),
+    "pkv_set_prefill_kernel": (_I32, [_I32]),
     "pkv_attention_decode_noalloc": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F,
                                             _F, _F, _I32, _P]),
     "pkv_attention_prefill": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _P, _I32, _I32, _I32, _I32,
@@ -408,6 +409,14 @@ def pkv_attention_partition(num_seqs, max_blocks, desc: pkv_kv_desc, partition_t
 def pkv_set_attention_kernel(kind) -> None:
     """Process-wide decode kernel choice: "auto", "simt", "tc" or "persistent"."""
     _check(lib().pkv_set_attention_kernel(KERNEL_OF_NAME.get(kind, kind)))
+
+
+PREFILL_KERNEL_OF_NAME = {"auto": 0, "mma_sync": 1, "tcgen05": 2}
+
+
+def pkv_set_prefill_kernel(kind) -> None:
+    """Process-wide prefill kernel choice: "auto", "mma_sync" or "tcgen05"."""
+    _check(lib().pkv_set_prefill_kernel(PREFILL_KERNEL_OF_NAME.get(kind, kind)))
 
 
 def workspace_for(num_seqs, num_q_heads, max_blocks, desc, partition_tokens=0, device="cuda"):

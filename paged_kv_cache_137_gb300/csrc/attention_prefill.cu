@@ -419,6 +419,48 @@ pkv_status launch_prefill_dt(const PrefillArgs& a, const CUtensorMap& kmap,
   return check_launch("pkv_attention_prefill");
 }
 
+}  // namespace tc
+}  // namespace pkv
+
+#include "attention_prefill_umma.cuh"
+
+namespace pkv {
+namespace tc {
+
+// Process-wide prefill kernel choice (pkv_set_prefill_kernel).
+std::atomic<int> g_prefill_choice{PKV_PREFILL_AUTO};
+
+template <typename KV, typename Q, int T>
+pkv_status launch_prefill_umma(PrefillArgs a, const CUtensorMap& kmap, const CUtensorMap& vmap,
+                               int32_t max_query_len, cudaStream_t st) {
+  constexpr int smem = umma::smem_bytes<T>();
+  auto kernel = umma::prefill_umma_kernel<KV, Q, T>;
+  static std::atomic<uint64_t> configured{0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return cuda_fail("pkv_attention_prefill: cudaGetDevice", e);
+  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
+  if (!bit || !(configured.load() & bit)) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e != cudaSuccess) return cuda_fail("pkv_attention_prefill: cudaFuncSetAttribute", e);
+    configured.fetch_or(bit);
+  }
+  a.max_q_tiles = (max_query_len + umma::kRows - 1) / umma::kRows;
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.max_q_tiles, a.num_q_heads, a.num_seqs);
+  cfg.blockDim = dim3(umma::kThreadsU);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, kernel, a, kmap, vmap);
+  if (e != cudaSuccess) return cuda_fail("pkv_attention_prefill: launch", e);
+  return check_launch("pkv_attention_prefill (tcgen05)");
+}
+
 template <typename KV, typename Q>
 pkv_status launch_prefill(const PrefillArgs& a, int D, int T, const CUtensorMap& kmap,
                           const CUtensorMap& vmap, cudaStream_t st) {
@@ -500,8 +542,26 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim, T = desc->block_size;
+  // 16-bit caches with head_dim 128 run on tcgen05 unless the mma.sync kernel is chosen
+  const int choice = tc::g_prefill_choice.load();
+  if (kv != PKV_E4M3 && D == 128 && choice != PKV_PREFILL_MMA_SYNC) {
+    if (kv == PKV_BF16)
+      return T == 16 ? tc::launch_prefill_umma<BF16, BF16, 16>(a, kmap, vmap, max_query_len, s)
+                     : tc::launch_prefill_umma<BF16, BF16, 32>(a, kmap, vmap, max_query_len, s);
+    return T == 16 ? tc::launch_prefill_umma<F16, F16, 16>(a, kmap, vmap, max_query_len, s)
+                   : tc::launch_prefill_umma<F16, F16, 32>(a, kmap, vmap, max_query_len, s);
+  }
+  if (choice == PKV_PREFILL_TCGEN05)
+    return fail(PKV_ERR_UNSUPPORTED, "the tcgen05 prefill kernel needs a 16-bit cache and head_dim 128");
   if (kv == PKV_BF16) return tc::launch_prefill<BF16, BF16>(a, D, T, kmap, vmap, s);
   if (kv == PKV_F16) return tc::launch_prefill<F16, F16>(a, D, T, kmap, vmap, s);
   return q_dtype == PKV_F16 ? tc::launch_prefill<E4M3, F16>(a, D, T, kmap, vmap, s)
                             : tc::launch_prefill<E4M3, BF16>(a, D, T, kmap, vmap, s);
+}
+
+extern "C" pkv_status pkv_set_prefill_kernel(int32_t kind) {
+  if (kind != PKV_PREFILL_AUTO && kind != PKV_PREFILL_MMA_SYNC && kind != PKV_PREFILL_TCGEN05)
+    return fail(PKV_ERR_INVALID_ARG, "unknown prefill kernel kind");
+  tc::g_prefill_choice.store(kind);
+  return PKV_OK;
 }

@@ -1,0 +1,477 @@
+// Prefill attention on the 5th-generation tensor cores (tcgen05 / UMMA with
+// TMEM accumulators), 16-bit caches, head_dim 128.
+//
+// Same computation as prefill_tc_kernel (the chunk's queries attend causally
+// over the cached positions through the block table); this is the GB300 form:
+//  * One CTA per (128-query tile, query head, sequence), 6 warps:
+//      warps 0-3  softmax: thread r owns query row r (TMEM lane r);
+//      warp 4     TMA producer of the K/V ring, TMEM allocation;
+//      warp 5     MMA issuer (one thread).
+//  * Per 64-key tile t:  S_t = Q K_t^T (M 128, N 64, K 128: 8 UMMAs) into one of
+//    two TMEM S buffers; the softmax threads read their S row (tcgen05.ld),
+//    apply the causal mask and the online softmax, write P_t (16-bit) to a
+//    shared-memory buffer in the 128-byte-swizzled K-major layout; then
+//    O += P_t V_t (M 128, N 128, K 64: 4 UMMAs, V read N-major) into TMEM.
+//    S_{t+1} is issued before P_t V_t, so the tensor core works on the next
+//    tile while the softmax threads work on this one.
+//  * O stays in TMEM.  A row's reference maximum moves only when the running
+//    maximum exceeds it by more than 8 (log2 units): then that row of O is
+//    read, scaled and written back (after the previous P V has completed).
+//    P = 2^(s - m_ref) <= 2^8 in between; the final O / l uses the same
+//    reference, so the result is the softmax whichever references were used.
+//  * Q is loaded by the softmax threads into the 128-byte-swizzled K-major
+//    layout; K and V arrive by 2-D TMA boxes of T rows x 128 bytes per
+//    (block, slab), the layout the UMMA shared-memory descriptors describe.
+//  * V rows at positions >= ctx are zeroed in shared memory before P V
+//    (0 * NaN would poison the product; the mask already zeroes P there).
+//  * Every mbarrier wait is bounded; a CTA whose wait gives up writes NaN
+//    rows, waits (bounded) for its copies and MMAs in flight, and frees its
+//    TMEM before it exits.
+
+namespace pkv {
+namespace tc {
+namespace umma {
+
+constexpr int kRows = 128;       // query rows per CTA (UMMA M)
+constexpr int kKeys = 64;        // keys per tile (UMMA N of S)
+constexpr int kStages = 3;       // K/V ring depth
+constexpr int kThreadsU = 192;   // 4 softmax warps, the producer warp, the MMA warp
+constexpr int kTmemCols = 256;   // S0 [0, 64), S1 [64, 128), O [128, 256)
+constexpr int kQBytes = kRows * 256;          // two slabs of 128 rows x 128 bytes
+constexpr int kSlab = kKeys * 128;            // one slab of a K or V tile
+constexpr int kKVBytes = 2 * kSlab;           // K (or V) tile: 64 rows x 256 bytes
+constexpr int kStageBytes = 2 * kKVBytes;     // K then V
+constexpr int kPBytes = kRows * 128;          // P: 128 rows x 64 keys x 2 bytes
+constexpr float kRescaleLog2 = 8.f;
+
+// ---------------------------------------------------------------- PTX
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
+}
+
+// D[tmem] (+)= A[smem desc] x B[smem desc], kind::f16, one CTA.
+__device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                     uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// Arrive on an mbarrier once every UMMA this thread issued so far is done.
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
+  asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
+               "r"(ncols)
+               : "memory");
+}
+__device__ __forceinline__ void tmem_relinquish() {
+  asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
+  asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
+               : "memory");
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading
+// and stride byte offsets (16-byte units), descriptor version 1, layout
+// type 2 (128-byte swizzle).  K-major operands: rows of 128 bytes, 8-row
+// groups SBO apart (the leading offset is not used).  N-major operands
+// (V): LBO between 64-element column blocks, SBO between 8-row groups.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = static_cast<uint64_t>((saddr >> 4) & 0x3FFFu);
+  d |= static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16;
+  d |= static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32;
+  d |= uint64_t{1} << 46;
+  d |= uint64_t{2} << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp32 accumulator, A and B both bf16
+// (or both f16), A K-major, B K-major or N-major, shape M x N.
+constexpr uint32_t idesc(bool bf, int M, int N, bool b_n_major) {
+  return (1u << 4) | (static_cast<uint32_t>(bf) << 7) | (static_cast<uint32_t>(bf) << 10) |
+         (static_cast<uint32_t>(b_n_major) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+
+// Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled
+// block of 128-byte rows (1024-byte aligned).
+__device__ __forceinline__ uint32_t sw(int r, int c) {
+  return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
+}
+
+template <int T>
+constexpr int smem_bytes() {
+  return kQBytes + kStages * kStageBytes + 2 * kPBytes + 256 + 1024;
+}
+
+template <typename KV, typename Q, int T>
+__global__ void __launch_bounds__(kThreadsU, 1)
+    prefill_umma_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap kmap,
+                        const __grid_constant__ CUtensorMap vmap) {
+  constexpr int D = 128;
+  constexpr bool kBf = std::is_same<KV, BF16>::value;
+  constexpr bool kOutBf = std::is_same<Q, BF16>::value;
+  constexpr int BPT = kKeys / T;   // blocks per key tile
+  constexpr uint32_t kIdQK = idesc(kBf, kRows, kKeys, false);
+  constexpr uint32_t kIdPV = idesc(kBf, kRows, D, true);
+
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+
+  const int qt_rev = blockIdx.x, j = blockIdx.y, s = blockIdx.z;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int HQ = a.num_q_heads;
+  const int ctx = a.ctx_lens[s];
+  const int q0 = a.query_start[s];
+  const int n = a.query_start[s + 1] - q0;
+  if (q0 < 0 || n <= 0 || q0 + n > a.total_q) return;  // no rows this CTA may write
+  const bool bad_len = ctx < 0 || ctx > a.max_blocks * T || n > ctx ||
+                       (n + kRows - 1) / kRows > a.max_q_tiles;
+  if (bad_len) {  // invalid lengths: the chunk's rows of head j become NaN
+    if (qt_rev == 0)
+      for (int i = tid; i < n * D; i += kThreadsU)
+        store_elem<Q>(a.out, (static_cast<size_t>(q0 + i / D) * HQ + j) * D + i % D, CUDART_NAN_F);
+    return;
+  }
+  const int ntq = (n + kRows - 1) / kRows;
+  if (qt_rev >= ntq) return;
+  const int qt = ntq - 1 - qt_rev;
+  const int first = ctx - n;                 // position of the chunk's first query
+  const int r_begin = qt * kRows;            // chunk row of the tile's first query
+  const int r_end = min(r_begin + kRows, n);
+  const int kv_end = first + r_end;          // keys 0 .. kv_end - 1
+  const int n_tiles = (kv_end + kKeys - 1) / kKeys;
+  const int kvh = j / a.group;
+  const HeadScales hs = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale, a.qk_scale,
+                                    a.v_scale, 1.f, 1.f);
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* q_s = smem;                                   // [2 slabs][128 rows][128 B]
+  uint8_t* ring = smem + kQBytes;                        // [stage][K slab0, K slab1, V slab0, V slab1]
+  uint8_t* p_s = ring + kStages * kStageBytes;           // [2][128 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p_s + 2 * kPBytes);
+  uint64_t* full = bars;                 // [kStages] K/V landed (TMA)
+  uint64_t* empty = bars + kStages;      // [kStages] P V of the stage done (commit)
+  uint64_t* s_full = empty + kStages;    // [2] S buffer written (commit)
+  uint64_t* s_free = s_full + 2;         // [2] S buffer read by the 128 softmax threads
+  uint64_t* p_full = s_free + 2;         // [2] P buffer written by the 128 softmax threads
+  uint64_t* o_done = p_full + 2;         // [2] P V of a tile done (commit)
+  uint64_t* fin = o_done + 2;            // every UMMA done (commit)
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+  __shared__ int s_bad;
+
+  if (tid == 0) {
+    s_bad = 0;
+    for (int i = 0; i < kStages; ++i) {
+      mbar_init(smem_u32(&full[i]), 1);
+      mbar_init(smem_u32(&empty[i]), 1);
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&s_full[i]), 1);
+      mbar_init(smem_u32(&s_free[i]), kRows);
+      mbar_init(smem_u32(&p_full[i]), kRows);
+      mbar_init(smem_u32(&o_done[i]), 1);
+    }
+    mbar_init(smem_u32(fin), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 4) {
+    __syncwarp();
+    tmem_alloc(smem_u32(tmem_slot), kTmemCols);
+    tmem_relinquish();
+  }
+
+  // Q rows (softmax threads): row r = chunk row r_begin + r, zero past the
+  // chunk's end, 128-byte-swizzled into two slabs
+  if (warp < 4) {
+    const int r = tid;
+    const int cr = r_begin + r;
+    const uint4* src = reinterpret_cast<const uint4*>(static_cast<const typename Q::raw*>(a.q) +
+                                                      (static_cast<size_t>(q0 + cr) * HQ + j) * D);
+#pragma unroll
+    for (int c = 0; c < 16; ++c) {
+      const uint4 v = cr < n ? src[c] : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kRows * 128) + sw(r, c & 7)) = v;
+    }
+    fence_proxy_async();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tS[2] = {tmem, tmem + 64};
+  const uint32_t tO = tmem + 128;
+
+  if (warp == 4) {
+    // ------------------------------------------------------------ producer
+    if (lane == 0) {
+      for (int t = 0; t < n_tiles; ++t) {
+        const int slot = t % kStages;
+        if (t >= kStages &&
+            !mbar_wait(smem_u32(&empty[slot]), ((t / kStages) - 1) & 1, kWaitNs)) {
+          s_bad = 1;
+          break;
+        }
+        uint8_t* st = ring + slot * kStageBytes;
+        int ids[BPT];
+        int nbox = 0;
+        for (int b = 0; b < BPT; ++b) {
+          const int lb = (t * kKeys) / T + b;
+          ids[b] = -1;
+          if (lb * T < ctx) {
+            const int id = a.tables[static_cast<size_t>(s) * a.max_blocks + lb];
+            if (id < 0 || id >= a.num_blocks) s_bad = 1;
+            else {
+              ids[b] = id;
+              ++nbox;
+            }
+          }
+        }
+        const uint32_t bar = smem_u32(&full[slot]);
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox) * 4u * (T * 128));
+        for (int b = 0; b < BPT; ++b) {
+          if (ids[b] < 0) continue;
+          const int row = (ids[b] * a.num_kv_heads + kvh) * T;
+          for (int sl = 0; sl < 2; ++sl) {
+            tma_load_2d(smem_u32(st + sl * kSlab + b * T * 128), &kmap, sl * 128, row, bar);
+            tma_load_2d(smem_u32(st + kKVBytes + sl * kSlab + b * T * 128), &vmap, sl * 128, row, bar);
+          }
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------------ MMA issuer
+    if (lane == 0) {
+      const uint32_t q_addr = smem_u32(q_s);
+      auto pv = [&](int t) -> bool {  // O += P_t V_t
+        const int b = t & 1;
+        if (!mbar_wait(smem_u32(&p_full[b]), (t >> 1) & 1, kWaitNs)) return false;
+        tc_fence_after();
+        const uint32_t p_addr = smem_u32(p_s + b * kPBytes);
+        const uint32_t v_addr = smem_u32(ring + (t % kStages) * kStageBytes + kKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          umma(tO, sw128_desc(p_addr + 32 * kk, 16, 1024), sw128_desc(v_addr + 2048 * kk, kSlab, 1024),
+               kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(smem_u32(&o_done[b]));
+        umma_commit(smem_u32(&empty[t % kStages]));
+        return true;
+      };
+      bool ok = true;
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        const int slot = t % kStages, b = t & 1;
+        ok = mbar_wait(smem_u32(&full[slot]), (t / kStages) & 1, kWaitNs) &&
+             (t < 2 || mbar_wait(smem_u32(&s_free[b]), ((t >> 1) - 1) & 1, kWaitNs));
+        if (!ok) break;
+        tc_fence_after();
+        const uint32_t k_addr = smem_u32(ring + slot * kStageBytes);
+#pragma unroll
+        for (int ks = 0; ks < D / 16; ++ks)
+          umma(tS[b], sw128_desc(q_addr + (ks >> 2) * (kRows * 128) + 32 * (ks & 3), 16, 1024),
+               sw128_desc(k_addr + (ks >> 2) * kSlab + 32 * (ks & 3), 16, 1024), kIdQK,
+               ks > 0 ? 1u : 0u);
+        umma_commit(smem_u32(&s_full[b]));
+        if (t > 0) ok = pv(t - 1);
+      }
+      if (ok) ok = pv(n_tiles - 1);
+      if (!ok) s_bad = 1;
+      umma_commit(smem_u32(fin));
+    }
+  } else {
+    // ------------------------------------------------------------ softmax
+    // Every branch around a TMEM load or store (warp-wide, .sync.aligned)
+    // is taken by the whole warp: waits are combined with __all_sync and a
+    // row that moves its reference moves it inside a warp-wide rescale.
+    constexpr unsigned FULL = 0xffffffffu;
+    const int r = tid;                        // query row, TMEM lane
+    const int cr = r_begin + r;
+    const int pos = first + cr;               // query position
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    float m_ref = -CUDART_INF_F, l = 0.f;
+    bool ok = true;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int b = t & 1;
+      if (!__all_sync(FULL, mbar_wait(smem_u32(&s_full[b]), (t >> 1) & 1, kWaitNs))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      float sv[64];
+      {
+        float h[32];
+        tmem_ld32(tS[b] + lane_off, h);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[i] = h[i];
+        tmem_ld32(tS[b] + lane_off + 32, h);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) sv[32 + i] = h[i];
+      }
+      tc_fence_before();
+      mbar_arrive(smem_u32(&s_free[b]));
+
+      const int kb = t * kKeys;
+      float mx = -CUDART_INF_F;
+#pragma unroll
+      for (int i = 0; i < 64; ++i) {
+        const int key = kb + i;
+        const float x = (key <= pos && key < ctx) ? sv[i] * hs.qk : -CUDART_INF_F;
+        sv[i] = x;
+        mx = fmaxf(mx, x);
+      }
+      const bool move = mx > m_ref + kRescaleLog2;
+      const bool scale = move && t > 0 && m_ref != -CUDART_INF_F;  // O holds earlier tiles
+      if (__any_sync(FULL, scale)) {
+        // rows that move their reference scale their row of O (every P V so
+        // far done); the others multiply by 1
+        if (!__all_sync(FULL, mbar_wait(smem_u32(&o_done[(t - 1) & 1]), ((t - 1) >> 1) & 1, kWaitNs))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const float f = scale ? exp2f(m_ref - mx) : 1.f;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float o[32];
+          tmem_ld32(tO + lane_off + c, o);
+#pragma unroll
+          for (int i = 0; i < 32; ++i) o[i] *= f;
+          tmem_st32(tO + lane_off + c, o);
+        }
+        l *= f;
+      }
+      if (move) m_ref = mx;
+      // the P buffer is free once P_{t-2} V_{t-2} is done
+      if (t >= 2 &&
+          !__all_sync(FULL, mbar_wait(smem_u32(&o_done[b]), ((t >> 1) - 1) & 1, kWaitNs))) {
+        ok = false;
+        break;
+      }
+      uint8_t* pb = p_s + b * kPBytes;
+      float sum = 0.f;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        uint32_t w[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float p0 = exp2f(sv[8 * c + 2 * e] - m_ref);
+          const float p1 = exp2f(sv[8 * c + 2 * e + 1] - m_ref);
+          sum += p0 + p1;
+          w[e] = pack2<kBf>(p0, p1);
+        }
+        *reinterpret_cast<uint4*>(pb + sw(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+      }
+      l += sum;
+      // V rows at positions >= ctx (the tail of the last block, blocks not
+      // loaded) are zeroed: 64 rows of 2 x 128 bytes, one row per thread
+      if (kb + kKeys > ctx && r < kKeys && kb + r >= ctx) {
+        uint8_t* vt = ring + (t % kStages) * kStageBytes + kKVBytes;
+#pragma unroll
+        for (int c = 0; c < 8; ++c) {
+          *reinterpret_cast<uint4*>(vt + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+          *reinterpret_cast<uint4*>(vt + kSlab + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      fence_proxy_async();
+      tc_fence_before();
+      mbar_arrive(smem_u32(&p_full[b]));
+    }
+    // epilogue: O / l of the row, after the last P V
+    const int tl = n_tiles - 1;
+    ok = __all_sync(FULL, ok && mbar_wait(smem_u32(&o_done[tl & 1]), (tl >> 1) & 1, kWaitNs));
+    tc_fence_after();
+    if (!ok) s_bad = 1;
+    const bool bad = !ok || *reinterpret_cast<volatile int*>(&s_bad) != 0;
+    const float inv = (l > 0.f || l != l) ? hs.v / l : 0.f;
+    typename Q::raw* dst = static_cast<typename Q::raw*>(a.out) + (static_cast<size_t>(q0 + cr) * HQ + j) * D;
+#pragma unroll 1
+    for (int c = 0; c < D; c += 32) {
+      float o[32];
+      tmem_ld32(tO + lane_off + c, o);
+      if (cr < r_end) {
+        uint32_t w[16];
+#pragma unroll
+        for (int e = 0; e < 16; ++e)
+          w[e] = pack2<kOutBf>(bad ? CUDART_NAN_F : o[2 * e] * inv, bad ? CUDART_NAN_F : o[2 * e + 1] * inv);
+        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+      }
+    }
+  }
+
+  // ---------------------------------------------------------------- exit
+  // every UMMA done and every copy landed before TMEM and shared memory go
+  __syncthreads();
+  if (tid == 0) {
+    mbar_wait(smem_u32(fin), 0, kDrainNs);
+    if (s_bad)
+      for (int t = max(0, n_tiles - kStages); t < n_tiles; ++t)
+        mbar_wait(smem_u32(&full[t % kStages]), (t / kStages) & 1, kDrainNs);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 4) {
+    __syncwarp();
+    tmem_dealloc(tmem, kTmemCols);
+  }
+}
+
+}  // namespace umma
+}  // namespace tc
+}  // namespace pkv

@@ -98,13 +98,51 @@ def check(got, ref, kv_dtype="bf16"):
         assert err.mean() <= mean_tol, f"mean abs error {err.mean():.3g}"
 
 
+@pytest.fixture(params=["auto", "mma_sync"])
+def prefill_kernel(request):
+    """Run a test with the default choice (tcgen05 UMMA for 16-bit caches with
+    head_dim 128) and with the mma.sync kernel forced."""
+    pkv.pkv_set_prefill_kernel(request.param)
+    yield request.param
+    pkv.pkv_set_prefill_kernel("auto")
+
+
 @pytest.mark.parametrize("name", list(CASES))
 @pytest.mark.parametrize("chunk", [1, 37, 64, 200, 10 ** 6])
-def test_prefill_matches_oracle(name, chunk):
+def test_prefill_matches_oracle(name, chunk, prefill_kernel):
     dev, scn = state(name)
     n = W.chunk_lens(dev.plan.w, dev.plan.ctx, chunk)
     q, qs = chunk_inputs(dev, n)
     check(run_prefill(dev, q, qs), oracle(scn, q, qs), dev.plan.w.kv_dtype)
+
+
+@pytest.mark.parametrize("name", ["qwen_small", "qwen_small_f16", "mha_t32"])
+def test_tcgen05_and_mma_sync_kernels_agree(name):
+    """The two prefill kernels compute the same attention (rounding apart)."""
+    dev, _ = state(name)
+    n = W.chunk_lens(dev.plan.w, dev.plan.ctx, 300)
+    q, qs = chunk_inputs(dev, n)
+    outs = []
+    for kind in ("tcgen05", "mma_sync"):
+        pkv.pkv_set_prefill_kernel(kind)
+        try:
+            outs.append(run_prefill(dev, q, qs).double())
+        finally:
+            pkv.pkv_set_prefill_kernel("auto")
+    err = (outs[0] - outs[1]).abs()
+    assert not torch.isnan(outs[0]).any() and err.max().item() <= 2e-2
+
+
+def test_tcgen05_choice_rejects_other_caches():
+    dev, _ = state("gqa16_d64")
+    n = W.chunk_lens(dev.plan.w, dev.plan.ctx, 10)
+    q, qs = chunk_inputs(dev, n)
+    pkv.pkv_set_prefill_kernel("tcgen05")
+    try:
+        with pytest.raises(pkv.PkvError):
+            run_prefill(dev, q, qs)
+    finally:
+        pkv.pkv_set_prefill_kernel("auto")
 
 
 @pytest.mark.parametrize("name", ["qwen_small", "gqa16_d64", "fp8_small"])
