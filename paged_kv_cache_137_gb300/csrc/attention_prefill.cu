@@ -433,7 +433,7 @@ std::atomic<int> g_prefill_choice{PKV_PREFILL_AUTO};
 template <typename KV, typename Q, int T>
 pkv_status launch_prefill_umma(PrefillArgs a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                int32_t max_query_len, cudaStream_t st) {
-  constexpr int smem = umma::smem_bytes<T>();
+  constexpr int smem = umma::smem_bytes();
   auto kernel = umma::prefill_umma_kernel<KV, Q, T>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -445,7 +445,7 @@ pkv_status launch_prefill_umma(PrefillArgs a, const CUtensorMap& kmap, const CUt
     if (e != cudaSuccess) return cuda_fail("pkv_attention_prefill: cudaFuncSetAttribute", e);
     configured.fetch_or(bit);
   }
-  a.max_q_tiles = (max_query_len + umma::kRows - 1) / umma::kRows;
+  a.max_q_tiles = ((max_query_len + umma::kRows - 1) / umma::kRows + 1) / 2;  // pairs of query tiles
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(a.max_q_tiles, a.num_q_heads, a.num_seqs);
   cfg.blockDim = dim3(umma::kThreadsU);

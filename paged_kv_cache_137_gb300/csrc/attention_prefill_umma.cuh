@@ -3,17 +3,22 @@
 //
 // Same computation as prefill_tc_kernel (the chunk's queries attend causally
 // over the cached positions through the block table); this is the GB300 form:
-//  * One CTA per (128-query tile, query head, sequence), 6 warps:
-//      warps 0-3  softmax: thread r owns query row r (TMEM lane r);
-//      warp 4     TMA producer of the K/V ring, TMEM allocation;
-//      warp 5     MMA issuer (one thread).
+//  * One CTA per (pair of 128-query tiles, query head, sequence), 10 warps:
+//      warps 0-3  softmax of query tile A: thread r owns row r (TMEM lane r);
+//      warps 4-7  softmax of query tile B (the next 128 positions);
+//      warp 8     TMA producer of the K/V ring, TMEM allocation;
+//      warp 9     MMA issuer (one thread).
+//    Both query tiles use every K/V tile the ring brings (B's last one or
+//    two only it), and each SM sub-partition holds two softmax warps, one
+//    per tile, so one works while the other waits on its loads.
 //  * Per 64-key tile t:  S_t = Q K_t^T (M 128, N 64, K 128: 8 UMMAs) into one of
 //    two TMEM S buffers; the softmax threads read their S row (tcgen05.ld),
 //    apply the causal mask and the online softmax, write P_t (16-bit) to a
 //    shared-memory buffer in the 128-byte-swizzled K-major layout; then
 //    O += P_t V_t (M 128, N 128, K 64: 4 UMMAs, V read N-major) into TMEM.
-//    S_{t+1} is issued before P_t V_t, so the tensor core works on the next
-//    tile while the softmax threads work on this one.
+//    S_{t+2} is issued right after P_t V_t, so the tensor core works two
+//    tiles ahead while the softmax threads work on this one, and a K/V load
+//    that is late holds up only the S product that needs it.
 //  * O stays in TMEM.  A row's reference maximum moves only when the running
 //    maximum exceeds it by more than 8 (log2 units): then that row of O is
 //    read, scaled and written back (after the previous P V has completed).
@@ -32,11 +37,11 @@ namespace pkv {
 namespace tc {
 namespace umma {
 
-constexpr int kRows = 128;       // query rows per CTA (UMMA M)
+constexpr int kRows = 128;       // query rows per query tile (UMMA M)
 constexpr int kKeys = 64;        // keys per tile (UMMA N of S)
 constexpr int kStages = 3;       // K/V ring depth
-constexpr int kThreadsU = 192;   // 4 softmax warps, the producer warp, the MMA warp
-constexpr int kTmemCols = 256;   // S0 [0, 64), S1 [64, 128), O [128, 256)
+constexpr int kThreadsU = 320;   // 2 x 4 softmax warps, the producer warp, the MMA warp
+constexpr int kTmemCols = 512;   // per query tile X: S0 [256X, +64), S1 [+64, +64), O [+128, +128)
 constexpr int kQBytes = kRows * 256;          // two slabs of 128 rows x 128 bytes
 constexpr int kSlab = kKeys * 128;            // one slab of a K or V tile
 constexpr int kKVBytes = 2 * kSlab;           // K (or V) tile: 64 rows x 256 bytes
@@ -84,6 +89,33 @@ __device__ __forceinline__ void tmem_relinquish() {
 __device__ __forceinline__ void tmem_dealloc(uint32_t taddr, uint32_t ncols) {
   asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols)
                : "memory");
+}
+
+// 2^x by the hardware approximation (ex2.approx.ftz: relative error about
+// 2^-22, -inf gives 0), for the softmax exponentials.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+// 32 consecutive fp32 columns of this thread's TMEM lane, without waiting
+// for them (tmem_wait_ld before use).
+__device__ __forceinline__ void tmem_ld32_async(uint32_t taddr, uint32_t (&r)[32]) {
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]),
+        "=r"(r[14]), "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]),
+        "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]),
+        "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr)
+      : "memory");
+}
+__device__ __forceinline__ void tmem_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
 }
 
 // 32 consecutive fp32 columns of this thread's TMEM lane.
@@ -153,9 +185,8 @@ __device__ __forceinline__ uint32_t sw(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
-template <int T>
 constexpr int smem_bytes() {
-  return kQBytes + kStages * kStageBytes + 2 * kPBytes + 256 + 1024;
+  return 2 * kQBytes + kStages * kStageBytes + 4 * kPBytes + 512 + 1024;
 }
 
 template <typename KV, typename Q, int T>
@@ -168,32 +199,39 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   constexpr int BPT = kKeys / T;   // blocks per key tile
   constexpr uint32_t kIdQK = idesc(kBf, kRows, kKeys, false);
   constexpr uint32_t kIdPV = idesc(kBf, kRows, D, true);
+  constexpr int kProd = 8, kMma = 9;  // warps
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const int qt_rev = blockIdx.x, j = blockIdx.y, s = blockIdx.z;
+  const int qp_rev = blockIdx.x, j = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int HQ = a.num_q_heads;
   const int ctx = a.ctx_lens[s];
   const int q0 = a.query_start[s];
   const int n = a.query_start[s + 1] - q0;
   if (q0 < 0 || n <= 0 || q0 + n > a.total_q) return;  // no rows this CTA may write
-  const bool bad_len = ctx < 0 || ctx > a.max_blocks * T || n > ctx ||
-                       (n + kRows - 1) / kRows > a.max_q_tiles;
+  const int ntq = (n + kRows - 1) / kRows;       // query tiles of the chunk
+  const int npairs = (ntq + 1) / 2;
+  const bool bad_len = ctx < 0 || ctx > a.max_blocks * T || n > ctx || npairs > a.max_q_tiles;
   if (bad_len) {  // invalid lengths: the chunk's rows of head j become NaN
-    if (qt_rev == 0)
+    if (qp_rev == 0)
       for (int i = tid; i < n * D; i += kThreadsU)
         store_elem<Q>(a.out, (static_cast<size_t>(q0 + i / D) * HQ + j) * D + i % D, CUDART_NAN_F);
     return;
   }
-  const int ntq = (n + kRows - 1) / kRows;
-  if (qt_rev >= ntq) return;
-  const int qt = ntq - 1 - qt_rev;
-  const int first = ctx - n;                 // position of the chunk's first query
-  const int r_begin = qt * kRows;            // chunk row of the tile's first query
-  const int r_end = min(r_begin + kRows, n);
-  const int kv_end = first + r_end;          // keys 0 .. kv_end - 1
-  const int n_tiles = (kv_end + kKeys - 1) / kKeys;
+  if (qp_rev >= npairs) return;
+  const int qp = npairs - 1 - qp_rev;
+  const int first = ctx - n;                      // position of the chunk's first query
+  // query tile X (0 = A, 1 = B): chunk rows r_begin[X] .. r_end[X] - 1
+  const bool hasB = 2 * qp + 1 < ntq;
+  int r_begin[2], r_end[2], nt[2];
+#pragma unroll
+  for (int X = 0; X < 2; ++X) {
+    r_begin[X] = (2 * qp + X) * kRows;
+    r_end[X] = min(r_begin[X] + kRows, n);
+    nt[X] = (X == 1 && !hasB) ? 0 : (first + r_end[X] + kKeys - 1) / kKeys;  // key tiles
+  }
+  const int n_tiles = max(nt[0], nt[1]);
   const int kvh = j / a.group;
   const HeadScales hs = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale, a.qk_scale,
                                     a.v_scale, 1.f, 1.f);
@@ -201,17 +239,17 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  uint8_t* q_s = smem;                                   // [2 slabs][128 rows][128 B]
-  uint8_t* ring = smem + kQBytes;                        // [stage][K slab0, K slab1, V slab0, V slab1]
-  uint8_t* p_s = ring + kStages * kStageBytes;           // [2][128 rows][128 B]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(p_s + 2 * kPBytes);
+  uint8_t* q_s = smem;                                  // [X][2 slabs][128 rows][128 B]
+  uint8_t* ring = smem + 2 * kQBytes;                   // [stage][K slab0, K slab1, V slab0, V slab1]
+  uint8_t* p_s = ring + kStages * kStageBytes;          // [X][2][128 rows][128 B]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(p_s + 4 * kPBytes);
   uint64_t* full = bars;                 // [kStages] K/V landed (TMA)
-  uint64_t* empty = bars + kStages;      // [kStages] P V of the stage done (commit)
-  uint64_t* s_full = empty + kStages;    // [2] S buffer written (commit)
-  uint64_t* s_free = s_full + 2;         // [2] S buffer read by the 128 softmax threads
-  uint64_t* p_full = s_free + 2;         // [2] P buffer written by the 128 softmax threads
-  uint64_t* o_done = p_full + 2;         // [2] P V of a tile done (commit)
-  uint64_t* fin = o_done + 2;            // every UMMA done (commit)
+  uint64_t* empty = bars + kStages;      // [kStages] every P V reading the stage done (commit)
+  uint64_t* s_full = empty + kStages;    // [X][2] S buffer written (commit)
+  uint64_t* s_free = s_full + 4;         // [X][2] S buffer read by the tile's 128 softmax threads
+  uint64_t* p_full = s_free + 4;         // [X][2] P buffer written by the tile's 128 softmax threads
+  uint64_t* o_done = p_full + 4;         // [X][2] P V of a key tile done (commit)
+  uint64_t* fin = o_done + 4;            // every UMMA done (commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
   __shared__ int s_bad;
 
@@ -221,7 +259,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), 1);
     }
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < 4; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
       mbar_init(smem_u32(&s_free[i]), kRows);
       mbar_init(smem_u32(&p_full[i]), kRows);
@@ -230,23 +268,25 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     mbar_init(smem_u32(fin), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 4) {
+  if (warp == kProd) {
     __syncwarp();
     tmem_alloc(smem_u32(tmem_slot), kTmemCols);
     tmem_relinquish();
   }
 
-  // Q rows (softmax threads): row r = chunk row r_begin + r, zero past the
-  // chunk's end, 128-byte-swizzled into two slabs
-  if (warp < 4) {
-    const int r = tid;
-    const int cr = r_begin + r;
+  // Q rows (softmax threads of tile X): row r = chunk row r_begin[X] + r, zero
+  // past the chunk's end, 128-byte-swizzled into two slabs
+  if (warp < 8) {
+    const int X = warp >> 2, r = tid & 127;
+    const int cr = r_begin[X] + r;
+    const bool in = cr < n && (X == 0 || hasB);
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const typename Q::raw*>(a.q) +
                                                       (static_cast<size_t>(q0 + cr) * HQ + j) * D);
+    uint8_t* qx = q_s + X * kQBytes;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const uint4 v = cr < n ? src[c] : make_uint4(0, 0, 0, 0);
-      *reinterpret_cast<uint4*>(q_s + (c >> 3) * (kRows * 128) + sw(r, c & 7)) = v;
+      const uint4 v = in ? src[c] : make_uint4(0, 0, 0, 0);
+      *reinterpret_cast<uint4*>(qx + (c >> 3) * (kRows * 128) + sw(r, c & 7)) = v;
     }
     fence_proxy_async();
   }
@@ -254,10 +294,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
-  const uint32_t tS[2] = {tmem, tmem + 64};
-  const uint32_t tO = tmem + 128;
 
-  if (warp == 4) {
+  if (warp == kProd) {
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       for (int t = 0; t < n_tiles; ++t) {
@@ -294,41 +332,51 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == kMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
-      const uint32_t q_addr = smem_u32(q_s);
-      auto pv = [&](int t) -> bool {  // O += P_t V_t
-        const int b = t & 1;
-        if (!mbar_wait(smem_u32(&p_full[b]), (t >> 1) & 1, kWaitNs)) return false;
+      auto qk = [&](int X, int t) -> bool {  // S_t of tile X into its buffer t & 1
+        const int slot = t % kStages, b = t & 1, i = 2 * X + b;
+        if (!mbar_wait(smem_u32(&full[slot]), (t / kStages) & 1, kWaitNs)) return false;
+        // the buffer's previous key tile (t - 2) has been read by the softmax threads
+        if (t >= 2 && !mbar_wait(smem_u32(&s_free[i]), ((t >> 1) - 1) & 1, kWaitNs)) return false;
         tc_fence_after();
-        const uint32_t p_addr = smem_u32(p_s + b * kPBytes);
-        const uint32_t v_addr = smem_u32(ring + (t % kStages) * kStageBytes + kKVBytes);
-#pragma unroll
-        for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma(tO, sw128_desc(p_addr + 32 * kk, 16, 1024), sw128_desc(v_addr + 2048 * kk, kSlab, 1024),
-               kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
-        umma_commit(smem_u32(&o_done[b]));
-        umma_commit(smem_u32(&empty[t % kStages]));
-        return true;
-      };
-      bool ok = true;
-      for (int t = 0; t < n_tiles && ok; ++t) {
-        const int slot = t % kStages, b = t & 1;
-        ok = mbar_wait(smem_u32(&full[slot]), (t / kStages) & 1, kWaitNs) &&
-             (t < 2 || mbar_wait(smem_u32(&s_free[b]), ((t >> 1) - 1) & 1, kWaitNs));
-        if (!ok) break;
-        tc_fence_after();
+        const uint32_t q_addr = smem_u32(q_s + X * kQBytes);
         const uint32_t k_addr = smem_u32(ring + slot * kStageBytes);
 #pragma unroll
         for (int ks = 0; ks < D / 16; ++ks)
-          umma(tS[b], sw128_desc(q_addr + (ks >> 2) * (kRows * 128) + 32 * (ks & 3), 16, 1024),
+          umma(tmem + 256 * X + 64 * b,
+               sw128_desc(q_addr + (ks >> 2) * (kRows * 128) + 32 * (ks & 3), 16, 1024),
                sw128_desc(k_addr + (ks >> 2) * kSlab + 32 * (ks & 3), 16, 1024), kIdQK,
                ks > 0 ? 1u : 0u);
-        umma_commit(smem_u32(&s_full[b]));
-        if (t > 0) ok = pv(t - 1);
+        umma_commit(smem_u32(&s_full[i]));
+        return true;
+      };
+      auto pv = [&](int X, int t) -> bool {  // O_X += P_t V_t
+        const int b = t & 1, i = 2 * X + b;
+        if (!mbar_wait(smem_u32(&p_full[i]), (t >> 1) & 1, kWaitNs)) return false;
+        tc_fence_after();
+        const uint32_t p_addr = smem_u32(p_s + i * kPBytes);
+        const uint32_t v_addr = smem_u32(ring + (t % kStages) * kStageBytes + kKVBytes);
+#pragma unroll
+        for (int kk = 0; kk < kKeys / 16; ++kk)
+          umma(tmem + 256 * X + 128, sw128_desc(p_addr + 32 * kk, 16, 1024),
+               sw128_desc(v_addr + 2048 * kk, kSlab, 1024), kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
+        umma_commit(smem_u32(&o_done[i]));
+        return true;
+      };
+      bool ok = true;
+      for (int t = 0; t < 2 && ok; ++t)
+        for (int X = 0; X < 2 && ok; ++X)
+          if (t < nt[X]) ok = qk(X, t);
+      for (int t = 0; t < n_tiles && ok; ++t) {
+        for (int X = 0; X < 2 && ok; ++X)
+          if (t < nt[X]) ok = pv(X, t);
+        if (!ok) break;
+        umma_commit(smem_u32(&empty[t % kStages]));  // both tiles' P V of this stage
+        for (int X = 0; X < 2 && ok; ++X)
+          if (t + 2 < nt[X]) ok = qk(X, t + 2);
       }
-      if (ok) ok = pv(n_tiles - 1);
       if (!ok) s_bad = 1;
       umma_commit(smem_u32(fin));
     }
@@ -338,58 +386,78 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // is taken by the whole warp: waits are combined with __all_sync and a
     // row that moves its reference moves it inside a warp-wide rescale.
     constexpr unsigned FULL = 0xffffffffu;
-    const int r = tid;                        // query row, TMEM lane
-    const int cr = r_begin + r;
+    const int X = warp >> 2;                  // query tile
+    const int r = tid & 127;                  // query row, TMEM lane
+    const int cr = r_begin[X] + r;
     const int pos = first + cr;               // query position
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const int ntx = nt[X];
+    const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t tO = tmem + 256 * X + 128;
     float m_ref = -CUDART_INF_F, l = 0.f;
     bool ok = true;
-    for (int t = 0; t < n_tiles; ++t) {
-      const int b = t & 1;
-      if (!__all_sync(FULL, mbar_wait(smem_u32(&s_full[b]), (t >> 1) & 1, kWaitNs))) {
+    for (int t = 0; t < ntx; ++t) {
+      const int b = t & 1, i = 2 * X + b;
+      if (!__all_sync(FULL, mbar_wait(smem_u32(&s_full[i]), (t >> 1) & 1, kWaitNs))) {
         ok = false;
         break;
       }
       tc_fence_after();
       float sv[64];
       {
-        float h[32];
-        tmem_ld32(tS[b] + lane_off, h);
+        uint32_t h0[32], h1[32];
+        const uint32_t ts = tmem + 256 * X + 64 * b + lane_off;
+        tmem_ld32_async(ts, h0);
+        tmem_ld32_async(ts + 32, h1);
+        tmem_wait_ld();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) sv[i] = h[i];
-        tmem_ld32(tS[b] + lane_off + 32, h);
-#pragma unroll
-        for (int i = 0; i < 32; ++i) sv[32 + i] = h[i];
+        for (int e = 0; e < 32; ++e) {
+          sv[e] = __uint_as_float(h0[e]);
+          sv[32 + e] = __uint_as_float(h1[e]);
+        }
       }
       tc_fence_before();
-      mbar_arrive(smem_u32(&s_free[b]));
+      mbar_arrive(smem_u32(&s_free[i]));
 
+      // scale, mask the keys after the query (and past ctx), row maximum in
+      // eight independent chains
       const int kb = t * kKeys;
-      float mx = -CUDART_INF_F;
+      const int lim = min(pos, ctx - 1) - kb;   // keys kb + e with e <= lim are attended
+      float mx8[8];
 #pragma unroll
-      for (int i = 0; i < 64; ++i) {
-        const int key = kb + i;
-        const float x = (key <= pos && key < ctx) ? sv[i] * hs.qk : -CUDART_INF_F;
-        sv[i] = x;
-        mx = fmaxf(mx, x);
+      for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
+      if (lim >= kKeys - 1) {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          sv[e] *= hs.qk;
+          mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
+        }
+      } else {
+#pragma unroll
+        for (int e = 0; e < 64; ++e) {
+          sv[e] = e <= lim ? sv[e] * hs.qk : -CUDART_INF_F;
+          mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
+        }
       }
+      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const bool move = mx > m_ref + kRescaleLog2;
       const bool scale = move && t > 0 && m_ref != -CUDART_INF_F;  // O holds earlier tiles
       if (__any_sync(FULL, scale)) {
         // rows that move their reference scale their row of O (every P V so
         // far done); the others multiply by 1
-        if (!__all_sync(FULL, mbar_wait(smem_u32(&o_done[(t - 1) & 1]), ((t - 1) >> 1) & 1, kWaitNs))) {
+        const int ip = 2 * X + ((t - 1) & 1);
+        if (!__all_sync(FULL, mbar_wait(smem_u32(&o_done[ip]), ((t - 1) >> 1) & 1, kWaitNs))) {
           ok = false;
           break;
         }
         tc_fence_after();
-        const float f = scale ? exp2f(m_ref - mx) : 1.f;
+        const float f = scale ? ex2(m_ref - mx) : 1.f;
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
           float o[32];
           tmem_ld32(tO + lane_off + c, o);
 #pragma unroll
-          for (int i = 0; i < 32; ++i) o[i] *= f;
+          for (int e = 0; e < 32; ++e) o[e] *= f;
           tmem_st32(tO + lane_off + c, o);
         }
         l *= f;
@@ -397,28 +465,32 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       if (move) m_ref = mx;
       // the P buffer is free once P_{t-2} V_{t-2} is done
       if (t >= 2 &&
-          !__all_sync(FULL, mbar_wait(smem_u32(&o_done[b]), ((t >> 1) - 1) & 1, kWaitNs))) {
+          !__all_sync(FULL, mbar_wait(smem_u32(&o_done[i]), ((t >> 1) - 1) & 1, kWaitNs))) {
         ok = false;
         break;
       }
-      uint8_t* pb = p_s + b * kPBytes;
-      float sum = 0.f;
+      uint8_t* pb = p_s + i * kPBytes;
+      float sum8[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = exp2f(sv[8 * c + 2 * e] - m_ref);
-          const float p1 = exp2f(sv[8 * c + 2 * e + 1] - m_ref);
-          sum += p0 + p1;
+          const float p0 = ex2(sv[8 * c + 2 * e] - m_ref);
+          const float p1 = ex2(sv[8 * c + 2 * e + 1] - m_ref);
+          sum8[2 * e] += p0;
+          sum8[2 * e + 1] += p1;
           w[e] = pack2<kBf>(p0, p1);
         }
         *reinterpret_cast<uint4*>(pb + sw(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
       }
-      l += sum;
+      l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       // V rows at positions >= ctx (the tail of the last block, blocks not
-      // loaded) are zeroed: 64 rows of 2 x 128 bytes, one row per thread
-      if (kb + kKeys > ctx && r < kKeys && kb + r >= ctx) {
+      // loaded) are zeroed by tile A's threads (tile B's too when A has no
+      // such tile): 64 rows of 2 x 128 bytes, one row per thread
+      if (kb + kKeys > ctx && r < kKeys && kb + r >= ctx && (X == 0 || t >= nt[0])) {
         uint8_t* vt = ring + (t % kStages) * kStageBytes + kKVBytes;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -428,28 +500,32 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       }
       fence_proxy_async();
       tc_fence_before();
-      mbar_arrive(smem_u32(&p_full[b]));
+      mbar_arrive(smem_u32(&p_full[i]));
     }
-    // epilogue: O / l of the row, after the last P V
-    const int tl = n_tiles - 1;
-    ok = __all_sync(FULL, ok && mbar_wait(smem_u32(&o_done[tl & 1]), (tl >> 1) & 1, kWaitNs));
-    tc_fence_after();
-    if (!ok) s_bad = 1;
-    const bool bad = !ok || *reinterpret_cast<volatile int*>(&s_bad) != 0;
-    const float inv = (l > 0.f || l != l) ? hs.v / l : 0.f;
-    typename Q::raw* dst = static_cast<typename Q::raw*>(a.out) + (static_cast<size_t>(q0 + cr) * HQ + j) * D;
+    // epilogue: O / l of the row, after the tile's last P V
+    if (ntx > 0) {
+      const int tl = ntx - 1;
+      ok = __all_sync(FULL, ok && mbar_wait(smem_u32(&o_done[2 * X + (tl & 1)]), (tl >> 1) & 1, kWaitNs));
+      tc_fence_after();
+      if (!ok) s_bad = 1;
+      const bool bad = !ok || *reinterpret_cast<volatile int*>(&s_bad) != 0;
+      const float inv = (l > 0.f || l != l) ? hs.v / l : 0.f;
+      typename Q::raw* dst =
+          static_cast<typename Q::raw*>(a.out) + (static_cast<size_t>(q0 + cr) * HQ + j) * D;
 #pragma unroll 1
-    for (int c = 0; c < D; c += 32) {
-      float o[32];
-      tmem_ld32(tO + lane_off + c, o);
-      if (cr < r_end) {
-        uint32_t w[16];
+      for (int c = 0; c < D; c += 32) {
+        float o[32];
+        tmem_ld32(tO + lane_off + c, o);
+        if (cr < r_end[X]) {
+          uint32_t w[16];
 #pragma unroll
-        for (int e = 0; e < 16; ++e)
-          w[e] = pack2<kOutBf>(bad ? CUDART_NAN_F : o[2 * e] * inv, bad ? CUDART_NAN_F : o[2 * e + 1] * inv);
-        uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+          for (int e = 0; e < 16; ++e)
+            w[e] = pack2<kOutBf>(bad ? CUDART_NAN_F : o[2 * e] * inv,
+                                 bad ? CUDART_NAN_F : o[2 * e + 1] * inv);
+          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
 #pragma unroll
-        for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+        }
       }
     }
   }
@@ -466,7 +542,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if (warp == 4) {
+  if (warp == kProd) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
   }
