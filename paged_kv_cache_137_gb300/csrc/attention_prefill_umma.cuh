@@ -335,20 +335,28 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   } else if (warp == kMma) {
     // ------------------------------------------------------------ MMA issuer
     if (lane == 0) {
+      // descriptors of the operand bases; an operand's offset (16-byte
+      // units) is added to the start-address field, which never carries
+      // (shared-memory addresses are below 2^18)
+      const uint64_t q_desc = sw128_desc(smem_u32(q_s), 16, 1024);
+      const uint64_t k_desc = sw128_desc(smem_u32(ring), 16, 1024);
+      const uint64_t v_desc = sw128_desc(smem_u32(ring + kKVBytes), kSlab, 1024);
+      const uint64_t p_desc = sw128_desc(smem_u32(p_s), 16, 1024);
       auto qk = [&](int X, int t) -> bool {  // S_t of tile X into its buffer t & 1
         const int slot = t % kStages, b = t & 1, i = 2 * X + b;
         if (!mbar_wait(smem_u32(&full[slot]), (t / kStages) & 1, kWaitNs)) return false;
         // the buffer's previous key tile (t - 2) has been read by the softmax threads
         if (t >= 2 && !mbar_wait(smem_u32(&s_free[i]), ((t >> 1) - 1) & 1, kWaitNs)) return false;
         tc_fence_after();
-        const uint32_t q_addr = smem_u32(q_s + X * kQBytes);
-        const uint32_t k_addr = smem_u32(ring + slot * kStageBytes);
+        const uint64_t qd = q_desc + ((X * kQBytes) >> 4);
+        const uint64_t kd = k_desc + ((slot * kStageBytes) >> 4);
+        const uint32_t d_tmem = tmem + 256 * X + 64 * b;
 #pragma unroll
-        for (int ks = 0; ks < D / 16; ++ks)
-          umma(tmem + 256 * X + 64 * b,
-               sw128_desc(q_addr + (ks >> 2) * (kRows * 128) + 32 * (ks & 3), 16, 1024),
-               sw128_desc(k_addr + (ks >> 2) * kSlab + 32 * (ks & 3), 16, 1024), kIdQK,
-               ks > 0 ? 1u : 0u);
+        for (int ks = 0; ks < D / 16; ++ks) {
+          const uint32_t off_q = ((ks >> 2) * (kRows * 128) + 32 * (ks & 3)) >> 4;
+          const uint32_t off_k = ((ks >> 2) * kSlab + 32 * (ks & 3)) >> 4;
+          umma(d_tmem, qd + off_q, kd + off_k, kIdQK, ks > 0 ? 1u : 0u);
+        }
         umma_commit(smem_u32(&s_full[i]));
         return true;
       };
@@ -356,12 +364,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int b = t & 1, i = 2 * X + b;
         if (!mbar_wait(smem_u32(&p_full[i]), (t >> 1) & 1, kWaitNs)) return false;
         tc_fence_after();
-        const uint32_t p_addr = smem_u32(p_s + i * kPBytes);
-        const uint32_t v_addr = smem_u32(ring + (t % kStages) * kStageBytes + kKVBytes);
+        const uint64_t pd = p_desc + ((i * kPBytes) >> 4);
+        const uint64_t vd = v_desc + (((t % kStages) * kStageBytes) >> 4);
+        const uint32_t d_tmem = tmem + 256 * X + 128;
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma(tmem + 256 * X + 128, sw128_desc(p_addr + 32 * kk, 16, 1024),
-               sw128_desc(v_addr + 2048 * kk, kSlab, 1024), kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
+          umma(d_tmem, pd + ((32 * kk) >> 4), vd + ((2048 * kk) >> 4), kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(smem_u32(&o_done[i]));
         return true;
       };

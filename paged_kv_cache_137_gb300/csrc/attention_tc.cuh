@@ -96,6 +96,7 @@ __device__ __forceinline__ uint64_t global_ns() {
 // Bounded wait: false if the phase did not complete within limit_ns (or
 // 2^26 attempts, whichever comes first).
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  if (mbar_try_wait(bar, parity)) return true;  // the common case reads no timer
   const uint64_t t0 = global_ns();
   for (uint32_t i = 0; i < (1u << 26); ++i) {
     if (mbar_try_wait(bar, parity)) return true;
