@@ -542,9 +542,11 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim, T = desc->block_size;
-  // 16-bit caches with head_dim 128 run on tcgen05 unless the mma.sync kernel is chosen
+  // 16-bit caches with head_dim 128 and a positive softmax scale run on
+  // tcgen05 unless the mma.sync kernel is chosen (that kernel folds the scale
+  // into the row maximum, which needs scale > 0)
   const int choice = tc::g_prefill_choice.load();
-  if (kv != PKV_E4M3 && D == 128 && choice != PKV_PREFILL_MMA_SYNC) {
+  if (kv != PKV_E4M3 && D == 128 && softmax_scale > 0.f && choice != PKV_PREFILL_MMA_SYNC) {
     if (kv == PKV_BF16)
       return T == 16 ? tc::launch_prefill_umma<BF16, BF16, 16>(a, kmap, vmap, max_query_len, s)
                      : tc::launch_prefill_umma<BF16, BF16, 32>(a, kmap, vmap, max_query_len, s);
@@ -552,7 +554,8 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
                    : tc::launch_prefill_umma<F16, F16, 32>(a, kmap, vmap, max_query_len, s);
   }
   if (choice == PKV_PREFILL_TCGEN05)
-    return fail(PKV_ERR_UNSUPPORTED, "the tcgen05 prefill kernel needs a 16-bit cache and head_dim 128");
+    return fail(PKV_ERR_UNSUPPORTED,
+                "the tcgen05 prefill kernel needs a 16-bit cache, head_dim 128 and softmax_scale > 0");
   if (kv == PKV_BF16) return tc::launch_prefill<BF16, BF16>(a, D, T, kmap, vmap, s);
   if (kv == PKV_F16) return tc::launch_prefill<F16, F16>(a, D, T, kmap, vmap, s);
   return q_dtype == PKV_F16 ? tc::launch_prefill<E4M3, F16>(a, D, T, kmap, vmap, s)

@@ -426,28 +426,25 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&s_free[i]));
 
-      // scale, mask the keys after the query (and past ctx), row maximum in
-      // eight independent chains
+      // mask the keys after the query (and past ctx); the row maximum of the
+      // raw scores in eight independent chains, scaled once (the scale is
+      // positive, so it commutes with the maximum); the exponent below takes
+      // s * scale - m as one fused multiply-add
       const int kb = t * kKeys;
       const int lim = min(pos, ctx - 1) - kb;   // keys kb + e with e <= lim are attended
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
-      if (lim >= kKeys - 1) {
+      if (lim < kKeys - 1) {
 #pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          sv[e] *= hs.qk;
-          mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
-        }
-      } else {
-#pragma unroll
-        for (int e = 0; e < 64; ++e) {
-          sv[e] = e <= lim ? sv[e] * hs.qk : -CUDART_INF_F;
-          mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
-        }
+        for (int e = 0; e < 64; ++e)
+          if (e > lim) sv[e] = -CUDART_INF_F;
       }
-      const float mx = fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                             fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+#pragma unroll
+      for (int e = 0; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
+      // the scale is positive (the host sends other scales to the mma.sync kernel)
+      const float mx = hs.qk * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const bool move = mx > m_ref + kRescaleLog2;
       const bool scale = move && t > 0 && m_ref != -CUDART_INF_F;  // O holds earlier tiles
       if (__any_sync(FULL, scale)) {
@@ -486,8 +483,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         uint32_t w[4];
 #pragma unroll
         for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2(sv[8 * c + 2 * e] - m_ref);
-          const float p1 = ex2(sv[8 * c + 2 * e + 1] - m_ref);
+          const float p0 = ex2(fmaf(sv[8 * c + 2 * e], hs.qk, -m_ref));
+          const float p1 = ex2(fmaf(sv[8 * c + 2 * e + 1], hs.qk, -m_ref));
           sum8[2 * e] += p0;
           sum8[2 * e + 1] += p1;
           w[e] = pack2<kBf>(p0, p1);

@@ -211,3 +211,18 @@ def test_unsupported_cache_is_rejected():
                                   torch.tensor([2, 1], dtype=torch.int32, device="cuda"),
                                   torch.tensor([0, 2, 3], dtype=torch.int32, device="cuda"),
                                   desc, 0.1)
+
+
+@pytest.mark.parametrize("scale", [-0.06, 0.0])
+def test_non_positive_softmax_scale(scale):
+    """Any finite scale is attention's (the automatic choice sends scales <= 0
+    to the mma.sync kernel)."""
+    dev, scn = state("qwen_small")
+    n = W.chunk_lens(dev.plan.w, dev.plan.ctx, 150)
+    q, qs = chunk_inputs(dev, n)
+    out = torch.full_like(q, float("nan"), device="cuda")
+    pkv.pkv_attention_prefill(out, q.cuda(), dev.k_cache, dev.v_cache, dev.tables, dev.ctx,
+                              torch.from_numpy(qs).cuda(), dev.desc, scale)
+    torch.cuda.synchronize()
+    ref = OP.paged_attention_prefill(q.double().numpy(), scn.pool, scn.tables, scn.ctx, qs, scale)
+    check(out, ref)
