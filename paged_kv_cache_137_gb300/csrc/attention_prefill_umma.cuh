@@ -13,9 +13,10 @@
 //    per tile, so one works while the other waits on its loads.
 //  * Per 64-key tile t:  S_t = Q K_t^T (M 128, N 64, K 128: 8 UMMAs) into one of
 //    two TMEM S buffers; the softmax threads read their S row (tcgen05.ld),
-//    apply the causal mask and the online softmax, write P_t (16-bit) to a
-//    shared-memory buffer in the 128-byte-swizzled K-major layout; then
-//    O += P_t V_t (M 128, N 128, K 64: 4 UMMAs, V read N-major) into TMEM.
+//    apply the causal mask and the online softmax, and write P_t (16-bit
+//    pairs) back over the S buffer they read (tcgen05.st); then
+//    O += P_t V_t (M 128, N 128, K 64: 4 UMMAs with A read from TMEM, V read
+//    N-major from shared memory) into TMEM.  P never touches shared memory.
 //    S_{t+2} is issued right after P_t V_t, so the tensor core works two
 //    tiles ahead while the softmax threads work on this one, and a K/V load
 //    that is late holds up only the S product that needs it.
@@ -39,14 +40,14 @@ namespace umma {
 
 constexpr int kRows = 128;       // query rows per query tile (UMMA M)
 constexpr int kKeys = 64;        // keys per tile (UMMA N of S)
-constexpr int kStages = 3;       // K/V ring depth
+constexpr int kStages = 5;       // K/V ring depth: loads run up to 4 tiles ahead
 constexpr int kThreadsU = 320;   // 2 x 4 softmax warps, the producer warp, the MMA warp
-constexpr int kTmemCols = 512;   // per query tile X: S0 [256X, +64), S1 [+64, +64), O [+128, +128)
+constexpr int kTmemCols = 512;   // per query tile X: S0 [256X, +64), S1 [+64, +64), O [+128, +128);
+                                 // P_t (16-bit pairs) overwrites the first 32 columns of its S buffer
 constexpr int kQBytes = kRows * 256;          // two slabs of 128 rows x 128 bytes
 constexpr int kSlab = kKeys * 128;            // one slab of a K or V tile
 constexpr int kKVBytes = 2 * kSlab;           // K (or V) tile: 64 rows x 256 bytes
 constexpr int kStageBytes = 2 * kKVBytes;     // K then V
-constexpr int kPBytes = kRows * 128;          // P: 128 rows x 64 keys x 2 bytes
 constexpr float kRescaleLog2 = 8.f;
 
 // ---------------------------------------------------------------- PTX
@@ -69,6 +70,18 @@ __device__ __forceinline__ void umma(uint32_t d_tmem, uint64_t adesc, uint64_t b
       "setp.ne.b32 p, %4, 0;\n\t"
       "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
       "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+// D[tmem] (+)= A[tmem] x B[smem desc]: A (M rows = TMEM lanes, two 16-bit K
+// elements per 32-bit column) read from tensor memory.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                        uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
       : "memory");
 }
 
@@ -137,6 +150,19 @@ __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float (&v)[32]) {
   for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
 }
 
+__device__ __forceinline__ void tmem_st32u(uint32_t taddr, const uint32_t (&v)[32]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]),
+      "r"(v[8]), "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]),
+      "r"(v[16]), "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]),
+      "r"(v[24]), "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
 __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float (&v)[32]) {
   asm volatile(
       "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
@@ -186,7 +212,7 @@ __device__ __forceinline__ uint32_t sw(int r, int c) {
 }
 
 constexpr int smem_bytes() {
-  return 2 * kQBytes + kStages * kStageBytes + 4 * kPBytes + 512 + 1024;
+  return 2 * kQBytes + kStages * kStageBytes + 512 + 1024;
 }
 
 template <typename KV, typename Q, int T>
@@ -241,13 +267,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                                              ~uintptr_t(1023));
   uint8_t* q_s = smem;                                  // [X][2 slabs][128 rows][128 B]
   uint8_t* ring = smem + 2 * kQBytes;                   // [stage][K slab0, K slab1, V slab0, V slab1]
-  uint8_t* p_s = ring + kStages * kStageBytes;          // [X][2][128 rows][128 B]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(p_s + 4 * kPBytes);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kStages * kStageBytes);
   uint64_t* full = bars;                 // [kStages] K/V landed (TMA)
   uint64_t* empty = bars + kStages;      // [kStages] every P V reading the stage done (commit)
   uint64_t* s_full = empty + kStages;    // [X][2] S buffer written (commit)
-  uint64_t* s_free = s_full + 4;         // [X][2] S buffer read by the tile's 128 softmax threads
-  uint64_t* p_full = s_free + 4;         // [X][2] P buffer written by the tile's 128 softmax threads
+  uint64_t* p_full = s_full + 4;         // [X][2] P written over S by the tile's 128 softmax threads
   uint64_t* o_done = p_full + 4;         // [X][2] P V of a key tile done (commit)
   uint64_t* fin = o_done + 4;            // every UMMA done (commit)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
@@ -261,7 +285,6 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
-      mbar_init(smem_u32(&s_free[i]), kRows);
       mbar_init(smem_u32(&p_full[i]), kRows);
       mbar_init(smem_u32(&o_done[i]), 1);
     }
@@ -341,12 +364,11 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       const uint64_t q_desc = sw128_desc(smem_u32(q_s), 16, 1024);
       const uint64_t k_desc = sw128_desc(smem_u32(ring), 16, 1024);
       const uint64_t v_desc = sw128_desc(smem_u32(ring + kKVBytes), kSlab, 1024);
-      const uint64_t p_desc = sw128_desc(smem_u32(p_s), 16, 1024);
       auto qk = [&](int X, int t) -> bool {  // S_t of tile X into its buffer t & 1
         const int slot = t % kStages, b = t & 1, i = 2 * X + b;
         if (!mbar_wait(smem_u32(&full[slot]), (t / kStages) & 1, kWaitNs)) return false;
-        // the buffer's previous key tile (t - 2) has been read by the softmax threads
-        if (t >= 2 && !mbar_wait(smem_u32(&s_free[i]), ((t >> 1) - 1) & 1, kWaitNs)) return false;
+        // the buffer's previous key tile (t - 2): its P has been read by P V
+        if (t >= 2 && !mbar_wait(smem_u32(&o_done[i]), ((t >> 1) - 1) & 1, kWaitNs)) return false;
         tc_fence_after();
         const uint64_t qd = q_desc + ((X * kQBytes) >> 4);
         const uint64_t kd = k_desc + ((slot * kStageBytes) >> 4);
@@ -364,12 +386,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int b = t & 1, i = 2 * X + b;
         if (!mbar_wait(smem_u32(&p_full[i]), (t >> 1) & 1, kWaitNs)) return false;
         tc_fence_after();
-        const uint64_t pd = p_desc + ((i * kPBytes) >> 4);
         const uint64_t vd = v_desc + (((t % kStages) * kStageBytes) >> 4);
         const uint32_t d_tmem = tmem + 256 * X + 128;
+        const uint32_t p_tmem = tmem + 256 * X + 64 * b;  // 8 columns per 16 keys
 #pragma unroll
         for (int kk = 0; kk < kKeys / 16; ++kk)
-          umma(d_tmem, pd + ((32 * kk) >> 4), vd + ((2048 * kk) >> 4), kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
+          umma_ts(d_tmem, p_tmem + 8 * kk, vd + ((2048 * kk) >> 4), kIdPV, (t > 0 || kk > 0) ? 1u : 0u);
         umma_commit(smem_u32(&o_done[i]));
         return true;
       };
@@ -423,8 +445,6 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           sv[32 + e] = __uint_as_float(h1[e]);
         }
       }
-      tc_fence_before();
-      mbar_arrive(smem_u32(&s_free[i]));
 
       // mask the keys after the query (and past ctx); the row maximum of the
       // raw scores in eight independent chains, scaled once (the scale is
@@ -468,29 +488,21 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         l *= f;
       }
       if (move) m_ref = mx;
-      // the P buffer is free once P_{t-2} V_{t-2} is done
-      if (t >= 2 &&
-          !__all_sync(FULL, mbar_wait(smem_u32(&o_done[i]), ((t >> 1) - 1) & 1, kWaitNs))) {
-        ok = false;
-        break;
-      }
-      uint8_t* pb = p_s + i * kPBytes;
+      // P_t over the first 32 columns of the S buffer just read: column c
+      // holds keys 2c, 2c + 1 (the K order of the A operand in TMEM)
       float sum8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) sum8[k] = 0.f;
+      uint32_t w[32];
 #pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        uint32_t w[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float p0 = ex2(fmaf(sv[8 * c + 2 * e], hs.qk, -m_ref));
-          const float p1 = ex2(fmaf(sv[8 * c + 2 * e + 1], hs.qk, -m_ref));
-          sum8[2 * e] += p0;
-          sum8[2 * e + 1] += p1;
-          w[e] = pack2<kBf>(p0, p1);
-        }
-        *reinterpret_cast<uint4*>(pb + sw(r, c)) = make_uint4(w[0], w[1], w[2], w[3]);
+      for (int c = 0; c < 32; ++c) {
+        const float p0 = ex2(fmaf(sv[2 * c], hs.qk, -m_ref));
+        const float p1 = ex2(fmaf(sv[2 * c + 1], hs.qk, -m_ref));
+        sum8[(2 * c) & 7] += p0;
+        sum8[(2 * c + 1) & 7] += p1;
+        w[c] = pack2<kBf>(p0, p1);
       }
+      tmem_st32u(tmem + 256 * X + 64 * b + lane_off, w);
       l += ((sum8[0] + sum8[1]) + (sum8[2] + sum8[3])) + ((sum8[4] + sum8[5]) + (sum8[6] + sum8[7]));
       // V rows at positions >= ctx (the tail of the last block, blocks not
       // loaded) are zeroed by tile A's threads (tile B's too when A has no
@@ -502,8 +514,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           *reinterpret_cast<uint4*>(vt + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
           *reinterpret_cast<uint4*>(vt + kSlab + r * 128 + c * 16) = make_uint4(0, 0, 0, 0);
         }
+        fence_proxy_async();  // before the tensor core reads V
       }
-      fence_proxy_async();
       tc_fence_before();
       mbar_arrive(smem_u32(&p_full[i]));
     }
