@@ -65,6 +65,7 @@ struct PrefillArgs {
   float v_scale;              // 1, or the E4M3 V scale
   const float* head_scales;   // E4M3 per-KV-head scales [4][N_kv], or NULL (replace the two above)
   float softmax_scale;
+  int32_t ranked;             // tcgen05 kernel: grid (head, unit rank), units ranked longest first
 };
 
 template <typename KV, typename Q, int D, int T, int NS>
@@ -446,8 +447,12 @@ pkv_status launch_prefill_umma(PrefillArgs a, const CUtensorMap& kmap, const CUt
     configured.fetch_or(bit);
   }
   a.max_q_tiles = ((max_query_len + umma::kRows - 1) / umma::kRows + 1) / 2;  // pairs of query tiles
+  // up to 256 (sequence, pair) units: ranked longest first in the kernel
+  const bool ranked = static_cast<int64_t>(a.num_seqs) * a.max_q_tiles <= umma::kMaxRanked;
+  a.ranked = ranked ? 1 : 0;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(a.max_q_tiles, a.num_q_heads, a.num_seqs);
+  cfg.gridDim = ranked ? dim3(a.num_q_heads, a.num_seqs * a.max_q_tiles, 1)
+                       : dim3(a.max_q_tiles, a.num_q_heads, a.num_seqs);
   cfg.blockDim = dim3(umma::kThreadsU);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

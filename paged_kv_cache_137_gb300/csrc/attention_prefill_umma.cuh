@@ -211,6 +211,86 @@ __device__ __forceinline__ uint32_t sw(int r, int c) {
   return static_cast<uint32_t>(r * 128 + ((c ^ (r & 7)) << 4));
 }
 
+constexpr int kMaxRanked = 256;   // units ranked in the kernel (longest first)
+
+// The (sequence, query-tile pair) unit of rank `rank` when the units are
+// ordered by work (the key tiles both query tiles read), longest first, ties
+// in sequence order.  The hardware dispatches CTAs in grid order, so the
+// long units start first and the short ones fill the gaps at the end (the
+// longest-processing-time rule).  Every CTA computes the same order from the
+// lengths: sequence t is thread t's, at most kMaxRanked units in all.
+// Returns the sequence (or -1: no unit of that rank) and the pair index.
+template <int T>
+__device__ __forceinline__ int ranked_unit(const PrefillArgs& a, int rank, int* scratch, int* pair_out) {
+  int* s_work = scratch;                     // [kMaxRanked]
+  int* s_seq = s_work + kMaxRanked;          // [kMaxRanked]
+  int* s_pair = s_seq + kMaxRanked;          // [kMaxRanked]
+  int* s_wsum = s_pair + kMaxRanked;         // [8] unit counts of the warps' sequences
+  int* s_pick = s_wsum + 8;                  // [2]
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  int np = 0, first = 0, n = 0;
+  bool bad = false;
+  if (tid < a.num_seqs) {
+    const int ctx = a.ctx_lens[tid];
+    const int q0 = a.query_start[tid];
+    n = a.query_start[tid + 1] - q0;
+    if (!(q0 < 0 || n <= 0 || q0 + n > a.total_q)) {
+      const int ntq = (n + kRows - 1) / kRows;
+      bad = ctx < 0 || ctx > a.max_blocks * T || n > ctx || (ntq + 1) / 2 > a.max_q_tiles;
+      np = bad ? 1 : (ntq + 1) / 2;  // an invalid sequence: one unit that writes its NaN rows
+      first = ctx - n;
+    }
+  }
+  // offset of sequence tid's units: a scan within each of the first 8 warps
+  // (num_seqs <= kMaxRanked = 256), then over the warps' totals
+  int incl = np;
+#pragma unroll
+  for (int d = 1; d < 32; d <<= 1) {
+    const int y = __shfl_up_sync(0xffffffffu, incl, d);
+    if (lane >= d) incl += y;
+  }
+  if (warp < 8 && lane == 31) s_wsum[warp] = incl;
+  if (tid < 2) s_pick[tid] = -1;
+  __syncthreads();
+  int base = 0, units = 0;
+  for (int w = 0; w < 8; ++w) {
+    base += w < warp ? s_wsum[w] : 0;
+    units += s_wsum[w];
+  }
+  if (tid < a.num_seqs) {
+    const int ntq = (n + kRows - 1) / kRows;
+    const int off = base + incl - np;
+    for (int k = 0; k < np; ++k) {
+      int w = -1;  // an invalid sequence's unit goes last
+      if (!bad) {
+        const int rA = min((2 * k + 1) * kRows, n), rB = min((2 * k + 2) * kRows, n);
+        w = (first + rA + kKeys - 1) / kKeys + (2 * k + 1 < ntq ? (first + rB + kKeys - 1) / kKeys : 0);
+      }
+      s_work[off + k] = w;
+      s_seq[off + k] = tid;
+      s_pair[off + k] = k;
+    }
+  }
+  __syncthreads();
+  for (int u = tid; u < units; u += blockDim.x) {
+    int r = 0;
+    const int wu = s_work[u];
+    for (int v = 0; v < units; ++v) {
+      const int wv = s_work[v];
+      r += (wv > wu) || (wv == wu && v < u);
+    }
+    if (r == rank) {
+      s_pick[0] = s_seq[u];
+      s_pick[1] = s_pair[u];
+    }
+  }
+  __syncthreads();
+  const int seq = s_pick[0];
+  *pair_out = s_pick[1];
+  __syncthreads();  // the scratch is reused by the caller
+  return seq;
+}
+
 constexpr int smem_bytes() {
   return 2 * kQBytes + kStages * kStageBytes + 512 + 1024;
 }
@@ -229,8 +309,24 @@ __global__ void __launch_bounds__(kThreadsU, 1)
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
-  const int qp_rev = blockIdx.x, j = blockIdx.y, s = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // grid: (query head, unit rank) with the units ranked longest first, or
+  // (pair counted from the chunk's end, query head, sequence)
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  int j, s, qp_rev;
+  if (a.ranked) {
+    int pair = 0;
+    j = blockIdx.x;
+    s = ranked_unit<T>(a, blockIdx.y, reinterpret_cast<int*>(smem), &pair);
+    if (s < 0) return;
+    qp_rev = -1 - pair;  // marks a pair index given directly
+  } else {
+    qp_rev = blockIdx.x;
+    j = blockIdx.y;
+    s = blockIdx.z;
+  }
   const int HQ = a.num_q_heads;
   const int ctx = a.ctx_lens[s];
   const int q0 = a.query_start[s];
@@ -240,13 +336,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   const int npairs = (ntq + 1) / 2;
   const bool bad_len = ctx < 0 || ctx > a.max_blocks * T || n > ctx || npairs > a.max_q_tiles;
   if (bad_len) {  // invalid lengths: the chunk's rows of head j become NaN
-    if (qp_rev == 0)
+    if (qp_rev == 0 || qp_rev == -1)
       for (int i = tid; i < n * D; i += kThreadsU)
         store_elem<Q>(a.out, (static_cast<size_t>(q0 + i / D) * HQ + j) * D + i % D, CUDART_NAN_F);
     return;
   }
   if (qp_rev >= npairs) return;
-  const int qp = npairs - 1 - qp_rev;
+  const int qp = qp_rev < 0 ? -1 - qp_rev : npairs - 1 - qp_rev;
   const int first = ctx - n;                      // position of the chunk's first query
   // query tile X (0 = A, 1 = B): chunk rows r_begin[X] .. r_end[X] - 1
   const bool hasB = 2 * qp + 1 < ntq;
@@ -262,9 +358,6 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   const HeadScales hs = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale, a.qk_scale,
                                     a.v_scale, 1.f, 1.f);
 
-  extern __shared__ uint8_t smem_raw[];
-  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
-                                             ~uintptr_t(1023));
   uint8_t* q_s = smem;                                  // [X][2 slabs][128 rows][128 B]
   uint8_t* ring = smem + 2 * kQBytes;                   // [stage][K slab0, K slab1, V slab0, V slab1]
   uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kStages * kStageBytes);

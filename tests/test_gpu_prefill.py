@@ -226,3 +226,13 @@ def test_non_positive_softmax_scale(scale):
     torch.cuda.synchronize()
     ref = OP.paged_attention_prefill(q.double().numpy(), scn.pool, scn.tables, scn.ctx, qs, scale)
     check(out, ref)
+
+
+def test_many_units_take_the_per_sequence_grid():
+    """More than 256 (sequence, query-tile pair) units (here through a large
+    max_query_len) launch the tcgen05 kernel on its (pair, head, sequence)
+    grid instead of the ranked one; same results."""
+    dev, scn = state("qwen_small")
+    n = W.chunk_lens(dev.plan.w, dev.plan.ctx, 300)
+    q, qs = chunk_inputs(dev, n)
+    check(run_prefill(dev, q, qs, max_query_len=70_000), oracle(scn, q, qs))
