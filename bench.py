@@ -96,6 +96,24 @@ def allocator_step_us(plan, steps: int = 200) -> float:
     return (time.perf_counter() - t0) / steps * 1e6
 
 
+def packed(tensors, device):
+    """One device buffer holding the given tensors back to back (each at a
+    256-byte boundary), so that a step's inputs arrive by ONE host-to-device
+    copy: the buffer and views of it holding the tensors' values."""
+    import torch
+    offs, total = [], 0
+    for t in tensors:
+        offs.append(total)
+        total += -(-t.numel() * t.element_size() // 256) * 256
+    buf = torch.zeros(total, dtype=torch.uint8, device=device)
+    views = []
+    for t, o in zip(tensors, offs):
+        v = buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+        v.copy_(t)
+        views.append(v)
+    return buf, views
+
+
 def workload_of(args):
     """The configured workload, with the ablation overrides applied: another
     block size keeps the pool's token capacity (plus one block per sequence,
@@ -414,15 +432,20 @@ def run_gpu(args, world, rank, local):
     # batch's sequences and their block tables exported, on a copy of the plan
     aux["allocator_step_us"] = round(allocator_step_us(scn.plan), 2)
 
-    # end to end through the C ABI from pinned host buffers
-    host = {n: getattr(scn, n).cpu().pin_memory() for n in ("q", "k_new", "v_new", "tables", "ctx")}
+    # end to end through the C ABI from pinned host buffers: the step's inputs
+    # (q, the new K/V, block tables, context lengths) packed in one pinned
+    # buffer and copied in once, the output copied back, then a sync
+    names = ("q", "k_new", "v_new", "tables", "ctx")
+    dev_in, views = packed([getattr(scn, n) for n in names], dev_name)
+    for n_, v_ in zip(names, views):
+        setattr(scn, n_, v_)
+    host_in = dev_in.cpu().pin_memory()
     out_host = torch.empty_like(scn.out, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = host_in.numel()
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        for n, t in host.items():
-            getattr(scn, n).copy_(t, non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
         scn.step()
         out_host.copy_(scn.out, non_blocking=True)
         torch.cuda.synchronize()
@@ -566,18 +589,20 @@ def run_prefill_gpu(args, world, rank, local):
     n = W.chunk_lens(w, ctx, w.prefill_chunk)
     qs_np = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
     total_q = int(qs_np[-1])
-    q = torch.cat([W.q_for_chunk(w, s, int(n[r])) for r, s in enumerate(scn.plan.seq_ids)]).to(dev_name)
-    out = torch.empty_like(q)
+    q = torch.cat([W.q_for_chunk(w, s, int(n[r])) for r, s in enumerate(scn.plan.seq_ids)])
+    out = torch.empty_like(q, device=dev_name)
     qs = torch.from_numpy(qs_np).to(dev_name)
     # the chunk's K/V and slots (the same values the pool already holds)
     kv = [W.kv_for_seq(w, s, int(n[r]), first_pos=int(ctx[r]) - int(n[r]))
           for r, s in enumerate(scn.plan.seq_ids)]
-    k_new = torch.cat([k for k, _ in kv]).to(dev_name)
-    v_new = torch.cat([v for _, v in kv]).to(dev_name)
+    k_new = torch.cat([k for k, _ in kv])
+    v_new = torch.cat([v for _, v in kv])
     slots_np = np.concatenate([
         [int(scn.plan.tables[r][p // w.block_size]) * w.block_size + p % w.block_size
          for p in range(int(ctx[r]) - int(n[r]), int(ctx[r]))] for r in range(len(ctx))]).astype(np.int64)
-    slots = torch.from_numpy(slots_np).to(dev_name)
+    slots = torch.from_numpy(slots_np)
+    # the step's inputs in one device buffer (one host-to-device copy end to end)
+    dev_in, (q, k_new, v_new, slots) = packed([q, k_new, v_new, slots], dev_name)
     scale = 1.0 / math.sqrt(w.head_dim)
     max_q = int(n.max())
     flops = prefill_flops(w, ctx, n)
@@ -625,18 +650,16 @@ def run_prefill_gpu(args, world, rank, local):
     attn = ev[2].elapsed_time(ev[3]) / K
     value = world * flops / (ms / 1e3) / 1e12
 
-    # end to end through the C ABI from pinned host buffers
-    host = {"q": q.cpu().pin_memory(), "k": k_new.cpu().pin_memory(), "v": v_new.cpu().pin_memory(),
-            "slots": slots.cpu().pin_memory()}
+    # end to end through the C ABI from pinned host buffers: q, the chunk's
+    # K/V and slots packed in one pinned buffer and copied in once, the
+    # output copied back, then a sync
+    host_in = dev_in.cpu().pin_memory()
     out_host = torch.empty_like(out, device="cpu").pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in host.values())
+    h2d = host_in.numel()
     d2h = out_host.numel() * out_host.element_size()
 
     def e2e_step():
-        q.copy_(host["q"], non_blocking=True)
-        k_new.copy_(host["k"], non_blocking=True)
-        v_new.copy_(host["v"], non_blocking=True)
-        slots.copy_(host["slots"], non_blocking=True)
+        dev_in.copy_(host_in, non_blocking=True)
         step()
         out_host.copy_(out, non_blocking=True)
         torch.cuda.synchronize()
