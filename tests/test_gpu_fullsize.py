@@ -84,3 +84,59 @@ def test_longest_context_at_table_capacity():
                                     1.0 / math.sqrt(w.head_dim), seqs=[0])
     err = np.abs(out.double().cpu().numpy()[0] - ref[0])
     assert err.max() <= 2e-2 and err.mean() <= 2e-3
+
+
+def test_prefill_full_size_sampled():
+    """The chunked-prefill benchmark workload (16 chunks of 512 on contexts
+    U[1024,4096], the tcgen05 kernel with ranked units), the whole batch on
+    the GPU; the oracle recomputes the longest and the shortest sequence."""
+    from oracle import prefill as OP
+    w = W.get("qwen_prefill_bf16")
+    dev = PS.materialize(PS.plan(w), "cuda")
+    dev.copy_blocks()
+    dev.write_step()
+    ctx = dev.plan.ctx
+    n = W.chunk_lens(w, ctx, w.prefill_chunk)
+    qs = np.concatenate([[0], np.cumsum(n)]).astype(np.int32)
+    q = torch.cat([W.q_for_chunk(w, s, int(n[r])) for r, s in enumerate(dev.plan.seq_ids)])
+    out = torch.full_like(q, float("nan"), device="cuda")
+    pkv.pkv_attention_prefill(out, q.cuda(), dev.k_cache, dev.v_cache, dev.tables, dev.ctx,
+                              torch.from_numpy(qs).cuda(), dev.desc, 1.0 / math.sqrt(w.head_dim))
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    assert not np.isnan(got).any()
+    rows = sorted({int(np.argmax(ctx)), int(np.argmin(ctx))})
+    ref_scn = OS.build(w, write_seqs=rows)
+    ref = OP.paged_attention_prefill(q.double().numpy(), ref_scn.pool, ref_scn.tables, ref_scn.ctx, qs,
+                                     1.0 / math.sqrt(w.head_dim), seqs=rows)
+    for r in rows:
+        err = np.abs(got[qs[r]:qs[r + 1]] - ref[qs[r]:qs[r + 1]])
+        assert err.max() <= 2e-2 and err.mean() <= 2e-3, (r, err.max(), err.mean())
+
+
+def test_prefill_one_long_prompt():
+    """A whole 8,192-token prompt as one chunk (32 query-tile pairs, every
+    causal diagonal), against the oracle on sampled query rows."""
+    from oracle import prefill as OP
+    w = W.scaled(W.get("qwen_prefill_bf16"), num_seqs=1, num_blocks=600, ctx_range=(8192, 8192),
+                 seed=1399)
+    dev = PS.materialize(PS.plan(w), "cuda")
+    dev.copy_blocks()
+    dev.write_step()
+    n = int(dev.plan.ctx[0])
+    qs = np.array([0, n], dtype=np.int32)
+    q = W.q_for_chunk(w, dev.plan.seq_ids[0], n)
+    out = torch.full_like(q, float("nan"), device="cuda")
+    pkv.pkv_attention_prefill(out, q.cuda(), dev.k_cache, dev.v_cache, dev.tables, dev.ctx,
+                              torch.from_numpy(qs).cuda(), dev.desc, 1.0 / math.sqrt(w.head_dim))
+    torch.cuda.synchronize()
+    got = out.double().cpu().numpy()
+    assert not np.isnan(got).any()
+    # the oracle on a few query rows: rows of a one-row chunk at position p are
+    # the prefill rows of the whole prompt at p
+    ref_scn = OS.build(w)
+    for p in (0, 1, 127, 128, 4095, 8191):
+        ref = OP.paged_attention_prefill(q[p:p + 1].double().numpy(), ref_scn.pool, ref_scn.tables,
+                                         np.array([p + 1]), np.array([0, 1]), 1.0 / math.sqrt(w.head_dim))
+        err = np.abs(got[p] - ref[0])
+        assert err.max() <= 2e-2, (p, err.max())
