@@ -17,9 +17,13 @@
 //    pairs) back over the S buffer they read (tcgen05.st); then
 //    O += P_t V_t (M 128, N 128, K 64: 4 UMMAs with A read from TMEM, V read
 //    N-major from shared memory) into TMEM.  P never touches shared memory.
-//    S_{t+2} is issued right after P_t V_t, so the tensor core works two
-//    tiles ahead while the softmax threads work on this one, and a K/V load
-//    that is late holds up only the S product that needs it.
+//    S_{t+2} is issued once P_t V_t is done (P_t occupies S_{t+2}'s buffer),
+//    so the tensor core works two tiles ahead while the softmax threads work
+//    on this one, and a K/V load that is late holds up only the S product
+//    that needs it.
+//  * With up to 256 (sequence, query-tile pair) units the grid is (query
+//    head, unit rank): each CTA ranks the units by the key tiles they read
+//    and takes the one of its rank, so long units are dispatched first.
 //  * O stays in TMEM.  A row's reference maximum moves only when the running
 //    maximum exceeds it by more than 8 (log2 units): then that row of O is
 //    read, scaled and written back (after the previous P V has completed).
@@ -27,7 +31,11 @@
 //    reference, so the result is the softmax whichever references were used.
 //  * Q is loaded by the softmax threads into the 128-byte-swizzled K-major
 //    layout; K and V arrive by 2-D TMA boxes of T rows x 128 bytes per
-//    (block, slab), the layout the UMMA shared-memory descriptors describe.
+//    (block, slab) into a 5-stage ring, the layout the UMMA shared-memory
+//    descriptors describe.
+//  * The softmax takes the row maximum on the raw scores and computes each
+//    exponent as 2^(s * scale - m) with one FFMA, which needs scale > 0 (the
+//    host sends other scales to the mma.sync kernel).
 //  * V rows at positions >= ctx are zeroed in shared memory before P V
 //    (0 * NaN would poison the product; the mask already zeroes P there).
 //  * Every mbarrier wait is bounded; a CTA whose wait gives up writes NaN
