@@ -48,3 +48,17 @@ def test_torchrun_reference_arm_prints_once():
     lines = [json.loads(x) for x in r.stdout.splitlines() if x.startswith("{")]
     assert len(lines) == 1
     assert lines[0]["impl"] == "reference" and lines[0]["n_gpus"] == 2
+
+
+def test_oracle_pool_spreads_the_batch_over_workers():
+    """The CPU baseline's process pool (spawn context) covers every sequence
+    once per pass and reports the workers it used."""
+    import bench
+    g, passes, el, cores, g1 = bench.parallel_oracle("tiny_fp32", 0.5, cores=2)
+    assert cores == 2 and passes >= 1 and el >= 0.5 and g > 0 and g1 > 0
+    p = bench.OraclePool("tiny_fp32", cores=3)
+    try:
+        assert sorted(r for c in p.chunks for r in c) == list(range(p.w.num_seqs))
+        assert p.one_pass() > 0
+    finally:
+        p.close()
