@@ -32,7 +32,8 @@ sys.path.insert(0, ROOT)
 DEFAULT_CONFIG = "qwen_gqa_bf16"
 METRIC = "paged decode attention KV GB/s & fraction of GB300 HBM peak; decode tokens/s"
 KERNEL_SOURCES = ["attention.cu", "attention.h", "attention_simt.cuh", "attention_tc.cuh",
-                  "attention_tc_launch.cuh", "attention_stream.cuh", "device_common.cuh"]
+                  "attention_tc_launch.cuh", "attention_stream.cuh", "device_common.cuh",
+                  "attention_prefill.cu", "attention_prefill_umma.cuh"]
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 
@@ -775,6 +776,9 @@ def run_prefill_gpu(args, world, rank, local):
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak, peak_kind = (float(d["bf16_tflops"]), "measured") if "bf16_tflops" in d else (1900.0, "fallback")
     achieved = flops / (attn / 1e3) / 1e12
+    pf_kernel = ("prefill_umma_kernel (tcgen05.mma, TMEM accumulators)"
+                 if w.head_dim == 128 and w.kv_dtype in ("bf16", "f16")
+                 else "prefill_tc_kernel (mma.sync m16n8k16)")
     line = {
         "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
         "steps": K, "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4),
@@ -788,10 +792,10 @@ def run_prefill_gpu(args, world, rank, local):
                    "launch": "the K steps captured back to back in one CUDA graph, replayed once",
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": round(world * total_q / (ms / 1e3), 1),
-        "roofline": {"bound": "tensor", "kernel": "prefill_umma_kernel (tcgen05.mma, TMEM accumulators)" if w.head_dim == 128 and w.kv_dtype in ("bf16", "f16") else "prefill_tc_kernel (mma.sync m16n8k16)",
+        "roofline": {"bound": "tensor", "kernel": pf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} bf16 burst",
-                     "traffic": None, "attention_ms": round(attn, 4)},
+                     "traffic": traffic_for(args.config, pf_kernel), "attention_ms": round(attn, 4)},
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4)},
