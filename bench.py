@@ -681,8 +681,11 @@ def run_prefill_gpu(args, world, rank, local):
     pkv.build()
     torch.cuda.set_device(local)
     dev_name = f"cuda:{local}"
-    w = W.get(args.config)
-    scn = PS.materialize(PS.plan(w), dev_name)
+    w = workload_of(args)
+    sc = {}
+    if w.kv_dtype == "e4m3":
+        sc = W.fp8_head_scales(w) if args.fp8_scales == "head" else W.fp8_scales(*W.kv_amax(w))
+    scn = PS.materialize(PS.plan(w), dev_name, sc)
     scn.copy_blocks()
     scn.write_step()
     ctx = scn.plan.ctx
@@ -708,12 +711,16 @@ def run_prefill_gpu(args, world, rank, local):
     flops = prefill_flops(w, ctx, n)
     stream = torch.cuda.current_stream()
 
+    ks, vs = scn.scales.get("k_scale", 1.0), scn.scales.get("v_scale", 1.0)
+
     def attend():
         pkv.pkv_attention_prefill(out, q, scn.k_cache, scn.v_cache, scn.tables, scn.ctx, qs, scn.desc,
-                                  scale, max_query_len=max_q)
+                                  scale, max_query_len=max_q, k_scale=ks, v_scale=vs)
+
+    kinv, vinv = scn.scales.get("k_inv_scale", 1.0), scn.scales.get("v_inv_scale", 1.0)
 
     def step():
-        pkv.pkv_write(scn.k_cache, scn.v_cache, k_new, v_new, slots, scn.desc)
+        pkv.pkv_write(scn.k_cache, scn.v_cache, k_new, v_new, slots, scn.desc, kinv, vinv)
         attend()
 
     side = torch.cuda.Stream(device=dev_name)
@@ -777,7 +784,7 @@ def run_prefill_gpu(args, world, rank, local):
     peak, peak_kind = (float(d["bf16_tflops"]), "measured") if "bf16_tflops" in d else (1900.0, "fallback")
     achieved = flops / (attn / 1e3) / 1e12
     pf_kernel = ("prefill_umma_kernel (tcgen05.mma, TMEM accumulators)"
-                 if w.head_dim == 128 and w.kv_dtype in ("bf16", "f16")
+                 if w.head_dim == 128
                  else "prefill_tc_kernel (mma.sync m16n8k16)")
     line = {
         "metric": PREFILL_METRIC, "value": round(value, 2), "unit": "TFLOP/s", "n_gpus": world,
@@ -786,7 +793,8 @@ def run_prefill_gpu(args, world, rank, local):
         "data": "synthetic",
         "config": {"workload": args.config, "num_seqs": w.num_seqs, "num_q_heads": w.num_q_heads,
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
-                   "chunk": w.prefill_chunk, "query_tokens": total_q,
+                   "chunk": w.prefill_chunk, "query_tokens": total_q, "kv_dtype": w.kv_dtype,
+                   **({"fp8_scales": args.fp8_scales} if w.kv_dtype == "e4m3" else {}),
                    "context_tokens": int(ctx.sum()), "flops_per_step": flops,
                    "l2": "no flush between steps (K/V of the chunks' contexts re-read each step)",
                    "launch": "the K steps captured back to back in one CUDA graph, replayed once",
@@ -795,7 +803,8 @@ def run_prefill_gpu(args, world, rank, local):
         "roofline": {"bound": "tensor", "kernel": pf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} bf16 burst",
-                     "traffic": traffic_for(args.config, pf_kernel), "attention_ms": round(attn, 4)},
+                     "traffic": traffic_for(args.config, pf_kernel) if w == W.get(args.config) else None,
+                     "attention_ms": round(attn, 4)},
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
                 "ms_per_step": round(e2e_s * 1e3, 4)},

@@ -369,10 +369,11 @@ PKV_API pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_dty
                                          void* stream);
 
 /* Prefill kernel choice, process-wide: PKV_PREFILL_AUTO (tcgen05 UMMA with
- * TMEM accumulators for 16-bit caches with head_dim 128 and softmax_scale >
- * 0, the mma.sync kernel otherwise), PKV_PREFILL_MMA_SYNC (always the mma.sync kernel) or
- * PKV_PREFILL_TCGEN05 (the tcgen05 kernel; other caches then return
- * PKV_ERR_UNSUPPORTED).  Both compute the same attention; their results
+ * TMEM accumulators for head_dim 128 and softmax_scale > 0 — 16-bit caches
+ * directly, E4M3 caches widened exactly to f16 in shared memory — the
+ * mma.sync kernel otherwise), PKV_PREFILL_MMA_SYNC (always the mma.sync
+ * kernel) or PKV_PREFILL_TCGEN05 (the tcgen05 kernel; other shapes then
+ * return PKV_ERR_UNSUPPORTED).  Both compute the same attention; their results
  * differ by rounding only.  PKV_ERR_INVALID_ARG for another value. */
 #define PKV_PREFILL_AUTO 0
 #define PKV_PREFILL_MMA_SYNC 1

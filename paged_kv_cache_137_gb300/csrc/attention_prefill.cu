@@ -434,7 +434,7 @@ std::atomic<int> g_prefill_choice{PKV_PREFILL_AUTO};
 template <typename KV, typename Q, int T>
 pkv_status launch_prefill_umma(PrefillArgs a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                                int32_t max_query_len, cudaStream_t st) {
-  constexpr int smem = umma::smem_bytes();
+  constexpr int smem = umma::smem_bytes<KV>();
   auto kernel = umma::prefill_umma_kernel<KV, Q, T>;
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -453,7 +453,7 @@ pkv_status launch_prefill_umma(PrefillArgs a, const CUtensorMap& kmap, const CUt
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = ranked ? dim3(a.num_q_heads, a.num_seqs * a.max_q_tiles, 1)
                        : dim3(a.max_q_tiles, a.num_q_heads, a.num_seqs);
-  cfg.blockDim = dim3(umma::kThreadsU);
+  cfg.blockDim = dim3(umma::threads<KV>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -547,20 +547,25 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
   if (st != PKV_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim, T = desc->block_size;
-  // 16-bit caches with head_dim 128 and a positive softmax scale run on
-  // tcgen05 unless the mma.sync kernel is chosen (that kernel folds the scale
-  // into the row maximum, which needs scale > 0)
+  // head_dim 128 with a positive softmax scale runs on tcgen05 (E4M3 caches
+  // widened to f16 in shared memory) unless the mma.sync kernel is chosen
+  // (the tcgen05 kernel folds the softmax scale into the row maximum)
   const int choice = tc::g_prefill_choice.load();
-  if (kv != PKV_E4M3 && D == 128 && softmax_scale > 0.f && choice != PKV_PREFILL_MMA_SYNC) {
+  if (D == 128 && softmax_scale > 0.f && choice != PKV_PREFILL_MMA_SYNC) {
     if (kv == PKV_BF16)
       return T == 16 ? tc::launch_prefill_umma<BF16, BF16, 16>(a, kmap, vmap, max_query_len, s)
                      : tc::launch_prefill_umma<BF16, BF16, 32>(a, kmap, vmap, max_query_len, s);
-    return T == 16 ? tc::launch_prefill_umma<F16, F16, 16>(a, kmap, vmap, max_query_len, s)
-                   : tc::launch_prefill_umma<F16, F16, 32>(a, kmap, vmap, max_query_len, s);
+    if (kv == PKV_F16)
+      return T == 16 ? tc::launch_prefill_umma<F16, F16, 16>(a, kmap, vmap, max_query_len, s)
+                     : tc::launch_prefill_umma<F16, F16, 32>(a, kmap, vmap, max_query_len, s);
+    if (q_dtype == PKV_BF16)
+      return T == 16 ? tc::launch_prefill_umma<E4M3, BF16, 16>(a, kmap, vmap, max_query_len, s)
+                     : tc::launch_prefill_umma<E4M3, BF16, 32>(a, kmap, vmap, max_query_len, s);
+    return T == 16 ? tc::launch_prefill_umma<E4M3, F16, 16>(a, kmap, vmap, max_query_len, s)
+                   : tc::launch_prefill_umma<E4M3, F16, 32>(a, kmap, vmap, max_query_len, s);
   }
   if (choice == PKV_PREFILL_TCGEN05)
-    return fail(PKV_ERR_UNSUPPORTED,
-                "the tcgen05 prefill kernel needs a 16-bit cache, head_dim 128 and softmax_scale > 0");
+    return fail(PKV_ERR_UNSUPPORTED, "the tcgen05 prefill kernel needs head_dim 128 and softmax_scale > 0");
   if (kv == PKV_BF16) return tc::launch_prefill<BF16, BF16>(a, D, T, kmap, vmap, s);
   if (kv == PKV_F16) return tc::launch_prefill<F16, F16>(a, D, T, kmap, vmap, s);
   return q_dtype == PKV_F16 ? tc::launch_prefill<E4M3, F16>(a, D, T, kmap, vmap, s)

@@ -299,21 +299,38 @@ __device__ __forceinline__ int ranked_unit(const PrefillArgs& a, int rank, int* 
   return seq;
 }
 
+// E4M3 caches: the TMA ring holds 8-bit tiles (K then V, 64 rows x 128 bytes
+// each) and a converter warp widens each tile (exactly) into one of two
+// 16-bit K/V buffers laid out as the 16-bit ring's stages.
+constexpr int kStages8 = 4;
+constexpr int kStage8Bytes = 2 * kKeys * 128;
+
+template <typename KV>
 constexpr int smem_bytes() {
-  return 2 * kQBytes + kStages * kStageBytes + 512 + 1024;
+  return std::is_same<KV, E4M3>::value
+             ? 2 * kQBytes + kStages8 * kStage8Bytes + 2 * kStageBytes + 512 + 1024
+             : 2 * kQBytes + kStages * kStageBytes + 512 + 1024;
+}
+
+template <typename KV>
+constexpr int threads() {
+  return std::is_same<KV, E4M3>::value ? kThreadsU + 64 : kThreadsU;  // + two converter warps
 }
 
 template <typename KV, typename Q, int T>
-__global__ void __launch_bounds__(kThreadsU, 1)
+__global__ void __launch_bounds__(threads<KV>(), 1)
     prefill_umma_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
   constexpr int D = 128;
-  constexpr bool kBf = std::is_same<KV, BF16>::value;
+  constexpr bool kFp8 = std::is_same<KV, E4M3>::value;
+  constexpr bool kBf = std::is_same<KV, BF16>::value;   // MMA type: bf16, else f16
   constexpr bool kOutBf = std::is_same<Q, BF16>::value;
   constexpr int BPT = kKeys / T;   // blocks per key tile
   constexpr uint32_t kIdQK = idesc(kBf, kRows, kKeys, false);
   constexpr uint32_t kIdPV = idesc(kBf, kRows, D, true);
-  constexpr int kProd = 8, kMma = 9;  // warps
+  constexpr int kProd = 8, kMma = 9, kConv = 10;  // warps (E4M3: converters 10 (K) and 11 (V))
+  constexpr int kNS = kFp8 ? kStages8 : kStages;  // TMA ring stages
+  constexpr int kNT = threads<KV>();
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
 
@@ -345,7 +362,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   const bool bad_len = ctx < 0 || ctx > a.max_blocks * T || n > ctx || npairs > a.max_q_tiles;
   if (bad_len) {  // invalid lengths: the chunk's rows of head j become NaN
     if (qp_rev == 0 || qp_rev == -1)
-      for (int i = tid; i < n * D; i += kThreadsU)
+      for (int i = tid; i < n * D; i += kNT)
         store_elem<Q>(a.out, (static_cast<size_t>(q0 + i / D) * HQ + j) * D + i % D, CUDART_NAN_F);
     return;
   }
@@ -367,22 +384,32 @@ __global__ void __launch_bounds__(kThreadsU, 1)
                                     a.v_scale, 1.f, 1.f);
 
   uint8_t* q_s = smem;                                  // [X][2 slabs][128 rows][128 B]
-  uint8_t* ring = smem + 2 * kQBytes;                   // [stage][K slab0, K slab1, V slab0, V slab1]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kStages * kStageBytes);
-  uint64_t* full = bars;                 // [kStages] K/V landed (TMA)
-  uint64_t* empty = bars + kStages;      // [kStages] every P V reading the stage done (commit)
-  uint64_t* s_full = empty + kStages;    // [X][2] S buffer written (commit)
+  // 16-bit: [stage][K slab0, K slab1, V slab0, V slab1]; E4M3: [stage][K, V]
+  // of 64 rows x 128 bytes, then the two widened 16-bit K/V buffers
+  uint8_t* ring = smem + 2 * kQBytes;
+  uint8_t* wide = ring + kStages8 * kStage8Bytes;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      kFp8 ? wide + 2 * kStageBytes : ring + kStages * kStageBytes);
+  uint64_t* full = bars;                 // [kNS] K/V landed (TMA)
+  uint64_t* empty = bars + kNS;          // [kNS] stage free (16-bit: P V done; E4M3: widened)
+  uint64_t* s_full = empty + kNS;        // [X][2] S buffer written (commit)
   uint64_t* p_full = s_full + 4;         // [X][2] P written over S by the tile's 128 softmax threads
   uint64_t* o_done = p_full + 4;         // [X][2] P V of a key tile done (commit)
   uint64_t* fin = o_done + 4;            // every UMMA done (commit)
-  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(fin + 1);
+  uint64_t* conv_full = fin + 1;         // E4M3: [2] widened buffer ready
+  uint64_t* wide_free = conv_full + 2;   // E4M3: [2] every UMMA reading the widened buffer done
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wide_free + 2);
   __shared__ int s_bad;
 
   if (tid == 0) {
     s_bad = 0;
-    for (int i = 0; i < kStages; ++i) {
+    for (int i = 0; i < kNS; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
-      mbar_init(smem_u32(&empty[i]), 1);
+      mbar_init(smem_u32(&empty[i]), kFp8 ? 2 : 1);  // E4M3: both converter warps
+    }
+    for (int i = 0; i < 2; ++i) {
+      mbar_init(smem_u32(&conv_full[i]), 2);
+      mbar_init(smem_u32(&wide_free[i]), 1);
     }
     for (int i = 0; i < 4; ++i) {
       mbar_init(smem_u32(&s_full[i]), 1);
@@ -409,7 +436,13 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     uint8_t* qx = q_s + X * kQBytes;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      const uint4 v = in ? src[c] : make_uint4(0, 0, 0, 0);
+      uint4 v = in ? src[c] : make_uint4(0, 0, 0, 0);
+      if constexpr (kFp8 && kOutBf) {  // the MMA is f16 (the widened E4M3): q to f16
+        float f[8];
+        LoadF32<Q, 8>::run(reinterpret_cast<const typename Q::raw*>(&v), f);
+        v = make_uint4(pack2<false>(f[0], f[1]), pack2<false>(f[2], f[3]), pack2<false>(f[4], f[5]),
+                       pack2<false>(f[6], f[7]));
+      }
       *reinterpret_cast<uint4*>(qx + (c >> 3) * (kRows * 128) + sw(r, c & 7)) = v;
     }
     fence_proxy_async();
@@ -423,13 +456,12 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     // ------------------------------------------------------------ producer
     if (lane == 0) {
       for (int t = 0; t < n_tiles; ++t) {
-        const int slot = t % kStages;
-        if (t >= kStages &&
-            !mbar_wait(smem_u32(&empty[slot]), ((t / kStages) - 1) & 1, kWaitNs)) {
+        const int slot = t % kNS;
+        if (t >= kNS && !mbar_wait(smem_u32(&empty[slot]), ((t / kNS) - 1) & 1, kWaitNs)) {
           s_bad = 1;
           break;
         }
-        uint8_t* st = ring + slot * kStageBytes;
+        uint8_t* st = ring + slot * (kFp8 ? kStage8Bytes : kStageBytes);
         int ids[BPT];
         int nbox = 0;
         for (int b = 0; b < BPT; ++b) {
@@ -445,13 +477,15 @@ __global__ void __launch_bounds__(kThreadsU, 1)
           }
         }
         const uint32_t bar = smem_u32(&full[slot]);
-        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox) * 4u * (T * 128));
+        constexpr int kSlabs = kFp8 ? 1 : 2;  // 128-byte slabs per row
+        mbar_arrive_expect_tx(bar, static_cast<uint32_t>(nbox) * 2u * kSlabs * (T * 128));
         for (int b = 0; b < BPT; ++b) {
           if (ids[b] < 0) continue;
           const int row = (ids[b] * a.num_kv_heads + kvh) * T;
-          for (int sl = 0; sl < 2; ++sl) {
+          for (int sl = 0; sl < kSlabs; ++sl) {
+            const int vo = kFp8 ? kKeys * 128 : kKVBytes;  // V after K
             tma_load_2d(smem_u32(st + sl * kSlab + b * T * 128), &kmap, sl * 128, row, bar);
-            tma_load_2d(smem_u32(st + kKVBytes + sl * kSlab + b * T * 128), &vmap, sl * 128, row, bar);
+            tma_load_2d(smem_u32(st + vo + sl * kSlab + b * T * 128), &vmap, sl * 128, row, bar);
           }
         }
       }
@@ -462,12 +496,18 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       // descriptors of the operand bases; an operand's offset (16-byte
       // units) is added to the start-address field, which never carries
       // (shared-memory addresses are below 2^18)
+      // 16-bit K/V of key tile t: ring stage t % kStages, or (E4M3) the
+      // widened buffer t % 2 once the converter has filled it
+      uint8_t* kv16 = kFp8 ? wide : ring;
       const uint64_t q_desc = sw128_desc(smem_u32(q_s), 16, 1024);
-      const uint64_t k_desc = sw128_desc(smem_u32(ring), 16, 1024);
-      const uint64_t v_desc = sw128_desc(smem_u32(ring + kKVBytes), kSlab, 1024);
+      const uint64_t k_desc = sw128_desc(smem_u32(kv16), 16, 1024);
+      const uint64_t v_desc = sw128_desc(smem_u32(kv16 + kKVBytes), kSlab, 1024);
+      auto kv_of = [&](int t) { return kFp8 ? (t & 1) : t % kStages; };
       auto qk = [&](int X, int t) -> bool {  // S_t of tile X into its buffer t & 1
-        const int slot = t % kStages, b = t & 1, i = 2 * X + b;
-        if (!mbar_wait(smem_u32(&full[slot]), (t / kStages) & 1, kWaitNs)) return false;
+        const int slot = kv_of(t), b = t & 1, i = 2 * X + b;
+        const bool landed = kFp8 ? mbar_wait(smem_u32(&conv_full[slot]), (t >> 1) & 1, kWaitNs)
+                                 : mbar_wait(smem_u32(&full[slot]), (t / kStages) & 1, kWaitNs);
+        if (!landed) return false;
         // the buffer's previous key tile (t - 2): its P has been read by P V
         if (t >= 2 && !mbar_wait(smem_u32(&o_done[i]), ((t >> 1) - 1) & 1, kWaitNs)) return false;
         tc_fence_after();
@@ -487,7 +527,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         const int b = t & 1, i = 2 * X + b;
         if (!mbar_wait(smem_u32(&p_full[i]), (t >> 1) & 1, kWaitNs)) return false;
         tc_fence_after();
-        const uint64_t vd = v_desc + (((t % kStages) * kStageBytes) >> 4);
+        const uint64_t vd = v_desc + ((kv_of(t) * kStageBytes) >> 4);
         const uint32_t d_tmem = tmem + 256 * X + 128;
         const uint32_t p_tmem = tmem + 256 * X + 64 * b;  // 8 columns per 16 keys
 #pragma unroll
@@ -504,14 +544,59 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         for (int X = 0; X < 2 && ok; ++X)
           if (t < nt[X]) ok = pv(X, t);
         if (!ok) break;
-        umma_commit(smem_u32(&empty[t % kStages]));  // both tiles' P V of this stage
+        // both tiles' P V of this stage done: the stage (E4M3: the widened buffer) is free
+        umma_commit(smem_u32(kFp8 ? &wide_free[t & 1] : &empty[t % kStages]));
         for (int X = 0; X < 2 && ok; ++X)
           if (t + 2 < nt[X]) ok = qk(X, t + 2);
       }
       if (!ok) s_bad = 1;
       umma_commit(smem_u32(fin));
     }
-  } else {
+  } else if (kFp8 && warp >= kConv) {
+    // ------------------------------------------------------------ converters
+    // Each 8-bit tile (K then V, 64 rows x 128 bytes, 128-byte swizzled)
+    // widened to f16 into buffer t % 2 in the 16-bit layout (two 128-byte
+    // slabs per row, swizzled), V rows at positions >= ctx written as zeros;
+    // warp 10 widens K, warp 11 V (on two SM sub-partitions).
+    // E4M3 -> f16 is exact; the scales stay in the logit scale and in O.
+    const int tv = warp - kConv;
+    constexpr unsigned FULL = 0xffffffffu;
+    for (int t = 0; t < n_tiles; ++t) {
+      const int slot = t % kStages8, w = t & 1;
+      const bool ready = mbar_wait(smem_u32(&full[slot]), (t / kStages8) & 1, kWaitNs) &&
+                         (t < 2 || mbar_wait(smem_u32(&wide_free[w]), ((t >> 1) - 1) & 1, kWaitNs));
+      if (!__all_sync(FULL, ready)) {
+        if (lane == 0) s_bad = 1;
+        break;
+      }
+      const uint8_t* src = ring + slot * kStage8Bytes;
+      uint8_t* dst = wide + w * kStageBytes;
+      const int kb = t * kKeys;
+#pragma unroll 4
+      for (int k = 0; k < 16; ++k) {
+        const int q = lane + 32 * k;               // 16-byte chunk: row, column
+        const int row = q >> 3, c = q & 7;
+        uint4 lo = make_uint4(0, 0, 0, 0), hi = make_uint4(0, 0, 0, 0);
+        if (!(tv == 1 && kb + row >= ctx)) {
+          const uint4 x = *reinterpret_cast<const uint4*>(src + tv * (kKeys * 128) + sw(row, c));
+          lo = make_uint4(e4m3x2_f16x2(x.x & 0xffffu), e4m3x2_f16x2(x.x >> 16),
+                          e4m3x2_f16x2(x.y & 0xffffu), e4m3x2_f16x2(x.y >> 16));
+          hi = make_uint4(e4m3x2_f16x2(x.z & 0xffffu), e4m3x2_f16x2(x.z >> 16),
+                          e4m3x2_f16x2(x.w & 0xffffu), e4m3x2_f16x2(x.w >> 16));
+        }
+        // head_dim 16c .. 16c + 15: slab c / 4, 16-byte chunks 2 (c % 4) and 2 (c % 4) + 1
+        uint8_t* d = dst + tv * kKVBytes + (c >> 2) * kSlab;
+        *reinterpret_cast<uint4*>(d + sw(row, 2 * (c & 3))) = lo;
+        *reinterpret_cast<uint4*>(d + sw(row, 2 * (c & 3) + 1)) = hi;
+      }
+      fence_proxy_async();  // the widened tile, before the tensor core reads it
+      __syncwarp();
+      if (lane == 0) {
+        mbar_arrive(smem_u32(&conv_full[w]));
+        mbar_arrive(smem_u32(&empty[slot]));  // the 8-bit stage may be refilled
+      }
+    }
+  } else if (warp < 8) {
     // ------------------------------------------------------------ softmax
     // Every branch around a TMEM load or store (warp-wide, .sync.aligned)
     // is taken by the whole warp: waits are combined with __all_sync and a
@@ -524,6 +609,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
     const int ntx = nt[X];
     const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
     const uint32_t tO = tmem + 256 * X + 128;
+    // the logit scale the exponent applies (16-bit caches: softmax_scale * log2 e > 0)
+    const float qe = (!kFp8 || hs.qk > 0.f) ? hs.qk : 1.f;
     float m_ref = -CUDART_INF_F, l = 0.f;
     bool ok = true;
     for (int t = 0; t < ntx; ++t) {
@@ -561,11 +648,17 @@ __global__ void __launch_bounds__(kThreadsU, 1)
         for (int e = 0; e < 64; ++e)
           if (e > lim) sv[e] = -CUDART_INF_F;
       }
+      if constexpr (kFp8) {
+        if (!(hs.qk > 0.f)) {  // an E4M3 scale <= 0 (the host sends softmax scales <= 0
+#pragma unroll               // to the mma.sync kernel): scale first, then the maximum
+          for (int e = 0; e < 64; ++e)
+            if (sv[e] != -CUDART_INF_F) sv[e] *= hs.qk;
+        }
+      }
 #pragma unroll
       for (int e = 0; e < 64; ++e) mx8[e & 7] = fmaxf(mx8[e & 7], sv[e]);
-      // the scale is positive (the host sends other scales to the mma.sync kernel)
-      const float mx = hs.qk * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
-                                     fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
+      const float mx = qe * fmaxf(fmaxf(fmaxf(mx8[0], mx8[1]), fmaxf(mx8[2], mx8[3])),
+                                  fmaxf(fmaxf(mx8[4], mx8[5]), fmaxf(mx8[6], mx8[7])));
       const bool move = mx > m_ref + kRescaleLog2;
       const bool scale = move && t > 0 && m_ref != -CUDART_INF_F;  // O holds earlier tiles
       if (__any_sync(FULL, scale)) {
@@ -597,8 +690,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       uint32_t w[32];
 #pragma unroll
       for (int c = 0; c < 32; ++c) {
-        const float p0 = ex2(fmaf(sv[2 * c], hs.qk, -m_ref));
-        const float p1 = ex2(fmaf(sv[2 * c + 1], hs.qk, -m_ref));
+        const float p0 = ex2(fmaf(sv[2 * c], qe, -m_ref));
+        const float p1 = ex2(fmaf(sv[2 * c + 1], qe, -m_ref));
         sum8[(2 * c) & 7] += p0;
         sum8[(2 * c + 1) & 7] += p1;
         w[c] = pack2<kBf>(p0, p1);
@@ -608,7 +701,7 @@ __global__ void __launch_bounds__(kThreadsU, 1)
       // V rows at positions >= ctx (the tail of the last block, blocks not
       // loaded) are zeroed by tile A's threads (tile B's too when A has no
       // such tile): 64 rows of 2 x 128 bytes, one row per thread
-      if (kb + kKeys > ctx && r < kKeys && kb + r >= ctx && (X == 0 || t >= nt[0])) {
+      if (!kFp8 && kb + kKeys > ctx && r < kKeys && kb + r >= ctx && (X == 0 || t >= nt[0])) {
         uint8_t* vt = ring + (t % kStages) * kStageBytes + kKVBytes;
 #pragma unroll
         for (int c = 0; c < 8; ++c) {
@@ -654,8 +747,8 @@ __global__ void __launch_bounds__(kThreadsU, 1)
   if (tid == 0) {
     mbar_wait(smem_u32(fin), 0, kDrainNs);
     if (s_bad)
-      for (int t = max(0, n_tiles - kStages); t < n_tiles; ++t)
-        mbar_wait(smem_u32(&full[t % kStages]), (t / kStages) & 1, kDrainNs);
+      for (int t = max(0, n_tiles - kNS); t < n_tiles; ++t)
+        mbar_wait(smem_u32(&full[t % kNS]), (t / kNS) & 1, kDrainNs);
   }
   tc_fence_before();
   __syncthreads();

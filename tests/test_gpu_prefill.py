@@ -116,9 +116,10 @@ def test_prefill_matches_oracle(name, chunk, prefill_kernel):
     check(run_prefill(dev, q, qs), oracle(scn, q, qs), dev.plan.w.kv_dtype)
 
 
-@pytest.mark.parametrize("name", ["qwen_small", "qwen_small_f16", "mha_t32"])
+@pytest.mark.parametrize("name", ["qwen_small", "qwen_small_f16", "mha_t32", "fp8_small"])
 def test_tcgen05_and_mma_sync_kernels_agree(name):
-    """The two prefill kernels compute the same attention (rounding apart)."""
+    """The two prefill kernels compute the same attention (rounding apart),
+    E4M3 caches included (widened to f16 in shared memory on tcgen05)."""
     dev, _ = state(name)
     n = W.chunk_lens(dev.plan.w, dev.plan.ctx, 300)
     q, qs = chunk_inputs(dev, n)
@@ -130,7 +131,7 @@ def test_tcgen05_and_mma_sync_kernels_agree(name):
         finally:
             pkv.pkv_set_prefill_kernel("auto")
     err = (outs[0] - outs[1]).abs()
-    assert not torch.isnan(outs[0]).any() and err.max().item() <= 2e-2
+    assert not torch.isnan(outs[0]).any() and err.max().item() <= TOL[dev.plan.w.kv_dtype][0]
 
 
 def test_tcgen05_choice_rejects_other_caches():
