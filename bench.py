@@ -31,9 +31,13 @@ sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = "qwen_gqa_bf16"
 METRIC = "paged decode attention KV GB/s & fraction of GB300 HBM peak; decode tokens/s"
-KERNEL_SOURCES = ["attention.cu", "attention.h", "attention_simt.cuh", "attention_tc.cuh",
-                  "attention_tc_launch.cuh", "attention_stream.cuh", "device_common.cuh",
-                  "attention_prefill.cu", "attention_prefill_umma.cuh"]
+# the sources each kernel family's recorded DRAM counters depend on
+KERNEL_SOURCES = {
+    "decode": ["attention.cu", "attention.h", "attention_simt.cuh", "attention_tc.cuh",
+               "attention_tc_launch.cuh", "attention_stream.cuh", "device_common.cuh"],
+    "prefill": ["attention_prefill.cu", "attention_prefill_umma.cuh", "attention_tc.cuh", "attention.h",
+                "device_common.cuh"],
+}
 NOMINAL_HBM_GBS = 7900.0  # GB300 HBM3e, nominal
 
 
@@ -67,9 +71,9 @@ def peaks():
     return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+def kernel_source_hash(family: str = "decode") -> str:
     h = hashlib.sha256()
-    for n in KERNEL_SOURCES:
+    for n in KERNEL_SOURCES[family]:
         h.update(open(os.path.join(ROOT, "paged_kv_cache_137_gb300", "csrc", n), "rb").read())
     return h.hexdigest()[:16]
 
@@ -149,7 +153,8 @@ def traffic_for(config: str, kernels: str):
         return None
     d = json.load(open(p))
     e = d.get(config)
-    if not e or e.get("kernel_sha") != kernel_source_hash():
+    family = "prefill" if e and e.get("kernel", "").startswith("prefill") else "decode"
+    if not e or e.get("kernel_sha") != kernel_source_hash(family):
         return None
     if not kernels.startswith(e.get("kernel", "?").split("<")[0]):
         return None
