@@ -31,6 +31,8 @@ CASES = {
                           head_dim=64, num_blocks=300, ctx_range=(1, 800), block_size=32, seed=93),
     "fp8_small": W.scaled(W.get("fp8_churn"), num_seqs=6, num_blocks=1024, churn=300,
                           ctx_range=(1, 900)),
+    "fp8_t32_qf16": W.scaled(W.get("fp8_churn"), num_seqs=4, num_blocks=512, churn=100,
+                             ctx_range=(300, 1100), block_size=32, q_dtype="f16", seed=1398),
 }
 
 
