@@ -237,8 +237,9 @@ PKV_API pkv_status pkv_set_attention_kernel(int32_t kind);
  * A pair of context ctx gets ceil(ctx / partition) splits (the tensor-core
  * kernel shares its 64-token tiles evenly over them).  For partition_tokens 0
  * it is the smallest multiple of 64 (and of the block size) for which the
- * expected splits fit in one wave of resident CTAs on the current device, or
- * 8192 when the (sequence, KV head) pairs alone exceed the slots. */
+ * expected splits fit in one wave of resident CTAs on the current device; when
+ * the (sequence, KV head) pairs alone fill two waves, half the longest context
+ * (max_blocks * T / 2, rounded up), at least 4096 and at most 8192 tokens. */
 PKV_API int32_t pkv_attention_partition(int32_t num_seqs, int32_t max_blocks, const pkv_kv_desc* desc,
                                 int32_t partition_tokens);
 

@@ -33,6 +33,7 @@ namespace {
 
 constexpr int kMinPartition = 256;
 constexpr int kMaxPartition = 8192;
+constexpr int kMultiWavePartition = 4096;  // the smallest split when the pairs fill two waves
 // Resident tensor-core split CTAs per SM: four for E4M3 caches (the
 // head-columns kernel that every query group up to 8 takes), else three.
 int resident_split_ctas(const pkv_kv_desc* d) { return d->kv_dtype == PKV_E4M3 ? 4 : 3; }
@@ -56,17 +57,22 @@ int device_sms() {
 
 // Automatic partition: the fewest tokens per split (a multiple of 64 and of
 // the block size) for which the expected (sequence, head, split) units fit in
-// one wave of resident CTAs, so that no unit waits for a slot; with more
-// (sequence, head) pairs than slots, no split at all (up to the maximum).
-// Lengths are expected to spread evenly up to max_ctx, and each pair's last
-// split to be half full.
+// one wave of resident CTAs, so that no unit waits for a slot.  Lengths are
+// expected to spread evenly up to max_ctx, and each pair's last split to be
+// half full.  With more (sequence, head) pairs than two waves of slots, the
+// hardware balances the waves itself and splits cost merges; only the longest
+// sequences are split in two (half of max_ctx, at least kMultiWavePartition),
+// so that no single unit holds the tail of the last wave.
 int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx, int32_t block_size,
                        int ctas_per_sm) {
   const int64_t slots = static_cast<int64_t>(device_sms()) * ctas_per_sm;
   const int64_t pairs = num_seqs * num_kv_heads;
   const int64_t est_tokens = pairs * std::max<int64_t>(max_ctx, 1) / 2;
   const int32_t step = std::max<int32_t>(64, block_size);
-  if (2 * slots <= pairs + 2) return kMaxPartition;
+  if (2 * slots <= pairs + 2) {
+    const int64_t half = (std::max<int64_t>(max_ctx, 1) / 2 + step - 1) / step * step;
+    return static_cast<int32_t>(std::min<int64_t>(kMaxPartition, std::max<int64_t>(kMultiWavePartition, half)));
+  }
   const int64_t free_slots = slots - pairs / 2;
   int64_t p = (est_tokens + free_slots - 1) / free_slots;
   p = (p + step - 1) / step * step;
