@@ -195,3 +195,23 @@ def test_descriptor_head_scales_are_checked_before_any_launch():
     d.head_scales = 0x1002                    # not 4-byte aligned
     assert lib.pkv_write(nothing, nothing, nothing, nothing, pkv.PKV_BF16, None, 0,
                          ctypes.byref(d), 1.0, 1.0, None) == pkv.PKV_ERR_INVALID_ARG
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="the automatic partition follows the device's SM count; pinned for 152 SMs")
+def test_automatic_partition_rule():
+    """pkv_attention_partition(0) on the host's default of 152 SMs: one wave of
+    split units when the pairs fit (Qwen-shaped batch: 1,536 tokens); when the
+    (sequence, KV head) pairs fill two waves, half the longest context, at
+    least 4,096 and at most 8,192 tokens."""
+    bf16 = pkv.kv_desc(8500, 4, 128, 16, "bf16")
+    e4m3 = pkv.kv_desc(65536, 8, 128, 16, "e4m3")
+    fork = pkv.kv_desc(8192, 8, 128, 16, "bf16")
+    assert pkv.pkv_attention_partition(64, 243, bf16) == 1536      # 452 units <= 456 slots
+    assert pkv.pkv_attention_partition(512, 509, e4m3) == 4096     # longest 8,144 split in two
+    assert pkv.pkv_attention_partition(256, 96, fork) == 4096      # 1,536-token contexts stay whole
+    assert pkv.pkv_attention_partition(4096, 2048, e4m3) == 8192   # half of 32,768, capped
+    assert pkv.pkv_attention_partition(64, 243, bf16, 512) == 512  # an explicit partition stands
+    for n, mb in ((1, 1), (3, 700), (200, 40)):
+        p = pkv.pkv_attention_partition(n, mb, bf16)
+        assert p % 64 == 0 and 256 <= p <= 8192
