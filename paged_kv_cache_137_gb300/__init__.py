@@ -143,6 +143,23 @@ def lib():
     return _lib
 
 
+_FAST = {}
+
+
+def _fast(name: str):
+    """The C function with its pointer arguments taken as plain addresses
+    (c_void_p) instead of typed pointers, for the allocator's per-step calls:
+    building a typed pointer per argument costs more than the call itself."""
+    f = _FAST.get(name)
+    if f is None:
+        restype, argtypes = _SIGNATURES[name]
+        f = lib()[name]  # a separate function object; the typed one stays as it is
+        f.restype = restype
+        f.argtypes = [_P if t in (_PI32, _PI64) else t for t in argtypes]
+        _FAST[name] = f
+    return f
+
+
 def _check(status: int):
     if status != PKV_OK:
         raise PkvError(status, lib().pkv_last_error().decode())
@@ -207,6 +224,7 @@ class Pool:
         _check(lib().pkv_pool_create(self.num_blocks, self.block_size,
                                      _i32p(order) if order is not None else None, ctypes.byref(h)))
         self._h = h
+        self._bufs = {}    # per-step scratch (a handle is used from one thread)
 
     def __del__(self):
         if getattr(self, "_h", None) and _lib is not None:
@@ -229,16 +247,25 @@ class Pool:
                                     ctypes.byref(n_cow)))
         return slots[:n_new], cow[:2 * n_cow.value].reshape(-1, 2)
 
+    def _buf(self, name: str, n: int, dtype):
+        """A reusable host buffer of at least n elements and its address."""
+        b = self._bufs.get(name)
+        if b is None or b[0].size < n:
+            arr = np.empty(max(n, 64), dtype=dtype)
+            b = self._bufs[name] = (arr, arr.ctypes.data)
+        return b
+
     def batch_append(self, seq_ids):
         """One token per sequence, all-or-nothing -> (slots int64[B], cow int32[n, 2])"""
-        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
-        n = len(ids)
-        slots = np.empty(max(n, 1), dtype=np.int64)
-        cow = np.empty(2 * max(n, 1), dtype=np.int32)
-        n_cow = ctypes.c_int32(0)
-        _check(lib().pkv_batch_append(self._h, _i64p(ids), n, _i64p(slots), _i32p(cow), n,
-                                      ctypes.byref(n_cow)))
-        return slots[:n], cow[:2 * n_cow.value].reshape(-1, 2)
+        n = len(seq_ids)
+        ids, ids_p = self._buf("ids", n, np.int64)
+        ids[:n] = seq_ids
+        slots, slots_p = self._buf("slots", n, np.int64)
+        cow, cow_p = self._buf("cow", 2 * n, np.int32)
+        ncow, ncow_p = self._buf("ncow", 1, np.int32)
+        _check(_fast("pkv_batch_append")(self._h.value, ids_p, n, slots_p, cow_p, n, ncow_p))
+        k = int(ncow[0])
+        return slots[:n].copy(), cow[:2 * k].reshape(-1, 2).copy()
 
     def seq_fork(self, parent: int, child: int):
         _check(lib().pkv_seq_fork(self._h, int(parent), int(child)))
@@ -258,11 +285,13 @@ class Pool:
 
     def block_tables(self, seq_ids, max_blocks: int):
         """-> (tables int32[B, max_blocks] padded with -1, context_lens int32[B])"""
-        ids = np.ascontiguousarray(seq_ids, dtype=np.int64)
-        tables = np.empty((len(ids), max_blocks), dtype=np.int32)
-        ctx = np.empty(len(ids), dtype=np.int32)
-        _check(lib().pkv_block_tables(self._h, _i64p(ids), len(ids), int(max_blocks), _i32p(tables),
-                                      _i32p(ctx)))
+        n = len(seq_ids)
+        ids, ids_p = self._buf("ids", n, np.int64)
+        ids[:n] = seq_ids
+        tables = np.empty((n, max_blocks), dtype=np.int32)
+        ctx = np.empty(n, dtype=np.int32)
+        _check(_fast("pkv_block_tables")(self._h.value, ids_p, n, int(max_blocks),
+                                            tables.ctypes.data, ctx.ctypes.data))
         return tables, ctx
 
     def block_refcount(self, block: int) -> int:
