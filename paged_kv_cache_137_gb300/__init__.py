@@ -160,6 +160,22 @@ def _fast(name: str):
     return f
 
 
+def _host_i32_address(x, shape, what: str) -> int:
+    """Address of a C-contiguous int32 host buffer of the given shape (a
+    NumPy array or a CPU tensor); ValueError otherwise."""
+    if isinstance(x, np.ndarray):
+        ok = x.dtype == np.int32 and x.flags.c_contiguous and x.flags.writeable
+        addr = x.ctypes.data
+    else:
+        import torch
+        ok = (isinstance(x, torch.Tensor) and x.device.type == "cpu" and x.dtype == torch.int32
+              and x.is_contiguous())
+        addr = x.data_ptr() if ok else 0
+    if not ok or tuple(x.shape) != tuple(shape):
+        raise ValueError(f"{what} must be a C-contiguous int32 host buffer of shape {tuple(shape)}")
+    return addr
+
+
 def _check(status: int):
     if status != PKV_OK:
         raise PkvError(status, lib().pkv_last_error().decode())
@@ -283,15 +299,25 @@ class Pool:
                                    ctypes.byref(ln)))
         return out[:n.value], ln.value
 
-    def block_tables(self, seq_ids, max_blocks: int):
-        """-> (tables int32[B, max_blocks] padded with -1, context_lens int32[B])"""
+    def block_tables(self, seq_ids, max_blocks: int, out=None):
+        """-> (tables int32[B, max_blocks] padded with -1, context_lens int32[B])
+
+        out: optional (tables, context_lens) to fill instead of fresh arrays:
+        C-contiguous int32 host arrays or CPU tensors (pinned ones can go
+        to the device by one copy each) of exactly those shapes; returned as
+        given.  On an error neither is written."""
         n = len(seq_ids)
         ids, ids_p = self._buf("ids", n, np.int64)
         ids[:n] = seq_ids
-        tables = np.empty((n, max_blocks), dtype=np.int32)
-        ctx = np.empty(n, dtype=np.int32)
-        _check(_fast("pkv_block_tables")(self._h.value, ids_p, n, int(max_blocks),
-                                            tables.ctypes.data, ctx.ctypes.data))
+        if out is None:
+            tables = np.empty((n, max_blocks), dtype=np.int32)
+            ctx = np.empty(n, dtype=np.int32)
+            t_p, c_p = tables.ctypes.data, ctx.ctypes.data
+        else:
+            tables, ctx = out
+            t_p = _host_i32_address(tables, (n, int(max_blocks)), "tables")
+            c_p = _host_i32_address(ctx, (n,), "context_lens")
+        _check(_fast("pkv_block_tables")(self._h.value, ids_p, n, int(max_blocks), t_p, c_p))
         return tables, ctx
 
     def block_refcount(self, block: int) -> int:

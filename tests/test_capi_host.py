@@ -8,6 +8,7 @@ import re
 
 import numpy as np
 import pytest
+import torch
 
 import workloads as W
 from oracle import scenario as OS
@@ -156,6 +157,29 @@ def test_block_tables_padding_and_usage():
     with pytest.raises(pkv.PkvError):
         p.block_tables([5], 1)
     assert p.usage() == (2, 20, 2)
+
+
+def test_block_tables_into_caller_buffers():
+    p = pkv.Pool(8, 16, [7, 6, 5, 4, 3, 2, 1, 0])
+    for s, n in ((5, 20), (6, 0), (9, 33)):
+        p.seq_create(s)
+        p.seq_append(s, n)
+    want_t, want_c = p.block_tables([9, 5, 6], 4)
+    for make in (lambda shape: np.full(shape, 77, np.int32),
+                 lambda shape: torch.full(shape, 77, dtype=torch.int32)):
+        t, c = make((3, 4)), make((3,))
+        got = p.block_tables([9, 5, 6], 4, out=(t, c))
+        assert got[0] is t and got[1] is c
+        assert np.array_equal(np.asarray(t), want_t) and np.array_equal(np.asarray(c), want_c)
+        # a failing call writes neither buffer
+        t2, c2 = make((1, 1)), make((1,))
+        with pytest.raises(pkv.PkvError):
+            p.block_tables([9], 1, out=(t2, c2))
+        assert np.asarray(t2).tolist() == [[77]] and np.asarray(c2).tolist() == [77]
+    for bad in (np.zeros((3, 4), np.int64), np.zeros((4, 3), np.int32),
+                np.zeros((4, 3), np.int32).T, torch.zeros((3, 4), dtype=torch.int64)):
+        with pytest.raises(ValueError):
+            p.block_tables([9, 5, 6], 4, out=(bad, np.zeros(3, np.int32)))
 
 
 @pytest.mark.parametrize("name", ["tiny_fp32", "qwen_gqa_bf16", "prefix_fork_bf16", "long_mha_bf16",
