@@ -155,9 +155,24 @@ class DeviceScenario:
         return self.decode_step(stream)
 
     def kv_bytes(self) -> int:
-        """Algorithmic K/V bytes one attention call reads: each element once."""
+        """Logical K/V bytes one attention call serves: every sequence's
+        context once (a block shared by n sequences counts n times)."""
         w = self.plan.w
         return int(2 * int(self.plan.ctx.sum()) * w.num_kv_heads * w.head_dim * w.kv_bytes)
+
+    def kv_unique_bytes(self) -> int:
+        """K/V bytes of the distinct cache slots the call reads: each stored
+        element once, however many sequences share its block (equal to
+        kv_bytes() when no block is shared)."""
+        w, tab, ctx = self.plan.w, self.plan.tables, self.plan.ctx
+        t = w.block_size
+        filled = {}  # physical block -> slots read in it (the longest use)
+        for r, c in enumerate(ctx):
+            c = int(c)
+            for j in range(-(-c // t)):
+                b = int(tab[r, j])
+                filled[b] = max(filled.get(b, 0), min(t, c - j * t))
+        return int(2 * sum(filled.values()) * w.num_kv_heads * w.head_dim * w.kv_bytes)
 
 
 def _kv_of(w, pw: PrefillWrite):

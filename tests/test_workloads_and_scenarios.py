@@ -81,6 +81,32 @@ def test_prefix_fork_scenario_structure():
         assert a.block_refcount(a.table(s)[-1]) == 1
 
 
+@pytest.mark.parametrize("name", ["tiny_fp32", "qwen_gqa_bf16", "long_mha_bf16", "fp8_churn",
+                                  "prefix_fork_bf16"])
+def test_unique_kv_bytes(name):
+    """The roofline's algorithmic bytes: with no shared block they are the
+    logical bytes; for the prefix fork, the distinct cached tokens are the
+    prefix once, every parent's tail, and per child the slots of its own
+    copied last block (positions floor(prior / T) * T .. prior)."""
+    from paged_kv_cache_137_gb300 import scenario as PS
+    w = W.get(name)
+
+    class Host:  # the byte counts need the plan only, not the device buffers
+        plan = PS.plan(w)
+
+    unique = PS.DeviceScenario.kv_unique_bytes(Host)
+    logical = PS.DeviceScenario.kv_bytes(Host)
+    per_token = 2 * w.num_kv_heads * w.head_dim * w.kv_bytes
+    if w.ctx_dist != "prefix_fork":
+        assert unique == logical == per_token * int(W.context_lens(w).sum())
+        return
+    f = W.fork_layout(w)
+    prior = w.prefix_len + f["tails"] - 1
+    tokens = w.prefix_len + int(f["tails"].sum()) + int((prior[f["parent_of_child"]] % w.block_size + 1).sum())
+    assert unique == per_token * tokens
+    assert logical == per_token * int(f["ctx"].sum()) > 6 * unique
+
+
 def test_churn_scrambles_but_returns_every_block():
     w = W.get("fp8_churn")
     from oracle.allocator import BlockAllocator
