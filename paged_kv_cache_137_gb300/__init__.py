@@ -63,10 +63,10 @@ def kv_desc(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype, head_scale
         kv_dtype = DTYPE_OF_NAME[kv_dtype]
     d = pkv_kv_desc(num_blocks, num_kv_heads, head_dim, block_size, kv_dtype)
     if head_scales is not None:
-        import torch
-        if (head_scales.dtype != torch.float32 or tuple(head_scales.shape) != (4, num_kv_heads)
+        if (not isinstance(head_scales, torch.Tensor) or not head_scales.is_cuda
+                or head_scales.dtype != torch.float32 or tuple(head_scales.shape) != (4, num_kv_heads)
                 or not head_scales.is_contiguous()):
-            raise ValueError("head_scales must be a contiguous float32 tensor [4, num_kv_heads]")
+            raise ValueError("head_scales must be a contiguous float32 CUDA tensor [4, num_kv_heads]")
         d.head_scales = head_scales.data_ptr()
         d._head_scales = head_scales
     return d

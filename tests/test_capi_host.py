@@ -215,6 +215,11 @@ def test_descriptor_head_scales_are_checked_before_any_launch():
         st = lib.pkv_write(nothing, nothing, nothing, nothing, pkv.PKV_BF16, None, 0,
                            ctypes.byref(d), 1.0, 1.0, None)
         assert st == want, (dtype, st, lib.pkv_last_error())
+    # the binding takes the table from a CUDA tensor only: a host address
+    # would reach the kernels as a device pointer
+    for bad in (torch.ones(4, 2), np.ones((4, 2), np.float32), torch.ones(2, 4, dtype=torch.float64)):
+        with pytest.raises(ValueError):
+            pkv.kv_desc(16, 2, 128, 16, "e4m3", head_scales=bad)
     d = pkv.kv_desc(16, 2, 128, 16, "e4m3")
     d.head_scales = 0x1002                    # not 4-byte aligned
     assert lib.pkv_write(nothing, nothing, nothing, nothing, pkv.PKV_BF16, None, 0,
