@@ -80,9 +80,9 @@ def kernel_source_hash(family: str = "decode") -> str:
 
 def allocator_step_us(plan, steps: int = 200) -> float:
     """Host time of one decode step of the native allocator for the plan's
-    batch: pkv_batch_append of one token per sequence, then pkv_block_tables
-    for the whole batch into reused host buffers (a fresh pool replaying the
-    plan's prefill)."""
+    batch: pkv_batch_append of one token per sequence, then
+    pkv_block_tables_update of the batch's tables kept across steps (a fresh
+    pool replaying the plan's prefill)."""
     import numpy as np
     import paged_kv_cache_137_gb300 as pkv
     w = plan.w
@@ -95,14 +95,16 @@ def allocator_step_us(plan, steps: int = 200) -> float:
         pool.seq_create(s)
         pool.seq_append(s, int(c))
     max_blocks = plan.max_blocks + steps // w.block_size + 2
-    # tables written into the same host buffers every step, as a serving loop
-    # that stages them for one copy to the device would
-    out = (np.empty((len(plan.seq_ids), max_blocks), dtype=np.int32),
-           np.empty(len(plan.seq_ids), dtype=np.int32))
+    # the batch's tables kept in host buffers across steps and brought up to
+    # date incrementally, as a serving loop that stages them for one copy to
+    # the device would
+    ids = np.asarray(plan.seq_ids, dtype=np.int64)
+    rows = pool.block_tables_rows(len(ids), max_blocks)
+    rows.update(ids)
     t0 = time.perf_counter()
     for _ in range(steps):
-        pool.batch_append(plan.seq_ids)
-        pool.block_tables(plan.seq_ids, max_blocks, out=out)
+        pool.batch_append(ids)
+        rows.update(ids)
     return (time.perf_counter() - t0) / steps * 1e6
 
 

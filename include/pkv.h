@@ -162,6 +162,33 @@ PKV_API pkv_status pkv_seq_table(const pkv_pool* pool, int64_t seq_id, int32_t* 
 PKV_API pkv_status pkv_block_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_t n_seqs,
                             int32_t max_blocks, int32_t* tables_out, int32_t* context_lens_out);
 
+/* pkv_block_tables for a buffer kept across decode steps: the same result
+ * (row i = the table of seq_ids[i] padded with -1, context lengths), but a
+ * row is only rewritten from its last entry on when it was last written by
+ * this call for the same sequence and max_blocks, so a step costs O(n_seqs +
+ * new entries) instead of O(n_seqs * max_blocks).  Between two calls a live
+ * sequence's table only grows at its end, and a copy-on-write replaces only
+ * the entry its next token lands in, which is never before the last entry
+ * the row held (a table gains a block only when the previous one is full
+ * [D][C "Concept"]; copy-on-write replaces the shared block being written
+ * [A "Complex Topologies"]).
+ *   tables_inout      host int32[n_seqs][max_blocks], caller-owned, kept
+ *                     between calls (its first contents do not matter).
+ *   rows_inout        host int64[n_seqs][2], caller-owned, opaque; all zero
+ *                     the first time (or to force a full rewrite).  It
+ *                     names the sequence incarnation a row holds (unique for
+ *                     the pool's life: a sequence created again under the
+ *                     same id, a fork child, a re-admitted sequence each get
+ *                     a new one), so batches may reorder or replace rows.
+ *   context_lens_out  host int32[n_seqs].
+ * Errors as pkv_block_tables, checked before anything is written.  The
+ * caller must not change a row between calls other than through this call
+ * (or must zero its state). */
+PKV_API pkv_status pkv_block_tables_update(const pkv_pool* pool, const int64_t* seq_ids,
+                                           int32_t n_seqs, int32_t max_blocks,
+                                           int32_t* tables_inout, int64_t* rows_inout,
+                                           int32_t* context_lens_out);
+
 /* Reference count of one block (0 = free). */
 PKV_API pkv_status pkv_block_refcount(const pkv_pool* pool, int32_t block, int32_t* refcount);
 

@@ -97,6 +97,7 @@ _SIGNATURES = {
     "pkv_seq_free": (_I32, [_P, _I64]),
     "pkv_seq_table": (_I32, [_P, _I64, _PI32, _I32, _PI32, _PI64]),
     "pkv_block_tables": (_I32, [_P, _PI64, _I32, _I32, _PI32, _PI32]),
+    "pkv_block_tables_update": (_I32, [_P, _PI64, _I32, _I32, _PI32, _PI64, _PI32]),
     "pkv_block_refcount": (_I32, [_P, _I32, _PI32]),
     "pkv_num_free_blocks": (_I32, [_P]),
     "pkv_free_stack": (_I32, [_P, _PI32, _I32, _PI32]),
@@ -226,6 +227,46 @@ def pkv_dtype_bytes(dtype) -> int:
 
 
 # --------------------------------------------------------------- allocator
+class BlockTableRows:
+    """A batch's block tables kept on the host across decode steps and
+    brought up to date by pkv_block_tables_update: each step rewrites only
+    the entries that can have changed (a row's last entry and what was
+    appended), or the whole row when it now holds another sequence.
+
+    tables: int32 CPU tensor [capacity, max_blocks]; context_lens: int32
+    [capacity] (pinned if asked, so that they reach the device by one copy
+    each).  update(seq_ids) fills their first len(seq_ids) rows and returns
+    those views.  The rows belong to this object: writing them otherwise
+    needs reset()."""
+
+    def __init__(self, pool: "Pool", capacity: int, max_blocks: int, pin_memory: bool = False):
+        self.pool, self.capacity, self.max_blocks = pool, int(capacity), int(max_blocks)
+        self.tables = torch.full((self.capacity, self.max_blocks), -1, dtype=torch.int32,
+                                 pin_memory=pin_memory)
+        self.context_lens = torch.zeros(self.capacity, dtype=torch.int32, pin_memory=pin_memory)
+        self._rows = np.zeros((self.capacity, 2), dtype=np.int64)
+        self._addr = (self.tables.data_ptr(), self._rows.ctypes.data, self.context_lens.data_ptr())
+        self._views = {}   # n -> (tables[:n], context_lens[:n]): slicing a tensor costs µs
+
+    def reset(self):
+        """Forget what the rows hold: the next update rewrites them whole."""
+        self._rows[:] = 0
+
+    def update(self, seq_ids):
+        n = len(seq_ids)
+        if n > self.capacity:
+            raise ValueError(f"{n} sequences exceed the {self.capacity} rows")
+        ids, ids_p = self.pool._buf("ids", n, np.int64)
+        ids[:n] = seq_ids
+        t_p, r_p, c_p = self._addr
+        _check(_fast("pkv_block_tables_update")(self.pool._h.value, ids_p, n, self.max_blocks, t_p,
+                                                r_p, c_p))
+        v = self._views.get(n)
+        if v is None:
+            v = self._views[n] = (self.tables[:n], self.context_lens[:n])
+        return v
+
+
 class Pool:
     """A native block allocator (free stack, tables, reference counts)."""
 
@@ -319,6 +360,11 @@ class Pool:
             c_p = _host_i32_address(ctx, (n,), "context_lens")
         _check(_fast("pkv_block_tables")(self._h.value, ids_p, n, int(max_blocks), t_p, c_p))
         return tables, ctx
+
+    def block_tables_rows(self, capacity: int, max_blocks: int, pin_memory: bool = False):
+        """Host buffers for pkv_block_tables_update, kept across decode steps
+        (see BlockTableRows)."""
+        return BlockTableRows(self, capacity, max_blocks, pin_memory)
 
     def block_refcount(self, block: int) -> int:
         rc = ctypes.c_int32(0)

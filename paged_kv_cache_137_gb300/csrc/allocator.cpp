@@ -66,6 +66,9 @@ struct Seq {
   // (-1: not published / unknown)
   std::vector<int32_t> tokens;
   std::vector<int64_t> chain;
+  // unique over the pool's life: a new sequence (also a fork child, or an id
+  // used again) gets a new one, so a caller's copy of a table can tell
+  int64_t incarnation = 0;
 };
 
 // One published block and its content key bytes (parent entry, token ids).
@@ -104,12 +107,19 @@ struct pkv_pool {
   std::vector<std::list<int32_t>::iterator> lru_pos;
   std::vector<char> in_lru;
   int64_t hit_tokens = 0, evictions = 0;
+  int64_t next_incarnation = 1;  // 0 never names a sequence
 };
 
 namespace pkv {
 namespace {
 
 inline int64_t blocks_for(int64_t tokens, int32_t t) { return (tokens + t - 1) / t; }
+
+// Insert a new sequence under a fresh incarnation number.
+Seq& add_seq(pkv_pool* p, int64_t seq_id, Seq&& s) {
+  s.incarnation = p->next_incarnation++;
+  return p->seqs.emplace(seq_id, std::move(s)).first->second;
+}
 
 // Blocks a pop can hand out: the free stack, then (with prefix caching) the
 // cached blocks nobody references.
@@ -372,7 +382,7 @@ pkv_status pkv_seq_create(pkv_pool* pool, int64_t seq_id) {
     pkv::set_error("sequence %lld exists", (long long)seq_id);
     return PKV_ERR_INVALID_ARG;
   }
-  pool->seqs.emplace(seq_id, pkv::Seq{});
+  pkv::add_seq(pool, seq_id, pkv::Seq{});
   return PKV_OK;
 }
 
@@ -406,6 +416,12 @@ pkv_status pkv_batch_append(pkv_pool* pool, const int64_t* seq_ids, int32_t n_se
   // no cached block is evicted for a batch that then fails)
   // (in batch order, with running totals, so that the first failing
   // sequence and its error are the ones a sequential append would meet)
+  // the sequences found here serve the second pass too (appends insert no
+  // sequence, so the pointers stay valid); both buffers are reused per thread
+  static thread_local std::vector<pkv::Seq*> batch;
+  static thread_local std::vector<pkv::AppendUndo> undo;
+  batch.clear();
+  undo.clear();
   {
     int64_t need = 0, cows = 0;
     for (int32_t i = 0; i < n_seqs; ++i) {
@@ -414,6 +430,7 @@ pkv_status pkv_batch_append(pkv_pool* pool, const int64_t* seq_ids, int32_t n_se
         pkv::set_error("unknown sequence %lld", (long long)seq_ids[i]);
         return PKV_ERR_UNKNOWN_SEQ;
       }
+      batch.push_back(&it->second);
       bool cow = false;
       need += pkv::blocks_needed(pool, it->second, 1, &cow);
       if (need > pkv::available(pool)) {
@@ -428,22 +445,13 @@ pkv_status pkv_batch_append(pkv_pool* pool, const int64_t* seq_ids, int32_t n_se
       }
     }
   }
-  std::vector<pkv::AppendUndo> undo;
-  undo.reserve(n_seqs);
   int32_t n_cow = 0;
   for (int32_t i = 0; i < n_seqs; ++i) {
-    auto it = pool->seqs.find(seq_ids[i]);
-    pkv_status st;
-    if (it == pool->seqs.end()) {
-      pkv::set_error("unknown sequence %lld", (long long)seq_ids[i]);
-      st = PKV_ERR_UNKNOWN_SEQ;
-    } else {
-      undo.emplace_back();
-      st = pkv::append_one(pool, seq_ids[i], it->second, 1, slots_out + i, cow_out, cow_cap,
-                           &n_cow, &undo.back());
-      if (st != PKV_OK) undo.pop_back();
-    }
+    undo.emplace_back();
+    const pkv_status st = pkv::append_one(pool, seq_ids[i], *batch[i], 1, slots_out + i, cow_out,
+                                          cow_cap, &n_cow, &undo.back());
     if (st != PKV_OK) {
+      undo.pop_back();
       for (auto u = undo.rbegin(); u != undo.rend(); ++u) pkv::undo_append(pool, *u);
       if (n_cow_out) *n_cow_out = 0;
       return st;
@@ -466,7 +474,7 @@ pkv_status pkv_seq_fork(pkv_pool* pool, int64_t parent_id, int64_t child_id) {
   }
   pkv::Seq child = it->second;  // copy the table, not the memory
   for (int32_t b : child.table) pool->refcount[b] += 1;
-  pool->seqs.emplace(child_id, std::move(child));
+  pkv::add_seq(pool, child_id, std::move(child));
   return PKV_OK;
 }
 
@@ -523,6 +531,50 @@ pkv_status pkv_block_tables(const pkv_pool* pool, const int64_t* seq_ids, int32_
     const int32_t n = static_cast<int32_t>(s.table.size());
     std::copy(s.table.begin(), s.table.end(), row);
     std::fill(row + n, row + max_blocks, -1);
+    context_lens_out[i] = static_cast<int32_t>(s.len);
+  }
+  return PKV_OK;
+}
+
+pkv_status pkv_block_tables_update(const pkv_pool* pool, const int64_t* seq_ids, int32_t n_seqs,
+                                   int32_t max_blocks, int32_t* tables_inout, int64_t* rows_inout,
+                                   int32_t* context_lens_out) {
+  if (!pool) return fail(PKV_ERR_INVALID_ARG, "pool is NULL");
+  if (n_seqs < 0 || max_blocks < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (n_seqs > 0 && (!seq_ids || !tables_inout || !rows_inout || !context_lens_out))
+    return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  for (int32_t i = 0; i < n_seqs; ++i) {
+    auto it = pool->seqs.find(seq_ids[i]);
+    if (it == pool->seqs.end()) {
+      pkv::set_error("unknown sequence %lld", (long long)seq_ids[i]);
+      return PKV_ERR_UNKNOWN_SEQ;
+    }
+    if (static_cast<int64_t>(it->second.table.size()) > max_blocks)
+      return fail(PKV_ERR_INVALID_ARG, "a block table is longer than max_blocks");
+    if (it->second.len > std::numeric_limits<int32_t>::max())
+      return fail(PKV_ERR_INVALID_ARG, "a context length exceeds INT32_MAX");
+  }
+  for (int32_t i = 0; i < n_seqs; ++i) {
+    const auto& s = pool->seqs.find(seq_ids[i])->second;
+    int32_t* row = tables_inout + static_cast<int64_t>(i) * max_blocks;
+    int64_t* state = rows_inout + 2 * static_cast<int64_t>(i);
+    const int64_t n = static_cast<int64_t>(s.table.size());
+    // Between two calls a live sequence's table only grows at its end, and
+    // a copy-on-write replaces the entry at len / T, which is at least the
+    // last entry the row held (len never shrinks).  So a row last written
+    // for this incarnation is rewritten from its last entry on; any other
+    // row is written whole.
+    // state: the incarnation, then (max_blocks << 32) | entries held
+    const int64_t held = state[1] & 0xffffffffLL;
+    int64_t from = 0;
+    if (state[0] == s.incarnation && (state[1] >> 32) == max_blocks && held <= n) {
+      from = std::max<int64_t>(held - 1, 0);
+    } else {
+      std::fill(row + n, row + max_blocks, -1);
+    }
+    std::copy(s.table.begin() + from, s.table.end(), row + from);
+    state[0] = s.incarnation;
+    state[1] = (static_cast<int64_t>(max_blocks) << 32) | n;
     context_lens_out[i] = static_cast<int32_t>(s.len);
   }
   return PKV_OK;
@@ -598,7 +650,7 @@ pkv_status pkv_seq_create_cached(pkv_pool* pool, int64_t seq_id, const int32_t* 
   s.tokens.assign(token_ids, token_ids + s.len);
   pool->hit_tokens += s.len;
   if (n_cached) *n_cached = static_cast<int32_t>(s.len);
-  pool->seqs.emplace(seq_id, std::move(s));
+  pkv::add_seq(pool, seq_id, std::move(s));
   return PKV_OK;
 }
 
@@ -713,10 +765,9 @@ pkv_status pkv_seq_admit(pkv_pool* pool, int64_t seq_id, int32_t n_tokens, int32
                    n_tokens, (long long)need, watermark_blocks, (long long)pkv::available(pool));
     return PKV_ERR_OUT_OF_BLOCKS;
   }
-  auto ins = pool->seqs.emplace(seq_id, pkv::Seq{});
+  pkv::Seq& s = pkv::add_seq(pool, seq_id, pkv::Seq{});
   int32_t n_cow = 0;
-  return pkv::append_one(pool, seq_id, ins.first->second, n_tokens, slots_out, nullptr, 0, &n_cow,
-                         nullptr);
+  return pkv::append_one(pool, seq_id, s, n_tokens, slots_out, nullptr, 0, &n_cow, nullptr);
 }
 
 }  // extern "C"

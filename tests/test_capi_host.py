@@ -244,3 +244,100 @@ def test_automatic_partition_rule():
     for n, mb in ((1, 1), (3, 700), (200, 40)):
         p = pkv.pkv_attention_partition(n, mb, bf16)
         assert p % 64 == 0 and 256 <= p <= 8192
+
+
+@pytest.mark.parametrize("seed", range(6))
+def test_incremental_block_tables_equal_full_ones(seed):
+    """pkv_block_tables_update against pkv_block_tables after every step of a
+    random stream of appends, batch appends, mid-block forks (copy-on-write),
+    frees, ids created again, preemption, watermark admission and prefix-cache
+    hits, with the batch reordered, shrunk and grown between steps and
+    max_blocks changed once: tables and lengths equal bit for bit."""
+    rnd = random.Random(seed)
+    t = 16
+    p = pkv.Pool(400, t)
+    caching = seed % 2 == 1
+    if caching:
+        p.enable_prefix_cache()
+    prompt = [rnd.randrange(50) for _ in range(8 * t)]
+    live, next_id = [], 0
+    rows = p.block_tables_rows(24, 40)
+    for step in range(300):
+        op = rnd.random()
+        try:
+            if op < 0.15 or not live:
+                if caching and rnd.random() < 0.5:
+                    n = rnd.randrange(1, len(prompt))
+                    p.seq_create_cached(next_id, prompt[:n])
+                    have = p.seq_table(next_id)[1]
+                    p.seq_append_tokens(next_id, prompt[have:n])
+                elif rnd.random() < 0.5:
+                    p.seq_admit(next_id, rnd.randrange(0, 60), watermark_blocks=4)
+                else:
+                    p.seq_create(next_id)
+                    p.seq_append(next_id, rnd.randrange(0, 60))
+                live.append(next_id)
+                next_id += 1
+            elif op < 0.25:
+                par = rnd.choice(live)
+                p.seq_fork(par, next_id)
+                live.append(next_id)
+                next_id += 1
+            elif op < 0.35:
+                s = rnd.choice(live)
+                p.seq_free(s)
+                live.remove(s)
+                if rnd.random() < 0.5:       # the same id again: a new sequence
+                    p.seq_create(s)
+                    p.seq_append(s, rnd.randrange(0, 40))
+                    live.append(s)
+            elif op < 0.45:
+                _, _, gone = p.batch_append_preempt(list(live))
+                live = [s for s in live if s not in gone]
+            elif op < 0.7:
+                p.seq_append(rnd.choice(live), rnd.randrange(1, 20))
+            else:
+                p.batch_append(rnd.sample(live, rnd.randrange(1, len(live) + 1)))
+        except pkv.PkvError as e:
+            assert e.code in ("OUT_OF_BLOCKS", "INVALID_ARG"), e
+        while live and max(len(p.seq_table(s)[0]) for s in live) > rows.max_blocks:
+            s = max(live, key=lambda x: len(p.seq_table(x)[0]))
+            p.seq_free(s)
+            live.remove(s)
+        if step == 150:
+            rows = p.block_tables_rows(24, 48)
+        batch = rnd.sample(live, min(len(live), rnd.randrange(1, 25)))
+        got_t, got_c = rows.update(batch)
+        want_t, want_c = p.block_tables(batch, rows.max_blocks)
+        assert np.array_equal(got_t.numpy(), want_t) and np.array_equal(got_c.numpy(), want_c), step
+
+
+def test_incremental_block_tables_rewrite_only_what_can_change():
+    """A row held for the same sequence is rewritten from its last entry on
+    (a sentinel planted before it survives); a row that now holds another
+    sequence, or whose state was reset, is rewritten whole; an error writes
+    nothing."""
+    p = pkv.Pool(64, 16)
+    for s, n in ((1, 40), (2, 70)):
+        p.seq_create(s)
+        p.seq_append(s, n)
+    rows = p.block_tables_rows(4, 8)
+    rows.update([1, 2])
+    rows.tables[0, 0] = 999                    # before row 0's last entry (index 2)
+    p.seq_append(1, 30)                        # 70 tokens: entries 3 and 4 added
+    t, c = rows.update([1, 2])
+    assert t[0, 0] == 999 and t[0, 2:5].tolist() == p.seq_table(1)[0][2:5].tolist()
+    assert c.tolist() == [70, 70]
+    t, _ = rows.update([2, 1])                 # rows swapped: both rewritten whole
+    want, _ = p.block_tables([2, 1], 8)
+    assert np.array_equal(t.numpy(), want)
+    rows.tables[1, 0] = 999
+    rows.reset()
+    t, _ = rows.update([2, 1])
+    assert np.array_equal(t.numpy(), want)
+    before = rows.tables.clone()
+    with pytest.raises(pkv.PkvError):
+        rows.update([2, 77])
+    assert torch.equal(rows.tables, before)
+    with pytest.raises(ValueError):
+        rows.update([1, 2, 1, 2, 1])
