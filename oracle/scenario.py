@@ -26,7 +26,7 @@ import numpy as np
 import workloads as W
 
 from .allocator import BlockAllocator
-from .pool import PoolModel, STORAGE
+from .pool import PoolModel
 
 CHURN_SEQ_BASE = 1 << 40
 
@@ -137,7 +137,3 @@ def build(w: W.Workload, write_seqs=None, scales: dict | None = None) -> Scenari
     q_bits = np.stack([torch_bits(W.q_for_seq(w, s)) for s in seq_ids])
     return Scenario(w=w, alloc=alloc, pool=pool, seq_ids=seq_ids, ctx=np.asarray(ctx),
                     q_bits=q_bits, step_slots=step_slots, cow_pairs=cow_pairs, scales=scales)
-
-
-def storage_dtype(kv_dtype: str):
-    return STORAGE[kv_dtype]
