@@ -341,3 +341,52 @@ def test_incremental_block_tables_rewrite_only_what_can_change():
     assert torch.equal(rows.tables, before)
     with pytest.raises(ValueError):
         rows.update([1, 2, 1, 2, 1])
+
+
+C_CLIENT = r"""
+#include "pkv.h"
+#include <stdio.h>
+int main(void) {
+  pkv_pool* p = NULL;
+  int64_t slots[40];
+  int32_t cow[2], n_cow = 0, table[8], n_blocks = 0;
+  int64_t ctx = 0;
+  if (pkv_pool_create(8, 16, NULL, &p) != PKV_OK) return 1;
+  if (pkv_seq_create(p, 1) != PKV_OK || pkv_seq_append(p, 1, 40, slots, cow, 1, &n_cow) != PKV_OK)
+    return 2;
+  if (pkv_seq_table(p, 1, table, 8, &n_blocks, &ctx) != PKV_OK) return 3;
+  if (pkv_seq_append(p, 2, 1, slots, cow, 1, &n_cow) != PKV_ERR_UNKNOWN_SEQ) return 4;
+  printf("%llu %d %lld %lld %d %d\n", (unsigned long long)pkv_block_bytes(28, 4, 128, 16, 2),
+         n_blocks, (long long)ctx, (long long)slots[39], pkv_num_free_blocks(p),
+         pkv_last_error()[0] != 0);
+  pkv_pool_destroy(p);
+  return 0;
+}
+"""
+
+
+def test_header_is_plain_c_and_links(tmp_path):
+    """The boundary is a C ABI: include/pkv.h compiles as strict C99 with no
+    warning, and a C program links libpkv.so and drives the host allocator
+    (no device call): the pages' 917,504-byte block, 3 blocks for 40 tokens,
+    error codes and messages."""
+    import shutil
+    import subprocess
+    gcc = shutil.which("gcc") or shutil.which("cc")
+    if gcc is None:
+        pytest.skip("no C compiler")
+    pkv.lib()
+    src = tmp_path / "client.c"
+    src.write_text(C_CLIENT)
+    exe = tmp_path / "client"
+    libdir = os.path.dirname(pkv.LIB)
+    inc = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include")
+    r = subprocess.run([gcc, "-std=c99", "-Wall", "-Wextra", "-pedantic", "-Werror", "-I", inc, str(src),
+                        "-L", libdir, "-lpkv", "-Wl,-rpath," + libdir, "-o", str(exe)],
+                       capture_output=True, text=True)
+    assert r.returncode == 0, r.stderr
+    r = subprocess.run([str(exe)], capture_output=True, text=True, timeout=60)
+    assert r.returncode == 0, (r.returncode, r.stderr)
+    # pool of 8 blocks, default order block 0 on top: 40 tokens -> blocks 0..2,
+    # token 39 in block 2 at offset 7
+    assert r.stdout.split() == ["917504", "3", "40", str(2 * 16 + 7), "5", "1"]
