@@ -21,7 +21,9 @@ import argparse
 import hashlib
 import json
 import os
+import shutil
 import statistics
+import subprocess
 import sys
 import threading
 import time
@@ -175,10 +177,13 @@ class ClockSampler:
     REASONS = {0x4: "sw_power_cap", 0x8: "hw_slowdown", 0x20: "sw_thermal_slowdown",
                0x40: "hw_thermal_slowdown", 0x80: "hw_power_brake_slowdown"}
 
+    SMI_QUERY = "clocks.sm,clocks.max.sm,clocks_event_reasons.active"
+
     def __init__(self, index: int):
         import ctypes
+        self.index = index
         self.samples, self.max_mhz, self.stop = [], None, threading.Event()
-        self.nvml = None
+        self.nvml, self.smi = None, None
         try:
             nv = ctypes.CDLL("libnvidia-ml.so.1")
             h = ctypes.c_void_p()
@@ -202,23 +207,55 @@ class ClockSampler:
                 self.samples.append((float(clk.value), int(rs.value)))
             time.sleep(0.0005)
 
+    @staticmethod
+    def parse_smi(text: str):
+        """Samples from `nvidia-smi --query-gpu=<SMI_QUERY> --format=csv,noheader,nounits`
+        lines: [(sm MHz, reasons bitmask)] and the max SM clock (None if absent)."""
+        samples, mx = [], None
+        for line in text.splitlines():
+            f = [x.strip() for x in line.split(",")]
+            if len(f) != 3:
+                continue
+            try:
+                clk, top, rs = float(f[0]), float(f[1]), int(f[2], 16)
+            except ValueError:
+                continue
+            samples.append((clk, rs))
+            mx = top
+        return samples, mx
+
     def __enter__(self):
         if self.nvml is not None:
             self.thread = threading.Thread(target=self._poll, daemon=True)
             self.thread.start()
+        elif shutil.which("nvidia-smi"):
+            # read-only query of this GPU every 200 ms, stopped in __exit__
+            self.smi = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.index), f"--query-gpu={self.SMI_QUERY}",
+                 "--format=csv,noheader,nounits", "-lms", "200"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
         return self
 
     def __exit__(self, *exc):
         self.stop.set()
         if self.nvml is not None:
             self.thread.join(timeout=2)
+        elif self.smi is not None:
+            self.smi.terminate()
+            try:
+                out, _ = self.smi.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.smi.kill()
+                out, _ = self.smi.communicate()
+            self.samples, self.max_mhz = self.parse_smi(out or "")
 
     def summary(self):
         if not self.samples:
             return {"sm_mhz": None, "sm_max_mhz": self.max_mhz, "reasons": ["unsampled"], "samples": 0}
         reasons = sorted({name for _, r in self.samples for bit, name in self.REASONS.items() if r & bit})
         return {"sm_mhz": statistics.median(c for c, _ in self.samples), "sm_max_mhz": self.max_mhz,
-                "reasons": reasons, "samples": len(self.samples), "source": "nvml"}
+                "reasons": reasons, "samples": len(self.samples),
+                "source": "nvml" if self.nvml is not None else "nvidia-smi"}
 
 
 def dist_setup(args):
