@@ -841,7 +841,12 @@ def run_prefill_gpu(args, world, rank, local):
     d = json.load(open(os.path.join(ROOT, "MEASURED_PEAKS.json"))) \
         if os.path.exists(os.path.join(ROOT, "MEASURED_PEAKS.json")) else {}
     peak, peak_kind = (float(d["bf16_tflops"]), "measured") if "bf16_tflops" in d else (1900.0, "fallback")
+    peak_sustained = float(d.get("bf16_tflops_sustained", 1700.0))
     achieved = flops / (attn / 1e3) / 1e12
+    # the step's inputs: queries and the K/V of the chunks' contexts
+    in_bytes = (total_q * w.num_q_heads * w.head_dim * 2
+                + 2 * int(ctx.sum()) * w.num_kv_heads * w.head_dim * w.kv_bytes)
+    l2_bytes = torch.cuda.get_device_properties(local).L2_cache_size
     pf_kernel = ("prefill_umma_kernel (tcgen05.mma, TMEM accumulators)"
                  if w.head_dim == 128
                  else "prefill_tc_kernel (mma.sync m16n8k16)")
@@ -855,13 +860,17 @@ def run_prefill_gpu(args, world, rank, local):
                    "chunk": w.prefill_chunk, "query_tokens": total_q, "kv_dtype": w.kv_dtype,
                    **({"fp8_scales": args.fp8_scales} if w.kv_dtype == "e4m3" else {}),
                    "context_tokens": int(ctx.sum()), "flops_per_step": flops,
-                   "l2": "no flush between steps (K/V of the chunks' contexts re-read each step)",
+                   "l2": ("inputs %s than L2 (q + K/V %d MB vs %d MB L2), no flush between steps"
+                          % ("larger" if in_bytes > l2_bytes else "smaller", in_bytes >> 20,
+                             l2_bytes >> 20)),
                    "launch": "the K steps captured back to back in one CUDA graph, replayed once",
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": round(world * total_q / (ms / 1e3), 1),
         "roofline": {"bound": "tensor", "kernel": pf_kernel,
                      "achieved": round(achieved, 2), "peak": peak, "unit": "TFLOP/s",
                      "frac": round(achieved / peak, 4), "peak_source": f"{peak_kind} bf16 burst",
+                     "peak_sustained": peak_sustained,
+                     "frac_of_sustained": round(achieved / peak_sustained, 4),
                      "traffic": traffic_for(args.config, pf_kernel) if w == W.get(args.config) else None,
                      "attention_ms": round(attn, 4)},
         "e2e": {"value": round(world * flops / e2e_s / 1e12, 2), "unit": "TFLOP/s",
