@@ -136,8 +136,9 @@ PKV_API pkv_status pkv_seq_append(pkv_pool* pool, int64_t seq_id, int32_t n_new,
 
 /* One decode step: append one token to each of n_seqs sequences, in order.
  * slots_out: host int64[n_seqs]; cow_out / cow_cap / n_cow_out as above (at
- * most n_seqs pairs).  All-or-nothing over the whole batch: if any sequence
- * cannot be served, no sequence changes. */
+ * most n_seqs pairs).  A sequence named k times gets k tokens, in batch
+ * order.  All-or-nothing over the whole batch: if any sequence cannot be
+ * served, no sequence changes. */
 PKV_API pkv_status pkv_batch_append(pkv_pool* pool, const int64_t* seq_ids, int32_t n_seqs,
                             int64_t* slots_out, int32_t* cow_out, int32_t cow_cap,
                             int32_t* n_cow_out);
