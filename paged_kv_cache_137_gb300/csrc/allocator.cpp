@@ -69,6 +69,9 @@ struct Seq {
   // unique over the pool's life: a new sequence (also a fork child, or an id
   // used again) gets a new one, so a caller's copy of a table can tell
   int64_t incarnation = 0;
+  // batch-append check only: tokens of the batch already counted for this
+  // sequence (0 outside the check)
+  int32_t pending = 0;
 };
 
 // One published block and its content key bytes (parent entry, token ids).
@@ -96,6 +99,9 @@ struct pkv_pool {
   int32_t block_size;
   std::vector<int32_t> free_stack;  // top = back()
   std::vector<int32_t> refcount;
+  // batch-append check only: counts the batch's earlier copies take from a
+  // block (0 outside the check)
+  std::vector<int32_t> rc_taken;
   std::unordered_map<int64_t, pkv::Seq> seqs;
   // prefix cache (off unless enabled)
   bool caching = false;
@@ -422,28 +428,53 @@ pkv_status pkv_batch_append(pkv_pool* pool, const int64_t* seq_ids, int32_t n_se
   static thread_local std::vector<pkv::AppendUndo> undo;
   batch.clear();
   undo.clear();
+  // The check follows the sequential appends exactly: a sequence named k
+  // times takes tokens len .. len + k - 1, each counted at its own position,
+  // and only its first can need a copy (the block it then writes is its
+  // own); a copy takes one count from its source block, so a later sharer
+  // of that block may find it private and write in place.
+  static thread_local std::vector<int32_t> taken;  // blocks with a count taken
+  taken.clear();
+  if (pool->rc_taken.size() != pool->refcount.size()) pool->rc_taken.assign(pool->refcount.size(), 0);
   {
+    pkv_status st = PKV_OK;
     int64_t need = 0, cows = 0;
-    for (int32_t i = 0; i < n_seqs; ++i) {
+    const int32_t t = pool->block_size;
+    for (int32_t i = 0; i < n_seqs && st == PKV_OK; ++i) {
       auto it = pool->seqs.find(seq_ids[i]);
       if (it == pool->seqs.end()) {
         pkv::set_error("unknown sequence %lld", (long long)seq_ids[i]);
-        return PKV_ERR_UNKNOWN_SEQ;
+        st = PKV_ERR_UNKNOWN_SEQ;
+        break;
       }
-      batch.push_back(&it->second);
+      pkv::Seq& s = it->second;
+      batch.push_back(&s);
+      const int64_t k = s.pending++;
+      const int64_t pos = s.len + k;
       bool cow = false;
-      need += pkv::blocks_needed(pool, it->second, 1, &cow);
+      if (pos % t == 0) {
+        need += 1;  // opens a block
+      } else if (k == 0) {
+        const int32_t b = s.table[pos / t];
+        cow = pool->refcount[b] - pool->rc_taken[b] > 1;
+        if (cow) {
+          need += 1;
+          if (pool->rc_taken[b]++ == 0) taken.push_back(b);
+        }
+      }
       if (need > pkv::available(pool)) {
         pkv::set_error("sequence %lld: the batch needs %lld blocks, %lld free",
                        (long long)seq_ids[i], (long long)need, (long long)pkv::available(pool));
-        return PKV_ERR_OUT_OF_BLOCKS;
-      }
-      if (cow && (cow_out == nullptr || ++cows > cow_cap)) {
+        st = PKV_ERR_OUT_OF_BLOCKS;
+      } else if (cow && (cow_out == nullptr || ++cows > cow_cap)) {
         pkv::set_error("sequence %lld needs a copy-on-write pair but cow_cap is exhausted",
                        (long long)seq_ids[i]);
-        return PKV_ERR_INVALID_ARG;
+        st = PKV_ERR_INVALID_ARG;
       }
     }
+    for (pkv::Seq* s : batch) s->pending = 0;
+    for (int32_t b : taken) pool->rc_taken[b] = 0;
+    if (st != PKV_OK) return st;
   }
   int32_t n_cow = 0;
   for (int32_t i = 0; i < n_seqs; ++i) {

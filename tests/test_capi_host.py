@@ -96,7 +96,9 @@ def test_native_allocator_matches_oracle_on_random_ops(seed):
                 slots, cow = native.seq_append(s, n)
                 assert slots.tolist() == exp[0] and [tuple(x) for x in cow.tolist()] == exp[1]
         elif op < 0.7:
-            batch = rnd.sample(live, min(len(live), rnd.randint(1, 6)))
+            k = rnd.randint(1, 6)
+            # half the batches may name a sequence more than once
+            batch = rnd.choices(live, k=k) if rnd.random() < 0.5 else rnd.sample(live, min(len(live), k))
             try:
                 exp = ref.append_batch(batch, 1)
             except AllocError as e:
@@ -119,6 +121,82 @@ def test_native_allocator_matches_oracle_on_random_ops(seed):
         if step % 25 == 0:
             _compare(native, ref, live)
     _compare(native, ref, live)
+
+
+def test_batch_naming_a_sequence_twice_is_two_sequential_tokens():
+    """The second token of a sequence named twice writes into the block its
+    first token copied, so the batch needs one copy, not two: with one free
+    block it is served exactly as the oracle's sequential appends serve it."""
+    native, ref = pkv.Pool(4, 16), BlockAllocator(4, 16)
+    for a in (native, ref):
+        (a.seq_create if a is native else a.create)(1)
+        (a.seq_append if a is native else a.append)(1, 20)
+        (a.seq_fork if a is native else a.fork)(1, 2)
+        (a.seq_create if a is native else a.create)(3)
+        (a.seq_append if a is native else a.append)(3, 1)
+    assert native.num_free_blocks() == ref.num_free() == 1
+    want = ref.append_batch([2, 2], 1)
+    slots, cow = native.batch_append([2, 2])
+    assert slots.tolist() == want[0] == [52, 53] and [tuple(x) for x in cow.tolist()] == want[1]
+    _compare(native, ref, [1, 2, 3])
+    # a third token of sequence 2 would open a block: none is left, nothing changes
+    native.seq_append(2, 10)
+    ref.append(2, 10)
+    with pytest.raises(pkv.PkvError) as e:
+        native.batch_append([2, 2])
+    with pytest.raises(AllocError) as f:
+        ref.append_batch([2, 2], 1)
+    assert e.value.code == f.value.code == "OUT_OF_BLOCKS"
+    _compare(native, ref, [1, 2, 3])
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_batches_with_repeats_on_a_nearly_full_pool_match_oracle(seed):
+    """Small pools, frequent mid-block forks and batches that repeat
+    sequences: every batch append (served or refused) as the oracle's
+    sequential appends, state compared after each."""
+    rnd = random.Random(500 + seed)
+    t, nb = 16, rnd.choice([6, 8, 12])
+    native, ref = pkv.Pool(nb, t), BlockAllocator(nb, t)
+    live, nxt = [], 0
+    for step in range(300):
+        op = rnd.random()
+        if op < 0.2 or not live:
+            ref.create(nxt)
+            native.seq_create(nxt)
+            live.append(nxt)
+            n = rnd.randint(1, 2 * t)
+            try:
+                ref.append(nxt, n)
+            except AllocError:
+                with pytest.raises(pkv.PkvError):
+                    native.seq_append(nxt, n)
+            else:
+                native.seq_append(nxt, n)
+            nxt += 1
+        elif op < 0.45:
+            parent = rnd.choice(live)
+            ref.fork(parent, nxt)
+            native.seq_fork(parent, nxt)
+            live.append(nxt)
+            nxt += 1
+        elif op < 0.55 and len(live) > 1:
+            s = live.pop(rnd.randrange(len(live)))
+            ref.free_seq(s)
+            native.seq_free(s)
+        else:
+            batch = rnd.choices(live, k=rnd.randint(1, 5))
+            try:
+                exp = ref.append_batch(batch, 1)
+            except AllocError as e:
+                with pytest.raises(pkv.PkvError) as got:
+                    native.batch_append(batch)
+                assert got.value.code == e.code, (step, batch)
+            else:
+                slots, cow = native.batch_append(batch)
+                assert slots.tolist() == exp[0], (step, batch)
+                assert [tuple(x) for x in cow.tolist()] == exp[1], (step, batch)
+        _compare(native, ref, live)
 
 
 def test_errors_leave_state_unchanged():
