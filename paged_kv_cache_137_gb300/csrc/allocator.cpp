@@ -476,6 +476,8 @@ pkv_status pkv_batch_append(pkv_pool* pool, const int64_t* seq_ids, int32_t n_se
     for (int32_t b : taken) pool->rc_taken[b] = 0;
     if (st != PKV_OK) return st;
   }
+  // The check above is exact, so no append below fails; the undo records
+  // are a safety net that would restore the state if one did.
   int32_t n_cow = 0;
   for (int32_t i = 0; i < n_seqs; ++i) {
     undo.emplace_back();

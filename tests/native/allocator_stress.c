@@ -3,7 +3,8 @@
  *
  * Every call of include/pkv.h that touches only host state is driven from one
  * seeded generator: create (+ append), fork, free, single and batch appends
- * (short pools make some fail and roll back), preemption, admission with a
+ * (short pools make some fail, which must change nothing; batches may repeat
+ * a sequence), preemption, admission with a
  * watermark, prefix-cache hits, full and incremental batch tables.  After
  * every step the invariants the pages fix are checked:
  *   - a block's reference count is the number of tables holding it, so the
@@ -153,8 +154,8 @@ int main(int argc, char** argv) {
     } else if (op <= 7) {
       int64_t batch[MAX_SEQS];
       const int n = 1 + below(n_live);
-      /* half the batches name some sequences twice: the second token's
-         append can then fail after the first one's, which must be undone */
+      /* half the batches name some sequences twice: such a sequence takes
+         one token per mention, in batch order */
       const int repeat = below(2);
       for (int i = 0; i < n; ++i) batch[i] = repeat ? live[below(n_live)] : live[i];
       const pkv_status st = pkv_batch_append(p, batch, n, slots, cow, n, &n_cow);

@@ -1,8 +1,8 @@
 """The host allocator under AddressSanitizer and UndefinedBehaviorSanitizer
 (no GPU): tests/native/allocator_stress.c drives every host call of the C ABI
-from a seeded random stream (failing appends that roll back, forks, frees,
-reused ids, preemption, admission, prefix-cache hits, full and incremental
-batch tables) and checks the allocator's invariants after every step; any
+from a seeded random stream (refused appends, batches that repeat a
+sequence, forks, frees, reused ids, preemption, admission, prefix-cache hits,
+full and incremental batch tables) and checks the allocator's invariants after every step; any
 out-of-bounds access, use after free, leak or undefined behaviour aborts."""
 import os
 import shutil
