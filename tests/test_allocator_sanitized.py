@@ -2,8 +2,9 @@
 (no GPU): tests/native/allocator_stress.c drives every host call of the C ABI
 from a seeded random stream (refused appends, batches that repeat a
 sequence, forks, frees, reused ids, preemption, admission, prefix-cache hits,
-full and incremental batch tables) and checks the allocator's invariants after every step; any
-out-of-bounds access, use after free, leak or undefined behaviour aborts."""
+full and incremental batch tables) and checks the allocator's invariants
+after every step; any out-of-bounds access, use after free, leak or
+undefined behaviour aborts."""
 import os
 import shutil
 import subprocess
