@@ -468,3 +468,41 @@ def test_header_is_plain_c_and_links(tmp_path):
     # pool of 8 blocks, default order block 0 on top: 40 tokens -> blocks 0..2,
     # token 39 in block 2 at offset 7
     assert r.stdout.split() == ["917504", "3", "40", str(2 * 16 + 7), "5", "1"]
+
+
+def _align256(x):
+    return (x + 255) // 256 * 256
+
+
+@pytest.mark.parametrize("b,hq,n_kv,d,t,max_blocks,p", [
+    (64, 28, 4, 128, 16, 243, 512), (64, 28, 4, 128, 16, 243, 1536), (3, 5, 1, 64, 32, 70, 64),
+    (512, 64, 8, 128, 16, 509, 4096), (8, 32, 32, 128, 32, 1024, 512), (7, 12, 4, 64, 16, 9, 64)])
+def test_workspace_bytes_follow_the_documented_layout(b, hq, n_kv, d, t, max_blocks, p):
+    """Split-K workspace for an explicit partition P: int32 arrival counters
+    [B][N_kv], then fp32 maxima and sums [B][Hq][S] and unnormalised outputs
+    [B][Hq][S][D], each part 256-byte aligned, S = ceil(max_blocks * T / P);
+    nothing when one split covers every sequence."""
+    desc = pkv.kv_desc(1000, n_kv, d, t, "bf16")
+    s = -(-max_blocks * t // p)
+    n = b * hq * s
+    want = 0 if s <= 1 else (_align256(4 * b * n_kv) + 2 * _align256(4 * n) + _align256(4 * n * d))
+    assert pkv.pkv_attention_workspace_bytes(b, hq, max_blocks, desc, p) == want
+
+
+def test_workspace_bytes_reject_bad_sizes():
+    desc = pkv.kv_desc(1000, 4, 128, 16, "bf16")
+    for args in ((64, 28, 243, 100), (64, 28, 243, 48), (64, 28, 243, -512), (0, 28, 243, 512),
+                 (64, 0, 243, 512), (64, 28, 0, 512)):
+        assert pkv.pkv_attention_workspace_bytes(*args[:3], desc, args[3]) == 0, args
+    desc32 = pkv.kv_desc(1000, 4, 128, 32, "bf16")
+    assert pkv.pkv_attention_workspace_bytes(4, 28, 100, desc32, 64) > 0   # 64 is a multiple of 32
+
+
+@pytest.mark.skipif(__import__("torch").cuda.is_available(),
+                    reason="on a GPU the automatic partition may add the stream-K schedule's slots")
+def test_automatic_workspace_is_the_resolved_partitions():
+    desc = pkv.kv_desc(8500, 4, 128, 16, "bf16")
+    p = pkv.pkv_attention_partition(64, 243, desc)
+    assert p == 1536
+    assert pkv.pkv_attention_workspace_bytes(64, 28, 243, desc, 0) == \
+        pkv.pkv_attention_workspace_bytes(64, 28, 243, desc, p)
