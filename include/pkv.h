@@ -200,9 +200,11 @@ PKV_API int32_t pkv_num_free_blocks(const pkv_pool* pool);
 /* The free stack, top first, into out[cap]; *n receives its size. */
 PKV_API pkv_status pkv_free_stack(const pkv_pool* pool, int32_t* out, int32_t cap, int32_t* n);
 
-/* Live sequences, tokens they hold, and token slots their blocks provide
- * (shared blocks counted once); slots - tokens is the reserved-but-empty
- * space the pages call waste ([C "Evals"]). */
+/* Live sequences, the tokens they hold (a shared token once per sequence
+ * holding it) and the blocks in use: referenced by a sequence (a shared
+ * block counted once), or, with prefix caching, neither free nor reusable.
+ * Without sharing, used_blocks * block_size - live_tokens is the
+ * reserved-but-empty space the pages call waste ([C "Evals"]). */
 PKV_API pkv_status pkv_pool_usage(const pkv_pool* pool, int64_t* live_seqs, int64_t* live_tokens,
                           int64_t* used_blocks);
 

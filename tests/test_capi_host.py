@@ -67,6 +67,9 @@ def _compare(native: pkv.Pool, ref: BlockAllocator, live):
         assert tab.tolist() == ref.table(s) and ln == ref.context_len(s)
     for b in range(ref.num_blocks):
         assert native.block_refcount(b) == ref.block_refcount(b)
+    # usage: live sequences, their tokens, blocks referenced (shared once)
+    used = sum(1 for b in range(ref.num_blocks) if ref.block_refcount(b) > 0)
+    assert native.usage() == (len(live), sum(ref.context_len(s) for s in live), used)
 
 
 @pytest.mark.parametrize("seed", range(8))
