@@ -11,10 +11,11 @@
  *       "Calculating Physical Block Sizes" and "Complex Topologies and Memory
  *       Sharing".
  *   [B] "What problem does PagedAttention solve for the KV cache in vLLM?"
- *       (katajob Q&A), sections "The paging idea" and "Sharing, the second
- *       dividend".
+ *       (katajob Q&A), sections "What the KV cache is", "The paging idea" and
+ *       "Sharing, the second dividend".
  *   [C] foundry page on paged block allocation for the KV cache, sections
- *       "In and out", "Concept", "The knobs".
+ *       "In and out", "Concept", "The knobs", "Effect", "Evals" and
+ *       "Failure modes".
  *   [D] "PagedAttention, clearly explained" (thread).
  *
  * Conventions
@@ -22,8 +23,10 @@
  *     message for the calling thread's last failure.
  *   - Host allocator calls are all-or-nothing: on error nothing changes.
  *   - Device buffers are owned by the caller (plain device pointers).  The
- *     library never allocates or frees device memory.  A pool handle owns only
- *     host-side allocator state.
+ *     library never allocates or frees device memory at run time; its only
+ *     device memory is the fixed static scratch of
+ *     pkv_attention_decode_noalloc, resident on each GPU that loads it.  A pool
+ *     handle owns only host-side allocator state.
  *   - Device calls enqueue kernels on the given CUDA stream (a cudaStream_t
  *     passed as void*, NULL = legacy default stream) and return without
  *     synchronising; a launch failure returns PKV_ERR_CUDA.
@@ -312,8 +315,8 @@ PKV_API pkv_status pkv_attention_decode(void* out, const void* q, int32_t q_dtyp
                                 size_t workspace_bytes, void* stream);
 
 /* One decode step: the step's new K/V of each sequence written at its logical
- * position ctx_s - 1 (the slot its block table gives: [F "In and out"], the
- * new tokens written into reserved slots; R3: the context length counts the
+ * position ctx_s - 1 (the slot its block table gives: [C "In and out"], the
+ * new tokens written into reserved slots; the context length counts the
  * step's token), then pkv_attention_decode over positions 0 .. ctx_s - 1.
  * The same as pkv_write (slots of positions ctx_s - 1) followed by
  * pkv_attention_decode, in one launch where the tensor-core split kernel
@@ -366,10 +369,10 @@ PKV_API pkv_status pkv_attention_decode_noalloc(void* out, const void* q, int32_
  * of sequence s is its last n_s = query_start[s+1] - query_start[s] logical
  * positions ctx_s - n_s .. ctx_s - 1, whose K/V are already in the pool
  * (written by pkv_write, like a decode step's token); the query at position
- * p attends to positions 0 .. p ("What the KV cache is": every earlier
- * token's key and value serve the next token's attention; "The paging idea":
- * a sequence starts with the blocks of its prompt; [T]: later tokens attend
- * over the cached prompt):
+ * p attends to positions 0 .. p ([B "What the KV cache is"]: every earlier
+ * token's key and value serve the next token's attention; [B "The paging
+ * idea"]: a sequence starts with the blocks of its prompt; [D]: later tokens
+ * attend over the cached prompt):
  *   out[r][j][:] = softmax_{p' <= p}( q[r][j] . K_s[p'] * softmax_scale ) V_s[p']
  * for row r = query_start[s] + i at position p = ctx_s - n_s + i, K_s, V_s
  * gathered through block_tables as in pkv_attention_decode (query head j
@@ -412,10 +415,10 @@ PKV_API pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_dty
 PKV_API pkv_status pkv_set_prefill_kernel(int32_t kind);
 
 /* ---------------------------------------------------------- prefix caching
- * [F "The knobs"]: enable_prefix_caching hashes each filled block so that
- * unrelated requests share physical blocks; [F "Failure modes"]: sharing is
+ * [C "The knobs"]: enable_prefix_caching hashes each filled block so that
+ * unrelated requests share physical blocks; [C "Failure modes"]: sharing is
  * block-granular (block size 32: a shared 1,000-token prefix reuses at most
- * 992 tokens; a divergence inside a block loses the whole block); [Q "Sharing,
+ * 992 tokens; a divergence inside a block loses the whole block); [B "Sharing,
  * the second dividend"]: when the tokens match, the blocks holding their KV
  * state are reused and that part of prefill is skipped.
  *
@@ -457,10 +460,10 @@ PKV_API pkv_status pkv_prefix_cache_stats(const pkv_pool* pool, int64_t* publish
 PKV_API pkv_status pkv_reusable_blocks(const pkv_pool* pool, int32_t* out, int32_t cap, int32_t* n);
 
 /* -------------------------------------------------------------- preemption
- * [F "The knobs"]: when the pool cannot satisfy a running sequence the engine
+ * [C "The knobs"]: when the pool cannot satisfy a running sequence the engine
  * preempts it, drops its blocks and re-prefills it later (recompute);
- * [F "Effect"]: the scheduler preempts running sequences rather than failing
- * them, and a request can be preempted and restarted several times; [F
+ * [C "Effect"]: the scheduler preempts running sequences rather than failing
+ * them, and a request can be preempted and restarted several times; [C
  * "Failure modes"]: the free-block watermark. */
 
 /* One decode step with preemption: append one token to each sequence in
