@@ -36,7 +36,7 @@ METRIC = "paged decode attention KV GB/s & fraction of GB300 HBM peak; decode to
 # the sources each kernel family's recorded DRAM counters depend on
 KERNEL_SOURCES = {
     "decode": ["attention.cu", "attention.h", "attention_simt.cuh", "attention_tc.cuh",
-               "attention_tc_launch.cuh", "attention_stream.cuh", "device_common.cuh"],
+               "attention_tc_launch.cuh", "device_common.cuh"],
     "prefill": ["attention_prefill.cu", "attention_prefill_umma.cuh", "attention_tc.cuh", "attention.h",
                 "device_common.cuh"],
 }
@@ -54,7 +54,7 @@ def parse():
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--partition", type=int, default=None,
                     help="split-K partition in tokens (default: the workload's, else automatic)")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc", "persistent"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"],
                     help="decode kernel (auto = tensor-core where it applies)")
     ap.add_argument("--block-size", type=int, default=None,
                     help="ablation: tokens per block (the pool keeps the same token capacity)")
@@ -179,8 +179,6 @@ def attention_kernels(kernel: str, w, splits: int) -> str:
     if w.kv_dtype == "f32" or kernel == "simt":
         k = "decode_simt_kernel"
         return k + (" + merge_kernel" if splits > 1 else "")
-    if kernel == "persistent":
-        return "decode_stream_kernel"
     return "decode_tc_kernel (split-K merge fused)"
 
 
@@ -505,7 +503,7 @@ def run_gpu(args, world, rank, local):
     # the split-K merge is its own launch only in the CUDA-core path, and so
     # is the slot write outside the tensor-core split kernel (which fuses it)
     separate_merge = args.kernel == "simt" or w.kv_dtype == "f32"
-    fused_write = not separate_merge and args.kernel != "persistent"
+    fused_write = not separate_merge
     attn_launches = 1 + (1 if separate_merge and splits > 1 else 0)
     launches_per_step = (0 if fused_write else 1) + attn_launches + \
         (-(-n_pairs // 1024) if n_pairs else 0)

@@ -253,17 +253,11 @@ PKV_API size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_hea
  * with head_dim 128 (16-bit also 64), groups of up to 16 query heads and
  * partitions of at most 1024 blocks, and the CUDA-core kernel otherwise.  SIMT
  * forces the CUDA-core kernel; TENSOR_CORE makes pkv_attention_decode return
- * PKV_ERR_UNSUPPORTED for sizes it does not cover; PERSISTENT selects, for
- * partition_tokens 0, the stream-K schedule of the tensor-core kernel (one wave
- * of three CTAs per SM, each taking an equal slice of all (sequence, KV head,
- * 64-token tile) work, shared pairs merged by the last CTA to finish), falling
- * back like TENSOR_CORE when the workspace is smaller than
- * pkv_attention_workspace_bytes(..., 0).  All kernels compute the same result
- * within rounding. */
+ * PKV_ERR_UNSUPPORTED for sizes it does not cover.  Both kernels compute the
+ * same result within rounding. */
 #define PKV_KERNEL_AUTO 0
 #define PKV_KERNEL_SIMT 1
 #define PKV_KERNEL_TENSOR_CORE 2
-#define PKV_KERNEL_PERSISTENT 3
 PKV_API pkv_status pkv_set_attention_kernel(int32_t kind);
 
 /* Partition (tokens per split) pkv_attention_decode uses for these sizes.
@@ -293,8 +287,7 @@ PKV_API int32_t pkv_attention_partition(int32_t num_seqs, int32_t max_blocks, co
  *                   choice; a multiple of 64 and of block_size.  Split and
  *                   tile boundaries depend only on logical positions and
  *                   lengths, so results do not depend on which physical
- *                   blocks hold the tokens (see PKV_KERNEL_PERSISTENT for the
- *                   stream-K schedule).
+ *                   blocks hold the tokens.
  *   workspace     : device buffer of at least
  *                   pkv_attention_workspace_bytes(...) bytes, 256-byte
  *                   aligned, ZERO-FILLED before its first use (every call

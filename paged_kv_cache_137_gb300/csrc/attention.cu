@@ -25,9 +25,6 @@ namespace pkv {
 template <typename KV, typename Q>
 pkv_status launch_decode_tc(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
                             const CUtensorMap& vmap, cudaStream_t stream);
-template <typename KV, typename Q>
-pkv_status launch_decode_stream(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, cudaStream_t stream);
 
 namespace {
 
@@ -100,54 +97,10 @@ WsLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t num_kv_
   return w;
 }
 
-constexpr int kStreamCtasPerSm = 3;  // the stream-K kernel's launch bound
-
-// CTAs of the stream-K kernel on the current device: three per SM (0 if the
-// device cannot be queried).  Cached per device.
-int stream_ctas() {
-  static std::atomic<int> cache[64];
-  int dev = 0, sms = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  if (dev < 64 && cache[dev].load() > 0) return cache[dev].load();
-  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) {
-    cudaGetLastError();
-    return 0;
-  }
-  const int c = sms * kStreamCtasPerSm;
-  if (dev < 64) cache[dev].store(c);
-  return c;
-}
-
-// Workspace of the stream-K kernel: the same counters, then two partial
-// slots per CTA of G rows of (max, sum, head_dim outputs).
-WsLayout stream_layout(int64_t num_seqs, const pkv_kv_desc* d, int64_t num_q_heads, int64_t ctas) {
-  WsLayout w{};
-  const int64_t group = num_q_heads / d->num_kv_heads;
-  w.counter_off = 0;
-  w.m_off = align_up(static_cast<size_t>(num_seqs * d->num_kv_heads) * sizeof(int), 256);
-  w.l_off = w.acc_off = w.m_off;
-  w.bytes = w.m_off + align_up(static_cast<size_t>(ctas) * 2 * group * (d->head_dim + 2) *
-                                   sizeof(float), 256);
-  return w;
-}
-
 
 // Process-wide kernel choice (pkv_set_attention_kernel).
 std::atomic<int> g_kernel_choice{PKV_KERNEL_AUTO};
 
-
-// Whether the stream-K kernel covers these sizes (automatic partition only).
-bool stream_eligible(const pkv_kv_desc* d, int num_seqs, int num_q_heads, int max_blocks) {
-  if (d->kv_dtype == PKV_F32 || num_q_heads % d->num_kv_heads != 0) return false;
-  if (num_q_heads / d->num_kv_heads > 16 || num_seqs > kStreamMaxSeqs) return false;
-  if (static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * d->block_size > INT32_MAX) return false;
-  const int64_t tiles = (static_cast<int64_t>(max_blocks) * d->block_size + 63) / 64;
-  if (tiles * d->num_kv_heads * num_seqs > INT32_MAX) return false;
-  return d->kv_dtype == PKV_E4M3 ? d->head_dim == 128 : (d->head_dim == 128 || d->head_dim == 64);
-}
 
 // Whether the tensor-core kernel covers these sizes.
 bool tc_supported(const pkv_kv_desc* d, int q_dtype, int group, int partition) {
@@ -280,12 +233,7 @@ extern "C" size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_
   int32_t p = 0;
   if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
   const int64_t s = num_splits(max_blocks, desc->block_size, p);
-  size_t bytes = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim).bytes;
-  if (partition_tokens == 0 && stream_eligible(desc, num_seqs, num_q_heads, max_blocks)) {
-    const int ctas = stream_ctas();
-    if (ctas > 0) bytes = std::max(bytes, stream_layout(num_seqs, desc, num_q_heads, ctas).bytes);
-  }
-  return bytes;
+  return workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim).bytes;
 }
 
 namespace pkv {
@@ -296,15 +244,13 @@ size_t attention_counter_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t ma
   if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
   const int64_t s = num_splits(max_blocks, desc->block_size, p);
   const WsLayout w = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim);
-  const bool stream = partition_tokens == 0 && stream_eligible(desc, num_seqs, num_q_heads, max_blocks);
-  if (!w.bytes && !stream) return 0;
+  if (!w.bytes) return 0;
   return align_up(static_cast<size_t>(num_seqs) * desc->num_kv_heads * sizeof(int), 256);
 }
 }  // namespace pkv
 
 extern "C" pkv_status pkv_set_attention_kernel(int32_t kind) {
-  if (kind != PKV_KERNEL_AUTO && kind != PKV_KERNEL_SIMT && kind != PKV_KERNEL_TENSOR_CORE &&
-      kind != PKV_KERNEL_PERSISTENT)
+  if (kind != PKV_KERNEL_AUTO && kind != PKV_KERNEL_SIMT && kind != PKV_KERNEL_TENSOR_CORE)
     return fail(PKV_ERR_INVALID_ARG, "unknown attention kernel kind");
   g_kernel_choice.store(kind);
   return PKV_OK;
@@ -358,17 +304,8 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   const int64_t splits = num_splits(max_blocks, desc->block_size, partition);
   if (splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits");
   const int choice = g_kernel_choice.load();
-  // The stream-K schedule needs its own workspace; with a smaller (or no)
-  // workspace the fixed-split schedule runs instead.
-  const int ctas = stream_ctas();
-  const WsLayout pws = stream_layout(num_seqs, desc, num_q_heads, ctas);
-  const bool use_stream = partition_tokens == 0 && choice == PKV_KERNEL_PERSISTENT && ctas > 0 &&
-                          stream_eligible(desc, num_seqs, num_q_heads, max_blocks) &&
-                          workspace != nullptr && workspace_bytes >= pws.bytes &&
-                          tc_supported(desc, q_dtype, group, 64);
-  const WsLayout ws = use_stream ? pws
-                              : workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, splits,
-                                                 desc->head_dim);
+  const WsLayout ws = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, splits,
+                                       desc->head_dim);
   if (ws.bytes > 0) {
     if (!workspace || workspace_bytes < ws.bytes)
       return fail(PKV_ERR_INVALID_ARG, "workspace missing or smaller than pkv_attention_workspace_bytes");
@@ -387,8 +324,6 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   a.ws_l = ws.bytes ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
   a.ws_acc = ws.bytes ? reinterpret_cast<float*>(wsb + ws.acc_off) : nullptr;
   a.counters = ws.bytes ? reinterpret_cast<int*>(wsb + ws.counter_off) : nullptr;
-  a.ws_part = use_stream ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
-  a.ctas = use_stream ? ctas : 0;
   a.max_blocks = max_blocks;
   a.num_seqs = num_seqs;
   a.num_q_heads = num_q_heads;
@@ -407,10 +342,10 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim;
   const bool tc_ok = tc_supported(desc, q_dtype, group, partition);
-  if ((choice == PKV_KERNEL_TENSOR_CORE || choice == PKV_KERNEL_PERSISTENT) && !tc_ok && !use_stream)
+  if (choice == PKV_KERNEL_TENSOR_CORE && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED, "the tensor-core kernel does not cover these sizes");
   if (k_new) {
-    if (!use_stream && tc_ok && choice != PKV_KERNEL_SIMT) {
+    if (tc_ok && choice != PKV_KERNEL_SIMT) {
       a.k_new = k_new;  // fused into the split kernel
       a.v_new = v_new;
       a.k_inv = kv == PKV_E4M3 ? k_inv : 1.0f;
@@ -422,20 +357,11 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
       if (st != PKV_OK) return st;
     }
   }
-  if (use_stream || (tc_ok && choice != PKV_KERNEL_SIMT)) {
+  if (tc_ok && choice != PKV_KERNEL_SIMT) {
     CUtensorMap kmap, vmap;
     st = pool_map(&kmap, k_cache, desc);
     if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc);
     if (st != PKV_OK) return st;
-    if (use_stream) {
-      switch (kv) {
-        case PKV_F16: return launch_decode_stream<F16, F16>(a, D, kmap, vmap, s);
-        case PKV_BF16: return launch_decode_stream<BF16, BF16>(a, D, kmap, vmap, s);
-        default:
-          return q_dtype == PKV_F16 ? launch_decode_stream<E4M3, F16>(a, D, kmap, vmap, s)
-                                    : launch_decode_stream<E4M3, BF16>(a, D, kmap, vmap, s);
-      }
-    }
     switch (kv) {
       case PKV_F16: return launch_decode_tc<F16, F16>(a, D, kmap, vmap, s);
       case PKV_BF16: return launch_decode_tc<BF16, BF16>(a, D, kmap, vmap, s);

@@ -23,8 +23,6 @@ struct DecodeArgs {
   float* ws_l;               // split-K partial sums      [B][Hq][S]
   float* ws_acc;             // split-K partial outputs   [B][Hq][S][D]
   int* counters;             // split-K arrival counters  [B][N_kv], zero between calls
-  float* ws_part;            // stream-K kernel: 2 partial slots per CTA, [ctas][2][G][D + 2]
-  int32_t ctas;              // stream-K kernel: grid size (three CTAs per SM)
   // fused slot write (tensor-core split kernel): when k_new is set, the CTA
   // holding position ctx - 1 of (sequence, KV head) first stores that
   // token's K/V ([B][N_kv][D], q dtype), E4M3-rounded with k_inv / v_inv
@@ -41,10 +39,6 @@ struct DecodeArgs {
   const float* head_scales;
   float softmax_scale;
 };
-
-// Limits of the stream-K tensor-core kernel: the per-sequence tile prefix sum
-// is built in its 64 KiB ring ((num_seqs + 1) ints), and tile indices are int.
-constexpr int kStreamMaxSeqs = 16383;
 
 // Bytes at the start of a decode workspace that hold the split-K arrival
 // counters (they must be zero when a call starts; every call leaves them

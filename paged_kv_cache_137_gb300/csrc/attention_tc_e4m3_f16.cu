@@ -1,9 +1,7 @@
-// Tensor-core decode attention kernels (split and stream-K) for a E4M3 cache with F16 queries.
+// Tensor-core decode attention kernel for a E4M3 cache with F16 queries.
 #include "attention_tc_launch.cuh"
 
 namespace pkv {
 template pkv_status launch_decode_tc<E4M3, F16>(const DecodeArgs&, int, const CUtensorMap&,
                                               const CUtensorMap&, cudaStream_t);
-template pkv_status launch_decode_stream<E4M3, F16>(const DecodeArgs&, int, const CUtensorMap&,
-                                                   const CUtensorMap&, cudaStream_t);
 }  // namespace pkv

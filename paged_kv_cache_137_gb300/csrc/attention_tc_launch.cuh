@@ -5,7 +5,7 @@
 #include <atomic>
 #include <utility>
 
-#include "attention_stream.cuh"
+#include "attention_tc.cuh"
 
 namespace pkv {
 namespace tc {
@@ -68,55 +68,7 @@ pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
                       : launch_form<KV, Q, D, T, false>(a, kmap, vmap, st);
 }
 
-// Stream-K kernel: a.ctas CTAs (three per SM, one wave), 64 KiB ring each.
-template <typename KV, typename Q, int D, int T>
-pkv_status launch_stream_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                            cudaStream_t st) {
-  constexpr int smem = stream_smem_bytes<KV, D>();
-  auto kernel = decode_stream_kernel<KV, Q, D, T>;
-  static std::atomic<uint64_t> configured{0};
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaGetDevice", e);
-  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
-  if (!bit || !(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaFuncSetAttribute", e);
-    configured.fetch_or(bit);
-  }
-  // One wave: if fewer than three CTAs fit on an SM, shrink the grid to what
-  // is resident (the partial slots are sized for three per SM).
-  static std::atomic<int> occupancy[64];
-  int occ = dev < 64 ? occupancy[dev].load() : 0;
-  if (occ == 0) {
-    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem);
-    if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: occupancy query", e);
-    if (occ < 1) return fail(PKV_ERR_UNSUPPORTED, "stream-K kernel: no CTA fits on an SM");
-    if (dev < 64) occupancy[dev].store(occ);
-  }
-  const int ctas = occ >= kStreamCtasPerSm ? a.ctas : a.ctas / kStreamCtasPerSm * occ;
-  e = launch_dependent(kernel, dim3(ctas), kThreads, smem, st, a, kmap, vmap);
-  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: stream-K launch", e);
-  return check_launch("pkv_attention_decode (stream-K)");
-}
-
 }  // namespace tc
-
-template <typename KV, typename Q>
-pkv_status launch_decode_stream(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
-                                const CUtensorMap& vmap, cudaStream_t st) {
-  const int T = a.block_size;
-  if constexpr (std::is_same<KV, E4M3>::value) {
-    if (head_dim == 128 && T == 16) return tc::launch_stream_dt<KV, Q, 128, 16>(a, kmap, vmap, st);
-    if (head_dim == 128 && T == 32) return tc::launch_stream_dt<KV, Q, 128, 32>(a, kmap, vmap, st);
-  } else {
-    if (head_dim == 128 && T == 16) return tc::launch_stream_dt<KV, Q, 128, 16>(a, kmap, vmap, st);
-    if (head_dim == 128 && T == 32) return tc::launch_stream_dt<KV, Q, 128, 32>(a, kmap, vmap, st);
-    if (head_dim == 64 && T == 16) return tc::launch_stream_dt<KV, Q, 64, 16>(a, kmap, vmap, st);
-    if (head_dim == 64 && T == 32) return tc::launch_stream_dt<KV, Q, 64, 32>(a, kmap, vmap, st);
-  }
-  return fail(PKV_ERR_UNSUPPORTED, "stream-K kernel: head_dim/block_size not compiled");
-}
 
 template <typename KV, typename Q>
 pkv_status launch_decode_tc(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,

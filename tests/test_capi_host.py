@@ -501,8 +501,6 @@ def test_workspace_bytes_reject_bad_sizes():
     assert pkv.pkv_attention_workspace_bytes(4, 28, 100, desc32, 64) > 0   # 64 is a multiple of 32
 
 
-@pytest.mark.skipif(__import__("torch").cuda.is_available(),
-                    reason="on a GPU the automatic partition may add the stream-K schedule's slots")
 def test_automatic_workspace_is_the_resolved_partitions():
     desc = pkv.kv_desc(8500, 4, 128, 16, "bf16")
     p = pkv.pkv_attention_partition(64, 243, desc)

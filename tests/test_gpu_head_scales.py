@@ -37,7 +37,7 @@ def built():
     assert torch.cuda.is_available()
 
 
-@pytest.fixture(params=["auto", "simt", "tc", "persistent"])
+@pytest.fixture(params=["auto", "simt", "tc"])
 def kernel(request):
     pkv.pkv_set_attention_kernel(request.param)
     yield request.param

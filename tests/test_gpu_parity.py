@@ -75,10 +75,9 @@ def built():
     assert torch.cuda.is_available()
 
 
-@pytest.fixture(params=["simt", "tc", "persistent"])
+@pytest.fixture(params=["simt", "tc"])
 def kernel(request):
-    """Run a test once per decode kernel (CUDA-core, tensor-core with fixed
-    splits, tensor-core persistent stream-K)."""
+    """Run a test once per decode kernel (CUDA-core, tensor-core)."""
     pkv.pkv_set_attention_kernel(request.param)
     yield request.param
     pkv.pkv_set_attention_kernel("auto")
@@ -92,7 +91,7 @@ def tc_covers(w):
 @pytest.mark.parametrize("name", list(SMALL))
 def test_step_matches_oracle(name, kernel):
     w = SMALL[name]
-    if kernel in ("tc", "persistent") and not tc_covers(w):
+    if kernel == "tc" and not tc_covers(w):
         pytest.skip("the tensor-core kernel does not cover this cache")
     sc = scales_for(w)
     dev = PS.materialize(PS.plan(w), "cuda", sc)
@@ -280,7 +279,7 @@ def test_kernels_agree(name):
     dev.write_step()
     outs = []
     try:
-        for k in ("simt", "tc", "persistent"):
+        for k in ("simt", "tc"):
             pkv.pkv_set_attention_kernel(k)
             outs.append(dev.attend().double().cpu().numpy().copy())
     finally:
@@ -302,12 +301,12 @@ def test_split_counters_are_zero_after_a_call():
 
 
 @pytest.mark.parametrize("name", ["qwen_small", "fp8_small", "gqa16_d64"])
-def test_persistent_kernel_with_edited_lengths(name, kernel):
-    """The automatic schedule (the persistent stream-K kernel for the tensor
-    cores) with some lengths cut to 0, 1, 63, 64 and 65 tokens, so that empty
-    sequences, one-token sequences and tile edges sit between long ones."""
+def test_automatic_partition_with_edited_lengths(name, kernel):
+    """The automatic partition with some lengths cut to 0, 1, 63, 64 and 65
+    tokens, so that empty sequences, one-token sequences and tile edges sit
+    between long ones."""
     w = SMALL[name]
-    if kernel in ("tc", "persistent") and not tc_covers(w):
+    if kernel == "tc" and not tc_covers(w):
         pytest.skip("the tensor-core kernel does not cover this cache")
     sc = scales_for(w)
     dev = PS.materialize(PS.plan(w), "cuda", sc, partition_tokens=0)
@@ -330,17 +329,9 @@ def test_persistent_kernel_with_edited_lengths(name, kernel):
         assert np.all(out[0] == 0)
 
 
-def test_persistent_kernel_batch_of_one_and_many_ctas():
-    """A single short sequence (fewer tiles than CTAs) and a single long one
-    (every CTA holds a piece of the same pair)."""
-    pkv.pkv_set_attention_kernel("persistent")
-    try:
-        _one_and_many()
-    finally:
-        pkv.pkv_set_attention_kernel("auto")
-
-
-def _one_and_many():
+def test_batch_of_one_short_and_one_long_sequence():
+    """A single short sequence (one tile) and a single long one (the
+    automatic partition splits it over many CTAs)."""
     for ctx_range in [(40, 40), (30000, 30000)]:
         w = W.scaled(W.get("long_mha_bf16"), num_seqs=1, num_q_heads=8, num_kv_heads=1,
                      num_blocks=1000, ctx_range=ctx_range, partition_tokens=0, seed=97)
