@@ -32,6 +32,8 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 sys.path.insert(0, ROOT)
 
 DEFAULT_CONFIG = "qwen_gqa_bf16"
+# the other decode workloads the default run also measures (``per_config``)
+OTHER_CONFIGS = ("tiny_fp32", "prefix_fork_bf16", "long_mha_bf16", "fp8_churn")
 METRIC = "paged decode attention KV GB/s & fraction of GB300 HBM peak; decode tokens/s"
 # the sources each kernel family's recorded DRAM counters depend on
 KERNEL_SOURCES = {
@@ -52,10 +54,20 @@ def parse():
     ap.add_argument("--config", default=DEFAULT_CONFIG)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="measure only the configured workload (default: also the other decode "
+                         "workloads, under per_config)")
+    ap.add_argument("--per-config-cpu-seconds", type=float, default=3.0)
+    ap.add_argument("--timed-ms", type=float, default=200.0,
+                    help="device time each timed graph is replayed for, at least (0: five replays "
+                         "and K end-to-end steps, for profiling runs)")
     ap.add_argument("--partition", type=int, default=None,
                     help="split-K partition in tokens (default: the workload's, else automatic)")
     ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"],
                     help="decode kernel (auto = tensor-core where it applies)")
+    ap.add_argument("--shared-prefix", default="auto", choices=["auto", "on", "off"],
+                    help="decode a batch's shared prefix once for all sequences (auto: when the "
+                         "batch shares at least 256 tokens over at least 128 query rows)")
     ap.add_argument("--block-size", type=int, default=None,
                     help="ablation: tokens per block (the pool keeps the same token capacity)")
     ap.add_argument("--fp8-scales", default="tensor", choices=["tensor", "head"],
@@ -174,11 +186,13 @@ def workload_of(args):
     return w
 
 
-def attention_kernels(kernel: str, w, splits: int) -> str:
+def attention_kernels(kernel: str, w, splits: int, shared_prefix: bool = False) -> str:
     """The kernels one attention call launches (timed together, as one graph)."""
     if w.kv_dtype == "f32" or kernel == "simt":
         k = "decode_simt_kernel"
         return k + (" + merge_kernel" if splits > 1 else "")
+    if shared_prefix:
+        return "prefill_umma_kernel<shared prefix> + decode_tc_kernel (merge fused)"
     return "decode_tc_kernel (split-K merge fused)"
 
 
@@ -470,22 +484,148 @@ def run_reference(args, world, rank):
 
 
 # --------------------------------------------------------------------- GPU
+def replay_timed(graph, stream, min_ms: float, max_replays: int = 5000):
+    """Replay a captured graph back to back until at least ``min_ms`` of
+    device time is timed (the first replay sizes the count, at least 5),
+    each replay bracketed by CUDA events on ``stream`` -> per-replay ms."""
+    import torch
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    graph.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    n = int(min(max_replays, max(5, -(-min_ms // max(a.elapsed_time(b), 1e-3)))))
+    evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for a, b in evs:
+        a.record(stream)
+        graph.replay()
+        b.record(stream)
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in evs]
+
+
+def capture(fn, K: int):
+    """K calls of ``fn`` captured back to back in one CUDA graph."""
+    import torch
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(K):
+            fn()
+    g.replay()
+    return g
+
+
+def warm(scn, n: int, device):
+    """n untimed steps on a side stream (the capture warm-up PyTorch asks for)."""
+    import torch
+    stream = torch.cuda.current_stream()
+    side = torch.cuda.Stream(device=device)
+    side.wait_stream(stream)
+    with torch.cuda.stream(side):
+        for _ in range(n):
+            scn.step()
+    stream.wait_stream(side)
+    torch.cuda.synchronize()
+
+
+def scenario_for(config: str, args, device, w=None):
+    import workloads as W
+    from paged_kv_cache_137_gb300 import scenario as PS
+    w = w or W.get(config)
+    sc = {}
+    if w.kv_dtype == "e4m3":
+        sc = W.fp8_head_scales(w) if args.fp8_scales == "head" else W.fp8_scales(*W.kv_amax(w))
+    return PS.materialize(PS.plan(w), device, sc, partition_tokens=args.partition,
+                          shared_prefix={"auto": None, "on": True, "off": False}[args.shared_prefix])
+
+
+def oracle_sample(config: str, seconds: float, n_rows: int = 4):
+    """The oracle (unchanged) on one host core over a bounded sample of a
+    workload: ``n_rows`` sequences spread over the batch (their pool blocks
+    written, the rest of the batch only planned), passes until ``seconds``
+    elapse -> cpu_baseline entry (GB/s of their logical K/V bytes)."""
+    import math
+    import numpy as np
+    import workloads as W
+    from oracle import attention as OA
+    from oracle import scenario as OS
+    w = W.get(config)
+    sc = W.fp8_scales(*W.kv_amax(w)) if w.kv_dtype == "e4m3" else {}
+    rows = sorted({int(r) for r in np.linspace(0, w.num_seqs - 1, min(n_rows, w.num_seqs))})
+    scn = OS.build(w, write_seqs=rows, scales=sc)
+    q = scn.q_f64()
+    nbytes = 2 * int(np.sum(np.asarray(scn.ctx)[rows])) * w.num_kv_heads * w.head_dim * w.kv_bytes
+    el, passes = 0.0, 0
+    while passes == 0 or el < seconds:
+        t0 = time.perf_counter()
+        OA.paged_attention_decode(q, scn.pool, scn.tables, scn.ctx, 1.0 / math.sqrt(w.head_dim),
+                                  sc.get("k_scale", 1.0), sc.get("v_scale", 1.0), seqs=rows)
+        el += time.perf_counter() - t0
+        passes += 1
+    return {"value": round(nbytes * passes / el / 1e9, 4), "unit": "GB/s", "cores": 1, "kind": "oracle",
+            "sample": f"sequences {rows} of {config} ({nbytes / 1e6:.1f} MB of K/V), {passes} pass(es) "
+                      f"in {el:.1f} s on one host core"}
+
+
+def per_config_entry(config: str, args, device, local, peak: float):
+    """One workload's device figures (no reference arm, no end-to-end leg):
+    the K-step graph and the K-attention graph each replayed for half of
+    --timed-ms (100 ms by default),
+    medians; the roofline over the distinct cache bytes; an oracle sample."""
+    import numpy as np
+    import torch
+    scn = scenario_for(config, args, device)
+    w = scn.plan.w
+    stream = torch.cuda.current_stream()
+    K = args.steps
+    warm(scn, max(args.warmup, 3), device)
+    g_steps, g_attns = capture(scn.step, K), capture(scn.attend, K)
+    torch.cuda.synchronize()
+    with ClockSampler(local) as clk:
+        steps = replay_timed(g_steps, stream, args.timed_ms / 2)
+        attns = replay_timed(g_attns, stream, args.timed_ms / 2)
+    ms = statistics.median(steps) / K
+    attn = statistics.median(attns) / K
+    kv_bytes, unique = scn.kv_bytes(), scn.kv_unique_bytes()
+    l2 = torch.cuda.get_device_properties(local).L2_cache_size
+    kernels = attention_kernels(args.kernel, w, 2, bool(scn.prefix_blocks))
+    traffic = traffic_for(config, kernels)
+    e = {"workload": config, "num_seqs": w.num_seqs, "kv_dtype": w.kv_dtype,
+         "kv_bytes_per_step": kv_bytes, "algorithmic_bytes": unique,
+         "shared_prefix_blocks": scn.prefix_blocks, "partition_tokens": scn.partition,
+         "ms_per_step": round(ms, 4), "value": round(kv_bytes / (ms / 1e3) / 1e9, 2), "unit": "GB/s",
+         "tokens_per_s": round(w.num_seqs / (ms / 1e3), 1),
+         "attention_ms": round(attn, 4), "kernel": kernels,
+         "achieved": round(unique / (attn / 1e3) / 1e9, 2),
+         "frac": round(unique / (attn / 1e3) / 1e9 / peak, 4),
+         "traffic": traffic,
+         **({"dram_achieved": round(traffic / (attn / 1e3) / 1e9, 2)} if traffic else {}),
+         "replays": {"steps": len(steps), "attention": len(attns)},
+         "l2": "inputs %s than L2 (distinct K/V %d MB vs %d MB)" % (
+             "larger" if unique > l2 else "smaller", unique >> 20, l2 >> 20),
+         "clocks": clk.summary()}
+    if unique != kv_bytes:
+        e["logical_achieved"] = round(kv_bytes / (attn / 1e3) / 1e9, 2)
+    if w.kv_dtype == "f32":
+        e["note"] = "correctness workload: too small to time meaningfully"
+    del scn, g_steps, g_attns
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return e
+
+
 def run_gpu(args, world, rank, local):
     import numpy as np
     import torch
     import workloads as W
     import paged_kv_cache_137_gb300 as pkv
-    from paged_kv_cache_137_gb300 import scenario as PS
 
     pkv.build()
     pkv.pkv_set_attention_kernel(args.kernel)
     torch.cuda.set_device(local)
     dev_name = f"cuda:{local}"
     w = workload_of(args)
-    sc = {}
-    if w.kv_dtype == "e4m3":
-        sc = W.fp8_head_scales(w) if args.fp8_scales == "head" else W.fp8_scales(*W.kv_amax(w))
-    scn = PS.materialize(PS.plan(w), dev_name, sc, partition_tokens=args.partition)
+    scn = scenario_for(args.config, args, dev_name, w)
     stream = torch.cuda.current_stream()
     kv_bytes = scn.kv_bytes()
     props = torch.cuda.get_device_properties(local)
@@ -504,52 +644,35 @@ def run_gpu(args, world, rank, local):
     # is the slot write outside the tensor-core split kernel (which fuses it)
     separate_merge = args.kernel == "simt" or w.kv_dtype == "f32"
     fused_write = not separate_merge
-    attn_launches = 1 + (1 if separate_merge and splits > 1 else 0)
+    attn_launches = 1 + (1 if separate_merge and splits > 1 else 0) + (1 if scn.prefix_blocks else 0)
     launches_per_step = (0 if fused_write else 1) + attn_launches + \
         (-(-n_pairs // 1024) if n_pairs else 0)
 
-    side = torch.cuda.Stream(device=dev_name)
-    side.wait_stream(stream)
-    with torch.cuda.stream(side):
-        for _ in range(max(args.warmup, 3)):
-            scn.step()
-    stream.wait_stream(side)
-    torch.cuda.synchronize()
+    warm(scn, max(args.warmup, 3), dev_name)
     # Timed region: the K steps (block copies, slot write, decode attention)
-    # captured back to back in ONE CUDA graph, replayed once, as a serving
-    # loop replays a whole decode step: no library call and no graph launch
-    # sits between two steps (one graph launch costs several microseconds on
-    # its own).  No L2 flush between steps: the K/V each step reads is larger
-    # than the L2.  K attention calls in a second graph give the decode
-    # kernel's average duration for the roofline.  The isolated figures (one
-    # step per graph launch, the L2 evicted by a read before each) are
-    # reported beside them.
+    # captured back to back in ONE CUDA graph, as a serving loop replays a
+    # whole decode step: no library call and no graph launch sits between two
+    # steps (one graph launch costs several microseconds on its own).  The
+    # graph is replayed back to back until at least --timed-ms (200 ms) of device time is
+    # timed, each replay between CUDA events; ms_per_step is the median
+    # replay / K.  No L2 flush between steps: the K/V each step reads is
+    # larger than the L2.  K attention calls in a second graph, timed the
+    # same way (half as long), give the decode kernel's average duration for the
+    # roofline.  The isolated figures (one step per graph launch, the L2
+    # evicted by a read before each) are reported beside them.
     K = args.steps
-    g_steps, g_attns = torch.cuda.CUDAGraph(), torch.cuda.CUDAGraph()
-    with torch.cuda.graph(g_steps):
-        for _ in range(K):
-            scn.step()
-    with torch.cuda.graph(g_attns):
-        for _ in range(K):
-            scn.attend()
-    g_steps.replay()
-    g_attns.replay()
+    g_steps, g_attns = capture(scn.step, K), capture(scn.attend, K)
     torch.cuda.synchronize()
 
-    ev = [torch.cuda.Event(enable_timing=True) for _ in range(4)]
     barrier(world)
     torch.cuda.synchronize()
     with ClockSampler(local) as clk:
-        ev[0].record(stream)
-        g_steps.replay()
-        ev[1].record(stream)
-        ev[2].record(stream)
-        g_attns.replay()
-        ev[3].record(stream)
+        step_reps = replay_timed(g_steps, stream, args.timed_ms)
         torch.cuda.synchronize()
         barrier(world)
-    ms = max_over_ranks(ev[0].elapsed_time(ev[1]) / K, world)
-    attn = ev[2].elapsed_time(ev[3]) / K
+        attn_reps = replay_timed(g_attns, stream, args.timed_ms / 2)
+    ms = max_over_ranks(statistics.median(step_reps) / K, world)
+    attn = statistics.median(attn_reps) / K
     value = world * kv_bytes / (ms / 1e3) / 1e9
 
     # isolated: one step (or one attention call) per graph launch, L2 evicted
@@ -574,11 +697,7 @@ def run_gpu(args, world, rank, local):
     # launch cost is spread over them (each call rewrites the same slots or
     # copies the same blocks)
     def per_call_us(fn, reps=20):
-        g = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(g):
-            for _ in range(reps):
-                fn()
-        g.replay()
+        g = capture(fn, reps)
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         g.replay()
@@ -603,37 +722,10 @@ def run_gpu(args, world, rank, local):
     # batch's sequences and their block tables exported, on a copy of the plan
     aux["allocator_step_us"] = round(allocator_step_us(scn.plan), 2)
 
-    # end to end through the C ABI from pinned host buffers: the step's inputs
-    # (q, the new K/V, block tables, context lengths) packed in one pinned
-    # buffer and copied in once, the output copied back, then a sync
-    names = ("q", "k_new", "v_new", "tables", "ctx")
-    dev_in, views = packed([getattr(scn, n) for n in names], dev_name)
-    for n_, v_ in zip(names, views):
-        setattr(scn, n_, v_)
-    host_in = dev_in.cpu().pin_memory()
-    out_host = torch.empty_like(scn.out, device="cpu").pin_memory()
-    h2d = host_in.numel()
-    d2h = out_host.numel() * out_host.element_size()
-
-    def e2e_step():
-        dev_in.copy_(host_in, non_blocking=True)
-        scn.step()
-        out_host.copy_(scn.out, non_blocking=True)
-        torch.cuda.synchronize()
-
-    for _ in range(3):
-        e2e_step()
-    barrier(world)
-    torch.cuda.synchronize()
-    t0 = time.perf_counter()
-    for _ in range(K):
-        e2e_step()
-    e2e_s = max_over_ranks((time.perf_counter() - t0) / K, world)
-    e2e_val = world * kv_bytes / e2e_s / 1e9
-    e2e_graph = e2e_graph_of(e2e_step, dev_in, host_in, scn, out_host, K, kv_bytes) if world == 1 else None
+    e2e, e2e_graph = end_to_end(scn, dev_name, K if args.timed_ms == 0 else max(K, 200), world, kv_bytes)
 
     peak, peak_kind = peaks()
-    kernels = attention_kernels(args.kernel, w, splits)
+    kernels = attention_kernels(args.kernel, w, splits, bool(scn.prefix_blocks))
     # the profiled counters describe the configured workload only
     traffic = traffic_for(args.config, kernels) if w == W.get(args.config) else None
     # the roofline's algorithmic bytes: each stored K/V element once, however
@@ -644,8 +736,7 @@ def run_gpu(args, world, rank, local):
     if unique_bytes != kv_bytes:
         shared = {"algorithmic_bytes": unique_bytes,
                   "logical_achieved": round(kv_bytes / (attn / 1e3) / 1e9, 2),
-                  "note": "blocks shared by several sequences count once in achieved; the L2 "
-                          "serves their re-reads, so the logical rate can exceed the HBM peak"}
+                  "note": "blocks shared by several sequences count once in achieved"}
     line = {
         "metric": METRIC, "value": round(value, 2), "unit": "GB/s", "n_gpus": world, "steps": K,
         "warmup": max(args.warmup, 3), "ms_per_step": round(ms, 4), "higher_is_better": True,
@@ -655,13 +746,16 @@ def run_gpu(args, world, rank, local):
                    "num_kv_heads": w.num_kv_heads, "head_dim": w.head_dim, "block_size": w.block_size,
                    "num_blocks": w.num_blocks, "context_tokens": int(scn.plan.ctx.sum()),
                    "kv_bytes_per_step": kv_bytes, "partition_tokens": scn.partition,
+                   "shared_prefix_blocks": scn.prefix_blocks,
                    "kv_dtype": w.kv_dtype, "table_entries": int(np.ceil(scn.plan.ctx / w.block_size).sum()),
                    **({"fp8_scales": args.fp8_scales} if w.kv_dtype == "e4m3" else {}),
                    "waste_slots_per_seq": round(float((np.ceil(scn.plan.ctx / w.block_size) * w.block_size
                                                        - scn.plan.ctx).mean()), 2),
                    "l2": ("inputs larger than L2 (K/V %d MB vs %d MB L2), no flush between steps"
                           % (kv_bytes >> 20, props.L2_cache_size >> 20)),
-                   "launch": "the K steps captured back to back in one CUDA graph, replayed once",
+                   "launch": ("the K steps captured back to back in one CUDA graph; the graph replayed "
+                              "%d times back to back (%.0f ms timed), median replay / K"
+                              % (len(step_reps), sum(step_reps))),
                    "parallelism": "replicas" if world > 1 else "single"},
         "tokens_per_s": round(world * w.num_seqs / (ms / 1e3), 1),
         "frac_of_hbm_peak": round(value / peak, 4),
@@ -670,18 +764,20 @@ def run_gpu(args, world, rank, local):
                      "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "peak_source": peak_kind,
                      "traffic": traffic, "attention_ms": round(attn, 4),
+                     "attention_replays": len(attn_reps),
                      **({"dram_achieved": round(traffic / (attn / 1e3) / 1e9, 2)} if traffic else {}),
                      **shared},
-        "e2e": {"value": round(e2e_val, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4)},
+        "e2e": e2e,
         **({"e2e_graph": e2e_graph} if e2e_graph is not None else {}),
-        "gpu_launches": K * (launches_per_step + attn_launches),
+        "gpu_launches": (len(step_reps) + 1) * K * launches_per_step
+                        + (len(attn_reps) + 1) * K * attn_launches,
         "aux": aux,
         "isolated": {"what": "one step (one attention call) per graph launch, L2 evicted by reading a "
                              "2x-L2 buffer before each; median of 20",
                      "step_ms": round(iso_ms["step"], 4), "attention_ms": round(iso_ms["attention"], 4),
                      "value": round(world * kv_bytes / (iso_ms["step"] / 1e3) / 1e9, 2),
-                     "attention_GBs": round(kv_bytes / (iso_ms["attention"] / 1e3) / 1e9, 2)},
+                     "attention_GBs": round(unique_bytes / (iso_ms["attention"] / 1e3) / 1e9, 2),
+                     "attention_frac": round(unique_bytes / (iso_ms["attention"] / 1e3) / 1e9 / peak, 4)},
         "clocks": clk.summary(),
     }
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -691,8 +787,97 @@ def run_gpu(args, world, rank, local):
                                 "sample": f"whole batch of {args.config}, {passes} pass(es) in {el:.1f} s "
                                           f"on {cores} worker processes (sequences interleaved); "
                                           f"one core: whole batch on one worker"}
+    # the other workloads (one GPU, default configuration only)
+    if world == 1 and not args.no_per_config and args.config == DEFAULT_CONFIG and w == W.get(args.config):
+        del scn, g_steps, g_attns, g_step, g_attn
+        torch.cuda.synchronize()
+        torch.cuda.empty_cache()
+        per = {}
+        for cfg in OTHER_CONFIGS:
+            e = per_config_entry(cfg, args, dev_name, local, peak)
+            if not args.no_cpu_baseline:
+                e["cpu_baseline"] = oracle_sample(cfg, args.per_config_cpu_seconds)
+            per[cfg] = e
+        line["per_config"] = per
     if rank == 0:
         print(json.dumps(line), flush=True)
+
+
+def end_to_end(scn, dev_name, n: int, world: int, kv_bytes: int):
+    """The step through the C ABI with its inputs copied from pinned host
+    memory and its output copied back, every step.  Two input/output buffer
+    pairs alternate: step i's host-to-device copy runs on a copy stream while
+    step i - 1 computes, its device-to-host copy after it, and the host waits
+    for step i - 1's output before issuing step i + 1 (one step in flight),
+    as a serving loop that overlaps transfers with compute does.  Inputs per
+    step: q, the new K/V, block tables and context lengths packed in one
+    pinned buffer (one copy); output: the attention result.  GB/s over the
+    host's wall clock.  The graph figure (copy in, step, copy out captured as
+    one CUDA graph, one replay and one host sync per step) is reported beside
+    it."""
+    import copy as _copy
+    import torch
+    names = ("q", "k_new", "v_new", "tables", "ctx")
+    slots = []
+    for _ in range(2):
+        dev_in, views = packed([getattr(scn, n) for n in names], dev_name)
+        s = _copy.copy(scn)
+        for n_, v_ in zip(names, views):
+            setattr(s, n_, v_)
+        s.out = torch.empty_like(scn.out)
+        host_in = dev_in.cpu().pin_memory()
+        host_out = torch.empty_like(scn.out, device="cpu").pin_memory()
+        slots.append({"scn": s, "dev_in": dev_in, "host_in": host_in, "host_out": host_out,
+                      "in_ev": torch.cuda.Event(), "done_ev": torch.cuda.Event(),
+                      "out_ev": torch.cuda.Event()})
+    h2d = slots[0]["host_in"].numel()
+    d2h = slots[0]["host_out"].numel() * slots[0]["host_out"].element_size()
+    compute = torch.cuda.current_stream()
+    copy_s = torch.cuda.Stream(device=dev_name)
+
+    def issue(i):
+        sl = slots[i % 2]
+        with torch.cuda.stream(copy_s):
+            copy_s.wait_event(sl["done_ev"])       # step i - 2 is done with this buffer
+            sl["dev_in"].copy_(sl["host_in"], non_blocking=True)
+            sl["in_ev"].record(copy_s)
+        compute.wait_event(sl["in_ev"])
+        sl["scn"].step()
+        sl["done_ev"].record(compute)
+        with torch.cuda.stream(copy_s):
+            copy_s.wait_event(sl["done_ev"])
+            sl["host_out"].copy_(sl["scn"].out, non_blocking=True)
+            sl["out_ev"].record(copy_s)
+
+    def run(n):
+        for i in range(n):
+            issue(i)
+            if i >= 1:
+                slots[(i - 1) % 2]["out_ev"].synchronize()   # step i - 1's output is on the host
+        slots[(n - 1) % 2]["out_ev"].synchronize()
+
+    run(4)
+    torch.cuda.synchronize()
+    barrier(world)
+    t0 = time.perf_counter()
+    run(n)
+    e2e_s = max_over_ranks((time.perf_counter() - t0) / n, world)
+    e2e = {"value": round(world * kv_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
+           "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4), "steps": n,
+           "what": "host-to-device copy of the step's inputs and device-to-host copy of its output "
+                   "every step, two buffer pairs alternating so that copies overlap the previous "
+                   "step's compute; host wall clock"}
+    g = None
+    if world == 1:
+        s0 = slots[0]
+
+        def serial_step():
+            s0["dev_in"].copy_(s0["host_in"], non_blocking=True)
+            s0["scn"].step()
+            s0["host_out"].copy_(s0["scn"].out, non_blocking=True)
+            torch.cuda.synchronize()
+        g = e2e_graph_of(serial_step, s0["dev_in"], s0["host_in"], s0["scn"], s0["host_out"], n, kv_bytes)
+    return e2e, g
 
 
 # ------------------------------------------------------------------ prefill

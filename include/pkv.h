@@ -24,9 +24,11 @@
  *   - Host allocator calls are all-or-nothing: on error nothing changes.
  *   - Device buffers are owned by the caller (plain device pointers).  The
  *     library never allocates or frees device memory at run time; its only
- *     device memory is the fixed static scratch of
- *     pkv_attention_decode_noalloc, resident on each GPU that loads it.  A pool
- *     handle owns only host-side allocator state.
+ *     device memory is two fixed static arrays resident on each GPU that
+ *     loads it: the device error word (pkv_device_status) and the scratch of
+ *     pkv_attention_decode_noalloc.  Their addresses are looked up once per
+ *     device and kept, so cudaDeviceReset while the library is in use is not
+ *     supported.  A pool handle owns only host-side allocator state.
  *   - Device calls enqueue kernels on the given CUDA stream (a cudaStream_t
  *     passed as void*, NULL = legacy default stream) and return without
  *     synchronising; a launch failure returns PKV_ERR_CUDA.
@@ -193,6 +195,17 @@ PKV_API pkv_status pkv_block_tables_update(const pkv_pool* pool, const int64_t* 
                                            int32_t* tables_inout, int64_t* rows_inout,
                                            int32_t* context_lens_out);
 
+/* Shared prefix of a batch: *n_blocks receives the number k of leading
+ * block-table entries that every listed sequence maps to the same physical
+ * blocks (one stored copy serves them all: [A "Complex Topologies"], [B
+ * "Sharing, the second dividend"]), limited so that k * block_size <= len - 1
+ * for every sequence (the block holding a sequence's last position, the one a
+ * decode step writes, is never part of it).  Pass k to
+ * pkv_attention_decode_shared_prefix.  UNKNOWN_SEQ / INVALID_ARG as
+ * pkv_block_tables; 0 for an empty batch. */
+PKV_API pkv_status pkv_shared_prefix_blocks(const pkv_pool* pool, const int64_t* seq_ids,
+                                            int32_t n_seqs, int32_t* n_blocks);
+
 /* Reference count of one block (0 = free). */
 PKV_API pkv_status pkv_block_refcount(const pkv_pool* pool, int32_t block, int32_t* refcount);
 
@@ -330,6 +343,79 @@ PKV_API pkv_status pkv_decode_step(void* out, const void* q, int32_t q_dtype, vo
                                    float k_inv_scale, float v_inv_scale, int32_t partition_tokens,
                                    void* workspace, size_t workspace_bytes, void* stream);
 
+/* Decode attention over a shared prefix ([A "Complex Topologies and Memory
+ * Sharing"]: several sequences map the same prompt blocks; [B "Sharing, the
+ * second dividend"]).  The same result as pkv_attention_decode (within
+ * rounding), for a batch whose first prefix_blocks table entries are the
+ * same physical blocks in every row (pkv_shared_prefix_blocks).  The call
+ * reads those blocks once for all sequences instead of once per sequence:
+ *   - a shared-prefix pass on the 5th-generation tensor cores (tcgen05)
+ *     attends the queries of all sequences and heads of a KV head (M rows =
+ *     num_seqs * group) to positions [0, P), P = prefix_blocks * block_size,
+ *     read through row 0 of block_tables, and leaves per-row partial results
+ *     (max, sum, unnormalised output) in the workspace;
+ *   - the decode kernel attends positions [P, ctx) of each sequence and
+ *     merges its partials with the prefix pass's.
+ * Because the reduction is split differently, results can differ from
+ * pkv_attention_decode in the low-order bits ([C "Effect"]: reusing shared
+ * blocks changes how the attention reduction is tiled).
+ * Requirements: every row's first prefix_blocks entries equal row 0's and
+ * every context length is > P (a row that breaks either gets NaN outputs and
+ * sets PKV_DEVICE_BAD_SHARED_PREFIX or PKV_DEVICE_BAD_LENGTH);
+ * 0 <= prefix_blocks <= max_blocks.  The shared-prefix pass covers head_dim
+ * 128 with 16-bit or E4M3 caches and softmax_scale > 0 under the tensor-core
+ * decode kernel; for other shapes, for prefix_blocks 0, or with
+ * PKV_KERNEL_SIMT the call is pkv_attention_decode.
+ *   workspace : pkv_shared_prefix_workspace_bytes(...) bytes, 256-byte
+ *               aligned, zero-filled before first use (left zeroed).
+ * The prefix pass is launched first, then the decode kernel as its
+ * programmatic dependent: the decode kernel starts on the SMs the pass leaves
+ * free and waits for the pass only where it merges. */
+PKV_API size_t pkv_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                                 int32_t max_blocks, const pkv_kv_desc* desc,
+                                                 int32_t prefix_blocks, int32_t partition_tokens);
+PKV_API pkv_status pkv_attention_decode_shared_prefix(
+    void* out, const void* q, int32_t q_dtype, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
+    int32_t num_seqs, int32_t num_q_heads, const pkv_kv_desc* desc, int32_t prefix_blocks,
+    float softmax_scale, float k_scale, float v_scale, int32_t partition_tokens, void* workspace,
+    size_t workspace_bytes, void* stream);
+
+/* pkv_decode_step over a shared prefix: the step's K/V written at position
+ * ctx_s - 1 (which is past the prefix), then
+ * pkv_attention_decode_shared_prefix; arguments as those two calls. */
+PKV_API pkv_status pkv_decode_step_shared_prefix(
+    void* out, const void* q, int32_t q_dtype, void* k_cache, void* v_cache, const void* k_new,
+    const void* v_new, const int32_t* block_tables, int32_t max_blocks,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, const pkv_kv_desc* desc,
+    int32_t prefix_blocks, float softmax_scale, float k_scale, float v_scale, float k_inv_scale,
+    float v_inv_scale, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+    void* stream);
+
+/* ------------------------------------------------------ device errors
+ * Invalid inputs that only the GPU sees (a table entry outside [0,
+ * num_blocks), a context length outside its range, a broken shared-prefix
+ * declaration) and bounded waits that gave up turn the affected outputs into
+ * NaN and set bits in one error word per device, which every attention
+ * kernel of the library ORs into (sticky until cleared). */
+#define PKV_DEVICE_BAD_LENGTH 1          /* a context / chunk length outside its range */
+#define PKV_DEVICE_BAD_TABLE 2           /* a block-table entry outside [0, num_blocks) */
+#define PKV_DEVICE_WAIT_TIMEOUT 4        /* a bounded wait for a copy or an MMA gave up */
+#define PKV_DEVICE_BAD_SHARED_PREFIX 8   /* a row does not map the declared shared prefix */
+
+/* Synchronise `stream` (NULL = legacy default stream), then *flags receives
+ * the current device's error word; clear != 0 then resets it to 0 (on that
+ * stream).  The first call on a device looks up the word's address; make it
+ * before any stream capture.  PKV_ERR_CUDA if a CUDA call fails. */
+PKV_API pkv_status pkv_device_status(int32_t* flags, int32_t clear, void* stream);
+
+/* Give-up limit, in nanoseconds, of the decode kernels' waits for a K/V stage
+ * (default 50,000,000 = 50 ms), process-wide; 0 makes every stage wait give
+ * up at once (used to exercise the failure path: the CTA still waits, with
+ * its own 10 ms limit per copy, for the copies it has in flight, then writes
+ * NaN and sets PKV_DEVICE_WAIT_TIMEOUT). */
+PKV_API pkv_status pkv_set_stage_wait_limit(uint64_t nanoseconds);
+
 /* Bytes of the fixed scratch array behind pkv_attention_decode_noalloc. */
 #define PKV_NOALLOC_SCRATCH_BYTES (16u << 20)
 
@@ -347,9 +433,10 @@ PKV_API pkv_status pkv_decode_step(void* out, const void* q, int32_t q_dtype, vo
  * The first call on a device, with that device current, looks up the array's
  * device address (cudaGetSymbolAddress) and caches it; make that first call
  * before any stream capture.  All calls on a device share the array: calls
- * that overlap on the GPU race.  Each call clears the array's split-K
- * counters on its stream before the kernel runs; nothing else needs
- * clearing between calls. */
+ * that overlap on the GPU race.  A completed call leaves the array's split-K
+ * counters at zero; each call also clears them on its stream before the
+ * kernel runs, so a call that never completed leaves nothing behind.
+ * Nothing else needs clearing between calls. */
 PKV_API pkv_status pkv_attention_decode_noalloc(void* out, const void* q, int32_t q_dtype,
                                                 const void* k_cache, const void* v_cache,
                                                 const int32_t* block_tables, int32_t max_blocks,

@@ -122,9 +122,20 @@ _SIGNATURES = {
     "pkv_seq_admit": (_I32, [_P, _I64, _I32, _I32, _PI64]),
     "pkv_decode_step": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC, _F, _F,
                                _F, _F, _F, _I32, _P, ctypes.c_size_t, _P]),
+    "pkv_shared_prefix_blocks": (_I32, [_P, _PI64, _I32, _PI32]),
+    "pkv_shared_prefix_workspace_bytes": (ctypes.c_size_t, [_I32, _I32, _I32, _PDESC, _I32, _I32]),
+    "pkv_attention_decode_shared_prefix": (_I32, [_P, _P, _I32, _P, _P, _P, _I32, _P, _I32, _I32, _PDESC,
+                                                  _I32, _F, _F, _F, _I32, _P, ctypes.c_size_t, _P]),
+    "pkv_decode_step_shared_prefix": (_I32, [_P, _P, _I32, _P, _P, _P, _P, _P, _I32, _P, _I32, _I32,
+                                             _PDESC, _I32, _F, _F, _F, _F, _F, _I32, _P,
+                                             ctypes.c_size_t, _P]),
+    "pkv_device_status": (_I32, [_PI32, _I32, _P]),
+    "pkv_set_stage_wait_limit": (_I32, [_U64]),
     "pkv_last_error": (ctypes.c_char_p, []),
 }
 NOALLOC_SCRATCH_BYTES = 16 << 20
+# device error bits (pkv_device_status)
+PKV_DEVICE_BAD_LENGTH, PKV_DEVICE_BAD_TABLE, PKV_DEVICE_WAIT_TIMEOUT, PKV_DEVICE_BAD_SHARED_PREFIX = 1, 2, 4, 8
 EXPORTED = tuple(_SIGNATURES)
 
 
@@ -364,6 +375,17 @@ class Pool:
         """Host buffers for pkv_block_tables_update, kept across decode steps
         (see BlockTableRows)."""
         return BlockTableRows(self, capacity, max_blocks, pin_memory)
+
+    def shared_prefix_blocks(self, seq_ids) -> int:
+        """Leading table entries every listed sequence maps to the same
+        physical blocks, short of each one's last position
+        (pkv_shared_prefix_blocks)."""
+        n = len(seq_ids)
+        ids, ids_p = self._buf("ids", n, np.int64)
+        ids[:n] = seq_ids
+        k = ctypes.c_int32(0)
+        _check(lib().pkv_shared_prefix_blocks(self._h, ids.ctypes.data_as(_PI64), n, ctypes.byref(k)))
+        return k.value
 
     def block_refcount(self, block: int) -> int:
         rc = ctypes.c_int32(0)
@@ -616,3 +638,81 @@ def pkv_attention_decode_noalloc(out, q, k_cache, v_cache, block_tables, context
         ctypes.byref(desc), float(softmax_scale), float(k_scale), float(v_scale),
         int(partition_tokens), _stream(stream)))
     return out
+
+
+def pkv_shared_prefix_workspace_bytes(num_seqs, num_q_heads, max_blocks, desc: pkv_kv_desc,
+                                      prefix_blocks, partition_tokens=0) -> int:
+    return int(lib().pkv_shared_prefix_workspace_bytes(num_seqs, num_q_heads, max_blocks,
+                                                       ctypes.byref(desc), int(prefix_blocks),
+                                                       partition_tokens))
+
+
+def shared_prefix_workspace_for(num_seqs, num_q_heads, max_blocks, desc, prefix_blocks,
+                                partition_tokens=0, device="cuda"):
+    """A zero-filled workspace for the shared-prefix decode calls (None if 0)."""
+    n = pkv_shared_prefix_workspace_bytes(num_seqs, num_q_heads, max_blocks, desc, prefix_blocks,
+                                          partition_tokens)
+    return torch.zeros(n, dtype=torch.uint8, device=device) if n else None
+
+
+def _ws(workspace):
+    if workspace is None:
+        return None, 0
+    return _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
+
+
+def pkv_attention_decode_shared_prefix(out, q, k_cache, v_cache, block_tables, context_lens,
+                                       desc: pkv_kv_desc, prefix_blocks, softmax_scale, k_scale=1.0,
+                                       v_scale=1.0, partition_tokens=0, workspace=None, stream=None):
+    """Decode attention whose first ``prefix_blocks`` table entries are the
+    same blocks in every row: the prefix is attended once for all sequences
+    (pkv_attention_decode_shared_prefix)."""
+    b, hq, d = q.shape
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    if block_tables.dim() != 2 or block_tables.shape[0] != b or context_lens.shape != (b,):
+        raise ValueError("block_tables int32[B, max_blocks], context_lens int32[B] expected")
+    ws_ptr, ws_bytes = _ws(workspace)
+    _check(lib().pkv_attention_decode_shared_prefix(
+        _dev(out, "out"), _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache", desc.torch_dtype),
+        _dev(v_cache, "v_cache", desc.torch_dtype), _dev(block_tables, "block_tables", torch.int32),
+        block_tables.shape[1], _dev(context_lens, "context_lens", torch.int32), b, hq,
+        ctypes.byref(desc), int(prefix_blocks), float(softmax_scale), float(k_scale), float(v_scale),
+        int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def pkv_decode_step_shared_prefix(out, q, k_cache, v_cache, k_new, v_new, block_tables,
+                                  context_lens, desc: pkv_kv_desc, prefix_blocks, softmax_scale,
+                                  k_scale=1.0, v_scale=1.0, k_inv_scale=1.0, v_inv_scale=1.0,
+                                  partition_tokens=0, workspace=None, stream=None):
+    """pkv_decode_step over a shared prefix (pkv_decode_step_shared_prefix)."""
+    b, hq, d = q.shape
+    if out.shape != q.shape or out.dtype != q.dtype:
+        raise ValueError("out must match q")
+    if k_new.shape != v_new.shape or k_new.shape[0] != b or k_new.dtype != q.dtype:
+        raise ValueError("k_new, v_new must be [B, N_kv, D] in q's dtype")
+    if block_tables.dim() != 2 or block_tables.shape[0] != b or context_lens.shape != (b,):
+        raise ValueError("block_tables int32[B, max_blocks], context_lens int32[B] expected")
+    ws_ptr, ws_bytes = _ws(workspace)
+    _check(lib().pkv_decode_step_shared_prefix(
+        _dev(out, "out"), _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache", desc.torch_dtype),
+        _dev(v_cache, "v_cache", desc.torch_dtype), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+        _dev(context_lens, "context_lens", torch.int32), b, hq, ctypes.byref(desc),
+        int(prefix_blocks), float(softmax_scale), float(k_scale), float(v_scale), float(k_inv_scale),
+        float(v_inv_scale), int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)))
+    return out
+
+
+def pkv_device_status(clear: bool = False, stream=None) -> int:
+    """The current device's error word (PKV_DEVICE_* bits), after
+    synchronising ``stream``; ``clear`` resets it."""
+    flags = ctypes.c_int32(0)
+    _check(lib().pkv_device_status(ctypes.byref(flags), 1 if clear else 0, _stream(stream)))
+    return flags.value
+
+
+def pkv_set_stage_wait_limit(nanoseconds: int) -> None:
+    """Give-up limit of the decode kernels' stage waits (default 50 ms)."""
+    _check(lib().pkv_set_stage_wait_limit(int(nanoseconds)))

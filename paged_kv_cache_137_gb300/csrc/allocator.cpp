@@ -613,6 +613,36 @@ pkv_status pkv_block_tables_update(const pkv_pool* pool, const int64_t* seq_ids,
   return PKV_OK;
 }
 
+pkv_status pkv_shared_prefix_blocks(const pkv_pool* pool, const int64_t* seq_ids, int32_t n_seqs,
+                                    int32_t* n_blocks) {
+  if (!pool || !n_blocks) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
+  if (n_seqs < 0) return fail(PKV_ERR_INVALID_ARG, "negative size");
+  if (n_seqs > 0 && !seq_ids) return fail(PKV_ERR_INVALID_ARG, "seq_ids is NULL");
+  std::vector<const pkv::Seq*> seqs(static_cast<size_t>(n_seqs));
+  for (int32_t i = 0; i < n_seqs; ++i) {
+    auto it = pool->seqs.find(seq_ids[i]);
+    if (it == pool->seqs.end()) {
+      pkv::set_error("unknown sequence %lld", (long long)seq_ids[i]);
+      return PKV_ERR_UNKNOWN_SEQ;
+    }
+    seqs[i] = &it->second;
+  }
+  int64_t k = 0;
+  if (n_seqs > 0) {
+    // full blocks before every sequence's last position
+    k = std::numeric_limits<int64_t>::max();
+    for (const pkv::Seq* s : seqs) k = std::min<int64_t>(k, s->len > 0 ? (s->len - 1) / pool->block_size : 0);
+    const std::vector<int32_t>& t0 = seqs[0]->table;
+    for (const pkv::Seq* s : seqs) {
+      int64_t i = 0;
+      while (i < k && s->table[i] == t0[i]) ++i;
+      k = i;
+    }
+  }
+  *n_blocks = static_cast<int32_t>(std::min<int64_t>(k, std::numeric_limits<int32_t>::max()));
+  return PKV_OK;
+}
+
 pkv_status pkv_block_refcount(const pkv_pool* pool, int32_t block, int32_t* refcount) {
   if (!pool || !refcount) return fail(PKV_ERR_INVALID_ARG, "NULL argument");
   if (block < 0 || block >= pool->num_blocks) return fail(PKV_ERR_INVALID_ARG, "block out of range");

@@ -130,6 +130,9 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
         L = fmaf(a.ws_l[base + i], f, L);
         A = fmaf(a.ws_acc[(base + i) * D + d], f, A);
       }
+    } else {
+      // no split attended a position: 0, or NaN from a split that failed
+      for (int i = 0; i < nsplit; ++i) L += a.ws_l[base + i];
     }
     const float o = (L > 0.f || L != L) ? A / L : 0.f;
     store_elem<Q>(a.out, (static_cast<size_t>(seq) * a.num_q_heads + qh) * D + d, o);
@@ -144,8 +147,10 @@ pkv_status launch_merge(const DecodeArgs& a, int head_dim, cudaStream_t st) {
   return check_launch("pkv_attention_decode (merge)");
 }
 
+// prefix_tokens: positions a shared-prefix pass covers (the decode kernel
+// splits only the rest of each context).
 pkv_status resolve_partition(int32_t requested, int32_t num_seqs, int32_t max_blocks,
-                             const pkv_kv_desc* d, int32_t* out) {
+                             const pkv_kv_desc* d, int32_t* out, int64_t prefix_tokens = 0) {
   if (requested < 0) return fail(PKV_ERR_INVALID_ARG, "partition_tokens is negative");
   if (requested > 0) {
     if (requested % 64 != 0 || requested % d->block_size != 0)
@@ -153,14 +158,45 @@ pkv_status resolve_partition(int32_t requested, int32_t num_seqs, int32_t max_bl
     *out = requested;
     return PKV_OK;
   }
-  *out = auto_partition(num_seqs, d->num_kv_heads, static_cast<int64_t>(max_blocks) * d->block_size,
+  *out = auto_partition(num_seqs, d->num_kv_heads,
+                        static_cast<int64_t>(max_blocks) * d->block_size - prefix_tokens,
                         d->block_size, resident_split_ctas(d));
   return PKV_OK;
 }
 
-int64_t num_splits(int32_t max_blocks, int32_t block_size, int32_t partition) {
-  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * block_size;
+int64_t num_splits(int32_t max_blocks, int32_t block_size, int32_t partition,
+                   int64_t prefix_tokens = 0) {
+  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * block_size - prefix_tokens;
   return std::max<int64_t>(1, (max_ctx + partition - 1) / partition);
+}
+
+// Shared-prefix pass geometry: the key ranges of the P prefix positions.
+// Each of the n_kv * ceil(rows / 256) row units gets enough ranges that the
+// pass has about one CTA per SM (it holds a whole SM); ranges are whole
+// 64-key tiles.
+struct PrefixPlan {
+  int32_t tokens = 0, key_splits = 0, split_tokens = 0;
+};
+PrefixPlan prefix_plan(int64_t num_seqs, int64_t group, int64_t num_kv_heads, int64_t prefix_tokens) {
+  PrefixPlan p;
+  if (prefix_tokens <= 0) return p;
+  const int64_t units = (num_seqs * group + 255) / 256 * num_kv_heads;
+  const int64_t tiles = (prefix_tokens + 63) / 64;
+  const int64_t want = std::max<int64_t>(1, std::min<int64_t>(tiles, device_sms() / std::max<int64_t>(units, 1)));
+  const int64_t per = (tiles + want - 1) / want;
+  p.tokens = static_cast<int32_t>(prefix_tokens);
+  p.split_tokens = static_cast<int32_t>(per * 64);
+  p.key_splits = static_cast<int32_t>((tiles + per - 1) / per);
+  return p;
+}
+
+// Whether the shared-prefix pass covers this call (else the prefix is read
+// per sequence by the plain decode path).
+bool prefix_pass_covers(const pkv_kv_desc* d, int q_dtype, float softmax_scale) {
+  if (d->head_dim != 128 || !(softmax_scale > 0.f)) return false;
+  if (d->kv_dtype == PKV_BF16) return q_dtype == PKV_BF16;
+  if (d->kv_dtype == PKV_F16) return q_dtype == PKV_F16;
+  return d->kv_dtype == PKV_E4M3 && (q_dtype == PKV_F16 || q_dtype == PKV_BF16);
 }
 
 }  // namespace
@@ -266,11 +302,13 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
                        const pkv_kv_desc* desc, float softmax_scale, float k_scale, float v_scale,
                        int32_t partition_tokens, void* workspace, size_t workspace_bytes,
                        void* stream, const void* k_new, const void* v_new, float k_inv,
-                       float v_inv) {
+                       float v_inv, int32_t prefix_blocks = 0) {
   pkv_status st = check_desc(desc);
   if (st != PKV_OK) return st;
   if (num_seqs < 0 || num_q_heads <= 0 || max_blocks < 0)
     return fail(PKV_ERR_INVALID_ARG, "negative size or no query heads");
+  if (prefix_blocks < 0 || prefix_blocks > max_blocks)
+    return fail(PKV_ERR_INVALID_ARG, "prefix_blocks outside [0, max_blocks]");
   if (num_seqs == 0) return PKV_OK;
   if (num_seqs > 65535) return fail(PKV_ERR_UNSUPPORTED, "more than 65535 sequences per call");
   if (max_blocks == 0) return fail(PKV_ERR_INVALID_ARG, "max_blocks is 0");
@@ -297,20 +335,35 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   int gm = 1;
   while (gm < group) gm = gm == 1 ? 4 : gm * 2;
   if (gm > 16) return fail(PKV_ERR_UNSUPPORTED, "more than 16 query heads per KV head");
-
-  int32_t partition = 0;
-  st = resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &partition);
-  if (st != PKV_OK) return st;
-  const int64_t splits = num_splits(max_blocks, desc->block_size, partition);
-  if (splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits");
   const int choice = g_kernel_choice.load();
+  if (static_cast<int64_t>(desc->num_blocks) * desc->num_kv_heads * desc->block_size > INT32_MAX &&
+      prefix_blocks > 0)
+    prefix_blocks = 0;  // the pass's TMA rows are int
+
+  // A declared shared prefix runs the prefix pass where it covers the shape
+  // under the tensor-core decode kernel; otherwise the prefix is read per
+  // sequence like the rest of the context (same attention).
+  const bool prefix_pass = prefix_blocks > 0 && choice != PKV_KERNEL_SIMT &&
+                           prefix_pass_covers(desc, q_dtype, softmax_scale) &&
+                           tc_supported(desc, q_dtype, group, 64);
+  const PrefixPlan pp = prefix_pass
+                            ? prefix_plan(num_seqs, group, desc->num_kv_heads,
+                                          static_cast<int64_t>(prefix_blocks) * desc->block_size)
+                            : PrefixPlan{};
+  int32_t partition = 0;
+  st = resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &partition, pp.tokens);
+  if (st != PKV_OK) return st;
+  const int64_t splits = num_splits(max_blocks, desc->block_size, partition, pp.tokens) + pp.key_splits;
+  if (splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits");
   const WsLayout ws = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, splits,
                                        desc->head_dim);
   if (ws.bytes > 0) {
     if (!workspace || workspace_bytes < ws.bytes)
-      return fail(PKV_ERR_INVALID_ARG, "workspace missing or smaller than pkv_attention_workspace_bytes");
+      return fail(PKV_ERR_INVALID_ARG, "workspace missing or smaller than the workspace size call");
     if (!aligned(workspace, 256)) return fail(PKV_ERR_INVALID_ARG, "workspace must be 256-byte aligned");
   }
+  int* status = device_status_word(&st);
+  if (!status) return st;
 
   DecodeArgs a{};
   a.out = out;
@@ -338,12 +391,18 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   a.v_scale = fp8 ? v_scale : 1.0f;
   a.head_scales = desc->head_scales;
   a.softmax_scale = softmax_scale;
+  a.prefix_tokens = pp.tokens;
+  a.prefix_splits = pp.key_splits;
+  a.status = status;
+  a.wait_ns = stage_wait_limit_ns();
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim;
   const bool tc_ok = tc_supported(desc, q_dtype, group, partition);
   if (choice == PKV_KERNEL_TENSOR_CORE && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED, "the tensor-core kernel does not cover these sizes");
+  if (prefix_pass && !tc_ok)
+    return fail(PKV_ERR_UNSUPPORTED, "partition too long for the tensor-core kernel");
   if (k_new) {
     if (tc_ok && choice != PKV_KERNEL_SIMT) {
       a.k_new = k_new;  // fused into the split kernel
@@ -356,6 +415,46 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
                              num_seqs, desc, s);
       if (st != PKV_OK) return st;
     }
+  }
+  if (prefix_pass) {
+    // the prefix pass first: its CTAs let the decode kernel start once they
+    // have all begun; the decode kernel reads their partials after its wait
+    PrefillArgs pa{};
+    pa.q = q;
+    pa.tables = block_tables;
+    pa.max_blocks = max_blocks;
+    pa.num_seqs = num_seqs;
+    pa.total_q = num_seqs * group;
+    pa.num_q_heads = num_q_heads;
+    pa.num_kv_heads = desc->num_kv_heads;
+    pa.group = group;
+    pa.num_blocks = desc->num_blocks;
+    pa.qk_scale = a.qk_scale;
+    pa.v_scale = a.v_scale;
+    pa.head_scales = desc->head_scales;
+    pa.softmax_scale = softmax_scale;
+    pa.status = status;
+    pa.sp_rows = num_seqs * group;
+    pa.sp_tokens = pp.tokens;
+    pa.sp_split = pp.split_tokens;
+    pa.sp_slot0 = static_cast<int32_t>(splits) - pp.key_splits;
+    pa.max_splits = static_cast<int32_t>(splits);
+    pa.ws_m = a.ws_m;
+    pa.ws_l = a.ws_l;
+    pa.ws_acc = a.ws_acc;
+    CUtensorMap pkmap, pvmap;
+    st = pool_map(&pkmap, k_cache, desc, false);
+    if (st == PKV_OK) st = pool_map(&pvmap, v_cache, desc, false);
+    if (st != PKV_OK) return st;
+    const int T = desc->block_size;
+    switch (kv) {
+      case PKV_F16: st = launch_shared_prefix_pass<F16, F16>(pa, T, pp.key_splits, pkmap, pvmap, s); break;
+      case PKV_BF16: st = launch_shared_prefix_pass<BF16, BF16>(pa, T, pp.key_splits, pkmap, pvmap, s); break;
+      default:
+        st = q_dtype == PKV_F16 ? launch_shared_prefix_pass<E4M3, F16>(pa, T, pp.key_splits, pkmap, pvmap, s)
+                                : launch_shared_prefix_pass<E4M3, BF16>(pa, T, pp.key_splits, pkmap, pvmap, s);
+    }
+    if (st != PKV_OK) return st;
   }
   if (tc_ok && choice != PKV_KERNEL_SIMT) {
     CUtensorMap kmap, vmap;
@@ -417,4 +516,47 @@ extern "C" pkv_status pkv_decode_step(void* out, const void* q, int32_t q_dtype,
   return decode_impl(out, q, q_dtype, k_cache, v_cache, block_tables, max_blocks, context_lens,
                      num_seqs, num_q_heads, desc, softmax_scale, k_scale, v_scale, partition_tokens,
                      workspace, workspace_bytes, stream, k_new, v_new, k_inv_scale, v_inv_scale);
+}
+
+extern "C" size_t pkv_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
+                                                    int32_t max_blocks, const pkv_kv_desc* desc,
+                                                    int32_t prefix_blocks, int32_t partition_tokens) {
+  if (check_desc(desc) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 || max_blocks <= 0) return 0;
+  if (prefix_blocks < 0 || prefix_blocks > max_blocks || num_q_heads % desc->num_kv_heads != 0) return 0;
+  // the size the prefix pass needs; calls that run without it need less
+  const PrefixPlan pp = prefix_plan(num_seqs, num_q_heads / desc->num_kv_heads, desc->num_kv_heads,
+                                    static_cast<int64_t>(prefix_blocks) * desc->block_size);
+  int32_t p = 0;
+  if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p, pp.tokens) != PKV_OK) return 0;
+  const int64_t s = num_splits(max_blocks, desc->block_size, p, pp.tokens) + pp.key_splits;
+  const size_t with = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim).bytes;
+  return std::max(with, pkv_attention_workspace_bytes(num_seqs, num_q_heads, max_blocks, desc,
+                                                      partition_tokens));
+}
+
+extern "C" pkv_status pkv_attention_decode_shared_prefix(
+    void* out, const void* q, int32_t q_dtype, const void* k_cache, const void* v_cache,
+    const int32_t* block_tables, int32_t max_blocks, const int32_t* context_lens,
+    int32_t num_seqs, int32_t num_q_heads, const pkv_kv_desc* desc, int32_t prefix_blocks,
+    float softmax_scale, float k_scale, float v_scale, int32_t partition_tokens, void* workspace,
+    size_t workspace_bytes, void* stream) {
+  return decode_impl(out, q, q_dtype, k_cache, v_cache, block_tables, max_blocks, context_lens,
+                     num_seqs, num_q_heads, desc, softmax_scale, k_scale, v_scale, partition_tokens,
+                     workspace, workspace_bytes, stream, nullptr, nullptr, 1.0f, 1.0f, prefix_blocks);
+}
+
+extern "C" pkv_status pkv_decode_step_shared_prefix(
+    void* out, const void* q, int32_t q_dtype, void* k_cache, void* v_cache, const void* k_new,
+    const void* v_new, const int32_t* block_tables, int32_t max_blocks,
+    const int32_t* context_lens, int32_t num_seqs, int32_t num_q_heads, const pkv_kv_desc* desc,
+    int32_t prefix_blocks, float softmax_scale, float k_scale, float v_scale, float k_inv_scale,
+    float v_inv_scale, int32_t partition_tokens, void* workspace, size_t workspace_bytes,
+    void* stream) {
+  if (num_seqs > 0 && (!k_new || !v_new)) return fail(PKV_ERR_INVALID_ARG, "k_new or v_new is NULL");
+  if (!aligned(k_new, 16) || !aligned(v_new, 16))
+    return fail(PKV_ERR_INVALID_ARG, "k_new and v_new must be 16-byte aligned");
+  return decode_impl(out, q, q_dtype, k_cache, v_cache, block_tables, max_blocks, context_lens,
+                     num_seqs, num_q_heads, desc, softmax_scale, k_scale, v_scale, partition_tokens,
+                     workspace, workspace_bytes, stream, k_new, v_new, k_inv_scale, v_inv_scale,
+                     prefix_blocks);
 }

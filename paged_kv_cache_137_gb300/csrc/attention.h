@@ -38,7 +38,56 @@ struct DecodeArgs {
   // NULL; when set they replace qk_scale's k_scale, v_scale, k_inv, v_inv
   const float* head_scales;
   float softmax_scale;
+  // shared prefix (0: none): positions [0, prefix_tokens) of every sequence
+  // were attended by the shared-prefix pass, whose prefix_splits partials
+  // sit in the last prefix_splits of the max_splits slots; this kernel
+  // covers [prefix_tokens, ctx) and merges everything
+  int32_t prefix_tokens, prefix_splits;
+  int* status;               // device error word (PKV_DEVICE_* bits, atomicOr)
+  uint64_t wait_ns;          // give-up limit of a stage wait; 0 = give up at once
 };
+
+// Prefill / shared-prefix pass arguments (attention_prefill.cu,
+// attention_prefill_umma.cuh).
+struct PrefillArgs {
+  void* out;                  // [total_q][Hq][D]
+  const void* q;              // [total_q][Hq][D]
+  const int32_t* tables;      // [B][max_blocks]
+  const int32_t* ctx_lens;    // [B], chunk included
+  const int32_t* query_start; // [B + 1] row offsets of the chunks in q / out
+  int32_t max_blocks, num_seqs, total_q, max_q_tiles, num_q_heads, num_kv_heads, group,
+      num_blocks;
+  float qk_scale;             // softmax_scale * log2(e) (* k_scale for E4M3)
+  float v_scale;              // 1, or the E4M3 V scale
+  const float* head_scales;   // E4M3 per-KV-head scales [4][N_kv], or NULL (replace the two above)
+  float softmax_scale;
+  int32_t ranked;             // tcgen05 kernel: grid (head, unit rank), units ranked longest first
+  int* status;                // device error word
+  // shared-prefix pass (grid (row pair, key split, KV head)): the query rows
+  // of a KV head are its (sequence, head) pairs, row r = s * group + j; the
+  // keys are positions [k * sp_split, min(sp_tokens, (k + 1) * sp_split)) of
+  // table row 0; row r's partial (max, sum, unnormalised output) goes to
+  // split slot sp_slot0 + k of the decode workspace (ws_*, max_splits slots)
+  int32_t sp_rows, sp_tokens, sp_split, sp_slot0, max_splits;
+  float* ws_m;
+  float* ws_l;
+  float* ws_acc;
+};
+
+// Device error word of the current device (looked up once per device);
+// nullptr with *st set when a CUDA call fails.  Defined in status.cu.
+int* device_status_word(pkv_status* st);
+
+// Give-up limit of the decode kernels' stage waits (pkv_set_stage_wait_limit).
+uint64_t stage_wait_limit_ns();
+
+// Launch the shared-prefix pass (tcgen05, head_dim 128) for one (cache, q)
+// dtype pair; grid (row pairs, key splits, KV heads).  Defined in
+// attention_shared_prefix.cu.
+template <typename KV, typename Q>
+pkv_status launch_shared_prefix_pass(const PrefillArgs& a, int block_size, int key_splits,
+                                     const CUtensorMap& kmap, const CUtensorMap& vmap,
+                                     cudaStream_t st);
 
 // Bytes at the start of a decode workspace that hold the split-K arrival
 // counters (they must be zero when a call starts; every call leaves them

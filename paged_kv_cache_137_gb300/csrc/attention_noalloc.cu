@@ -20,10 +20,16 @@
 //
 // Every call on a device shares the one array, which keeps whatever the last
 // call left in it.  Only the split-K arrival counters at its start must be
-// zero when a call begins; each call clears them on its stream before the
-// decode kernel runs (a memset, not an allocation).  Every other scratch
-// value is written before it is read within the same call.  Calls that
-// overlap on the GPU (two streams at once) race on the array.
+// zero when a call begins.  A call that runs to completion leaves them zero
+// (the CTA that merges a sequence's splits resets its counter, also after a
+// wait gave up); each call still clears them on its stream before the
+// decode kernel runs (a memset, not an allocation), so that a call that never
+// completed (its process or context torn down mid-kernel) cannot leave a
+// count behind for the next one.  Every other scratch value is written before
+// it is read within the same call.  Calls that overlap on the GPU (two
+// streams at once) race on the array.  The array's address is looked up once
+// per device and kept: cudaDeviceReset while the library is loaded is not
+// supported.
 #include <mutex>
 
 #include "attention.h"

@@ -53,20 +53,6 @@ __device__ __forceinline__ uint32_t swz_slab(int r, int c) {
 
 }  // namespace
 
-struct PrefillArgs {
-  void* out;                  // [total_q][Hq][D]
-  const void* q;              // [total_q][Hq][D]
-  const int32_t* tables;      // [B][max_blocks]
-  const int32_t* ctx_lens;    // [B], chunk included
-  const int32_t* query_start; // [B + 1] row offsets of the chunks in q / out
-  int32_t max_blocks, num_seqs, total_q, max_q_tiles, num_q_heads, num_kv_heads, group,
-      num_blocks;
-  float qk_scale;             // softmax_scale * log2(e) (* k_scale for E4M3)
-  float v_scale;              // 1, or the E4M3 V scale
-  const float* head_scales;   // E4M3 per-KV-head scales [4][N_kv], or NULL (replace the two above)
-  float softmax_scale;
-  int32_t ranked;             // tcgen05 kernel: grid (head, unit rank), units ranked longest first
-};
 
 template <typename KV, typename Q, int D, int T, int NS>
 __global__ void __launch_bounds__(kThreads, 2)
@@ -100,6 +86,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   const bool bad = ctx < 0 || ctx > a.max_blocks * T || n > ctx ||
                    (n + kTile - 1) / kTile > a.max_q_tiles;
   if (bad) {  // invalid lengths: the chunk's rows of head j become NaN
+    if (tid == 0 && a.status != nullptr) atomicOr(a.status, kBadLength);
     if (qt_rev == 0)
       for (int i = tid; i < n * D; i += kThreads)
         store_elem<Q>(a.out, (static_cast<size_t>(q0 + i / D) * HQ + j) * D + i % D,
@@ -122,7 +109,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t* ring = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(ring + NS * G_::kStageBytes);
-  __shared__ int s_bad;
+  __shared__ int s_bad;  // PKV_DEVICE_* bits, written by thread 0 only
   if (tid == 0) {
     s_bad = 0;
     for (int i = 0; i < NS; ++i) mbar_init(smem_u32(&s_bar[i]), 1);
@@ -145,7 +132,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     const unsigned badmask = __ballot_sync(FULL, id == kBadBox);
     const uint32_t bar = smem_u32(&s_bar[slot]);
     if (lane == 0) {
-      if (badmask) s_bad = 1;
+      if (badmask) s_bad |= kBadTable;
       mbar_arrive_expect_tx(bar, __popc(okmask) * static_cast<uint32_t>(kBoxBytes));
     }
     __syncwarp();
@@ -345,12 +332,13 @@ __global__ void __launch_bounds__(kThreads, 2)
 
   if (timed_out && tid == 0) {
     // wait (bounded) for the copies still in flight before the CTA exits
-    s_bad = 1;
+    s_bad |= kTimeout;
     for (int t = stalled_at; t < n_kv_tiles && t < stalled_at + NS; ++t)
       mbar_wait(smem_u32(&s_bar[t % NS]), (t / NS) & 1, kDrainNs);
   }
   __syncthreads();
   const bool any_bad = s_bad != 0;
+  if (tid == 0 && any_bad && a.status != nullptr) atomicOr(a.status, s_bad);
 
   // ---------------------------------------------------------- epilogue
 #pragma unroll
@@ -521,7 +509,7 @@ extern "C" pkv_status pkv_attention_prefill(void* out, const void* q, int32_t q_
   const int64_t q_tiles = (static_cast<int64_t>(max_query_len) + 63) / 64;
   if (q_tiles > 65535) return fail(PKV_ERR_UNSUPPORTED, "max_query_len too large");
 
-  tc::PrefillArgs a{};
+  PrefillArgs a{};
   a.out = out;
   a.q = q;
   a.tables = block_tables;

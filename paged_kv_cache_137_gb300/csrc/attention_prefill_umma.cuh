@@ -41,6 +41,28 @@
 //  * Every mbarrier wait is bounded; a CTA whose wait gives up writes NaN
 //    rows, waits (bounded) for its copies and MMAs in flight, and frees its
 //    TMEM before it exits.
+//
+// Shared-prefix pass (kCasc): the same pipeline computes, for one KV head,
+// the attention of every (sequence, query head) row of a decode batch (row
+// r = s * G + j, M = num_seqs * G rows, two 128-row tiles per CTA) over one
+// key range of the positions [0, P) that all sequences share, read through
+// table row 0 (the katajob Q&A, "Sharing, the second dividend": sequences
+// that share a prompt list the same physical blocks; "PagedAttention Memory
+// Management", "Complex Topologies and Memory Sharing").  Nothing is masked
+// but the end of the range, and each row leaves its partial result (running
+// maximum, sum, unnormalised output times the V scale) in a split slot of the
+// decode workspace, where the decode kernel merges it with the rest of the
+// sequence's context.  The CTAs let the decode kernel launch as soon as they
+// have all started (griddepcontrol.launch_dependents after their own wait).
+#pragma once
+
+#include <math_constants.h>
+
+#include <type_traits>
+
+#include "attention.h"
+#include "attention_tc.cuh"
+#include "device_common.cuh"
 
 namespace pkv {
 namespace tc {
@@ -317,7 +339,7 @@ constexpr int threads() {
   return std::is_same<KV, E4M3>::value ? kThreadsU + 64 : kThreadsU;  // + two converter warps
 }
 
-template <typename KV, typename Q, int T>
+template <typename KV, typename Q, int T, bool kCasc = false>
 __global__ void __launch_bounds__(threads<KV>(), 1)
     prefill_umma_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap kmap,
                         const __grid_constant__ CUtensorMap vmap) {
@@ -333,15 +355,24 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   constexpr int kNT = threads<KV>();
 
   asm volatile("griddepcontrol.wait;" ::: "memory");
+  // the shared-prefix pass: the decode kernel behind it may start now (it
+  // reads this grid's partials only after its own wait)
+  if constexpr (kCasc) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   // grid: (query head, unit rank) with the units ranked longest first, or
-  // (pair counted from the chunk's end, query head, sequence)
+  // (pair counted from the chunk's end, query head, sequence); shared-prefix
+  // pass: (row pair, key range, KV head)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  int j, s, qp_rev;
-  if (a.ranked) {
+  int j, s, qp_rev, kbeg = 0;
+  if constexpr (kCasc) {
+    j = blockIdx.z * a.group;   // first query head of the KV head
+    s = 0;                      // the shared blocks are read through table row 0
+    qp_rev = -1 - static_cast<int>(blockIdx.x);
+    kbeg = blockIdx.y * a.sp_split;
+  } else if (a.ranked) {
     int pair = 0;
     j = blockIdx.x;
     s = ranked_unit<T>(a, blockIdx.y, reinterpret_cast<int*>(smem), &pair);
@@ -353,14 +384,16 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
     s = blockIdx.z;
   }
   const int HQ = a.num_q_heads;
-  const int ctx = a.ctx_lens[s];
-  const int q0 = a.query_start[s];
-  const int n = a.query_start[s + 1] - q0;
+  // keys: positions [kbeg, ctx) (prefill: 0 .. ctx - 1, causal)
+  const int ctx = kCasc ? min(a.sp_tokens, kbeg + a.sp_split) : a.ctx_lens[s];
+  const int q0 = kCasc ? 0 : a.query_start[s];
+  const int n = kCasc ? a.sp_rows : a.query_start[s + 1] - q0;
   if (q0 < 0 || n <= 0 || q0 + n > a.total_q) return;  // no rows this CTA may write
   const int ntq = (n + kRows - 1) / kRows;       // query tiles of the chunk
   const int npairs = (ntq + 1) / 2;
-  const bool bad_len = ctx < 0 || ctx > a.max_blocks * T || n > ctx || npairs > a.max_q_tiles;
+  const bool bad_len = !kCasc && (ctx < 0 || ctx > a.max_blocks * T || n > ctx || npairs > a.max_q_tiles);
   if (bad_len) {  // invalid lengths: the chunk's rows of head j become NaN
+    if (tid == 0 && a.status != nullptr) atomicOr(a.status, kBadLength);
     if (qp_rev == 0 || qp_rev == -1)
       for (int i = tid; i < n * D; i += kNT)
         store_elem<Q>(a.out, (static_cast<size_t>(q0 + i / D) * HQ + j) * D + i % D, CUDART_NAN_F);
@@ -368,6 +401,7 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   }
   if (qp_rev >= npairs) return;
   const int qp = qp_rev < 0 ? -1 - qp_rev : npairs - 1 - qp_rev;
+  if (qp >= npairs || ctx <= kbeg) return;
   const int first = ctx - n;                      // position of the chunk's first query
   // query tile X (0 = A, 1 = B): chunk rows r_begin[X] .. r_end[X] - 1
   const bool hasB = 2 * qp + 1 < ntq;
@@ -376,7 +410,9 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   for (int X = 0; X < 2; ++X) {
     r_begin[X] = (2 * qp + X) * kRows;
     r_end[X] = min(r_begin[X] + kRows, n);
-    nt[X] = (X == 1 && !hasB) ? 0 : (first + r_end[X] + kKeys - 1) / kKeys;  // key tiles
+    nt[X] = (X == 1 && !hasB) ? 0
+            : kCasc ? (ctx - kbeg + kKeys - 1) / kKeys      // key tiles
+                    : (first + r_end[X] + kKeys - 1) / kKeys;
   }
   const int n_tiles = max(nt[0], nt[1]);
   const int kvh = j / a.group;
@@ -399,10 +435,12 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   uint64_t* conv_full = fin + 1;         // E4M3: [2] widened buffer ready
   uint64_t* wide_free = conv_full + 2;   // E4M3: [2] every UMMA reading the widened buffer done
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wide_free + 2);
-  __shared__ int s_bad;
+  __shared__ int s_bad;      // PKV_DEVICE_* bits (atomicOr: several warps may set them)
+  __shared__ int s_issued;   // key tiles the producer has issued
 
   if (tid == 0) {
     s_bad = 0;
+    s_issued = 0;
     for (int i = 0; i < kNS; ++i) {
       mbar_init(smem_u32(&full[i]), 1);
       mbar_init(smem_u32(&empty[i]), kFp8 ? 2 : 1);  // E4M3: both converter warps
@@ -431,8 +469,12 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
     const int X = warp >> 2, r = tid & 127;
     const int cr = r_begin[X] + r;
     const bool in = cr < n && (X == 0 || hasB);
+    // query row: chunk row cr of head j, or (shared-prefix pass) head
+    // j + cr % G of sequence cr / G
+    const size_t qrow = kCasc ? static_cast<size_t>(cr / a.group) * HQ + j + cr % a.group
+                              : static_cast<size_t>(q0 + cr) * HQ + j;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const typename Q::raw*>(a.q) +
-                                                      (static_cast<size_t>(q0 + cr) * HQ + j) * D);
+                                                      qrow * D);
     uint8_t* qx = q_s + X * kQBytes;
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
@@ -458,18 +500,18 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
       for (int t = 0; t < n_tiles; ++t) {
         const int slot = t % kNS;
         if (t >= kNS && !mbar_wait(smem_u32(&empty[slot]), ((t / kNS) - 1) & 1, kWaitNs)) {
-          s_bad = 1;
+          atomicOr(&s_bad, kTimeout);
           break;
         }
         uint8_t* st = ring + slot * (kFp8 ? kStage8Bytes : kStageBytes);
         int ids[BPT];
         int nbox = 0;
         for (int b = 0; b < BPT; ++b) {
-          const int lb = (t * kKeys) / T + b;
+          const int lb = (kbeg + t * kKeys) / T + b;
           ids[b] = -1;
           if (lb * T < ctx) {
             const int id = a.tables[static_cast<size_t>(s) * a.max_blocks + lb];
-            if (id < 0 || id >= a.num_blocks) s_bad = 1;
+            if (id < 0 || id >= a.num_blocks) atomicOr(&s_bad, kBadTable);
             else {
               ids[b] = id;
               ++nbox;
@@ -488,6 +530,7 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
             tma_load_2d(smem_u32(st + vo + sl * kSlab + b * T * 128), &vmap, sl * 128, row, bar);
           }
         }
+        s_issued = t + 1;
       }
     }
   } else if (warp == kMma) {
@@ -549,7 +592,7 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
         for (int X = 0; X < 2 && ok; ++X)
           if (t + 2 < nt[X]) ok = qk(X, t + 2);
       }
-      if (!ok) s_bad = 1;
+      if (!ok) atomicOr(&s_bad, kTimeout);
       umma_commit(smem_u32(fin));
     }
   } else if (kFp8 && warp >= kConv) {
@@ -566,12 +609,12 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
       const bool ready = mbar_wait(smem_u32(&full[slot]), (t / kStages8) & 1, kWaitNs) &&
                          (t < 2 || mbar_wait(smem_u32(&wide_free[w]), ((t >> 1) - 1) & 1, kWaitNs));
       if (!__all_sync(FULL, ready)) {
-        if (lane == 0) s_bad = 1;
+        if (lane == 0) atomicOr(&s_bad, kTimeout);
         break;
       }
       const uint8_t* src = ring + slot * kStage8Bytes;
       uint8_t* dst = wide + w * kStageBytes;
-      const int kb = t * kKeys;
+      const int kb = kbeg + t * kKeys;
 #pragma unroll 4
       for (int k = 0; k < 16; ++k) {
         const int q = lane + 32 * k;               // 16-byte chunk: row, column
@@ -638,8 +681,8 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
       // raw scores in eight independent chains, scaled once (the scale is
       // positive, so it commutes with the maximum); the exponent below takes
       // s * scale - m as one fused multiply-add
-      const int kb = t * kKeys;
-      const int lim = min(pos, ctx - 1) - kb;   // keys kb + e with e <= lim are attended
+      const int kb = kbeg + t * kKeys;
+      const int lim = (kCasc ? ctx - 1 : min(pos, ctx - 1)) - kb;   // keys kb + e, e <= lim, attended
       float mx8[8];
 #pragma unroll
       for (int k = 0; k < 8; ++k) mx8[k] = -CUDART_INF_F;
@@ -713,29 +756,54 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
       tc_fence_before();
       mbar_arrive(smem_u32(&p_full[i]));
     }
-    // epilogue: O / l of the row, after the tile's last P V
+    // epilogue: O / l of the row, after the tile's last P V (shared-prefix
+    // pass: the row's partial m_ref, l and O times the V scale)
     if (ntx > 0) {
       const int tl = ntx - 1;
       ok = __all_sync(FULL, ok && mbar_wait(smem_u32(&o_done[2 * X + (tl & 1)]), (tl >> 1) & 1, kWaitNs));
       tc_fence_after();
-      if (!ok) s_bad = 1;
+      if (!ok) atomicOr(&s_bad, kTimeout);
       const bool bad = !ok || *reinterpret_cast<volatile int*>(&s_bad) != 0;
-      const float inv = (l > 0.f || l != l) ? hs.v / l : 0.f;
-      typename Q::raw* dst =
-          static_cast<typename Q::raw*>(a.out) + (static_cast<size_t>(q0 + cr) * HQ + j) * D;
+      const bool row_in = cr < r_end[X];
+      if constexpr (kCasc) {
+        const size_t pidx = (static_cast<size_t>(cr / a.group) * HQ + j + cr % a.group) * a.max_splits +
+                            a.sp_slot0 + blockIdx.y;
+        float* acc = a.ws_acc + pidx * D;
 #pragma unroll 1
-      for (int c = 0; c < D; c += 32) {
-        float o[32];
-        tmem_ld32(tO + lane_off + c, o);
-        if (cr < r_end[X]) {
-          uint32_t w[16];
+        for (int c = 0; c < D; c += 32) {
+          float o[32];
+          tmem_ld32(tO + lane_off + c, o);
+          if (row_in) {
+            float4* d4 = reinterpret_cast<float4*>(acc + c);
 #pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack2<kOutBf>(bad ? CUDART_NAN_F : o[2 * e] * inv,
-                                 bad ? CUDART_NAN_F : o[2 * e + 1] * inv);
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+            for (int e = 0; e < 8; ++e)
+              d4[e] = bad ? make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F)
+                          : make_float4(o[4 * e] * hs.v, o[4 * e + 1] * hs.v, o[4 * e + 2] * hs.v,
+                                        o[4 * e + 3] * hs.v);
+          }
+        }
+        if (row_in) {
+          a.ws_m[pidx] = m_ref;
+          a.ws_l[pidx] = bad ? CUDART_NAN_F : l;
+        }
+      } else {
+        const float inv = (l > 0.f || l != l) ? hs.v / l : 0.f;
+        typename Q::raw* dst =
+            static_cast<typename Q::raw*>(a.out) + (static_cast<size_t>(q0 + cr) * HQ + j) * D;
+#pragma unroll 1
+        for (int c = 0; c < D; c += 32) {
+          float o[32];
+          tmem_ld32(tO + lane_off + c, o);
+          if (row_in) {
+            uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+            for (int e = 0; e < 16; ++e)
+              w[e] = pack2<kOutBf>(bad ? CUDART_NAN_F : o[2 * e] * inv,
+                                   bad ? CUDART_NAN_F : o[2 * e + 1] * inv);
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
+          }
         }
       }
     }
@@ -746,9 +814,13 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   __syncthreads();
   if (tid == 0) {
     mbar_wait(smem_u32(fin), 0, kDrainNs);
-    if (s_bad)
-      for (int t = max(0, n_tiles - kNS); t < n_tiles; ++t)
+    if (s_bad) {
+      // the copies of the last tiles issued may still be landing
+      const int issued = s_issued;
+      for (int t = max(0, issued - kNS); t < issued; ++t)
         mbar_wait(smem_u32(&full[t % kNS]), (t / kNS) & 1, kDrainNs);
+      if (a.status != nullptr) atomicOr(a.status, s_bad);
+    }
   }
   tc_fence_before();
   __syncthreads();

@@ -57,7 +57,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const Deco
   __shared__ float q_s[GM][D];
   __shared__ float m_s[kSimtWarps][GM];
   __shared__ float l_s[kSimtWarps][GM];
-  __shared__ int bad_s;
+  __shared__ int bad_s;  // PKV_DEVICE_* bits
   // p_s lives during the block loop, acc_s after it
   __shared__ union {
     float p[kSimtWarps][T][GM];
@@ -66,7 +66,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const Deco
   auto& p_s = u_s.p;
   auto& acc_s = u_s.acc;
 
-  if (threadIdx.x == 0) bad_s = bad_ctx ? 1 : 0;
+  if (threadIdx.x == 0) bad_s = bad_ctx ? PKV_DEVICE_BAD_LENGTH : 0;
   for (int i = threadIdx.x; i < GM * D; i += blockDim.x) {
     const int j = i / D, d = i % D;
     float x = 0.f;
@@ -159,7 +159,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const Deco
     }
     __syncwarp();
   }
-  if (bad && lane == 0) atomicOr(&bad_s, 1);
+  if (bad && lane == 0) atomicOr(&bad_s, PKV_DEVICE_BAD_TABLE);
   __syncthreads();  // every warp is done with p_s before acc_s overwrites it
 
   if (lane == 0) {
@@ -176,6 +176,7 @@ __global__ void __launch_bounds__(kSimtWarps * 32) decode_simt_kernel(const Deco
   __syncthreads();
 
   const bool any_bad = bad_s != 0;
+  if (threadIdx.x == 0 && any_bad && a.status != nullptr) atomicOr(a.status, bad_s);
   for (int i = threadIdx.x; i < G * D; i += blockDim.x) {
     const int j = i / D, d = i % D;
     float M = -CUDART_INF_F;

@@ -105,6 +105,18 @@ __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_
   return false;
 }
 
+// A decode stage wait: bounded by limit_ns; a limit of 0 gives up at once
+// (the failure path, exercised on purpose).
+__device__ __forceinline__ bool stage_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns) {
+  return limit_ns != 0 && mbar_wait(bar, parity, limit_ns);
+}
+
+// Device error bits (the PKV_DEVICE_* values of the C ABI).
+constexpr int kBadLength = PKV_DEVICE_BAD_LENGTH;
+constexpr int kBadTable = PKV_DEVICE_BAD_TABLE;
+constexpr int kTimeout = PKV_DEVICE_WAIT_TIMEOUT;
+constexpr int kBadPrefix = PKV_DEVICE_BAD_SHARED_PREFIX;
+
 __device__ __forceinline__ void fence_proxy_async() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
@@ -643,14 +655,18 @@ __device__ __forceinline__ void combine_warps(const float* mS, const float* lS, 
   }
 }
 
-// Combine the nsplit partials (max m_i, sum l_i, unnormalised output a_i) of
-// the G heads at head0:  M = max m_i, L = sum l_i 2^(m_i - M),
+// Combine the partials (max m_i, sum l_i, unnormalised output a_i) of the G
+// heads at head0, from split slots 0 .. nsplit - 1 and extra_base ..
+// extra_base + n_extra - 1:  M = max m_i, L = sum l_i 2^(m_i - M),
 // o = sum a_i 2^(m_i - M) / L.  Every load is a global round trip of several
 // microseconds while the GPU streams, so all partials are first gathered into
 // shared memory (stage, `cap` floats) with independent loads.
 template <typename Q, int D>
-__device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit, float* stage, int cap) {
+__device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit_tail, int extra_base,
+                             int n_extra, float* stage, int cap) {
   const int tid = threadIdx.x, G = a.group;
+  const int nsplit = nsplit_tail + n_extra;   // partials in all
+  auto slot = [&](int i) { return i < nsplit_tail ? i : extra_base + (i - nsplit_tail); };
   const int nacc = G * nsplit * D;
   float* g_acc = stage;
   float* g_m = g_acc + nacc;
@@ -658,7 +674,7 @@ __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit, floa
   if (G * nsplit <= kThreads && nacc + 2 * G * nsplit <= cap) {
     float mv = 0.f, lv = 0.f;
     if (tid < G * nsplit) {
-      const size_t pidx = (head0 + tid / nsplit) * a.max_splits + tid % nsplit;
+      const size_t pidx = (head0 + tid / nsplit) * a.max_splits + slot(tid % nsplit);
       mv = __ldcg(a.ws_m + pidx);
       lv = __ldcg(a.ws_l + pidx);
     }
@@ -672,7 +688,7 @@ __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit, floa
           const int e = 4 * i, row = e / (nsplit * D), rem = e - row * nsplit * D;
           const int sp = rem / D, d = rem - sp * D;
           v[u] = __ldcg(reinterpret_cast<const float4*>(
-              a.ws_acc + ((head0 + row) * a.max_splits + sp) * D + d));
+              a.ws_acc + ((head0 + row) * a.max_splits + slot(sp)) * D + d));
         }
       }
 #pragma unroll
@@ -697,6 +713,10 @@ __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit, floa
           L = fmaf(g_l[row * nsplit + sp], f, L);
           A = fmaf(g_acc[(row * nsplit + sp) * D + d], f, A);
         }
+      } else {
+        // no split attended a position: the sums are 0, or NaN for a split
+        // that failed, which must reach the output
+        for (int sp = 0; sp < nsplit; ++sp) L += g_l[row * nsplit + sp];
       }
       store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
     }
@@ -705,14 +725,16 @@ __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit, floa
       const int row = i / D, d = i % D;
       const size_t base = (head0 + row) * a.max_splits;
       float M = -CUDART_INF_F;
-      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(a.ws_m + base + sp));
+      for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, __ldcg(a.ws_m + base + slot(sp)));
       float L = 0.f, A = 0.f;
       if (M != -CUDART_INF_F) {
         for (int sp = 0; sp < nsplit; ++sp) {
-          const float f = exp2f(__ldcg(a.ws_m + base + sp) - M);
-          L = fmaf(__ldcg(a.ws_l + base + sp), f, L);
-          A = fmaf(__ldcg(a.ws_acc + (base + sp) * D + d), f, A);
+          const float f = exp2f(__ldcg(a.ws_m + base + slot(sp)) - M);
+          L = fmaf(__ldcg(a.ws_l + base + slot(sp)), f, L);
+          A = fmaf(__ldcg(a.ws_acc + (base + slot(sp)) * D + d), f, A);
         }
+      } else {
+        for (int sp = 0; sp < nsplit; ++sp) L += __ldcg(a.ws_l + base + slot(sp));
       }
       store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
     }
@@ -743,14 +765,21 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   // second split, so that the short last splits of long pairs come last
   const int kvh = blockIdx.x, seq = blockIdx.y, split = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  // Positions [0, P) were attended by the shared-prefix pass (P = 0: none);
+  // this CTA covers part of [P, ctx).
+  const int P = a.prefix_tokens;
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: nothing that kernel may write is read before it has completed.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Behind the shared-prefix pass (which waited for every kernel before it
+  // before letting this grid start), the pass's partials are the only such
+  // data, and the wait moves to the merge that reads them.
+  if (P == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int g = lane >> 2, q4 = lane & 3;
   const int G = a.group;
   const int ctx = a.ctx_lens[seq];
-  const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T;
-  const int nsplit = bad_ctx ? 1 : max(1, (ctx + a.partition - 1) / a.partition);
+  const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T || (P > 0 && ctx <= P);
+  const int own = bad_ctx ? 0 : ctx - P;  // positions this kernel attends
+  const int nsplit = bad_ctx ? 1 : max(1, (own + a.partition - 1) / a.partition);
   if (split >= nsplit) return;
   const HeadScales sc = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale,
                                     a.qk_scale, a.v_scale, a.k_inv, a.v_inv);
@@ -758,9 +787,9 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   // [i n_t / nsplit, (i + 1) n_t / nsplit), at most partition / 64 of them.
   // Near-equal pieces keep the longest units of the grid on pairs that need
   // no merge, and the boundaries still depend only on the length.
-  const int64_t n_t = bad_ctx ? 0 : (ctx + kTile - 1) / kTile;
-  const int t_begin = static_cast<int>(split * n_t / nsplit) * kTile;
-  const int t_end = bad_ctx ? 0 : min(static_cast<int>((split + 1) * n_t / nsplit) * kTile, ctx);
+  const int64_t n_t = (own + kTile - 1) / kTile;
+  const int t_begin = P + static_cast<int>(split * n_t / nsplit) * kTile;
+  const int t_end = bad_ctx ? P : min(P + static_cast<int>((split + 1) * n_t / nsplit) * kTile, ctx);
   const int first_blk = t_begin / T;
   const int n_blk = (t_end - t_begin + T - 1) / T;
   const int n_tiles = (t_end - t_begin + kTile - 1) / kTile;
@@ -771,18 +800,24 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   uint8_t* stages = smem;                                            // NS * kStageBytes
   int32_t* s_tab = reinterpret_cast<int32_t*>(smem + NS * G_::kStageBytes);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(s_tab + kMaxTableEntries);
-  __shared__ int s_bad, s_last;
+  __shared__ int s_bad, s_last;  // s_bad: PKV_DEVICE_* bits, written by thread 0 only
 
   static_assert(NS * G_::kStageBytes >= (2 * kWarps * 16 + kWarps * 16 * D) * 4,
                 "the warp merge reuses the stage buffers");
   if (tid == 0) {
-    s_bad = bad_ctx ? 1 : 0;
+    s_bad = bad_ctx ? kBadLength : 0;
     for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&s_bar[s]), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async();
   }
   for (int i = tid; i < n_blk; i += kThreads)
     s_tab[i] = a.tables[static_cast<size_t>(seq) * a.max_blocks + first_blk + i];
+  // With a shared prefix, split 0 checks that this row maps the prefix
+  // blocks of row 0 (which the prefix pass read for every row).
+  bool prefix_mismatch = false;
+  if (P > 0 && split == 0 && !bad_ctx)
+    for (int i = tid; i < P / T; i += kThreads)
+      prefix_mismatch |= a.tables[static_cast<size_t>(seq) * a.max_blocks + i] != a.tables[i];
 
   // Fused slot write: the split holding position ctx - 1 stores the step's
   // token of its KV head before any copy is issued (a block never spans two
@@ -808,7 +843,7 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
     if constexpr (HC) load_qt<KV, Q, D>(qa, qrows, G, g, q4);
     else load_q<KV, Q, D>(qa, qrows, G, g, q4);
   }
-  __syncthreads();
+  const bool prefix_bad = __syncthreads_or(prefix_mismatch);
 
   // ---------------------------------------------------------- producer
   // Warp 0 refills a stage with one warp instruction: lane l issues box l
@@ -832,7 +867,7 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
     const unsigned badmask = __ballot_sync(0xffffffffu, inb && !good);
     const uint32_t bar = smem_u32(&s_bar[s]);
     if (lane == 0) {
-      if (badmask) s_bad = 1;
+      if (badmask) s_bad |= kBadTable;
       mbar_arrive_expect_tx(bar, __popc(okmask) * static_cast<uint32_t>(kBoxBytes));
     }
     __syncwarp();
@@ -851,7 +886,7 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   for (int tile = 0; tile < n_tiles; ++tile) {
     const int s = tile % NS;
     const uint32_t parity = (tile / NS) & 1;
-    const bool arrived = mbar_wait(smem_u32(&s_bar[s]), parity, kWaitNs);
+    const bool arrived = stage_wait(smem_u32(&s_bar[s]), parity, a.wait_ns);
     const uint8_t* kt = stages + s * G_::kStageBytes;
     uint8_t* vt = stages + s * G_::kStageBytes + G_::kTileBytes;
     const int row0 = warp * 16;
@@ -875,7 +910,7 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
     // wait (bounded) for the copies still in flight, tiles stalled_at ..
     // stalled_at + NS - 1, before the CTA's shared memory can be reused
     if (tid == 0) {
-      s_bad = 1;
+      s_bad |= kTimeout;
       for (int t = stalled_at; t < n_tiles && t < stalled_at + NS; ++t)
         mbar_wait(smem_u32(&s_bar[t % NS]), (t / NS) & 1, kDrainNs);
     }
@@ -890,14 +925,18 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   else publish<KV, D>(st, mS, lS, oS, warp, G, 16, lane);
   __syncthreads();
 
-  const bool any_bad = s_bad != 0;
+  const int bad_bits = s_bad | (prefix_bad ? kBadPrefix : 0);
+  if (tid == 0 && bad_bits != 0 && a.status != nullptr) atomicOr(a.status, bad_bits);
+  const bool any_bad = bad_bits != 0;
+  // A lone split writes the output unless a shared-prefix partial joins it.
+  const bool direct = nsplit == 1 && P == 0;
   const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
   for (int i = tid; i < G * D; i += kThreads) {
     const int row = i / D, d = i % D;
     float M, L, A;
     combine_warps(mS, lS, oS, kWarps, 16, row, d, D, M, L, A);
     A *= sc.v;
-    if (nsplit == 1) {
+    if (direct) {
       const float out = any_bad ? CUDART_NAN_F : (L > 0.f ? A / L : 0.f);
       store_elem<Q>(a.out, (head0 + row) * D + d, out);
     } else {
@@ -910,22 +949,28 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
     }
   }
 
-  if (nsplit == 1) return;
+  if (direct) return;
 
   // ------------------------------------------- split-K: the last CTA merges
   // Each CTA counts itself in (an atomic counter, never a wait); the last of
-  // the pair's splits to finish combines all partials and resets the counter.
+  // the pair's splits to finish combines all partials (and the shared-prefix
+  // pass's) and resets the counter.
   __threadfence();
   __syncthreads();
-  if (tid == 0) {
-    const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
-    s_last = prev == nsplit - 1;
+  if (nsplit > 1) {
+    if (tid == 0) {
+      const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
+      s_last = prev == nsplit - 1;
+    }
+    __syncthreads();
+    if (!s_last) return;
+    __threadfence();
   }
-  __syncthreads();
-  if (!s_last) return;
-  __threadfence();
-  merge_splits<Q, D>(a, head0, nsplit, reinterpret_cast<float*>(smem), NS * G_::kStageBytes / 4);
-  if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
+  // the shared-prefix pass's partials: written by the preceding grid
+  if (P > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  merge_splits<Q, D>(a, head0, nsplit, a.max_splits - a.prefix_splits, P > 0 ? a.prefix_splits : 0,
+                     reinterpret_cast<float*>(smem), NS * G_::kStageBytes / 4);
+  if (nsplit > 1 && tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
 }
 
 template <typename KV, int D, int NS>

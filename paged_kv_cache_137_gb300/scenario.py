@@ -28,8 +28,9 @@ import torch
 
 import workloads as W
 
-from . import (Pool, empty_cache, kv_desc, pkv_attention_decode, pkv_copy_blocks,
-               pkv_decode_step, pkv_write, workspace_for)
+from . import (Pool, empty_cache, kv_desc, pkv_attention_decode, pkv_attention_decode_shared_prefix,
+               pkv_copy_blocks, pkv_decode_step, pkv_decode_step_shared_prefix, pkv_write,
+               shared_prefix_workspace_for, workspace_for)
 
 CHURN_ID0 = 1 << 40
 POISON_BYTE = 0xFF
@@ -56,6 +57,7 @@ class Plan:
     max_blocks: int
     tables: np.ndarray = field(default=None)
     ctx_i32: np.ndarray = field(default=None)
+    shared_prefix_blocks: int = 0   # leading blocks every sequence of the batch maps
 
 
 def churn(pool: Pool, coin, pick, block_size: int):
@@ -103,7 +105,8 @@ def plan(w: W.Workload) -> Plan:
     max_blocks = max(1, max(-(-int(c) // w.block_size) for c in ctx))
     tables, ctx32 = pool.block_tables(seq_ids, max_blocks)
     return Plan(w=w, pool=pool, seq_ids=seq_ids, ctx=ctx, prefill=writes, step_slots=step_slots,
-                cow_pairs=cow, max_blocks=max_blocks, tables=tables, ctx_i32=ctx32)
+                cow_pairs=cow, max_blocks=max_blocks, tables=tables, ctx_i32=ctx32,
+                shared_prefix_blocks=pool.shared_prefix_blocks(seq_ids))
 
 
 @dataclass
@@ -123,6 +126,7 @@ class DeviceScenario:
     scales: dict             # per-tensor E4M3 scale arguments ({} with per-head scales in desc)
     partition: int           # partition_tokens passed to the decode call (0 = automatic)
     softmax_scale: float
+    prefix_blocks: int = 0   # > 0: the decode calls attend this shared prefix once for all rows
 
     def copy_blocks(self, stream=None):
         pkv_copy_blocks([self.k_cache], [self.v_cache], self.plan.cow_pairs, self.desc, stream)
@@ -134,13 +138,26 @@ class DeviceScenario:
     def attend(self, stream=None, partition_tokens=None, out=None, workspace=None):
         p = self.partition if partition_tokens is None else partition_tokens
         ws = self.workspace if workspace is None else workspace
+        if self.prefix_blocks:
+            return pkv_attention_decode_shared_prefix(
+                self.out if out is None else out, self.q, self.k_cache, self.v_cache, self.tables,
+                self.ctx, self.desc, self.prefix_blocks, self.softmax_scale,
+                self.scales.get("k_scale", 1.0), self.scales.get("v_scale", 1.0), p, ws, stream)
         return pkv_attention_decode(self.out if out is None else out, self.q, self.k_cache,
                                     self.v_cache, self.tables, self.ctx, self.desc,
                                     self.softmax_scale, self.scales.get("k_scale", 1.0),
                                     self.scales.get("v_scale", 1.0), p, ws, stream)
 
     def decode_step(self, stream=None, out=None):
-        """Slot write of the step's token fused with attention (pkv_decode_step)."""
+        """Slot write of the step's token fused with attention (pkv_decode_step,
+        or pkv_decode_step_shared_prefix over a shared prefix)."""
+        if self.prefix_blocks:
+            return pkv_decode_step_shared_prefix(
+                self.out if out is None else out, self.q, self.k_cache, self.v_cache, self.k_new,
+                self.v_new, self.tables, self.ctx, self.desc, self.prefix_blocks, self.softmax_scale,
+                self.scales.get("k_scale", 1.0), self.scales.get("v_scale", 1.0),
+                self.scales.get("k_inv_scale", 1.0), self.scales.get("v_inv_scale", 1.0),
+                self.partition, self.workspace, stream)
         return pkv_decode_step(self.out if out is None else out, self.q, self.k_cache, self.v_cache,
                                self.k_new, self.v_new, self.tables, self.ctx, self.desc,
                                self.softmax_scale, self.scales.get("k_scale", 1.0),
@@ -181,8 +198,19 @@ def _kv_of(w, pw: PrefillWrite):
     return W.kv_for_seq(w, pw.seq, pw.n_tokens, first_pos=pw.first_pos)
 
 
+def use_shared_prefix(p: Plan) -> bool:
+    """Whether the decode calls take the shared-prefix path by default: a
+    prefix of at least 256 tokens shared by enough (sequence, head) rows to
+    fill one 128-row tensor-core tile per KV head."""
+    w = p.w
+    return (p.shared_prefix_blocks * w.block_size >= 256 and len(p.seq_ids) * w.group >= 128
+            and w.head_dim == 128 and w.kv_dtype != "f32")
+
+
 def materialize(p: Plan, device="cuda", scales: dict | None = None, chunk_tokens: int = 1 << 19,
-                partition_tokens: int | None = None) -> DeviceScenario:
+                partition_tokens: int | None = None, shared_prefix: bool | None = None) -> DeviceScenario:
+    """The device state of a plan.  shared_prefix: take the shared-prefix
+    decode path over the plan's shared blocks (None: use_shared_prefix)."""
     w = p.w
     scales = dict(scales or {})
     if w.kv_dtype == "e4m3" and "k_inv_scale" not in scales:
@@ -228,11 +256,18 @@ def materialize(p: Plan, device="cuda", scales: dict | None = None, chunk_tokens
     v_new = torch.cat([v for _, v in news]).to(device)
     q = torch.stack([W.q_for_seq(w, s) for s in p.seq_ids]).to(device)
     part = w.partition_tokens if partition_tokens is None else partition_tokens
-    ws = workspace_for(len(p.seq_ids), w.num_q_heads, p.max_blocks, desc, part, device)
+    if shared_prefix is None:
+        shared_prefix = use_shared_prefix(p)
+    pfx = p.shared_prefix_blocks if shared_prefix else 0
+    if pfx:
+        ws = shared_prefix_workspace_for(len(p.seq_ids), w.num_q_heads, p.max_blocks, desc, pfx, part,
+                                         device)
+    else:
+        ws = workspace_for(len(p.seq_ids), w.num_q_heads, p.max_blocks, desc, part, device)
     return DeviceScenario(
         plan=p, desc=desc, k_cache=k_cache, v_cache=v_cache, q=q, out=torch.empty_like(q),
         tables=torch.from_numpy(p.tables).to(device), ctx=torch.from_numpy(p.ctx_i32).to(device),
         step_slots=torch.from_numpy(np.asarray(p.step_slots, dtype=np.int64)).to(device),
         k_new=k_new, v_new=v_new, workspace=ws, scales=scales,
         partition=part,
-        softmax_scale=1.0 / math.sqrt(w.head_dim))
+        softmax_scale=1.0 / math.sqrt(w.head_dim), prefix_blocks=pfx)

@@ -207,17 +207,57 @@ def test_zero_context_gives_zero_and_poison_is_never_read(kernel):
 
 
 def test_invalid_table_entry_or_length_gives_nan(kernel):
+    """Invalid device inputs give NaN outputs and set their bit in the
+    device error word, which the host reads and clears."""
     desc, kc, vc, k, v, q, tables = _single_block_case(16)
+    pkv.pkv_device_status(clear=True)
     out = torch.zeros_like(q)
     bad = torch.tensor([[3, 99]], dtype=torch.int32).cuda()   # 99 >= num_blocks
     pkv.pkv_attention_decode(out, q, kc, vc, bad, torch.tensor([20], dtype=torch.int32).cuda(), desc, 0.1)
     torch.cuda.synchronize()
     assert torch.isnan(out).all()
+    assert pkv.pkv_device_status(clear=True) == pkv.PKV_DEVICE_BAD_TABLE
     out.zero_()
     pkv.pkv_attention_decode(out, q, kc, vc, tables, torch.tensor([33], dtype=torch.int32).cuda(),
                              desc, 0.1)   # longer than 2 blocks
     torch.cuda.synchronize()
     assert torch.isnan(out).all()
+    assert pkv.pkv_device_status(clear=True) == pkv.PKV_DEVICE_BAD_LENGTH
+    # valid inputs leave the word clear
+    pkv.pkv_attention_decode(out, q, kc, vc, tables, torch.tensor([16], dtype=torch.int32).cuda(),
+                             desc, 0.1)
+    assert pkv.pkv_device_status() == 0
+    assert not torch.isnan(out).any()
+
+
+def test_stage_wait_give_up_sets_status_and_nan_then_recovers():
+    """The decode kernel's failure path, run on purpose: with a stage-wait
+    limit of 0 every CTA gives up at its first stage wait, still waits (with
+    its own bounded limit) for the copies it has in flight, writes NaN and
+    sets PKV_DEVICE_WAIT_TIMEOUT; split partials merge into NaN and the
+    arrival counters end at zero.  Afterwards the same call is correct."""
+    w = SMALL["qwen_small"]
+    pkv.pkv_set_attention_kernel("tc")
+    dev = PS.materialize(PS.plan(w), "cuda", partition_tokens=256)
+    dev.copy_blocks()
+    dev.write_step()
+    pkv.pkv_device_status(clear=True)
+    try:
+        pkv.pkv_set_stage_wait_limit(0)
+        out = dev.attend().clone()
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_set_stage_wait_limit(50_000_000)
+        pkv.pkv_set_attention_kernel("auto")
+    assert pkv.pkv_device_status(clear=True) & pkv.PKV_DEVICE_WAIT_TIMEOUT
+    ctx = dev.plan.ctx
+    assert torch.isnan(out[torch.from_numpy(ctx > 0)]).all()
+    n = len(dev.plan.seq_ids) * w.num_kv_heads
+    assert torch.count_nonzero(dev.workspace[: 4 * n]).item() == 0
+    out = dev.attend()
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status() == 0
+    check_close(out.double().cpu().numpy(), oracle_out(OS.build(w)), w.kv_dtype)
 
 
 def test_write_skips_negative_and_out_of_pool_slots():

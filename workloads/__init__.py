@@ -272,8 +272,12 @@ def fork_layout(w: Workload) -> dict:
     ``num_children`` parents whose prior length is not a multiple of the block
     size (a fork in the middle of a block) each get one child.  The batch
     order is children first, then parents; ``ctx`` is in batch order, and a
-    child attends the same length as its parent.
+    child attends the same length as its parent.  The prefix is whole blocks
+    (its last block full), so every parent's tail starts in a block of its
+    own and only the decode step copies blocks.
     """
+    if w.prefix_len % w.block_size:
+        raise ValueError(f"prefix_len {w.prefix_len} is not a multiple of block_size {w.block_size}")
     n_children = int(round(w.num_seqs * w.fork_fraction))
     n_parents = w.num_seqs - n_children
     lo, hi = w.tail_range
