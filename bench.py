@@ -63,7 +63,7 @@ def parse():
                          "and K end-to-end steps, for profiling runs)")
     ap.add_argument("--partition", type=int, default=None,
                     help="split-K partition in tokens (default: the workload's, else automatic)")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc", "persistent"],
                     help="decode kernel (auto = tensor-core where it applies)")
     ap.add_argument("--shared-prefix", default="auto", choices=["auto", "on", "off"],
                     help="decode a batch's shared prefix once for all sequences (auto: when the "
@@ -192,7 +192,9 @@ def attention_kernels(kernel: str, w, splits: int, shared_prefix: bool = False) 
         k = "decode_simt_kernel"
         return k + (" + merge_kernel" if splits > 1 else "")
     if shared_prefix:
-        return "prefill_umma_kernel<shared prefix> + decode_tc_kernel (merge fused)"
+        return "prefill_umma_kernel<shared prefix> + decode_pd_kernel (persistent; merges fused)"
+    if kernel == "persistent":
+        return "decode_pd_kernel (persistent; merges fused)"
     return "decode_tc_kernel (split-K merge fused)"
 
 

@@ -79,18 +79,26 @@ int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx, 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t counter_off, m_off, l_off, acc_off, bytes;
+  size_t counter_off, done_off, work_off, m_off, l_off, acc_off, bytes;
 };
 
-// Workspace: split-K arrival counters (zero between calls), then the
-// partial maxima, sums and unnormalised outputs, each 256-byte aligned.
+// Workspace: split-K arrival counters [B][N_kv] (zero between calls), then
+// extra_ints more counters (the grid's exit count behind a shared-prefix
+// pass; the persistent kernel's exit count and unit queue), then the partial
+// maxima, sums and unnormalised outputs (when there are splits), each part
+// 256-byte aligned.  Nothing when neither is needed.
 WsLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t num_kv_heads,
-                          int64_t splits, int64_t head_dim) {
+                          int64_t splits, int64_t head_dim, int extra_ints = 0) {
   WsLayout w{};
+  if (splits <= 1 && extra_ints == 0) return w;
+  const size_t counters = static_cast<size_t>(num_seqs * num_kv_heads) + extra_ints;
+  w.counter_off = 0;
+  w.done_off = static_cast<size_t>(num_seqs * num_kv_heads) * sizeof(int);
+  w.work_off = w.done_off + sizeof(int);
+  w.m_off = align_up(counters * sizeof(int), 256);
+  w.bytes = w.m_off;
   if (splits <= 1) return w;
   const size_t n = static_cast<size_t>(num_seqs * num_q_heads * splits);
-  w.counter_off = 0;
-  w.m_off = align_up(static_cast<size_t>(num_seqs * num_kv_heads) * sizeof(int), 256);
   w.l_off = w.m_off + align_up(n * sizeof(float), 256);
   w.acc_off = w.l_off + align_up(n * sizeof(float), 256);
   w.bytes = w.acc_off + align_up(n * head_dim * sizeof(float), 256);
@@ -175,12 +183,14 @@ int64_t num_splits(int32_t max_blocks, int32_t block_size, int32_t partition,
 // pass has about one CTA per SM (it holds a whole SM); ranges are whole
 // 64-key tiles.
 struct PrefixPlan {
-  int32_t tokens = 0, key_splits = 0, split_tokens = 0;
+  int32_t tokens = 0, key_splits = 0, split_tokens = 0, seqs_per_cta = 0;
 };
 PrefixPlan prefix_plan(int64_t num_seqs, int64_t group, int64_t num_kv_heads, int64_t prefix_tokens) {
   PrefixPlan p;
   if (prefix_tokens <= 0) return p;
-  const int64_t units = (num_seqs * group + 255) / 256 * num_kv_heads;
+  // a CTA's 256 query rows hold whole sequences (all G heads of each)
+  p.seqs_per_cta = static_cast<int32_t>(256 / group);
+  const int64_t units = (num_seqs + p.seqs_per_cta - 1) / p.seqs_per_cta * num_kv_heads;
   const int64_t tiles = (prefix_tokens + 63) / 64;
   const int64_t want = std::max<int64_t>(1, std::min<int64_t>(tiles, device_sms() / std::max<int64_t>(units, 1)));
   const int64_t per = (tiles + want - 1) / want;
@@ -198,6 +208,77 @@ bool prefix_pass_covers(const pkv_kv_desc* d, int q_dtype, float softmax_scale) 
   if (d->kv_dtype == PKV_F16) return q_dtype == PKV_F16;
   return d->kv_dtype == PKV_E4M3 && (q_dtype == PKV_F16 || q_dtype == PKV_BF16);
 }
+
+// Whether the persistent kernel covers these sizes (16-bit caches, groups of
+// up to 8 query heads, at most kPdMaxSeqs sequences, units of at most
+// kPdUnitBlocks blocks).
+bool pd_supported(const pkv_kv_desc* d, int group, int num_seqs, int partition) {
+  if (d->kv_dtype != PKV_BF16 && d->kv_dtype != PKV_F16) return false;
+  if (d->head_dim != 128 && d->head_dim != 64) return false;
+  if (group > 8 || num_seqs > kPdMaxSeqs) return false;
+  if (partition > kPdUnitBlocks * d->block_size) return false;
+  return static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * d->block_size <= INT32_MAX;
+}
+
+// Partition of the persistent kernel for partition_tokens 0: one split per
+// pair when every context (past a shared prefix) fits 1,024 tokens, else
+// 512-token splits (units of at most 8 tiles, which the queue balances).
+int32_t pd_partition(int64_t max_ctx, int32_t block_size) {
+  const int64_t step = std::max<int32_t>(64, block_size);
+  if (max_ctx <= 1024) return static_cast<int32_t>(std::max<int64_t>(step, (max_ctx + step - 1) / step * step));
+  return static_cast<int32_t>(std::max<int64_t>(step, 512));
+}
+
+// Everything a decode call decides before launching: the kernels, the
+// partition, the split slots and the workspace layout.  sizing: for the
+// workspace-size queries (q dtype and softmax scale taken as the ones that
+// run the most kernels).
+struct CallPlan {
+  bool prefix_pass = false, pd = false;
+  PrefixPlan pp;
+  int32_t partition = 0;
+  int64_t splits = 1;   // tail splits + prefix key ranges
+  WsLayout ws{};
+};
+pkv_status plan_call(const pkv_kv_desc* d, int q_dtype, float softmax_scale, int32_t num_seqs,
+                     int32_t num_q_heads, int32_t max_blocks, int32_t partition_tokens,
+                     int32_t prefix_blocks, CallPlan* out) {
+  CallPlan c;
+  const int group = num_q_heads / d->num_kv_heads;
+  const int choice = g_kernel_choice.load();
+  const bool rows_fit = static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * d->block_size <= INT32_MAX;
+  c.prefix_pass = prefix_blocks > 0 && choice != PKV_KERNEL_SIMT && rows_fit &&
+                  prefix_pass_covers(d, q_dtype, softmax_scale) && tc_supported(d, q_dtype, group, 64);
+  if (c.prefix_pass)
+    c.pp = prefix_plan(num_seqs, group, d->num_kv_heads, static_cast<int64_t>(prefix_blocks) * d->block_size);
+  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * d->block_size - c.pp.tokens;
+  // the persistent kernel: when chosen, and for the tails behind a prefix pass
+  const bool want_pd = choice == PKV_KERNEL_PERSISTENT || (c.prefix_pass && choice == PKV_KERNEL_AUTO);
+  if (want_pd) {
+    int32_t p = partition_tokens;
+    if (p < 0) return fail(PKV_ERR_INVALID_ARG, "partition_tokens is negative");
+    if (p > 0 && (p % 64 != 0 || p % d->block_size != 0))
+      return fail(PKV_ERR_INVALID_ARG, "partition_tokens must be a multiple of 64 and of block_size");
+    if (p == 0) p = pd_partition(max_ctx, d->block_size);
+    const int64_t units = static_cast<int64_t>(num_seqs) * d->num_kv_heads *
+                          std::max<int64_t>(1, (max_ctx + p - 1) / p);
+    if (pd_supported(d, group, num_seqs, p) && units < (int64_t{1} << 30)) {
+      c.pd = true;
+      c.partition = p;
+    }
+  }
+  if (!c.pd) {
+    pkv_status st = resolve_partition(partition_tokens, num_seqs, max_blocks, d, &c.partition, c.pp.tokens);
+    if (st != PKV_OK) return st;
+  }
+  c.splits = num_splits(max_blocks, d->block_size, c.partition, c.pp.tokens) + c.pp.key_splits;
+  const int extra = c.pd ? 2 : (c.prefix_pass ? 1 : 0);
+  c.ws = workspace_layout(num_seqs, num_q_heads, d->num_kv_heads, c.splits, d->head_dim, extra);
+  *out = c;
+  return PKV_OK;
+}
+
+int sizing_q_dtype(const pkv_kv_desc* d) { return d->kv_dtype == PKV_E4M3 ? PKV_BF16 : d->kv_dtype; }
 
 }  // namespace
 
@@ -266,27 +347,30 @@ extern "C" size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_
                                                 int32_t max_blocks, const pkv_kv_desc* desc,
                                                 int32_t partition_tokens) {
   if (check_desc(desc) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 || max_blocks <= 0) return 0;
-  int32_t p = 0;
-  if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
-  const int64_t s = num_splits(max_blocks, desc->block_size, p);
-  return workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim).bytes;
+  if (num_q_heads % desc->num_kv_heads != 0) return 0;
+  CallPlan c;
+  if (plan_call(desc, sizing_q_dtype(desc), 1.f, num_seqs, num_q_heads, max_blocks, partition_tokens,
+                0, &c) != PKV_OK)
+    return 0;
+  return c.ws.bytes;
 }
 
 namespace pkv {
 size_t attention_counter_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t max_blocks,
                                const pkv_kv_desc* desc, int32_t partition_tokens) {
   if (check_desc(desc) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 || max_blocks <= 0) return 0;
-  int32_t p = 0;
-  if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p) != PKV_OK) return 0;
-  const int64_t s = num_splits(max_blocks, desc->block_size, p);
-  const WsLayout w = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim);
-  if (!w.bytes) return 0;
-  return align_up(static_cast<size_t>(num_seqs) * desc->num_kv_heads * sizeof(int), 256);
+  if (num_q_heads % desc->num_kv_heads != 0) return 0;
+  CallPlan c;
+  if (plan_call(desc, sizing_q_dtype(desc), 1.f, num_seqs, num_q_heads, max_blocks, partition_tokens,
+                0, &c) != PKV_OK)
+    return 0;
+  return c.ws.bytes ? c.ws.m_off : 0;
 }
 }  // namespace pkv
 
 extern "C" pkv_status pkv_set_attention_kernel(int32_t kind) {
-  if (kind != PKV_KERNEL_AUTO && kind != PKV_KERNEL_SIMT && kind != PKV_KERNEL_TENSOR_CORE)
+  if (kind != PKV_KERNEL_AUTO && kind != PKV_KERNEL_SIMT && kind != PKV_KERNEL_TENSOR_CORE &&
+      kind != PKV_KERNEL_PERSISTENT)
     return fail(PKV_ERR_INVALID_ARG, "unknown attention kernel kind");
   g_kernel_choice.store(kind);
   return PKV_OK;
@@ -336,27 +420,20 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   while (gm < group) gm = gm == 1 ? 4 : gm * 2;
   if (gm > 16) return fail(PKV_ERR_UNSUPPORTED, "more than 16 query heads per KV head");
   const int choice = g_kernel_choice.load();
-  if (static_cast<int64_t>(desc->num_blocks) * desc->num_kv_heads * desc->block_size > INT32_MAX &&
-      prefix_blocks > 0)
-    prefix_blocks = 0;  // the pass's TMA rows are int
 
   // A declared shared prefix runs the prefix pass where it covers the shape
-  // under the tensor-core decode kernel; otherwise the prefix is read per
+  // under the tensor-core decode kernels; otherwise the prefix is read per
   // sequence like the rest of the context (same attention).
-  const bool prefix_pass = prefix_blocks > 0 && choice != PKV_KERNEL_SIMT &&
-                           prefix_pass_covers(desc, q_dtype, softmax_scale) &&
-                           tc_supported(desc, q_dtype, group, 64);
-  const PrefixPlan pp = prefix_pass
-                            ? prefix_plan(num_seqs, group, desc->num_kv_heads,
-                                          static_cast<int64_t>(prefix_blocks) * desc->block_size)
-                            : PrefixPlan{};
-  int32_t partition = 0;
-  st = resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &partition, pp.tokens);
+  CallPlan plan;
+  st = plan_call(desc, q_dtype, softmax_scale, num_seqs, num_q_heads, max_blocks, partition_tokens,
+                 prefix_blocks, &plan);
   if (st != PKV_OK) return st;
-  const int64_t splits = num_splits(max_blocks, desc->block_size, partition, pp.tokens) + pp.key_splits;
+  const bool prefix_pass = plan.prefix_pass;
+  const PrefixPlan pp = plan.pp;
+  const int32_t partition = plan.partition;
+  const int64_t splits = plan.splits;
   if (splits > 65535) return fail(PKV_ERR_UNSUPPORTED, "too many splits");
-  const WsLayout ws = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, splits,
-                                       desc->head_dim);
+  const WsLayout ws = plan.ws;
   if (ws.bytes > 0) {
     if (!workspace || workspace_bytes < ws.bytes)
       return fail(PKV_ERR_INVALID_ARG, "workspace missing or smaller than the workspace size call");
@@ -373,9 +450,10 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   a.tables = block_tables;
   a.ctx_lens = context_lens;
   uint8_t* wsb = static_cast<uint8_t*>(workspace);
-  a.ws_m = ws.bytes ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
-  a.ws_l = ws.bytes ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
-  a.ws_acc = ws.bytes ? reinterpret_cast<float*>(wsb + ws.acc_off) : nullptr;
+  const bool partials = ws.bytes > ws.m_off;
+  a.ws_m = partials ? reinterpret_cast<float*>(wsb + ws.m_off) : nullptr;
+  a.ws_l = partials ? reinterpret_cast<float*>(wsb + ws.l_off) : nullptr;
+  a.ws_acc = partials ? reinterpret_cast<float*>(wsb + ws.acc_off) : nullptr;
   a.counters = ws.bytes ? reinterpret_cast<int*>(wsb + ws.counter_off) : nullptr;
   a.max_blocks = max_blocks;
   a.num_seqs = num_seqs;
@@ -393,18 +471,20 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   a.softmax_scale = softmax_scale;
   a.prefix_tokens = pp.tokens;
   a.prefix_splits = pp.key_splits;
+  a.done = (prefix_pass || plan.pd) ? reinterpret_cast<int*>(wsb + ws.done_off) : nullptr;
+  a.work = plan.pd ? reinterpret_cast<int*>(wsb + ws.work_off) : nullptr;
   a.status = status;
   a.wait_ns = stage_wait_limit_ns();
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim;
   const bool tc_ok = tc_supported(desc, q_dtype, group, partition);
-  if (choice == PKV_KERNEL_TENSOR_CORE && !tc_ok)
+  if ((choice == PKV_KERNEL_TENSOR_CORE || choice == PKV_KERNEL_PERSISTENT) && !tc_ok && !plan.pd)
     return fail(PKV_ERR_UNSUPPORTED, "the tensor-core kernel does not cover these sizes");
   if (prefix_pass && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED, "partition too long for the tensor-core kernel");
   if (k_new) {
-    if (tc_ok && choice != PKV_KERNEL_SIMT) {
+    if (plan.pd || (tc_ok && choice != PKV_KERNEL_SIMT)) {
       a.k_new = k_new;  // fused into the split kernel
       a.v_new = v_new;
       a.k_inv = kv == PKV_E4M3 ? k_inv : 1.0f;
@@ -442,6 +522,11 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
     pa.ws_m = a.ws_m;
     pa.ws_l = a.ws_l;
     pa.ws_acc = a.ws_acc;
+    pa.out = out;
+    pa.ctx_lens = context_lens;
+    pa.counters = a.counters;
+    pa.partition = partition;
+    pa.sp_seqs = pp.seqs_per_cta;
     CUtensorMap pkmap, pvmap;
     st = pool_map(&pkmap, k_cache, desc, false);
     if (st == PKV_OK) st = pool_map(&pvmap, v_cache, desc, false);
@@ -455,6 +540,14 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
                                 : launch_shared_prefix_pass<E4M3, BF16>(pa, T, pp.key_splits, pkmap, pvmap, s);
     }
     if (st != PKV_OK) return st;
+  }
+  if (plan.pd) {
+    CUtensorMap kmap, vmap;
+    st = pool_map(&kmap, k_cache, desc);
+    if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc);
+    if (st != PKV_OK) return st;
+    return kv == PKV_F16 ? launch_decode_pd<F16, F16>(a, D, kmap, vmap, s)
+                         : launch_decode_pd<BF16, BF16>(a, D, kmap, vmap, s);
   }
   if (tc_ok && choice != PKV_KERNEL_SIMT) {
     CUtensorMap kmap, vmap;
@@ -523,15 +616,14 @@ extern "C" size_t pkv_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t nu
                                                     int32_t prefix_blocks, int32_t partition_tokens) {
   if (check_desc(desc) != PKV_OK || num_seqs <= 0 || num_q_heads <= 0 || max_blocks <= 0) return 0;
   if (prefix_blocks < 0 || prefix_blocks > max_blocks || num_q_heads % desc->num_kv_heads != 0) return 0;
-  // the size the prefix pass needs; calls that run without it need less
-  const PrefixPlan pp = prefix_plan(num_seqs, num_q_heads / desc->num_kv_heads, desc->num_kv_heads,
-                                    static_cast<int64_t>(prefix_blocks) * desc->block_size);
-  int32_t p = 0;
-  if (resolve_partition(partition_tokens, num_seqs, max_blocks, desc, &p, pp.tokens) != PKV_OK) return 0;
-  const int64_t s = num_splits(max_blocks, desc->block_size, p, pp.tokens) + pp.key_splits;
-  const size_t with = workspace_layout(num_seqs, num_q_heads, desc->num_kv_heads, s, desc->head_dim).bytes;
-  return std::max(with, pkv_attention_workspace_bytes(num_seqs, num_q_heads, max_blocks, desc,
-                                                      partition_tokens));
+  // the size the prefix pass needs; calls that run without it need no more
+  // than the plain call
+  CallPlan c;
+  if (plan_call(desc, sizing_q_dtype(desc), 1.f, num_seqs, num_q_heads, max_blocks, partition_tokens,
+                prefix_blocks, &c) != PKV_OK)
+    return 0;
+  return std::max(c.ws.bytes, pkv_attention_workspace_bytes(num_seqs, num_q_heads, max_blocks, desc,
+                                                            partition_tokens));
 }
 
 extern "C" pkv_status pkv_attention_decode_shared_prefix(

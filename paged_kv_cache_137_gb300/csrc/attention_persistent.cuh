@@ -1,0 +1,597 @@
+// Persistent decode attention: a grid of resident CTAs that take work units
+// (sequence, KV head, split) from a queue until it is empty.
+//
+// What it computes is the split kernel's (attention_tc.cuh): for the G query
+// heads of one KV head, softmax(q . K^T * scale) V over the positions of one
+// split, K/V gathered through the block table (the katajob Q&A, "The paging
+// idea"; the foundry page on paged block allocation, "Concept"), the splits
+// merged by the last to finish.
+//
+// Why a second schedule: when the units are short (a few 64-token tiles, as
+// the private tails of sequences that share a prompt), a CTA per unit spends
+// most of its life outside the stream of K/V: reading the length, then the
+// block table, then waiting for the first tile, and at the end combining its
+// warps and counting itself in, each a global round trip that costs several
+// microseconds while HBM is saturated.  Here a CTA lives for the whole call:
+//  * Every CTA numbers the units the same way (sequence by sequence, the
+//    splits of a sequence, then its KV heads) from the lengths, which it
+//    reads once into shared memory with a prefix sum of the units per
+//    sequence.  A CTA takes the next unit number from a global counter one
+//    unit ahead of need.
+//  * Warp 0 resolves a unit ahead of the consumers: its block ids, the G
+//    query rows and (for the step's token) the new K/V rows are copied into a
+//    shared-memory slot by cp.async, with no thread waiting on them.  Two
+//    slots: the unit being consumed and the next one.
+//  * The K/V ring (three 32 KiB stages for 16-bit head_dim 128) is refilled
+//    across unit boundaries: the next unit's first tiles are in flight while
+//    the current unit finishes.
+//  * Warps split head_dim, not tokens: each warp computes S^T = K q^T for 16
+//    tokens of a tile, the tile's row maxima and sums are exchanged through
+//    shared memory, P^T (64 tokens x 8 heads) goes through shared memory, and
+//    each warp accumulates O^T for its D / 4 rows of head_dim over all 64
+//    tokens.  No warp merge is needed at a unit's end: each warp writes its
+//    rows of the output (or of the split partial) from registers.
+//  * Split partials are counted in at the end of the CTA's life (or when 64
+//    are pending): one fence, one atomic per unit, and the last of a pair's
+//    partials to arrive merges them.  With a shared prefix the prefix pass's
+//    partials join the same count.
+//  * Every wait is bounded; a CTA whose stage wait gives up drains its copies
+//    in flight, stops issuing, and finishes every unit it takes from then on
+//    (including the rest of the queue, if no other CTA does) with NaN.
+#pragma once
+
+#include "attention_tc.cuh"
+
+namespace pkv {
+namespace tc {
+namespace pd {
+
+constexpr int kCtasPerSm = 2;
+constexpr int kRingBytes = 98304;   // K/V stages per CTA
+constexpr int kMaxSeqs = kPdMaxSeqs;        // sequences a call may hold (schedule in shared memory)
+constexpr int kUnitBlocks = kPdUnitBlocks;  // block ids of one unit (a partition of at most 128 blocks)
+constexpr int kDefer = 64;          // partials counted in at once
+constexpr int kPStride = kTile + 8; // P^T row (one head) in 16-bit elements, padded against bank conflicts
+
+template <typename KV, int D>
+constexpr int stages() {
+  return kRingBytes / Geom<KV, D>::kStageBytes;
+}
+
+// A resolved unit.
+struct Unit {
+  int seq, kvh, split, nsplit;
+  int t_begin, t_end, n_tiles, first_blk;
+  int n_blk, flags, bad, ctx;
+};
+constexpr int kValid = 1, kEnd = 2, kWrite = 4;
+
+// Shared-memory layout (bytes from the 1024-aligned base).
+template <typename KV, int D>
+struct Layout {
+  static constexpr int kStage = Geom<KV, D>::kStageBytes;
+  static constexpr int kSlotTab = kUnitBlocks * 4;          // int32 block ids
+  static constexpr int kSlotQ = 8 * D * 2;                  // up to 8 query rows (16-bit)
+  static constexpr int kSlotNew = 2 * D * 2;                // the step's K and V rows
+  static constexpr int kSlot = kSlotTab + kSlotQ + kSlotNew;
+  static constexpr int ring = 0;
+  static constexpr int slots = ring + stages<KV, D>() * kStage;
+  static constexpr int p = slots + 2 * kSlot;               // P^T [8 heads][kPStride] 16-bit
+  static constexpr int red = p + 8 * kPStride * 2;          // float [2][warps][8]
+  static constexpr int ctx = red + 2 * kWarps * 8 * 4;      // int32 [kMaxSeqs]
+  static constexpr int cum = ctx + kMaxSeqs * 4;            // int32 [kMaxSeqs + 1], padded
+  static constexpr int units = cum + (kMaxSeqs + 4) * 4;    // Unit [2]
+  static constexpr int defer = units + 2 * static_cast<int>(sizeof(Unit));  // int4 [kDefer]
+  static constexpr int bars = defer + kDefer * 16;          // uint64 [stages]
+  static constexpr int bytes = bars + stages<KV, D>() * 8 + 1024;  // + base alignment
+};
+
+__device__ __forceinline__ void cp_async4(void* dst, const void* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async16(void* dst, const void* src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+
+template <typename KV, typename Q, int D, int T>
+__global__ void __launch_bounds__(kThreads, kCtasPerSm)
+    decode_pd_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
+                     const __grid_constant__ CUtensorMap vmap) {
+  static_assert(!std::is_same<KV, E4M3>::value, "16-bit caches");
+  static_assert(std::is_same<KV, Q>::value, "16-bit caches take queries of their own type");
+  using G_ = Geom<KV, D>;
+  using L_ = Layout<KV, D>;
+  using raw = typename KV::raw;
+  constexpr int NS = stages<KV, D>();
+  constexpr int KS = D / 16;          // k-steps of S^T = K q^T
+  constexpr int MTW = D / 64;         // 16-row m-tiles of O^T per warp (head_dim split 4 ways)
+  constexpr int BPT = kTile / T;      // blocks per tile
+  constexpr int BPB = BPT * 2;        // TMA boxes per tile (K and V of each block)
+  constexpr int kBoxBytes = T * G_::kRowBytes;
+  constexpr bool kBf = std::is_same<KV, BF16>::value;
+  constexpr unsigned FULL = 0xffffffffu;
+  static_assert(NS >= 2 && BPB <= 32, "ring and box lanes");
+
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int g = lane >> 2, q4 = lane & 3, li = lane & 7, mi = lane >> 3;
+  const int P = a.prefix_tokens;
+  // Launched as a programmatic dependent of the previous kernel: nothing it
+  // may write is read before it has completed.  Behind the shared-prefix
+  // pass (which waited for everything before it before letting this grid
+  // start) there is nothing to wait for: the pass's partials meet this
+  // grid's through the arrival counters.
+  if (P == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int B = a.num_seqs, NKV = a.num_kv_heads, G = a.group, HQ = a.num_q_heads;
+  const int max_ctx = a.max_blocks * T;
+  const int n_extra = P > 0 ? a.prefix_splits : 0;
+
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
+                                             ~uintptr_t(1023));
+  uint8_t* ring = smem + L_::ring;
+  raw* s_p = reinterpret_cast<raw*>(smem + L_::p);
+  float* red_m = reinterpret_cast<float*>(smem + L_::red);
+  float* red_l = red_m + kWarps * 8;
+  int* s_ctx = reinterpret_cast<int*>(smem + L_::ctx);
+  int* s_cum = reinterpret_cast<int*>(smem + L_::cum);
+  Unit* s_unit = reinterpret_cast<Unit*>(smem + L_::units);
+  int4* s_defer = reinterpret_cast<int4*>(smem + L_::defer);
+  uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L_::bars);
+  auto slot_tab = [&](int s) { return reinterpret_cast<int32_t*>(smem + L_::slots + s * L_::kSlot); };
+  auto slot_q = [&](int s) {
+    return reinterpret_cast<raw*>(smem + L_::slots + s * L_::kSlot + L_::kSlotTab);
+  };
+  auto slot_new = [&](int s) {
+    return reinterpret_cast<raw*>(smem + L_::slots + s * L_::kSlot + L_::kSlotTab + L_::kSlotQ);
+  };
+  __shared__ int s_wsum[kWarps];
+  __shared__ int s_ndefer, s_nlast, s_last[kDefer];
+
+  // ------------------------------------------------------------ schedule
+  // The units of sequence i: nsplit_i splits x N_kv heads, numbered sequence
+  // by sequence; s_cum[i] = units before sequence i.
+  auto nsplit_of = [&](int c) {
+    const bool bad = c < 0 || c > max_ctx || (P > 0 && c <= P);
+    return bad ? 1 : max(1, (c - P + a.partition - 1) / a.partition);
+  };
+  if (tid == 0) {
+    for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&s_bar[s]), 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    s_ndefer = 0;
+  }
+  {
+    const int per = (B + kThreads - 1) / kThreads;
+    const int b0 = min(B, tid * per), b1 = min(B, b0 + per);
+    int run = 0;
+    for (int i = b0; i < b1; ++i) {
+      const int c = a.ctx_lens[i];
+      s_ctx[i] = c;
+      run += nsplit_of(c) * NKV;
+    }
+    int x = run;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+      const int y = __shfl_up_sync(FULL, x, off);
+      if (lane >= off) x += y;
+    }
+    if (lane == 31) s_wsum[warp] = x;
+    __syncthreads();
+    int excl = x - run;
+    for (int w = 0; w < warp; ++w) excl += s_wsum[w];
+    for (int i = b0; i < b1; ++i) {
+      s_cum[i] = excl;
+      excl += nsplit_of(s_ctx[i]) * NKV;
+    }
+    if (tid == kThreads - 1) s_cum[B] = excl;
+    __syncthreads();
+  }
+  const int U = s_cum[B];
+
+  // ------------------------------------------------- unit resolution (warp 0)
+  // Unit v into slot s: geometry from the lengths, then the block ids, the
+  // query rows and the step's K/V rows copied into the slot by cp.async.
+  auto resolve = [&](int s, int v) {
+    Unit u{};
+    if (v >= U) {
+      u.flags = kEnd;
+    } else {
+      int lo = 0, hi = B;  // s_cum[lo] <= v < s_cum[hi]
+      while (hi - lo > 1) {
+        const int mid = (lo + hi) >> 1;
+        if (s_cum[mid] <= v) lo = mid;
+        else hi = mid;
+      }
+      const int r = v - s_cum[lo];
+      u.seq = lo;
+      u.split = r / NKV;
+      u.kvh = r - u.split * NKV;
+      const int c = s_ctx[lo];
+      const bool bad = c < 0 || c > max_ctx || (P > 0 && c <= P);
+      const int own = bad ? 0 : c - P;
+      u.nsplit = nsplit_of(c);
+      const int n_t = (own + kTile - 1) / kTile;
+      u.t_begin = P + (u.split * n_t / u.nsplit) * kTile;
+      u.t_end = bad ? P : min(P + ((u.split + 1) * n_t / u.nsplit) * kTile, c);
+      u.first_blk = u.t_begin / T;
+      u.n_blk = (u.t_end - u.t_begin + T - 1) / T;
+      u.n_tiles = (u.t_end - u.t_begin + kTile - 1) / kTile;
+      u.bad = bad ? kBadLength : 0;
+      u.ctx = c;
+      const bool write = a.k_new != nullptr && !bad && c > 0 && u.split == u.nsplit - 1;
+      u.flags = kValid | (write ? kWrite : 0);
+      int32_t* tab = slot_tab(s);
+      const int32_t* src = a.tables + static_cast<size_t>(u.seq) * a.max_blocks + u.first_blk;
+      for (int i = lane; i < u.n_blk; i += 32) cp_async4(tab + i, src + i);
+      const raw* qsrc = static_cast<const raw*>(a.q) + (static_cast<size_t>(u.seq) * HQ + u.kvh * G) * D;
+      raw* qdst = slot_q(s);
+      for (int i = lane; i < G * D / 8; i += 32) cp_async16(qdst + 8 * i, qsrc + 8 * i);
+      if (write) {
+        const size_t row = (static_cast<size_t>(u.seq) * NKV + u.kvh) * D;
+        raw* ndst = slot_new(s);
+        for (int i = lane; i < 2 * D / 8; i += 32)
+          cp_async16(ndst + 8 * i, static_cast<const raw*>(i < D / 8 ? a.k_new : a.v_new) + row + 8 * (i % (D / 8)));
+      }
+    }
+    cp_async_commit();
+    if (lane == 0) s_unit[s] = u;
+    __syncwarp();
+  };
+
+  // ------------------------------------------------------- producer (warp 0)
+  int pu = 0, ptile = 0, issued = 0, pstarted = -1;  // warp 0's view
+  int released = 0;                                  // tiles consumed (all threads)
+  int cu = 0;                                        // unit being consumed (all threads)
+  bool dead = false;                                 // a stage wait gave up
+  auto issue = [&](int s, const Unit& u, int tile) {
+    const int st = issued % NS;
+    uint8_t* kt = ring + st * L_::kStage;
+    const int lb0 = tile * BPT;
+    const int blk = lane / 2, isv = lane & 1;
+    int phys = -1;
+    bool inb = false;
+    if (lane < BPB && lb0 + blk < u.n_blk) {
+      inb = true;
+      phys = slot_tab(s)[lb0 + blk];
+    }
+    const bool good = inb && phys >= 0 && phys < a.num_blocks;
+    const unsigned okmask = __ballot_sync(FULL, good);
+    const unsigned badmask = __ballot_sync(FULL, inb && !good);
+    const uint32_t bar = smem_u32(&s_bar[st]);
+    if (lane == 0) {
+      if (badmask) s_unit[s].bad |= kBadTable;
+      mbar_arrive_expect_tx(bar, __popc(okmask) * static_cast<uint32_t>(kBoxBytes));
+    }
+    __syncwarp();
+    if (good)
+      tma_box<KV, D>(smem_u32(kt + (isv ? G_::kTileBytes : 0) + blk * kBoxBytes), isv ? &vmap : &kmap,
+                     (phys * NKV + u.kvh) * T, bar);
+    ++issued;
+  };
+  // The step's token of the unit in slot s, written into the cache before any
+  // of the unit's tiles is fetched (the unit that holds position ctx - 1).
+  auto store_new = [&](int s, const Unit& u) {
+    const int p = u.ctx - 1;
+    const int blk = slot_tab(s)[p / T - u.first_blk];
+    if (blk >= 0 && blk < a.num_blocks) {
+      const size_t dst = ((static_cast<size_t>(blk) * NKV + u.kvh) * T + p % T) * D;
+      for (int i = lane; i < 2 * D / 8; i += 32) {
+        raw* cache = static_cast<raw*>(const_cast<void*>(i < D / 8 ? a.k_cache : a.v_cache));
+        *reinterpret_cast<uint4*>(cache + dst + 8 * (i % (D / 8))) =
+            *reinterpret_cast<const uint4*>(slot_new(s) + 8 * i);
+      }
+      asm volatile("fence.proxy.async.global;" ::: "memory");  // before the TMA reads it
+    }
+    __syncwarp();
+  };
+  // Issue tiles while a stage is free, in unit order, up to one unit ahead of
+  // the consumers (two slots).
+  auto pump = [&]() {
+    while (!dead && issued < released + NS && pu <= cu + 1) {
+      const int s = pu & 1;
+      const Unit u = s_unit[s];
+      if (u.flags & kEnd) break;
+      if (pstarted != pu) {  // the unit's copies have landed; its token is written first
+        cp_async_wait_all();
+        __syncwarp();
+        if (u.flags & kWrite) store_new(s, u);
+        pstarted = pu;
+      }
+      if (ptile < u.n_tiles) {
+        issue(s, s_unit[s], ptile);
+        ++ptile;
+      } else {
+        ++pu;
+        ptile = 0;
+      }
+    }
+  };
+
+  int next_v = 0;
+  if (warp == 0) {
+    int v0 = 0, v1 = 0;
+    if (lane == 0) {
+      v0 = atomicAdd(a.work, 1);
+      v1 = atomicAdd(a.work, 1);
+      next_v = atomicAdd(a.work, 1);
+    }
+    v0 = __shfl_sync(FULL, v0, 0);
+    v1 = __shfl_sync(FULL, v1, 0);
+    resolve(0, v0);
+    resolve(1, v1);
+    pump();
+  }
+
+  // q fragments (B operand of S^T = K q^T) and the running state of the
+  // current unit: per head (2 q4, 2 q4 + 1) its maximum and sum, identical in
+  // every warp; O^T for this warp's rows of head_dim
+  uint32_t qb[KS][2];
+  float m[2], l[2];
+  float o[MTW][4];
+
+  // ------------------------------------------------------- deferred counting
+  // Pending partials (seq, kvh, nsplit) are counted in; where a pair's last
+  // partial has arrived its partials are merged into the output.
+  auto flush = [&]() {
+    __threadfence();
+    if (tid == 0) s_nlast = 0;
+    __syncthreads();
+    const int nd = s_ndefer;
+    for (int i = tid; i < nd; i += kThreads) {
+      const int4 d = s_defer[i];
+      const int prev = atomicAdd(&a.counters[static_cast<size_t>(d.x) * NKV + d.y], 1);
+      if (prev == d.z + n_extra - 1) s_last[atomicAdd(&s_nlast, 1)] = i;
+    }
+    __syncthreads();
+    const int nl = s_nlast;
+    if (nl > 0) {
+      __threadfence();
+      for (int e = tid; e < nl * G * D; e += kThreads) {
+        const int4 d = s_defer[s_last[e / (G * D)]];
+        const int head = (e / D) % G, dd = e % D;
+        const int nsplit = d.z, np = nsplit + n_extra;
+        const size_t base = (static_cast<size_t>(d.x) * HQ + d.y * G + head) * a.max_splits;
+        auto slot = [&](int i) { return i < nsplit ? i : a.max_splits - n_extra + (i - nsplit); };
+        float M = -CUDART_INF_F;
+        for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(a.ws_m + base + slot(i)));
+        float Ls = 0.f, A = 0.f;
+        if (M != -CUDART_INF_F) {
+          for (int i = 0; i < np; ++i) {
+            const float f = exp2f(__ldcg(a.ws_m + base + slot(i)) - M);
+            Ls = fmaf(__ldcg(a.ws_l + base + slot(i)), f, Ls);
+            A = fmaf(__ldcg(a.ws_acc + (base + slot(i)) * D + dd), f, A);
+          }
+        } else {
+          for (int i = 0; i < np; ++i) Ls += __ldcg(a.ws_l + base + slot(i));
+        }
+        store_elem<Q>(a.out, (static_cast<size_t>(d.x) * HQ + d.y * G + head) * D + dd,
+                      (Ls > 0.f || Ls != Ls) ? A / Ls : 0.f);
+      }
+      __syncthreads();
+      for (int i = tid; i < nl; i += kThreads) {
+        const int4 d = s_defer[s_last[i]];
+        atomicExch(&a.counters[static_cast<size_t>(d.x) * NKV + d.y], 0);
+      }
+    }
+    __syncthreads();
+    if (tid == 0) s_ndefer = 0;
+    __syncthreads();
+  };
+
+  __syncthreads();
+  // ------------------------------------------------------------- consumers
+  for (;;) {
+    if (warp == 0) cp_async_wait_all();
+    __syncthreads();
+    const int s = cu & 1;
+    const Unit u = s_unit[s];
+    if (u.flags & kEnd) break;
+    {
+      const raw* qrows = slot_q(s);
+      load_qt<KV, Q, D>(qb, qrows, G, g, q4);
+    }
+    m[0] = m[1] = -CUDART_INF_F;
+    l[0] = l[1] = 0.f;
+#pragma unroll
+    for (int mt = 0; mt < MTW; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    const HeadScales sc = head_scales(a.head_scales, NKV, u.kvh, a.softmax_scale, a.qk_scale,
+                                      a.v_scale, a.k_inv, a.v_inv);
+
+    for (int tile = 0; tile < u.n_tiles && !dead; ++tile) {
+      const int st = released % NS;
+      const bool arrived = stage_wait(smem_u32(&s_bar[st]), (released / NS) & 1, a.wait_ns);
+      const uint8_t* kt = ring + st * L_::kStage;
+      uint8_t* vt = ring + st * L_::kStage + G_::kTileBytes;
+      const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+      const int row0 = warp * 16;
+      const int nvalid = min(16, u.t_end - (u.t_begin + tile * kTile + row0));
+      // S^T = K q^T for this warp's 16 tokens (rows) x 8 heads (columns)
+      float scr[4] = {0.f, 0.f, 0.f, 0.f};
+      if (arrived) {
+        const int r = row0 + (mi & 1) * 8 + li;
+#pragma unroll
+        for (int ks = 0; ks < KS; ++ks) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(kbase + swz<G_::kSlabs>(r, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
+          mma16816<kBf>(scr, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
+        }
+      }
+      float v0[2], v1[2], mx[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        v0[j] = g < nvalid ? scr[j] * sc.qk : -CUDART_INF_F;
+        v1[j] = g + 8 < nvalid ? scr[2 + j] * sc.qk : -CUDART_INF_F;
+        float x = fmaxf(v0[j], v1[j]);
+        x = fmaxf(x, __shfl_xor_sync(FULL, x, 4));
+        x = fmaxf(x, __shfl_xor_sync(FULL, x, 8));
+        x = fmaxf(x, __shfl_xor_sync(FULL, x, 16));
+        mx[j] = x;
+      }
+      if (g == 0) {
+        red_m[warp * 8 + 2 * q4] = mx[0];
+        red_m[warp * 8 + 2 * q4 + 1] = mx[1];
+      }
+      // V rows past the context end are zeroed (0 * NaN would poison P V)
+      const bool zero_rows = nvalid < 16;
+      if (zero_rows) {
+        const int nz = (16 - max(nvalid, 0)) * G_::kSlabs * 8;
+        for (int i = lane; i < nz; i += 32) {
+          const int rr = row0 + max(nvalid, 0) + i / (G_::kSlabs * 8);
+          const int c = i % (G_::kSlabs * 8);
+          *reinterpret_cast<uint4*>(vt + swz<G_::kSlabs>(rr, c)) = make_uint4(0, 0, 0, 0);
+        }
+      }
+      if (__syncthreads_or(!arrived)) {  // (A) maxima of all warps
+        dead = true;
+        break;
+      }
+      float corr[2], p0[2], p1[2], ps[2];
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float tm = red_m[2 * q4 + j];
+#pragma unroll
+        for (int w = 1; w < kWarps; ++w) tm = fmaxf(tm, red_m[w * 8 + 2 * q4 + j]);
+        const float mn = fmaxf(m[j], tm);
+        corr[j] = exp2f(m[j] - mn);
+        m[j] = mn;
+        p0[j] = exp2f(v0[j] - mn);
+        p1[j] = exp2f(v1[j] - mn);
+        float x = p0[j] + p1[j];
+        x += __shfl_xor_sync(FULL, x, 4);
+        x += __shfl_xor_sync(FULL, x, 8);
+        x += __shfl_xor_sync(FULL, x, 16);
+        ps[j] = x;
+      }
+      // P^T to shared memory: head-major, 64 tokens per head
+      {
+        raw* pp = s_p + (2 * q4) * kPStride + row0;
+        const uint32_t lo = pack2<kBf>(p0[0], p1[0]), hi = pack2<kBf>(p0[1], p1[1]);
+        pp[g] = *reinterpret_cast<const raw*>(&lo);
+        pp[g + 8] = reinterpret_cast<const raw*>(&lo)[1];
+        pp[kPStride + g] = *reinterpret_cast<const raw*>(&hi);
+        pp[kPStride + g + 8] = reinterpret_cast<const raw*>(&hi)[1];
+      }
+      if (g == 0) {
+        red_l[warp * 8 + 2 * q4] = ps[0];
+        red_l[warp * 8 + 2 * q4 + 1] = ps[1];
+      }
+      __syncthreads();  // (B) P^T and the sums of all warps
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        float t = 0.f;
+#pragma unroll
+        for (int w = 0; w < kWarps; ++w) t += red_l[w * 8 + 2 * q4 + j];
+        l[j] = l[j] * corr[j] + t;
+      }
+      if (corr[0] != 1.f || corr[1] != 1.f) {
+#pragma unroll
+        for (int mt = 0; mt < MTW; ++mt) {
+          o[mt][0] *= corr[0];
+          o[mt][1] *= corr[1];
+          o[mt][2] *= corr[0];
+          o[mt][3] *= corr[1];
+        }
+      }
+      // O^T (this warp's head_dim rows) += V^T P^T over the tile's 64 tokens
+#pragma unroll
+      for (int kk = 0; kk < kTile / 16; ++kk) {
+        const uint32_t* pw = reinterpret_cast<const uint32_t*>(s_p + g * kPStride + 16 * kk + 2 * q4);
+        const uint32_t b0 = pw[0], b1 = pw[4];
+        const int rv = 16 * kk + (mi >> 1) * 8 + li;
+#pragma unroll
+        for (int mt = 0; mt < MTW; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, 2 * (warp * MTW + mt) + (mi & 1)), a0, a1, a2, a3);
+          mma16816<kBf>(o[mt], a0, a1, a2, a3, b0, b1);
+        }
+      }
+      if (zero_rows) fence_proxy_async();  // the zeroed rows, before TMA refills the stage
+      __syncthreads();  // (C) the stage and P^T are free
+      ++released;
+      if (warp == 0) pump();
+    }
+
+    if (dead) {
+      // drain the copies still in flight before anything else touches the
+      // ring; from now on no tile is issued or waited for
+      if (warp == 0) {
+        if (lane == 0)
+          for (int t = released; t < issued; ++t)
+            mbar_wait(smem_u32(&s_bar[t % NS]), (t / NS) & 1, kDrainNs);
+        released = issued;
+        // a unit taken but never started still writes its token
+        if (pstarted < cu && (u.flags & kWrite)) {
+          cp_async_wait_all();
+          __syncwarp();
+          store_new(s, u);
+          pstarted = cu;
+        }
+      }
+      __syncthreads();
+    }
+
+    // ---------------------------------------------------- finish the unit
+    const int bad = u.bad | s_unit[s].bad | (dead ? kTimeout : 0);
+    const bool direct = u.nsplit == 1 && P == 0;
+    const size_t head0 = static_cast<size_t>(u.seq) * HQ + static_cast<size_t>(u.kvh) * G;
+#pragma unroll
+    for (int mt = 0; mt < MTW; ++mt)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const int head = 2 * q4 + (e & 1);
+        const int d = 16 * (warp * MTW + mt) + g + 8 * (e >> 1);
+        if (head >= G) continue;
+        const float lj = l[e & 1];
+        if (direct) {
+          store_elem<Q>(a.out, (head0 + head) * D + d,
+                        bad ? CUDART_NAN_F : (lj > 0.f ? o[mt][e] * sc.v / lj : 0.f));
+        } else {
+          a.ws_acc[((head0 + head) * a.max_splits + u.split) * D + d] = bad ? CUDART_NAN_F : o[mt][e] * sc.v;
+        }
+      }
+    if (!direct && warp == 0 && g == 0) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) {
+        const int head = 2 * q4 + j;
+        if (head < G) {
+          const size_t pidx = (head0 + head) * a.max_splits + u.split;
+          a.ws_m[pidx] = m[j];
+          a.ws_l[pidx] = bad ? CUDART_NAN_F : l[j];
+        }
+      }
+    }
+    if (tid == 0) {
+      if (bad && a.status != nullptr) atomicOr(a.status, bad);
+      if (!direct) s_defer[s_ndefer++] = make_int4(u.seq, u.kvh, u.nsplit, u.split);
+    }
+    // the slot is free: resolve the unit after next into it
+    __syncthreads();
+    if (warp == 0) {
+      int v = next_v;
+      if (lane == 0) next_v = atomicAdd(a.work, 1);
+      v = __shfl_sync(FULL, v, 0);
+      resolve(s, v);
+    }
+    ++cu;
+    if (warp == 0) pump();
+    if (s_ndefer >= kDefer) flush();
+  }
+
+  // -------------------------------------------------------------- finish
+  flush();
+  if (tid == 0) {
+    const int total = static_cast<int>(gridDim.x);
+    if (atomicAdd(a.done, 1) == total - 1) {
+      // the last CTA: the shared-prefix pass (if any) is complete before
+      // this grid is, and the queue counter starts from 0 next call
+      if (P > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+      atomicExch(a.work, 0);
+      atomicExch(a.done, 0);
+    }
+  }
+}
+
+}  // namespace pd
+}  // namespace tc
+}  // namespace pkv

@@ -366,12 +366,13 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   extern __shared__ uint8_t smem_raw[];
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
-  int j, s, qp_rev, kbeg = 0;
+  int j, s, qp_rev, kbeg = 0, seq0 = 0;
   if constexpr (kCasc) {
     j = blockIdx.z * a.group;   // first query head of the KV head
     s = 0;                      // the shared blocks are read through table row 0
-    qp_rev = -1 - static_cast<int>(blockIdx.x);
+    qp_rev = -1;                // one pair of query tiles: rows seq * G + head of this CTA's sequences
     kbeg = blockIdx.y * a.sp_split;
+    seq0 = blockIdx.x * a.sp_seqs;
   } else if (a.ranked) {
     int pair = 0;
     j = blockIdx.x;
@@ -387,7 +388,7 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   // keys: positions [kbeg, ctx) (prefill: 0 .. ctx - 1, causal)
   const int ctx = kCasc ? min(a.sp_tokens, kbeg + a.sp_split) : a.ctx_lens[s];
   const int q0 = kCasc ? 0 : a.query_start[s];
-  const int n = kCasc ? a.sp_rows : a.query_start[s + 1] - q0;
+  const int n = kCasc ? min(a.sp_seqs, a.num_seqs - seq0) * a.group : a.query_start[s + 1] - q0;
   if (q0 < 0 || n <= 0 || q0 + n > a.total_q) return;  // no rows this CTA may write
   const int ntq = (n + kRows - 1) / kRows;       // query tiles of the chunk
   const int npairs = (ntq + 1) / 2;
@@ -437,6 +438,7 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(wide_free + 2);
   __shared__ int s_bad;      // PKV_DEVICE_* bits (atomicOr: several warps may set them)
   __shared__ int s_issued;   // key tiles the producer has issued
+  __shared__ uint8_t s_pbad[kCasc ? 256 : 1];  // shared-prefix pass: sequence breaks the declaration
 
   if (tid == 0) {
     s_bad = 0;
@@ -470,15 +472,19 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
     const int cr = r_begin[X] + r;
     const bool in = cr < n && (X == 0 || hasB);
     // query row: chunk row cr of head j, or (shared-prefix pass) head
-    // j + cr % G of sequence cr / G
-    const size_t qrow = kCasc ? static_cast<size_t>(cr / a.group) * HQ + j + cr % a.group
+    // j + cr % G of sequence seq0 + cr / G
+    const size_t qrow = kCasc ? static_cast<size_t>(seq0 + cr / a.group) * HQ + j + cr % a.group
                               : static_cast<size_t>(q0 + cr) * HQ + j;
     const uint4* src = reinterpret_cast<const uint4*>(static_cast<const typename Q::raw*>(a.q) +
                                                       qrow * D);
     uint8_t* qx = q_s + X * kQBytes;
+    // all 16 loads first (one round trip), then the shared-memory stores
+    uint4 qv[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) qv[c] = in ? __ldg(src + c) : make_uint4(0, 0, 0, 0);
 #pragma unroll
     for (int c = 0; c < 16; ++c) {
-      uint4 v = in ? src[c] : make_uint4(0, 0, 0, 0);
+      uint4 v = qv[c];
       if constexpr (kFp8 && kOutBf) {  // the MMA is f16 (the widened E4M3): q to f16
         float f[8];
         LoadF32<Q, 8>::run(reinterpret_cast<const typename Q::raw*>(&v), f);
@@ -488,6 +494,18 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
       *reinterpret_cast<uint4*>(qx + (c >> 3) * (kRows * 128) + sw(r, c & 7)) = v;
     }
     fence_proxy_async();
+  }
+  if constexpr (kCasc) {
+    // the first key range of each KV head checks that its sequences' tables
+    // start with the shared blocks (row 0's, which this pass reads for all)
+    const int nseq = n / a.group, nb = a.sp_tokens / T;
+    for (int i = tid; i < nseq; i += kNT) s_pbad[i] = 0;
+    __syncthreads();
+    if (blockIdx.y == 0)
+      for (int e = tid; e < nseq * nb; e += kNT) {
+        const int sq = seq0 + e / nb, b = e % nb;
+        if (a.tables[static_cast<size_t>(sq) * a.max_blocks + b] != a.tables[b]) s_pbad[e / nb] = 1;
+      }
   }
   tc_fence_before();
   __syncthreads();
@@ -763,11 +781,17 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
       ok = __all_sync(FULL, ok && mbar_wait(smem_u32(&o_done[2 * X + (tl & 1)]), (tl >> 1) & 1, kWaitNs));
       tc_fence_after();
       if (!ok) atomicOr(&s_bad, kTimeout);
-      const bool bad = !ok || *reinterpret_cast<volatile int*>(&s_bad) != 0;
       const bool row_in = cr < r_end[X];
+      bool bad = !ok || *reinterpret_cast<volatile int*>(&s_bad) != 0;
       if constexpr (kCasc) {
-        const size_t pidx = (static_cast<size_t>(cr / a.group) * HQ + j + cr % a.group) * a.max_splits +
-                            a.sp_slot0 + blockIdx.y;
+        if (row_in && s_pbad[cr / a.group]) {
+          bad = true;
+          if (a.status != nullptr) atomicOr(a.status, kBadPrefix);
+        }
+      }
+      if constexpr (kCasc) {
+        const size_t pidx = (static_cast<size_t>(seq0 + cr / a.group) * HQ + j + cr % a.group) *
+                                a.max_splits + a.sp_slot0 + blockIdx.y;
         float* acc = a.ws_acc + pidx * D;
 #pragma unroll 1
         for (int c = 0; c < D; c += 32) {
@@ -811,6 +835,8 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
 
   // ---------------------------------------------------------------- exit
   // every UMMA done and every copy landed before TMEM and shared memory go
+  // (shared-prefix pass: the partials written, before they are counted in)
+  if constexpr (kCasc) __threadfence();
   __syncthreads();
   if (tid == 0) {
     mbar_wait(smem_u32(fin), 0, kDrainNs);
@@ -828,6 +854,59 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   if (warp == kProd) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
+  }
+  if constexpr (kCasc) {
+    // Count this CTA's partials in on each of its (sequence, KV head) pairs;
+    // the last of a pair's partials to arrive (the decode kernel's splits of
+    // the positions past the prefix, and the key ranges of this pass) merges
+    // them.  The split count is the decode kernel's, from the same length.
+    __shared__ int s_merge[256];
+    __shared__ int s_nmerge;
+    const int kvh_c = blockIdx.z;
+    if (tid == 0) s_nmerge = 0;
+    __syncthreads();
+    const int nseq = min(a.sp_seqs, a.num_seqs - seq0);
+    for (int i = tid; i < nseq; i += kNT) {
+      const int sq = seq0 + i;
+      const int c = a.ctx_lens[sq];
+      const bool bad_c = c < 0 || c > a.max_blocks * T || c <= a.sp_tokens;
+      const int nsplit = bad_c ? 1 : max(1, (c - a.sp_tokens + a.partition - 1) / a.partition);
+      const int prev = atomicAdd(&a.counters[static_cast<size_t>(sq) * a.num_kv_heads + kvh_c], 1);
+      if (prev == nsplit + static_cast<int>(gridDim.y) - 1) s_merge[atomicAdd(&s_nmerge, 1)] = sq;
+    }
+    __syncthreads();
+    const int nm = s_nmerge;
+    if (nm > 0) {
+      __threadfence();
+      const int G = a.group;
+      for (int e = tid; e < nm * G * D; e += kNT) {
+        const int sq = s_merge[e / (G * D)];
+        const int row = (e / D) % G, d = e % D;
+        const int c = a.ctx_lens[sq];
+        const bool bad_c = c < 0 || c > a.max_blocks * T || c <= a.sp_tokens;
+        const int nsplit = bad_c ? 1 : max(1, (c - a.sp_tokens + a.partition - 1) / a.partition);
+        const int np = nsplit + static_cast<int>(gridDim.y);
+        const size_t base = (static_cast<size_t>(sq) * HQ + j + row) * a.max_splits;
+        auto slot = [&](int i) { return i < nsplit ? i : a.sp_slot0 + (i - nsplit); };
+        float M = -CUDART_INF_F;
+        for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(a.ws_m + base + slot(i)));
+        float L = 0.f, A = 0.f;
+        if (M != -CUDART_INF_F) {
+          for (int i = 0; i < np; ++i) {
+            const float f = exp2f(__ldcg(a.ws_m + base + slot(i)) - M);
+            L = fmaf(__ldcg(a.ws_l + base + slot(i)), f, L);
+            A = fmaf(__ldcg(a.ws_acc + (base + slot(i)) * D + d), f, A);
+          }
+        } else {
+          for (int i = 0; i < np; ++i) L += __ldcg(a.ws_l + base + slot(i));
+        }
+        store_elem<Q>(a.out, (static_cast<size_t>(sq) * HQ + j + row) * D + d,
+                      (L > 0.f || L != L) ? A / L : 0.f);
+      }
+      __syncthreads();
+      for (int i = tid; i < nm; i += kNT)
+        atomicExch(&a.counters[static_cast<size_t>(s_merge[i]) * a.num_kv_heads + kvh_c], 0);
+    }
   }
 }
 

@@ -1,6 +1,6 @@
 // Launch of the shared-prefix pass: the tcgen05 attention pipeline of
 // attention_prefill_umma.cuh in its shared-prefix form (kCasc), one CTA per
-// (pair of 128-row query tiles, key range, KV head).
+// (group of whole sequences filling up to 256 query rows, key range, KV head).
 #include <atomic>
 
 #include "attention_prefill_umma.cuh"
@@ -25,10 +25,10 @@ pkv_status launch_shared_prefix_pass(const PrefillArgs& a, int block_size, int k
     if (e != cudaSuccess) return cuda_fail("shared-prefix pass: cudaFuncSetAttribute", e);
     done.fetch_or(bit);
   }
-  const int rows = a.sp_rows;
-  const int pairs = (rows + 2 * tc::umma::kRows - 1) / (2 * tc::umma::kRows);
+  // each CTA: sp_seqs whole sequences (all their query heads of one KV head)
+  const int groups = (a.num_seqs + a.sp_seqs - 1) / a.sp_seqs;
   cudaLaunchConfig_t cfg{};
-  cfg.gridDim = dim3(pairs, key_splits, a.num_kv_heads);
+  cfg.gridDim = dim3(groups, key_splits, a.num_kv_heads);
   cfg.blockDim = dim3(tc::umma::threads<KV>());
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;

@@ -765,22 +765,36 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   // second split, so that the short last splits of long pairs come last
   const int kvh = blockIdx.x, seq = blockIdx.y, split = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-  // Positions [0, P) were attended by the shared-prefix pass (P = 0: none);
+  // Positions [0, P) are attended by the shared-prefix pass (P = 0: none);
   // this CTA covers part of [P, ctx).
   const int P = a.prefix_tokens;
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: nothing that kernel may write is read before it has completed.
-  // Behind the shared-prefix pass (which waited for every kernel before it
-  // before letting this grid start), the pass's partials are the only such
-  // data, and the wait moves to the merge that reads them.
+  // Behind the shared-prefix pass, which waits for every kernel before it
+  // before it lets this grid start, nothing is waited for: the pass's
+  // partials meet this grid's through the arrival counters (whoever comes
+  // last merges), and the last CTA of this grid to finish waits for the
+  // pass, so that the grid never completes before it.
   if (P == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  auto finish = [&]() {
+    if (P > 0 && threadIdx.x == 0) {
+      const int total = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
+      if (atomicAdd(a.done, 1) == total - 1) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        atomicExch(a.done, 0);
+      }
+    }
+  };
   const int g = lane >> 2, q4 = lane & 3;
   const int G = a.group;
   const int ctx = a.ctx_lens[seq];
   const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T || (P > 0 && ctx <= P);
   const int own = bad_ctx ? 0 : ctx - P;  // positions this kernel attends
   const int nsplit = bad_ctx ? 1 : max(1, (own + a.partition - 1) / a.partition);
-  if (split >= nsplit) return;
+  if (split >= nsplit) {
+    finish();
+    return;
+  }
   const HeadScales sc = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale,
                                     a.qk_scale, a.v_scale, a.k_inv, a.v_inv);
   // The pair's n_t tiles are shared out evenly: split i takes tiles
@@ -812,12 +826,6 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   }
   for (int i = tid; i < n_blk; i += kThreads)
     s_tab[i] = a.tables[static_cast<size_t>(seq) * a.max_blocks + first_blk + i];
-  // With a shared prefix, split 0 checks that this row maps the prefix
-  // blocks of row 0 (which the prefix pass read for every row).
-  bool prefix_mismatch = false;
-  if (P > 0 && split == 0 && !bad_ctx)
-    for (int i = tid; i < P / T; i += kThreads)
-      prefix_mismatch |= a.tables[static_cast<size_t>(seq) * a.max_blocks + i] != a.tables[i];
 
   // Fused slot write: the split holding position ctx - 1 stores the step's
   // token of its KV head before any copy is issued (a block never spans two
@@ -843,7 +851,7 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
     if constexpr (HC) load_qt<KV, Q, D>(qa, qrows, G, g, q4);
     else load_q<KV, Q, D>(qa, qrows, G, g, q4);
   }
-  const bool prefix_bad = __syncthreads_or(prefix_mismatch);
+  __syncthreads();
 
   // ---------------------------------------------------------- producer
   // Warp 0 refills a stage with one warp instruction: lane l issues box l
@@ -925,7 +933,7 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   else publish<KV, D>(st, mS, lS, oS, warp, G, 16, lane);
   __syncthreads();
 
-  const int bad_bits = s_bad | (prefix_bad ? kBadPrefix : 0);
+  const int bad_bits = s_bad;
   if (tid == 0 && bad_bits != 0 && a.status != nullptr) atomicOr(a.status, bad_bits);
   const bool any_bad = bad_bits != 0;
   // A lone split writes the output unless a shared-prefix partial joins it.
@@ -953,24 +961,25 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
 
   // ------------------------------------------- split-K: the last CTA merges
   // Each CTA counts itself in (an atomic counter, never a wait); the last of
-  // the pair's splits to finish combines all partials (and the shared-prefix
-  // pass's) and resets the counter.
+  // the pair's partials to arrive (its splits and, with a shared prefix, the
+  // prefix pass's key ranges) combines them all and resets the counter.
   __threadfence();
   __syncthreads();
-  if (nsplit > 1) {
-    if (tid == 0) {
-      const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
-      s_last = prev == nsplit - 1;
-    }
-    __syncthreads();
-    if (!s_last) return;
-    __threadfence();
+  const int n_extra = P > 0 ? a.prefix_splits : 0;
+  if (tid == 0) {
+    const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
+    s_last = prev == nsplit + n_extra - 1;
   }
-  // the shared-prefix pass's partials: written by the preceding grid
-  if (P > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-  merge_splits<Q, D>(a, head0, nsplit, a.max_splits - a.prefix_splits, P > 0 ? a.prefix_splits : 0,
+  __syncthreads();
+  if (!s_last) {
+    finish();
+    return;
+  }
+  __threadfence();
+  merge_splits<Q, D>(a, head0, nsplit, a.max_splits - a.prefix_splits, n_extra,
                      reinterpret_cast<float*>(smem), NS * G_::kStageBytes / 4);
-  if (nsplit > 1 && tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
+  if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
+  finish();
 }
 
 template <typename KV, int D, int NS>

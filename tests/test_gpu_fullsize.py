@@ -44,9 +44,11 @@ def test_full_size_sampled(name):
     dev.write_step()
     outs = {}
     try:
-        for k in ("simt", "tc") if w.kv_dtype != "f32" else ("simt",):
-            pkv.pkv_set_attention_kernel(k)
-            outs[k] = dev.attend().double().cpu().numpy().copy()
+        for k in ("simt", "tc", "persistent") if w.kv_dtype != "f32" else ("simt",):
+            pkv.pkv_set_attention_kernel(k)   # the workspace size follows the kernel choice
+            ws = pkv.workspace_for(len(dev.plan.seq_ids), w.num_q_heads, dev.plan.max_blocks, dev.desc,
+                                   dev.partition)
+            outs[k] = dev.attend(workspace=ws).double().cpu().numpy().copy()
     finally:
         pkv.pkv_set_attention_kernel("auto")
     torch.cuda.synchronize()
