@@ -274,7 +274,9 @@ PKV_API size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_hea
  * 512 sequences, partitions of at most 128 blocks; the split kernel
  * otherwise), whose automatic partition is one split per pair up to 1,024
  * tokens of context and 512 tokens beyond.  The workspace-size calls follow
- * the current choice.  All kernels compute the same result within rounding. */
+ * the current choice; a call given a workspace smaller than the persistent
+ * kernel's (or none) runs the split kernel.  All kernels compute the same
+ * result within rounding. */
 #define PKV_KERNEL_AUTO 0
 #define PKV_KERNEL_SIMT 1
 #define PKV_KERNEL_TENSOR_CORE 2

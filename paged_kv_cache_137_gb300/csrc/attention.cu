@@ -242,7 +242,7 @@ struct CallPlan {
 };
 pkv_status plan_call(const pkv_kv_desc* d, int q_dtype, float softmax_scale, int32_t num_seqs,
                      int32_t num_q_heads, int32_t max_blocks, int32_t partition_tokens,
-                     int32_t prefix_blocks, CallPlan* out) {
+                     int32_t prefix_blocks, CallPlan* out, bool allow_pd = true) {
   CallPlan c;
   const int group = num_q_heads / d->num_kv_heads;
   const int choice = g_kernel_choice.load();
@@ -253,7 +253,8 @@ pkv_status plan_call(const pkv_kv_desc* d, int q_dtype, float softmax_scale, int
     c.pp = prefix_plan(num_seqs, group, d->num_kv_heads, static_cast<int64_t>(prefix_blocks) * d->block_size);
   const int64_t max_ctx = static_cast<int64_t>(max_blocks) * d->block_size - c.pp.tokens;
   // the persistent kernel: when chosen, and for the tails behind a prefix pass
-  const bool want_pd = choice == PKV_KERNEL_PERSISTENT || (c.prefix_pass && choice == PKV_KERNEL_AUTO);
+  const bool want_pd =
+      allow_pd && (choice == PKV_KERNEL_PERSISTENT || (c.prefix_pass && choice == PKV_KERNEL_AUTO));
   if (want_pd) {
     int32_t p = partition_tokens;
     if (p < 0) return fail(PKV_ERR_INVALID_ARG, "partition_tokens is negative");
@@ -428,6 +429,12 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   st = plan_call(desc, q_dtype, softmax_scale, num_seqs, num_q_heads, max_blocks, partition_tokens,
                  prefix_blocks, &plan);
   if (st != PKV_OK) return st;
+  if (plan.pd && (workspace == nullptr || workspace_bytes < plan.ws.bytes)) {
+    // a workspace sized for the split kernel: run that
+    st = plan_call(desc, q_dtype, softmax_scale, num_seqs, num_q_heads, max_blocks, partition_tokens,
+                   prefix_blocks, &plan, false);
+    if (st != PKV_OK) return st;
+  }
   const bool prefix_pass = plan.prefix_pass;
   const PrefixPlan pp = plan.pp;
   const int32_t partition = plan.partition;

@@ -82,8 +82,8 @@ struct Layout {
   static constexpr int cum = ctx + kMaxSeqs * 4;            // int32 [kMaxSeqs + 1], padded
   static constexpr int units = cum + (kMaxSeqs + 4) * 4;    // Unit [2]
   static constexpr int defer = units + 2 * static_cast<int>(sizeof(Unit));  // int4 [kDefer]
-  static constexpr int bars = defer + kDefer * 16;          // uint64 [stages]
-  static constexpr int bytes = bars + stages<KV, D>() * 8 + 1024;  // + base alignment
+  static constexpr int bars = defer + kDefer * 16;          // uint64 [stages], then [2] slot ready
+  static constexpr int bytes = bars + (stages<KV, D>() + 2) * 8 + 1024;  // + base alignment
 };
 
 __device__ __forceinline__ void cp_async4(void* dst, const void* src) {
@@ -94,6 +94,11 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 }
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_all;" ::: "memory"); }
+// The mbarrier at bar counts one arrival from this thread once all its
+// cp.async copies issued so far have landed.
+__device__ __forceinline__ void cp_async_arrive(uint32_t bar) {
+  asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
 
 template <typename KV, typename Q, int D, int T>
 __global__ void __launch_bounds__(kThreads, kCtasPerSm)
@@ -139,6 +144,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   Unit* s_unit = reinterpret_cast<Unit*>(smem + L_::units);
   int4* s_defer = reinterpret_cast<int4*>(smem + L_::defer);
   uint64_t* s_bar = reinterpret_cast<uint64_t*>(smem + L_::bars);
+  uint64_t* s_ready = s_bar + NS;  // per slot: the resolved unit's copies have landed (32 arrivals)
   auto slot_tab = [&](int s) { return reinterpret_cast<int32_t*>(smem + L_::slots + s * L_::kSlot); };
   auto slot_q = [&](int s) {
     return reinterpret_cast<raw*>(smem + L_::slots + s * L_::kSlot + L_::kSlotTab);
@@ -158,6 +164,7 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   };
   if (tid == 0) {
     for (int s = 0; s < NS; ++s) mbar_init(smem_u32(&s_bar[s]), 1);
+    for (int s = 0; s < 2; ++s) mbar_init(smem_u32(&s_ready[s]), 32);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     s_ndefer = 0;
   }
@@ -234,10 +241,12 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           cp_async16(ndst + 8 * i, static_cast<const raw*>(i < D / 8 ? a.k_new : a.v_new) + row + 8 * (i % (D / 8)));
       }
     }
-    cp_async_commit();
+    cp_async_arrive(smem_u32(&s_ready[s]));  // every lane: once its copies have landed
     if (lane == 0) s_unit[s] = u;
     __syncwarp();
   };
+  // Unit k is in slot k & 1, the ((k >> 1) + 1)-th use of that slot.
+  auto ready_parity = [](int k) { return static_cast<uint32_t>((k >> 1) & 1); };
 
   // ------------------------------------------------------- producer (warp 0)
   int pu = 0, ptile = 0, issued = 0, pstarted = -1;  // warp 0's view
@@ -292,9 +301,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const int s = pu & 1;
       const Unit u = s_unit[s];
       if (u.flags & kEnd) break;
-      if (pstarted != pu) {  // the unit's copies have landed; its token is written first
-        cp_async_wait_all();
-        __syncwarp();
+      if (pstarted != pu) {  // the unit's copies must have landed; its token is written first
+        if (!__all_sync(FULL, mbar_try_wait(smem_u32(&s_ready[s]), ready_parity(pu)))) break;
         if (u.flags & kWrite) store_new(s, u);
         pstarted = pu;
       }
@@ -382,11 +390,15 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   __syncthreads();
   // ------------------------------------------------------------- consumers
   for (;;) {
-    if (warp == 0) cp_async_wait_all();
     __syncthreads();
     const int s = cu & 1;
     const Unit u = s_unit[s];
     if (u.flags & kEnd) break;
+    // this unit's copies (tables, queries, new token); then the producer can
+    // start it if it has not yet
+    if (!mbar_wait(smem_u32(&s_ready[s]), ready_parity(cu), kDrainNs)) dead = true;
+    if (__syncthreads_or(dead)) dead = true;
+    if (warp == 0) pump();
     {
       const raw* qrows = slot_q(s);
       load_qt<KV, Q, D>(qb, qrows, G, g, q4);
@@ -520,7 +532,8 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
           for (int t = released; t < issued; ++t)
             mbar_wait(smem_u32(&s_bar[t % NS]), (t / NS) & 1, kDrainNs);
         released = issued;
-        // a unit taken but never started still writes its token
+        // a unit taken but never started still writes its token (its copies
+        // have landed or the wait for them gave up)
         if (pstarted < cu && (u.flags & kWrite)) {
           cp_async_wait_all();
           __syncwarp();

@@ -2,6 +2,7 @@
 // per-dtype instantiation units).
 #pragma once
 
+#include <algorithm>
 #include <atomic>
 #include <utility>
 
@@ -51,6 +52,9 @@ pkv_status launch_form(const DecodeArgs& a, const CUtensorMap& kmap, const CUten
   const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
   if (!bit || !(configured.load() & bit)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaFuncSetAttribute", e);
     configured.fetch_or(bit);
   }
@@ -76,22 +80,28 @@ pkv_status launch_pd_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUte
   constexpr int smem = pd::Layout<KV, D>::bytes;
   auto kernel = pd::decode_pd_kernel<KV, Q, D, T>;
   static std::atomic<uint64_t> configured{0};
-  static std::atomic<int> sms[64];
+  static std::atomic<int> ctas[64];   // resident CTAs of the whole device
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaGetDevice", e);
   const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
   if (!bit || !(configured.load() & bit)) {
     e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+    // all of the unified L1 / shared storage as shared memory: two CTAs per SM
+    if (e == cudaSuccess)
+      e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                               cudaSharedmemCarveoutMaxShared);
     if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaFuncSetAttribute", e);
-    int n = 0;
+    int n = 0, occ = 0;
     e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: SM count", e);
-    if (dev < 64) sms[dev].store(n);
+    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem);
+    if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: persistent occupancy", e);
+    if (occ < 1) return fail(PKV_ERR_UNSUPPORTED, "persistent kernel: no CTA fits on an SM");
+    if (dev < 64) ctas[dev].store(n * std::min(occ, pd::kCtasPerSm));
     configured.fetch_or(bit);
   }
-  const int n_sm = dev < 64 ? sms[dev].load() : 152;
-  e = launch_dependent(kernel, dim3(n_sm * pd::kCtasPerSm), kThreads, smem, st, a, kmap, vmap);
+  const int grid = dev < 64 ? ctas[dev].load() : 152 * pd::kCtasPerSm;
+  e = launch_dependent(kernel, dim3(grid), kThreads, smem, st, a, kmap, vmap);
   if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: persistent launch", e);
   return check_launch("pkv_attention_decode (persistent)");
 }

@@ -46,8 +46,13 @@ def test_full_size_sampled(name):
     try:
         for k in ("simt", "tc", "persistent") if w.kv_dtype != "f32" else ("simt",):
             pkv.pkv_set_attention_kernel(k)   # the workspace size follows the kernel choice
-            ws = pkv.workspace_for(len(dev.plan.seq_ids), w.num_q_heads, dev.plan.max_blocks, dev.desc,
-                                   dev.partition)
+            if dev.prefix_blocks:
+                ws = pkv.shared_prefix_workspace_for(len(dev.plan.seq_ids), w.num_q_heads,
+                                                     dev.plan.max_blocks, dev.desc, dev.prefix_blocks,
+                                                     dev.partition)
+            else:
+                ws = pkv.workspace_for(len(dev.plan.seq_ids), w.num_q_heads, dev.plan.max_blocks,
+                                       dev.desc, dev.partition)
             outs[k] = dev.attend(workspace=ws).double().cpu().numpy().copy()
     finally:
         pkv.pkv_set_attention_kernel("auto")

@@ -165,8 +165,9 @@ def test_shared_prefix_equals_private_copies_bitwise(kernel):
             put(s, *tails[s])
         tables, ctx = pool.block_tables([0, 1], 4)
         out = torch.empty_like(q)
+        ws = pkv.workspace_for(2, 4, 4, desc)   # sized for the kernel chosen
         pkv.pkv_attention_decode(out, q, kc, vc, torch.from_numpy(tables).cuda(),
-                                 torch.from_numpy(ctx).cuda(), desc, 1 / math.sqrt(128))
+                                 torch.from_numpy(ctx).cuda(), desc, 1 / math.sqrt(128), workspace=ws)
         torch.cuda.synchronize()
         outs.append(out.view(torch.int16).cpu())
     assert torch.equal(outs[0], outs[1])
@@ -189,7 +190,7 @@ def test_single_token_context_returns_its_value_exactly(kernel):
     desc, kc, vc, k, v, q, tables = _single_block_case(1)
     out = torch.empty_like(q)
     pkv.pkv_attention_decode(out, q, kc, vc, tables, torch.tensor([1], dtype=torch.int32).cuda(),
-                             desc, 0.1)
+                             desc, 0.1, workspace=pkv.workspace_for(1, 4, 2, desc))
     torch.cuda.synchronize()
     expect = v[0].repeat_interleave(2, dim=0)  # heads 0,1 -> kv 0; 2,3 -> kv 1
     assert torch.equal(out[0].cpu(), expect)
@@ -199,11 +200,11 @@ def test_zero_context_gives_zero_and_poison_is_never_read(kernel):
     desc, kc, vc, k, v, q, tables = _single_block_case(5)
     out = torch.full_like(q, 7.0)
     pkv.pkv_attention_decode(out, q, kc, vc, tables, torch.tensor([0], dtype=torch.int32).cuda(),
-                             desc, 0.1)
+                             desc, 0.1, workspace=pkv.workspace_for(1, 4, 2, desc))
     torch.cuda.synchronize()
     assert torch.equal(out.cpu(), torch.zeros_like(out.cpu()))
     pkv.pkv_attention_decode(out, q, kc, vc, tables, torch.tensor([5], dtype=torch.int32).cuda(),
-                             desc, 0.1)
+                             desc, 0.1, workspace=pkv.workspace_for(1, 4, 2, desc))
     torch.cuda.synchronize()
     assert not torch.isnan(out).any()   # slots 5..15 of the block hold NaN bits
 
@@ -215,19 +216,20 @@ def test_invalid_table_entry_or_length_gives_nan(kernel):
     pkv.pkv_device_status(clear=True)
     out = torch.zeros_like(q)
     bad = torch.tensor([[3, 99]], dtype=torch.int32).cuda()   # 99 >= num_blocks
-    pkv.pkv_attention_decode(out, q, kc, vc, bad, torch.tensor([20], dtype=torch.int32).cuda(), desc, 0.1)
+    pkv.pkv_attention_decode(out, q, kc, vc, bad, torch.tensor([20], dtype=torch.int32).cuda(), desc, 0.1,
+                             workspace=pkv.workspace_for(1, 4, 2, desc))
     torch.cuda.synchronize()
     assert torch.isnan(out).all()
     assert pkv.pkv_device_status(clear=True) == pkv.PKV_DEVICE_BAD_TABLE
     out.zero_()
     pkv.pkv_attention_decode(out, q, kc, vc, tables, torch.tensor([33], dtype=torch.int32).cuda(),
-                             desc, 0.1)   # longer than 2 blocks
+                             desc, 0.1, workspace=pkv.workspace_for(1, 4, 2, desc))   # longer than 2 blocks
     torch.cuda.synchronize()
     assert torch.isnan(out).all()
     assert pkv.pkv_device_status(clear=True) == pkv.PKV_DEVICE_BAD_LENGTH
     # valid inputs leave the word clear
     pkv.pkv_attention_decode(out, q, kc, vc, tables, torch.tensor([16], dtype=torch.int32).cuda(),
-                             desc, 0.1)
+                             desc, 0.1, workspace=pkv.workspace_for(1, 4, 2, desc))
     assert pkv.pkv_device_status() == 0
     assert not torch.isnan(out).any()
 
