@@ -191,10 +191,11 @@ def attention_kernels(kernel: str, w, splits: int, shared_prefix: bool = False) 
     if w.kv_dtype == "f32" or kernel == "simt":
         k = "decode_simt_kernel"
         return k + (" + merge_kernel" if splits > 1 else "")
-    if shared_prefix:
-        return "prefill_umma_kernel<shared prefix> + decode_pd_kernel (persistent; merges fused)"
     if kernel == "persistent":
-        return "decode_pd_kernel (persistent; merges fused)"
+        return (("prefill_umma_kernel<shared prefix> + " if shared_prefix else "")
+                + "decode_pd_kernel (persistent; merges fused)")
+    if shared_prefix:
+        return "prefill_umma_kernel<shared prefix> + decode_tc_kernel (merges fused)"
     return "decode_tc_kernel (split-K merge fused)"
 
 

@@ -265,13 +265,12 @@ PKV_API size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_hea
  * CTA per (KV head, sequence, split), split-K merge fused) for 16-bit and
  * E4M3 caches with head_dim 128 (16-bit also 64), groups of up to 16 query
  * heads and partitions of at most 1024 blocks, and the CUDA-core kernel
- * otherwise; behind a shared-prefix pass it uses the persistent kernel where
- * that covers the shape.  SIMT forces the CUDA-core kernel; TENSOR_CORE makes
+ * otherwise.  SIMT forces the CUDA-core kernel; TENSOR_CORE makes
  * pkv_attention_decode return PKV_ERR_UNSUPPORTED for sizes it does not
- * cover.  PERSISTENT selects the persistent tensor-core kernel (two resident
+ * cover.  PERSISTENT selects the persistent tensor-core kernel (three resident
  * CTAs per SM take (sequence, KV head, split) units from a queue in the
  * workspace; 16-bit caches, head_dim 64 or 128, groups of up to 8, at most
- * 512 sequences, partitions of at most 128 blocks; the split kernel
+ * 256 sequences, partitions of at most 64 blocks; the split kernel
  * otherwise), whose automatic partition is one split per pair up to 1,024
  * tokens of context and 512 tokens beyond.  The workspace-size calls follow
  * the current choice; a call given a workspace smaller than the persistent

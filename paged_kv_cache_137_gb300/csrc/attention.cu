@@ -225,8 +225,8 @@ bool pd_supported(const pkv_kv_desc* d, int group, int num_seqs, int partition) 
 // 512-token splits (units of at most 8 tiles, which the queue balances).
 int32_t pd_partition(int64_t max_ctx, int32_t block_size) {
   const int64_t step = std::max<int32_t>(64, block_size);
-  if (max_ctx <= 1024) return static_cast<int32_t>(std::max<int64_t>(step, (max_ctx + step - 1) / step * step));
-  return static_cast<int32_t>(std::max<int64_t>(step, 512));
+  const int64_t p = max_ctx <= 1024 ? (max_ctx + step - 1) / step * step : 512;
+  return static_cast<int32_t>(std::min<int64_t>(std::max<int64_t>(step, p), int64_t{kPdUnitBlocks} * block_size));
 }
 
 // Everything a decode call decides before launching: the kernels, the
@@ -252,9 +252,8 @@ pkv_status plan_call(const pkv_kv_desc* d, int q_dtype, float softmax_scale, int
   if (c.prefix_pass)
     c.pp = prefix_plan(num_seqs, group, d->num_kv_heads, static_cast<int64_t>(prefix_blocks) * d->block_size);
   const int64_t max_ctx = static_cast<int64_t>(max_blocks) * d->block_size - c.pp.tokens;
-  // the persistent kernel: when chosen, and for the tails behind a prefix pass
-  const bool want_pd =
-      allow_pd && (choice == PKV_KERNEL_PERSISTENT || (c.prefix_pass && choice == PKV_KERNEL_AUTO));
+  // the persistent kernel: when chosen
+  const bool want_pd = allow_pd && choice == PKV_KERNEL_PERSISTENT;
   if (want_pd) {
     int32_t p = partition_tokens;
     if (p < 0) return fail(PKV_ERR_INVALID_ARG, "partition_tokens is negative");

@@ -118,14 +118,14 @@ pkv_status launch_write_last(void* k_cache, void* v_cache, const void* k_new, co
                              int32_t num_seqs, const pkv_kv_desc* desc, cudaStream_t st);
 
 // Launch the persistent tensor-core decode kernel (16-bit caches, query
-// groups of up to 8, at most pd_max_seqs sequences, units of at most 128
-// blocks); PKV_ERR_UNSUPPORTED for other shapes.  Defined in the per-dtype
+// groups of up to 8, at most kPdMaxSeqs sequences, units of at most
+// kPdUnitBlocks blocks); PKV_ERR_UNSUPPORTED for other shapes.  Defined in the per-dtype
 // tensor-core units.
 template <typename KV, typename Q>
 pkv_status launch_decode_pd(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
                             const CUtensorMap& vmap, cudaStream_t stream);
-constexpr int kPdMaxSeqs = 512;
-constexpr int kPdUnitBlocks = 128;
+constexpr int kPdMaxSeqs = 256;
+constexpr int kPdUnitBlocks = 64;
 
 // Launch the CUDA-core decode kernel for one (cache dtype, q dtype) pair;
 // returns PKV_ERR_UNSUPPORTED for a shape it was not compiled for.

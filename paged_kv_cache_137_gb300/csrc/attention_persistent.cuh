@@ -22,15 +22,15 @@
 //    query rows and (for the step's token) the new K/V rows are copied into a
 //    shared-memory slot by cp.async, with no thread waiting on them.  Two
 //    slots: the unit being consumed and the next one.
-//  * The K/V ring (three 32 KiB stages for 16-bit head_dim 128) is refilled
-//    across unit boundaries: the next unit's first tiles are in flight while
-//    the current unit finishes.
-//  * Warps split head_dim, not tokens: each warp computes S^T = K q^T for 16
-//    tokens of a tile, the tile's row maxima and sums are exchanged through
-//    shared memory, P^T (64 tokens x 8 heads) goes through shared memory, and
-//    each warp accumulates O^T for its D / 4 rows of head_dim over all 64
-//    tokens.  No warp merge is needed at a unit's end: each warp writes its
-//    rows of the output (or of the split partial) from registers.
+//  * The K/V ring (two 32 KiB stages for 16-bit head_dim 128, three CTAs
+//    per SM) is refilled across unit boundaries: the next unit's first tiles
+//    are in flight while the current unit finishes.
+//  * The tile math is the split kernel's (head-columns form, query groups of
+//    up to 8): each warp folds 16 tokens of a tile into its own running
+//    state, with one CTA barrier per tile.  At a unit's end the warps' states
+//    are combined through the stage buffer of the unit's last tile, which is
+//    handed back to the producer only after that; the other stage keeps the
+//    next unit's first tile in flight.
 //  * Split partials are counted in at the end of the CTA's life (or when 64
 //    are pending): one fence, one atomic per unit, and the last of a pair's
 //    partials to arrive merges them.  With a shared prefix the prefix pass's
@@ -46,12 +46,11 @@ namespace pkv {
 namespace tc {
 namespace pd {
 
-constexpr int kCtasPerSm = 2;
-constexpr int kRingBytes = 98304;   // K/V stages per CTA
+constexpr int kCtasPerSm = 3;
+constexpr int kRingBytes = 65536;   // K/V stages per CTA
 constexpr int kMaxSeqs = kPdMaxSeqs;        // sequences a call may hold (schedule in shared memory)
 constexpr int kUnitBlocks = kPdUnitBlocks;  // block ids of one unit (a partition of at most 128 blocks)
 constexpr int kDefer = 64;          // partials counted in at once
-constexpr int kPStride = kTile + 8; // P^T row (one head) in 16-bit elements, padded against bank conflicts
 
 template <typename KV, int D>
 constexpr int stages() {
@@ -76,9 +75,7 @@ struct Layout {
   static constexpr int kSlot = kSlotTab + kSlotQ + kSlotNew;
   static constexpr int ring = 0;
   static constexpr int slots = ring + stages<KV, D>() * kStage;
-  static constexpr int p = slots + 2 * kSlot;               // P^T [8 heads][kPStride] 16-bit
-  static constexpr int red = p + 8 * kPStride * 2;          // float [2][warps][8]
-  static constexpr int ctx = red + 2 * kWarps * 8 * 4;      // int32 [kMaxSeqs]
+  static constexpr int ctx = slots + 2 * kSlot;             // int32 [kMaxSeqs]
   static constexpr int cum = ctx + kMaxSeqs * 4;            // int32 [kMaxSeqs + 1], padded
   static constexpr int units = cum + (kMaxSeqs + 4) * 4;    // Unit [2]
   static constexpr int defer = units + 2 * static_cast<int>(sizeof(Unit));  // int4 [kDefer]
@@ -111,7 +108,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   using raw = typename KV::raw;
   constexpr int NS = stages<KV, D>();
   constexpr int KS = D / 16;          // k-steps of S^T = K q^T
-  constexpr int MTW = D / 64;         // 16-row m-tiles of O^T per warp (head_dim split 4 ways)
   constexpr int BPT = kTile / T;      // blocks per tile
   constexpr int BPB = BPT * 2;        // TMA boxes per tile (K and V of each block)
   constexpr int kBoxBytes = T * G_::kRowBytes;
@@ -136,9 +132,6 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
   uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) &
                                              ~uintptr_t(1023));
   uint8_t* ring = smem + L_::ring;
-  raw* s_p = reinterpret_cast<raw*>(smem + L_::p);
-  float* red_m = reinterpret_cast<float*>(smem + L_::red);
-  float* red_l = red_m + kWarps * 8;
   int* s_ctx = reinterpret_cast<int*>(smem + L_::ctx);
   int* s_cum = reinterpret_cast<int*>(smem + L_::cum);
   Unit* s_unit = reinterpret_cast<Unit*>(smem + L_::units);
@@ -331,12 +324,10 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     pump();
   }
 
-  // q fragments (B operand of S^T = K q^T) and the running state of the
-  // current unit: per head (2 q4, 2 q4 + 1) its maximum and sum, identical in
-  // every warp; O^T for this warp's rows of head_dim
+  // q fragments (B operand of S^T = K q^T) and this warp's running state of
+  // the current unit (its tokens of every tile)
   uint32_t qb[KS][2];
-  float m[2], l[2];
-  float o[MTW][4];
+  WarpStateT<D> st;
 
   // ------------------------------------------------------- deferred counting
   // Pending partials (seq, kvh, nsplit) are counted in; where a pair's last
@@ -403,125 +394,33 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
       const raw* qrows = slot_q(s);
       load_qt<KV, Q, D>(qb, qrows, G, g, q4);
     }
-    m[0] = m[1] = -CUDART_INF_F;
-    l[0] = l[1] = 0.f;
-#pragma unroll
-    for (int mt = 0; mt < MTW; ++mt) o[mt][0] = o[mt][1] = o[mt][2] = o[mt][3] = 0.f;
+    st.reset();
     const HeadScales sc = head_scales(a.head_scales, NKV, u.kvh, a.softmax_scale, a.qk_scale,
                                       a.v_scale, a.k_inv, a.v_inv);
 
+    // the stage of the unit's last tile stays with the consumers for the
+    // warp merge
+    int held = -1;
     for (int tile = 0; tile < u.n_tiles && !dead; ++tile) {
-      const int st = released % NS;
-      const bool arrived = stage_wait(smem_u32(&s_bar[st]), (released / NS) & 1, a.wait_ns);
-      const uint8_t* kt = ring + st * L_::kStage;
-      uint8_t* vt = ring + st * L_::kStage + G_::kTileBytes;
-      const uint32_t kbase = smem_u32(kt), vbase = smem_u32(vt);
+      const int stg = released % NS;
+      const bool arrived = stage_wait(smem_u32(&s_bar[stg]), (released / NS) & 1, a.wait_ns);
+      const uint8_t* kt = ring + stg * L_::kStage;
+      uint8_t* vt = ring + stg * L_::kStage + G_::kTileBytes;
       const int row0 = warp * 16;
       const int nvalid = min(16, u.t_end - (u.t_begin + tile * kTile + row0));
-      // S^T = K q^T for this warp's 16 tokens (rows) x 8 heads (columns)
-      float scr[4] = {0.f, 0.f, 0.f, 0.f};
-      if (arrived) {
-        const int r = row0 + (mi & 1) * 8 + li;
-#pragma unroll
-        for (int ks = 0; ks < KS; ++ks) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4(kbase + swz<G_::kSlabs>(r, 2 * ks + (mi >> 1)), a0, a1, a2, a3);
-          mma16816<kBf>(scr, a0, a1, a2, a3, qb[ks][0], qb[ks][1]);
-        }
-      }
-      float v0[2], v1[2], mx[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        v0[j] = g < nvalid ? scr[j] * sc.qk : -CUDART_INF_F;
-        v1[j] = g + 8 < nvalid ? scr[2 + j] * sc.qk : -CUDART_INF_F;
-        float x = fmaxf(v0[j], v1[j]);
-        x = fmaxf(x, __shfl_xor_sync(FULL, x, 4));
-        x = fmaxf(x, __shfl_xor_sync(FULL, x, 8));
-        x = fmaxf(x, __shfl_xor_sync(FULL, x, 16));
-        mx[j] = x;
-      }
-      if (g == 0) {
-        red_m[warp * 8 + 2 * q4] = mx[0];
-        red_m[warp * 8 + 2 * q4 + 1] = mx[1];
-      }
-      // V rows past the context end are zeroed (0 * NaN would poison P V)
-      const bool zero_rows = nvalid < 16;
-      if (zero_rows) {
-        const int nz = (16 - max(nvalid, 0)) * G_::kSlabs * 8;
-        for (int i = lane; i < nz; i += 32) {
-          const int rr = row0 + max(nvalid, 0) + i / (G_::kSlabs * 8);
-          const int c = i % (G_::kSlabs * 8);
-          *reinterpret_cast<uint4*>(vt + swz<G_::kSlabs>(rr, c)) = make_uint4(0, 0, 0, 0);
-        }
-      }
-      if (__syncthreads_or(!arrived)) {  // (A) maxima of all warps
+      bool zeroed = false;
+      if (arrived && nvalid > 0) zeroed = tile_step_t<KV, D>(st, qb, kt, vt, row0, nvalid, sc.qk, lane);
+      if (zeroed) fence_proxy_async();  // the zeroed rows, before the stage is refilled by TMA
+      if (__syncthreads_or(!arrived)) {
         dead = true;
         break;
       }
-      float corr[2], p0[2], p1[2], ps[2];
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float tm = red_m[2 * q4 + j];
-#pragma unroll
-        for (int w = 1; w < kWarps; ++w) tm = fmaxf(tm, red_m[w * 8 + 2 * q4 + j]);
-        const float mn = fmaxf(m[j], tm);
-        corr[j] = exp2f(m[j] - mn);
-        m[j] = mn;
-        p0[j] = exp2f(v0[j] - mn);
-        p1[j] = exp2f(v1[j] - mn);
-        float x = p0[j] + p1[j];
-        x += __shfl_xor_sync(FULL, x, 4);
-        x += __shfl_xor_sync(FULL, x, 8);
-        x += __shfl_xor_sync(FULL, x, 16);
-        ps[j] = x;
+      if (tile + 1 < u.n_tiles) {
+        ++released;
+        if (warp == 0) pump();
+      } else {
+        held = stg;
       }
-      // P^T to shared memory: head-major, 64 tokens per head
-      {
-        raw* pp = s_p + (2 * q4) * kPStride + row0;
-        const uint32_t lo = pack2<kBf>(p0[0], p1[0]), hi = pack2<kBf>(p0[1], p1[1]);
-        pp[g] = *reinterpret_cast<const raw*>(&lo);
-        pp[g + 8] = reinterpret_cast<const raw*>(&lo)[1];
-        pp[kPStride + g] = *reinterpret_cast<const raw*>(&hi);
-        pp[kPStride + g + 8] = reinterpret_cast<const raw*>(&hi)[1];
-      }
-      if (g == 0) {
-        red_l[warp * 8 + 2 * q4] = ps[0];
-        red_l[warp * 8 + 2 * q4 + 1] = ps[1];
-      }
-      __syncthreads();  // (B) P^T and the sums of all warps
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        float t = 0.f;
-#pragma unroll
-        for (int w = 0; w < kWarps; ++w) t += red_l[w * 8 + 2 * q4 + j];
-        l[j] = l[j] * corr[j] + t;
-      }
-      if (corr[0] != 1.f || corr[1] != 1.f) {
-#pragma unroll
-        for (int mt = 0; mt < MTW; ++mt) {
-          o[mt][0] *= corr[0];
-          o[mt][1] *= corr[1];
-          o[mt][2] *= corr[0];
-          o[mt][3] *= corr[1];
-        }
-      }
-      // O^T (this warp's head_dim rows) += V^T P^T over the tile's 64 tokens
-#pragma unroll
-      for (int kk = 0; kk < kTile / 16; ++kk) {
-        const uint32_t* pw = reinterpret_cast<const uint32_t*>(s_p + g * kPStride + 16 * kk + 2 * q4);
-        const uint32_t b0 = pw[0], b1 = pw[4];
-        const int rv = 16 * kk + (mi >> 1) * 8 + li;
-#pragma unroll
-        for (int mt = 0; mt < MTW; ++mt) {
-          uint32_t a0, a1, a2, a3;
-          ldsm_x4_t(vbase + swz<G_::kSlabs>(rv, 2 * (warp * MTW + mt) + (mi & 1)), a0, a1, a2, a3);
-          mma16816<kBf>(o[mt], a0, a1, a2, a3, b0, b1);
-        }
-      }
-      if (zero_rows) fence_proxy_async();  // the zeroed rows, before TMA refills the stage
-      __syncthreads();  // (C) the stage and P^T are free
-      ++released;
-      if (warp == 0) pump();
     }
 
     if (dead) {
@@ -548,29 +447,47 @@ __global__ void __launch_bounds__(kThreads, kCtasPerSm)
     const int bad = u.bad | s_unit[s].bad | (dead ? kTimeout : 0);
     const bool direct = u.nsplit == 1 && P == 0;
     const size_t head0 = static_cast<size_t>(u.seq) * HQ + static_cast<size_t>(u.kvh) * G;
-#pragma unroll
-    for (int mt = 0; mt < MTW; ++mt)
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int head = 2 * q4 + (e & 1);
-        const int d = 16 * (warp * MTW + mt) + g + 8 * (e >> 1);
-        if (head >= G) continue;
-        const float lj = l[e & 1];
+    if (held >= 0 && !dead) {
+      // the warps' states combined in the held stage buffer: maxima and sums
+      // [warp][16], outputs [warp][8 heads][D]
+      float* mS = reinterpret_cast<float*>(ring + held * L_::kStage);
+      float* lS = mS + kWarps * 16;
+      float* oS = lS + kWarps * 16;
+      publish_t<KV, D>(st, mS, lS, oS, warp, G, 8, lane);
+      __syncthreads();
+      for (int i = tid; i < G * D; i += kThreads) {
+        const int row = i / D, d = i % D;
+        float M, L, A;
+        combine_warps(mS, lS, oS, kWarps, 8, row, d, D, M, L, A);
+        A *= sc.v;
         if (direct) {
-          store_elem<Q>(a.out, (head0 + head) * D + d,
-                        bad ? CUDART_NAN_F : (lj > 0.f ? o[mt][e] * sc.v / lj : 0.f));
+          store_elem<Q>(a.out, (head0 + row) * D + d, bad ? CUDART_NAN_F : (L > 0.f ? A / L : 0.f));
         } else {
-          a.ws_acc[((head0 + head) * a.max_splits + u.split) * D + d] = bad ? CUDART_NAN_F : o[mt][e] * sc.v;
+          const size_t pidx = (head0 + row) * a.max_splits + u.split;
+          a.ws_acc[pidx * D + d] = bad ? CUDART_NAN_F : A;
+          if (d == 0) {
+            a.ws_m[pidx] = M;
+            a.ws_l[pidx] = bad ? CUDART_NAN_F : L;
+          }
         }
       }
-    if (!direct && warp == 0 && g == 0) {
-#pragma unroll
-      for (int j = 0; j < 2; ++j) {
-        const int head = 2 * q4 + j;
-        if (head < G) {
-          const size_t pidx = (head0 + head) * a.max_splits + u.split;
-          a.ws_m[pidx] = m[j];
-          a.ws_l[pidx] = bad ? CUDART_NAN_F : l[j];
+      fence_proxy_async();  // the generic writes into the stage, before TMA refills it
+      __syncthreads();
+      ++released;
+      if (warp == 0) pump();
+    } else {
+      // nothing attended (an empty or invalid unit) or a wait gave up
+      for (int i = tid; i < G * D; i += kThreads) {
+        const int row = i / D, d = i % D;
+        if (direct) {
+          store_elem<Q>(a.out, (head0 + row) * D + d, bad ? CUDART_NAN_F : 0.f);
+        } else {
+          const size_t pidx = (head0 + row) * a.max_splits + u.split;
+          a.ws_acc[pidx * D + d] = bad ? CUDART_NAN_F : 0.f;
+          if (d == 0) {
+            a.ws_m[pidx] = -CUDART_INF_F;
+            a.ws_l[pidx] = bad ? CUDART_NAN_F : 0.f;
+          }
         }
       }
     }
