@@ -38,7 +38,8 @@ METRIC = "paged decode attention KV GB/s & fraction of GB300 HBM peak; decode to
 # the sources each kernel family's recorded DRAM counters depend on
 KERNEL_SOURCES = {
     "decode": ["attention.cu", "attention.h", "attention_simt.cuh", "attention_tc.cuh",
-               "attention_tc_launch.cuh", "device_common.cuh"],
+               "attention_tc_launch.cuh", "device_common.cuh", "attention_prefill_umma.cuh",
+               "attention_shared_prefix.cu"],
     "prefill": ["attention_prefill.cu", "attention_prefill_umma.cuh", "attention_tc.cuh", "attention.h",
                 "device_common.cuh"],
 }
@@ -63,7 +64,7 @@ def parse():
                          "and K end-to-end steps, for profiling runs)")
     ap.add_argument("--partition", type=int, default=None,
                     help="split-K partition in tokens (default: the workload's, else automatic)")
-    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc", "persistent"],
+    ap.add_argument("--kernel", default="auto", choices=["auto", "simt", "tc"],
                     help="decode kernel (auto = tensor-core where it applies)")
     ap.add_argument("--shared-prefix", default="auto", choices=["auto", "on", "off"],
                     help="decode a batch's shared prefix once for all sequences (auto: when the "
@@ -191,9 +192,6 @@ def attention_kernels(kernel: str, w, splits: int, shared_prefix: bool = False) 
     if w.kv_dtype == "f32" or kernel == "simt":
         k = "decode_simt_kernel"
         return k + (" + merge_kernel" if splits > 1 else "")
-    if kernel == "persistent":
-        return (("prefill_umma_kernel<shared prefix> + " if shared_prefix else "")
-                + "decode_pd_kernel (persistent; merges fused)")
     if shared_prefix:
         return "prefill_umma_kernel<shared prefix> + decode_tc_kernel (merges fused)"
     return "decode_tc_kernel (split-K merge fused)"
@@ -809,15 +807,18 @@ def run_gpu(args, world, rank, local):
 def end_to_end(scn, dev_name, n: int, world: int, kv_bytes: int):
     """The step through the C ABI with its inputs copied from pinned host
     memory and its output copied back, every step.  Two input/output buffer
-    pairs alternate: step i's host-to-device copy runs on a copy stream while
-    step i - 1 computes, its device-to-host copy after it, and the host waits
-    for step i - 1's output before issuing step i + 1 (one step in flight),
-    as a serving loop that overlaps transfers with compute does.  Inputs per
-    step: q, the new K/V, block tables and context lengths packed in one
-    pinned buffer (one copy); output: the attention result.  GB/s over the
-    host's wall clock.  The graph figure (copy in, step, copy out captured as
-    one CUDA graph, one replay and one host sync per step) is reported beside
-    it."""
+    pairs alternate: step i's host-to-device copy runs on an input-copy
+    stream while step i - 1 computes, step i - 1's device-to-host copy on an
+    output-copy stream while step i computes, and the host waits for step
+    i - 1's output before issuing step i + 1 (one step in flight), as a
+    serving loop that overlaps transfers with compute does.  (With one copy
+    stream for both directions, step i's input copy would queue behind step
+    i - 1's output copy, which waits for step i - 1's compute: no overlap.)
+    Inputs per step: q, the new K/V, block tables and context lengths packed
+    in one pinned buffer (one copy); output: the attention result.  GB/s over
+    the host's wall clock.  The graph figure (copy in, step, copy out
+    captured as one CUDA graph, one replay and one host sync per step) is
+    reported beside it."""
     import copy as _copy
     import torch
     names = ("q", "k_new", "v_new", "tables", "ctx")
@@ -836,21 +837,24 @@ def end_to_end(scn, dev_name, n: int, world: int, kv_bytes: int):
     h2d = slots[0]["host_in"].numel()
     d2h = slots[0]["host_out"].numel() * slots[0]["host_out"].element_size()
     compute = torch.cuda.current_stream()
-    copy_s = torch.cuda.Stream(device=dev_name)
+    in_s = torch.cuda.Stream(device=dev_name)
+    out_s = torch.cuda.Stream(device=dev_name)
 
     def issue(i):
         sl = slots[i % 2]
-        with torch.cuda.stream(copy_s):
-            copy_s.wait_event(sl["done_ev"])       # step i - 2 is done with this buffer
+        # step i - 2 used this pair: its compute is done (done_ev) and its
+        # output has reached the host (the host waited for out_ev)
+        in_s.wait_event(sl["done_ev"])
+        with torch.cuda.stream(in_s):
             sl["dev_in"].copy_(sl["host_in"], non_blocking=True)
-            sl["in_ev"].record(copy_s)
+        sl["in_ev"].record(in_s)
         compute.wait_event(sl["in_ev"])
         sl["scn"].step()
         sl["done_ev"].record(compute)
-        with torch.cuda.stream(copy_s):
-            copy_s.wait_event(sl["done_ev"])
+        out_s.wait_event(sl["done_ev"])
+        with torch.cuda.stream(out_s):
             sl["host_out"].copy_(sl["scn"].out, non_blocking=True)
-            sl["out_ev"].record(copy_s)
+        sl["out_ev"].record(out_s)
 
     def run(n):
         for i in range(n):

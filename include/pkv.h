@@ -267,19 +267,10 @@ PKV_API size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_hea
  * heads and partitions of at most 1024 blocks, and the CUDA-core kernel
  * otherwise.  SIMT forces the CUDA-core kernel; TENSOR_CORE makes
  * pkv_attention_decode return PKV_ERR_UNSUPPORTED for sizes it does not
- * cover.  PERSISTENT selects the persistent tensor-core kernel (three resident
- * CTAs per SM take (sequence, KV head, split) units from a queue in the
- * workspace; 16-bit caches, head_dim 64 or 128, groups of up to 8, at most
- * 256 sequences, partitions of at most 64 blocks; the split kernel
- * otherwise), whose automatic partition is one split per pair up to 1,024
- * tokens of context and 512 tokens beyond.  The workspace-size calls follow
- * the current choice; a call given a workspace smaller than the persistent
- * kernel's (or none) runs the split kernel.  All kernels compute the same
- * result within rounding. */
+ * cover.  All kernels compute the same result within rounding. */
 #define PKV_KERNEL_AUTO 0
 #define PKV_KERNEL_SIMT 1
 #define PKV_KERNEL_TENSOR_CORE 2
-#define PKV_KERNEL_PERSISTENT 3
 PKV_API pkv_status pkv_set_attention_kernel(int32_t kind);
 
 /* Partition (tokens per split) pkv_attention_decode uses for these sizes.

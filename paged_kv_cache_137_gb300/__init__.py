@@ -19,9 +19,8 @@ from ._build import LIB, build  # noqa: F401
 PKV_OK, PKV_ERR_INVALID_ARG, PKV_ERR_OUT_OF_BLOCKS, PKV_ERR_UNKNOWN_SEQ, PKV_ERR_UNSUPPORTED, \
     PKV_ERR_CUDA = range(6)
 PKV_F32, PKV_F16, PKV_BF16, PKV_E4M3 = range(4)
-PKV_KERNEL_AUTO, PKV_KERNEL_SIMT, PKV_KERNEL_TENSOR_CORE, PKV_KERNEL_PERSISTENT = range(4)
-KERNEL_OF_NAME = {"auto": PKV_KERNEL_AUTO, "simt": PKV_KERNEL_SIMT, "tc": PKV_KERNEL_TENSOR_CORE,
-                  "persistent": PKV_KERNEL_PERSISTENT}
+PKV_KERNEL_AUTO, PKV_KERNEL_SIMT, PKV_KERNEL_TENSOR_CORE = range(3)
+KERNEL_OF_NAME = {"auto": PKV_KERNEL_AUTO, "simt": PKV_KERNEL_SIMT, "tc": PKV_KERNEL_TENSOR_CORE}
 
 STATUS_NAMES = {0: "OK", 1: "INVALID_ARG", 2: "OUT_OF_BLOCKS", 3: "UNKNOWN_SEQ", 4: "UNSUPPORTED",
                 5: "CUDA"}
@@ -530,7 +529,7 @@ def pkv_attention_partition(num_seqs, max_blocks, desc: pkv_kv_desc, partition_t
 
 
 def pkv_set_attention_kernel(kind) -> None:
-    """Process-wide decode kernel choice: "auto", "simt", "tc" or "persistent"."""
+    """Process-wide decode kernel choice: "auto", "simt" or "tc"."""
     _check(lib().pkv_set_attention_kernel(KERNEL_OF_NAME.get(kind, kind)))
 
 

@@ -79,25 +79,19 @@ int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx, 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t counter_off, done_off, work_off, m_off, l_off, acc_off, bytes;
+  size_t counter_off, m_off, l_off, acc_off, bytes;
 };
 
 // Workspace: split-K arrival counters [B][N_kv] (zero between calls), then
-// extra_ints more counters (the grid's exit count behind a shared-prefix
-// pass; the persistent kernel's exit count and unit queue), then the partial
-// maxima, sums and unnormalised outputs (when there are splits), each part
-// 256-byte aligned.  Nothing when neither is needed.
+// the partial maxima, sums and unnormalised outputs, each part 256-byte
+// aligned.  Nothing without splits.
 WsLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t num_kv_heads,
-                          int64_t splits, int64_t head_dim, int extra_ints = 0) {
+                          int64_t splits, int64_t head_dim) {
   WsLayout w{};
-  if (splits <= 1 && extra_ints == 0) return w;
-  const size_t counters = static_cast<size_t>(num_seqs * num_kv_heads) + extra_ints;
-  w.counter_off = 0;
-  w.done_off = static_cast<size_t>(num_seqs * num_kv_heads) * sizeof(int);
-  w.work_off = w.done_off + sizeof(int);
-  w.m_off = align_up(counters * sizeof(int), 256);
-  w.bytes = w.m_off;
   if (splits <= 1) return w;
+  const size_t counters = static_cast<size_t>(num_seqs * num_kv_heads);
+  w.counter_off = 0;
+  w.m_off = align_up(counters * sizeof(int), 256);
   const size_t n = static_cast<size_t>(num_seqs * num_q_heads * splits);
   w.l_off = w.m_off + align_up(n * sizeof(float), 256);
   w.acc_off = w.l_off + align_up(n * sizeof(float), 256);
@@ -209,32 +203,12 @@ bool prefix_pass_covers(const pkv_kv_desc* d, int q_dtype, float softmax_scale) 
   return d->kv_dtype == PKV_E4M3 && (q_dtype == PKV_F16 || q_dtype == PKV_BF16);
 }
 
-// Whether the persistent kernel covers these sizes (16-bit caches, groups of
-// up to 8 query heads, at most kPdMaxSeqs sequences, units of at most
-// kPdUnitBlocks blocks).
-bool pd_supported(const pkv_kv_desc* d, int group, int num_seqs, int partition) {
-  if (d->kv_dtype != PKV_BF16 && d->kv_dtype != PKV_F16) return false;
-  if (d->head_dim != 128 && d->head_dim != 64) return false;
-  if (group > 8 || num_seqs > kPdMaxSeqs) return false;
-  if (partition > kPdUnitBlocks * d->block_size) return false;
-  return static_cast<int64_t>(d->num_blocks) * d->num_kv_heads * d->block_size <= INT32_MAX;
-}
-
-// Partition of the persistent kernel for partition_tokens 0: one split per
-// pair when every context (past a shared prefix) fits 1,024 tokens, else
-// 512-token splits (units of at most 8 tiles, which the queue balances).
-int32_t pd_partition(int64_t max_ctx, int32_t block_size) {
-  const int64_t step = std::max<int32_t>(64, block_size);
-  const int64_t p = max_ctx <= 1024 ? (max_ctx + step - 1) / step * step : 512;
-  return static_cast<int32_t>(std::min<int64_t>(std::max<int64_t>(step, p), int64_t{kPdUnitBlocks} * block_size));
-}
-
 // Everything a decode call decides before launching: the kernels, the
 // partition, the split slots and the workspace layout.  sizing: for the
 // workspace-size queries (q dtype and softmax scale taken as the ones that
 // run the most kernels).
 struct CallPlan {
-  bool prefix_pass = false, pd = false;
+  bool prefix_pass = false;
   PrefixPlan pp;
   int32_t partition = 0;
   int64_t splits = 1;   // tail splits + prefix key ranges
@@ -242,7 +216,7 @@ struct CallPlan {
 };
 pkv_status plan_call(const pkv_kv_desc* d, int q_dtype, float softmax_scale, int32_t num_seqs,
                      int32_t num_q_heads, int32_t max_blocks, int32_t partition_tokens,
-                     int32_t prefix_blocks, CallPlan* out, bool allow_pd = true) {
+                     int32_t prefix_blocks, CallPlan* out) {
   CallPlan c;
   const int group = num_q_heads / d->num_kv_heads;
   const int choice = g_kernel_choice.load();
@@ -251,29 +225,10 @@ pkv_status plan_call(const pkv_kv_desc* d, int q_dtype, float softmax_scale, int
                   prefix_pass_covers(d, q_dtype, softmax_scale) && tc_supported(d, q_dtype, group, 64);
   if (c.prefix_pass)
     c.pp = prefix_plan(num_seqs, group, d->num_kv_heads, static_cast<int64_t>(prefix_blocks) * d->block_size);
-  const int64_t max_ctx = static_cast<int64_t>(max_blocks) * d->block_size - c.pp.tokens;
-  // the persistent kernel: when chosen
-  const bool want_pd = allow_pd && choice == PKV_KERNEL_PERSISTENT;
-  if (want_pd) {
-    int32_t p = partition_tokens;
-    if (p < 0) return fail(PKV_ERR_INVALID_ARG, "partition_tokens is negative");
-    if (p > 0 && (p % 64 != 0 || p % d->block_size != 0))
-      return fail(PKV_ERR_INVALID_ARG, "partition_tokens must be a multiple of 64 and of block_size");
-    if (p == 0) p = pd_partition(max_ctx, d->block_size);
-    const int64_t units = static_cast<int64_t>(num_seqs) * d->num_kv_heads *
-                          std::max<int64_t>(1, (max_ctx + p - 1) / p);
-    if (pd_supported(d, group, num_seqs, p) && units < (int64_t{1} << 30)) {
-      c.pd = true;
-      c.partition = p;
-    }
-  }
-  if (!c.pd) {
-    pkv_status st = resolve_partition(partition_tokens, num_seqs, max_blocks, d, &c.partition, c.pp.tokens);
-    if (st != PKV_OK) return st;
-  }
+  pkv_status st = resolve_partition(partition_tokens, num_seqs, max_blocks, d, &c.partition, c.pp.tokens);
+  if (st != PKV_OK) return st;
   c.splits = num_splits(max_blocks, d->block_size, c.partition, c.pp.tokens) + c.pp.key_splits;
-  const int extra = c.pd ? 2 : (c.prefix_pass ? 1 : 0);
-  c.ws = workspace_layout(num_seqs, num_q_heads, d->num_kv_heads, c.splits, d->head_dim, extra);
+  c.ws = workspace_layout(num_seqs, num_q_heads, d->num_kv_heads, c.splits, d->head_dim);
   *out = c;
   return PKV_OK;
 }
@@ -369,8 +324,7 @@ size_t attention_counter_bytes(int32_t num_seqs, int32_t num_q_heads, int32_t ma
 }  // namespace pkv
 
 extern "C" pkv_status pkv_set_attention_kernel(int32_t kind) {
-  if (kind != PKV_KERNEL_AUTO && kind != PKV_KERNEL_SIMT && kind != PKV_KERNEL_TENSOR_CORE &&
-      kind != PKV_KERNEL_PERSISTENT)
+  if (kind != PKV_KERNEL_AUTO && kind != PKV_KERNEL_SIMT && kind != PKV_KERNEL_TENSOR_CORE)
     return fail(PKV_ERR_INVALID_ARG, "unknown attention kernel kind");
   g_kernel_choice.store(kind);
   return PKV_OK;
@@ -428,12 +382,6 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   st = plan_call(desc, q_dtype, softmax_scale, num_seqs, num_q_heads, max_blocks, partition_tokens,
                  prefix_blocks, &plan);
   if (st != PKV_OK) return st;
-  if (plan.pd && (workspace == nullptr || workspace_bytes < plan.ws.bytes)) {
-    // a workspace sized for the split kernel: run that
-    st = plan_call(desc, q_dtype, softmax_scale, num_seqs, num_q_heads, max_blocks, partition_tokens,
-                   prefix_blocks, &plan, false);
-    if (st != PKV_OK) return st;
-  }
   const bool prefix_pass = plan.prefix_pass;
   const PrefixPlan pp = plan.pp;
   const int32_t partition = plan.partition;
@@ -477,20 +425,18 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   a.softmax_scale = softmax_scale;
   a.prefix_tokens = pp.tokens;
   a.prefix_splits = pp.key_splits;
-  a.done = (prefix_pass || plan.pd) ? reinterpret_cast<int*>(wsb + ws.done_off) : nullptr;
-  a.work = plan.pd ? reinterpret_cast<int*>(wsb + ws.work_off) : nullptr;
   a.status = status;
   a.wait_ns = stage_wait_limit_ns();
 
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   const int D = desc->head_dim;
   const bool tc_ok = tc_supported(desc, q_dtype, group, partition);
-  if ((choice == PKV_KERNEL_TENSOR_CORE || choice == PKV_KERNEL_PERSISTENT) && !tc_ok && !plan.pd)
+  if (choice == PKV_KERNEL_TENSOR_CORE && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED, "the tensor-core kernel does not cover these sizes");
   if (prefix_pass && !tc_ok)
     return fail(PKV_ERR_UNSUPPORTED, "partition too long for the tensor-core kernel");
   if (k_new) {
-    if (plan.pd || (tc_ok && choice != PKV_KERNEL_SIMT)) {
+    if (tc_ok && choice != PKV_KERNEL_SIMT) {
       a.k_new = k_new;  // fused into the split kernel
       a.v_new = v_new;
       a.k_inv = kv == PKV_E4M3 ? k_inv : 1.0f;
@@ -504,7 +450,8 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   }
   if (prefix_pass) {
     // the prefix pass first: its CTAs let the decode kernel start once they
-    // have all begun; the decode kernel reads their partials after its wait
+    // have all begun; the decode kernel's CTAs wait for the whole pass (a
+    // grid dependency wait, not a flag) before they read its partials
     PrefillArgs pa{};
     pa.q = q;
     pa.tables = block_tables;
@@ -528,10 +475,6 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
     pa.ws_m = a.ws_m;
     pa.ws_l = a.ws_l;
     pa.ws_acc = a.ws_acc;
-    pa.out = out;
-    pa.ctx_lens = context_lens;
-    pa.counters = a.counters;
-    pa.partition = partition;
     pa.sp_seqs = pp.seqs_per_cta;
     CUtensorMap pkmap, pvmap;
     st = pool_map(&pkmap, k_cache, desc, false);
@@ -546,14 +489,6 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
                                 : launch_shared_prefix_pass<E4M3, BF16>(pa, T, pp.key_splits, pkmap, pvmap, s);
     }
     if (st != PKV_OK) return st;
-  }
-  if (plan.pd) {
-    CUtensorMap kmap, vmap;
-    st = pool_map(&kmap, k_cache, desc);
-    if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc);
-    if (st != PKV_OK) return st;
-    return kv == PKV_F16 ? launch_decode_pd<F16, F16>(a, D, kmap, vmap, s)
-                         : launch_decode_pd<BF16, BF16>(a, D, kmap, vmap, s);
   }
   if (tc_ok && choice != PKV_KERNEL_SIMT) {
     CUtensorMap kmap, vmap;

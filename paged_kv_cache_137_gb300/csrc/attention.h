@@ -39,14 +39,13 @@ struct DecodeArgs {
   const float* head_scales;
   float softmax_scale;
   // shared prefix (0: none): positions [0, prefix_tokens) of every sequence
-  // were attended by the shared-prefix pass, whose prefix_splits partials
-  // sit in the last prefix_splits of the max_splits slots; this kernel
-  // covers [prefix_tokens, ctx) and merges everything
+  // are attended by the shared-prefix pass, the kernel launched just before
+  // this one, whose prefix_splits partials sit in the last prefix_splits of
+  // the max_splits slots; this kernel covers [prefix_tokens, ctx) and merges
+  // everything once that pass has completed
   int32_t prefix_tokens, prefix_splits;
   int* status;               // device error word (PKV_DEVICE_* bits, atomicOr)
   uint64_t wait_ns;          // give-up limit of a stage wait; 0 = give up at once
-  int* done;                 // shared prefix / persistent kernel: CTAs of this grid that have finished
-  int* work;                 // persistent kernel: next unit of the queue
 };
 
 // Prefill / shared-prefix pass arguments (attention_prefill.cu,
@@ -71,15 +70,11 @@ struct PrefillArgs {
   // the keys are positions [k * sp_split, min(sp_tokens, (k + 1) * sp_split))
   // of table row 0; row (s, j)'s partial (max, sum, unnormalised output)
   // goes to split slot sp_slot0 + k of the decode workspace (ws_*, max_splits
-  // slots).  Each CTA then counts itself in on counters[s][kvh] and, where it
-  // is the last of the pair's partials (the decode kernel's splits of the
-  // positions >= sp_tokens, partition tokens each, and the key ranges),
-  // merges them into out.
-  int32_t sp_rows, sp_tokens, sp_split, sp_slot0, max_splits, sp_seqs, partition;
+  // slots), which the decode kernel behind the pass merges.
+  int32_t sp_rows, sp_tokens, sp_split, sp_slot0, max_splits, sp_seqs;
   float* ws_m;
   float* ws_l;
   float* ws_acc;
-  int* counters;
 };
 
 // Device error word of the current device (looked up once per device);
@@ -116,16 +111,6 @@ pkv_status launch_write_last(void* k_cache, void* v_cache, const void* k_new, co
                              int32_t src_dtype, float k_inv_scale, float v_inv_scale,
                              const int32_t* tables, int32_t max_blocks, const int32_t* ctx_lens,
                              int32_t num_seqs, const pkv_kv_desc* desc, cudaStream_t st);
-
-// Launch the persistent tensor-core decode kernel (16-bit caches, query
-// groups of up to 8, at most kPdMaxSeqs sequences, units of at most
-// kPdUnitBlocks blocks); PKV_ERR_UNSUPPORTED for other shapes.  Defined in the per-dtype
-// tensor-core units.
-template <typename KV, typename Q>
-pkv_status launch_decode_pd(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
-                            const CUtensorMap& vmap, cudaStream_t stream);
-constexpr int kPdMaxSeqs = 256;
-constexpr int kPdUnitBlocks = 64;
 
 // Launch the CUDA-core decode kernel for one (cache dtype, q dtype) pair;
 // returns PKV_ERR_UNSUPPORTED for a shape it was not compiled for.

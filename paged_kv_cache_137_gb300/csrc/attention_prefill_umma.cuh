@@ -53,7 +53,8 @@
 // maximum, sum, unnormalised output times the V scale) in a split slot of the
 // decode workspace, where the decode kernel merges it with the rest of the
 // sequence's context.  The CTAs let the decode kernel launch as soon as they
-// have all started (griddepcontrol.launch_dependents after their own wait).
+// have all started (griddepcontrol.launch_dependents after their own wait);
+// that kernel waits for this grid to complete before it reads the partials.
 #pragma once
 
 #include <math_constants.h>
@@ -501,11 +502,26 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
     const int nseq = n / a.group, nb = a.sp_tokens / T;
     for (int i = tid; i < nseq; i += kNT) s_pbad[i] = 0;
     __syncthreads();
-    if (blockIdx.y == 0)
-      for (int e = tid; e < nseq * nb; e += kNT) {
-        const int sq = seq0 + e / nb, b = e % nb;
-        if (a.tables[static_cast<size_t>(sq) * a.max_blocks + b] != a.tables[b]) s_pbad[e / nb] = 1;
+    if (blockIdx.y == 0) {
+      // kU entries (and row 0's matching ones) in flight per thread
+      constexpr int kU = 8;
+      const int total = nseq * nb;
+      for (int e0 = tid; e0 < total; e0 += kU * kNT) {
+        int mine[kU], ref[kU];
+#pragma unroll
+        for (int u = 0; u < kU; ++u) {
+          const int e = e0 + u * kNT;
+          mine[u] = ref[u] = 0;
+          if (e < total) {
+            mine[u] = __ldg(a.tables + static_cast<size_t>(seq0 + e / nb) * a.max_blocks + e % nb);
+            ref[u] = __ldg(a.tables + e % nb);
+          }
+        }
+#pragma unroll
+        for (int u = 0; u < kU; ++u)
+          if (e0 + u * kNT < total && mine[u] != ref[u]) s_pbad[(e0 + u * kNT) / nb] = 1;
       }
+    }
   }
   tc_fence_before();
   __syncthreads();
@@ -835,8 +851,6 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
 
   // ---------------------------------------------------------------- exit
   // every UMMA done and every copy landed before TMEM and shared memory go
-  // (shared-prefix pass: the partials written, before they are counted in)
-  if constexpr (kCasc) __threadfence();
   __syncthreads();
   if (tid == 0) {
     mbar_wait(smem_u32(fin), 0, kDrainNs);
@@ -854,59 +868,6 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   if (warp == kProd) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);
-  }
-  if constexpr (kCasc) {
-    // Count this CTA's partials in on each of its (sequence, KV head) pairs;
-    // the last of a pair's partials to arrive (the decode kernel's splits of
-    // the positions past the prefix, and the key ranges of this pass) merges
-    // them.  The split count is the decode kernel's, from the same length.
-    __shared__ int s_merge[256];
-    __shared__ int s_nmerge;
-    const int kvh_c = blockIdx.z;
-    if (tid == 0) s_nmerge = 0;
-    __syncthreads();
-    const int nseq = min(a.sp_seqs, a.num_seqs - seq0);
-    for (int i = tid; i < nseq; i += kNT) {
-      const int sq = seq0 + i;
-      const int c = a.ctx_lens[sq];
-      const bool bad_c = c < 0 || c > a.max_blocks * T || c <= a.sp_tokens;
-      const int nsplit = bad_c ? 1 : max(1, (c - a.sp_tokens + a.partition - 1) / a.partition);
-      const int prev = atomicAdd(&a.counters[static_cast<size_t>(sq) * a.num_kv_heads + kvh_c], 1);
-      if (prev == nsplit + static_cast<int>(gridDim.y) - 1) s_merge[atomicAdd(&s_nmerge, 1)] = sq;
-    }
-    __syncthreads();
-    const int nm = s_nmerge;
-    if (nm > 0) {
-      __threadfence();
-      const int G = a.group;
-      for (int e = tid; e < nm * G * D; e += kNT) {
-        const int sq = s_merge[e / (G * D)];
-        const int row = (e / D) % G, d = e % D;
-        const int c = a.ctx_lens[sq];
-        const bool bad_c = c < 0 || c > a.max_blocks * T || c <= a.sp_tokens;
-        const int nsplit = bad_c ? 1 : max(1, (c - a.sp_tokens + a.partition - 1) / a.partition);
-        const int np = nsplit + static_cast<int>(gridDim.y);
-        const size_t base = (static_cast<size_t>(sq) * HQ + j + row) * a.max_splits;
-        auto slot = [&](int i) { return i < nsplit ? i : a.sp_slot0 + (i - nsplit); };
-        float M = -CUDART_INF_F;
-        for (int i = 0; i < np; ++i) M = fmaxf(M, __ldcg(a.ws_m + base + slot(i)));
-        float L = 0.f, A = 0.f;
-        if (M != -CUDART_INF_F) {
-          for (int i = 0; i < np; ++i) {
-            const float f = exp2f(__ldcg(a.ws_m + base + slot(i)) - M);
-            L = fmaf(__ldcg(a.ws_l + base + slot(i)), f, L);
-            A = fmaf(__ldcg(a.ws_acc + (base + slot(i)) * D + d), f, A);
-          }
-        } else {
-          for (int i = 0; i < np; ++i) L += __ldcg(a.ws_l + base + slot(i));
-        }
-        store_elem<Q>(a.out, (static_cast<size_t>(sq) * HQ + j + row) * D + d,
-                      (L > 0.f || L != L) ? A / L : 0.f);
-      }
-      __syncthreads();
-      for (int i = tid; i < nm; i += kNT)
-        atomicExch(&a.counters[static_cast<size_t>(s_merge[i]) * a.num_kv_heads + kvh_c], 0);
-    }
   }
 }
 

@@ -655,53 +655,74 @@ __device__ __forceinline__ void combine_warps(const float* mS, const float* lS, 
   }
 }
 
+// Whether the partials of nsplit split slots of a query group fit the
+// shared-memory gather below (`cap` floats).
+template <int D>
+__device__ __forceinline__ bool gather_fits(int G, int nsplit, int cap) {
+  return G * nsplit <= kThreads && G * nsplit * (D + 2) <= cap;
+}
+
+// Gather the partials (m, l, a) of the G heads at head0 from the split slots
+// slot(0) .. slot(nsplit - 1) into shared memory: a [G][nsplit][D], then m
+// and l [G][nsplit].  Every load is a global round trip of several
+// microseconds while the GPU streams, so they are all issued before any is
+// used.  Ends with a CTA barrier.
+template <int D, typename Slot>
+__device__ void gather_partials(const DecodeArgs& a, size_t head0, int nsplit, Slot slot,
+                                float* stage) {
+  const int tid = threadIdx.x, G = a.group;
+  const int nacc = G * nsplit * D;
+  float* g_acc = stage;
+  float* g_m = g_acc + nacc;
+  float* g_l = g_m + G * nsplit;
+  float mv = 0.f, lv = 0.f;
+  if (tid < G * nsplit) {
+    const size_t pidx = (head0 + tid / nsplit) * a.max_splits + slot(tid % nsplit);
+    mv = __ldcg(a.ws_m + pidx);
+    lv = __ldcg(a.ws_l + pidx);
+  }
+  constexpr int kU = 8;  // float4 loads in flight per thread
+  for (int i0 = 0; i0 < nacc / 4; i0 += kU * kThreads) {
+    float4 v[kU];
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * kThreads + tid;
+      if (i < nacc / 4) {
+        const int e = 4 * i, row = e / (nsplit * D), rem = e - row * nsplit * D;
+        const int sp = rem / D, d = rem - sp * D;
+        v[u] = __ldcg(reinterpret_cast<const float4*>(
+            a.ws_acc + ((head0 + row) * a.max_splits + slot(sp)) * D + d));
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kU; ++u) {
+      const int i = i0 + u * kThreads + tid;
+      if (i < nacc / 4) reinterpret_cast<float4*>(g_acc)[i] = v[u];
+    }
+  }
+  if (tid < G * nsplit) {
+    g_m[tid] = mv;
+    g_l[tid] = lv;
+  }
+  __syncthreads();
+}
+
 // Combine the partials (max m_i, sum l_i, unnormalised output a_i) of the G
 // heads at head0, from split slots 0 .. nsplit - 1 and extra_base ..
 // extra_base + n_extra - 1:  M = max m_i, L = sum l_i 2^(m_i - M),
-// o = sum a_i 2^(m_i - M) / L.  Every load is a global round trip of several
-// microseconds while the GPU streams, so all partials are first gathered into
-// shared memory (stage, `cap` floats) with independent loads.
+// o = sum a_i 2^(m_i - M) / L.  The partials are gathered into shared
+// memory (stage, `cap` floats) first where they fit.
 template <typename Q, int D>
 __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit_tail, int extra_base,
                              int n_extra, float* stage, int cap) {
   const int tid = threadIdx.x, G = a.group;
   const int nsplit = nsplit_tail + n_extra;   // partials in all
   auto slot = [&](int i) { return i < nsplit_tail ? i : extra_base + (i - nsplit_tail); };
-  const int nacc = G * nsplit * D;
-  float* g_acc = stage;
-  float* g_m = g_acc + nacc;
-  float* g_l = g_m + G * nsplit;
-  if (G * nsplit <= kThreads && nacc + 2 * G * nsplit <= cap) {
-    float mv = 0.f, lv = 0.f;
-    if (tid < G * nsplit) {
-      const size_t pidx = (head0 + tid / nsplit) * a.max_splits + slot(tid % nsplit);
-      mv = __ldcg(a.ws_m + pidx);
-      lv = __ldcg(a.ws_l + pidx);
-    }
-    constexpr int kU = 8;  // float4 loads in flight per thread
-    for (int i0 = 0; i0 < nacc / 4; i0 += kU * kThreads) {
-      float4 v[kU];
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * kThreads + tid;
-        if (i < nacc / 4) {
-          const int e = 4 * i, row = e / (nsplit * D), rem = e - row * nsplit * D;
-          const int sp = rem / D, d = rem - sp * D;
-          v[u] = __ldcg(reinterpret_cast<const float4*>(
-              a.ws_acc + ((head0 + row) * a.max_splits + slot(sp)) * D + d));
-        }
-      }
-#pragma unroll
-      for (int u = 0; u < kU; ++u) {
-        const int i = i0 + u * kThreads + tid;
-        if (i < nacc / 4) reinterpret_cast<float4*>(g_acc)[i] = v[u];
-      }
-    }
-    if (tid < G * nsplit) {
-      g_m[tid] = mv;
-      g_l[tid] = lv;
-    }
-    __syncthreads();
+  if (gather_fits<D>(G, nsplit, cap)) {
+    gather_partials<D>(a, head0, nsplit, slot, stage);
+    const float* g_acc = stage;
+    const float* g_m = g_acc + G * nsplit * D;
+    const float* g_l = g_m + G * nsplit;
     for (int i = tid; i < G * D; i += kThreads) {
       const int row = i / D, d = i % D;
       float M = -CUDART_INF_F;
@@ -741,6 +762,65 @@ __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit_tail,
   }
 }
 
+// A pair's only split behind a shared prefix: combine the CTA's own result
+// (the warps' partials mS / lS / oS at the start of smem_f, nw warps of 16
+// rows) with the prefix pass's partials, slots max_splits - prefix_splits ..
+// max_splits - 1, into the output; the same sums, in the same order, as
+// merge_splits over the CTA's written partial and the pass's.  The CTA's
+// values are taken into registers first, so the gather may overwrite the
+// warps' partials.  `bad`: the CTA failed, its l and a become NaN.
+template <typename Q, int D>
+__device__ void merge_with_prefix(const DecodeArgs& a, size_t head0, int nw, bool bad,
+                                  float v_scale, float* smem_f) {
+  const int tid = threadIdx.x, G = a.group, n = a.prefix_splits;
+  const float* mS = smem_f;
+  const float* lS = mS + nw * 16;
+  const float* oS = lS + nw * 16;
+  constexpr int kE = (16 * D + kThreads - 1) / kThreads;   // elements per thread, G <= 16
+  float om[kE], ol[kE], oa[kE];
+#pragma unroll
+  for (int k = 0; k < kE; ++k) {
+    const int i = tid + k * kThreads;
+    om[k] = -CUDART_INF_F;
+    ol[k] = oa[k] = 0.f;
+    if (i < G * D) {
+      combine_warps(mS, lS, oS, nw, 16, i / D, i % D, D, om[k], ol[k], oa[k]);
+      oa[k] *= v_scale;
+      if (bad) ol[k] = oa[k] = CUDART_NAN_F;
+    }
+  }
+  __syncthreads();  // the warps' partials are read: the stage memory is free
+  const int base = a.max_splits - n;
+  gather_partials<D>(a, head0, n, [&](int i) { return base + i; }, smem_f);
+  const float* g_acc = smem_f;
+  const float* g_m = g_acc + G * n * D;
+  const float* g_l = g_m + G * n;
+#pragma unroll
+  for (int k = 0; k < kE; ++k) {
+    const int i = tid + k * kThreads;
+    if (i >= G * D) continue;
+    const int row = i / D, d = i % D;
+    float M = om[k];
+    for (int sp = 0; sp < n; ++sp) M = fmaxf(M, g_m[row * n + sp]);
+    float L, A;
+    if (M != -CUDART_INF_F) {
+      const float f0 = exp2f(om[k] - M);
+      L = fmaf(ol[k], f0, 0.f);
+      A = fmaf(oa[k], f0, 0.f);
+      for (int sp = 0; sp < n; ++sp) {
+        const float f = exp2f(g_m[row * n + sp] - M);
+        L = fmaf(g_l[row * n + sp], f, L);
+        A = fmaf(g_acc[(row * n + sp) * D + d], f, A);
+      }
+    } else {
+      L = ol[k];
+      A = 0.f;
+      for (int sp = 0; sp < n; ++sp) L += g_l[row * n + sp];
+    }
+    store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
+  }
+}
+
 // ------------------------------------------------------------------ kernel
 // Resident CTAs per SM the split kernel is compiled for: four for the E4M3
 // head-columns form (126 registers, a 48 KiB ring), three otherwise.
@@ -770,31 +850,19 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   const int P = a.prefix_tokens;
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: nothing that kernel may write is read before it has completed.
-  // Behind the shared-prefix pass, which waits for every kernel before it
-  // before it lets this grid start, nothing is waited for: the pass's
-  // partials meet this grid's through the arrival counters (whoever comes
-  // last merges), and the last CTA of this grid to finish waits for the
-  // pass, so that the grid never completes before it.
+  // Behind the shared-prefix pass, which itself waits for every kernel
+  // before it and then lets this grid start, the CTA streams its positions
+  // at once and waits for the pass to complete only before it reads the
+  // pass's partials.  Every pair's merging CTA does, so this grid never
+  // completes before the pass.
   if (P == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
-  auto finish = [&]() {
-    if (P > 0 && threadIdx.x == 0) {
-      const int total = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
-      if (atomicAdd(a.done, 1) == total - 1) {
-        asm volatile("griddepcontrol.wait;" ::: "memory");
-        atomicExch(a.done, 0);
-      }
-    }
-  };
   const int g = lane >> 2, q4 = lane & 3;
   const int G = a.group;
   const int ctx = a.ctx_lens[seq];
   const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T || (P > 0 && ctx <= P);
   const int own = bad_ctx ? 0 : ctx - P;  // positions this kernel attends
   const int nsplit = bad_ctx ? 1 : max(1, (own + a.partition - 1) / a.partition);
-  if (split >= nsplit) {
-    finish();
-    return;
-  }
+  if (split >= nsplit) return;  // the pair's split 0 holds its merge
   const HeadScales sc = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale,
                                     a.qk_scale, a.v_scale, a.k_inv, a.v_inv);
   // The pair's n_t tiles are shared out evenly: split i takes tiles
@@ -936,9 +1004,17 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   const int bad_bits = s_bad;
   if (tid == 0 && bad_bits != 0 && a.status != nullptr) atomicOr(a.status, bad_bits);
   const bool any_bad = bad_bits != 0;
-  // A lone split writes the output unless a shared-prefix partial joins it.
-  const bool direct = nsplit == 1 && P == 0;
   const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
+  constexpr int kCap = NS * G_::kStageBytes / 4;  // floats of stage memory
+  // A lone split behind a shared prefix merges its result with the pass's
+  // partials without writing it out or counting in.
+  if (nsplit == 1 && P > 0 && gather_fits<D>(G, a.prefix_splits, kCap)) {
+    asm volatile("griddepcontrol.wait;" ::: "memory");
+    merge_with_prefix<Q, D>(a, head0, kWarps, any_bad, sc.v, mS);
+    return;
+  }
+  // A lone split without one writes the output.
+  const bool direct = nsplit == 1 && P == 0;
   for (int i = tid; i < G * D; i += kThreads) {
     const int row = i / D, d = i % D;
     float M, L, A;
@@ -960,26 +1036,24 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   if (direct) return;
 
   // ------------------------------------------- split-K: the last CTA merges
-  // Each CTA counts itself in (an atomic counter, never a wait); the last of
-  // the pair's partials to arrive (its splits and, with a shared prefix, the
-  // prefix pass's key ranges) combines them all and resets the counter.
+  // Each CTA counts itself in (an atomic counter, never a wait on another
+  // CTA); the last of the pair's splits to arrive combines their partials
+  // (with a shared prefix, the pass's too, once the pass has completed) and
+  // resets the counter.
   __threadfence();
   __syncthreads();
-  const int n_extra = P > 0 ? a.prefix_splits : 0;
   if (tid == 0) {
     const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
-    s_last = prev == nsplit + n_extra - 1;
+    s_last = prev == nsplit - 1;
   }
   __syncthreads();
-  if (!s_last) {
-    finish();
-    return;
-  }
+  if (!s_last) return;
   __threadfence();
-  merge_splits<Q, D>(a, head0, nsplit, a.max_splits - a.prefix_splits, n_extra,
-                     reinterpret_cast<float*>(smem), NS * G_::kStageBytes / 4);
+  const int n_extra = P > 0 ? a.prefix_splits : 0;
+  if (n_extra > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  merge_splits<Q, D>(a, head0, nsplit, a.max_splits - n_extra, n_extra,
+                     reinterpret_cast<float*>(smem), kCap);
   if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
-  finish();
 }
 
 template <typename KV, int D, int NS>

@@ -1,9 +1,7 @@
-// Tensor-core decode attention kernels (split and persistent) for a BF16 cache with BF16 queries.
+// Tensor-core decode attention kernel for a BF16 cache with BF16 queries.
 #include "attention_tc_launch.cuh"
 
 namespace pkv {
 template pkv_status launch_decode_tc<BF16, BF16>(const DecodeArgs&, int, const CUtensorMap&,
-                                              const CUtensorMap&, cudaStream_t);
-template pkv_status launch_decode_pd<BF16, BF16>(const DecodeArgs&, int, const CUtensorMap&,
                                               const CUtensorMap&, cudaStream_t);
 }  // namespace pkv

@@ -6,7 +6,7 @@
 #include <atomic>
 #include <utility>
 
-#include "attention_persistent.cuh"
+#include "attention_tc.cuh"
 
 namespace pkv {
 namespace tc {
@@ -73,53 +73,7 @@ pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtenso
                       : launch_form<KV, Q, D, T, false>(a, kmap, vmap, st);
 }
 
-// Persistent kernel: two CTAs per SM, one wave.
-template <typename KV, typename Q, int D, int T>
-pkv_status launch_pd_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
-                        cudaStream_t st) {
-  constexpr int smem = pd::Layout<KV, D>::bytes;
-  auto kernel = pd::decode_pd_kernel<KV, Q, D, T>;
-  static std::atomic<uint64_t> configured{0};
-  static std::atomic<int> ctas[64];   // resident CTAs of the whole device
-  int dev = 0;
-  cudaError_t e = cudaGetDevice(&dev);
-  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaGetDevice", e);
-  const uint64_t bit = dev < 64 ? (uint64_t{1} << dev) : 0;
-  if (!bit || !(configured.load() & bit)) {
-    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
-    // all of the unified L1 / shared storage as shared memory: two CTAs per SM
-    if (e == cudaSuccess)
-      e = cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
-                               cudaSharedmemCarveoutMaxShared);
-    if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: cudaFuncSetAttribute", e);
-    int n = 0, occ = 0;
-    e = cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess) e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kernel, kThreads, smem);
-    if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: persistent occupancy", e);
-    if (occ < 1) return fail(PKV_ERR_UNSUPPORTED, "persistent kernel: no CTA fits on an SM");
-    if (dev < 64) ctas[dev].store(n * std::min(occ, pd::kCtasPerSm));
-    configured.fetch_or(bit);
-  }
-  const int grid = dev < 64 ? ctas[dev].load() : 152 * pd::kCtasPerSm;
-  e = launch_dependent(kernel, dim3(grid), kThreads, smem, st, a, kmap, vmap);
-  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: persistent launch", e);
-  return check_launch("pkv_attention_decode (persistent)");
-}
-
 }  // namespace tc
-
-template <typename KV, typename Q>
-pkv_status launch_decode_pd(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,
-                            const CUtensorMap& vmap, cudaStream_t st) {
-  const int T = a.block_size;
-  if constexpr (!std::is_same<KV, E4M3>::value) {
-    if (head_dim == 128 && T == 16) return tc::launch_pd_dt<KV, Q, 128, 16>(a, kmap, vmap, st);
-    if (head_dim == 128 && T == 32) return tc::launch_pd_dt<KV, Q, 128, 32>(a, kmap, vmap, st);
-    if (head_dim == 64 && T == 16) return tc::launch_pd_dt<KV, Q, 64, 16>(a, kmap, vmap, st);
-    if (head_dim == 64 && T == 32) return tc::launch_pd_dt<KV, Q, 64, 32>(a, kmap, vmap, st);
-  }
-  return fail(PKV_ERR_UNSUPPORTED, "persistent kernel: 16-bit caches with head_dim 64 or 128");
-}
 
 template <typename KV, typename Q>
 pkv_status launch_decode_tc(const DecodeArgs& a, int head_dim, const CUtensorMap& kmap,

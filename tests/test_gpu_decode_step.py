@@ -40,7 +40,7 @@ def scales_for(w):
 
 
 @pytest.mark.parametrize("name", list(CASES))
-@pytest.mark.parametrize("kernel", ["auto", "simt", "persistent"])
+@pytest.mark.parametrize("kernel", ["auto", "simt"])
 def test_fused_step_equals_write_then_attend(name, kernel):
     w = CASES[name]
     if kernel != "auto" and w.kv_dtype == "f32":

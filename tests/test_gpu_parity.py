@@ -75,11 +75,9 @@ def built():
     assert torch.cuda.is_available()
 
 
-@pytest.fixture(params=["simt", "tc", "persistent"])
+@pytest.fixture(params=["simt", "tc"])
 def kernel(request):
-    """Run a test once per decode kernel (CUDA-core, tensor-core split,
-    tensor-core persistent; the last falls back to the split kernel for the
-    shapes it does not cover)."""
+    """Run a test once per decode kernel (CUDA-core, tensor-core split)."""
     pkv.pkv_set_attention_kernel(request.param)
     yield request.param
     pkv.pkv_set_attention_kernel("auto")
@@ -93,7 +91,7 @@ def tc_covers(w):
 @pytest.mark.parametrize("name", list(SMALL))
 def test_step_matches_oracle(name, kernel):
     w = SMALL[name]
-    if kernel in ("tc", "persistent") and not tc_covers(w):
+    if kernel == "tc" and not tc_covers(w):
         pytest.skip("the tensor-core kernel does not cover this cache")
     sc = scales_for(w)
     dev = PS.materialize(PS.plan(w), "cuda", sc)
@@ -234,13 +232,12 @@ def test_invalid_table_entry_or_length_gives_nan(kernel):
     assert not torch.isnan(out).any()
 
 
-@pytest.mark.parametrize("which", ["tc", "persistent"])
+@pytest.mark.parametrize("which", ["tc"])
 def test_stage_wait_give_up_sets_status_and_nan_then_recovers(which):
-    """The decode kernels' failure path, run on purpose: with a stage-wait
+    """The decode kernel's failure path, run on purpose: with a stage-wait
     limit of 0 every CTA gives up at its first stage wait, still waits (with
     its own bounded limit) for the copies it has in flight, writes NaN and
-    sets PKV_DEVICE_WAIT_TIMEOUT (the persistent kernel's CTAs then finish
-    every unit they take with NaN); split partials merge into NaN and the
+    sets PKV_DEVICE_WAIT_TIMEOUT; split partials merge into NaN and the
     counters end at zero.  Afterwards the same call is correct."""
     w = SMALL["qwen_small"]
     pkv.pkv_set_attention_kernel(which)
@@ -258,7 +255,7 @@ def test_stage_wait_give_up_sets_status_and_nan_then_recovers(which):
     assert pkv.pkv_device_status(clear=True) & pkv.PKV_DEVICE_WAIT_TIMEOUT
     ctx = dev.plan.ctx
     assert torch.isnan(out[torch.from_numpy(ctx > 0)]).all()
-    n = len(dev.plan.seq_ids) * w.num_kv_heads + (2 if which == "persistent" else 0)
+    n = len(dev.plan.seq_ids) * w.num_kv_heads
     assert torch.count_nonzero(dev.workspace[: 4 * n]).item() == 0
     pkv.pkv_set_attention_kernel(which)
     try:
@@ -329,8 +326,8 @@ def test_kernels_agree(name):
     dev.write_step()
     outs = []
     try:
-        for k in ("simt", "tc", "persistent"):
-            pkv.pkv_set_attention_kernel(k)   # the workspace size follows the kernel choice
+        for k in ("simt", "tc"):
+            pkv.pkv_set_attention_kernel(k)
             ws = pkv.workspace_for(len(dev.plan.seq_ids), w.num_q_heads, dev.plan.max_blocks, dev.desc,
                                    dev.partition)
             outs.append(dev.attend(workspace=ws).double().cpu().numpy().copy())
@@ -358,7 +355,7 @@ def test_automatic_partition_with_edited_lengths(name, kernel):
     tokens, so that empty sequences, one-token sequences and tile edges sit
     between long ones."""
     w = SMALL[name]
-    if kernel in ("tc", "persistent") and not tc_covers(w):
+    if kernel == "tc" and not tc_covers(w):
         pytest.skip("the tensor-core kernel does not cover this cache")
     sc = scales_for(w)
     dev = PS.materialize(PS.plan(w), "cuda", sc, partition_tokens=0)
