@@ -858,13 +858,31 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   if (P == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
   const int g = lane >> 2, q4 = lane & 3;
   const int G = a.group;
+  const int32_t* trow = a.tables + static_cast<size_t>(seq) * a.max_blocks;
+  // Split 0 starts at position P whatever the length, so its query rows and
+  // the block ids of its first NS tiles (one per lane of warp 0) are fetched
+  // together with the length instead of after it; its first copies then go
+  // out without waiting for the rest of the CTA.
+  constexpr int kPre = NS * BPT;
+  static_assert(kPre <= 32, "one lane per early block id");
+  const bool early = split == 0;
+  int pre = -1;
+  if (early && warp == 0 && lane < kPre && P / T + lane < a.max_blocks) pre = trow[P / T + lane];
+  uint32_t qa[KS][HC ? 2 : 4];
+  const typename Q::raw* qrows = static_cast<const typename Q::raw*>(a.q) +
+      (static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G) * D;
+  auto load_query = [&]() {
+    if constexpr (HC) load_qt<KV, Q, D>(qa, qrows, G, g, q4);
+    else load_q<KV, Q, D>(qa, qrows, G, g, q4);
+  };
+  if (early) load_query();
+  const HeadScales sc = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale,
+                                    a.qk_scale, a.v_scale, a.k_inv, a.v_inv);
   const int ctx = a.ctx_lens[seq];
   const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T || (P > 0 && ctx <= P);
   const int own = bad_ctx ? 0 : ctx - P;  // positions this kernel attends
   const int nsplit = bad_ctx ? 1 : max(1, (own + a.partition - 1) / a.partition);
   if (split >= nsplit) return;  // the pair's split 0 holds its merge
-  const HeadScales sc = head_scales(a.head_scales, a.num_kv_heads, kvh, a.softmax_scale,
-                                    a.qk_scale, a.v_scale, a.k_inv, a.v_inv);
   // The pair's n_t tiles are shared out evenly: split i takes tiles
   // [i n_t / nsplit, (i + 1) n_t / nsplit), at most partition / 64 of them.
   // Near-equal pieces keep the longest units of the grid on pairs that need
@@ -892,18 +910,22 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     fence_proxy_async();
   }
-  for (int i = tid; i < n_blk; i += kThreads)
-    s_tab[i] = a.tables[static_cast<size_t>(seq) * a.max_blocks + first_blk + i];
+  // the split's block ids (split 0: those past warp 0's early ones)
+  for (int i = (early ? kPre : 0) + tid; i < n_blk; i += kThreads) s_tab[i] = trow[first_blk + i];
 
   // Fused slot write: the split holding position ctx - 1 stores the step's
   // token of its KV head before any copy is issued (a block never spans two
   // splits, and other heads' rows are disjoint, so no other CTA reads it).
-  if (a.k_new != nullptr && !bad_ctx && ctx > 0 && split == nsplit - 1) {
+  // Warp 0 writes, and issues every copy after it.
+  constexpr int kUnits = D / 8;
+  static_assert(2 * kUnits <= 32, "warp 0 writes the step's K and V rows");
+  if (a.k_new != nullptr && !bad_ctx && ctx > 0 && split == nsplit - 1 && warp == 0) {
     const int p = ctx - 1;
-    const int blk = a.tables[static_cast<size_t>(seq) * a.max_blocks + p / T];
-    constexpr int kUnits = D / 8;
-    if (blk >= 0 && blk < a.num_blocks && tid < 2 * kUnits) {
-      const int which = tid / kUnits, d0 = (tid % kUnits) * 8;
+    const int lb = p / T - first_blk;  // its block within the split
+    int blk = __shfl_sync(0xffffffffu, pre, lb & 31);
+    if (!(early && lb < kPre)) blk = trow[p / T];
+    if (blk >= 0 && blk < a.num_blocks && lane < 2 * kUnits) {
+      const int which = lane / kUnits, d0 = (lane % kUnits) * 8;
       const size_t src = (static_cast<size_t>(seq) * a.num_kv_heads + kvh) * D + d0;
       const size_t dst = ((static_cast<size_t>(blk) * a.num_kv_heads + kvh) * T + p % T) * D + d0;
       store8<Q, KV>(static_cast<const typename Q::raw*>(which ? a.v_new : a.k_new) + src,
@@ -912,14 +934,6 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
       asm volatile("fence.proxy.async.global;" ::: "memory");  // before the TMA reads it
     }
   }
-  uint32_t qa[KS][HC ? 2 : 4];
-  {
-    const typename Q::raw* qrows = static_cast<const typename Q::raw*>(a.q) +
-        (static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G) * D;
-    if constexpr (HC) load_qt<KV, Q, D>(qa, qrows, G, g, q4);
-    else load_q<KV, Q, D>(qa, qrows, G, g, q4);
-  }
-  __syncthreads();
 
   // ---------------------------------------------------------- producer
   // Warp 0 refills a stage with one warp instruction: lane l issues box l
@@ -951,7 +965,16 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
       tma_box<KV, D>(smem_u32(kt + (isv ? G_::kTileBytes : 0) + blk * kBoxBytes), isv ? &vmap : &kmap,
                      (phys * a.num_kv_heads + kvh) * T, bar);
   };
-  if (warp == 0)
+  if (early && warp == 0) {
+    // the early block ids: to shared memory (the refills and the table checks
+    // read them there), then the first tiles' copies
+    if (lane < kPre && lane < n_blk) s_tab[lane] = pre;
+    __syncwarp();
+    for (int t = 0; t < NS && t < n_tiles; ++t) issue(t);
+  }
+  if (!early) load_query();
+  __syncthreads();
+  if (!early && warp == 0)
     for (int t = 0; t < NS && t < n_tiles; ++t) issue(t);
 
   // ---------------------------------------------------------- consumers
