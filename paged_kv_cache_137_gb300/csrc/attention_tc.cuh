@@ -848,6 +848,10 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   // Positions [0, P) are attended by the shared-prefix pass (P = 0: none);
   // this CTA covers part of [P, ctx).
   const int P = a.prefix_tokens;
+  // the two tensor maps: fetched while the grid waits for its inputs
+  if (warp == 0 && lane < 2)
+    asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(lane ? &vmap : &kmap))
+                 : "memory");
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: nothing that kernel may write is read before it has completed.
   // Behind the shared-prefix pass, which itself waits for every kernel
@@ -883,6 +887,21 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   const int own = bad_ctx ? 0 : ctx - P;  // positions this kernel attends
   const int nsplit = bad_ctx ? 1 : max(1, (own + a.partition - 1) / a.partition);
   if (split >= nsplit) return;  // the pair's split 0 holds its merge
+  const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
+  // A lone split behind a shared prefix reads the pass's partials at its end:
+  // warps 1.. ask L2 for their lines now (L2 is where the pass's writes land,
+  // so a line fetched before the pass writes it is updated, never stale).
+  if (P > 0 && nsplit == 1 && warp > 0 && a.ws_acc != nullptr) {
+    const int n = a.prefix_splits;
+    const int acc_lines = (n * D * 4 + 127) / 128, per_row = acc_lines + 2;
+    for (int i = tid - 32; i < G * per_row; i += kThreads - 32) {
+      const int row = i / per_row, k = i % per_row;
+      const size_t pidx = (head0 + row) * a.max_splits + (a.max_splits - n);
+      const float* line = k < acc_lines ? a.ws_acc + pidx * D + 32 * k
+                                        : (k == acc_lines ? a.ws_m : a.ws_l) + pidx;
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
+    }
+  }
   // The pair's n_t tiles are shared out evenly: split i takes tiles
   // [i n_t / nsplit, (i + 1) n_t / nsplit), at most partition / 64 of them.
   // Near-equal pieces keep the longest units of the grid on pairs that need
@@ -1027,7 +1046,6 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   const int bad_bits = s_bad;
   if (tid == 0 && bad_bits != 0 && a.status != nullptr) atomicOr(a.status, bad_bits);
   const bool any_bad = bad_bits != 0;
-  const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
   constexpr int kCap = NS * G_::kStageBytes / 4;  // floats of stage memory
   // A lone split behind a shared prefix merges its result with the pass's
   // partials without writing it out or counting in.

@@ -8,6 +8,7 @@
 #include <cuda_fp16.h>
 #include <stdint.h>
 
+#include <atomic>
 #include <type_traits>
 
 #include "common.h"
@@ -152,6 +153,26 @@ template <> __device__ __forceinline__ float load_elem<BF16>(const void* b, size
 }
 
 // ------------------------------------------------------------ host side
+// Ask once per device for the largest shared-memory carveout for `kernel` (a
+// hint the driver may follow).  The attention kernels run with it; a small
+// kernel launched between them that asks for the same split spares the SMs a
+// reconfiguration of their shared memory and L1.  Failures are cleared and
+// ignored (the kernel then runs with the driver's choice).
+template <typename Kernel>
+inline void prefer_max_shared(Kernel kernel, std::atomic<uint64_t>& configured) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) {
+    (void)cudaGetLastError();
+    return;
+  }
+  const uint64_t bit = uint64_t{1} << dev;
+  if (configured.load() & bit) return;
+  if (cudaFuncSetAttribute(kernel, cudaFuncAttributePreferredSharedMemoryCarveout,
+                           cudaSharedmemCarveoutMaxShared) != cudaSuccess)
+    (void)cudaGetLastError();
+  configured.fetch_or(bit);
+}
+
 inline pkv_status check_launch(const char* what) {
   const cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) {

@@ -11,6 +11,7 @@
 // (pair, layer, K|V) tile for the copy.  The copy takes its pairs and layer
 // pointers as kernel parameters, so it needs no device-side staging buffer.
 #include <algorithm>
+#include <atomic>
 #include <type_traits>
 
 #include "device_common.cuh"
@@ -125,6 +126,8 @@ pkv_status launch_write(const WriteArgs& a, cudaStream_t st) {
   const int64_t units = a.n_tokens * a.n_kv * (a.head_dim / 8);
   const int threads = 256;
   const int64_t blocks = std::min<int64_t>((units + threads - 1) / threads, 4096);
+  static std::atomic<uint64_t> carveout{0};
+  prefer_max_shared(write_kernel<Src, Dst>, carveout);
   write_kernel<Src, Dst><<<dim3(static_cast<unsigned>(blocks), 2), threads, 0, st>>>(a);
   return check_launch("pkv_write");
 }
@@ -207,6 +210,8 @@ extern "C" pkv_status pkv_copy_blocks(void* const* k_caches, void* const* v_cach
   a.block_bytes = static_cast<int64_t>(desc->num_kv_heads) * desc->block_size * desc->head_dim *
                   pkv_dtype_bytes(desc->kv_dtype);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
+  static std::atomic<uint64_t> carveout{0};
+  prefer_max_shared(copy_blocks_kernel, carveout);
   for (int32_t base = 0; base < n_pairs; base += kMaxCopyPairs) {
     const int32_t n = std::min(kMaxCopyPairs, n_pairs - base);
     for (int32_t i = 0; i < n; ++i) {
@@ -224,6 +229,8 @@ namespace pkv {
 
 template <typename Src, typename Dst>
 static pkv_status launch_write_last_dt(const WriteLastArgs& a, int32_t num_seqs, cudaStream_t st) {
+  static std::atomic<uint64_t> carveout{0};
+  prefer_max_shared(write_last_kernel<Src, Dst>, carveout);
   write_last_kernel<Src, Dst><<<dim3(num_seqs, 2), 128, 0, st>>>(a);
   return check_launch("pkv_decode_step (write)");
 }
