@@ -79,18 +79,20 @@ int32_t auto_partition(int64_t num_seqs, int64_t num_kv_heads, int64_t max_ctx, 
 size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 struct WsLayout {
-  size_t counter_off, m_off, l_off, acc_off, bytes;
+  size_t counter_off, done_off, m_off, l_off, acc_off, bytes;
 };
 
 // Workspace: split-K arrival counters [B][N_kv] (zero between calls), then
-// the partial maxima, sums and unnormalised outputs, each part 256-byte
-// aligned.  Nothing without splits.
+// extra_ints more (behind a shared-prefix pass: the decode grid's exit
+// count), then the partial maxima, sums and unnormalised outputs, each part
+// 256-byte aligned.  Nothing without splits.
 WsLayout workspace_layout(int64_t num_seqs, int64_t num_q_heads, int64_t num_kv_heads,
-                          int64_t splits, int64_t head_dim) {
+                          int64_t splits, int64_t head_dim, int extra_ints = 0) {
   WsLayout w{};
   if (splits <= 1) return w;
-  const size_t counters = static_cast<size_t>(num_seqs * num_kv_heads);
+  const size_t counters = static_cast<size_t>(num_seqs * num_kv_heads) + extra_ints;
   w.counter_off = 0;
+  w.done_off = static_cast<size_t>(num_seqs * num_kv_heads) * sizeof(int);
   w.m_off = align_up(counters * sizeof(int), 256);
   const size_t n = static_cast<size_t>(num_seqs * num_q_heads * splits);
   w.l_off = w.m_off + align_up(n * sizeof(float), 256);
@@ -173,8 +175,10 @@ int64_t num_splits(int32_t max_blocks, int32_t block_size, int32_t partition,
 }
 
 // Shared-prefix pass geometry: the key ranges of the P prefix positions.
-// Each of the n_kv * ceil(rows / 256) row units gets enough ranges that the
-// pass has about one CTA per SM (it holds a whole SM); ranges are whole
+// A pass CTA holds a whole SM, and the decode kernel behind it streams the
+// positions past the prefix on the SMs the pass leaves free, so the pass
+// takes about a quarter of the SMs: each of the n_kv * ceil(rows / 256) row
+// units gets that share of key ranges (at least one); ranges are whole
 // 64-key tiles.
 struct PrefixPlan {
   int32_t tokens = 0, key_splits = 0, split_tokens = 0, seqs_per_cta = 0;
@@ -186,7 +190,8 @@ PrefixPlan prefix_plan(int64_t num_seqs, int64_t group, int64_t num_kv_heads, in
   p.seqs_per_cta = static_cast<int32_t>(256 / group);
   const int64_t units = (num_seqs + p.seqs_per_cta - 1) / p.seqs_per_cta * num_kv_heads;
   const int64_t tiles = (prefix_tokens + 63) / 64;
-  const int64_t want = std::max<int64_t>(1, std::min<int64_t>(tiles, device_sms() / std::max<int64_t>(units, 1)));
+  const int64_t want =
+      std::max<int64_t>(1, std::min<int64_t>(tiles, device_sms() / (4 * std::max<int64_t>(units, 1))));
   const int64_t per = (tiles + want - 1) / want;
   p.tokens = static_cast<int32_t>(prefix_tokens);
   p.split_tokens = static_cast<int32_t>(per * 64);
@@ -228,7 +233,8 @@ pkv_status plan_call(const pkv_kv_desc* d, int q_dtype, float softmax_scale, int
   pkv_status st = resolve_partition(partition_tokens, num_seqs, max_blocks, d, &c.partition, c.pp.tokens);
   if (st != PKV_OK) return st;
   c.splits = num_splits(max_blocks, d->block_size, c.partition, c.pp.tokens) + c.pp.key_splits;
-  c.ws = workspace_layout(num_seqs, num_q_heads, d->num_kv_heads, c.splits, d->head_dim);
+  c.ws = workspace_layout(num_seqs, num_q_heads, d->num_kv_heads, c.splits, d->head_dim,
+                          c.prefix_pass ? 1 : 0);
   *out = c;
   return PKV_OK;
 }
@@ -425,6 +431,7 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   a.softmax_scale = softmax_scale;
   a.prefix_tokens = pp.tokens;
   a.prefix_splits = pp.key_splits;
+  a.done = prefix_pass ? reinterpret_cast<int*>(wsb + ws.done_off) : nullptr;
   a.status = status;
   a.wait_ns = stage_wait_limit_ns();
 
@@ -450,8 +457,8 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   }
   if (prefix_pass) {
     // the prefix pass first: its CTAs let the decode kernel start once they
-    // have all begun; the decode kernel's CTAs wait for the whole pass (a
-    // grid dependency wait, not a flag) before they read its partials
+    // have all begun, on the SMs the pass leaves free; the pairs' partials
+    // meet through the arrival counters (whoever arrives last merges)
     PrefillArgs pa{};
     pa.q = q;
     pa.tables = block_tables;
@@ -475,6 +482,10 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
     pa.ws_m = a.ws_m;
     pa.ws_l = a.ws_l;
     pa.ws_acc = a.ws_acc;
+    pa.out = out;
+    pa.ctx_lens = context_lens;
+    pa.counters = a.counters;
+    pa.partition = partition;
     pa.sp_seqs = pp.seqs_per_cta;
     CUtensorMap pkmap, pvmap;
     st = pool_map(&pkmap, k_cache, desc, false);

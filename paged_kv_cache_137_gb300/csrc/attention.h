@@ -41,11 +41,12 @@ struct DecodeArgs {
   // shared prefix (0: none): positions [0, prefix_tokens) of every sequence
   // are attended by the shared-prefix pass, the kernel launched just before
   // this one, whose prefix_splits partials sit in the last prefix_splits of
-  // the max_splits slots; this kernel covers [prefix_tokens, ctx) and merges
-  // everything once that pass has completed
+  // the max_splits slots; this kernel covers [prefix_tokens, ctx), and the
+  // last of a pair's partials to arrive (its splits and the pass's) merges
   int32_t prefix_tokens, prefix_splits;
   int* status;               // device error word (PKV_DEVICE_* bits, atomicOr)
   uint64_t wait_ns;          // give-up limit of a stage wait; 0 = give up at once
+  int* done;                 // behind a shared-prefix pass: CTAs of this grid that have finished
 };
 
 // Prefill / shared-prefix pass arguments (attention_prefill.cu,
@@ -70,11 +71,15 @@ struct PrefillArgs {
   // the keys are positions [k * sp_split, min(sp_tokens, (k + 1) * sp_split))
   // of table row 0; row (s, j)'s partial (max, sum, unnormalised output)
   // goes to split slot sp_slot0 + k of the decode workspace (ws_*, max_splits
-  // slots), which the decode kernel behind the pass merges.
-  int32_t sp_rows, sp_tokens, sp_split, sp_slot0, max_splits, sp_seqs;
+  // slots).  Each CTA then counts itself in on counters[s][kvh] (with the
+  // decode kernel's splits of the positions past the prefix, partition tokens
+  // each, and the pass's key ranges), and the rows of the pairs whose last
+  // partial it is merge them all into out.
+  int32_t sp_rows, sp_tokens, sp_split, sp_slot0, max_splits, sp_seqs, partition;
   float* ws_m;
   float* ws_l;
   float* ws_acc;
+  int* counters;
 };
 
 // Device error word of the current device (looked up once per device);

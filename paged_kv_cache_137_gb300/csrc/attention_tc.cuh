@@ -762,65 +762,6 @@ __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit_tail,
   }
 }
 
-// A pair's only split behind a shared prefix: combine the CTA's own result
-// (the warps' partials mS / lS / oS at the start of smem_f, nw warps of 16
-// rows) with the prefix pass's partials, slots max_splits - prefix_splits ..
-// max_splits - 1, into the output; the same sums, in the same order, as
-// merge_splits over the CTA's written partial and the pass's.  The CTA's
-// values are taken into registers first, so the gather may overwrite the
-// warps' partials.  `bad`: the CTA failed, its l and a become NaN.
-template <typename Q, int D>
-__device__ void merge_with_prefix(const DecodeArgs& a, size_t head0, int nw, bool bad,
-                                  float v_scale, float* smem_f) {
-  const int tid = threadIdx.x, G = a.group, n = a.prefix_splits;
-  const float* mS = smem_f;
-  const float* lS = mS + nw * 16;
-  const float* oS = lS + nw * 16;
-  constexpr int kE = (16 * D + kThreads - 1) / kThreads;   // elements per thread, G <= 16
-  float om[kE], ol[kE], oa[kE];
-#pragma unroll
-  for (int k = 0; k < kE; ++k) {
-    const int i = tid + k * kThreads;
-    om[k] = -CUDART_INF_F;
-    ol[k] = oa[k] = 0.f;
-    if (i < G * D) {
-      combine_warps(mS, lS, oS, nw, 16, i / D, i % D, D, om[k], ol[k], oa[k]);
-      oa[k] *= v_scale;
-      if (bad) ol[k] = oa[k] = CUDART_NAN_F;
-    }
-  }
-  __syncthreads();  // the warps' partials are read: the stage memory is free
-  const int base = a.max_splits - n;
-  gather_partials<D>(a, head0, n, [&](int i) { return base + i; }, smem_f);
-  const float* g_acc = smem_f;
-  const float* g_m = g_acc + G * n * D;
-  const float* g_l = g_m + G * n;
-#pragma unroll
-  for (int k = 0; k < kE; ++k) {
-    const int i = tid + k * kThreads;
-    if (i >= G * D) continue;
-    const int row = i / D, d = i % D;
-    float M = om[k];
-    for (int sp = 0; sp < n; ++sp) M = fmaxf(M, g_m[row * n + sp]);
-    float L, A;
-    if (M != -CUDART_INF_F) {
-      const float f0 = exp2f(om[k] - M);
-      L = fmaf(ol[k], f0, 0.f);
-      A = fmaf(oa[k], f0, 0.f);
-      for (int sp = 0; sp < n; ++sp) {
-        const float f = exp2f(g_m[row * n + sp] - M);
-        L = fmaf(g_l[row * n + sp], f, L);
-        A = fmaf(g_acc[(row * n + sp) * D + d], f, A);
-      }
-    } else {
-      L = ol[k];
-      A = 0.f;
-      for (int sp = 0; sp < n; ++sp) L += g_l[row * n + sp];
-    }
-    store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
-  }
-}
-
 // ------------------------------------------------------------------ kernel
 // Resident CTAs per SM the split kernel is compiled for: four for the E4M3
 // head-columns form (126 registers, a 48 KiB ring), three otherwise.
@@ -855,11 +796,21 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   // Launched as a programmatic dependent of the previous kernel in the
   // stream: nothing that kernel may write is read before it has completed.
   // Behind the shared-prefix pass, which itself waits for every kernel
-  // before it and then lets this grid start, the CTA streams its positions
-  // at once and waits for the pass to complete only before it reads the
-  // pass's partials.  Every pair's merging CTA does, so this grid never
-  // completes before the pass.
+  // before it and then lets this grid start on the SMs it leaves free,
+  // nothing is waited for: the pass's partials meet this grid's through the
+  // arrival counters (whoever arrives last merges), and the last CTA of this
+  // grid to finish waits for the pass, so that the grid never completes
+  // before it (a pass CTA may write the outputs of the pairs it completes).
   if (P == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  auto finish = [&]() {
+    if (P > 0 && threadIdx.x == 0) {
+      const int total = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
+      if (atomicAdd(a.done, 1) == total - 1) {
+        asm volatile("griddepcontrol.wait;" ::: "memory");
+        atomicExch(a.done, 0);
+      }
+    }
+  };
   const int g = lane >> 2, q4 = lane & 3;
   const int G = a.group;
   const int32_t* trow = a.tables + static_cast<size_t>(seq) * a.max_blocks;
@@ -886,12 +837,15 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   const bool bad_ctx = ctx < 0 || ctx > a.max_blocks * T || (P > 0 && ctx <= P);
   const int own = bad_ctx ? 0 : ctx - P;  // positions this kernel attends
   const int nsplit = bad_ctx ? 1 : max(1, (own + a.partition - 1) / a.partition);
-  if (split >= nsplit) return;  // the pair's split 0 holds its merge
+  if (split >= nsplit) {
+    finish();
+    return;
+  }
   const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
-  // A lone split behind a shared prefix reads the pass's partials at its end:
-  // warps 1.. ask L2 for their lines now (L2 is where the pass's writes land,
-  // so a line fetched before the pass writes it is updated, never stale).
-  if (P > 0 && nsplit == 1 && warp > 0 && a.ws_acc != nullptr) {
+  // Behind a shared prefix the merging CTA reads the pass's partials: warps
+  // 1.. ask L2 for their lines now (L2 is where the pass's writes land, so a
+  // line fetched before the pass writes it is updated, never stale).
+  if (P > 0 && warp > 0 && a.ws_acc != nullptr) {
     const int n = a.prefix_splits;
     const int acc_lines = (n * D * 4 + 127) / 128, per_row = acc_lines + 2;
     for (int i = tid - 32; i < G * per_row; i += kThreads - 32) {
@@ -1047,14 +1001,7 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
   if (tid == 0 && bad_bits != 0 && a.status != nullptr) atomicOr(a.status, bad_bits);
   const bool any_bad = bad_bits != 0;
   constexpr int kCap = NS * G_::kStageBytes / 4;  // floats of stage memory
-  // A lone split behind a shared prefix merges its result with the pass's
-  // partials without writing it out or counting in.
-  if (nsplit == 1 && P > 0 && gather_fits<D>(G, a.prefix_splits, kCap)) {
-    asm volatile("griddepcontrol.wait;" ::: "memory");
-    merge_with_prefix<Q, D>(a, head0, kWarps, any_bad, sc.v, mS);
-    return;
-  }
-  // A lone split without one writes the output.
+  // A lone split writes the output unless a shared-prefix partial joins it.
   const bool direct = nsplit == 1 && P == 0;
   for (int i = tid; i < G * D; i += kThreads) {
     const int row = i / D, d = i % D;
@@ -1078,23 +1025,26 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
 
   // ------------------------------------------- split-K: the last CTA merges
   // Each CTA counts itself in (an atomic counter, never a wait on another
-  // CTA); the last of the pair's splits to arrive combines their partials
-  // (with a shared prefix, the pass's too, once the pass has completed) and
-  // resets the counter.
+  // CTA); the last of the pair's partials to arrive (its splits and, with a
+  // shared prefix, the pass's key ranges) combines them all and resets the
+  // counter.
   __threadfence();
   __syncthreads();
+  const int n_extra = P > 0 ? a.prefix_splits : 0;
   if (tid == 0) {
     const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
-    s_last = prev == nsplit - 1;
+    s_last = prev == nsplit + n_extra - 1;
   }
   __syncthreads();
-  if (!s_last) return;
+  if (!s_last) {
+    finish();
+    return;
+  }
   __threadfence();
-  const int n_extra = P > 0 ? a.prefix_splits : 0;
-  if (n_extra > 0) asm volatile("griddepcontrol.wait;" ::: "memory");
   merge_splits<Q, D>(a, head0, nsplit, a.max_splits - n_extra, n_extra,
                      reinterpret_cast<float*>(smem), kCap);
   if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
+  finish();
 }
 
 template <typename KV, int D, int NS>
