@@ -33,7 +33,13 @@ constexpr int kMaxPartition = 8192;
 constexpr int kMultiWavePartition = 4096;  // the smallest split when the pairs fill two waves
 // Resident tensor-core split CTAs per SM: four for E4M3 caches (the
 // head-columns kernel that every query group up to 8 takes), else three.
-int resident_split_ctas(const pkv_kv_desc* d) { return d->kv_dtype == PKV_E4M3 ? 4 : 3; }
+// Resident CTAs per SM of the tensor-core split kernel: four for E4M3, three
+// otherwise, six in the two-warp form 16-bit head_dim-128 caches take behind
+// a shared-prefix pass.
+int resident_split_ctas(const pkv_kv_desc* d, bool behind_prefix = false) {
+  if (d->kv_dtype == PKV_E4M3) return 4;
+  return behind_prefix && d->head_dim == 128 ? 6 : 3;
+}
 constexpr int kDefaultSms = 152;       // used when no device can be queried
 
 int device_sms() {
@@ -164,7 +170,7 @@ pkv_status resolve_partition(int32_t requested, int32_t num_seqs, int32_t max_bl
   }
   *out = auto_partition(num_seqs, d->num_kv_heads,
                         static_cast<int64_t>(max_blocks) * d->block_size - prefix_tokens,
-                        d->block_size, resident_split_ctas(d));
+                        d->block_size, resident_split_ctas(d, prefix_tokens > 0));
   return PKV_OK;
 }
 

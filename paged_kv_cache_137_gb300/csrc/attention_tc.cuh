@@ -44,19 +44,24 @@
 namespace pkv {
 namespace tc {
 
-constexpr int kWarps = 4;
+constexpr int kWarps = 4;                 // warps of the split kernel's CTA (or 2: see below)
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 64;                 // tokens per stage, 16 per warp
 constexpr int kMaxTableEntries = 1024;    // block ids of one split kept in shared memory
+// The two-warp form (16-bit head_dim-128 caches behind a shared-prefix pass):
+// 32-token stages of 16 KiB, six CTAs per SM, at most 512 block ids a split.
+constexpr int kMaxTableEntries2 = 512;
+template <int W>
+constexpr int max_table_entries() { return W == 2 ? kMaxTableEntries2 : kMaxTableEntries; }
 constexpr uint64_t kWaitNs = 50000000ull;  // a stage wait gives up after 50 ms
 constexpr uint64_t kDrainNs = 10000000ull; // after a give-up, 10 ms per copy in flight
 
-template <typename KV, int D>
+template <typename KV, int D, int W = kWarps>
 struct Geom {
   static constexpr int kElemBytes = KV::bytes;
   static constexpr int kRowBytes = D * kElemBytes;
   static constexpr int kSlabs = kRowBytes / 128;  // 128-byte column slabs per row (1 or 2)
-  static constexpr int kTileBytes = kTile * kRowBytes;
+  static constexpr int kTileBytes = 16 * W * kRowBytes;  // 16 tokens per warp
   static constexpr int kStageBytes = 2 * kTileBytes;  // K and V
   static_assert(kRowBytes % 128 == 0, "rows must be whole 128-byte slabs");
 };
@@ -656,10 +661,10 @@ __device__ __forceinline__ void combine_warps(const float* mS, const float* lS, 
 }
 
 // Whether the partials of nsplit split slots of a query group fit the
-// shared-memory gather below (`cap` floats).
-template <int D>
+// shared-memory gather below (`cap` floats, NT threads).
+template <int D, int NT>
 __device__ __forceinline__ bool gather_fits(int G, int nsplit, int cap) {
-  return G * nsplit <= kThreads && G * nsplit * (D + 2) <= cap;
+  return G * nsplit <= NT && G * nsplit * (D + 2) <= cap;
 }
 
 // Gather the partials (m, l, a) of the G heads at head0 from the split slots
@@ -667,7 +672,7 @@ __device__ __forceinline__ bool gather_fits(int G, int nsplit, int cap) {
 // and l [G][nsplit].  Every load is a global round trip of several
 // microseconds while the GPU streams, so they are all issued before any is
 // used.  Ends with a CTA barrier.
-template <int D, typename Slot>
+template <int D, int NT, typename Slot>
 __device__ void gather_partials(const DecodeArgs& a, size_t head0, int nsplit, Slot slot,
                                 float* stage) {
   const int tid = threadIdx.x, G = a.group;
@@ -682,11 +687,11 @@ __device__ void gather_partials(const DecodeArgs& a, size_t head0, int nsplit, S
     lv = __ldcg(a.ws_l + pidx);
   }
   constexpr int kU = 8;  // float4 loads in flight per thread
-  for (int i0 = 0; i0 < nacc / 4; i0 += kU * kThreads) {
+  for (int i0 = 0; i0 < nacc / 4; i0 += kU * NT) {
     float4 v[kU];
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      const int i = i0 + u * kThreads + tid;
+      const int i = i0 + u * NT + tid;
       if (i < nacc / 4) {
         const int e = 4 * i, row = e / (nsplit * D), rem = e - row * nsplit * D;
         const int sp = rem / D, d = rem - sp * D;
@@ -696,7 +701,7 @@ __device__ void gather_partials(const DecodeArgs& a, size_t head0, int nsplit, S
     }
 #pragma unroll
     for (int u = 0; u < kU; ++u) {
-      const int i = i0 + u * kThreads + tid;
+      const int i = i0 + u * NT + tid;
       if (i < nacc / 4) reinterpret_cast<float4*>(g_acc)[i] = v[u];
     }
   }
@@ -712,18 +717,18 @@ __device__ void gather_partials(const DecodeArgs& a, size_t head0, int nsplit, S
 // extra_base + n_extra - 1:  M = max m_i, L = sum l_i 2^(m_i - M),
 // o = sum a_i 2^(m_i - M) / L.  The partials are gathered into shared
 // memory (stage, `cap` floats) first where they fit.
-template <typename Q, int D>
+template <typename Q, int D, int NT>
 __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit_tail, int extra_base,
                              int n_extra, float* stage, int cap) {
   const int tid = threadIdx.x, G = a.group;
   const int nsplit = nsplit_tail + n_extra;   // partials in all
   auto slot = [&](int i) { return i < nsplit_tail ? i : extra_base + (i - nsplit_tail); };
-  if (gather_fits<D>(G, nsplit, cap)) {
-    gather_partials<D>(a, head0, nsplit, slot, stage);
+  if (gather_fits<D, NT>(G, nsplit, cap)) {
+    gather_partials<D, NT>(a, head0, nsplit, slot, stage);
     const float* g_acc = stage;
     const float* g_m = g_acc + G * nsplit * D;
     const float* g_l = g_m + G * nsplit;
-    for (int i = tid; i < G * D; i += kThreads) {
+    for (int i = tid; i < G * D; i += NT) {
       const int row = i / D, d = i % D;
       float M = -CUDART_INF_F;
       for (int sp = 0; sp < nsplit; ++sp) M = fmaxf(M, g_m[row * nsplit + sp]);
@@ -742,7 +747,7 @@ __device__ void merge_splits(const DecodeArgs& a, size_t head0, int nsplit_tail,
       store_elem<Q>(a.out, (head0 + row) * D + d, (L > 0.f || L != L) ? A / L : 0.f);
     }
   } else {
-    for (int i = tid; i < G * D; i += kThreads) {
+    for (int i = tid; i < G * D; i += NT) {
       const int row = i / D, d = i % D;
       const size_t base = (head0 + row) * a.max_splits;
       float M = -CUDART_INF_F;
@@ -770,12 +775,16 @@ constexpr int split_ctas_per_sm() {
   return HC && std::is_same<KV, E4M3>::value ? 4 : 3;
 }
 
-// HC: the head-columns form of the tile products (query group <= 8).
-template <typename KV, typename Q, int D, int T, int NS, bool HC>
-__global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
+// HC: the head-columns form of the tile products (query group <= 8).  W:
+// warps per CTA, 16 tokens of each W * 16-token tile per warp (4; or 2, six
+// CTAs per SM, for short contexts past a shared prefix).
+template <typename KV, typename Q, int D, int T, int NS, bool HC, int W = kWarps>
+__global__ void __launch_bounds__(32 * W, W == 2 ? 6 : split_ctas_per_sm<KV, HC>())
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
-  using G_ = Geom<KV, D>;
+  using G_ = Geom<KV, D, W>;
+  constexpr int kWarps = W, kThreads = 32 * W, kTile = 16 * W;
+  constexpr int kMaxTableEntries = max_table_entries<W>();
   using State = std::conditional_t<HC, WarpStateT<D>, WarpState<D>>;
   constexpr int KS = D / 16;        // k-steps of q . K^T
   constexpr int BPT = kTile / T;    // blocks per tile
@@ -1041,15 +1050,15 @@ __global__ void __launch_bounds__(kThreads, split_ctas_per_sm<KV, HC>())
     return;
   }
   __threadfence();
-  merge_splits<Q, D>(a, head0, nsplit, a.max_splits - n_extra, n_extra,
-                     reinterpret_cast<float*>(smem), kCap);
+  merge_splits<Q, D, kThreads>(a, head0, nsplit, a.max_splits - n_extra, n_extra,
+                               reinterpret_cast<float*>(smem), kCap);
   if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
   finish();
 }
 
-template <typename KV, int D, int NS>
+template <typename KV, int D, int NS, int W = kWarps>
 constexpr int smem_bytes() {
-  return NS * Geom<KV, D>::kStageBytes + kMaxTableEntries * 4 + NS * 8 + 1024;
+  return NS * Geom<KV, D, W>::kStageBytes + max_table_entries<W>() * 4 + NS * 8 + 1024;
 }
 
 }  // namespace tc

@@ -31,19 +31,21 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, int threads, 
 }
 
 // Stages per CTA: 64 KiB of ring at three CTAs per SM (2 x 32 KiB or
-// 4 x 16 KiB), 48 KiB (3 x 16 KiB) at four.
-template <typename KV, int D, bool HC>
+// 4 x 16 KiB), 48 KiB (3 x 16 KiB) at four; the two-warp form: 2 x 16 KiB at
+// six.
+template <typename KV, int D, bool HC, int W>
 constexpr int stages() {
+  if (W == 2) return 2;
   if (Geom<KV, D>::kStageBytes >= 32768) return 2;
   return split_ctas_per_sm<KV, HC>() == 4 ? 3 : 4;
 }
 
-template <typename KV, typename Q, int D, int T, bool HC>
+template <typename KV, typename Q, int D, int T, bool HC, int W = kWarps>
 pkv_status launch_form(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                        cudaStream_t st) {
-  constexpr int NS = stages<KV, D, HC>();
-  constexpr int smem = smem_bytes<KV, D, NS>();
-  auto kernel = decode_tc_kernel<KV, Q, D, T, NS, HC>;
+  constexpr int NS = stages<KV, D, HC, W>();
+  constexpr int smem = smem_bytes<KV, D, NS, W>();
+  auto kernel = decode_tc_kernel<KV, Q, D, T, NS, HC, W>;
   // the shared-memory opt-in is per device
   static std::atomic<uint64_t> configured{0};
   int dev = 0;
@@ -60,15 +62,23 @@ pkv_status launch_form(const DecodeArgs& a, const CUtensorMap& kmap, const CUten
   }
   // the last prefix_splits split slots belong to the shared-prefix pass
   const dim3 grid(a.num_kv_heads, a.num_seqs, a.max_splits - (a.prefix_tokens > 0 ? a.prefix_splits : 0));
-  e = launch_dependent(kernel, grid, kThreads, smem, st, a, kmap, vmap);
+  e = launch_dependent(kernel, grid, 32 * W, smem, st, a, kmap, vmap);
   if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: launch", e);
   return check_launch("pkv_attention_decode (tensor core)");
 }
 
-// query groups of up to 8 heads take the head-columns form
+// Query groups of up to 8 heads take the head-columns form.  Behind a
+// shared-prefix pass the contexts left are short: 16-bit head_dim-128 caches
+// take the two-warp form there (six CTAs per SM, so more CTAs overlap the
+// fixed latency each spends reading its length, block ids and first tile and
+// merging), when the partition fits its 512-entry table.
 template <typename KV, typename Q, int D, int T>
 pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                      cudaStream_t st) {
+  if constexpr (!std::is_same<KV, E4M3>::value && D == 128) {
+    if (a.prefix_tokens > 0 && a.group <= 8 && a.partition / T <= kMaxTableEntries2)
+      return launch_form<KV, Q, D, T, true, 2>(a, kmap, vmap, st);
+  }
   return a.group <= 8 ? launch_form<KV, Q, D, T, true>(a, kmap, vmap, st)
                       : launch_form<KV, Q, D, T, false>(a, kmap, vmap, st);
 }
