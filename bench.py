@@ -205,7 +205,7 @@ def traffic_for(config: str, kernels: str):
         return None
     d = json.load(open(p))
     e = d.get(config)
-    family = "prefill" if e and e.get("kernel", "").startswith("prefill") else "decode"
+    family = e.get("family", "decode") if e else "decode"
     if not e or e.get("kernel_sha") != kernel_source_hash(family):
         return None
     if not kernels.startswith(e.get("kernel", "?").split("<")[0]):
@@ -804,6 +804,59 @@ def run_gpu(args, world, rank, local):
         print(json.dumps(line), flush=True)
 
 
+class CudaRuntime:
+    """The CUDA runtime's asynchronous copy and event calls through ctypes, for
+    the end-to-end loop: each is one C call, where torch's stream context,
+    copy and event wrappers cost several microseconds of host time apiece,
+    which a host-bound loop pays every step.  The runtime is the one this
+    process already mapped (torch's), else the toolkit's."""
+
+    H2D, D2H = 1, 2
+
+    def __init__(self):
+        import ctypes
+        paths = []
+        try:
+            with open("/proc/self/maps") as f:
+                for line in f:
+                    path = line.split()[-1] if "/" in line else ""
+                    if os.path.basename(path).startswith("libcudart") and path not in paths:
+                        paths.append(path)
+        except OSError:
+            pass
+        paths += ["/usr/local/cuda/lib64/libcudart.so", "libcudart.so"]
+        self.rt = None
+        for p in paths:
+            try:
+                self.rt = ctypes.CDLL(p)
+                break
+            except OSError:
+                continue
+        if self.rt is None:
+            raise OSError("no CUDA runtime library found")
+        vp, c = ctypes.c_void_p, ctypes
+        self.rt.cudaMemcpyAsync.argtypes = [vp, vp, c.c_size_t, c.c_int, vp]
+        self.rt.cudaEventCreateWithFlags.argtypes = [c.POINTER(vp), c.c_uint]
+        self.rt.cudaEventRecord.argtypes = [vp, vp]
+        self.rt.cudaStreamWaitEvent.argtypes = [vp, vp, c.c_uint]
+        self.rt.cudaEventSynchronize.argtypes = [vp]
+        self.rt.cudaEventDestroy.argtypes = [vp]
+        self.events = []
+
+    def event(self):
+        import ctypes
+        e = ctypes.c_void_p()
+        if self.rt.cudaEventCreateWithFlags(ctypes.byref(e), 2) != 0:  # timing disabled
+            raise RuntimeError("cudaEventCreateWithFlags failed")
+        self.events.append(e)
+        return e
+
+    def close(self):
+        for e in self.events:
+            self.rt.cudaEventDestroy(e)
+        self.events = []
+
+
 def end_to_end(scn, dev_name, n: int, world: int, kv_bytes: int):
     """The step through the C ABI with its inputs copied from pinned host
     memory and its output copied back, every step.  Two input/output buffer
@@ -814,11 +867,14 @@ def end_to_end(scn, dev_name, n: int, world: int, kv_bytes: int):
     serving loop that overlaps transfers with compute does.  (With one copy
     stream for both directions, step i's input copy would queue behind step
     i - 1's output copy, which waits for step i - 1's compute: no overlap.)
-    Inputs per step: q, the new K/V, block tables and context lengths packed
-    in one pinned buffer (one copy); output: the attention result.  GB/s over
-    the host's wall clock.  The graph figure (copy in, step, copy out
-    captured as one CUDA graph, one replay and one host sync per step) is
-    reported beside it."""
+    The step is the library's Prepared calls (arguments checked once, as a
+    serving loop re-issuing one step on the same buffers does), and the copies
+    and events go to the CUDA runtime directly; the loop is host-bound
+    otherwise.  Inputs per step: q, the new K/V, block tables and context
+    lengths packed in one pinned buffer (one copy); output: the attention
+    result.  GB/s over the host's wall clock.  The graph figure (copy in,
+    step, copy out captured as one CUDA graph, one replay and one host sync
+    per step) is reported beside it."""
     import copy as _copy
     import torch
     names = ("q", "k_new", "v_new", "tables", "ctx")
@@ -832,36 +888,67 @@ def end_to_end(scn, dev_name, n: int, world: int, kv_bytes: int):
         host_in = dev_in.cpu().pin_memory()
         host_out = torch.empty_like(scn.out, device="cpu").pin_memory()
         slots.append({"scn": s, "dev_in": dev_in, "host_in": host_in, "host_out": host_out,
-                      "in_ev": torch.cuda.Event(), "done_ev": torch.cuda.Event(),
-                      "out_ev": torch.cuda.Event()})
+                      "step": s.prepare_step()})
     h2d = slots[0]["host_in"].numel()
     d2h = slots[0]["host_out"].numel() * slots[0]["host_out"].element_size()
     compute = torch.cuda.current_stream()
     in_s = torch.cuda.Stream(device=dev_name)
     out_s = torch.cuda.Stream(device=dev_name)
+    try:
+        rt = CudaRuntime()
+        for sl in slots:
+            sl["in_ev"], sl["done_ev"], sl["out_ev"] = rt.event(), rt.event(), rt.event()
+            sl["p"] = (sl["dev_in"].data_ptr(), sl["host_in"].data_ptr(), sl["scn"].out.data_ptr(),
+                       sl["host_out"].data_ptr())
+        hc, hi, ho = compute.cuda_stream, in_s.cuda_stream, out_s.cuda_stream
 
-    def issue(i):
-        sl = slots[i % 2]
-        # step i - 2 used this pair: its compute is done (done_ev) and its
-        # output has reached the host (the host waited for out_ev)
-        in_s.wait_event(sl["done_ev"])
-        with torch.cuda.stream(in_s):
-            sl["dev_in"].copy_(sl["host_in"], non_blocking=True)
-        sl["in_ev"].record(in_s)
-        compute.wait_event(sl["in_ev"])
-        sl["scn"].step()
-        sl["done_ev"].record(compute)
-        out_s.wait_event(sl["done_ev"])
-        with torch.cuda.stream(out_s):
-            sl["host_out"].copy_(sl["scn"].out, non_blocking=True)
-        sl["out_ev"].record(out_s)
+        def issue(i):
+            # step i - 2 used this pair: the host has already waited for its output
+            sl = slots[i % 2]
+            di, hin, do, hout = sl["p"]
+            r = rt.rt
+            r.cudaMemcpyAsync(di, hin, h2d, rt.H2D, hi)
+            r.cudaEventRecord(sl["in_ev"], hi)
+            r.cudaStreamWaitEvent(hc, sl["in_ev"], 0)
+            sl["step"](hc)
+            r.cudaEventRecord(sl["done_ev"], hc)
+            r.cudaStreamWaitEvent(ho, sl["done_ev"], 0)
+            r.cudaMemcpyAsync(hout, do, d2h, rt.D2H, ho)
+            r.cudaEventRecord(sl["out_ev"], ho)
+
+        def wait_out(i):
+            if rt.rt.cudaEventSynchronize(slots[i % 2]["out_ev"]) != 0:
+                raise RuntimeError("cudaEventSynchronize failed")
+        how = "CUDA runtime calls through ctypes"
+    except (OSError, RuntimeError, AttributeError):
+        rt = None
+        for sl in slots:
+            sl["in_ev"], sl["done_ev"], sl["out_ev"] = (torch.cuda.Event(), torch.cuda.Event(),
+                                                        torch.cuda.Event())
+
+        def issue(i):
+            sl = slots[i % 2]
+            with torch.cuda.stream(in_s):
+                sl["dev_in"].copy_(sl["host_in"], non_blocking=True)
+            sl["in_ev"].record(in_s)
+            compute.wait_event(sl["in_ev"])
+            sl["step"](compute)
+            sl["done_ev"].record(compute)
+            out_s.wait_event(sl["done_ev"])
+            with torch.cuda.stream(out_s):
+                sl["host_out"].copy_(sl["scn"].out, non_blocking=True)
+            sl["out_ev"].record(out_s)
+
+        def wait_out(i):
+            slots[i % 2]["out_ev"].synchronize()
+        how = "torch copies and events"
 
     def run(n):
         for i in range(n):
             issue(i)
             if i >= 1:
-                slots[(i - 1) % 2]["out_ev"].synchronize()   # step i - 1's output is on the host
-        slots[(n - 1) % 2]["out_ev"].synchronize()
+                wait_out(i - 1)   # step i - 1's output is on the host
+        wait_out(n - 1)
 
     run(4)
     torch.cuda.synchronize()
@@ -869,11 +956,15 @@ def end_to_end(scn, dev_name, n: int, world: int, kv_bytes: int):
     t0 = time.perf_counter()
     run(n)
     e2e_s = max_over_ranks((time.perf_counter() - t0) / n, world)
+    torch.cuda.synchronize()
+    if rt is not None:
+        rt.close()
     e2e = {"value": round(world * kv_bytes / e2e_s / 1e9, 2), "unit": "GB/s", "h2d_bytes_per_step": h2d,
            "d2h_bytes_per_step": d2h, "ms_per_step": round(e2e_s * 1e3, 4), "steps": n,
            "what": "host-to-device copy of the step's inputs and device-to-host copy of its output "
                    "every step, two buffer pairs alternating so that copies overlap the previous "
-                   "step's compute; host wall clock"}
+                   "step's compute; the step as the library's prepared calls; copies and events "
+                   "by " + how + "; host wall clock"}
     g = None
     if world == 1:
         s0 = slots[0]

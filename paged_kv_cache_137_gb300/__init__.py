@@ -501,12 +501,11 @@ def pkv_write(k_cache, v_cache, k, v, slot_mapping, desc: pkv_kv_desc, k_inv_sca
                            _stream(stream)))
 
 
-def pkv_copy_blocks(k_caches, v_caches, src_dst, desc: pkv_kv_desc, stream=None):
-    """Copy blocks src -> dst in every layer; src_dst is a host int32 [n, 2]."""
+def _copy_blocks_args(k_caches, v_caches, src_dst, desc):
     pairs = np.ascontiguousarray(np.asarray(src_dst, dtype=np.int32).reshape(-1))
     n = len(pairs) // 2
     if n == 0:
-        return
+        return None
     if len(k_caches) != len(v_caches):
         raise ValueError("k_caches and v_caches differ in length")
     for t in list(k_caches) + list(v_caches):
@@ -514,8 +513,22 @@ def pkv_copy_blocks(k_caches, v_caches, src_dst, desc: pkv_kv_desc, stream=None)
             raise ValueError("cache tensors do not match desc")
     kp = (_P * len(k_caches))(*[_dev(t, "k_cache") for t in k_caches])
     vp = (_P * len(v_caches))(*[_dev(t, "v_cache") for t in v_caches])
-    _check(lib().pkv_copy_blocks(kp, vp, len(k_caches), _i32p(pairs), n, ctypes.byref(desc),
-                                 _stream(stream)))
+    return (kp, vp, len(k_caches), _i32p(pairs), n, ctypes.byref(desc)), (pairs, kp, vp, desc)
+
+
+def pkv_copy_blocks(k_caches, v_caches, src_dst, desc: pkv_kv_desc, stream=None):
+    """Copy blocks src -> dst in every layer; src_dst is a host int32 [n, 2]."""
+    a = _copy_blocks_args(k_caches, v_caches, src_dst, desc)
+    if a is not None:
+        _check(lib().pkv_copy_blocks(*a[0], _stream(stream)))
+
+
+def prepare_copy_blocks(k_caches, v_caches, src_dst, desc: pkv_kv_desc):
+    """pkv_copy_blocks on these caches and pairs as a Prepared call (None when
+    there are no pairs: nothing to launch)."""
+    a = _copy_blocks_args(k_caches, v_caches, src_dst, desc)
+    return None if a is None else Prepared(lib().pkv_copy_blocks, a[0], (a[1], list(k_caches),
+                                                                           list(v_caches)))
 
 
 def pkv_attention_workspace_bytes(num_seqs, num_q_heads, max_blocks, desc: pkv_kv_desc,
@@ -570,11 +583,11 @@ def pkv_attention_decode(out, q, k_cache, v_cache, block_tables, context_lens, d
     return out
 
 
-def pkv_decode_step(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
-                    desc: pkv_kv_desc, softmax_scale, k_scale=1.0, v_scale=1.0, k_inv_scale=1.0,
-                    v_inv_scale=1.0, partition_tokens=0, workspace=None, stream=None):
-    """The step's K/V written at position ctx - 1 of each sequence, then decode
-    attention (one launch where the tensor-core split kernel applies)."""
+def _decode_step_args(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                      desc, prefix_blocks, softmax_scale, k_scale, v_scale, k_inv_scale,
+                      v_inv_scale, partition_tokens, workspace):
+    """The checked, marshalled arguments of pkv_decode_step (prefix_blocks
+    None) or pkv_decode_step_shared_prefix, without the stream."""
     b, hq, d = q.shape
     if out.shape != q.shape or out.dtype != q.dtype:
         raise ValueError("out must match q")
@@ -582,17 +595,55 @@ def pkv_decode_step(out, q, k_cache, v_cache, k_new, v_new, block_tables, contex
         raise ValueError("k_new, v_new must be [B, N_kv, D] in q's dtype")
     if block_tables.dim() != 2 or block_tables.shape[0] != b or context_lens.shape != (b,):
         raise ValueError("block_tables int32[B, max_blocks], context_lens int32[B] expected")
-    ws_ptr, ws_bytes = None, 0
-    if workspace is not None:
-        ws_ptr, ws_bytes = _dev(workspace, "workspace"), workspace.numel() * workspace.element_size()
-    _check(lib().pkv_decode_step(
-        _dev(out, "out"), _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache", desc.torch_dtype),
-        _dev(v_cache, "v_cache", desc.torch_dtype), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
-        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-        _dev(context_lens, "context_lens", torch.int32), b, hq, ctypes.byref(desc),
-        float(softmax_scale), float(k_scale), float(v_scale), float(k_inv_scale), float(v_inv_scale),
-        int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)))
+    ws_ptr, ws_bytes = _ws(workspace)
+    head = (_dev(out, "out"), _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache", desc.torch_dtype),
+            _dev(v_cache, "v_cache", desc.torch_dtype), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
+            _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
+            _dev(context_lens, "context_lens", torch.int32), b, hq, ctypes.byref(desc))
+    tail = (float(softmax_scale), float(k_scale), float(v_scale), float(k_inv_scale),
+            float(v_inv_scale), int(partition_tokens), ws_ptr, ws_bytes)
+    if prefix_blocks is None:
+        return lib().pkv_decode_step, head + tail
+    return lib().pkv_decode_step_shared_prefix, head + (int(prefix_blocks),) + tail
+
+
+class Prepared:
+    """A library call whose arguments were checked and marshalled once, for a
+    loop that repeats it on the same buffers (a serving step re-issued with
+    new contents in the same device memory).  ``call(stream)`` launches it on
+    ``stream`` (a torch stream, a raw cudaStream_t as int, or None for the
+    current stream).  The buffers must stay alive and keep their shapes."""
+
+    def __init__(self, fn, args, keep):
+        self._fn, self._args, self._keep = fn, args, keep
+
+    def __call__(self, stream=None):
+        _check(self._fn(*self._args, stream if isinstance(stream, int) else _stream(stream)))
+
+
+def pkv_decode_step(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                    desc: pkv_kv_desc, softmax_scale, k_scale=1.0, v_scale=1.0, k_inv_scale=1.0,
+                    v_inv_scale=1.0, partition_tokens=0, workspace=None, stream=None):
+    """The step's K/V written at position ctx - 1 of each sequence, then decode
+    attention (one launch where the tensor-core split kernel applies)."""
+    fn, args = _decode_step_args(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                                 desc, None, softmax_scale, k_scale, v_scale, k_inv_scale,
+                                 v_inv_scale, partition_tokens, workspace)
+    _check(fn(*args, _stream(stream)))
     return out
+
+
+def prepare_decode_step(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                        desc: pkv_kv_desc, softmax_scale, k_scale=1.0, v_scale=1.0,
+                        k_inv_scale=1.0, v_inv_scale=1.0, partition_tokens=0, workspace=None,
+                        prefix_blocks=None) -> Prepared:
+    """pkv_decode_step (or, with prefix_blocks, pkv_decode_step_shared_prefix)
+    as a Prepared call on these buffers."""
+    fn, args = _decode_step_args(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                                 desc, prefix_blocks, softmax_scale, k_scale, v_scale, k_inv_scale,
+                                 v_inv_scale, partition_tokens, workspace)
+    return Prepared(fn, args, (out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                               desc, workspace))
 
 
 def pkv_attention_prefill(out, q, k_cache, v_cache, block_tables, context_lens, query_start,
@@ -687,21 +738,10 @@ def pkv_decode_step_shared_prefix(out, q, k_cache, v_cache, k_new, v_new, block_
                                   k_scale=1.0, v_scale=1.0, k_inv_scale=1.0, v_inv_scale=1.0,
                                   partition_tokens=0, workspace=None, stream=None):
     """pkv_decode_step over a shared prefix (pkv_decode_step_shared_prefix)."""
-    b, hq, d = q.shape
-    if out.shape != q.shape or out.dtype != q.dtype:
-        raise ValueError("out must match q")
-    if k_new.shape != v_new.shape or k_new.shape[0] != b or k_new.dtype != q.dtype:
-        raise ValueError("k_new, v_new must be [B, N_kv, D] in q's dtype")
-    if block_tables.dim() != 2 or block_tables.shape[0] != b or context_lens.shape != (b,):
-        raise ValueError("block_tables int32[B, max_blocks], context_lens int32[B] expected")
-    ws_ptr, ws_bytes = _ws(workspace)
-    _check(lib().pkv_decode_step_shared_prefix(
-        _dev(out, "out"), _dev(q, "q"), _dtype_code(q), _dev(k_cache, "k_cache", desc.torch_dtype),
-        _dev(v_cache, "v_cache", desc.torch_dtype), _dev(k_new, "k_new"), _dev(v_new, "v_new"),
-        _dev(block_tables, "block_tables", torch.int32), block_tables.shape[1],
-        _dev(context_lens, "context_lens", torch.int32), b, hq, ctypes.byref(desc),
-        int(prefix_blocks), float(softmax_scale), float(k_scale), float(v_scale), float(k_inv_scale),
-        float(v_inv_scale), int(partition_tokens), ws_ptr, ws_bytes, _stream(stream)))
+    fn, args = _decode_step_args(out, q, k_cache, v_cache, k_new, v_new, block_tables, context_lens,
+                                 desc, prefix_blocks, softmax_scale, k_scale, v_scale, k_inv_scale,
+                                 v_inv_scale, partition_tokens, workspace)
+    _check(fn(*args, _stream(stream)))
     return out
 
 

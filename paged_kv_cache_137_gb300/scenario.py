@@ -30,7 +30,8 @@ import workloads as W
 
 from . import (Pool, empty_cache, kv_desc, pkv_attention_decode, pkv_attention_decode_shared_prefix,
                pkv_copy_blocks, pkv_decode_step, pkv_decode_step_shared_prefix, pkv_write,
-               shared_prefix_workspace_for, workspace_for)
+               prepare_copy_blocks, prepare_decode_step, shared_prefix_workspace_for,
+               workspace_for)
 
 CHURN_ID0 = 1 << 40
 POISON_BYTE = 0xFF
@@ -170,6 +171,24 @@ class DeviceScenario:
         fused with attention."""
         self.copy_blocks(stream)
         return self.decode_step(stream)
+
+    def prepare_step(self):
+        """step() as Prepared calls on this scenario's buffers: a function of
+        the stream (a raw cudaStream_t int or a torch stream) that launches the
+        block copies, then the fused slot write and attention."""
+        copies = prepare_copy_blocks([self.k_cache], [self.v_cache], self.plan.cow_pairs, self.desc)
+        decode = prepare_decode_step(
+            self.out, self.q, self.k_cache, self.v_cache, self.k_new, self.v_new, self.tables,
+            self.ctx, self.desc, self.softmax_scale, self.scales.get("k_scale", 1.0),
+            self.scales.get("v_scale", 1.0), self.scales.get("k_inv_scale", 1.0),
+            self.scales.get("v_inv_scale", 1.0), self.partition, self.workspace,
+            prefix_blocks=self.prefix_blocks or None)
+
+        def run(stream):
+            if copies is not None:
+                copies(stream)
+            decode(stream)
+        return run
 
     def kv_bytes(self) -> int:
         """Logical K/V bytes one attention call serves: every sequence's

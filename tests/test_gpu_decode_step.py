@@ -80,3 +80,26 @@ def test_fused_step_matches_the_oracle(name):
     err = np.abs(out - ref)
     tol = 6e-2 if w.kv_dtype == "e4m3" else 2e-2
     assert not np.isnan(out).any() and err.max() <= tol
+
+
+@pytest.mark.parametrize("name", ["qwen_small", "prefix_small", "fp8_small"])
+@pytest.mark.parametrize("shared", [False, True])
+def test_prepared_step_equals_the_call(name, shared):
+    """DeviceScenario.prepare_step (the library's Prepared calls: arguments
+    checked once, launched on a raw stream handle) gives the same pool bytes
+    and outputs, bit for bit, as the step through the plain calls."""
+    w = CASES[name]
+    plan = PS.plan(w)
+    if shared and not plan.shared_prefix_blocks:
+        pytest.skip("no shared prefix in this batch")
+    dev = PS.materialize(plan, "cuda", scales_for(w), shared_prefix=shared)
+    ref = dev.step().clone()
+    k_ref, v_ref = dev.k_cache.clone(), dev.v_cache.clone()
+    run = dev.prepare_step()
+    dev.out.fill_(float("nan"))
+    run(torch.cuda.current_stream().cuda_stream)
+    torch.cuda.synchronize()
+    assert torch.equal(dev.out.view(torch.int16), ref.view(torch.int16))
+    # (bytes: unwritten slots hold a NaN poison pattern)
+    assert torch.equal(dev.k_cache.view(torch.uint8), k_ref.view(torch.uint8))
+    assert torch.equal(dev.v_cache.view(torch.uint8), v_ref.view(torch.uint8))
