@@ -34,11 +34,13 @@ constexpr int kMultiWavePartition = 4096;  // the smallest split when the pairs 
 // Resident tensor-core split CTAs per SM: four for E4M3 caches (the
 // head-columns kernel that every query group up to 8 takes), else three.
 // Resident CTAs per SM of the tensor-core split kernel: four for E4M3, three
-// otherwise, six in the two-warp form 16-bit head_dim-128 caches take behind
-// a shared-prefix pass.
+// otherwise; behind a shared-prefix pass 16-bit head_dim-128 caches take the
+// narrow forms, eleven one-warp CTAs per SM at block size 16, six two-warp
+// CTAs at 32.
 int resident_split_ctas(const pkv_kv_desc* d, bool behind_prefix = false) {
   if (d->kv_dtype == PKV_E4M3) return 4;
-  return behind_prefix && d->head_dim == 128 ? 6 : 3;
+  if (behind_prefix && d->head_dim == 128) return d->block_size == 16 ? 11 : 6;
+  return 3;
 }
 constexpr int kDefaultSms = 152;       // used when no device can be queried
 

@@ -48,11 +48,15 @@ constexpr int kWarps = 4;                 // warps of the split kernel's CTA (or
 constexpr int kThreads = kWarps * 32;
 constexpr int kTile = 64;                 // tokens per stage, 16 per warp
 constexpr int kMaxTableEntries = 1024;    // block ids of one split kept in shared memory
-// The two-warp form (16-bit head_dim-128 caches behind a shared-prefix pass):
-// 32-token stages of 16 KiB, six CTAs per SM, at most 512 block ids a split.
+// The narrow forms (16-bit head_dim-128 caches behind a shared-prefix pass,
+// where the contexts left are short): one warp per CTA with 16-token stages of
+// 8 KiB, eleven CTAs per SM (block size 16), or two warps with 32-token
+// stages of 16 KiB, six CTAs per SM (block size 32); at most 512 block ids a
+// split.
 constexpr int kMaxTableEntries2 = 512;
 template <int W>
-constexpr int max_table_entries() { return W == 2 ? kMaxTableEntries2 : kMaxTableEntries; }
+constexpr int max_table_entries() { return W <= 2 ? kMaxTableEntries2 : kMaxTableEntries; }
+
 constexpr uint64_t kWaitNs = 50000000ull;  // a stage wait gives up after 50 ms
 constexpr uint64_t kDrainNs = 10000000ull; // after a give-up, 10 ms per copy in flight
 
@@ -775,11 +779,14 @@ constexpr int split_ctas_per_sm() {
   return HC && std::is_same<KV, E4M3>::value ? 4 : 3;
 }
 
+template <typename KV, bool HC, int W>
+constexpr int resident_ctas() { return W == 1 ? 11 : W == 2 ? 6 : split_ctas_per_sm<KV, HC>(); }
+
 // HC: the head-columns form of the tile products (query group <= 8).  W:
-// warps per CTA, 16 tokens of each W * 16-token tile per warp (4; or 2, six
-// CTAs per SM, for short contexts past a shared prefix).
+// warps per CTA, 16 tokens of each W * 16-token tile per warp (4; or 1 or 2,
+// with more CTAs per SM, for the short contexts past a shared prefix).
 template <typename KV, typename Q, int D, int T, int NS, bool HC, int W = kWarps>
-__global__ void __launch_bounds__(32 * W, W == 2 ? 6 : split_ctas_per_sm<KV, HC>())
+__global__ void __launch_bounds__(32 * W, resident_ctas<KV, HC, W>())
     decode_tc_kernel(const DecodeArgs a, const __grid_constant__ CUtensorMap kmap,
                      const __grid_constant__ CUtensorMap vmap) {
   using G_ = Geom<KV, D, W>;
@@ -854,7 +861,7 @@ __global__ void __launch_bounds__(32 * W, W == 2 ? 6 : split_ctas_per_sm<KV, HC>
   // Behind a shared prefix the merging CTA reads the pass's partials: warps
   // 1.. ask L2 for their lines now (L2 is where the pass's writes land, so a
   // line fetched before the pass writes it is updated, never stale).
-  if (P > 0 && warp > 0 && a.ws_acc != nullptr) {
+  if (kWarps > 1 && P > 0 && warp > 0 && a.ws_acc != nullptr) {
     const int n = a.prefix_splits;
     const int acc_lines = (n * D * 4 + 127) / 128, per_row = acc_lines + 2;
     for (int i = tid - 32; i < G * per_row; i += kThreads - 32) {

@@ -31,11 +31,11 @@ cudaError_t launch_dependent(void (*kernel)(Params...), dim3 grid, int threads, 
 }
 
 // Stages per CTA: 64 KiB of ring at three CTAs per SM (2 x 32 KiB or
-// 4 x 16 KiB), 48 KiB (3 x 16 KiB) at four; the two-warp form: 2 x 16 KiB at
-// six.
+// 4 x 16 KiB), 48 KiB (3 x 16 KiB) at four; the narrow forms two stages of
+// their 8 or 16 KiB tiles.
 template <typename KV, int D, bool HC, int W>
 constexpr int stages() {
-  if (W == 2) return 2;
+  if (W <= 2) return 2;
   if (Geom<KV, D>::kStageBytes >= 32768) return 2;
   return split_ctas_per_sm<KV, HC>() == 4 ? 3 : 4;
 }
@@ -69,15 +69,16 @@ pkv_status launch_form(const DecodeArgs& a, const CUtensorMap& kmap, const CUten
 
 // Query groups of up to 8 heads take the head-columns form.  Behind a
 // shared-prefix pass the contexts left are short: 16-bit head_dim-128 caches
-// take the two-warp form there (six CTAs per SM, so more CTAs overlap the
-// fixed latency each spends reading its length, block ids and first tile and
-// merging), when the partition fits its 512-entry table.
+// take a narrow form there (one warp per CTA at block size 16, two at 32:
+// eleven or six CTAs per SM, so more CTAs overlap the fixed latency each
+// spends reading its length, block ids and first tile and merging), when the
+// partition fits its 512-entry table.
 template <typename KV, typename Q, int D, int T>
 pkv_status launch_dt(const DecodeArgs& a, const CUtensorMap& kmap, const CUtensorMap& vmap,
                      cudaStream_t st) {
   if constexpr (!std::is_same<KV, E4M3>::value && D == 128) {
     if (a.prefix_tokens > 0 && a.group <= 8 && a.partition / T <= kMaxTableEntries2)
-      return launch_form<KV, Q, D, T, true, 2>(a, kmap, vmap, st);
+      return launch_form<KV, Q, D, T, true, (T == 16 ? 1 : 2)>(a, kmap, vmap, st);
   }
   return a.group <= 8 ? launch_form<KV, Q, D, T, true>(a, kmap, vmap, st)
                       : launch_form<KV, Q, D, T, false>(a, kmap, vmap, st);
