@@ -182,3 +182,33 @@ def test_shared_prefix_full_size():
     ref = OS.build(w)
     check_close(out.double().cpu().numpy(), oracle_out(ref), "bf16")
     assert pkv.pkv_device_status() == 0
+
+
+@pytest.mark.parametrize("name", ["pfx_rows192", "pfx_t32"])
+def test_tail_wait_give_up_gives_nan_and_status_then_recovers(name):
+    """The tail kernel's failure path behind a shared prefix (the one-warp
+    form at block size 16, the two-warp form at 32), run on purpose: with a
+    stage-wait limit of 0 every tail CTA gives up at its first stage wait,
+    drains its copies in flight (its own bounded limit), writes a NaN partial
+    and sets PKV_DEVICE_WAIT_TIMEOUT; the merges, by a tail CTA or by a pass
+    CTA, carry the NaN to every output whose context extends past the prefix,
+    and the counters end at zero.  The next call, with the normal limit, is
+    correct."""
+    w = CASES[name]
+    dev, sc = shared(w)
+    dev.copy_blocks()
+    try:
+        pkv.pkv_set_stage_wait_limit(0)
+        out = dev.decode_step().clone()
+        torch.cuda.synchronize()
+    finally:
+        pkv.pkv_set_stage_wait_limit(50_000_000)
+    assert pkv.pkv_device_status(clear=True) & pkv.PKV_DEVICE_WAIT_TIMEOUT
+    assert torch.isnan(out).all()   # every context extends past the prefix
+    n = len(dev.plan.seq_ids) * w.num_kv_heads
+    assert torch.count_nonzero(dev.workspace[: 4 * n + 4]).item() == 0   # counters and exit count
+    out = dev.decode_step()
+    torch.cuda.synchronize()
+    assert pkv.pkv_device_status() == 0
+    ref = OS.build(w, scales=sc)
+    check_close(out.double().cpu().numpy(), oracle_out(ref), w.kv_dtype)
