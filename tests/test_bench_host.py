@@ -76,3 +76,21 @@ def test_kernel_source_hash_covers_its_files(family):
     assert len(h) == 16 and int(h, 16) >= 0
     for n in bench.KERNEL_SOURCES[family]:
         assert os.path.exists(os.path.join(bench.ROOT, "paged_kv_cache_137_gb300", "csrc", n))
+
+
+def test_every_traffic_entry_names_its_kernel_family():
+    """Each committed DRAM figure says which source family it was taken on; the
+    shared-prefix call (a prefill-kernel pass and the decode kernel) is the
+    decode family, so a change to either kernel's sources retires the figure."""
+    d = json.load(open(os.path.join(bench.ROOT, "profiles", "attention_traffic.json")))
+    for name, e in d.items():
+        assert e["family"] in bench.KERNEL_SOURCES, name
+        assert e["dram_bytes_per_launch"] > 0
+    assert d["prefix_fork_bf16"]["family"] == "decode"
+    for n in ("attention_prefill_umma.cuh", "attention_shared_prefix.cu"):
+        assert n in bench.KERNEL_SOURCES["decode"]
+    import workloads as W
+    e = d["prefix_fork_bf16"]
+    label = bench.attention_kernels("auto", W.get("prefix_fork_bf16"), 1, shared_prefix=True)
+    fresh = e["kernel_sha"] == bench.kernel_source_hash("decode")
+    assert bench.traffic_for("prefix_fork_bf16", label) == (e["dram_bytes_per_launch"] if fresh else None)
