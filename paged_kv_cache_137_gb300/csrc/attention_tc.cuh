@@ -7,30 +7,41 @@
 // "Concept").
 //
 // How, on GB300:
-//  * One CTA (4 warps) per (split, KV head, sequence).  The split's block ids
-//    are read once into shared memory.  Thread 0 feeds a ring of NS stages:
-//    each stage is a 64-token tile of K and of V, fetched as one TMA box per
-//    block: its T rows of the head, at row (block * N_kv + head) * T of the
-//    pool viewed as [rows][row_bytes] (a 3-D (128 bytes, slab, row) view for
-//    256-byte rows, so one box carries both slabs), with the hardware 128-byte
-//    swizzle so that ldmatrix reads are conflict-free.
-//    Completion is tracked by one mbarrier per stage (expect-tx bytes).
-//  * Each warp owns 16 tokens of a tile.  q . K^T is an m16n8k16 MMA with the
-//    (up to 16) query heads of the group as the M rows, so each K element is
-//    read from shared memory once for all heads; the online softmax runs on
-//    the accumulator fragments (quad shuffles for the row maxima); p . V is a
-//    second m16n8k16 MMA whose A operand is the probability fragment reused
-//    from registers.  16-bit caches use bf16/f16 MMAs; an E4M3 cache is
-//    converted to f16 in registers (exact) and q is converted to f16.
+//  * One CTA per (KV head, sequence, split): four warps and 64-token tiles by
+//    default; behind a shared-prefix pass, where the contexts left are short,
+//    one warp (block size 16) or two (block size 32) with 16- or 32-token
+//    tiles, so that more CTAs per SM overlap each one's fixed latencies.  The
+//    split's block ids are read into shared memory; split 0 fetches its first
+//    tiles' ids and its query rows together with the length.  Warp 0 refills
+//    a ring of NS stages, one lane per TMA box: each stage is a tile of K and
+//    of V, one box per (block, K|V) carrying the block's T rows of the head,
+//    at row (block * N_kv + head) * T of the pool viewed as [rows][row_bytes]
+//    (a 3-D (128 bytes, slab, row) view for 256-byte rows, so one box carries
+//    both slabs), with the hardware 128-byte swizzle so that ldmatrix reads
+//    are conflict-free.  Completion is tracked by one mbarrier per stage
+//    (expect-tx bytes).
+//  * Each warp owns 16 tokens of a tile.  Groups of up to 8 query heads take
+//    the head-columns form: S^T = K q^T and O^T += V^T P^T by m16n8k16 MMAs
+//    with the tokens (then head_dim) as the 16 MMA rows and the heads as the
+//    8 columns, P^T reaching the B operand through movmatrix; larger groups
+//    (up to 16) the head-rows form (q K^T with the heads as M).  The online
+//    softmax runs on the accumulator fragments in the log2 domain.  16-bit
+//    caches use bf16/f16 MMAs; an E4M3 cache is widened to f16 in registers
+//    (exact) and q is converted to f16.
 //  * Tokens past the context end are masked to -inf, and their V rows are
-//    zeroed in shared memory before the p . V MMA (0 * NaN would poison it).
-//  * The four warps' (max, sum, output) are merged through shared memory.
-//    A pair's tiles are shared out evenly over its splits.  With several
-//    splits, each CTA writes its partial and the last CTA of the (sequence,
-//    KV head) to finish (an atomic counter, no waiting) gathers all splits'
-//    partials into shared memory, merges them and resets the counter.
-//  * Every mbarrier wait is bounded; a timeout turns the heads' output into NaN
-//    after waiting (also bounded) for the copies still in flight.
+//    zeroed in shared memory before the P V MMA (0 * NaN would poison it).
+//  * The warps' (max, sum, output) are merged through shared memory.  A
+//    pair's tiles are shared out evenly over its splits.  With several
+//    splits, or behind a shared-prefix pass, each CTA writes its partial and
+//    the last of the (sequence, KV head)'s partials to arrive (an atomic
+//    counter, no waiting; the pass's CTAs count in on the same counter)
+//    gathers them all into shared memory, merges them and resets the counter.
+//  * The step's new token can be written by the CTA that holds position
+//    ctx - 1, before any copy is issued (the fused slot write).
+//  * Every mbarrier wait is bounded; a stage wait that gives up (its limit is
+//    pkv_set_stage_wait_limit's) turns the heads' output into NaN and sets a
+//    bit in the device error word, after waiting (with its own bound) for the
+//    copies still in flight.
 #pragma once
 
 #include <cuda.h>
