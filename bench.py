@@ -204,7 +204,7 @@ def attention_kernels(kernel: str, w, splits: int, shared_prefix: bool = False) 
         k = "decode_simt_kernel"
         return k + (" + merge_kernel" if splits > 1 else "")
     if shared_prefix:
-        return "prefill_umma_kernel<shared prefix> + decode_tc_kernel (merges fused)"
+        return "prefill_umma_kernel<shared prefix> + decode_tc_kernel + prefix_merge_kernel"
     return "decode_tc_kernel (split-K merge fused)"
 
 
@@ -656,7 +656,8 @@ def run_gpu(args, world, rank, local):
     # is the slot write outside the tensor-core split kernel (which fuses it)
     separate_merge = args.kernel == "simt" or w.kv_dtype == "f32"
     fused_write = not separate_merge
-    attn_launches = 1 + (1 if separate_merge and splits > 1 else 0) + (1 if scn.prefix_blocks else 0)
+    # a shared prefix adds its pass before the decode kernel and the merge kernel after it
+    attn_launches = 1 + (1 if separate_merge and splits > 1 else 0) + (2 if scn.prefix_blocks else 0)
     launches_per_step = (0 if fused_write else 1) + attn_launches + \
         (-(-n_pairs // 1024) if n_pairs else 0)
 

@@ -354,9 +354,9 @@ PKV_API pkv_status pkv_decode_step(void* out, const void* q, int32_t q_dtype, vo
  *     num_seqs * group) to positions [0, P), P = prefix_blocks * block_size,
  *     read through row 0 of block_tables, and leaves per-row partial results
  *     (max, sum, unnormalised output) in the workspace;
- *   - the decode kernel attends positions [P, ctx) of each sequence; the
- *     last of a (sequence, KV head)'s partials to arrive, a decode CTA or a
- *     pass CTA, merges them all into out.
+ *   - the decode kernel attends positions [P, ctx) of each sequence and
+ *     leaves its partials in the workspace too;
+ *   - a merge kernel combines every row's partials into out.
  * Because the reduction is split differently, results can differ from
  * pkv_attention_decode in the low-order bits ([C "Effect"]: reusing shared
  * blocks changes how the attention reduction is tiled).
@@ -371,10 +371,9 @@ PKV_API pkv_status pkv_decode_step(void* out, const void* q, int32_t q_dtype, vo
  *               aligned, zero-filled before first use (left zeroed).
  * The prefix pass is launched first (on about a quarter of the SMs), then the
  * decode kernel as its programmatic dependent, which starts on the SMs the
- * pass leaves free; the two kernels' partials meet through arrival counters
- * in the workspace, and whichever arrives last for a (sequence, KV head)
- * merges them, so neither waits for the other.  The decode grid completes
- * only after the pass (its last CTA waits for the pass's grid). */
+ * pass leaves free (neither waits for the other; the decode grid completes
+ * only after the pass: its last CTA waits for the pass's grid), then the
+ * merge kernel. */
 PKV_API size_t pkv_shared_prefix_workspace_bytes(int32_t num_seqs, int32_t num_q_heads,
                                                  int32_t max_blocks, const pkv_kv_desc* desc,
                                                  int32_t prefix_blocks, int32_t partition_tokens);

@@ -124,8 +124,12 @@ bool tc_supported(const pkv_kv_desc* d, int q_dtype, int group, int partition) {
   return d->head_dim == 128 || d->head_dim == 64;
 }
 
+// The split-K merge of the CUDA-core kernel, one CTA per (sequence, query
+// head); a programmatic dependent of the decode kernel (it reads the
+// partials after that grid has completed).
 template <typename Q, int D>
 __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int qh = blockIdx.x, seq = blockIdx.y;
   const int ctx = a.ctx_lens[seq];
   if (ctx < 0 || ctx > a.max_blocks * a.block_size) return;  // written by the decode kernel
@@ -153,9 +157,18 @@ __global__ void __launch_bounds__(128) merge_kernel(const DecodeArgs a) {
 
 template <typename Q>
 pkv_status launch_merge(const DecodeArgs& a, int head_dim, cudaStream_t st) {
-  const dim3 grid(a.num_q_heads, a.num_seqs);
-  if (head_dim == 128) merge_kernel<Q, 128><<<grid, 128, 0, st>>>(a);
-  else merge_kernel<Q, 64><<<grid, 64, 0, st>>>(a);
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.num_q_heads, a.num_seqs);
+  cfg.blockDim = dim3(head_dim == 128 ? 128 : 64);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = head_dim == 128 ? cudaLaunchKernelEx(&cfg, merge_kernel<Q, 128>, a)
+                                        : cudaLaunchKernelEx(&cfg, merge_kernel<Q, 64>, a);
+  if (e != cudaSuccess) return cuda_fail("pkv_attention_decode: merge launch", e);
   return check_launch("pkv_attention_decode (merge)");
 }
 
@@ -465,8 +478,8 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
   }
   if (prefix_pass) {
     // the prefix pass first: its CTAs let the decode kernel start once they
-    // have all begun, on the SMs the pass leaves free; the pairs' partials
-    // meet through the arrival counters (whoever arrives last merges)
+    // have all begun, on the SMs the pass leaves free; both write partials,
+    // which the merge kernel after the decode kernel combines
     PrefillArgs pa{};
     pa.q = q;
     pa.tables = block_tables;
@@ -490,10 +503,6 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
     pa.ws_m = a.ws_m;
     pa.ws_l = a.ws_l;
     pa.ws_acc = a.ws_acc;
-    pa.out = out;
-    pa.ctx_lens = context_lens;
-    pa.counters = a.counters;
-    pa.partition = partition;
     pa.sp_seqs = pp.seqs_per_cta;
     CUtensorMap pkmap, pvmap;
     st = pool_map(&pkmap, k_cache, desc, false);
@@ -515,12 +524,15 @@ pkv_status decode_impl(void* out, const void* q, int32_t q_dtype, const void* k_
     if (st == PKV_OK) st = pool_map(&vmap, v_cache, desc);
     if (st != PKV_OK) return st;
     switch (kv) {
-      case PKV_F16: return launch_decode_tc<F16, F16>(a, D, kmap, vmap, s);
-      case PKV_BF16: return launch_decode_tc<BF16, BF16>(a, D, kmap, vmap, s);
+      case PKV_F16: st = launch_decode_tc<F16, F16>(a, D, kmap, vmap, s); break;
+      case PKV_BF16: st = launch_decode_tc<BF16, BF16>(a, D, kmap, vmap, s); break;
       default:
-        return q_dtype == PKV_F16 ? launch_decode_tc<E4M3, F16>(a, D, kmap, vmap, s)
-                                  : launch_decode_tc<E4M3, BF16>(a, D, kmap, vmap, s);
+        st = q_dtype == PKV_F16 ? launch_decode_tc<E4M3, F16>(a, D, kmap, vmap, s)
+                                : launch_decode_tc<E4M3, BF16>(a, D, kmap, vmap, s);
     }
+    // behind a shared-prefix pass every partial is merged by the merge kernel
+    if (st != PKV_OK || !prefix_pass) return st;
+    return q_dtype == PKV_F16 ? launch_prefix_merge<F16>(a, s) : launch_prefix_merge<BF16>(a, s);
   }
   switch (kv) {
     case PKV_F32: st = launch_decode_simt<F32, F32>(a, D, gm, s); break;

@@ -41,8 +41,8 @@ struct DecodeArgs {
   // shared prefix (0: none): positions [0, prefix_tokens) of every sequence
   // are attended by the shared-prefix pass, the kernel launched just before
   // this one, whose prefix_splits partials sit in the last prefix_splits of
-  // the max_splits slots; this kernel covers [prefix_tokens, ctx), and the
-  // last of a pair's partials to arrive (its splits and the pass's) merges
+  // the max_splits slots; this kernel covers [prefix_tokens, ctx) and writes
+  // partials, and the merge kernel after it combines them all
   int32_t prefix_tokens, prefix_splits;
   int* status;               // device error word (PKV_DEVICE_* bits, atomicOr)
   uint64_t wait_ns;          // give-up limit of a stage wait; 0 = give up at once
@@ -71,15 +71,11 @@ struct PrefillArgs {
   // the keys are positions [k * sp_split, min(sp_tokens, (k + 1) * sp_split))
   // of table row 0; row (s, j)'s partial (max, sum, unnormalised output)
   // goes to split slot sp_slot0 + k of the decode workspace (ws_*, max_splits
-  // slots).  Each CTA then counts itself in on counters[s][kvh] (with the
-  // decode kernel's splits of the positions past the prefix, partition tokens
-  // each, and the pass's key ranges), and the rows of the pairs whose last
-  // partial it is merge them all into out.
-  int32_t sp_rows, sp_tokens, sp_split, sp_slot0, max_splits, sp_seqs, partition;
+  // slots), which the merge kernel after the decode kernel combines.
+  int32_t sp_rows, sp_tokens, sp_split, sp_slot0, max_splits, sp_seqs;
   float* ws_m;
   float* ws_l;
   float* ws_acc;
-  int* counters;
 };
 
 // Device error word of the current device (looked up once per device);
@@ -96,6 +92,12 @@ template <typename KV, typename Q>
 pkv_status launch_shared_prefix_pass(const PrefillArgs& a, int block_size, int key_splits,
                                      const CUtensorMap& kmap, const CUtensorMap& vmap,
                                      cudaStream_t st);
+
+// The merge kernel after the decode kernel on the shared-prefix path
+// (head_dim 128): every (sequence, query head)'s partials into out.  Defined
+// in attention_shared_prefix.cu.
+template <typename Q>
+pkv_status launch_prefix_merge(const DecodeArgs& a, cudaStream_t st);
 
 // Bytes at the start of a decode workspace that hold the split-K arrival
 // counters (they must be zero when a call starts; every call leaves them

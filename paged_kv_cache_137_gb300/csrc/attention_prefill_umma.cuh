@@ -51,10 +51,10 @@
 // Management", "Complex Topologies and Memory Sharing").  Nothing is masked
 // but the end of the range, and each row leaves its partial result (running
 // maximum, sum, unnormalised output times the V scale) in a split slot of the
-// decode workspace, where the decode kernel merges it with the rest of the
-// sequence's context.  The CTAs let the decode kernel launch as soon as they
-// have all started (griddepcontrol.launch_dependents after their own wait);
-// that kernel waits for this grid to complete before it reads the partials.
+// decode workspace; the merge kernel after the decode kernel combines it with
+// the rest of the sequence's context.  The CTAs let the decode kernel launch
+// as soon as they have all started (griddepcontrol.launch_dependents after
+// their own wait), on the SMs this grid leaves free.
 #pragma once
 
 #include <math_constants.h>
@@ -340,15 +340,6 @@ constexpr int threads() {
   return std::is_same<KV, E4M3>::value ? kThreadsU + 64 : kThreadsU;  // + two converter warps
 }
 
-// Shared-prefix pass: the decode kernel's split count for the positions of a
-// sequence past the prefix (1 for an invalid length, whose merge gives NaN).
-template <int T>
-__device__ __forceinline__ int tail_splits(const PrefillArgs& a, int seq) {
-  const int c = a.ctx_lens[seq];
-  const bool bad = c < 0 || c > a.max_blocks * T || c <= a.sp_tokens;
-  return bad ? 1 : max(1, (c - a.sp_tokens + a.partition - 1) / a.partition);
-}
-
 template <typename KV, typename Q, int T, bool kCasc = false>
 __global__ void __launch_bounds__(threads<KV>(), 1)
     prefill_umma_kernel(const PrefillArgs a, const __grid_constant__ CUtensorMap kmap,
@@ -449,7 +440,6 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
   __shared__ int s_bad;      // PKV_DEVICE_* bits (atomicOr: several warps may set them)
   __shared__ int s_issued;   // key tiles the producer has issued
   __shared__ uint8_t s_pbad[kCasc ? 256 : 1];  // shared-prefix pass: sequence breaks the declaration
-  __shared__ uint8_t s_mlast[kCasc ? 256 : 1]; // shared-prefix pass: this CTA merges the sequence
 
   if (tid == 0) {
     s_bad = 0;
@@ -861,8 +851,6 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
 
   // ---------------------------------------------------------------- exit
   // every UMMA done and every copy landed before TMEM and shared memory go
-  // (shared-prefix pass: every row's partial written before any is counted in)
-  if constexpr (kCasc) __threadfence();
   __syncthreads();
   if (tid == 0) {
     mbar_wait(smem_u32(fin), 0, kDrainNs);
@@ -874,98 +862,9 @@ __global__ void __launch_bounds__(threads<KV>(), 1)
       if (a.status != nullptr) atomicOr(a.status, s_bad);
     }
   }
-  if constexpr (kCasc) {
-    // Count this CTA's partials in on each of its (sequence, KV head) pairs
-    // (an atomic counter, never a wait); where they are the last of the
-    // pair's partials to arrive (the decode kernel's splits and the pass's
-    // key ranges), the pair's rows merge below, and the counter is reset.
-    const int nseq = n / a.group;
-    for (int i = tid; i < nseq; i += kNT) {
-      const int sq = seq0 + i;
-      int* cnt = a.counters + static_cast<size_t>(sq) * a.num_kv_heads + blockIdx.z;
-      const int prev = atomicAdd(cnt, 1);
-      const bool last = prev == tail_splits<T>(a, sq) + static_cast<int>(gridDim.y) - 1;
-      s_mlast[i] = last;
-      if (last) atomicExch(cnt, 0);
-    }
-  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
-  if constexpr (kCasc) {
-    // The rows of the pairs this CTA completes: M = max m_i, L = sum l_i
-    // 2^(m_i - M), o = sum a_i 2^(m_i - M) / L over the decode kernel's splits
-    // then the key ranges, in slot order (the decode kernel's merge, value
-    // for value), this CTA's own partial read back from TMEM.
-    if (warp < 8) {
-      const int X = warp >> 2, r = tid & 127;
-      const int cr = r_begin[X] + r;
-      const bool row_in = (X == 0 || hasB) && cr < r_end[X];
-      const bool mine = row_in && s_mlast[cr / a.group];
-      if (__any_sync(0xffffffffu, mine)) {
-        __threadfence();
-        const int sq = seq0 + cr / a.group;
-        const size_t base = (static_cast<size_t>(sq) * HQ + j + cr % a.group) * a.max_splits;
-        const int nt = mine ? tail_splits<T>(a, sq) : 0;
-        const int np = nt + static_cast<int>(gridDim.y);
-        const int own = nt + static_cast<int>(blockIdx.y);
-        auto slot = [&](int i) { return i < nt ? i : a.sp_slot0 + (i - nt); };
-        float M = -CUDART_INF_F, L = 0.f;
-        for (int i = 0; mine && i < np; ++i) M = fmaxf(M, __ldcg(a.ws_m + base + slot(i)));
-        for (int i = 0; mine && i < np; ++i) {
-          const float li = __ldcg(a.ws_l + base + slot(i));
-          L = M != -CUDART_INF_F ? fmaf(li, exp2f(__ldcg(a.ws_m + base + slot(i)) - M), L) : L + li;
-        }
-        // the own partial as written (NaN l: the row failed, its a is NaN)
-        const float l_own = mine ? __ldcg(a.ws_l + base + slot(own)) : 0.f;
-        const bool bad_own = l_own != l_own;
-        const bool nz = L > 0.f || L != L;
-        const uint32_t lane_off = static_cast<uint32_t>((warp & 3) * 32) << 16;
-        const uint32_t tO = tmem + 256 * X + 128;
-        typename Q::raw* dst = static_cast<typename Q::raw*>(a.out) +
-                               (static_cast<size_t>(sq) * HQ + j + cr % a.group) * D;
-#pragma unroll 1
-        for (int c = 0; c < D; c += 32) {
-          float o[32];
-          tmem_ld32(tO + lane_off + c, o);   // warp-wide: every lane takes part
-          if (!mine) continue;
-          float A[32];
-#pragma unroll
-          for (int e = 0; e < 32; ++e) A[e] = 0.f;
-          if (M != -CUDART_INF_F) {
-            for (int i = 0; i < np; ++i) {
-              const float f = exp2f(__ldcg(a.ws_m + base + slot(i)) - M);
-              if (i == own) {
-#pragma unroll
-                for (int e = 0; e < 32; ++e)
-                  A[e] = fmaf(bad_own ? CUDART_NAN_F : o[e] * hs.v, f, A[e]);
-              } else {
-                const float4* src = reinterpret_cast<const float4*>(a.ws_acc + (base + slot(i)) * D + c);
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                  const float4 v = __ldcg(src + e);
-                  A[4 * e] = fmaf(v.x, f, A[4 * e]);
-                  A[4 * e + 1] = fmaf(v.y, f, A[4 * e + 1]);
-                  A[4 * e + 2] = fmaf(v.z, f, A[4 * e + 2]);
-                  A[4 * e + 3] = fmaf(v.w, f, A[4 * e + 3]);
-                }
-              }
-            }
-          }
-          uint32_t w[16];
-#pragma unroll
-          for (int e = 0; e < 16; ++e)
-            w[e] = pack2<kOutBf>(nz ? A[2 * e] / L : 0.f, nz ? A[2 * e + 1] / L : 0.f);
-          uint4* d4 = reinterpret_cast<uint4*>(dst + c);
-#pragma unroll
-          for (int e = 0; e < 4; ++e) d4[e] = make_uint4(w[4 * e], w[4 * e + 1], w[4 * e + 2], w[4 * e + 3]);
-        }
-      }
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-  }
   if (warp == kProd) {
     __syncwarp();
     tmem_dealloc(tmem, kTmemCols);

@@ -1,6 +1,7 @@
 // Launch of the shared-prefix pass: the tcgen05 attention pipeline of
 // attention_prefill_umma.cuh in its shared-prefix form (kCasc), one CTA per
-// (group of whole sequences filling up to 256 query rows, key range, KV head).
+// (group of whole sequences filling up to 256 query rows, key range, KV head);
+// and the merge kernel that follows the decode kernel on that path.
 #include <atomic>
 
 #include "attention_prefill_umma.cuh"
@@ -41,6 +42,48 @@ pkv_status launch_shared_prefix_pass(const PrefillArgs& a, int block_size, int k
   if (e != cudaSuccess) return cuda_fail("shared-prefix pass: launch", e);
   return check_launch("shared-prefix pass (tcgen05)");
 }
+
+// The merge after the decode kernel on the shared-prefix path: one CTA per
+// (sequence, KV head) combines its G query heads' partials, the decode
+// kernel's splits of the positions past the prefix (slots 0 .. nsplit - 1)
+// then the pass's key ranges (the last prefix_splits slots), gathered into
+// shared memory with one round trip (the decode kernel's merge_splits, so the
+// sums are the fused merge's, value for value).  A programmatic dependent of
+// the decode grid, which completes only after the pass.
+constexpr int kMergeStage = 4096;  // floats of gathered partials; more fall back to direct loads
+
+template <typename Q>
+__global__ void __launch_bounds__(tc::kThreads) prefix_merge_kernel(const DecodeArgs a) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  __shared__ __align__(16) float stage[kMergeStage];
+  const int kvh = blockIdx.x, seq = blockIdx.y;
+  const int P = a.prefix_tokens, n_extra = a.prefix_splits;
+  const int ctx = a.ctx_lens[seq];
+  const bool bad = ctx < 0 || ctx > a.max_blocks * a.block_size || ctx <= P;
+  const int nsplit = bad ? 1 : max(1, (ctx - P + a.partition - 1) / a.partition);
+  const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * a.group;
+  tc::merge_splits<Q, 128, tc::kThreads>(a, head0, nsplit, a.max_splits - n_extra, n_extra, stage,
+                                         kMergeStage);
+}
+
+template <typename Q>
+pkv_status launch_prefix_merge(const DecodeArgs& a, cudaStream_t st) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(a.num_kv_heads, a.num_seqs);
+  cfg.blockDim = dim3(tc::kThreads);
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const cudaError_t e = cudaLaunchKernelEx(&cfg, prefix_merge_kernel<Q>, a);
+  if (e != cudaSuccess) return cuda_fail("shared-prefix merge: launch", e);
+  return check_launch("shared-prefix merge");
+}
+
+template pkv_status launch_prefix_merge<BF16>(const DecodeArgs&, cudaStream_t);
+template pkv_status launch_prefix_merge<F16>(const DecodeArgs&, cudaStream_t);
 
 template pkv_status launch_shared_prefix_pass<BF16, BF16>(const PrefillArgs&, int, int,
                                                           const CUtensorMap&, const CUtensorMap&,

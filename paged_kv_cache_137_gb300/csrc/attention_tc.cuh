@@ -32,10 +32,11 @@
 //    zeroed in shared memory before the P V MMA (0 * NaN would poison it).
 //  * The warps' (max, sum, output) are merged through shared memory.  A
 //    pair's tiles are shared out evenly over its splits.  With several
-//    splits, or behind a shared-prefix pass, each CTA writes its partial and
-//    the last of the (sequence, KV head)'s partials to arrive (an atomic
-//    counter, no waiting; the pass's CTAs count in on the same counter)
-//    gathers them all into shared memory, merges them and resets the counter.
+//    splits each CTA writes its partial and the last of the (sequence, KV
+//    head)'s splits to arrive (an atomic counter, no waiting) gathers them
+//    all into shared memory, merges them and resets the counter.  Behind a
+//    shared-prefix pass the CTAs only write their partials; a merge kernel
+//    after this one combines them with the pass's.
 //  * The step's new token can be written by the CTA that holds position
 //    ctx - 1, before any copy is issued (the fused slot write).
 //  * Every mbarrier wait is bounded; a stage wait that gives up (its limit is
@@ -824,11 +825,15 @@ __global__ void __launch_bounds__(32 * W, resident_ctas<KV, HC, W>())
   // stream: nothing that kernel may write is read before it has completed.
   // Behind the shared-prefix pass, which itself waits for every kernel
   // before it and then lets this grid start on the SMs it leaves free,
-  // nothing is waited for: the pass's partials meet this grid's through the
-  // arrival counters (whoever arrives last merges), and the last CTA of this
-  // grid to finish waits for the pass, so that the grid never completes
-  // before it (a pass CTA may write the outputs of the pairs it completes).
+  // nothing is waited for: both grids write partials, and the last CTA of
+  // this grid to finish waits for the pass, so that the grid never completes
+  // before it (the merge kernel after this grid reads the pass's partials).
   if (P == 0) asm volatile("griddepcontrol.wait;" ::: "memory");
+  // Behind a shared prefix the merge kernel that follows may be scheduled as
+  // soon as every CTA of this grid is running: it waits for this grid to
+  // complete before it reads anything, and holds only slots this grid no
+  // longer needs.
+  if (P > 0) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   auto finish = [&]() {
     if (P > 0 && threadIdx.x == 0) {
       const int total = static_cast<int>(gridDim.x * gridDim.y * gridDim.z);
@@ -869,20 +874,6 @@ __global__ void __launch_bounds__(32 * W, resident_ctas<KV, HC, W>())
     return;
   }
   const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * G;
-  // Behind a shared prefix the merging CTA reads the pass's partials: warps
-  // 1.. ask L2 for their lines now (L2 is where the pass's writes land, so a
-  // line fetched before the pass writes it is updated, never stale).
-  if (kWarps > 1 && P > 0 && warp > 0 && a.ws_acc != nullptr) {
-    const int n = a.prefix_splits;
-    const int acc_lines = (n * D * 4 + 127) / 128, per_row = acc_lines + 2;
-    for (int i = tid - 32; i < G * per_row; i += kThreads - 32) {
-      const int row = i / per_row, k = i % per_row;
-      const size_t pidx = (head0 + row) * a.max_splits + (a.max_splits - n);
-      const float* line = k < acc_lines ? a.ws_acc + pidx * D + 32 * k
-                                        : (k == acc_lines ? a.ws_m : a.ws_l) + pidx;
-      asm volatile("prefetch.global.L2 [%0];" ::"l"(line));
-    }
-  }
   // The pair's n_t tiles are shared out evenly: split i takes tiles
   // [i n_t / nsplit, (i + 1) n_t / nsplit), at most partition / 64 of them.
   // Near-equal pieces keep the longest units of the grid on pairs that need
@@ -1049,29 +1040,29 @@ __global__ void __launch_bounds__(32 * W, resident_ctas<KV, HC, W>())
   }
 
   if (direct) return;
-
-  // ------------------------------------------- split-K: the last CTA merges
-  // Each CTA counts itself in (an atomic counter, never a wait on another
-  // CTA); the last of the pair's partials to arrive (its splits and, with a
-  // shared prefix, the pass's key ranges) combines them all and resets the
-  // counter.
-  __threadfence();
-  __syncthreads();
-  const int n_extra = P > 0 ? a.prefix_splits : 0;
-  if (tid == 0) {
-    const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
-    s_last = prev == nsplit + n_extra - 1;
-  }
-  __syncthreads();
-  if (!s_last) {
+  // behind a shared-prefix pass the merge kernel that follows merges every
+  // partial (the units here are short: counting in would cost each CTA the
+  // fence and atomic latency at its end)
+  if (P > 0) {
     finish();
     return;
   }
+
+  // ------------------------------------------- split-K: the last CTA merges
+  // Each CTA counts itself in (an atomic counter, never a wait on another
+  // CTA); the last of the pair's splits to arrive combines their partials
+  // and resets the counter.
   __threadfence();
-  merge_splits<Q, D, kThreads>(a, head0, nsplit, a.max_splits - n_extra, n_extra,
-                               reinterpret_cast<float*>(smem), kCap);
+  __syncthreads();
+  if (tid == 0) {
+    const int prev = atomicAdd(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 1);
+    s_last = prev == nsplit - 1;
+  }
+  __syncthreads();
+  if (!s_last) return;
+  __threadfence();
+  merge_splits<Q, D, kThreads>(a, head0, nsplit, a.max_splits, 0, reinterpret_cast<float*>(smem), kCap);
   if (tid == 0) atomicExch(&a.counters[static_cast<size_t>(seq) * a.num_kv_heads + kvh], 0);
-  finish();
 }
 
 template <typename KV, int D, int NS, int W = kWarps>
