@@ -40,7 +40,7 @@ METRIC = "paged decode attention KV GB/s & fraction of GB300 HBM peak; decode to
 KERNEL_SOURCES = {
     "decode": ["attention.cu", "attention.h", "attention_simt.cuh", "attention_tc.cuh",
                "attention_tc_launch.cuh", "device_common.cuh", "attention_prefill_umma.cuh",
-               "attention_shared_prefix.cu"],
+               "attention_shared_prefix.cu", "attention_tail.cuh"],
     "prefill": ["attention_prefill.cu", "attention_prefill_umma.cuh", "attention_tc.cuh", "attention.h",
                 "device_common.cuh"],
 }
@@ -204,7 +204,9 @@ def attention_kernels(kernel: str, w, splits: int, shared_prefix: bool = False) 
         k = "decode_simt_kernel"
         return k + (" + merge_kernel" if splits > 1 else "")
     if shared_prefix:
-        return "prefill_umma_kernel<shared prefix> + decode_tc_kernel + prefix_merge_kernel"
+        queue = kernel == "auto" and w.kv_dtype in ("bf16", "f16") and w.block_size == 16 and w.head_dim == 128
+        tails = "tail_stream_kernel" if queue else "decode_tc_kernel"
+        return f"prefill_umma_kernel<shared prefix> + {tails} + prefix_merge_kernel"
     return "decode_tc_kernel (split-K merge fused)"
 
 

@@ -267,7 +267,11 @@ PKV_API size_t pkv_attention_workspace_bytes(int32_t num_seqs, int32_t num_q_hea
  * heads and partitions of at most 1024 blocks, and the CUDA-core kernel
  * otherwise.  SIMT forces the CUDA-core kernel; TENSOR_CORE makes
  * pkv_attention_decode return PKV_ERR_UNSUPPORTED for sizes it does not
- * cover.  All kernels compute the same result within rounding. */
+ * cover, and keeps the positions past a shared prefix on the split kernel
+ * (AUTO streams them through the tail queue where it applies: 16-bit caches,
+ * head_dim 128, block size 16).  All kernels compute the same result within
+ * rounding; the tail queue and the split kernel at the same partition give
+ * the same bits. */
 #define PKV_KERNEL_AUTO 0
 #define PKV_KERNEL_SIMT 1
 #define PKV_KERNEL_TENSOR_CORE 2
@@ -355,11 +359,17 @@ PKV_API pkv_status pkv_decode_step(void* out, const void* q, int32_t q_dtype, vo
  *     read through row 0 of block_tables, and leaves per-row partial results
  *     (max, sum, unnormalised output) in the workspace;
  *   - the decode kernel attends positions [P, ctx) of each sequence and
- *     leaves its partials in the workspace too;
+ *     leaves its partials in the workspace too (16-bit caches at head_dim 128
+ *     and block size 16: one-warp CTAs on every resident slot take (sequence,
+ *     split, KV head) units from a queue in the workspace, longest first,
+ *     keeping their copies streaming from one unit into the next);
  *   - a merge kernel combines every row's partials into out.
  * Because the reduction is split differently, results can differ from
  * pkv_attention_decode in the low-order bits ([C "Effect"]: reusing shared
  * blocks changes how the attention reduction is tiled).
+ * partition_tokens (positions per split past the prefix): 0 picks 512 for
+ * 16-bit caches at head_dim 128 and block size 16, else as
+ * pkv_attention_partition with the longest context less P.
  * Requirements: every row's first prefix_blocks entries equal row 0's and
  * every context length is > P (a row that breaks either gets NaN outputs and
  * sets PKV_DEVICE_BAD_SHARED_PREFIX or PKV_DEVICE_BAD_LENGTH);

@@ -46,7 +46,9 @@ struct DecodeArgs {
   int32_t prefix_tokens, prefix_splits;
   int* status;               // device error word (PKV_DEVICE_* bits, atomicOr)
   uint64_t wait_ns;          // give-up limit of a stage wait; 0 = give up at once
-  int* done;                 // behind a shared-prefix pass: CTAs of this grid that have finished
+  int* done;                 // behind a shared-prefix pass: CTAs of this grid that have finished,
+                             // then the tail queue's claim counter
+  int32_t tail_queue;        // behind a shared-prefix pass: the tail queue form may run
 };
 
 // Prefill / shared-prefix pass arguments (attention_prefill.cu,

@@ -54,14 +54,18 @@ constexpr int kMergeStage = 4096;  // floats of gathered partials; more fall bac
 
 template <typename Q>
 __global__ void __launch_bounds__(tc::kThreads) prefix_merge_kernel(const DecodeArgs a) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   __shared__ __align__(16) float stage[kMergeStage];
   const int kvh = blockIdx.x, seq = blockIdx.y;
   const int P = a.prefix_tokens, n_extra = a.prefix_splits;
+  // The lengths are read before the grid dependency wait: none of the three
+  // kernels of the call writes them, and this grid starts only after every
+  // decode CTA has started, hence after the pass has passed its own wait on
+  // the work before the call.
   const int ctx = a.ctx_lens[seq];
   const bool bad = ctx < 0 || ctx > a.max_blocks * a.block_size || ctx <= P;
   const int nsplit = bad ? 1 : max(1, (ctx - P + a.partition - 1) / a.partition);
   const size_t head0 = static_cast<size_t>(seq) * a.num_q_heads + static_cast<size_t>(kvh) * a.group;
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   tc::merge_splits<Q, 128, tc::kThreads>(a, head0, nsplit, a.max_splits - n_extra, n_extra, stage,
                                          kMergeStage);
 }

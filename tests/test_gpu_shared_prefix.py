@@ -88,17 +88,18 @@ def test_shared_prefix_step_matches_oracle(name):
     assert pkv.pkv_device_status() == 0
 
 
-@pytest.mark.parametrize("partition", [0, 64, 128, 512])
+@pytest.mark.parametrize("partition", [0, 64, 128, 512, 1024])
 def test_shared_prefix_with_split_tails(partition):
-    """Tails split over several CTAs: the last one merges the tail splits
-    with the prefix pass's partials."""
+    """Tails split over several units (the tail queue up to 32 tiles a unit,
+    the split kernel past it: 64 and 1,024 tokens): the merge kernel combines
+    the tail splits with the prefix pass's partials."""
     w = CASES["pfx_rows192"]
     dev, sc = shared(w, partition)
     out = dev.step()
     torch.cuda.synchronize()
     check_close(out.double().cpu().numpy(), oracle_out(OS.build(w, scales=sc)), w.kv_dtype)
     n = len(dev.plan.seq_ids) * w.num_kv_heads
-    assert torch.count_nonzero(dev.workspace[: 4 * n]).item() == 0   # counters back at zero
+    assert torch.count_nonzero(dev.workspace[: 4 * n + 8]).item() == 0   # counters back at zero
 
 
 def test_shared_and_plain_paths_agree():
@@ -184,31 +185,62 @@ def test_shared_prefix_full_size():
     assert pkv.pkv_device_status() == 0
 
 
-@pytest.mark.parametrize("name", ["pfx_rows192", "pfx_t32"])
-def test_tail_wait_give_up_gives_nan_and_status_then_recovers(name):
-    """The tail kernel's failure path behind a shared prefix (the one-warp
-    form at block size 16, the two-warp form at 32), run on purpose: with a
-    stage-wait limit of 0 every tail CTA gives up at its first stage wait,
-    drains its copies in flight (its own bounded limit), writes a NaN partial
-    and sets PKV_DEVICE_WAIT_TIMEOUT; the merges, by a tail CTA or by a pass
-    CTA, carry the NaN to every output whose context extends past the prefix,
-    and the counters end at zero.  The next call, with the normal limit, is
-    correct."""
+@pytest.mark.parametrize("name,kernel", [("pfx_rows192", "auto"), ("pfx_rows192", "tc"),
+                                         ("pfx_t32", "auto")])
+def test_tail_wait_give_up_gives_nan_and_status_then_recovers(name, kernel):
+    """The tail kernels' failure path behind a shared prefix (the tail queue
+    at block size 16, the one-warp split form when the split kernel is
+    forced, the two-warp form at 32), run on purpose: with a stage-wait limit
+    of 0 every tail CTA gives up at its first stage wait, drains its copies in
+    flight (its own bounded limit), writes NaN partials (the queue form for
+    every unit it holds or claims afterwards) and sets
+    PKV_DEVICE_WAIT_TIMEOUT; the merge kernel carries the NaN to every output
+    whose context extends past the prefix, and the counters end at zero.  The
+    next call, with the normal limit, is correct."""
     w = CASES[name]
     dev, sc = shared(w)
     dev.copy_blocks()
     try:
+        pkv.pkv_set_attention_kernel(kernel)
         pkv.pkv_set_stage_wait_limit(0)
         out = dev.decode_step().clone()
         torch.cuda.synchronize()
     finally:
         pkv.pkv_set_stage_wait_limit(50_000_000)
+        pkv.pkv_set_attention_kernel("auto")
     assert pkv.pkv_device_status(clear=True) & pkv.PKV_DEVICE_WAIT_TIMEOUT
     assert torch.isnan(out).all()   # every context extends past the prefix
     n = len(dev.plan.seq_ids) * w.num_kv_heads
-    assert torch.count_nonzero(dev.workspace[: 4 * n + 4]).item() == 0   # counters and exit count
+    # counters, the exit count and the queue's claim counter
+    assert torch.count_nonzero(dev.workspace[: 4 * n + 8]).item() == 0
     out = dev.decode_step()
     torch.cuda.synchronize()
     assert pkv.pkv_device_status() == 0
     ref = OS.build(w, scales=sc)
     check_close(out.double().cpu().numpy(), oracle_out(ref), w.kv_dtype)
+
+
+@pytest.mark.parametrize("name,partition", [("pfx_rows192", 0), ("pfx_rows192", 128),
+                                            ("pfx_rows320", 512), ("pfx_f16", 0), ("pfx_g8", 256)])
+def test_tail_queue_equals_split_kernel_bit_for_bit(name, partition):
+    """The tail queue (one-warp CTAs taking units longest first) and the
+    one-warp split kernel (one CTA per unit) attend the same splits in the
+    same tile order with the same arithmetic: the outputs are the same bits,
+    and so are the step's pool writes."""
+    w = CASES[name]
+    outs, pools = [], []
+    for kernel in ("auto", "tc"):
+        dev, sc = shared(w, partition)
+        try:
+            pkv.pkv_set_attention_kernel(kernel)
+            out = dev.step()
+            torch.cuda.synchronize()
+        finally:
+            pkv.pkv_set_attention_kernel("auto")
+        outs.append(out.clone())
+        pools.append((dev.k_cache.clone(), dev.v_cache.clone()))
+        assert pkv.pkv_device_status() == 0
+    assert torch.equal(outs[0].view(torch.int16), outs[1].view(torch.int16))
+    assert torch.equal(pools[0][0].view(torch.uint8), pools[1][0].view(torch.uint8))
+    assert torch.equal(pools[0][1].view(torch.uint8), pools[1][1].view(torch.uint8))
+    check_close(outs[0].double().cpu().numpy(), oracle_out(OS.build(w, scales=sc)), w.kv_dtype)

@@ -98,17 +98,20 @@ def _align256(x):
 
 
 def test_shared_prefix_workspace_layout():
-    """The prefix-fork batch: one tail split per sequence (the automatic
-    partition of the 528-token tails) plus the prefix pass's key ranges (on
-    152 SMs the pass takes about a quarter of them: 8 KV heads x 4 row pairs
-    = 32 row units, 38 / 32 -> one range of all 1,024 keys), laid out as the
-    decode workspace with S = 1 + 1 slots and one more counter."""
+    """The prefix-fork batch: two tail split slots (the automatic 512
+    positions per split past the prefix for 16-bit caches at block size 16;
+    the tails reach 97 * 16 - 1,024 = 528 positions) plus the prefix pass's
+    key ranges (on 152 SMs the pass takes about a quarter of them: 8 KV heads
+    x 4 row pairs = 32 row units, 38 / 32 -> one range of all 1,024 keys),
+    laid out as the decode workspace with S = 2 + 1 slots and two more
+    counters."""
     desc = pkv.kv_desc(8192, 8, 128, 16, "bf16")
     b, hq, max_blocks = 256, 32, 97
-    s = 1 + 1
+    s = 2 + 1
     n = b * hq * s
-    # counters [B][N_kv] and the decode grid's exit count, then the partials
-    want = _align256(4 * (b * 8 + 1)) + 2 * _align256(4 * n) + _align256(4 * n * 128)
+    # counters [B][N_kv], the decode grid's exit count and the tail queue's
+    # claim counter, then the partials
+    want = _align256(4 * (b * 8 + 2)) + 2 * _align256(4 * n) + _align256(4 * n * 128)
     assert pkv.pkv_shared_prefix_workspace_bytes(b, hq, max_blocks, desc, 64, 0) == want
     # never smaller than the plain call's (used where the pass does not run)
     for pfx in (0, 1, 10, 96, 97):
