@@ -45,16 +45,21 @@ constexpr int kTailBuckets = kTailMaxTiles + 1;  // unit sizes 0 .. 32 tiles
 constexpr int kTailLead = 4;         // tiles before a unit's end at which the next is claimed
 // Largest batch the per-CTA unit list covers (lengths, per-chunk size counts
 // and units in shared memory): past it the one-warp split form runs instead.
-constexpr int kTailMaxSeqs = 1024;
-constexpr int kTailMaxUnits = 2048;  // (sequence, split) entries
+constexpr int kTailMaxSeqs = 512;
+constexpr int kTailMaxUnits = 1024;  // (sequence, split) entries
+// A warp's partial goes out through shared memory, four heads at a time:
+// rows of 132 floats (the padding keeps the fragment writes conflict-free).
+constexpr int kTailStageHeads = 4;
+constexpr int kTailStageRow = 132;
 
 // Dynamic shared memory of the queue kernel (NW warps of NS stages) for a
 // batch of B sequences and E (sequence, split) entries: the 1024-aligned
-// rings, their barriers, the size counts per 32-sequence chunk, the bucket
-// offsets, the lengths and the entries.
+// rings, their barriers, the partial staging rows, the size counts per
+// 32-sequence chunk, the bucket offsets, the lengths and the entries.
 __host__ __device__ constexpr int tail_smem_bytes(int NW, int NS, int B, int E) {
   return 1024 + NW * NS * Geom<BF16, 128, 1>::kStageBytes + NW * NS * 8 +
-         ((B + 31) / 32) * kTailBuckets * 4 + (kTailBuckets + 1) * 4 + 4 * B + 4 * E;
+         NW * kTailStageHeads * kTailStageRow * 4 + ((B + 31) / 32) * kTailBuckets * 4 +
+         (kTailBuckets + 1) * 4 + 4 * B + 4 * E;
 }
 
 // One unit: a (sequence, split) entry of the list and a KV head.
@@ -91,7 +96,9 @@ __global__ void __launch_bounds__(32 * NW, 1)
                                              ~uintptr_t(1023));
   uint8_t* stages = base + warp * NS * G_::kStageBytes;  // this warp's ring
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + NW * NS * G_::kStageBytes) + warp * NS;
-  int* s_tab = reinterpret_cast<int*>(base + NW * NS * G_::kStageBytes + NW * NS * 8);
+  float* s_part_all = reinterpret_cast<float*>(base + NW * NS * G_::kStageBytes + NW * NS * 8);
+  float* s_part = s_part_all + warp * kTailStageHeads * kTailStageRow;  // this warp's staging rows
+  int* s_tab = reinterpret_cast<int*>(s_part_all + NW * kTailStageHeads * kTailStageRow);
   int* s_off = s_tab + n_chunks * kTailBuckets;  // bucket offsets, then the entry count
   int* s_ctx = s_off + kTailBuckets + 1;
   uint32_t* s_ent = reinterpret_cast<uint32_t*>(s_ctx + B);
@@ -259,18 +266,32 @@ __global__ void __launch_bounds__(32 * NW, 1)
         a.ws_l[pidx] = bad ? CUDART_NAN_F : L[j];
       }
     }
+    // the outputs, four heads at a time: fragments into the staging rows,
+    // then whole 512-byte rows out with 16-byte stores
 #pragma unroll
-    for (int mt = 0; mt < D / 16; ++mt)
+    for (int h0 = 0; h0 < 8; h0 += kTailStageHeads) {
+      if (h0 >= G) break;
 #pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const int j = e & 1, head = 2 * q4 + j;
-        if (head < G) {
-          const size_t pidx = (head0 + head) * a.max_splits + u.split;
-          float A = M[j] != -CUDART_INF_F ? fmaf(st.o[mt][e], exp2f(M[j] - M[j]), 0.f) : 0.f;
-          A *= sc.v;
-          a.ws_acc[pidx * D + out_row_t<false>(mt, g, e >> 1)] = bad ? CUDART_NAN_F : A;
+      for (int mt = 0; mt < D / 16; ++mt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const int j = e & 1, head = 2 * q4 + j;
+          if (head >= h0 && head < h0 + kTailStageHeads) {
+            float A = M[j] != -CUDART_INF_F ? fmaf(st.o[mt][e], exp2f(M[j] - M[j]), 0.f) : 0.f;
+            A *= sc.v;
+            s_part[(head - h0) * kTailStageRow + out_row_t<false>(mt, g, e >> 1)] = bad ? CUDART_NAN_F : A;
+          }
         }
+      __syncwarp();
+      const int nh = min(kTailStageHeads, G - h0);
+      for (int i = lane; i < nh * (D / 4); i += 32) {
+        const int hl = i / (D / 4), c4 = i % (D / 4);
+        const size_t pidx = (head0 + h0 + hl) * a.max_splits + u.split;
+        reinterpret_cast<float4*>(a.ws_acc + pidx * D)[c4] =
+            *reinterpret_cast<const float4*>(s_part + hl * kTailStageRow + 4 * c4);
       }
+      __syncwarp();
+    }
   };
 
   // ------------------------------------------------ stream
