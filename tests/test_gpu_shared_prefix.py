@@ -4,8 +4,10 @@ A batch whose sequences all map the same leading blocks (forks of one
 prompt: "PagedAttention Memory Management", "Complex Topologies and Memory
 Sharing"; the katajob Q&A, "Sharing, the second dividend") is decoded by
 pkv_decode_step_shared_prefix: a tcgen05 pass attends every sequence's
-queries to the shared blocks once, the decode kernel attends the rest of each
-context and merges.  The result is plain attention, so it is compared with
+queries to the shared blocks once, the tail queue (or, where it does not
+apply, the split kernel's narrow forms) attends the rest of each context, and
+a merge kernel combines the partials.  The result is plain attention, so it is
+compared with
 the oracle at the decode tolerances; the reduction is split differently from
 the plain path, so the two paths agree within rounding, not bit for bit (the
 foundry page, "Effect": reusing shared blocks changes how the attention
