@@ -24,10 +24,10 @@
 // the batch's lengths (all its warps together, once), so that the last ones
 // claimed are short and the SMs drain together.
 //
-// Bounded waits as in the decode kernel: a stage wait that gives up sets the
-// device error bit and turns every unit the CTA holds or claims later into
-// NaN partials (no copy is issued after it), after waiting, with its own
-// bound, for the copies in flight.  A table entry out of range or a bad
+// Bounded waits as in the decode kernel: a warp whose stage wait gives up
+// sets the device error bit and turns every unit it holds or claims later
+// into NaN partials (it issues no copy after it), after waiting, with its own
+// bound, for its copies in flight.  A table entry out of range or a bad
 // length makes that unit's partial NaN.  The queue counter and the grid's
 // exit counter are reset by the last CTA to finish, which first waits for
 // the pass's grid, so this grid completes after the pass.
