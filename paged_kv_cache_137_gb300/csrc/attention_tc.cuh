@@ -10,7 +10,9 @@
 //  * One CTA per (KV head, sequence, split): four warps and 64-token tiles by
 //    default; behind a shared-prefix pass, where the contexts left are short,
 //    one warp (block size 16) or two (block size 32) with 16- or 32-token
-//    tiles, so that more CTAs per SM overlap each one's fixed latencies.  The
+//    tiles, so that more CTAs per SM overlap each one's fixed latencies (at
+//    block size 16 the tail queue of attention_tail.cuh runs instead where
+//    its unit list fits).  The
 //    split's block ids are read into shared memory; split 0 fetches its first
 //    tiles' ids and its query rows together with the length.  Warp 0 refills
 //    a ring of NS stages, one lane per TMA box: each stage is a tile of K and
