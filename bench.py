@@ -204,7 +204,11 @@ def attention_kernels(kernel: str, w, splits: int, shared_prefix: bool = False) 
         k = "decode_simt_kernel"
         return k + (" + merge_kernel" if splits > 1 else "")
     if shared_prefix:
-        queue = kernel == "auto" and w.kv_dtype in ("bf16", "f16") and w.block_size == 16 and w.head_dim == 128
+        # the tail queue: 16-bit caches, head_dim 128, block size 16, groups of
+        # up to 8 and a unit list of at most 512 sequences (else the split
+        # kernel's narrow forms)
+        queue = (kernel == "auto" and w.kv_dtype in ("bf16", "f16") and w.block_size == 16 and
+                 w.head_dim == 128 and w.num_q_heads // w.num_kv_heads <= 8 and w.num_seqs <= 512)
         tails = "tail_stream_kernel" if queue else "decode_tc_kernel"
         return f"prefill_umma_kernel<shared prefix> + {tails} + prefix_merge_kernel"
     return "decode_tc_kernel (split-K merge fused)"
